@@ -1,0 +1,198 @@
+// api.cu -- the C ABI (include/fp8q.h): argument validation, schedule
+// selection and kernel launches.  No allocation, no synchronization (except
+// fp8q_device_status, which exists to synchronize), no exceptions.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "../../include/fp8q.h"
+#include "internal.h"
+
+namespace {
+
+using namespace fp8q;
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+inline fp8q_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA; }
+
+inline cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
+
+// The kernels index with 32-bit ints in places; keep every extent in range.
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
+
+fp8q_status check_quant_common(const void *x, int64_t M, int64_t K, int64_t ldx, const void *xq, const float *xs,
+                               float eps)
+{
+    if (M < 0 || K <= 0 || M > kMaxDim || K > kMaxDim) return FP8Q_ERR_INVALID_ARG;
+    if (K % 16 != 0 || ldx < K || ldx % 8 != 0) return FP8Q_ERR_INVALID_ARG;
+    if (!(eps > 0.0f) || !isfinite(eps)) return FP8Q_ERR_INVALID_ARG;
+    if (M == 0) return FP8Q_OK;
+    if (x == nullptr || xq == nullptr || xs == nullptr) return FP8Q_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xq) || !aligned4(xs)) return FP8Q_ERR_INVALID_ARG;
+    return FP8Q_OK;
+}
+
+fp8q_status run_gemm(const GemmProblem &p, cudaStream_t st)
+{
+    fp8q_plan pl;
+    const fp8q_status s = fp8q_gemm_plan(p.M, p.N, p.K, p.blockwise ? 1 : 0, 0, &pl);
+    if (s != FP8Q_OK) return s;
+    unsigned *status = device_status_ptr();
+    if (status == nullptr) return FP8Q_ERR_CUDA;
+    GemmLaunch l;
+    l.swap_ab = pl.swap_ab != 0;
+    l.mma_n = pl.mma_n;
+    l.split = pl.split_k;
+    l.grid = pl.grid;
+    l.stages = pl.stages;
+    const cudaError_t e = p.blockwise ? launch_gemm_blockwise(p, l, status, st)
+                                      : launch_gemm_channelwise(p, l, status, st);
+    return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+fp8q_status fp8q_quant_per_token(const void *x, int64_t M, int64_t K, int64_t ldx, void *xq, float *x_scale,
+                                 float eps, void *stream)
+{
+    const fp8q_status s = check_quant_common(x, M, K, ldx, xq, x_scale, eps);
+    if (s != FP8Q_OK || M == 0) return s;
+    return from_cuda(launch_quant_per_token(x, M, K, ldx, xq, x_scale, eps, as_stream(stream)));
+}
+
+fp8q_status fp8q_quant_per_token_group_row_padded(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                                  int32_t group_size, float eps, int32_t row_alignment, void *xq,
+                                                  float *x_scale, int64_t m_pad, void *stream)
+{
+    if (group_size != 16 && group_size != 32 && group_size != 64 && group_size != 128) {
+        if (group_size <= 0) return FP8Q_ERR_INVALID_ARG;
+        return FP8Q_ERR_UNSUPPORTED;
+    }
+    if (row_alignment <= 0 || m_pad < M || m_pad % row_alignment != 0 || m_pad > kMaxDim)
+        return FP8Q_ERR_INVALID_ARG;
+    if (K > 0 && K % group_size != 0) return FP8Q_ERR_INVALID_ARG;
+    const fp8q_status s = check_quant_common(x, M, K, ldx, xq, x_scale, eps);
+    if (s != FP8Q_OK || M == 0) return s;
+    return from_cuda(launch_quant_group(x, M, K, ldx, group_size, xq, x_scale, m_pad, eps, current_device_sms(),
+                                        as_stream(stream)));
+}
+
+fp8q_status fp8q_quant_weight_block128(const void *w, int64_t N, int64_t K, void *wq, float *w_scale, float eps,
+                                       void *stream)
+{
+    if (N <= 0 || K <= 0 || N > kMaxDim || K > kMaxDim) return FP8Q_ERR_INVALID_ARG;
+    if (N % 128 != 0 || K % 128 != 0) return FP8Q_ERR_UNSUPPORTED;
+    if (!(eps > 0.0f) || !isfinite(eps)) return FP8Q_ERR_INVALID_ARG;
+    if (w == nullptr || wq == nullptr || w_scale == nullptr) return FP8Q_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(wq) || !aligned4(w_scale)) return FP8Q_ERR_INVALID_ARG;
+    return from_cuda(launch_quant_weight_block128(w, N, K, wq, w_scale, eps, as_stream(stream)));
+}
+
+fp8q_status fp8q_scaled_mm_channelwise(const void *a, const void *b, int64_t ldb, const float *a_scale,
+                                       const float *b_scale, const void *bias, void *out, int64_t M, int64_t N,
+                                       int64_t K, fp8q_out_dtype out_dtype, void *stream)
+{
+    if (M < 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return FP8Q_ERR_INVALID_ARG;
+    if (out_dtype != FP8Q_OUT_BF16 && out_dtype != FP8Q_OUT_FP16) return FP8Q_ERR_UNSUPPORTED;
+    if (K % 16 != 0 || ldb < K || ldb % 16 != 0 || N % 8 != 0) return FP8Q_ERR_INVALID_ARG;
+    if (M == 0) return FP8Q_OK;
+    if (a == nullptr || b == nullptr || a_scale == nullptr || b_scale == nullptr || out == nullptr)
+        return FP8Q_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(out) || !aligned4(a_scale) || !aligned4(b_scale))
+        return FP8Q_ERR_INVALID_ARG;
+    if (bias != nullptr && (reinterpret_cast<uintptr_t>(bias) & 1u)) return FP8Q_ERR_INVALID_ARG;
+    GemmProblem p;
+    p.M = M; p.N = N; p.K = K; p.m_pad = M;
+    p.a = a; p.w = b; p.ldw = ldb;
+    p.a_scale = a_scale; p.w_scale = b_scale; p.bias = bias; p.out = out;
+    p.out_fp16 = out_dtype == FP8Q_OUT_FP16;
+    p.blockwise = false;
+    return run_gemm(p, as_stream(stream));
+}
+
+fp8q_status fp8q_scaled_mm_blockwise(const void *a, const void *w, const float *a_scale, const float *w_scale,
+                                     const void *bias, void *out, int64_t M, int64_t m_pad, int64_t N, int64_t K,
+                                     fp8q_out_dtype out_dtype, void *stream)
+{
+    if (M < 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return FP8Q_ERR_INVALID_ARG;
+    if (out_dtype != FP8Q_OUT_BF16 && out_dtype != FP8Q_OUT_FP16) return FP8Q_ERR_UNSUPPORTED;
+    if (N % 128 != 0 || K % 128 != 0) return FP8Q_ERR_UNSUPPORTED;
+    if (m_pad < M || m_pad % 4 != 0 || m_pad > kMaxDim) return FP8Q_ERR_INVALID_ARG;
+    if (M == 0) return FP8Q_OK;
+    if (a == nullptr || w == nullptr || a_scale == nullptr || w_scale == nullptr || out == nullptr)
+        return FP8Q_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(w) || !aligned16(out) || !aligned16(a_scale) || !aligned4(w_scale))
+        return FP8Q_ERR_INVALID_ARG;
+    if (bias != nullptr && (reinterpret_cast<uintptr_t>(bias) & 1u)) return FP8Q_ERR_INVALID_ARG;
+    GemmProblem p;
+    p.M = M; p.N = N; p.K = K; p.m_pad = m_pad;
+    p.a = a; p.w = w; p.ldw = K;
+    p.a_scale = a_scale; p.w_scale = w_scale; p.bias = bias; p.out = out;
+    p.out_fp16 = out_dtype == FP8Q_OUT_FP16;
+    p.blockwise = true;
+    return run_gemm(p, as_stream(stream));
+}
+
+fp8q_status fp8q_linear_channelwise(const void *x, const void *b, int64_t ldb, const float *b_scale, const void *bias,
+                                    void *out, int64_t M, int64_t N, int64_t K, void *xq, float *xs,
+                                    fp8q_out_dtype out_dtype, void *stream)
+{
+    // Validate the GEMM's arguments before enqueueing the quantizer so that
+    // an error leaves nothing enqueued.
+    if (M < 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return FP8Q_ERR_INVALID_ARG;
+    if (out_dtype != FP8Q_OUT_BF16 && out_dtype != FP8Q_OUT_FP16) return FP8Q_ERR_UNSUPPORTED;
+    if (ldb < K || ldb % 16 != 0 || N % 8 != 0) return FP8Q_ERR_INVALID_ARG;
+    fp8q_status s = check_quant_common(x, M, K, K, xq, xs, 1e-10f);
+    if (s != FP8Q_OK || M == 0) return s;
+    if (b == nullptr || b_scale == nullptr || out == nullptr || !aligned16(b) || !aligned16(out) || !aligned4(b_scale))
+        return FP8Q_ERR_INVALID_ARG;
+    s = fp8q_quant_per_token(x, M, K, K, xq, xs, 1e-10f, stream);
+    if (s != FP8Q_OK) return s;
+    return fp8q_scaled_mm_channelwise(xq, b, ldb, xs, b_scale, bias, out, M, N, K, out_dtype, stream);
+}
+
+fp8q_status fp8q_linear_blockwise(const void *x, const void *w, const float *w_scale, const void *bias, void *out,
+                                  int64_t M, int64_t N, int64_t K, void *xq, float *xs, int64_t m_pad,
+                                  fp8q_out_dtype out_dtype, void *stream)
+{
+    if (M < 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return FP8Q_ERR_INVALID_ARG;
+    if (out_dtype != FP8Q_OUT_BF16 && out_dtype != FP8Q_OUT_FP16) return FP8Q_ERR_UNSUPPORTED;
+    if (N % 128 != 0 || K % 128 != 0) return FP8Q_ERR_UNSUPPORTED;
+    if (m_pad < M || m_pad % 4 != 0 || m_pad > kMaxDim) return FP8Q_ERR_INVALID_ARG;
+    fp8q_status s = check_quant_common(x, M, K, K, xq, xs, 1e-10f);
+    if (s != FP8Q_OK || M == 0) return s;
+    if (w == nullptr || w_scale == nullptr || out == nullptr || !aligned16(w) || !aligned16(out) ||
+        !aligned16(xs) || !aligned4(w_scale))
+        return FP8Q_ERR_INVALID_ARG;
+    s = fp8q_quant_per_token_group_row_padded(x, M, K, K, 128, 1e-10f, 4, xq, xs, m_pad, stream);
+    if (s != FP8Q_OK) return s;
+    return fp8q_scaled_mm_blockwise(xq, w, xs, w_scale, bias, out, M, m_pad, N, K, out_dtype, stream);
+}
+
+fp8q_status fp8q_device_status(void *stream, int32_t reset)
+{
+    unsigned v = 0;
+    if (read_status_word(&v, reset != 0, as_stream(stream)) != cudaSuccess) return FP8Q_ERR_CUDA;
+    if (v & 4u) return FP8Q_ERR_TIMEOUT;
+    return v == 0 ? FP8Q_OK : FP8Q_ERR_CUDA;
+}
+
+const char *fp8q_status_str(fp8q_status status)
+{
+    switch (status) {
+        case FP8Q_OK: return "FP8Q_OK";
+        case FP8Q_ERR_INVALID_ARG: return "FP8Q_ERR_INVALID_ARG";
+        case FP8Q_ERR_UNSUPPORTED: return "FP8Q_ERR_UNSUPPORTED";
+        case FP8Q_ERR_CUDA: return "FP8Q_ERR_CUDA";
+        case FP8Q_ERR_TIMEOUT: return "FP8Q_ERR_TIMEOUT";
+        default: return "FP8Q_UNKNOWN_STATUS";
+    }
+}
+
+int32_t fp8q_version(void) { return (1 << 16) | 0; }
+
+}  // extern "C"

@@ -1,0 +1,26 @@
+// gemm_instances.cuh -- the instantiations a translation unit provides:
+// swapped (decode) tiles of 16/32/64/128 tokens and non-swapped (prefill)
+// tiles of 128 tokens x 256 output columns, bf16 or fp16 output.
+#pragma once
+
+#include "gemm_launch.cuh"
+
+namespace fp8q {
+
+template <bool BLOCKWISE, typename OutT>
+cudaError_t dispatch_gemm(const GemmProblem &p, const GemmLaunch &l, unsigned *status, cudaStream_t st)
+{
+    if (l.swap_ab) {
+        switch (l.mma_n) {
+            case 16: return launch_gemm_inst<true, 16, stages_for(true, 16), BLOCKWISE, OutT>(p, l, status, st);
+            case 32: return launch_gemm_inst<true, 32, stages_for(true, 32), BLOCKWISE, OutT>(p, l, status, st);
+            case 64: return launch_gemm_inst<true, 64, stages_for(true, 64), BLOCKWISE, OutT>(p, l, status, st);
+            case 128: return launch_gemm_inst<true, 128, stages_for(true, 128), BLOCKWISE, OutT>(p, l, status, st);
+            default: return cudaErrorInvalidValue;
+        }
+    }
+    if (l.mma_n == 256) return launch_gemm_inst<false, 256, stages_for(false, 256), BLOCKWISE, OutT>(p, l, status, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace fp8q

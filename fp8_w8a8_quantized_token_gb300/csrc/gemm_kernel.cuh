@@ -1,0 +1,489 @@
+// gemm_kernel.cuh -- the scaled FP8 (E4M3 x E4M3 -> fp32) GEMM for sm_103a.
+//
+// Computes, for the channelwise scheme ("Tune FP8 GEMM Triton tiles on L40S
+// and enable by default" page, key source snippets: fp8_scaled_mm)
+//     out[m,n] = cvt( acc[m,n] * a_scale[m] * w_scale[n] (+ bias[n]) ),
+//     acc[m,n] = sum_k a[m,k] * w[n,k]
+// and for the blockwise scheme ("Remove per-call padding overhead of the FP8
+// blockwise GEMM" page, key source snippets: fp8_blockwise_scaled_mm)
+//     out[m,n] = cvt( sum_kb P_kb[m,n] * a_scale[kb*m_pad + m]
+//                                      * w_scale[(n/128)*(K/128) + kb] (+ bias[n]) )
+// where P_kb is the product over the 128 k of block kb.
+//
+// Structure (one CTA, warp-specialised):
+//   warp 0        TMA producer: streams 128-byte-wide K slices of the A and
+//                 B operand tiles (and, blockwise, the tile's activation
+//                 scales of that K block) into a STAGES-deep shared-memory
+//                 ring, 128-byte swizzled.
+//   warp 1        TMEM allocator + MMA issuer: one thread issues four
+//                 tcgen05.mma.kind::f8f6f4 (K = 32 each) per ring slot into
+//                 a TMEM accumulator (M = 128 lanes x N = BN fp32 columns)
+//                 and commits completion to mbarriers.
+//   warps 2..     epilogue: tcgen05.ld the accumulator, apply the scales
+//                 (blockwise: after every K block, "promotion" into fp32
+//                 registers), add the bias, convert and store.
+// TMEM holds two accumulator slots so MMA on the next tile (channelwise) or
+// the next K block (blockwise) overlaps the epilogue of the current one.
+//
+// Orientation.  The MMA's M side is always 128 rows of the A operand.
+//   SWAP = true  (decode-size M): A = 128 weight rows, B = BN tokens;
+//                 TMEM lane = output column n, TMEM column = token m.
+//   SWAP = false (prefill M):      A = 128 tokens, B = BN weight rows;
+//                 TMEM lane = token m, TMEM column = output column n.
+//
+// Split-K.  split > 1 launches thread-block clusters of `split` CTAs that
+// share one output tile and take consecutive ranges of K blocks; each CTA
+// writes its fp32 partial tile to its own shared memory, and after a
+// cluster barrier every CTA sums a slice of rows over all CTAs of the
+// cluster in rank order (distributed shared memory), so the result is
+// deterministic and needs no global workspace.
+//
+// Every mbarrier wait is bounded (device_common.cuh); a wait that runs out
+// records a timeout in the status word and all roles wind down, waiting
+// (bounded) for their in-flight TMA copies and MMAs before TMEM is freed.
+#pragma once
+
+#include "device_common.cuh"
+
+namespace fp8q {
+
+struct GemmArgs {
+    int M, N, K;
+    int num_kb;            // ceil(K / 128)
+    int m_tiles, n_tiles;  // tile counts along tokens and output columns
+    int num_tiles;
+    int split;             // CTAs per cluster along K
+    int group;             // tile rasterisation group (A-operand tiles)
+    const float *a_scale;
+    const float *w_scale;
+    const __nv_bfloat16 *bias;
+    void *out;
+    long long ldo;
+    unsigned *status;
+};
+
+template <bool SWAP, int BN, int STAGES, bool BLOCKWISE>
+struct GemmCfg {
+    static constexpr int kEpiWarps = BN > 128 ? 8 : 4;
+    static constexpr int kColGroups = kEpiWarps / 4;
+    static constexpr int kCols = BN / kColGroups;  // TMEM columns per epilogue thread
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    static constexpr int kEpiThreads = 32 * kEpiWarps;
+    static constexpr int kTokTile = SWAP ? BN : 128;     // tokens per tile
+    static constexpr int kColTile = SWAP ? 128 : BN;     // output columns per tile
+    static constexpr uint32_t kABytes = 128u * 128u;
+    static constexpr uint32_t kBBytes = static_cast<uint32_t>(BN) * 128u;
+    static constexpr uint32_t kSABytes = BLOCKWISE ? static_cast<uint32_t>(kTokTile) * 4u : 0u;  // TMA box
+    // Scale slots are 128-byte aligned (TMA destination alignment).
+    static constexpr uint32_t kSASlot = BLOCKWISE ? (kSABytes + 127u) / 128u * 128u : 0u;
+    static constexpr int kSASlotFloats = static_cast<int>(kSASlot / 4u);
+    static constexpr uint32_t kStageTx = kABytes + kBBytes + kSABytes;
+    static constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32u : static_cast<uint32_t>(2 * BN);
+    static constexpr uint32_t kOffA = 0;
+    static constexpr uint32_t kOffB = kOffA + STAGES * kABytes;
+    static constexpr uint32_t kOffSA = kOffB + STAGES * kBBytes;
+    static constexpr uint32_t kOffBar = kOffSA + STAGES * kSASlot;
+    static constexpr uint32_t kNumBars = 2 * STAGES + 5;  // full, empty, tfull[2], tempty[2], drain
+    static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr uint32_t kOffCol = (kOffMisc + 16 + 15) / 16 * 16;  // staged column scale, bias
+    static constexpr uint32_t kSmemBytes = kOffCol + 2u * BN * 4u + 1024u;  // + alignment slack
+    static constexpr uint32_t kRedBytes = 128u * BN * 4u;
+    static constexpr uint32_t kIdesc = idesc_e4m3_f32<128, BN>();
+    static_assert(kRedBytes <= kOffBar, "the split-K partial tile must fit in the stage ring");
+    static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
+    static_assert(kCols % 32 == 0 || kCols == 16, "epilogue column chunking");
+};
+
+// Waits that only give up on the time limit (used while draining).
+__device__ __forceinline__ void mbar_wait_drain(uint64_t *bar, uint32_t parity, unsigned *status)
+{
+    const uint32_t a = smem_u32(bar);
+    const unsigned long long t0 = globaltimer_ns();
+    while (!mbar_try_wait(a, parity)) {
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            atomicOr(status, kStatusTimeout);
+            return;
+        }
+    }
+}
+
+__device__ __forceinline__ uint64_t policy_evict_normal()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Tile index -> (A-operand tile, B-operand tile) with grouped rasterisation:
+// `group` consecutive A tiles sweep all B tiles together so concurrently
+// running CTAs share operands in L2.
+__device__ __forceinline__ void tile_coords(int tile, int a_tiles, int b_tiles, int group, int &a_t, int &b_t)
+{
+    const int per_group = group * b_tiles;
+    const int g = tile / per_group;
+    const int first = g * group;
+    const int gsize = min(group, a_tiles - first);
+    const int idx = tile - g * per_group;
+    a_t = first + idx % gsize;
+    b_t = idx / gsize;
+}
+
+template <typename OutT>
+__device__ __forceinline__ void store_out(OutT *out, long long idx, float v)
+{
+    out[idx] = to_out<OutT>(v);
+}
+
+template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT>
+__global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads, 1)
+    fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                    const __grid_constant__ CUtensorMap tm_sa, const GemmArgs p)
+{
+    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *sA = smem + C::kOffA;
+    uint8_t *sB = smem + C::kOffB;
+    float *sSA = reinterpret_cast<float *>(smem + C::kOffSA);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+    uint64_t *empty = full + STAGES;
+    uint64_t *tfull = empty + STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+    float *sColScale = reinterpret_cast<float *>(smem + C::kOffCol);
+    float *sColBias = sColScale + BN;
+    float *sRed = reinterpret_cast<float *>(smem);  // split-K partial tile, [BN][128], reuses the ring
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int split = p.split;
+    const int rank = split > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int cluster_id = blockIdx.x / split;
+    const int num_clusters = gridDim.x / split;
+    const int kb_begin = static_cast<int>(static_cast<long long>(p.num_kb) * rank / split);
+    const int kb_end = static_cast<int>(static_cast<long long>(p.num_kb) * (rank + 1) / split);
+    const int nkb = kb_end - kb_begin;
+    const int a_tiles = SWAP ? p.n_tiles : p.m_tiles;
+    const int b_tiles = SWAP ? p.m_tiles : p.n_tiles;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], BLOCKWISE ? 1 + C::kEpiWarps : 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], C::kEpiWarps);
+        }
+        mbar_init(drain, 1);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tm_a);
+        tma_prefetch_map(&tm_b);
+        if (BLOCKWISE) tma_prefetch_map(&tm_sa);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------
+        // TMA producer
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            const uint64_t pol_a = SWAP ? policy_evict_first() : policy_evict_normal();
+            const uint64_t pol_b = SWAP ? policy_evict_last() : policy_evict_normal();
+            uint32_t stage = 0, phase = 0;
+            long long issued = 0;
+            for (int tile = cluster_id; tile < p.num_tiles; tile += num_clusters) {
+                int a_t, b_t;
+                tile_coords(tile, a_tiles, b_tiles, p.group, a_t, b_t);
+                const int m_tile = SWAP ? b_t : a_t;
+                const int a_row = a_t * 128;
+                const int b_row = b_t * BN;
+                bool ok = true;
+                for (int i = 0; i < nkb; ++i) {
+                    const int kb = kb_begin + i;
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort, p.status)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&full[stage], C::kStageTx);
+                    tma_load_2d(sA + stage * C::kABytes, &tm_a, &full[stage], kb * 128, a_row, pol_a);
+                    tma_load_2d(sB + stage * C::kBBytes, &tm_b, &full[stage], kb * 128, b_row, pol_b);
+                    if (BLOCKWISE)
+                        tma_load_2d(sSA + stage * C::kSASlotFloats, &tm_sa, &full[stage], m_tile * C::kTokTile, kb,
+                                    pol_b);
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+            }
+            // Drain: the last STAGES copies must have landed before the CTA
+            // may exit (they complete in the normal flow long before this).
+            const long long first = issued > STAGES ? issued - STAGES : 0;
+            for (long long j = first; j < issued; ++j)
+                mbar_wait_drain(&full[j % STAGES], static_cast<uint32_t>((j / STAGES) & 1), p.status);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------
+        // MMA issuer (one thread)
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, slot = 0, tphase = 0;
+            bool ok = true;
+            for (int tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
+                if (!BLOCKWISE) {
+                    if (!mbar_wait(&tempty[slot], tphase ^ 1u, abort, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                }
+                for (int i = 0; i < nkb; ++i) {
+                    if (BLOCKWISE) {
+                        if (!mbar_wait(&tempty[slot], tphase ^ 1u, abort, p.status)) { ok = false; break; }
+                        tc_fence_after();
+                    }
+                    if (!mbar_wait(&full[stage], phase, abort, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(sA + stage * C::kABytes);
+                    const uint32_t b_addr = smem_u32(sB + stage * C::kBBytes);
+                    const uint32_t d = tmem_base + slot * BN;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t acc = BLOCKWISE ? (k > 0) : (i > 0 || k > 0);
+                        umma_e4m3(d, umma_desc_sw128(a_addr + k * 32), umma_desc_sw128(b_addr + k * 32), C::kIdesc,
+                                  acc);
+                    }
+                    umma_commit(&empty[stage]);
+                    if (BLOCKWISE) {
+                        umma_commit(&tfull[slot]);
+                        slot ^= 1u;
+                        if (slot == 0) tphase ^= 1u;
+                    }
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                if (!BLOCKWISE) {
+                    umma_commit(&tfull[slot]);
+                    slot ^= 1u;
+                    if (slot == 0) tphase ^= 1u;
+                }
+            }
+            // Every MMA this thread issued has finished before TMEM is freed.
+            umma_commit(drain);
+            mbar_wait_drain(drain, 0, p.status);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------------
+        // Epilogue warps
+        // ------------------------------------------------------------------
+        const int ew = warp - 2;
+        const int quarter = warp & 3;          // TMEM lanes this warp may access
+        const int cgroup = ew >> 2;            // column group
+        const int row = quarter * 32 + lane;   // TMEM lane = accumulator row
+        const int col0 = cgroup * C::kCols;
+        const int etid = threadIdx.x - 64;
+        OutT *out = static_cast<OutT *>(p.out);
+        uint32_t slot = 0, tphase = 0, estage = 0, ephase = 0;
+
+        for (int tile = cluster_id; tile < p.num_tiles; tile += num_clusters) {
+            int a_t, b_t;
+            tile_coords(tile, a_tiles, b_tiles, p.group, a_t, b_t);
+            const int m0 = (SWAP ? b_t : a_t) * C::kTokTile;
+            const int n0 = (SWAP ? a_t : b_t) * C::kColTile;
+            // Row-wise (per thread) values.
+            const int rm = SWAP ? 0 : m0 + row;       // token of this row (non-swapped)
+            const int rn = SWAP ? n0 + row : 0;       // output column of this row (swapped)
+            float row_scale = 0.0f, row_bias = 0.0f;
+            if (!BLOCKWISE) {
+                if (SWAP) row_scale = rn < p.N ? __ldg(p.w_scale + rn) : 0.0f;
+                else row_scale = rm < p.M ? __ldg(p.a_scale + rm) : 0.0f;
+            }
+            if (SWAP && p.bias != nullptr && rn < p.N) row_bias = __bfloat162float(p.bias[rn]);
+
+            // Column-wise values staged in shared memory.
+            named_barrier_sync(1, C::kEpiThreads);
+            for (int c = etid; c < BN; c += C::kEpiThreads) {
+                if (SWAP) {
+                    const int m = m0 + c;
+                    sColScale[c] = (!BLOCKWISE && m < p.M) ? __ldg(p.a_scale + m) : 0.0f;
+                    sColBias[c] = 0.0f;
+                } else {
+                    const int n = n0 + c;
+                    sColScale[c] = (!BLOCKWISE && n < p.N) ? __ldg(p.w_scale + n) : 0.0f;
+                    sColBias[c] = (p.bias != nullptr && n < p.N) ? __bfloat162float(p.bias[n]) : 0.0f;
+                }
+            }
+            named_barrier_sync(1, C::kEpiThreads);
+
+            float acc[C::kCols];
+            bool ok = true;
+            if (BLOCKWISE) {
+#pragma unroll
+                for (int j = 0; j < C::kCols; ++j) acc[j] = 0.0f;
+                const int wblk = SWAP ? a_t : (n0 >> 7) + cgroup;  // 128-row weight block
+                const float *sw_row = p.w_scale + static_cast<long long>(wblk) * p.num_kb;
+                for (int i = 0; i < nkb; ++i) {
+                    const int kb = kb_begin + i;
+                    // Warp-uniform outcome: the __syncwarp below needs every lane.
+                    bool got = mbar_wait(&full[estage], ephase, abort, p.status);
+                    got = got && mbar_wait(&tfull[slot], tphase, abort, p.status);
+                    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                    tc_fence_after();
+                    const float swk = __ldg(sw_row + kb);
+                    const float *sa = sSA + estage * C::kSASlotFloats;
+                    const float srow = SWAP ? 0.0f : sa[row] * swk;
+                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + slot * BN + col0;
+#pragma unroll
+                    for (int c = 0; c < C::kCols; c += 16) {
+                        uint32_t r[16];
+                        tmem_ld16(taddr + c, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float s = SWAP ? sa[col0 + c + j] * swk : srow;
+                            acc[c + j] = fmaf(__uint_as_float(r[j]), s, acc[c + j]);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&tempty[slot]);
+                        mbar_arrive(&empty[estage]);
+                    }
+                    slot ^= 1u;
+                    if (slot == 0) tphase ^= 1u;
+                    if (++estage == STAGES) { estage = 0; ephase ^= 1u; }
+                }
+            } else {
+                ok = __all_sync(0xffffffffu, mbar_wait(&tfull[slot], tphase, abort, p.status));
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + slot * BN + col0;
+#pragma unroll
+                    for (int c = 0; c < C::kCols; c += 16) {
+                        uint32_t r[16];
+                        tmem_ld16(taddr + c, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) acc[c + j] = __uint_as_float(r[j]);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[slot]);
+                    slot ^= 1u;
+                    if (slot == 0) tphase ^= 1u;
+                }
+            }
+            // No early exit from the tile loop: every epilogue thread must
+            // reach the same named barriers.  After a timeout every further
+            // wait fails at once and the stores below are skipped.
+            if (!ok) continue;
+
+            if (split == 1) {
+                // Scale, add bias, convert, store.
+                if (SWAP) {
+                    if (rn < p.N) {
+#pragma unroll
+                        for (int j = 0; j < C::kCols; ++j) {
+                            const int m = m0 + col0 + j;
+                            if (m < p.M) {
+                                const float y = BLOCKWISE ? acc[j] + row_bias
+                                                          : fmaf(acc[j] * row_scale, sColScale[col0 + j], row_bias);
+                                store_out(out, static_cast<long long>(m) * p.ldo + rn, y);
+                            }
+                        }
+                    }
+                } else if (rm < p.M) {
+                    OutT *orow = out + static_cast<long long>(rm) * p.ldo;
+#pragma unroll
+                    for (int j = 0; j < C::kCols; j += 8) {
+                        const int n = n0 + col0 + j;
+                        float y[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int c = col0 + j + e;
+                            y[e] = BLOCKWISE ? acc[j + e] + sColBias[c]
+                                             : fmaf(acc[j + e] * row_scale, sColScale[c], sColBias[c]);
+                        }
+                        if (n + 8 <= p.N) {
+                            uint4 v;
+                            uint32_t *vw = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const OutT lo = to_out<OutT>(y[2 * e]), hi = to_out<OutT>(y[2 * e + 1]);
+                                vw[e] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(&lo)) |
+                                        (static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(&hi)) << 16);
+                            }
+                            *reinterpret_cast<uint4 *>(orow + n) = v;
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                if (n + e < p.N) orow[n + e] = to_out<OutT>(y[e]);
+                        }
+                    }
+                }
+            } else {
+                // Split-K: publish this CTA's partial tile (the ring is idle:
+                // every copy was consumed and every MMA has completed).
+                named_barrier_sync(1, C::kEpiThreads);
+#pragma unroll
+                for (int j = 0; j < C::kCols; ++j) sRed[(col0 + j) * 128 + row] = acc[j];
+            }
+        }
+    }
+
+    if (split > 1) {
+        cluster_sync();
+        if (warp >= 2 && !*abort) {
+            // Reduce rows [r_lo, r_hi) (whole groups of 4) over the cluster.
+            const int etid = threadIdx.x - 64;
+            const int r_lo = 4 * (32 * rank / split), r_hi = 4 * (32 * (rank + 1) / split);
+            const int quads = (r_hi - r_lo) >> 2;
+            int a_t, b_t;
+            tile_coords(cluster_id, a_tiles, b_tiles, p.group, a_t, b_t);
+            const int m0 = (SWAP ? b_t : a_t) * C::kTokTile;
+            const int n0 = (SWAP ? a_t : b_t) * C::kColTile;
+            OutT *out = static_cast<OutT *>(p.out);
+            const uint32_t red_base = smem_u32(sRed);
+            for (int item = etid; item < BN * quads; item += C::kEpiThreads) {
+                const int c = item / quads;
+                const int r = r_lo + 4 * (item - c * quads);
+                const uint32_t off = static_cast<uint32_t>((c * 128 + r) * 4);
+                float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int q = 0; q < split; ++q) {
+                    const float4 v = dsmem_ld_f4(dsmem_map(red_base + off, static_cast<uint32_t>(q)));
+                    s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+                }
+                const float sv[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int m = SWAP ? m0 + c : m0 + r + e;
+                    const int n = SWAP ? n0 + r + e : n0 + c;
+                    if (m < p.M && n < p.N) {
+                        float y = sv[e];
+                        if (!BLOCKWISE) y *= __ldg(p.a_scale + m) * __ldg(p.w_scale + n);
+                        if (p.bias != nullptr) y += __bfloat162float(p.bias[n]);
+                        store_out(out, static_cast<long long>(m) * p.ldo + n, y);
+                    }
+                }
+            }
+        }
+        cluster_sync();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+}  // namespace fp8q

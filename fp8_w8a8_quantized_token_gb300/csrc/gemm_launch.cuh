@@ -1,0 +1,94 @@
+// gemm_launch.cuh -- host-side launch of one fp8_gemm_kernel instantiation:
+// tensor maps, kernel attributes, cluster launch.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "gemm_kernel.cuh"
+#include "internal.h"
+
+namespace fp8q {
+
+constexpr int kMaxDevices = 64;
+
+template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT>
+cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigned *status, cudaStream_t st)
+{
+    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE>;
+    auto kernel = fp8_gemm_kernel<SWAP, BN, STAGES, BLOCKWISE, OutT>;
+
+    static std::atomic<uint64_t> attr_done[kMaxDevices / 64 + 1];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_done[dev >> 6].load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmemBytes));
+        if (e != cudaSuccess) return e;
+        attr_done[dev >> 6].fetch_or(bit, std::memory_order_acq_rel);
+    }
+
+    // Operand maps: e4m3 rows of K bytes, boxes of 128 (K) x rows.
+    CUtensorMap tm_w, tm_x, tm_sa;
+    const int tok_box = C::kTokTile;
+    const int wrow_box = SWAP ? 128 : BN;
+    if (!make_tmap_2d(&tm_w, pr.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(pr.K),
+                      static_cast<uint64_t>(pr.N), static_cast<uint64_t>(pr.ldw), 128, wrow_box, true))
+        return cudaErrorInvalidValue;
+    if (!make_tmap_2d(&tm_x, pr.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(pr.K),
+                      static_cast<uint64_t>(pr.M), static_cast<uint64_t>(pr.K), 128, tok_box, true))
+        return cudaErrorInvalidValue;
+    if (BLOCKWISE) {
+        // Column-major activation scales: K/128 columns of m_pad floats; only
+        // the first M entries of each column are real (the rest read as 0).
+        if (!make_tmap_2d(&tm_sa, pr.a_scale, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, static_cast<uint64_t>(pr.M),
+                          static_cast<uint64_t>(pr.K / 128), static_cast<uint64_t>(pr.m_pad) * 4u, tok_box, 1,
+                          false))
+            return cudaErrorInvalidValue;
+    } else {
+        tm_sa = tm_x;  // unused
+    }
+
+    GemmArgs a;
+    a.M = static_cast<int>(pr.M);
+    a.N = static_cast<int>(pr.N);
+    a.K = static_cast<int>(pr.K);
+    a.num_kb = static_cast<int>((pr.K + 127) / 128);
+    a.m_tiles = static_cast<int>((pr.M + C::kTokTile - 1) / C::kTokTile);
+    a.n_tiles = static_cast<int>((pr.N + C::kColTile - 1) / C::kColTile);
+    a.num_tiles = a.m_tiles * a.n_tiles;
+    a.split = l.split;
+    a.group = SWAP ? a.n_tiles : 8;
+    if (a.group < 1) a.group = 1;
+    a.a_scale = pr.a_scale;
+    a.w_scale = pr.w_scale;
+    a.bias = static_cast<const __nv_bfloat16 *>(pr.bias);
+    a.out = pr.out;
+    a.ldo = pr.N;
+    a.status = status;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(l.grid));
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attrs[1];
+    int na = 0;
+    if (l.split > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = static_cast<unsigned>(l.split);
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    // A operand: the 128-row side of the MMA; B operand: the BN-row side.
+    const CUtensorMap &tm_a = SWAP ? tm_w : tm_x;
+    const CUtensorMap &tm_b = SWAP ? tm_x : tm_w;
+    return cudaLaunchKernelEx(&cfg, kernel, tm_a, tm_b, tm_sa, a);
+}
+
+}  // namespace fp8q

@@ -1,0 +1,76 @@
+// internal.h -- declarations shared by the library's translation units
+// (host side only; no CUDA device code here).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fp8q {
+
+// ---- quantizers (quant.cu) ------------------------------------------------
+cudaError_t launch_quant_per_token(const void *x, int64_t M, int64_t K, int64_t ldx, void *xq, float *xs, float eps,
+                                   cudaStream_t st);
+cudaError_t launch_quant_group(const void *x, int64_t M, int64_t K, int64_t ldx, int group, void *xq, float *xs,
+                               int64_t m_pad, float eps, int num_sms, cudaStream_t st);
+cudaError_t launch_quant_weight_block128(const void *w, int64_t N, int64_t K, void *wq, float *ws, float eps,
+                                         cudaStream_t st);
+
+// ---- GEMM (gemm_*.cu) -------------------------------------------------------
+// A GEMM launch as the planner decided it.
+struct GemmLaunch {
+    bool swap_ab;      // true: MMA A = 128 weight rows, MMA N = tokens
+    int mma_n;         // MMA N extent (tile width along the B operand)
+    int split;         // K-split count = cluster size
+    int grid;          // CTAs
+    int stages;        // pipeline depth the instantiation uses
+};
+
+struct GemmProblem {
+    int64_t M, N, K;
+    int64_t m_pad;          // blockwise: leading dimension of the scale columns
+    const void *a;          // e4m3 activations, row stride K
+    const void *w;          // e4m3 weights [N, K] with row stride ldw
+    int64_t ldw;
+    const float *a_scale;   // channelwise [M]; blockwise column-major [K/128][m_pad]
+    const float *w_scale;   // channelwise [N]; blockwise [N/128][K/128]
+    const void *bias;       // bf16 [N] or null
+    void *out;              // [M, N]
+    bool out_fp16;
+    bool blockwise;
+};
+
+// Launchers return cudaSuccess or the launch error; a tensor map the driver
+// rejects is reported as cudaErrorInvalidValue.
+
+cudaError_t launch_gemm_channelwise(const GemmProblem &p, const GemmLaunch &l, unsigned *status, cudaStream_t st);
+cudaError_t launch_gemm_blockwise(const GemmProblem &p, const GemmLaunch &l, unsigned *status, cudaStream_t st);
+
+// Pipeline depth of the instantiation serving (swap_ab, mma_n): the
+// shared-memory ring holds `stages` slots of 16 KB (A) + mma_n*128 B (B).
+constexpr int stages_for(bool swap_ab, int mma_n) { return swap_ab ? (mma_n <= 64 ? 8 : 6) : 4; }
+
+// True if an instantiation exists for (swap_ab, mma_n).
+constexpr bool gemm_shape_supported(bool swap_ab, int mma_n)
+{
+    return swap_ab ? (mma_n == 16 || mma_n == 32 || mma_n == 64 || mma_n == 128) : (mma_n == 256);
+}
+
+// ---- tensor maps (host_util.cu) ------------------------------------------------
+// 2-D tensor map over a row-major matrix of `rows` x `cols` elements with a
+// row stride of `row_bytes`, box = box_cols x box_rows, optional 128-byte
+// swizzle.  Returns false if the driver rejects it.
+bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, uint64_t cols, uint64_t rows,
+                  uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows, bool swizzle128);
+
+// ---- device status word (host_util.cu) --------------------------------------
+unsigned *device_status_ptr();   // of the current device, or null
+int current_device_sms();        // SM count of the current device (cached)
+
+}  // namespace fp8q
+
+namespace fp8q {
+// Copies the current device's status word to *value (synchronizing `st`);
+// reset clears it afterwards.
+cudaError_t read_status_word(unsigned *value, bool reset, cudaStream_t st);
+}  // namespace fp8q

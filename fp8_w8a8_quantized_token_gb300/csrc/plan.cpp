@@ -1,0 +1,184 @@
+// plan.cpp -- GEMM schedule selection (host only).
+//
+// A compiled-in table keyed by (N, K, scheme) holds the schedules the
+// build's own sweep on GB300 found fastest at a set of M values; a problem
+// takes the entry of the nearest M, ties going to the smaller M (the
+// nearest-M rule of get_w8a8_channelwise_fp8_config on the "Tune FP8 GEMM
+// Triton tiles on L40S and enable by default" page, key source snippets,
+// whose keys are scanned in ascending order).  Shapes without a table entry
+// use the generic rule.  fp8q_set_plan_override (or FP8Q_PLAN="swap,mma_n,
+// split" at start-up) forces a schedule for tests and sweeps; FP8Q_LOG=1
+// prints each new choice once to stderr.
+#include <stdio.h>
+#include <stdlib.h>
+
+#include <atomic>
+#include <mutex>
+#include <set>
+#include <tuple>
+
+#include "../../include/fp8q.h"
+#include "internal.h"
+
+namespace fp8q {
+namespace {
+
+struct TableEntry {
+    int64_t N, K;
+    int blockwise;
+    int64_t M;
+    int swap_ab, mma_n, split;
+};
+
+// Rows "{N, K, blockwise, M, swap_ab, mma_n, split}," from the sweep.
+const TableEntry kTable[] = {
+#include "tile_table.inc"
+    {0, 0, 0, 0, 0, 0, 0}};
+const int kTableSize = static_cast<int>(sizeof(kTable) / sizeof(kTable[0])) - 1;
+
+int next_pow2(int64_t v)
+{
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+// Generic rule: decode-size M puts the weights on the MMA's 128-row side
+// and the tokens on its N side (smallest MMA N >= M); larger M uses
+// 128 x 256 tiles.  If the tiles cannot fill the GPU, K is split across a
+// cluster of up to 8 CTAs.
+void generic_rule(int64_t M, int64_t N, int64_t K, int num_sms, fp8q_plan *pl)
+{
+    if (M <= 128) {
+        pl->swap_ab = 1;
+        pl->mma_n = next_pow2(M < 16 ? 16 : M);
+    } else {
+        pl->swap_ab = 0;
+        pl->mma_n = 256;
+    }
+    const int tile_m = pl->swap_ab ? pl->mma_n : 128;
+    const int tile_n = pl->swap_ab ? 128 : pl->mma_n;
+    const int64_t tiles = ((M + tile_m - 1) / tile_m) * ((N + tile_n - 1) / tile_n);
+    int64_t split = 1;
+    if (tiles < num_sms) split = num_sms / (tiles > 0 ? tiles : 1);
+    pl->split_k = static_cast<int32_t>(split);
+}
+
+// Process-wide schedule override (fp8q_set_plan_override), initialised
+// from FP8Q_PLAN="swap,mma_n,split".
+std::atomic<int> g_ovr_swap{-2}, g_ovr_n{0}, g_ovr_split{0};
+
+bool override_plan(fp8q_plan *pl)
+{
+    if (g_ovr_swap.load() == -2) {
+        int swap = -1, mma_n = 0, split = 0;
+        const char *s = getenv("FP8Q_PLAN");
+        if (s == nullptr || sscanf(s, "%d,%d,%d", &swap, &mma_n, &split) != 3 ||
+            !gemm_shape_supported(swap != 0, mma_n))
+            swap = -1;
+        g_ovr_n.store(mma_n);
+        g_ovr_split.store(split);
+        int expected = -2;
+        g_ovr_swap.compare_exchange_strong(expected, swap);
+    }
+    const int swap = g_ovr_swap.load();
+    if (swap < 0) return false;
+    pl->swap_ab = swap;
+    pl->mma_n = g_ovr_n.load();
+    pl->split_k = g_ovr_split.load();
+    return true;
+}
+
+bool table_plan(int64_t M, int64_t N, int64_t K, int blockwise, fp8q_plan *pl)
+{
+    const TableEntry *best = nullptr;
+    int64_t best_d = 0;
+    for (int i = 0; i < kTableSize; ++i) {
+        const TableEntry &e = kTable[i];
+        if (e.N != N || e.K != K || e.blockwise != blockwise) continue;
+        const int64_t d = e.M > M ? e.M - M : M - e.M;
+        if (best == nullptr || d < best_d || (d == best_d && e.M < best->M)) {
+            best = &e;
+            best_d = d;
+        }
+    }
+    if (best == nullptr || !gemm_shape_supported(best->swap_ab != 0, best->mma_n)) return false;
+    pl->swap_ab = best->swap_ab;
+    pl->mma_n = best->mma_n;
+    pl->split_k = best->split;
+    return true;
+}
+
+}  // namespace
+
+// Tile sizes, grid and persistence for a chosen (swap_ab, mma_n, split_k).
+void plan_finish(int64_t M, int64_t N, int64_t K, int num_sms, fp8q_plan *pl)
+{
+    pl->tile_m = pl->swap_ab ? pl->mma_n : 128;
+    pl->tile_n = pl->swap_ab ? 128 : pl->mma_n;
+    const int64_t tiles = ((M + pl->tile_m - 1) / pl->tile_m) * ((N + pl->tile_n - 1) / pl->tile_n);
+    const int64_t num_kb = (K + 127) / 128;
+    int64_t split = pl->split_k;
+    if (split > 8) split = 8;
+    if (split > num_kb) split = num_kb;
+    if (split < 1) split = 1;
+    pl->split_k = static_cast<int32_t>(split);
+    if (split > 1) {
+        pl->grid = static_cast<int32_t>(tiles * split);
+        pl->persistent = 0;
+    } else {
+        pl->grid = static_cast<int32_t>(tiles < num_sms ? tiles : num_sms);
+        pl->persistent = tiles > num_sms ? 1 : 0;
+    }
+    pl->stages = stages_for(pl->swap_ab != 0, pl->mma_n);
+}
+
+}  // namespace fp8q
+
+extern "C" fp8q_status fp8q_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t blockwise, int32_t num_sms,
+                                      fp8q_plan *plan)
+{
+    using namespace fp8q;
+    if (plan == nullptr || M < 0 || N <= 0 || K <= 0) return FP8Q_ERR_INVALID_ARG;
+    if (num_sms <= 0) {
+        num_sms = current_device_sms();
+        if (num_sms <= 0) return FP8Q_ERR_CUDA;
+    }
+    fp8q_plan pl = {};
+    if (override_plan(&pl)) {
+        pl.from_table = 0;
+    } else if (table_plan(M, N, K, blockwise ? 1 : 0, &pl)) {
+        pl.from_table = 1;
+    } else {
+        generic_rule(M, N, K, num_sms, &pl);
+        pl.from_table = 0;
+    }
+    plan_finish(M, N, K, num_sms, &pl);
+    static const bool log = getenv("FP8Q_LOG") != nullptr && getenv("FP8Q_LOG")[0] == '1';
+    if (log) {
+        static std::mutex mu;
+        static std::set<std::tuple<int64_t, int64_t, int64_t, int>> seen;
+        std::lock_guard<std::mutex> g(mu);
+        if (seen.insert(std::make_tuple(M, N, K, blockwise)).second)
+            fprintf(stderr, "fp8q plan M=%lld N=%lld K=%lld %s: swap_ab=%d mma_n=%d split_k=%d grid=%d%s\n",
+                    static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K),
+                    blockwise ? "blockwise" : "channelwise", pl.swap_ab, pl.mma_n, pl.split_k, pl.grid,
+                    pl.from_table ? " (table)" : "");
+    }
+    *plan = pl;
+    return FP8Q_OK;
+}
+
+extern "C" fp8q_status fp8q_set_plan_override(int32_t swap_ab, int32_t mma_n, int32_t split_k)
+{
+    using namespace fp8q;
+    if (swap_ab < 0) {
+        g_ovr_swap.store(-1);
+        return FP8Q_OK;
+    }
+    if (swap_ab > 1 || !gemm_shape_supported(swap_ab != 0, mma_n) || split_k < 1) return FP8Q_ERR_INVALID_ARG;
+    g_ovr_n.store(mma_n);
+    g_ovr_split.store(split_k);
+    g_ovr_swap.store(swap_ab);
+    return FP8Q_OK;
+}

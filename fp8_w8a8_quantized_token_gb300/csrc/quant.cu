@@ -1,0 +1,279 @@
+// quant.cu -- dynamic activation quantization bf16 -> E4M3 (and the 128x128
+// block weight quantizer used to prepare blockwise weights).
+//
+// Rule (all in fp32, IEEE division, no fast-math):
+//   s = max(amax(|x| over the group), eps) / 448
+//   q = cvt.rn.satfinite.e4m3(x / s)
+// Per-token groups are whole rows ("qinput"/"x_scale" of the channelwise
+// path, "Tune FP8 GEMM Triton tiles on L40S..." page, key source snippets);
+// per-token-group groups are g consecutive columns, written into a
+// row-padded buffer with column-major scales ("Remove per-call padding
+// overhead of the FP8 blockwise GEMM" page, key source snippets,
+// sglang_per_token_group_quant_fp8_row_padded).
+//
+// These kernels are HBM-bound streams (2 bytes in, 1 byte out per element):
+// 16-byte vector loads and stores, warp-shuffle amax reductions, no shared
+// memory staging needed.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace fp8q {
+namespace {
+
+// 16 consecutive bf16 values held as 8 packed registers.
+struct Chunk16 {
+    uint4 lo, hi;
+};
+
+__device__ __forceinline__ Chunk16 load_chunk(const __nv_bfloat16 *p)
+{
+    Chunk16 c;
+    c.lo = __ldg(reinterpret_cast<const uint4 *>(p));
+    c.hi = __ldg(reinterpret_cast<const uint4 *>(p) + 1);
+    return c;
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ float amax_word(uint32_t w, float m)
+{
+    return fmaxf(m, fmaxf(fabsf(bf_lo(w)), fabsf(bf_hi(w))));
+}
+
+__device__ __forceinline__ float chunk_amax(const Chunk16 &c, float m)
+{
+    m = amax_word(c.lo.x, m); m = amax_word(c.lo.y, m); m = amax_word(c.lo.z, m); m = amax_word(c.lo.w, m);
+    m = amax_word(c.hi.x, m); m = amax_word(c.hi.y, m); m = amax_word(c.hi.z, m); m = amax_word(c.hi.w, m);
+    return m;
+}
+
+// Four bf16 (two words) / s -> four E4M3 bytes packed little-endian.
+__device__ __forceinline__ uint32_t quant4(uint32_t w0, uint32_t w1, float s)
+{
+    const uint32_t a = cvt_e4m3x2(bf_lo(w0) / s, bf_hi(w0) / s);
+    const uint32_t b = cvt_e4m3x2(bf_lo(w1) / s, bf_hi(w1) / s);
+    return a | (b << 16);
+}
+
+__device__ __forceinline__ uint4 quant_chunk(const Chunk16 &c, float s)
+{
+    uint4 q;
+    q.x = quant4(c.lo.x, c.lo.y, s);
+    q.y = quant4(c.lo.z, c.lo.w, s);
+    q.z = quant4(c.hi.x, c.hi.y, s);
+    q.w = quant4(c.hi.z, c.hi.w, s);
+    return q;
+}
+
+__device__ __forceinline__ float scale_of(float amax, float eps) { return fmaxf(amax, eps) / 448.0f; }
+
+// ---------------------------------------------------------------------------
+// Per-token quantization: one CTA per row, blockDim.x = T (multiple of 32),
+// each thread caches up to VPT 16-element chunks in registers so the row is
+// read from HBM exactly once.  Rows longer than T*VPT chunks take the
+// two-pass kernel below.
+// ---------------------------------------------------------------------------
+template <int VPT>
+__global__ void __launch_bounds__(1024) quant_per_token_kernel(const __nv_bfloat16 *__restrict__ x, int64_t ldx,
+                                                               uint8_t *__restrict__ xq, float *__restrict__ xs,
+                                                               int K, float eps)
+{
+    __shared__ float warp_max[32];
+    const int64_t row = blockIdx.x;
+    const int chunks = K >> 4;
+    const __nv_bfloat16 *xr = x + row * ldx;
+    Chunk16 c[VPT];
+    float m = 0.0f;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int ci = threadIdx.x + v * blockDim.x;
+        if (ci < chunks) {
+            c[v] = load_chunk(xr + (ci << 4));
+            m = chunk_amax(c[v], m);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (blockDim.x > 32) {
+        if (lane == 0) warp_max[warp] = m;
+        __syncthreads();
+        m = (lane < (blockDim.x >> 5)) ? warp_max[lane] : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    }
+    const float s = scale_of(m, eps);
+    if (threadIdx.x == 0) xs[row] = s;
+    uint8_t *qr = xq + row * static_cast<int64_t>(K);
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int ci = threadIdx.x + v * blockDim.x;
+        if (ci < chunks) *reinterpret_cast<uint4 *>(qr + (ci << 4)) = quant_chunk(c[v], s);
+    }
+}
+
+__global__ void __launch_bounds__(1024) quant_per_token_two_pass_kernel(const __nv_bfloat16 *__restrict__ x,
+                                                                        int64_t ldx, uint8_t *__restrict__ xq,
+                                                                        float *__restrict__ xs, int K, float eps)
+{
+    __shared__ float warp_max[32];
+    const int64_t row = blockIdx.x;
+    const int chunks = K >> 4;
+    const __nv_bfloat16 *xr = x + row * ldx;
+    float m = 0.0f;
+    for (int ci = threadIdx.x; ci < chunks; ci += blockDim.x) m = chunk_amax(load_chunk(xr + (ci << 4)), m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) warp_max[warp] = m;
+    __syncthreads();
+    m = (lane < (blockDim.x >> 5)) ? warp_max[lane] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float s = scale_of(m, eps);
+    if (threadIdx.x == 0) xs[row] = s;
+    uint8_t *qr = xq + row * static_cast<int64_t>(K);
+    for (int ci = threadIdx.x; ci < chunks; ci += blockDim.x)
+        *reinterpret_cast<uint4 *>(qr + (ci << 4)) = quant_chunk(load_chunk(xr + (ci << 4)), s);
+}
+
+// ---------------------------------------------------------------------------
+// Per-token-group quantization into the row-padded buffer.  TPG = g / 16
+// threads own one group (16 elements each); the amax is reduced with XOR
+// shuffles inside aligned TPG-lane segments.  Consecutive threads walk a row
+// left to right, so loads and stores are fully coalesced; the scale of
+// (row r, group j) goes to xs[j * m_pad + r].
+// ---------------------------------------------------------------------------
+template <int TPG>
+__global__ void __launch_bounds__(256) quant_group_kernel(const __nv_bfloat16 *__restrict__ x, int64_t ldx,
+                                                          uint8_t *__restrict__ xq, float *__restrict__ xs,
+                                                          int64_t M, int K, int64_t m_pad, float eps)
+{
+    const int chunks_per_row = K >> 4;
+    const int64_t total = M * chunks_per_row;
+    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+         t - (threadIdx.x & 31) < total;  // whole warps stay in the loop for the shuffles
+         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const bool active = t < total;
+        const int64_t row = active ? t / chunks_per_row : 0;
+        const int ci = active ? static_cast<int>(t - row * chunks_per_row) : 0;
+        Chunk16 c;
+        float m = 0.0f;
+        if (active) {
+            c = load_chunk(x + row * ldx + (ci << 4));
+            m = chunk_amax(c, 0.0f);
+        }
+#pragma unroll
+        for (int o = TPG >> 1; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (active) {
+            const float s = scale_of(m, eps);
+            *reinterpret_cast<uint4 *>(xq + row * static_cast<int64_t>(K) + (ci << 4)) = quant_chunk(c, s);
+            if ((ci & (TPG - 1)) == 0) xs[static_cast<int64_t>(ci / TPG) * m_pad + row] = s;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 128 x 128 block weight quantization: one CTA (256 threads) per block.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) quant_weight_block128_kernel(const __nv_bfloat16 *__restrict__ w,
+                                                                    uint8_t *__restrict__ wq,
+                                                                    float *__restrict__ ws, int64_t K, float eps)
+{
+    __shared__ float warp_max[8];
+    const int64_t bn = blockIdx.y, bk = blockIdx.x;
+    // 128 rows x 8 chunks of 16; thread t handles chunks t, t + 256, ...
+    Chunk16 c[4];
+    float m = 0.0f;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const int idx = threadIdx.x + v * 256;
+        const int r = idx >> 3, cc = idx & 7;
+        c[v] = load_chunk(w + (bn * 128 + r) * K + bk * 128 + cc * 16);
+        m = chunk_amax(c[v], m);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = warp_max[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) m = fmaxf(m, warp_max[i]);
+    const float s = scale_of(m, eps);
+    if (threadIdx.x == 0) ws[bn * (K >> 7) + bk] = s;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const int idx = threadIdx.x + v * 256;
+        const int r = idx >> 3, cc = idx & 7;
+        *reinterpret_cast<uint4 *>(wq + (bn * 128 + r) * K + bk * 128 + cc * 16) = quant_chunk(c[v], s);
+    }
+}
+
+template <int VPT>
+cudaError_t launch_per_token(const void *x, int64_t M, int K, int64_t ldx, void *xq, float *xs, float eps, int threads,
+                             cudaStream_t st)
+{
+    quant_per_token_kernel<VPT><<<static_cast<unsigned>(M), threads, 0, st>>>(
+        static_cast<const __nv_bfloat16 *>(x), ldx, static_cast<uint8_t *>(xq), xs, K, eps);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quant_per_token(const void *x, int64_t M, int64_t K, int64_t ldx, void *xq, float *xs, float eps,
+                                   cudaStream_t st)
+{
+    const int chunks = static_cast<int>(K >> 4);
+    // Threads per row: enough that each thread holds at most 4 chunks, in
+    // whole warps, at most 1024.
+    int threads = ((chunks + 3) / 4 + 31) / 32 * 32;
+    if (threads > 1024) threads = 1024;
+    if (threads < 32) threads = 32;
+    const int vpt = (chunks + threads - 1) / threads;
+    switch (vpt) {
+        case 1: return launch_per_token<1>(x, M, static_cast<int>(K), ldx, xq, xs, eps, threads, st);
+        case 2: return launch_per_token<2>(x, M, static_cast<int>(K), ldx, xq, xs, eps, threads, st);
+        case 3: return launch_per_token<3>(x, M, static_cast<int>(K), ldx, xq, xs, eps, threads, st);
+        case 4: return launch_per_token<4>(x, M, static_cast<int>(K), ldx, xq, xs, eps, threads, st);
+        default:
+            quant_per_token_two_pass_kernel<<<static_cast<unsigned>(M), 1024, 0, st>>>(
+                static_cast<const __nv_bfloat16 *>(x), ldx, static_cast<uint8_t *>(xq), xs, static_cast<int>(K), eps);
+            return cudaGetLastError();
+    }
+}
+
+cudaError_t launch_quant_group(const void *x, int64_t M, int64_t K, int64_t ldx, int group, void *xq, float *xs,
+                               int64_t m_pad, float eps, int num_sms, cudaStream_t st)
+{
+    const int64_t total = M * (K >> 4);
+    const int threads = 256;
+    int64_t blocks = (total + threads - 1) / threads;
+    const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 148) * 64;
+    if (blocks > cap) blocks = cap;
+    const auto *xb = static_cast<const __nv_bfloat16 *>(x);
+    auto *q = static_cast<uint8_t *>(xq);
+    const unsigned b = static_cast<unsigned>(blocks);
+    switch (group) {
+        case 16: quant_group_kernel<1><<<b, threads, 0, st>>>(xb, ldx, q, xs, M, static_cast<int>(K), m_pad, eps); break;
+        case 32: quant_group_kernel<2><<<b, threads, 0, st>>>(xb, ldx, q, xs, M, static_cast<int>(K), m_pad, eps); break;
+        case 64: quant_group_kernel<4><<<b, threads, 0, st>>>(xb, ldx, q, xs, M, static_cast<int>(K), m_pad, eps); break;
+        default: quant_group_kernel<8><<<b, threads, 0, st>>>(xb, ldx, q, xs, M, static_cast<int>(K), m_pad, eps); break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_weight_block128(const void *w, int64_t N, int64_t K, void *wq, float *ws, float eps,
+                                         cudaStream_t st)
+{
+    dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(N / 128));
+    quant_weight_block128_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(w),
+                                                        static_cast<uint8_t *>(wq), ws, K, eps);
+    return cudaGetLastError();
+}
+
+}  // namespace fp8q

@@ -1,0 +1,241 @@
+/*
+ * fp8q.h -- C ABI of libfp8q: the FP8 W8A8 linear layer on NVIDIA GB300
+ * (sm_103a).
+ *
+ * Two steps make up the layer:
+ *   1. dynamic activation quantization, bf16 -> E4M3 (torch.float8_e4m3fn),
+ *      either one fp32 scale per token (row) or one per (token, 128-column
+ *      group) written into a row-padded buffer with column-major scales;
+ *   2. the scaled FP8 GEMM, either per-token x per-output-channel scales or
+ *      1x128 (activation) x 128x128 (weight) blockwise scales, with fp32
+ *      accumulation, optional bias and bf16 (or fp16) output.
+ *
+ * Sources, cited by page title and section:
+ *   [PR34331] "Tune FP8 GEMM Triton tiles on L40S and enable by default"
+ *             (sgl-project/sglang PR 34331), "Key source snippets":
+ *             apply_fp8_linear's channelwise branch calling
+ *             fp8_scaled_mm(qinput, weight, x_scale, weight_scale,
+ *             out_dtype, bias); the weight is [K, N]; the nearest-M tile
+ *             lookup get_w8a8_channelwise_fp8_config.
+ *   [PR27896] "Remove per-call padding overhead of the FP8 blockwise GEMM"
+ *             (sgl-project/sglang PR 27896), "Key source snippets":
+ *             sglang_per_token_group_quant_fp8_row_padded(x, group_size,
+ *             eps=1e-10, row_alignment=4) and
+ *             cutlass_w8a8_block_fp8_linear_with_fallback, which calls
+ *             fp8_blockwise_scaled_mm(q_input, weight.T, x_scale,
+ *             weight_scale.T, out_dtype) and slices the output to M rows.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named x, a, b, w, bias, out, *_scale and the quantized
+ *     buffers are DEVICE pointers owned by the caller.  The library never
+ *     allocates, frees or synchronizes; it only enqueues kernels.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  All work is asynchronous on that stream.
+ *   - "bf16" data is bfloat16, "e4m3" data is one byte per element in the
+ *     float8_e4m3fn encoding, scales are IEEE fp32.
+ *   - Matrices are row-major with the given leading dimension (elements).
+ *   - Device pointers to matrix data must be 16-byte aligned and leading
+ *     dimensions must keep every row 16-byte aligned (the kernels use
+ *     16-byte vector accesses and the Tensor Memory Accelerator).
+ *   - Return value: FP8Q_OK, or an error code; on an error nothing was
+ *     enqueued.  FP8Q_ERR_CUDA reports a failed launch (cudaGetLastError is
+ *     consumed).  A GEMM whose internal pipeline wait exceeds its time limit
+ *     records FP8Q_ERR_TIMEOUT in a device status word and returns early
+ *     instead of hanging; read it with fp8q_device_status().
+ *   - M == 0 is valid and enqueues nothing.
+ *   - No C++ exception crosses this interface.
+ */
+#ifndef FP8Q_H_
+#define FP8Q_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FP8Q_API __attribute__((visibility("default")))
+#else
+#define FP8Q_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8Q_OK = 0,
+    FP8Q_ERR_INVALID_ARG = 1, /* null pointer, bad size, stride or alignment */
+    FP8Q_ERR_UNSUPPORTED = 2, /* a shape or option this build does not implement */
+    FP8Q_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+    FP8Q_ERR_TIMEOUT = 4      /* a device-side pipeline wait ran out of time */
+} fp8q_status;
+
+typedef enum { FP8Q_OUT_BF16 = 0, FP8Q_OUT_FP16 = 1 } fp8q_out_dtype;
+
+/* Largest finite E4M3 value: the quantizers map amax to +-448. */
+#define FP8Q_E4M3_MAX 448.0f
+
+/* ---------------------------------------------------------------------------
+ * fp8q_quant_per_token -- per-token dynamic quantization.
+ * Defined by the channelwise path of [PR34331] "Key source snippets"
+ * (qinput with one x_scale entry per row):
+ *   s[m]    = max(amax_k |x[m,k]|, eps) / 448          (fp32, IEEE division)
+ *   xq[m,k] = e4m3_rne_satfinite(x[m,k] / s[m])        (fp32 quotient)
+ * x       : bf16 [M, K], row stride ldx >= K (ldx % 8 == 0), 16-byte aligned.
+ * xq      : e4m3 [M, K], row stride K (K % 16 == 0), 16-byte aligned.
+ * x_scale : fp32 [M].
+ * eps     : floor on amax (the pages use 1e-10); must be > 0 and finite.
+ * Errors  : INVALID_ARG for M < 0, K <= 0, K % 16 != 0, ldx < K, ldx % 8,
+ *           null or misaligned pointers, eps <= 0.
+ * ------------------------------------------------------------------------- */
+FP8Q_API fp8q_status fp8q_quant_per_token(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                 void *xq, float *x_scale, float eps, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * fp8q_quant_per_token_group_row_padded -- per-token-group quantization into
+ * a row-padded buffer, [PR27896] "Key source snippets"
+ * (sglang_per_token_group_quant_fp8_row_padded):
+ *   for each row m < M and group j < K/g:
+ *     s        = max(amax over x[m, j*g : (j+1)*g], eps) / 448
+ *     x_scale[j * m_pad + m] = s            (column-major (m_pad, K/g) view)
+ *     xq[m, j*g + i] = e4m3_rne_satfinite(x[m, j*g + i] / s)
+ *   Rows m >= M of xq and of x_scale are NEVER written (the caller's
+ *   padding; the GEMM never lets them reach the first M output rows).
+ * x          : bf16 [M, K], row stride ldx >= K (ldx % 8 == 0).
+ * group_size : g in {16, 32, 64, 128}; K % g == 0.
+ * row_alignment : the padding multiple (the pages use 4); m_pad >= M and
+ *              m_pad % row_alignment == 0 (the pages allocate
+ *              m_pad = ceil(M / row_alignment) * row_alignment).
+ * xq         : e4m3 [m_pad, K], row stride K (K % 16 == 0).
+ * x_scale    : fp32 storage of K/g columns of m_pad entries (column-major).
+ * Errors     : INVALID_ARG for bad sizes, m_pad < M, m_pad % row_alignment,
+ *              K % g, null or misaligned pointers; UNSUPPORTED for other g.
+ * ------------------------------------------------------------------------- */
+FP8Q_API fp8q_status fp8q_quant_per_token_group_row_padded(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                                  int32_t group_size, float eps,
+                                                  int32_t row_alignment, void *xq,
+                                                  float *x_scale, int64_t m_pad, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * fp8q_quant_weight_block128 -- weight preparation for the blockwise GEMM
+ * (one fp32 scale per 128 x 128 block, same scale and cast rule as the
+ * activations).  Not on the per-call hot path: weights are quantized once.
+ * w       : bf16 [N, K] row-major (ld = K), N % 128 == 0, K % 128 == 0.
+ * wq      : e4m3 [N, K]; w_scale: fp32 [N/128][K/128] row-major.
+ * ------------------------------------------------------------------------- */
+FP8Q_API fp8q_status fp8q_quant_weight_block128(const void *w, int64_t N, int64_t K, void *wq,
+                                       float *w_scale, float eps, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * fp8q_scaled_mm_channelwise -- [PR34331] "Key source snippets",
+ * fp8_scaled_mm(qinput, weight, x_scale, weight_scale, out_dtype, bias):
+ *   out[m,n] = cvt( (sum_k a[m,k] * b[k,n]) * a_scale[m] * b_scale[n]
+ *                   (+ bias[n]) )
+ *   fp32 accumulation; one rounding to the output type.
+ * a       : e4m3 [M, K] row-major, ld = K (K % 16 == 0).
+ * b       : e4m3 weight, logically [K, N], stored K-contiguous: element
+ *           (k, n) at b[n * ldb + k]  (i.e. an [N, K] row-major matrix);
+ *           ldb >= K, ldb % 16 == 0.
+ * a_scale : fp32 [M]; b_scale : fp32 [N]; bias : bf16 [N] or NULL.
+ * out     : [M, N] row-major (ld = N) of out_dtype (N % 8 == 0).
+ * Errors  : INVALID_ARG / UNSUPPORTED as above.
+ * ------------------------------------------------------------------------- */
+FP8Q_API fp8q_status fp8q_scaled_mm_channelwise(const void *a, const void *b, int64_t ldb,
+                                       const float *a_scale, const float *b_scale,
+                                       const void *bias, void *out, int64_t M, int64_t N,
+                                       int64_t K, fp8q_out_dtype out_dtype, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * fp8q_scaled_mm_blockwise -- [PR27896] "Key source snippets",
+ * fp8_blockwise_scaled_mm(q_input, weight.T, x_scale, weight_scale.T) with
+ * the output sliced to the first M rows and the bias added after:
+ *   out[m,n] = cvt( sum_kb P_kb(m,n) * a_scale[kb * m_pad + m]
+ *                                   * w_scale[(n/128) * (K/128) + kb]
+ *                   (+ bias[n]) ),
+ *   P_kb(m,n) = sum over the 128 k of block kb of a[m,k] * w[n,k]
+ * a       : e4m3 [m_pad, K] (the row-padded quantizer's output); rows >= M
+ *           are ignored, whatever they hold.
+ * w       : e4m3 [N, K] row-major; N % 128 == 0, K % 128 == 0.
+ * a_scale : fp32 column-major activation scales, K/128 columns of m_pad.
+ * w_scale : fp32 [N/128][K/128] row-major.
+ * bias    : bf16 [N] or NULL.   out : [M, N] row-major of out_dtype.
+ * m_pad   : >= M and a multiple of 4 (keeps each scale column 16-byte
+ *           aligned for the Tensor Memory Accelerator).
+ * Errors  : UNSUPPORTED when N or K is not a multiple of 128 (the pages
+ *           fall back to another kernel there; this library refuses).
+ * ------------------------------------------------------------------------- */
+FP8Q_API fp8q_status fp8q_scaled_mm_blockwise(const void *a, const void *w, const float *a_scale,
+                                     const float *w_scale, const void *bias, void *out,
+                                     int64_t M, int64_t m_pad, int64_t N, int64_t K,
+                                     fp8q_out_dtype out_dtype, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Linear-layer compositions (two launches each, no padding copies):
+ * quantize x into the caller's buffers, then run the GEMM on them.
+ * fp8q_linear_channelwise : xq e4m3 [M, K], xs fp32 [M].
+ * fp8q_linear_blockwise   : xq e4m3 [m_pad, K], xs fp32 [K/128][m_pad],
+ *   m_pad = ceil(M/4)*4 or a larger multiple of 4 -- the row-padded
+ *   pipeline of [PR27896] "Implementation breakdown" (quantizer writes the
+ *   GEMM's final layout; output sliced to M rows).
+ * ------------------------------------------------------------------------- */
+FP8Q_API fp8q_status fp8q_linear_channelwise(const void *x, const void *b, int64_t ldb,
+                                    const float *b_scale, const void *bias, void *out,
+                                    int64_t M, int64_t N, int64_t K, void *xq, float *xs,
+                                    fp8q_out_dtype out_dtype, void *stream);
+FP8Q_API fp8q_status fp8q_linear_blockwise(const void *x, const void *w, const float *w_scale,
+                                  const void *bias, void *out, int64_t M, int64_t N, int64_t K,
+                                  void *xq, float *xs, int64_t m_pad, fp8q_out_dtype out_dtype,
+                                  void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Tile selection (host only, no GPU needed).  The GEMM schedule for a
+ * problem: which operand sits on the MMA's 128-row side, the MMA N extent,
+ * the K-split count (CTAs of one thread-block cluster that share a tile and
+ * reduce their partial sums in distributed shared memory), pipeline depth
+ * and grid size.  The choice comes from a compiled-in table keyed by
+ * (N, K, scheme) with nearest-M lookup, ties to the smaller M, as in
+ * get_w8a8_channelwise_fp8_config of [PR34331] "Key source snippets";
+ * shapes without an entry use a generic rule.  num_sms <= 0 means "ask the
+ * current device".  Errors: INVALID_ARG for M < 0, N <= 0, K <= 0 or a null
+ * plan; ERR_CUDA if the SM count cannot be read.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    int32_t swap_ab;    /* 1: 128 weight rows x mma_n tokens per tile (decode);
+                           0: 128 tokens x mma_n weight rows per tile (prefill) */
+    int32_t mma_n;      /* tcgen05.mma N extent: 16, 32, 64, 128 or 256 */
+    int32_t tile_m;     /* tokens per output tile */
+    int32_t tile_n;     /* output columns per output tile */
+    int32_t split_k;    /* CTAs per cluster sharing one tile along K (1..8) */
+    int32_t stages;     /* shared-memory pipeline depth */
+    int32_t grid;       /* CTAs launched */
+    int32_t persistent; /* 1: CTAs loop over several tiles */
+    int32_t from_table; /* 1: taken from the compiled-in table */
+} fp8q_plan;
+
+FP8Q_API fp8q_status fp8q_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t blockwise, int32_t num_sms,
+                           fp8q_plan *plan);
+
+/* Force the schedule of every following GEMM in this process (for tests
+ * and tuning sweeps): swap_ab in {0, 1} with an mma_n that has a kernel
+ * instantiation (swapped: 16, 32, 64, 128; non-swapped: 256) and
+ * split_k >= 1 (clamped to 8 and to the number of 128-wide K blocks).
+ * swap_ab < 0 removes the override.  Errors: INVALID_ARG for a
+ * combination without an instantiation.  Not thread-safe with concurrent
+ * GEMM calls. */
+FP8Q_API fp8q_status fp8q_set_plan_override(int32_t swap_ab, int32_t mma_n, int32_t split_k);
+
+/* Device status word: returns FP8Q_OK or the first device-side error the
+ * GEMM kernels recorded on the current device (FP8Q_ERR_TIMEOUT).
+ * Synchronizes `stream`.  reset != 0 clears the word afterwards. */
+FP8Q_API fp8q_status fp8q_device_status(void *stream, int32_t reset);
+
+/* Human-readable name of a status code (static string). */
+FP8Q_API const char *fp8q_status_str(fp8q_status status);
+
+/* ABI version: (major << 16) | minor. */
+FP8Q_API int32_t fp8q_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8Q_H_ */

@@ -1,0 +1,174 @@
+"""GPU parity of the scaled FP8 GEMMs through the C ABI against the oracle,
+element by element, within |gpu - ref| <= 1e-2 * (|ref| + 1).
+
+Both sides quantize the same seeded bf16 inputs independently (the codes
+and scales are first checked bit-exact), then each side runs its own GEMM.
+Every kernel instantiation and K-split is exercised by forcing the
+schedule, on shapes with ragged M, N and K tails."""
+import numpy as np
+import pytest
+import torch
+
+import fp8_w8a8_quantized_token_gb300 as fq
+import oracle
+import synthetic
+from gpu_util import (THREADS, assert_gemm_close, out_values, quant_both_group, quant_both_per_token, ref_values,
+                      u8)
+
+pytestmark = pytest.mark.gpu
+
+SCHEDULES = [(1, 16, 1), (1, 16, 3), (1, 32, 2), (1, 32, 8), (1, 64, 1), (1, 64, 4), (1, 128, 1), (1, 128, 2),
+             (0, 256, 1), (0, 256, 2), (0, 256, 5)]
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import __graft_entry__
+    __graft_entry__.build()
+    d = torch.device("cuda", 0)
+    torch.cuda.set_device(d)
+    fq.fp8q_set_plan_override(-1)
+    return d
+
+
+@pytest.fixture
+def schedule():
+    yield
+    fq.fp8q_set_plan_override(-1)
+
+
+def channelwise_case(dev, M, N, K, seed=0, bias=False, outliers=True, out_dtype=torch.bfloat16):
+    x = synthetic.activations(M, K, seed=seed, outliers=outliers)
+    w = synthetic.weights(N, K, seed=seed)
+    b = synthetic.bias(N, seed=seed) if bias else None
+    xq, xs, rq, rs = quant_both_per_token(x, dev)
+    wq, ws, rwq, rws = quant_both_per_token(w, dev)
+    out = fq.fp8q_scaled_mm_channelwise(xq, wq, xs, ws, bias=None if b is None else b.to(dev),
+                                        out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    fp16 = out_dtype == torch.float16
+    ref = ref_values(oracle.gemm_channelwise(rq, rwq, rs, rws, bias=b, out_fp16=fp16, threads=THREADS), fp16)
+    return out, ref
+
+
+def test_tiny_layer_with_bias(dev):
+    out, ref = channelwise_case(dev, 16, 256, 512, bias=True, outliers=False)
+    assert_gemm_close(out_values(out), ref, "16x256x512+bias")
+
+
+@pytest.mark.parametrize("swap,mma_n,split", SCHEDULES)
+def test_channelwise_every_schedule(dev, schedule, swap, mma_n, split):
+    fq.fp8q_set_plan_override(swap, mma_n, split)
+    for M in (1, 70, 300):
+        out, ref = channelwise_case(dev, M, 392, 1040, seed=M, bias=True)
+        assert_gemm_close(out_values(out), ref, f"sched {swap},{mma_n},{split} M={M}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 5, 16, 33, 64, 100, 128, 129, 256, 300, 512])
+def test_channelwise_default_plan(dev, M):
+    out, ref = channelwise_case(dev, M, 384, 1024, seed=M)
+    assert_gemm_close(out_values(out), ref, f"M={M}")
+
+
+def test_channelwise_fp16_output(dev):
+    out, ref = channelwise_case(dev, 40, 256, 512, bias=True, out_dtype=torch.float16)
+    assert out.dtype == torch.float16
+    assert_gemm_close(out_values(out), ref, "fp16")
+
+
+def test_channelwise_strided_weight_and_output_canary(dev):
+    M, N, K, ldb = 24, 256, 512, 640
+    x = synthetic.activations(M, K, seed=11)
+    wbig = synthetic.weights(N, ldb, seed=11)
+    xq, xs, rq, rs = quant_both_per_token(x, dev)
+    wq_full, ws = fq.fp8q_quant_per_token(wbig.to(dev)[:, :K].contiguous())
+    wstore = torch.zeros((N, ldb), dtype=fq.E4M3, device=dev)
+    wstore[:, :K] = wq_full
+    out_buf = torch.full((M + 2, N), 7.0, dtype=torch.bfloat16, device=dev)
+    fq.fp8q_scaled_mm_channelwise(xq, wstore[:, :K], xs, ws, out=out_buf[:M])
+    torch.cuda.synchronize()
+    ref = ref_values(oracle.gemm_channelwise(rq, u8(wq_full), rs, ws.cpu().numpy()))
+    assert_gemm_close(out_values(out_buf[:M]), ref, "strided b")
+    assert torch.all(out_buf[M:] == 7.0)
+
+
+def blockwise_case(dev, M, N, K, seed=0, bias=False, outliers=True, garbage_padding=False):
+    x = synthetic.activations(M, K, seed=seed, outliers=outliers)
+    w = synthetic.weights(N, K, seed=seed)
+    b = synthetic.bias(N, seed=seed) if bias else None
+    fills = dict(xq_fill=0x7F, xs_fill=float("nan")) if garbage_padding else {}
+    xq, xs, rq, rs = quant_both_group(x, dev, 128, **fills)
+    wq, ws = fq.fp8q_quant_weight_block128(w.to(dev))
+    torch.cuda.synchronize()
+    rwq, rws = oracle.quant_weight_blocks(w, 128, 128)
+    assert np.array_equal(u8(wq), rwq) and np.array_equal(ws.cpu().numpy(), rws)
+    out = fq.fp8q_scaled_mm_blockwise(xq, wq, xs, ws, M=M, bias=None if b is None else b.to(dev))
+    torch.cuda.synchronize()
+    return out, (x, w, b, rq, rs, rwq, rws)
+
+
+def blockwise_ref(ctx, M, threads=THREADS):
+    x, w, b, rq, rs, rwq, rws = ctx
+    return ref_values(oracle.gemm_blockwise(rq, rwq, rs, rws, M, bias=b, threads=threads))
+
+
+@pytest.mark.parametrize("swap,mma_n,split", SCHEDULES)
+def test_blockwise_every_schedule(dev, schedule, swap, mma_n, split):
+    fq.fp8q_set_plan_override(swap, mma_n, split)
+    for M in (3, 70, 260):
+        out, ctx = blockwise_case(dev, M, 384, 1024, seed=M, bias=True)
+        assert_gemm_close(out_values(out), blockwise_ref(ctx, M), f"sched {swap},{mma_n},{split} M={M}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 13, 16, 31, 64, 256])
+def test_blockwise_decode_layer_full_size(dev, M):
+    """The row-padded decode layer: N = 4096, K = 7168, every M of the
+    row-padding page's test, padding rows filled with NaN codes and NaN
+    scales (they must not reach the output)."""
+    out, ctx = blockwise_case(dev, M, 4096, 7168, seed=M, garbage_padding=True)
+    got = out_values(out)
+    assert got.shape == (M, 4096)
+    if M <= 16:
+        assert_gemm_close(got, blockwise_ref(ctx, M), f"M={M}")
+    else:
+        rng = np.random.default_rng(M)
+        ms, ns = rng.integers(0, M, 4096), rng.integers(0, 4096, 4096)
+        _, _, b, rq, rs, rwq, rws = ctx
+        ref = ref_values(oracle.gemm_blockwise_at(rq, rwq, rs, rws, ms, ns, bias=b))
+        assert_gemm_close(got[ms, ns], ref, f"M={M} sampled")
+
+
+def test_blockwise_padding_rows_do_not_matter(dev):
+    M = 13
+    out1, _ = blockwise_case(dev, M, 512, 1024, seed=9, garbage_padding=True)
+    out2, _ = blockwise_case(dev, M, 512, 1024, seed=9, garbage_padding=False)
+    assert torch.equal(out1, out2)
+
+
+def test_linear_compositions(dev):
+    M, N, K = 37, 256, 1024
+    x = synthetic.activations(M, K, seed=4, outliers=True)
+    w = synthetic.weights(N, K, seed=4)
+    b = synthetic.bias(N, seed=4)
+    wq, ws = fq.fp8q_quant_per_token(w.to(dev))
+    out = fq.fp8q_linear_channelwise(x.to(dev), wq, ws, bias=b.to(dev))
+    torch.cuda.synchronize()
+    rq, rs = oracle.quant_per_token(x)
+    ref = ref_values(oracle.gemm_channelwise(rq, u8(wq), rs, ws.cpu().numpy(), bias=b))
+    assert_gemm_close(out_values(out), ref, "linear channelwise")
+    wq, ws = fq.fp8q_quant_weight_block128(w.to(dev))
+    out = fq.fp8q_linear_blockwise(x.to(dev), wq, ws, bias=b.to(dev))
+    torch.cuda.synchronize()
+    assert out.shape == (M, N)
+    rq, rs = oracle.quant_group_row_padded(x, 128)
+    ref = ref_values(oracle.gemm_blockwise(rq, u8(wq), rs, ws.cpu().numpy(), M, bias=b))
+    assert_gemm_close(out_values(out), ref, "linear blockwise")
+
+
+def test_m0_and_status_word(dev):
+    a = torch.empty((0, 256), dtype=fq.E4M3, device=dev)
+    w = torch.zeros((128, 256), dtype=fq.E4M3, device=dev)
+    s = torch.ones(128, dtype=torch.float32, device=dev)
+    out = fq.fp8q_scaled_mm_channelwise(a, w, torch.empty(0, device=dev), s)
+    assert out.shape == (0, 128)
+    assert fq.fp8q_device_status() == fq.FP8Q_OK

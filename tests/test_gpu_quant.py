@@ -1,0 +1,114 @@
+"""GPU parity of the quantizers through the C ABI: codes and fp32 scales
+bit-exact against the oracle on the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import fp8_w8a8_quantized_token_gb300 as fq
+import oracle
+import synthetic
+from gpu_util import THREADS, quant_both_group, quant_both_per_token, u8
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import __graft_entry__
+    __graft_entry__.build()
+    d = torch.device("cuda", 0)
+    torch.cuda.set_device(d)
+    return d
+
+
+@pytest.mark.parametrize("M,K,outliers", [
+    (16, 512, False),        # the tiny channelwise layer
+    (1, 4096, True), (7, 4096, True), (300, 4096, True),
+    (33, 12288, True), (5, 16, False), (64, 7168, False), (3, 3072, True),
+    (2, 65552, False),       # longer than the register-cached path: two-pass kernel
+])
+def test_per_token_bit_exact(dev, M, K, outliers):
+    x = synthetic.activations(M, K, seed=M * 7 + K, outliers=outliers)
+    quant_both_per_token(x, dev)
+
+
+def test_per_token_strided_input_and_no_overrun(dev):
+    M, K, ldx = 9, 1024, 1536
+    big = synthetic.activations(M, ldx, seed=3, outliers=True)
+    x_gpu = big.to(dev)[:, :K]
+    xq = torch.empty((M + 1, K), dtype=fq.E4M3, device=dev)
+    xq.view(torch.uint8).fill_(0x5A)
+    xs = torch.full((M + 4,), -1.0, dtype=torch.float32, device=dev)
+    fq.fp8q_quant_per_token(x_gpu, xq=xq[:M], x_scale=xs)
+    torch.cuda.synchronize()
+    rq, rs = oracle.quant_per_token(big[:, :K].contiguous())
+    assert np.array_equal(u8(xq)[:M], rq)
+    assert np.array_equal(xs.cpu().numpy()[:M], rs)
+    assert np.all(u8(xq)[M] == 0x5A) and np.all(xs.cpu().numpy()[M:] == -1.0)
+
+
+def test_per_token_special_rows(dev):
+    K = 256
+    x = torch.zeros((6, K), dtype=torch.float32)
+    x[1, 3] = 1e-12                 # below the eps floor
+    x[2] = torch.linspace(-448, 448, K)
+    x[3, :] = -0.0
+    x[4, 0] = 3e38                  # huge amax: everything else underflows (signed zeros)
+    x[4, 1:] = -torch.linspace(1, 2, K - 1)
+    x[5] = torch.tensor([(-1) ** i * 2.0 ** (-(i % 20)) for i in range(K)])
+    quant_both_per_token(x.to(torch.bfloat16), dev)
+
+
+def test_per_token_m0_is_noop(dev):
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device=dev)
+    xq, xs = fq.fp8q_quant_per_token(x)
+    assert xq.shape == (0, 64) and xs.shape == (0,)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 13, 16, 31, 64, 256])
+def test_group_row_padded_decode_sizes(dev, M):
+    x = synthetic.activations(M, 7168, seed=M)
+    xq, xs, _, _ = quant_both_group(x, dev, 128, xq_fill=0xA5, xs_fill=-7.0)
+    m_pad = fq.ceil_align(M, 4)
+    assert xq.shape == (m_pad, 7168) and xs.shape == (56, m_pad)
+    # padding rows are never written
+    assert np.all(u8(xq)[M:] == 0xA5)
+    assert np.all(xs.cpu().numpy()[:, M:] == -7.0)
+
+
+@pytest.mark.parametrize("M,K", [(8192, 3072), (1000, 12288), (37, 1024)])
+def test_group_row_padded_prefill_sizes_with_outliers(dev, M, K):
+    x = synthetic.activations(M, K, seed=K, outliers=True)
+    quant_both_group(x, dev, 128)
+
+
+@pytest.mark.parametrize("group", [16, 32, 64])
+def test_group_sizes(dev, group):
+    x = synthetic.activations(21, 1024, seed=group, outliers=True)
+    quant_both_group(x, dev, group, xq_fill=0xA5, xs_fill=-7.0)
+
+
+def test_group_quant_view_matches_the_pages_layout(dev):
+    M, K = 5, 384
+    x = synthetic.activations(M, K, seed=2).to(dev)
+    xq, xsv = fq.fp8q_quant_per_token_group_row_padded(x, 128)
+    assert tuple(xsv.shape) == (8, 3) and xsv.stride() == (1, 8)
+    assert tuple(xq.shape) == (8, K)
+
+
+def test_weight_block128_quant(dev):
+    N, K = 384, 1024
+    w = synthetic.weights(N, K, seed=5)
+    wq, ws = fq.fp8q_quant_weight_block128(w.to(dev))
+    torch.cuda.synchronize()
+    rq, rs = oracle.quant_weight_blocks(w, 128, 128)
+    assert np.array_equal(u8(wq), rq)
+    assert np.array_equal(ws.cpu().numpy(), rs)
+
+
+def test_weight_per_channel_quant_is_per_token_quant_of_rows(dev):
+    w = synthetic.weights(512, 4096, seed=6)
+    wq, ws = fq.fp8q_quant_per_token(w.to(dev))
+    torch.cuda.synchronize()
+    rq, rs = oracle.quant_weight_per_channel(w)
+    assert np.array_equal(u8(wq), rq) and np.array_equal(ws.cpu().numpy(), rs)

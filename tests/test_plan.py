@@ -1,0 +1,68 @@
+"""Host-side schedule selection (no GPU needed): every plan the library can
+produce launches a kernel instantiation that exists, covers every tile once,
+splits K only across whole 128-wide K blocks and stays inside the shared
+memory budget."""
+import itertools
+
+import pytest
+
+import fp8_w8a8_quantized_token_gb300 as fq
+from fp8_w8a8_quantized_token_gb300 import build as fbuild
+
+SUPPORTED = {(1, 16), (1, 32), (1, 64), (1, 128), (0, 256)}
+SMEM_LIMIT = 232448
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    fbuild.build()
+    L = fq.load_library()
+    L.fp8q_set_plan_override(-1, 0, 0)
+    return L
+
+
+def stage_bytes(swap, mma_n, blockwise):
+    tok_tile = mma_n if swap else 128
+    return 128 * 128 + mma_n * 128 + (tok_tile * 4 if blockwise else 0)
+
+
+SHAPES = [(4096, 4096), (6144, 4096), (4096, 12288), (24576, 4096), (4096, 7168), (24576, 3072), (3072, 12288),
+          (256, 512), (384, 1040)]
+MS = [1, 2, 3, 4, 5, 7, 13, 16, 31, 32, 64, 100, 128, 129, 256, 512, 1024, 2048, 4096, 8192]
+
+
+@pytest.mark.parametrize("num_sms", [148, 152])
+def test_plans_are_launchable(num_sms):
+    for (N, K), M, bw in itertools.product(SHAPES, MS, (0, 1)):
+        if bw and (N % 128 or K % 128):
+            continue
+        p = fq.fp8q_gemm_plan(M, N, K, bool(bw), num_sms=num_sms)
+        assert (p["swap_ab"], p["mma_n"]) in SUPPORTED
+        assert p["tile_m"] == (p["mma_n"] if p["swap_ab"] else 128)
+        assert p["tile_n"] == (128 if p["swap_ab"] else p["mma_n"])
+        tiles = -(-M // p["tile_m"]) * -(-N // p["tile_n"])
+        num_kb = -(-K // 128)
+        assert 1 <= p["split_k"] <= min(8, num_kb)
+        if p["split_k"] > 1:
+            assert p["grid"] == tiles * p["split_k"] and not p["persistent"]
+        else:
+            assert p["grid"] == min(tiles, num_sms)
+            assert p["persistent"] == int(tiles > num_sms)
+        assert p["stages"] * stage_bytes(p["swap_ab"], p["mma_n"], bw) + 4096 <= SMEM_LIMIT
+
+
+def test_decode_sizes_put_weights_on_the_mma_m_side():
+    for M in (1, 8, 16, 33, 64):
+        p = fq.fp8q_gemm_plan(M, 4096, 4096, num_sms=148)
+        assert p["swap_ab"] == 1 and p["tile_m"] >= M or p["tile_m"] == 128
+
+
+def test_override_forces_the_schedule_and_clamps_split():
+    try:
+        fq.fp8q_set_plan_override(0, 256, 16)
+        p = fq.fp8q_gemm_plan(300, 4096, 512, num_sms=148)
+        assert (p["swap_ab"], p["mma_n"], p["split_k"]) == (0, 256, 4)   # 512 / 128 = 4 K blocks
+        fq.fp8q_set_plan_override(1, 16, 20)
+        assert fq.fp8q_gemm_plan(1, 4096, 4096, num_sms=148)["split_k"] == 8
+    finally:
+        fq.fp8q_set_plan_override(-1)
