@@ -1,0 +1,523 @@
+"""Benchmark of the FP8 W8A8 linear layer on GB300.
+
+One step = one pass of the whole hot path over one batch: for every M of the
+sweep, per-token quantization of the bf16 activations followed by the scaled
+FP8 GEMM.  The default workload is the channelwise o_proj linear (N = K =
+4096) over M in {1, 2, 4, ..., 8192}; ``--workload`` selects the other
+linear shapes for measurement runs.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FP8 W8A8 GEMM TFLOP/s & GB/s vs M (1-8192) and % of roofline"
+UNIT = "TFLOP/s"
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
+# kernel, from the ncu capture summarised under profiles/ (None until a
+# capture of the current kernel exists).
+DOMINANT_TRAFFIC_BYTES = {}
+
+WORKLOADS = {
+    # name: (list of (label, N, K, blockwise), M sweep, outliers)
+    "oproj_sweep": ([("o_proj", 4096, 4096, False)],
+                    [1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096, 8192], True),
+    "qwen3_8b": ([("qkv", 6144, 4096, False), ("down", 4096, 12288, False), ("gate_up", 24576, 4096, False)],
+                 [1, 16, 128, 512, 2048, 8192], True),
+    "blockwise_decode": ([("blk_4096x7168", 4096, 7168, True)], [1, 2, 3, 4, 5, 7, 13, 16, 31, 64, 256], False),
+    "blockwise_prefill": ([("blk_24576x3072", 24576, 3072, True), ("blk_3072x12288", 3072, 12288, True)],
+                          [8192], True),
+    "tiny": ([("tiny", 256, 512, False)], [16], False),
+}
+WORKLOAD_DESC = {
+    "oproj_sweep": "channelwise o_proj N=K=4096, M sweep 1..8192, per-token x per-channel, outliers 1% x20",
+    "qwen3_8b": "channelwise Qwen3-8B-shaped qkv/down/gate_up at M in {1,16,128,512,2048,8192}",
+    "blockwise_decode": "blockwise N=4096 K=7168, row-padded group-128 quant, M in {1..256}",
+    "blockwise_prefill": "blockwise M=8192: 24576x3072 and 3072x12288, row-padded group-128 quant",
+    "tiny": "channelwise 16x256x512",
+}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "fp8_tflops": 2.0 * float(p["bf16_tflops"]),
+                "source": "measured (MEASURED_PEAKS.json: copy GB/s; FP8 = 2 x measured bf16 burst)"}
+    return {"hbm_gbs": 6800.0, "fp8_tflops": 2.0 * 1900.0, "source": "fallback (6.8 TB/s; FP8 = 2 x 1.9 PF bf16)"}
+
+
+def gemm_bytes(M, N, K, blockwise):
+    m_pad = (M + 3) // 4 * 4
+    if blockwise:
+        return M * K + N * K + 2 * M * N + 4 * m_pad * (K // 128) + 4 * (N // 128) * (K // 128)
+    return M * K + N * K + 2 * M * N + 4 * M + 4 * N
+
+
+def quant_bytes(M, K, blockwise):
+    m_pad = (M + 3) // 4 * 4
+    return 3 * M * K + (4 * m_pad * (K // 128) if blockwise else 4 * M)
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.reader.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle on a bounded sample
+# ---------------------------------------------------------------------------
+
+def oracle_sample_step(problems, rows_per_m, threads):
+    """Oracle quant + GEMM on the first rows of every (shape, M); returns FLOPs."""
+    import oracle
+    flops = 0
+    for (label, N, K, bw, M, x, wq, ws) in problems:
+        r = min(M, rows_per_m)
+        xs_ = x[:r]
+        if bw:
+            q, s = oracle.quant_group_row_padded(xs_, 128, threads=threads)
+            oracle.gemm_blockwise(q, wq, s, ws, r, threads=threads)
+        else:
+            q, s = oracle.quant_per_token(xs_, threads=threads)
+            oracle.gemm_channelwise(q, wq, s, ws, threads=threads)
+        flops += 2 * r * N * K
+    return flops
+
+
+def build_oracle_problems(workload, rows_per_m):
+    import oracle
+    import synthetic
+    shapes, ms, outliers = WORKLOADS[workload]
+    problems = []
+    for (label, N, K, bw) in shapes:
+        w = synthetic.weights(N, K)
+        if bw:
+            wq, ws = oracle.quant_weight_blocks(w, 128, 128)
+        else:
+            wq, ws = oracle.quant_weight_per_channel(w)
+        for M in ms:
+            x = synthetic.activations(min(M, rows_per_m), K, outliers=outliers)
+            problems.append((label, N, K, bw, M, x, wq, ws))
+    return problems
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    threads = os.cpu_count() or 1
+    rows = args.ref_rows
+    problems = build_oracle_problems(args.workload, rows)
+    # Size each step so the whole run stays within a few minutes: if a full
+    # pass over every problem would take too long, each step takes the next
+    # few problems round-robin (the metric is FLOPs / time either way).
+    t0 = time.perf_counter()
+    oracle_sample_step(problems, rows, threads)
+    per_pass = time.perf_counter() - t0
+    budget = 150.0
+    per_step = len(problems)
+    if per_pass * (args.steps + args.warmup) > budget:
+        per_step = max(1, int(len(problems) * budget / (per_pass * (args.steps + args.warmup))))
+    cursor = 0
+
+    def one_step():
+        nonlocal cursor
+        chosen = [problems[(cursor + i) % len(problems)] for i in range(per_step)]
+        cursor = (cursor + per_step) % len(problems)
+        return oracle_sample_step(chosen, rows, threads)
+
+    for _ in range(args.warmup):
+        one_step()
+    t0 = time.perf_counter()
+    flops = 0
+    for _ in range(args.steps):
+        flops += one_step()
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    sample = (f"oracle per-token quant + exact GEMM on the first min(M, {rows}) rows of {per_step} of the "
+              f"{len(problems)} (shape, M) problems per step, round-robin")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD_DESC[args.workload]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# the CUDA path
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="fp8q", choices=["fp8q", "reference"])
+    ap.add_argument("--workload", default="oproj_sweep", choices=sorted(WORKLOADS))
+    ap.add_argument("--ref-rows", type=int, default=2, help="oracle rows per M in the reference arm")
+    ap.add_argument("--cpu-rows", type=int, default=32, help="oracle rows per M for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--kernel-replays", type=int, default=20)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    import fp8_w8a8_quantized_token_gb300 as fq
+    import synthetic
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    L = fq.load_library()
+    peaks = load_peaks()
+
+    shapes, ms, outliers = WORKLOADS[args.workload]
+    # ---- inputs resident in HBM -------------------------------------------
+    problems = []
+    wcopies = {}
+    wbytes_total = 0
+    for (label, N, K, bw) in shapes:
+        w = synthetic.weights(N, K)
+        wbytes = N * K
+        copies = max(2, math.ceil(2 * L2_BYTES / wbytes))  # rotate > 2x L2 of weight bytes
+        copies = min(copies, len(ms))  # one copy per M at most
+        wdev = w.to(dev)
+        if bw:
+            wq0, ws0 = fq.fp8q_quant_weight_block128(wdev)
+        else:
+            wq0, ws0 = fq.fp8q_quant_per_token(wdev)
+        wqs = [wq0] + [wq0.clone() for _ in range(copies - 1)]
+        wcopies[label] = wqs
+        wbytes_total += wbytes * copies
+        for i, M in enumerate(ms):
+            x = synthetic.activations(M, K, outliers=outliers).to(dev)
+            m_pad = (M + 3) // 4 * 4
+            if bw:
+                xq = torch.empty((m_pad, K), dtype=fq.E4M3, device=dev)
+                xs = torch.empty((K // 128, m_pad), dtype=torch.float32, device=dev)
+            else:
+                xq = torch.empty((M, K), dtype=fq.E4M3, device=dev)
+                xs = torch.empty((M,), dtype=torch.float32, device=dev)
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            plan = fq.fp8q_gemm_plan(M, N, K, bw)
+            problems.append(dict(label=label, N=N, K=K, bw=bw, M=M, m_pad=m_pad, x=x, xq=xq, xs=xs, out=out,
+                                 wq=wqs[i % copies], ws=ws0, plan=plan))
+    del w
+    torch.cuda.synchronize()
+
+    import ctypes
+    P = ctypes.c_void_p
+
+    def launch(p, sp):
+        """The public linear entry point: quantize, then GEMM (two kernels)."""
+        if p["bw"]:
+            st = L.fp8q_linear_blockwise(P(p["x"].data_ptr()), P(p["wq"].data_ptr()), P(p["ws"].data_ptr()), None,
+                                         P(p["out"].data_ptr()), p["M"], p["N"], p["K"], P(p["xq"].data_ptr()),
+                                         P(p["xs"].data_ptr()), p["m_pad"], 0, sp)
+        else:
+            st = L.fp8q_linear_channelwise(P(p["x"].data_ptr()), P(p["wq"].data_ptr()), p["K"],
+                                           P(p["ws"].data_ptr()), None, P(p["out"].data_ptr()), p["M"], p["N"],
+                                           p["K"], P(p["xq"].data_ptr()), P(p["xs"].data_ptr()), 0, sp)
+        if st != 0:
+            raise RuntimeError(f"linear failed: {fq.status_str(st)}")
+
+    def launch_gemm(p, wq, sp):
+        if p["bw"]:
+            st = L.fp8q_scaled_mm_blockwise(P(p["xq"].data_ptr()), P(wq.data_ptr()), P(p["xs"].data_ptr()),
+                                            P(p["ws"].data_ptr()), None, P(p["out"].data_ptr()), p["M"], p["m_pad"],
+                                            p["N"], p["K"], 0, sp)
+        else:
+            st = L.fp8q_scaled_mm_channelwise(P(p["xq"].data_ptr()), P(wq.data_ptr()), p["K"],
+                                              P(p["xs"].data_ptr()), P(p["ws"].data_ptr()), None,
+                                              P(p["out"].data_ptr()), p["M"], p["N"], p["K"], 0, sp)
+        if st != 0:
+            raise RuntimeError(f"gemm failed: {fq.status_str(st)}")
+
+    def launch_quant(p, sp):
+        if p["bw"]:
+            st = L.fp8q_quant_per_token_group_row_padded(P(p["x"].data_ptr()), p["M"], p["K"], p["K"], 128, 1e-10, 4,
+                                                         P(p["xq"].data_ptr()), P(p["xs"].data_ptr()), p["m_pad"], sp)
+        else:
+            st = L.fp8q_quant_per_token(P(p["x"].data_ptr()), p["M"], p["K"], p["K"], P(p["xq"].data_ptr()),
+                                        P(p["xs"].data_ptr()), 1e-10, sp)
+        if st != 0:
+            raise RuntimeError(f"quant failed: {fq.status_str(st)}")
+
+    def capture(body):
+        """A CUDA graph of body(stream): the library's launches are captured
+        like any other stream work (one eager run first sets kernel
+        attributes outside the capture)."""
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            body(side)
+        side.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            body(side)
+        torch.cuda.synchronize()
+        return g
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def mk():
+        return torch.cuda.Event(enable_timing=True)
+
+    stream = torch.cuda.current_stream(dev)
+
+    # ---- one step = every problem's quant + GEMM, captured as one graph ----
+    step_graph = capture(lambda st: [launch(p, P(st.cuda_stream)) for p in problems])
+    for _ in range(args.warmup):
+        step_graph.replay()
+    barrier()
+    start, end = mk(), mk()
+    with ClockSampler(local) as clk:
+        barrier()
+        start.record(stream)
+        for _ in range(args.steps):
+            step_graph.replay()
+        end.record(stream)
+        barrier()
+    elapsed_ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    flops_step = sum(2 * p["M"] * p["N"] * p["K"] for p in problems)
+    value = flops_step * world / (ms_per_step * 1e-3) / 1e12
+
+    # ---- per-kernel durations: each problem's GEMM (and quantizer) launched
+    # REPS times back to back in a graph, the GEMM over rotating weight
+    # copies (> L2 in total), timed with CUDA events on the launching stream.
+    reps = 8
+
+    def time_graph(body, n_launch):
+        g = capture(body)
+        e0, e1 = mk(), mk()
+        g.replay()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.kernel_replays):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (args.kernel_replays * n_launch)
+
+    g_us, q_us = [], []
+    for i, p in enumerate(problems):
+        copies = wcopies[p["label"]]
+
+        def body_g(st, p=p, copies=copies, i=i):
+            for r in range(reps):
+                launch_gemm(p, copies[(i + r) % len(copies)], P(st.cuda_stream))
+
+        def body_q(st, p=p):
+            for _ in range(reps):
+                launch_quant(p, P(st.cuda_stream))
+
+        g_us.append(time_graph(body_g, reps))
+        q_us.append(time_graph(body_q, reps))
+
+    sweep = []
+    for p, qu, gu in zip(problems, q_us, g_us):
+        fl = 2 * p["M"] * p["N"] * p["K"]
+        by = gemm_bytes(p["M"], p["N"], p["K"], p["bw"])
+        t_roof = max(fl / (peaks["fp8_tflops"] * 1e12), by / (peaks["hbm_gbs"] * 1e9))
+        qb = quant_bytes(p["M"], p["K"], p["bw"])
+        pl = p["plan"]
+        sweep.append({"shape": p["label"], "M": p["M"], "N": p["N"], "K": p["K"], "gemm_us": round(gu, 3),
+                      "tflops": round(fl / (gu * 1e-6) / 1e12, 2), "gbs": round(by / (gu * 1e-6) / 1e9, 1),
+                      "roofline_frac": round(t_roof / (gu * 1e-6), 3),
+                      "bound": "tensor" if fl / (peaks["fp8_tflops"] * 1e12) > by / (peaks["hbm_gbs"] * 1e9)
+                      else "hbm",
+                      "quant_us": round(qu, 3), "quant_gbs": round(qb / (qu * 1e-6) / 1e9, 1),
+                      "plan": f"{'swap' if pl['swap_ab'] else 'noswap'}{pl['mma_n']}x{pl['split_k']}"})
+
+    # dominant kernel = the GEMM instantiation (scheme, swap, mma_n) with the
+    # largest total time per step
+    groups = {}
+    for p, gu in zip(problems, g_us):
+        pl = p["plan"]
+        key = ("blockwise" if p["bw"] else "channelwise", pl["swap_ab"], pl["mma_n"])
+        g = groups.setdefault(key, {"us": 0.0, "flops": 0, "bytes": 0, "n": 0})
+        g["us"] += gu
+        g["flops"] += 2 * p["M"] * p["N"] * p["K"]
+        g["bytes"] += gemm_bytes(p["M"], p["N"], p["K"], p["bw"])
+        g["n"] += 1
+    quant_total = sum(q_us)
+    gemm_total = sum(g_us)
+    dom_key, dom = max(groups.items(), key=lambda kv: kv[1]["us"])
+    tensor_bound = dom["flops"] / (peaks["fp8_tflops"] * 1e12) > dom["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    if tensor_bound:
+        achieved = dom["flops"] / (dom["us"] * 1e-6) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peaks["fp8_tflops"], 1),
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["fp8_tflops"], 3)}
+    else:
+        achieved = dom["bytes"] / (dom["us"] * 1e-6) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": round(peaks["hbm_gbs"], 1),
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 3)}
+    roof["traffic"] = DOMINANT_TRAFFIC_BYTES.get(dom_key) if DOMINANT_TRAFFIC_BYTES else None
+    roof["kernel"] = (f"fp8_gemm_kernel<{'swap' if dom_key[1] else 'noswap'}, mma_n={dom_key[2]}, {dom_key[0]}> "
+                      f"({dom['n']} launches/step; achieved = their FLOPs / their summed durations)")
+    roof["share_of_step"] = round(dom["us"] / (quant_total + gemm_total), 3)
+    roof["peak_source"] = peaks["source"]
+
+    # ---- end to end through the C ABI with host buffers --------------------
+    h2d = sum(p["x"].numel() * 2 for p in problems)
+    d2h = sum(p["out"].numel() * 2 for p in problems)
+    hx = [p["x"].cpu().pin_memory() for p in problems]
+    ho = [torch.empty(p["out"].shape, dtype=torch.bfloat16).pin_memory() for p in problems]
+
+    def e2e_body(st):
+        for p, hxi, hoi in zip(problems, hx, ho):
+            p["x"].copy_(hxi, non_blocking=True)
+            launch(p, P(st.cuda_stream))
+            hoi.copy_(p["out"], non_blocking=True)
+
+    e2e_graph = capture(e2e_body)
+    for _ in range(3):
+        e2e_graph.replay()
+    barrier()
+    e0, e1 = mk(), mk()
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_graph.replay()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": round(flops_step * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+           "how": "CUDA graph per step: pinned-host->device copy of each M's activations, the linear "
+                  "entry point (quant + GEMM), device->pinned-host copy of its output"}
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline:
+            rows = args.cpu_rows
+            threads = os.cpu_count() or 1
+            cp = build_oracle_problems(args.workload, rows)
+            t0 = time.perf_counter()
+            fl = oracle_sample_step(cp, rows, threads)
+            dt = time.perf_counter() - t0
+            cpu = {"value": round(fl / dt / 1e12, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+                   "sample": f"quant + exact GEMM on the first min(M, {rows}) rows of every M ({dt:.1f} s)"}
+        l2note = (f"inputs larger than L2 per step: {len(set(id(p['wq']) for p in problems))} rotating "
+                  f"weight copies ({wbytes_total / 2**20:.0f} MiB) + {sum(p['x'].numel() * 2 for p in problems) / 2**20:.0f}"
+                  f" MiB activations per step")
+        line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate)",
+                "data": "synthetic",
+                "config": {"workload": WORKLOAD_DESC[args.workload], "shapes": [s[:3] for s in shapes],
+                           "M": ms, "l2": l2note, "parallelism": f"replicas x{world}" if world > 1 else "single"},
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": 2 * len(problems) * args.steps,
+                "timing": "K replays of a CUDA graph holding one step; per-kernel durations from graphs of "
+                          "8 back-to-back launches of each problem's kernel (GEMMs over rotating weight copies)",
+                "clocks": clk.summary(),
+                "kernel_time_us": {"quant": round(quant_total, 2), "gemm": round(gemm_total, 2)},
+                "sweep": sweep}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -133,6 +133,29 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// Prefetch one tile of a tensor map into L2 (no shared-memory destination,
+// no completion tracking).  L2 is the point of coherence for device memory,
+// so a prefetch can never make a later load observe stale data.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32_t c0, int32_t c1)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start while the previous kernel in the
+// stream is still running.  pdl_wait() blocks until that kernel has
+// completed and its memory is visible; it must precede every global read
+// of data the previous kernel may have written and every global write.
+// pdl_trigger() lets the next kernel start launching early.  Both are
+// no-ops for a kernel launched without the attribute.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // tcgen05: tensor memory and the 5th-generation tensor-core MMA
 // ---------------------------------------------------------------------------

@@ -129,6 +129,10 @@ __device__ __forceinline__ void tile_coords(int tile, int a_tiles, int b_tiles, 
     b_t = idx / gsize;
 }
 
+// Weight K blocks per CTA prefetched into L2 before the previous kernel
+// has finished.
+constexpr int kPrefetchKBlocks = 16;
+
 template <typename OutT>
 __device__ __forceinline__ void store_out(OutT *out, long long idx, float v)
 {
@@ -181,10 +185,23 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
         *abort = 0;
         fence_mbar_init();
     }
+    pdl_trigger();
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tm_a);
         tma_prefetch_map(&tm_b);
         if (BLOCKWISE) tma_prefetch_map(&tm_sa);
+        // Weights never come from the previous kernel of a linear layer's
+        // pipeline, but they are only READ from L2 after pdl_wait(); this
+        // prefetch just starts streaming the first tile's weight slices from
+        // HBM while the previous kernel finishes.
+        if (cluster_id < p.num_tiles) {
+            int a_t, b_t;
+            tile_coords(cluster_id, a_tiles, b_tiles, p.group, a_t, b_t);
+            const CUtensorMap *wmap = SWAP ? &tm_a : &tm_b;
+            const int wrow = SWAP ? a_t * 128 : b_t * BN;
+            const int pf = nkb < kPrefetchKBlocks ? nkb : kPrefetchKBlocks;
+            for (int i = 0; i < pf; ++i) tma_prefetch_l2_2d(wmap, (kb_begin + i) * 128, wrow);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_holder, C::kTmemCols);
@@ -194,6 +211,9 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // Everything below may read the previous kernel's output (activations,
+    // scales) or overwrite buffers it reads (out).
+    pdl_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------------------

@@ -84,6 +84,8 @@ __global__ void __launch_bounds__(1024) quant_per_token_kernel(const __nv_bfloat
                                                                int K, float eps)
 {
     __shared__ float warp_max[32];
+    pdl_trigger();
+    pdl_wait();
     const int64_t row = blockIdx.x;
     const int chunks = K >> 4;
     const __nv_bfloat16 *xr = x + row * ldx;
@@ -122,6 +124,8 @@ __global__ void __launch_bounds__(1024) quant_per_token_two_pass_kernel(const __
                                                                         float *__restrict__ xs, int K, float eps)
 {
     __shared__ float warp_max[32];
+    pdl_trigger();
+    pdl_wait();
     const int64_t row = blockIdx.x;
     const int chunks = K >> 4;
     const __nv_bfloat16 *xr = x + row * ldx;
@@ -154,6 +158,8 @@ __global__ void __launch_bounds__(256) quant_group_kernel(const __nv_bfloat16 *_
                                                           uint8_t *__restrict__ xq, float *__restrict__ xs,
                                                           int64_t M, int K, int64_t m_pad, float eps)
 {
+    pdl_trigger();
+    pdl_wait();
     const int chunks_per_row = K >> 4;
     const int64_t total = M * chunks_per_row;
     for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
@@ -186,6 +192,8 @@ __global__ void __launch_bounds__(256) quant_weight_block128_kernel(const __nv_b
                                                                     float *__restrict__ ws, int64_t K, float eps)
 {
     __shared__ float warp_max[8];
+    pdl_trigger();
+    pdl_wait();
     const int64_t bn = blockIdx.y, bk = blockIdx.x;
     // 128 rows x 8 chunks of 16; thread t handles chunks t, t + 256, ...
     Chunk16 c[4];
@@ -214,13 +222,31 @@ __global__ void __launch_bounds__(256) quant_weight_block128_kernel(const __nv_b
     }
 }
 
+// Launch with programmatic stream serialization so the kernel's launch
+// overlaps the tail of the previous kernel in the stream (each kernel waits
+// for it with griddepcontrol.wait before touching global memory).
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, cudaStream_t st, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
 template <int VPT>
 cudaError_t launch_per_token(const void *x, int64_t M, int K, int64_t ldx, void *xq, float *xs, float eps, int threads,
                              cudaStream_t st)
 {
-    quant_per_token_kernel<VPT><<<static_cast<unsigned>(M), threads, 0, st>>>(
-        static_cast<const __nv_bfloat16 *>(x), ldx, static_cast<uint8_t *>(xq), xs, K, eps);
-    return cudaGetLastError();
+    return launch_pdl(quant_per_token_kernel<VPT>, dim3(static_cast<unsigned>(M)), dim3(threads), st,
+                      static_cast<const __nv_bfloat16 *>(x), ldx, static_cast<uint8_t *>(xq), xs, K, eps);
 }
 
 }  // namespace
@@ -229,11 +255,12 @@ cudaError_t launch_quant_per_token(const void *x, int64_t M, int64_t K, int64_t 
                                    cudaStream_t st)
 {
     const int chunks = static_cast<int>(K >> 4);
-    // Threads per row: enough that each thread holds at most 4 chunks, in
-    // whole warps, at most 1024.
-    int threads = ((chunks + 3) / 4 + 31) / 32 * 32;
+    // One 16-element chunk per thread where possible (short dependent
+    // chains: decode-size M runs one CTA per row and is latency-bound), in
+    // whole warps, at most 1024 threads; rows longer than 4 chunks per
+    // thread take the two-pass kernel.
+    int threads = (chunks + 31) / 32 * 32;
     if (threads > 1024) threads = 1024;
-    if (threads < 32) threads = 32;
     const int vpt = (chunks + threads - 1) / threads;
     switch (vpt) {
         case 1: return launch_per_token<1>(x, M, static_cast<int>(K), ldx, xq, xs, eps, threads, st);
@@ -241,9 +268,9 @@ cudaError_t launch_quant_per_token(const void *x, int64_t M, int64_t K, int64_t 
         case 3: return launch_per_token<3>(x, M, static_cast<int>(K), ldx, xq, xs, eps, threads, st);
         case 4: return launch_per_token<4>(x, M, static_cast<int>(K), ldx, xq, xs, eps, threads, st);
         default:
-            quant_per_token_two_pass_kernel<<<static_cast<unsigned>(M), 1024, 0, st>>>(
-                static_cast<const __nv_bfloat16 *>(x), ldx, static_cast<uint8_t *>(xq), xs, static_cast<int>(K), eps);
-            return cudaGetLastError();
+            return launch_pdl(quant_per_token_two_pass_kernel, dim3(static_cast<unsigned>(M)), dim3(1024), st,
+                              static_cast<const __nv_bfloat16 *>(x), ldx, static_cast<uint8_t *>(xq), xs,
+                              static_cast<int>(K), eps);
     }
 }
 
@@ -257,23 +284,22 @@ cudaError_t launch_quant_group(const void *x, int64_t M, int64_t K, int64_t ldx,
     if (blocks > cap) blocks = cap;
     const auto *xb = static_cast<const __nv_bfloat16 *>(x);
     auto *q = static_cast<uint8_t *>(xq);
-    const unsigned b = static_cast<unsigned>(blocks);
+    const dim3 g(static_cast<unsigned>(blocks)), b(threads);
+    const int k = static_cast<int>(K);
     switch (group) {
-        case 16: quant_group_kernel<1><<<b, threads, 0, st>>>(xb, ldx, q, xs, M, static_cast<int>(K), m_pad, eps); break;
-        case 32: quant_group_kernel<2><<<b, threads, 0, st>>>(xb, ldx, q, xs, M, static_cast<int>(K), m_pad, eps); break;
-        case 64: quant_group_kernel<4><<<b, threads, 0, st>>>(xb, ldx, q, xs, M, static_cast<int>(K), m_pad, eps); break;
-        default: quant_group_kernel<8><<<b, threads, 0, st>>>(xb, ldx, q, xs, M, static_cast<int>(K), m_pad, eps); break;
+        case 16: return launch_pdl(quant_group_kernel<1>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps);
+        case 32: return launch_pdl(quant_group_kernel<2>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps);
+        case 64: return launch_pdl(quant_group_kernel<4>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps);
+        default: return launch_pdl(quant_group_kernel<8>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps);
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_quant_weight_block128(const void *w, int64_t N, int64_t K, void *wq, float *ws, float eps,
                                          cudaStream_t st)
 {
     dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(N / 128));
-    quant_weight_block128_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(w),
-                                                        static_cast<uint8_t *>(wq), ws, K, eps);
-    return cudaGetLastError();
+    return launch_pdl(quant_weight_block128_kernel, grid, dim3(256), st, static_cast<const __nv_bfloat16 *>(w),
+                      static_cast<uint8_t *>(wq), ws, K, eps);
 }
 
 }  // namespace fp8q
