@@ -18,6 +18,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "libfp8q.so")
+TRACE_LIB = os.path.join(HERE, "libfp8q_trace.so")
 OBJ_DIR = os.path.join(HERE, "_build")
 
 SOURCES = ["api.cu", "host_util.cu", "quant.cu", "gemm_channelwise.cu", "gemm_blockwise.cu", "plan.cpp"]
@@ -33,7 +34,7 @@ def _nvcc() -> str:
     return cand
 
 
-def _inputs_digest() -> str:
+def _inputs_digest(extra: str = "") -> str:
     h = hashlib.sha256()
     names = sorted(os.listdir(CSRC)) + ["fp8q.h"]
     for n in names:
@@ -43,23 +44,30 @@ def _inputs_digest() -> str:
             with open(path, "rb") as f:
                 h.update(f.read())
     h.update(" ".join(ARCH + NVCC_FLAGS).encode())
+    h.update(extra.encode())
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile the library if its sources changed; returns the .so path."""
-    digest = _inputs_digest()
-    stamp = LIB + ".digest"
-    if not force and os.path.exists(LIB) and os.path.exists(stamp):
+def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
+    """Compile the library if its sources changed; returns the .so path.
+
+    trace=True builds libfp8q_trace.so instead: the same library with the
+    GEMM's per-CTA phase timestamps compiled in (include/fp8q_trace.h)."""
+    lib = TRACE_LIB if trace else LIB
+    defines = ["-DFP8Q_TRACE"] if trace else []
+    obj_dir = OBJ_DIR + ("_trace" if trace else "")
+    digest = _inputs_digest(" ".join(defines))
+    stamp = lib + ".digest"
+    if not force and os.path.exists(lib) and os.path.exists(stamp):
         with open(stamp) as f:
             if f.read().strip() == digest:
-                return LIB
-    os.makedirs(OBJ_DIR, exist_ok=True)
+                return lib
+    os.makedirs(obj_dir, exist_ok=True)
     nvcc = _nvcc()
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OBJ_DIR, src + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(obj_dir, src + ".o")
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *defines, "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
         if src.endswith(".cpp"):
             cmd = [nvcc, "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
                    "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
@@ -72,16 +80,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp, "w") as f:
         f.write(digest)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, trace="--trace" in sys.argv))

@@ -34,8 +34,11 @@ fp8q_status check_quant_common(const void *x, int64_t M, int64_t K, int64_t ldx,
     return FP8Q_OK;
 }
 
-fp8q_status run_gemm(const GemmProblem &p, cudaStream_t st)
+fp8q_status run_gemm(GemmProblem p, cudaStream_t st)
 {
+    // Weight bytes the kernel may read before waiting for its predecessor.
+    const size_t wbytes = static_cast<size_t>(p.N - 1) * static_cast<size_t>(p.ldw) + static_cast<size_t>(p.K);
+    p.preload = !last_launch_writes_overlap(st, p.w, wbytes);
     fp8q_plan pl;
     const fp8q_status s = fp8q_gemm_plan(p.M, p.N, p.K, p.blockwise ? 1 : 0, 0, &pl);
     if (s != FP8Q_OK) return s;
@@ -49,6 +52,7 @@ fp8q_status run_gemm(const GemmProblem &p, cudaStream_t st)
     l.stages = pl.stages;
     const cudaError_t e = p.blockwise ? launch_gemm_blockwise(p, l, status, st)
                                       : launch_gemm_channelwise(p, l, status, st);
+    if (e == cudaSuccess) note_launch_writes(st, p.out, static_cast<size_t>(p.M) * p.N * 2);
     return from_cuda(e);
 }
 
@@ -61,7 +65,9 @@ fp8q_status fp8q_quant_per_token(const void *x, int64_t M, int64_t K, int64_t ld
 {
     const fp8q_status s = check_quant_common(x, M, K, ldx, xq, x_scale, eps);
     if (s != FP8Q_OK || M == 0) return s;
-    return from_cuda(launch_quant_per_token(x, M, K, ldx, xq, x_scale, eps, as_stream(stream)));
+    const cudaError_t e = launch_quant_per_token(x, M, K, ldx, xq, x_scale, eps, as_stream(stream));
+    if (e == cudaSuccess) note_launch_writes(as_stream(stream), xq, static_cast<size_t>(M) * K);
+    return from_cuda(e);
 }
 
 fp8q_status fp8q_quant_per_token_group_row_padded(const void *x, int64_t M, int64_t K, int64_t ldx,
@@ -77,8 +83,10 @@ fp8q_status fp8q_quant_per_token_group_row_padded(const void *x, int64_t M, int6
     if (K > 0 && K % group_size != 0) return FP8Q_ERR_INVALID_ARG;
     const fp8q_status s = check_quant_common(x, M, K, ldx, xq, x_scale, eps);
     if (s != FP8Q_OK || M == 0) return s;
-    return from_cuda(launch_quant_group(x, M, K, ldx, group_size, xq, x_scale, m_pad, eps, current_device_sms(),
-                                        as_stream(stream)));
+    const cudaError_t e = launch_quant_group(x, M, K, ldx, group_size, xq, x_scale, m_pad, eps, current_device_sms(),
+                                             as_stream(stream));
+    if (e == cudaSuccess) note_launch_writes(as_stream(stream), xq, static_cast<size_t>(M) * K);
+    return from_cuda(e);
 }
 
 fp8q_status fp8q_quant_weight_block128(const void *w, int64_t N, int64_t K, void *wq, float *w_scale, float eps,
@@ -89,7 +97,9 @@ fp8q_status fp8q_quant_weight_block128(const void *w, int64_t N, int64_t K, void
     if (!(eps > 0.0f) || !isfinite(eps)) return FP8Q_ERR_INVALID_ARG;
     if (w == nullptr || wq == nullptr || w_scale == nullptr) return FP8Q_ERR_INVALID_ARG;
     if (!aligned16(w) || !aligned16(wq) || !aligned4(w_scale)) return FP8Q_ERR_INVALID_ARG;
-    return from_cuda(launch_quant_weight_block128(w, N, K, wq, w_scale, eps, as_stream(stream)));
+    const cudaError_t e = launch_quant_weight_block128(w, N, K, wq, w_scale, eps, as_stream(stream));
+    if (e == cudaSuccess) note_launch_writes(as_stream(stream), wq, static_cast<size_t>(N) * K);
+    return from_cuda(e);
 }
 
 fp8q_status fp8q_scaled_mm_channelwise(const void *a, const void *b, int64_t ldb, const float *a_scale,
@@ -111,6 +121,7 @@ fp8q_status fp8q_scaled_mm_channelwise(const void *a, const void *b, int64_t ldb
     p.a_scale = a_scale; p.w_scale = b_scale; p.bias = bias; p.out = out;
     p.out_fp16 = out_dtype == FP8Q_OUT_FP16;
     p.blockwise = false;
+    p.preload = false;
     return run_gemm(p, as_stream(stream));
 }
 
@@ -134,6 +145,7 @@ fp8q_status fp8q_scaled_mm_blockwise(const void *a, const void *w, const float *
     p.a_scale = a_scale; p.w_scale = w_scale; p.bias = bias; p.out = out;
     p.out_fp16 = out_dtype == FP8Q_OUT_FP16;
     p.blockwise = true;
+    p.preload = false;
     return run_gemm(p, as_stream(stream));
 }
 

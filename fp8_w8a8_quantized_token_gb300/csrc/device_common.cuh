@@ -256,6 +256,19 @@ __device__ __forceinline__ void cluster_sync()
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Split cluster barrier without release semantics on the arrive (used after
+// fence.mbarrier_init, which already orders the barrier initialisations):
+// every thread of the cluster arrives, does other work, then waits.
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t dsmem_map(uint32_t local_smem_addr, uint32_t rank)
 {
@@ -274,10 +287,53 @@ __device__ __forceinline__ float4 dsmem_ld_f4(uint32_t cluster_addr)
     return v;
 }
 
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned)
+// from this CTA's shared memory into shared memory of another CTA of the
+// cluster; completion is signalled to an mbarrier of the DESTINATION CTA
+// (both addresses in the shared::cluster window, from dsmem_map).
+__device__ __forceinline__ void dsmem_bulk_push(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                                uint32_t mbar_cluster)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst_cluster),
+        "r"(src_cta), "r"(bytes), "r"(mbar_cluster)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until the source side of every committed bulk copy of this thread
+// has been read (its shared memory may then be reused or released).
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Make this thread's generic-proxy shared-memory writes visible to later
+// async-proxy (bulk copy / TMA) reads.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Named barrier for a subset of the CTA's warps.
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also returns the AND of every participant's `pred`:
+// all participants leave with the same answer.
+__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t nthreads, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %3, 0;\n\t"
+        "bar.red.and.pred po, %1, %2, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(id), "r"(nthreads), "r"(static_cast<uint32_t>(pred))
+        : "memory");
+    return r != 0;
 }
 
 template <typename T>

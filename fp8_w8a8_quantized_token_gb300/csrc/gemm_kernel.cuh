@@ -60,7 +60,29 @@ struct GemmArgs {
     void *out;
     long long ldo;
     unsigned *status;
+    unsigned long long *trace;  // per-CTA phase timestamps (trace builds only), or null
+    int prefetch_kb;            // weight K blocks per CTA prefetched into L2 before the dependency wait
+    int preload;                // 1: load the first tile's weight slices before the dependency wait
 };
+
+// Phase timestamps of a trace build (-DFP8Q_TRACE): kTraceSlots 64-bit
+// %globaltimer values per CTA, written by one designated thread per phase.
+constexpr int kTraceSlots = 16;
+enum TracePhase {
+    kTrEntry = 0, kTrPrologue, kTrPdlWait, kTrFirstTma, kTrFirstMma, kTrLastCommit, kTrEpiFull, kTrEpiDone,
+    kTrCluster1, kTrReduced, kTrCluster2, kTrExit, kTrPreloaded, kTrTmemAlloc, kTrSmid = 14, kTrRank = 15
+};
+#ifdef FP8Q_TRACE
+#define FP8Q_TRACE_AT(p, phase)                                                                   \
+    do {                                                                                          \
+        if ((p).trace != nullptr && blockIdx.x < 4096)                                            \
+            (p).trace[blockIdx.x * kTraceSlots + (phase)] = globaltimer_ns();                     \
+    } while (0)
+#else
+#define FP8Q_TRACE_AT(p, phase) \
+    do {                        \
+    } while (0)
+#endif
 
 template <bool SWAP, int BN, int STAGES, bool BLOCKWISE>
 struct GemmCfg {
@@ -82,14 +104,25 @@ struct GemmCfg {
     static constexpr uint32_t kOffA = 0;
     static constexpr uint32_t kOffB = kOffA + STAGES * kABytes;
     static constexpr uint32_t kOffSA = kOffB + STAGES * kBBytes;
-    static constexpr uint32_t kOffBar = kOffSA + STAGES * kSASlot;
-    static constexpr uint32_t kNumBars = 2 * STAGES + 5;  // full, empty, tfull[2], tempty[2], drain
+    // Split-K with the swapped (decode) orientation pushes partial rows into
+    // the owning CTA's receive buffer: slots for every source rank, each of
+    // up to 4*ceil(32/split) rows of BN floats (at most 144 rows in total).
+    static constexpr bool kPush = SWAP;
+    // Row stride (floats) of the partial tiles exchanged by the push
+    // reduction: padded by 4 so float4 accesses of consecutive rows by
+    // consecutive lanes hit distinct shared-memory banks.
+    static constexpr int kPartStride = BN + 4;
+    static constexpr uint32_t kRecvBytes = kPush ? 144u * kPartStride * 4u : 0u;
+    static constexpr uint32_t kOffRecv = kOffSA + STAGES * kSASlot;
+    static constexpr uint32_t kOffBar = kOffRecv + kRecvBytes;
+    static constexpr uint32_t kNumBars = 2 * STAGES + 6;  // full, empty, tfull[2], tempty[2], drain, recv
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr uint32_t kOffCol = (kOffMisc + 16 + 15) / 16 * 16;  // staged column scale, bias
     static constexpr uint32_t kSmemBytes = kOffCol + 2u * BN * 4u + 1024u;  // + alignment slack
     static constexpr uint32_t kRedBytes = 128u * BN * 4u;
     static constexpr uint32_t kIdesc = idesc_e4m3_f32<128, BN>();
-    static_assert(kRedBytes <= kOffBar, "the split-K partial tile must fit in the stage ring");
+    static_assert(kRedBytes <= kOffSA, "the split-K partial tile must fit in the stage ring");
+    static_assert(!kPush || 128u * kPartStride * 4u <= kOffSA, "the staged partial tile must fit in the ring");
     static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
     static_assert(kCols % 32 == 0 || kCols == 16, "epilogue column chunking");
@@ -129,10 +162,6 @@ __device__ __forceinline__ void tile_coords(int tile, int a_tiles, int b_tiles, 
     b_t = idx / gsize;
 }
 
-// Weight K blocks per CTA prefetched into L2 before the previous kernel
-// has finished.
-constexpr int kPrefetchKBlocks = 16;
-
 template <typename OutT>
 __device__ __forceinline__ void store_out(OutT *out, long long idx, float v)
 {
@@ -155,11 +184,15 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
     uint64_t *tfull = empty + STAGES;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
+    uint64_t *recv_full = drain + 1;
+    float *sRecv = reinterpret_cast<float *>(smem + C::kOffRecv);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
     float *sColScale = reinterpret_cast<float *>(smem + C::kOffCol);
     float *sColBias = sColScale + BN;
-    float *sRed = reinterpret_cast<float *>(smem);  // split-K partial tile, [BN][128], reuses the ring
+    // Split-K partial tile, reusing the (then idle) ring: [BN][128] for the
+    // pull reduction, [128][BN] (rows contiguous) for the push reduction.
+    float *sRed = reinterpret_cast<float *>(smem);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = p.split;
@@ -182,38 +215,81 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
             mbar_init(&tempty[i], C::kEpiWarps);
         }
         mbar_init(drain, 1);
+        mbar_init(recv_full, 1);
         *abort = 0;
         fence_mbar_init();
+        if (C::kPush && split > 1) {
+            // Expect the partial rows this CTA owns from every other rank
+            // (armed before the cluster barrier below, so before any push).
+            const int my_rows = 4 * (32 * (rank + 1) / split) - 4 * (32 * rank / split);
+            mbar_arrive_expect_tx(recv_full, static_cast<uint32_t>((split - 1) * my_rows * C::kPartStride * 4));
+        }
     }
-    pdl_trigger();
+    // Weight slices of the first tile issued before the dependency wait.
+    int npre = 0;
+    if (threadIdx.x == 0) {
+        FP8Q_TRACE_AT(p, kTrEntry);
+#ifdef FP8Q_TRACE
+        if (p.trace != nullptr && blockIdx.x < 4096) {
+            unsigned smid;
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+            p.trace[blockIdx.x * kTraceSlots + kTrSmid] = smid;
+            p.trace[blockIdx.x * kTraceSlots + kTrRank] = static_cast<unsigned long long>(rank);
+        }
+#endif
+    }
+    // Barriers must be initialised before the early weight loads below.
+    __syncthreads();
+    // Push reduction: every CTA's receive barrier must be initialised and
+    // armed before any CTA of the cluster may push into it.  Arrive now,
+    // wait just before the dependency wait (the latency overlaps the rest of
+    // the prologue).
+    if (C::kPush && split > 1) cluster_arrive_relaxed();
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tm_a);
         tma_prefetch_map(&tm_b);
         if (BLOCKWISE) tma_prefetch_map(&tm_sa);
-        // Weights never come from the previous kernel of a linear layer's
-        // pipeline, but they are only READ from L2 after pdl_wait(); this
-        // prefetch just starts streaming the first tile's weight slices from
-        // HBM while the previous kernel finishes.
+        // Every kernel of the library triggers its dependents only after
+        // its own dependency wait, so the only kernel that may still run
+        // now is the immediate predecessor; the host clears p.preload when
+        // that kernel writes the weights.  Otherwise the first tile's weight
+        // slices stream into the ring right away and the activation slices
+        // follow after pdl_wait().  Further weight slices of the first tile
+        // are prefetched into L2 (always safe: L2 is the coherence point).
         if (cluster_id < p.num_tiles) {
             int a_t, b_t;
             tile_coords(cluster_id, a_tiles, b_tiles, p.group, a_t, b_t);
             const CUtensorMap *wmap = SWAP ? &tm_a : &tm_b;
             const int wrow = SWAP ? a_t * 128 : b_t * BN;
-            const int pf = nkb < kPrefetchKBlocks ? nkb : kPrefetchKBlocks;
-            for (int i = 0; i < pf; ++i) tma_prefetch_l2_2d(wmap, (kb_begin + i) * 128, wrow);
+            uint8_t *wbuf = SWAP ? sA : sB;
+            const uint32_t wbytes = SWAP ? C::kABytes : C::kBBytes;
+            const uint64_t pol_w = SWAP ? policy_evict_first() : policy_evict_normal();
+            npre = p.preload ? (nkb < STAGES ? nkb : STAGES) : 0;
+            for (int i = 0; i < npre; ++i) {
+                mbar_arrive_expect_tx(&full[i], C::kStageTx);
+                tma_load_2d(wbuf + i * wbytes, wmap, &full[i], (kb_begin + i) * 128, wrow, pol_w);
+            }
+            const int pf = nkb < p.prefetch_kb ? nkb : p.prefetch_kb;
+            for (int i = npre; i < pf; ++i) tma_prefetch_l2_2d(wmap, (kb_begin + i) * 128, wrow);
         }
+        FP8Q_TRACE_AT(p, kTrPreloaded);
     }
     if (warp == 1) {
         tmem_alloc(tmem_holder, C::kTmemCols);
         tmem_relinquish();
+        if (lane == 0) FP8Q_TRACE_AT(p, kTrTmemAlloc);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    if (C::kPush && split > 1) cluster_wait();
+    if (threadIdx.x == 0) FP8Q_TRACE_AT(p, kTrPrologue);
     // Everything below may read the previous kernel's output (activations,
     // scales) or overwrite buffers it reads (out).
     pdl_wait();
+    pdl_trigger();
+    if (threadIdx.x == 0) FP8Q_TRACE_AT(p, kTrPdlWait);
 
     if (warp == 0) {
         // ------------------------------------------------------------------
@@ -233,10 +309,19 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
                 bool ok = true;
                 for (int i = 0; i < nkb; ++i) {
                     const int kb = kb_begin + i;
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort, p.status)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&full[stage], C::kStageTx);
-                    tma_load_2d(sA + stage * C::kABytes, &tm_a, &full[stage], kb * 128, a_row, pol_a);
-                    tma_load_2d(sB + stage * C::kBBytes, &tm_b, &full[stage], kb * 128, b_row, pol_b);
+                    if (issued == 0) FP8Q_TRACE_AT(p, kTrFirstTma);
+                    if (issued < npre) {
+                        // Weight slice already in flight; barrier armed.
+                        if (SWAP)
+                            tma_load_2d(sB + stage * C::kBBytes, &tm_b, &full[stage], kb * 128, b_row, pol_b);
+                        else
+                            tma_load_2d(sA + stage * C::kABytes, &tm_a, &full[stage], kb * 128, a_row, pol_a);
+                    } else {
+                        if (!mbar_wait(&empty[stage], phase ^ 1u, abort, p.status)) { ok = false; break; }
+                        mbar_arrive_expect_tx(&full[stage], C::kStageTx);
+                        tma_load_2d(sA + stage * C::kABytes, &tm_a, &full[stage], kb * 128, a_row, pol_a);
+                        tma_load_2d(sB + stage * C::kBBytes, &tm_b, &full[stage], kb * 128, b_row, pol_b);
+                    }
                     if (BLOCKWISE)
                         tma_load_2d(sSA + stage * C::kSASlotFloats, &tm_sa, &full[stage], m_tile * C::kTokTile, kb,
                                     pol_b);
@@ -247,6 +332,10 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
             }
             // Drain: the last STAGES copies must have landed before the CTA
             // may exit (they complete in the normal flow long before this).
+            // Preloaded weight slices whose stage never got its activation
+            // slice (an early abort) are waited for as well: their barrier
+            // phase cannot complete, so the wait only ends on the timeout.
+            if (issued < npre) issued = npre;
             const long long first = issued > STAGES ? issued - STAGES : 0;
             for (long long j = first; j < issued; ++j)
                 mbar_wait_drain(&full[j % STAGES], static_cast<uint32_t>((j / STAGES) & 1), p.status);
@@ -270,6 +359,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
                     }
                     if (!mbar_wait(&full[stage], phase, abort, p.status)) { ok = false; break; }
                     tc_fence_after();
+                    if (tile == cluster_id && i == 0) FP8Q_TRACE_AT(p, kTrFirstMma);
                     const uint32_t a_addr = smem_u32(sA + stage * C::kABytes);
                     const uint32_t b_addr = smem_u32(sB + stage * C::kBBytes);
                     const uint32_t d = tmem_base + slot * BN;
@@ -294,6 +384,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
                     if (slot == 0) tphase ^= 1u;
                 }
             }
+            FP8Q_TRACE_AT(p, kTrLastCommit);
             // Every MMA this thread issued has finished before TMEM is freed.
             umma_commit(drain);
             mbar_wait_drain(drain, 0, p.status);
@@ -385,6 +476,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
                 ok = __all_sync(0xffffffffu, mbar_wait(&tfull[slot], tphase, abort, p.status));
                 if (ok) {
                     tc_fence_after();
+                    if (warp == 2 && lane == 0) FP8Q_TRACE_AT(p, kTrEpiFull);
                     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + slot * BN + col0;
 #pragma unroll
                     for (int c = 0; c < C::kCols; c += 16) {
@@ -402,9 +494,10 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
                 }
             }
             // No early exit from the tile loop: every epilogue thread must
-            // reach the same named barriers.  After a timeout every further
-            // wait fails at once and the stores below are skipped.
-            if (!ok) continue;
+            // reach the same named barriers, so all of them take the same
+            // decision (after a timeout every further wait fails at once
+            // and the output below is skipped).
+            if (!named_barrier_and(1, C::kEpiThreads, ok && !*abort)) continue;
 
             if (split == 1) {
                 // Scale, add bias, convert, store.
@@ -449,18 +542,81 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
                         }
                     }
                 }
+            } else if (C::kPush) {
+                // Split-K, push: stage the partial tile row-major in the idle
+                // ring, push each other rank's rows into its receive buffer
+                // (bulk DSMEM copies completing on its mbarrier), then the
+                // epilogue warps together add up the rows this CTA owns, over
+                // the ranks in increasing order (a fixed order: the result is
+                // deterministic).
+                constexpr int SP = C::kPartStride;
+                named_barrier_sync(1, C::kEpiThreads);
+#pragma unroll
+                for (int j = 0; j < C::kCols; j += 4)
+                    *reinterpret_cast<float4 *>(sRed + row * SP + col0 + j) =
+                        make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                fence_proxy_async_smem();
+                named_barrier_sync(1, C::kEpiThreads);
+                const int slot_rows = 4 * ((32 + split - 1) / split);
+                if (etid == 0) {
+                    for (int q = 0; q < split; ++q) {
+                        if (q == rank) continue;
+                        const int q_lo = 4 * (32 * q / split), q_hi = 4 * (32 * (q + 1) / split);
+                        const uint32_t src = smem_u32(sRed + q_lo * SP);
+                        const uint32_t dst = dsmem_map(smem_u32(sRecv + rank * slot_rows * SP), q);
+                        dsmem_bulk_push(dst, src, static_cast<uint32_t>((q_hi - q_lo) * SP * 4),
+                                        dsmem_map(smem_u32(recv_full), q));
+                    }
+                    bulk_commit();
+                }
+                const int my_lo = 4 * (32 * rank / split), my_hi = 4 * (32 * (rank + 1) / split);
+                const int my_rows = my_hi - my_lo;
+                if (mbar_wait(recv_full, 0, abort, p.status)) {
+                    // Items (owned row r, 4-column group c4), rows fastest so a
+                    // warp's stores of one column group are contiguous in n.
+                    for (int item = etid; item < my_rows * (BN / 4); item += C::kEpiThreads) {
+                        const int c4 = item / my_rows;
+                        const int r = my_lo + (item - c4 * my_rows);
+                        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int q = 0; q < split; ++q) {
+                            const float *src = q == rank ? sRed + r * SP
+                                                         : sRecv + (q * slot_rows + (r - my_lo)) * SP;
+                            const float4 v = *reinterpret_cast<const float4 *>(src + c4 * 4);
+                            sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+                        }
+                        const int n = n0 + r;
+                        if (n < p.N) {
+                            const float ws = BLOCKWISE ? 1.0f : __ldg(p.w_scale + n);
+                            const float bv = p.bias != nullptr ? __bfloat162float(p.bias[n]) : 0.0f;
+                            const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int m = m0 + c4 * 4 + e;
+                                if (m < p.M) {
+                                    const float y = BLOCKWISE ? sv[e] + bv : fmaf(sv[e] * ws, sColScale[c4 * 4 + e], bv);
+                                    store_out(out, static_cast<long long>(m) * p.ldo + n, y);
+                                }
+                            }
+                        }
+                    }
+                }
+                // The pushed rows must have left this CTA's shared memory
+                // before it may exit.
+                if (etid == 0) bulk_wait_read();
             } else {
-                // Split-K: publish this CTA's partial tile (the ring is idle:
-                // every copy was consumed and every MMA has completed).
+                // Split-K, pull: publish this CTA's partial tile (the ring is
+                // idle: every copy was consumed and every MMA has completed).
                 named_barrier_sync(1, C::kEpiThreads);
 #pragma unroll
                 for (int j = 0; j < C::kCols; ++j) sRed[(col0 + j) * 128 + row] = acc[j];
             }
+            if (warp == 2 && lane == 0) FP8Q_TRACE_AT(p, kTrEpiDone);
         }
     }
 
-    if (split > 1) {
+    if (split > 1 && !C::kPush) {
         cluster_sync();
+        if (threadIdx.x == 64) FP8Q_TRACE_AT(p, kTrCluster1);
         if (warp >= 2 && !*abort) {
             // Reduce rows [r_lo, r_hi) (whole groups of 4) over the cluster.
             const int etid = threadIdx.x - 64;
@@ -495,7 +651,9 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
                 }
             }
         }
+        if (threadIdx.x == 64) FP8Q_TRACE_AT(p, kTrReduced);
         cluster_sync();
+        if (threadIdx.x == 64) FP8Q_TRACE_AT(p, kTrCluster2);
     }
 
     tc_fence_before();
@@ -503,6 +661,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::kTmemCols);
+        if (lane == 0) FP8Q_TRACE_AT(p, kTrExit);
     }
 }
 

@@ -68,6 +68,9 @@ cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigne
     a.out = pr.out;
     a.ldo = pr.N;
     a.status = status;
+    a.trace = trace_buffer();
+    a.prefetch_kb = prefetch_kblocks();
+    a.preload = pr.preload ? 1 : 0;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(l.grid));

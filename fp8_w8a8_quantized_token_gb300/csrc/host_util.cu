@@ -3,6 +3,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <stdlib.h>
+
 #include <atomic>
 #include <mutex>
 
@@ -13,6 +15,13 @@ namespace fp8q {
 // Device status word: one per device that loads the library, written only
 // by kernels that give up on a bounded wait.
 __device__ unsigned g_status_word;
+
+#ifdef FP8Q_TRACE
+// Trace builds: 16 timestamps for each of the first 4096 CTAs of each of
+// the 4 most recent GEMM launches (launch i uses block i % 4).
+__device__ unsigned long long g_trace_buf[4 * 4096 * 16];
+std::atomic<unsigned> g_trace_launch{0};
+#endif
 
 namespace {
 
@@ -71,6 +80,61 @@ unsigned *device_status_ptr()
     return p;
 }
 
+unsigned long long *trace_buffer()
+{
+#ifdef FP8Q_TRACE
+    void *addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_trace_buf) != cudaSuccess) return nullptr;
+    const unsigned i = g_trace_launch.fetch_add(1) % 4u;
+    return static_cast<unsigned long long *>(addr) + static_cast<size_t>(i) * 4096 * 16;
+#else
+    return nullptr;
+#endif
+}
+
+int prefetch_kblocks()
+{
+    static const int v = [] {
+        const char *s = getenv("FP8Q_PREFETCH_KB");
+        return s != nullptr ? atoi(s) : 16;
+    }();
+    return v;
+}
+
+namespace {
+struct LaunchRecord {
+    cudaStream_t stream;
+    uintptr_t lo, hi;
+};
+std::mutex g_launch_mu;
+LaunchRecord g_launches[64];
+int g_launch_next = 0;
+}  // namespace
+
+void note_launch_writes(cudaStream_t st, const void *base, size_t bytes)
+{
+    std::lock_guard<std::mutex> g(g_launch_mu);
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(base);
+    for (auto &r : g_launches)
+        if (r.stream == st && r.hi != 0) {
+            r.lo = lo;
+            r.hi = lo + bytes;
+            return;
+        }
+    g_launches[g_launch_next] = {st, lo, lo + bytes};
+    g_launch_next = (g_launch_next + 1) % 64;
+}
+
+bool last_launch_writes_overlap(cudaStream_t st, const void *base, size_t bytes)
+{
+    std::lock_guard<std::mutex> g(g_launch_mu);
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(base), hi = lo + bytes;
+    for (const auto &r : g_launches)
+        if (r.stream == st && r.hi != 0) return r.lo < hi && lo < r.hi;
+    // No record for this stream (evicted or never seen): assume the worst.
+    return true;
+}
+
 int current_device_sms()
 {
     int dev = 0;
@@ -97,3 +161,19 @@ cudaError_t read_status_word(unsigned *value, bool reset, cudaStream_t st)
 }
 
 }  // namespace fp8q
+
+#ifdef FP8Q_TRACE
+// Diagnostics ABI of trace builds (include/fp8q_trace.h).
+extern "C" __attribute__((visibility("default"))) int fp8q_trace_read(unsigned long long *host, int count)
+{
+    if (count > 4 * 4096 * 16) count = 4 * 4096 * 16;
+    return cudaMemcpyFromSymbol(host, fp8q::g_trace_buf, sizeof(unsigned long long) * count) == cudaSuccess ? 0 : 3;
+}
+extern "C" __attribute__((visibility("default"))) int fp8q_trace_clear(void)
+{
+    void *addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, fp8q::g_trace_buf) != cudaSuccess) return 3;
+    fp8q::g_trace_launch.store(0);
+    return cudaMemset(addr, 0, sizeof(unsigned long long) * 4 * 4096 * 16) == cudaSuccess ? 0 : 3;
+}
+#endif

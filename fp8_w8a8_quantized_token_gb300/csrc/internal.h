@@ -38,6 +38,7 @@ struct GemmProblem {
     void *out;              // [M, N]
     bool out_fp16;
     bool blockwise;
+    bool preload;           // weights may be read before the dependency wait
 };
 
 // Launchers return cudaSuccess or the launch error; a tensor map the driver
@@ -48,7 +49,13 @@ cudaError_t launch_gemm_blockwise(const GemmProblem &p, const GemmLaunch &l, uns
 
 // Pipeline depth of the instantiation serving (swap_ab, mma_n): the
 // shared-memory ring holds `stages` slots of 16 KB (A) + mma_n*128 B (B).
-constexpr int stages_for(bool swap_ab, int mma_n) { return swap_ab ? (mma_n <= 64 ? 8 : 6) : 4; }
+// The 16- and 32-token decode tiles keep their footprint near 100 KB so two
+// CTAs fit on one SM: a layer's GEMM can then start (prologue, L2 weight
+// prefetch) on SMs still running the previous layer's tail.
+constexpr int stages_for(bool swap_ab, int mma_n)
+{
+    return swap_ab ? (mma_n == 16 ? 5 : mma_n == 32 ? 4 : mma_n == 64 ? 7 : 4) : 4;
+}
 
 // True if an instantiation exists for (swap_ab, mma_n).
 constexpr bool gemm_shape_supported(bool swap_ab, int mma_n)
@@ -65,6 +72,19 @@ bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
 
 // ---- device status word (host_util.cu) --------------------------------------
 unsigned *device_status_ptr();   // of the current device, or null
+// Per-CTA phase timestamps of a trace build (-DFP8Q_TRACE); null otherwise.
+unsigned long long *trace_buffer();
+// Weight K blocks each GEMM CTA prefetches into L2 before its dependency
+// wait (default 16; FP8Q_PREFETCH_KB overrides it at start-up, 0 disables).
+int prefetch_kblocks();
+
+// Per-stream record of the byte range the library's most recent launch on
+// that stream writes.  With programmatic dependent launch, that launch is the
+// only kernel that may still be running when the next one starts (every
+// kernel triggers its dependents only after its own dependency wait), so a
+// GEMM may read its weights early unless they overlap this range.
+void note_launch_writes(cudaStream_t st, const void *base, size_t bytes);
+bool last_launch_writes_overlap(cudaStream_t st, const void *base, size_t bytes);
 int current_device_sms();        // SM count of the current device (cached)
 
 }  // namespace fp8q

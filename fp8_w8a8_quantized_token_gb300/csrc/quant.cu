@@ -72,6 +72,16 @@ __device__ __forceinline__ uint4 quant_chunk(const Chunk16 &c, float s)
 
 __device__ __forceinline__ float scale_of(float amax, float eps) { return fmaxf(amax, eps) / 448.0f; }
 
+// Programmatic dependent launch: each quantizer first waits for the
+// previous kernel in the stream (so every earlier kernel has completed), then
+// lets the next kernel launch.  When any kernel of this library starts, at
+// most its immediate predecessor can still be running.
+__device__ __forceinline__ void pdl_enter()
+{
+    pdl_wait();
+    pdl_trigger();
+}
+
 // ---------------------------------------------------------------------------
 // Per-token quantization: one CTA per row, blockDim.x = T (multiple of 32),
 // each thread caches up to VPT 16-element chunks in registers so the row is
@@ -84,8 +94,7 @@ __global__ void __launch_bounds__(1024) quant_per_token_kernel(const __nv_bfloat
                                                                int K, float eps)
 {
     __shared__ float warp_max[32];
-    pdl_trigger();
-    pdl_wait();
+    pdl_enter();
     const int64_t row = blockIdx.x;
     const int chunks = K >> 4;
     const __nv_bfloat16 *xr = x + row * ldx;
@@ -124,8 +133,7 @@ __global__ void __launch_bounds__(1024) quant_per_token_two_pass_kernel(const __
                                                                         float *__restrict__ xs, int K, float eps)
 {
     __shared__ float warp_max[32];
-    pdl_trigger();
-    pdl_wait();
+    pdl_enter();
     const int64_t row = blockIdx.x;
     const int chunks = K >> 4;
     const __nv_bfloat16 *xr = x + row * ldx;
@@ -158,8 +166,7 @@ __global__ void __launch_bounds__(256) quant_group_kernel(const __nv_bfloat16 *_
                                                           uint8_t *__restrict__ xq, float *__restrict__ xs,
                                                           int64_t M, int K, int64_t m_pad, float eps)
 {
-    pdl_trigger();
-    pdl_wait();
+    pdl_enter();
     const int chunks_per_row = K >> 4;
     const int64_t total = M * chunks_per_row;
     for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
@@ -192,8 +199,7 @@ __global__ void __launch_bounds__(256) quant_weight_block128_kernel(const __nv_b
                                                                     float *__restrict__ ws, int64_t K, float eps)
 {
     __shared__ float warp_max[8];
-    pdl_trigger();
-    pdl_wait();
+    pdl_enter();
     const int64_t bn = blockIdx.y, bk = blockIdx.x;
     // 128 rows x 8 chunks of 16; thread t handles chunks t, t + 256, ...
     Chunk16 c[4];

@@ -44,6 +44,19 @@
  *     instead of hanging; read it with fp8q_device_status().
  *   - M == 0 is valid and enqueues nothing.
  *   - No C++ exception crosses this interface.
+ *   - Kernels are launched with programmatic dependent launch: a kernel
+ *     may start while the previous kernel in the stream is still running.
+ *     Every kernel of the library first waits for its predecessor and only
+ *     then lets its own successor launch, so at most the immediate
+ *     predecessor can be running when a kernel starts.  A GEMM streams its
+ *     WEIGHT operand before that wait unless the library's own most recent
+ *     launch on the same stream writes an overlapping byte range (then it
+ *     waits first).  A foreign kernel that triggers programmatic
+ *     dependents before its writes are complete must therefore not write
+ *     the weights of a GEMM launched right after it; ordinary kernels and
+ *     copies (no such trigger) are always safe producers.
+ *   - Consecutive calls on one stream are ordered as usual; calls racing on
+ *     different streams need the caller's own synchronization.
  */
 #ifndef FP8Q_H_
 #define FP8Q_H_

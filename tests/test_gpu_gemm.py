@@ -17,8 +17,8 @@ from gpu_util import (THREADS, assert_gemm_close, out_values, quant_both_group, 
 
 pytestmark = pytest.mark.gpu
 
-SCHEDULES = [(1, 16, 1), (1, 16, 3), (1, 32, 2), (1, 32, 8), (1, 64, 1), (1, 64, 4), (1, 128, 1), (1, 128, 2),
-             (0, 256, 1), (0, 256, 2), (0, 256, 5)]
+SCHEDULES = [(1, 16, 1), (1, 16, 3), (1, 16, 5), (1, 32, 2), (1, 32, 8), (1, 64, 1), (1, 64, 4), (1, 64, 7),
+             (1, 128, 1), (1, 128, 2), (1, 128, 6), (0, 256, 1), (0, 256, 2), (0, 256, 5)]
 
 
 @pytest.fixture(scope="module")
@@ -172,3 +172,36 @@ def test_m0_and_status_word(dev):
     out = fq.fp8q_scaled_mm_channelwise(a, w, torch.empty(0, device=dev), s)
     assert out.shape == (0, 128)
     assert fq.fp8q_device_status() == fq.FP8Q_OK
+
+
+@pytest.mark.parametrize("order", ["weights_then_gemm", "weights_act_gemm"])
+def test_weights_rewritten_right_before_the_gemm(dev, order):
+    """The GEMM streams weights before waiting for its predecessor; a weight
+    buffer rewritten by the immediately preceding (or the one before that)
+    launch on the stream must still be read fresh.  Each iteration writes
+    new values into the SAME weight buffer with no synchronization."""
+    M, N, K = 8, 512, 2048
+    x = synthetic.activations(M, K, seed=50)
+    xd = x.to(dev)
+    wq = torch.empty((N, K), dtype=fq.E4M3, device=dev)
+    ws = torch.empty((N,), dtype=torch.float32, device=dev)
+    xq = torch.empty((M, K), dtype=fq.E4M3, device=dev)
+    xs = torch.empty((M,), dtype=torch.float32, device=dev)
+    ws_cpu, outs = [], []
+    for i in range(4):
+        w = synthetic.weights(N, K, seed=100 + i).to(dev)
+        torch.cuda.synchronize()
+        if order == "weights_then_gemm":
+            fq.fp8q_quant_per_token(xd, xq=xq, x_scale=xs)
+            fq.fp8q_quant_per_token(w, xq=wq, x_scale=ws)
+        else:
+            fq.fp8q_quant_per_token(w, xq=wq, x_scale=ws)
+            fq.fp8q_quant_per_token(xd, xq=xq, x_scale=xs)
+        outs.append(fq.fp8q_scaled_mm_channelwise(xq, wq, xs, ws))
+        ws_cpu.append(w.cpu())
+    torch.cuda.synchronize()
+    rq, rs = oracle.quant_per_token(x)
+    for i in range(4):
+        rwq, rws = oracle.quant_weight_per_channel(ws_cpu[i])
+        ref = ref_values(oracle.gemm_channelwise(rq, rwq, rs, rws, threads=THREADS))
+        assert_gemm_close(out_values(outs[i]), ref, f"iteration {i}")
