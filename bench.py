@@ -28,9 +28,10 @@ METRIC = "FP8 W8A8 GEMM TFLOP/s & GB/s vs M (1-8192) and % of roofline"
 UNIT = "TFLOP/s"
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
-# kernel, from the ncu capture summarised under profiles/ (None until a
-# capture of the current kernel exists).
-DOMINANT_TRAFFIC_BYTES = {}
+# kernel, keyed by (scheme, swap_ab, mma_n), averaged over that kernel's
+# launches in the ncu launch list of this benchmark (profiles/
+# launches_oproj_sweep.md).  A key is dropped whenever its kernel changes.
+DOMINANT_TRAFFIC_BYTES = {("channelwise", 0, 256): 31.1e6}
 
 WORKLOADS = {
     # name: (list of (label, N, K, blockwise), M sweep, outliers)
@@ -51,6 +52,22 @@ WORKLOAD_DESC = {
     "tiny": "channelwise 16x256x512",
 }
 L2_BYTES = 129 * 1024 * 1024
+
+
+def reduce_max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(flops_per_rank_step: float, world: int, ms_per_step_max: float) -> float:
+    """Whole-job TFLOP/s: every rank processes its own batch (weak scaling)."""
+    return flops_per_rank_step * world / (ms_per_step_max * 1e-3) / 1e12
 
 
 def load_peaks():
@@ -89,7 +106,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.reader = threading.Thread(target=self._read, daemon=True)
             self.reader.start()
@@ -221,12 +238,12 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="fp8q", choices=["fp8q", "reference"])
     ap.add_argument("--workload", default="oproj_sweep", choices=sorted(WORKLOADS))
     ap.add_argument("--ref-rows", type=int, default=2, help="oracle rows per M in the reference arm")
-    ap.add_argument("--cpu-rows", type=int, default=32, help="oracle rows per M for cpu_baseline")
+    ap.add_argument("--cpu-rows", type=int, default=256, help="oracle rows per M for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--kernel-replays", type=int, default=20)
@@ -367,14 +384,10 @@ def main():
             step_graph.replay()
         end.record(stream)
         barrier()
-    elapsed_ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = reduce_max_over_ranks(start.elapsed_time(end), world, dev)
     ms_per_step = elapsed_ms / args.steps
     flops_step = sum(2 * p["M"] * p["N"] * p["K"] for p in problems)
-    value = flops_step * world / (ms_per_step * 1e-3) / 1e12
+    value = aggregate_value(flops_step, world, ms_per_step)
 
     # ---- per-kernel durations: each problem's GEMM (and quantizer) launched
     # REPS times back to back in a graph, the GEMM over rotating weight
@@ -474,12 +487,8 @@ def main():
         e2e_graph.replay()
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": round(flops_step * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+    e2e_ms = reduce_max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
+    e2e = {"value": round(aggregate_value(flops_step, world, e2e_ms), 2), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
            "how": "CUDA graph per step: pinned-host->device copy of each M's activations, the linear "
                   "entry point (quant + GEMM), device->pinned-host copy of its output"}

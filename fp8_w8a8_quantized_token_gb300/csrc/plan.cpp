@@ -43,15 +43,20 @@ int next_pow2(int64_t v)
     return p;
 }
 
-// Generic rule: decode-size M puts the weights on the MMA's 128-row side
-// and the tokens on its N side (smallest MMA N >= M); larger M uses
-// 128 x 256 tiles.  If the tiles cannot fill the GPU, K is split across a
-// cluster of up to 8 CTAs.
+// Generic rule (shapes without table rows), following what the sweep found
+// on the measured shapes: up to 64 tokens the weights take the MMA's
+// 128-row side and the tokens its N side (smallest MMA N >= M); up to 512
+// tokens 128-token swapped tiles; beyond that 128 x 256 tiles.  If the tiles
+// cannot fill the GPU, K is split across a cluster of 2, 4 or 8 CTAs (odd
+// cluster sizes measured slower).
 void generic_rule(int64_t M, int64_t N, int64_t K, int num_sms, fp8q_plan *pl)
 {
-    if (M <= 128) {
+    if (M <= 64) {
         pl->swap_ab = 1;
         pl->mma_n = next_pow2(M < 16 ? 16 : M);
+    } else if (M <= 512) {
+        pl->swap_ab = 1;
+        pl->mma_n = 128;
     } else {
         pl->swap_ab = 0;
         pl->mma_n = 256;
@@ -59,9 +64,9 @@ void generic_rule(int64_t M, int64_t N, int64_t K, int num_sms, fp8q_plan *pl)
     const int tile_m = pl->swap_ab ? pl->mma_n : 128;
     const int tile_n = pl->swap_ab ? 128 : pl->mma_n;
     const int64_t tiles = ((M + tile_m - 1) / tile_m) * ((N + tile_n - 1) / tile_n);
-    int64_t split = 1;
-    if (tiles < num_sms) split = num_sms / (tiles > 0 ? tiles : 1);
-    pl->split_k = static_cast<int32_t>(split);
+    int split = 1;
+    while (split < 8 && tiles * split * 2 <= num_sms) split *= 2;
+    pl->split_k = split;
 }
 
 // Process-wide schedule override (fp8q_set_plan_override), initialised

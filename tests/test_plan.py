@@ -53,8 +53,8 @@ def test_plans_are_launchable(num_sms):
 
 def test_decode_sizes_put_weights_on_the_mma_m_side():
     for M in (1, 8, 16, 33, 64):
-        p = fq.fp8q_gemm_plan(M, 4096, 4096, num_sms=148)
-        assert p["swap_ab"] == 1 and p["tile_m"] >= M or p["tile_m"] == 128
+        for N, K in ((4096, 4096), (8000, 1024)):   # a tabulated and an untabulated shape
+            assert fq.fp8q_gemm_plan(M, N, K, num_sms=148)["swap_ab"] == 1
 
 
 def test_override_forces_the_schedule_and_clamps_split():
@@ -66,3 +66,45 @@ def test_override_forces_the_schedule_and_clamps_split():
         assert fq.fp8q_gemm_plan(1, 4096, 4096, num_sms=148)["split_k"] == 8
     finally:
         fq.fp8q_set_plan_override(-1)
+
+
+def load_table():
+    import os
+    import re
+    path = os.path.join(os.path.dirname(fq.__file__), "csrc", "tile_table.inc")
+    rows = []
+    for line in open(path):
+        m = re.match(r"\s*\{(-?\d+), (-?\d+), (-?\d+), (-?\d+), (-?\d+), (-?\d+), (-?\d+)\},", line)
+        if m:
+            rows.append(tuple(int(v) for v in m.groups()))
+    return rows
+
+
+def test_table_lookup_is_nearest_m_with_ties_to_the_smaller_m():
+    """The rule of get_w8a8_channelwise_fp8_config: configs[min(keys, key=|k - M|)]
+    with keys scanned in ascending order, so a tie goes to the smaller key."""
+    rows = load_table()
+    assert rows, "the sweep table is empty"
+    by_shape = {}
+    for N, K, bw, M, swap, mma_n, split in rows:
+        by_shape.setdefault((N, K, bw), []).append((M, (swap, mma_n, split)))
+    for (N, K, bw), entries in by_shape.items():
+        entries.sort()
+        keys = [m for m, _ in entries]
+        table = dict(entries)
+        probe = sorted(set(keys + [(a + b) // 2 for a, b in zip(keys, keys[1:])] + [k + 1 for k in keys] + [3, 10000]))
+        for M in probe:
+            best = min(keys, key=lambda k: abs(k - M))   # Python's min keeps the first (smallest) on ties
+            swap, mma_n, split = table[best]
+            p = fq.fp8q_gemm_plan(M, N, K, bool(bw), num_sms=148)
+            assert p["from_table"] == 1
+            assert (p["swap_ab"], p["mma_n"]) == (swap, mma_n), (N, K, bw, M, best)
+            assert p["split_k"] == min(split, 8, -(-K // 128)), (N, K, bw, M, best)
+
+
+def test_shapes_without_rows_use_the_generic_rule():
+    p = fq.fp8q_gemm_plan(7, 1000 * 8, 1024, num_sms=148)
+    assert p["from_table"] == 0 and p["swap_ab"] == 1 and p["mma_n"] == 16
+    assert p["split_k"] in (1, 2, 4, 8)
+    p = fq.fp8q_gemm_plan(4000, 8000, 1024, num_sms=148)
+    assert p["from_table"] == 0 and (p["swap_ab"], p["mma_n"], p["split_k"]) == (0, 256, 1)
