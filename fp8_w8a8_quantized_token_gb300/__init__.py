@@ -26,6 +26,8 @@ LIB_PATH = os.path.join(_HERE, "libfp8q.so")
 FP8Q_OK, FP8Q_ERR_INVALID_ARG, FP8Q_ERR_UNSUPPORTED, FP8Q_ERR_CUDA, FP8Q_ERR_TIMEOUT = range(5)
 FP8Q_OUT_BF16, FP8Q_OUT_FP16 = 0, 1
 E4M3 = torch.float8_e4m3fn
+# Capacity of the library's own scratch array (fp8q_linear_channelwise_noalloc).
+NOALLOC_MAX_CODES, NOALLOC_MAX_ROWS = 16 * 1024 * 1024, 16384
 
 # Every symbol include/fp8q.h declares (checked by the ABI test).
 EXPORTED = (
@@ -36,6 +38,7 @@ EXPORTED = (
     "fp8q_scaled_mm_blockwise",
     "fp8q_linear_channelwise",
     "fp8q_linear_blockwise",
+    "fp8q_linear_channelwise_noalloc",
     "fp8q_gemm_plan",
     "fp8q_set_plan_override",
     "fp8q_device_status",
@@ -80,6 +83,7 @@ def load_library(path: str | None = None):
         "fp8q_scaled_mm_blockwise": [P, P, P, P, P, P, I64, I64, I64, I64, ctypes.c_int, P],
         "fp8q_linear_channelwise": [P, P, I64, P, P, P, I64, I64, I64, P, P, ctypes.c_int, P],
         "fp8q_linear_blockwise": [P, P, P, P, P, I64, I64, I64, P, P, I64, ctypes.c_int, P],
+        "fp8q_linear_channelwise_noalloc": [P, P, I64, P, P, P, I64, I64, I64, ctypes.c_int, P],
         "fp8q_gemm_plan": [I64, I64, I64, I32, I32, ctypes.POINTER(Plan)],
         "fp8q_device_status": [P, I32],
         "fp8q_set_plan_override": [I32, I32, I32],
@@ -313,6 +317,39 @@ def fp8q_linear_blockwise(x: torch.Tensor, w: torch.Tensor, w_scale: torch.Tenso
     _check("fp8q_linear_blockwise",
            L.fp8q_linear_blockwise(_ptr(x), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(out), M, N, K, _ptr(xq),
                                    _ptr(xs), m_pad, _out_code(out_dtype), _stream(x.device)))
+    return out
+
+
+def fp8q_linear_channelwise_noalloc(x: torch.Tensor, b: torch.Tensor, b_scale: torch.Tensor, bias=None,
+                                    out_dtype=torch.bfloat16, out: torch.Tensor | None = None):
+    """fp8q_linear_channelwise without scratch buffers: the quantized
+    activations live in the library's fixed device array, so the C call
+    allocates nothing (for callers whose device memory is owned by another
+    allocator, or that cannot take cudaMalloc's synchronisation).  Only
+    ``out`` is the caller's; pass it to keep this wrapper from allocating.
+    Limits: M <= NOALLOC_MAX_ROWS and M * K <= NOALLOC_MAX_CODES.  Calls that
+    can overlap on the GPU (other streams) share that array and race."""
+    L = load_library()
+    _need(x, torch.bfloat16, "x")
+    _need(b, E4M3, "b", x.device)
+    _need(b_scale, torch.float32, "b_scale", x.device)
+    if bias is not None:
+        _need(bias, torch.bfloat16, "bias", x.device)
+    if x.dim() != 2 or not x.is_contiguous() or b.stride(1) != 1:
+        raise ValueError("x must be contiguous [M, K]; b [N, K] with contiguous rows")
+    M, K = x.shape
+    N = b.shape[0]
+    if M > NOALLOC_MAX_ROWS or M * K > NOALLOC_MAX_CODES:
+        raise ValueError(f"x is {M} x {K}: the no-alloc scratch holds at most {NOALLOC_MAX_ROWS} rows and "
+                         f"{NOALLOC_MAX_CODES} elements; use fp8q_linear_channelwise with your own buffers")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    _need(out, out_dtype, "out", x.device)
+    if tuple(out.shape) != (M, N) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [M, N] tensor")
+    _check("fp8q_linear_channelwise_noalloc",
+           L.fp8q_linear_channelwise_noalloc(_ptr(x), _ptr(b), b.stride(0), _ptr(b_scale), _ptr(bias), _ptr(out),
+                                             M, N, K, _out_code(out_dtype), _stream(x.device)))
     return out
 
 

@@ -200,6 +200,42 @@ FP8Q_API fp8q_status fp8q_linear_blockwise(const void *x, const void *w, const f
                                   void *stream);
 
 /* ---------------------------------------------------------------------------
+ * fp8q_linear_channelwise_noalloc -- the pages have no counterpart: this is
+ * an addition of this library for callers that cannot allocate.
+ *
+ * Same computation, arguments and errors as fp8q_linear_channelwise, minus
+ * the scratch buffers xq and xs: the E4M3 codes and per-token scales live
+ * in a fixed array inside the library (a file-scope __device__ array of
+ * FP8Q_NOALLOC_MAX_CODES + 4 * FP8Q_NOALLOC_MAX_ROWS bytes = 16 MiB + 64 KiB,
+ * held on every GPU that loads the library until the process exits).
+ * It is meant for callers that cannot call cudaMalloc: code whose device
+ * memory is handed out entirely by a host framework's own pool (a plugin
+ * given no workspace, an engine that budgets every byte up front), or a
+ * latency-bound loop that cannot take the device synchronisation that
+ * cudaMalloc / cudaFree imply.  The call allocates and frees nothing.
+ *
+ * Limits  : M <= FP8Q_NOALLOC_MAX_ROWS and M * K <= FP8Q_NOALLOC_MAX_CODES;
+ *           larger problems return FP8Q_ERR_UNSUPPORTED before any CUDA
+ *           call (use fp8q_linear_channelwise with your own buffers).
+ * Set-up  : the first call on each device looks up the array's device
+ *           address (cudaGetSymbolAddress, with that device current) and
+ *           caches it; make that first call before any stream capture.
+ *           A failed look-up returns FP8Q_ERR_CUDA.
+ * Sharing : every call on a device uses the same array, which keeps the
+ *           last call's contents (nothing in it needs to start at zero:
+ *           the quantizer writes every code and scale the GEMM reads).
+ *           Calls in order on one stream are safe; calls that can overlap
+ *           on the GPU (different streams without synchronisation between
+ *           them) race on the array and give wrong results.
+ * ------------------------------------------------------------------------- */
+#define FP8Q_NOALLOC_MAX_CODES (16LL * 1024 * 1024)
+#define FP8Q_NOALLOC_MAX_ROWS 16384LL
+FP8Q_API fp8q_status fp8q_linear_channelwise_noalloc(const void *x, const void *b, int64_t ldb,
+                                            const float *b_scale, const void *bias, void *out,
+                                            int64_t M, int64_t N, int64_t K,
+                                            fp8q_out_dtype out_dtype, void *stream);
+
+/* ---------------------------------------------------------------------------
  * Tile selection (host only, no GPU needed).  The GEMM schedule for a
  * problem: which operand sits on the MMA's 128-row side, the MMA N extent,
  * the K-split count (CTAs of one thread-block cluster that share a tile and
