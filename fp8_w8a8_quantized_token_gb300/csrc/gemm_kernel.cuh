@@ -31,6 +31,13 @@
 //   SWAP = false (prefill M):      A = 128 tokens, B = BN weight rows;
 //                 TMEM lane = token m, TMEM column = output column n.
 //
+// Paired tiles (non-swapped, split 1).  Two CTAs of a 2-CTA cluster take
+// the token tiles 2t and 2t+1 against the same BN weight rows; each loads
+// half of the weight slice and multicasts it into both CTAs' rings, so
+// every weight byte leaves L2 once per pair.  A ring slot is refilled only
+// after both CTAs' MMAs have consumed it (each MMA commit arrives on both
+// CTAs' empty barriers).
+//
 // Split-K.  split > 1 launches thread-block clusters of `split` CTAs that
 // share one output tile and take consecutive ranges of K blocks; each CTA
 // writes its fp32 partial tile to its own shared memory, and after a
@@ -53,7 +60,9 @@ struct GemmArgs {
     int m_tiles, n_tiles;  // tile counts along tokens and output columns
     int num_tiles;
     int split;             // CTAs per cluster along K
-    int group;             // tile rasterisation group (A-operand tiles)
+    int group;             // tile rasterisation group
+    int raster_b;          // 1: groups of B-operand tiles sweep the A tiles (else the reverse)
+    int pair;              // 1: paired tiles (non-swapped, split 1): num_tiles counts tile pairs
     const float *a_scale;
     const float *w_scale;
     const __nv_bfloat16 *bias;
@@ -162,6 +171,15 @@ __device__ __forceinline__ void tile_coords(int tile, int a_tiles, int b_tiles, 
     b_t = idx / gsize;
 }
 
+// The kernel's tile order: groups of `group` A tiles (or B tiles when
+// raster_b) sweep all tiles of the other operand.
+__device__ __forceinline__ void tile_order(int tile, int a_tiles, int b_tiles, int group, int raster_b, int &a_t,
+                                           int &b_t)
+{
+    if (raster_b) tile_coords(tile, b_tiles, a_tiles, group, b_t, a_t);
+    else tile_coords(tile, a_tiles, b_tiles, group, a_t, b_t);
+}
+
 template <typename OutT>
 __device__ __forceinline__ void store_out(OutT *out, long long idx, float v)
 {
@@ -196,19 +214,32 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = p.split;
-    const int rank = split > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-    const int cluster_id = blockIdx.x / split;
-    const int num_clusters = gridDim.x / split;
-    const int kb_begin = static_cast<int>(static_cast<long long>(p.num_kb) * rank / split);
-    const int kb_end = static_cast<int>(static_cast<long long>(p.num_kb) * (rank + 1) / split);
+    const bool pair = !SWAP && p.pair != 0;   // then split == 1
+    const int csize = pair ? 2 : split;       // CTAs per cluster
+    const int rank = csize > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int krank = pair ? 0 : rank;        // position along K
+    const int cluster_id = blockIdx.x / csize;
+    const int num_clusters = gridDim.x / csize;
+    const int kb_begin = static_cast<int>(static_cast<long long>(p.num_kb) * krank / split);
+    const int kb_end = static_cast<int>(static_cast<long long>(p.num_kb) * (krank + 1) / split);
     const int nkb = kb_end - kb_begin;
-    const int a_tiles = SWAP ? p.n_tiles : p.m_tiles;
+    // Paired: the A-tile index walks token-tile pairs; this CTA's token tile
+    // is 2 * pair_index + rank.
+    const int a_tiles = SWAP ? p.n_tiles : (pair ? (p.m_tiles + 1) / 2 : p.m_tiles);
     const int b_tiles = SWAP ? p.m_tiles : p.n_tiles;
+    auto coords = [&](int tile, int &a_t, int &b_t) {
+        tile_order(tile, a_tiles, b_tiles, p.group, p.raster_b, a_t, b_t);
+        if (pair) a_t = 2 * a_t + rank;
+    };
+    // Paired: this CTA's half of the weight slice (rows and ring offset).
+    constexpr int kHalfRows = BN / 2;
+    const int w_half_row = pair ? rank * kHalfRows : 0;
+    const uint32_t w_half_off = pair ? static_cast<uint32_t>(rank) * kHalfRows * 128u : 0u;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], BLOCKWISE ? 1 + C::kEpiWarps : 1);
+            mbar_init(&empty[s], (BLOCKWISE ? C::kEpiWarps : 0) + (pair ? 2 : 1));
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
@@ -238,8 +269,10 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
         }
 #endif
     }
-    // Barriers must be initialised before the early weight loads below.
+    // Barriers must be initialised before the early weight loads below (in
+    // both CTAs of a pair: each multicasts into the other).
     __syncthreads();
+    if (pair) cluster_sync();
     // Push reduction: every CTA's receive barrier must be initialised and
     // armed before any CTA of the cluster may push into it.  Arrive now,
     // wait just before the dependency wait (the latency overlaps the rest of
@@ -258,7 +291,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
         // are prefetched into L2 (always safe: L2 is the coherence point).
         if (cluster_id < p.num_tiles) {
             int a_t, b_t;
-            tile_coords(cluster_id, a_tiles, b_tiles, p.group, a_t, b_t);
+            coords(cluster_id, a_t, b_t);
             const CUtensorMap *wmap = SWAP ? &tm_a : &tm_b;
             const int wrow = SWAP ? a_t * 128 : b_t * BN;
             uint8_t *wbuf = SWAP ? sA : sB;
@@ -267,10 +300,14 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
             npre = p.preload ? (nkb < STAGES ? nkb : STAGES) : 0;
             for (int i = 0; i < npre; ++i) {
                 mbar_arrive_expect_tx(&full[i], C::kStageTx);
-                tma_load_2d(wbuf + i * wbytes, wmap, &full[i], (kb_begin + i) * 128, wrow, pol_w);
+                if (pair)
+                    tma_load_2d_mc(wbuf + i * wbytes + w_half_off, wmap, &full[i], (kb_begin + i) * 128,
+                                   wrow + w_half_row, 3, pol_w);
+                else
+                    tma_load_2d(wbuf + i * wbytes, wmap, &full[i], (kb_begin + i) * 128, wrow, pol_w);
             }
             const int pf = nkb < p.prefetch_kb ? nkb : p.prefetch_kb;
-            for (int i = npre; i < pf; ++i) tma_prefetch_l2_2d(wmap, (kb_begin + i) * 128, wrow);
+            for (int i = npre; i < pf; ++i) tma_prefetch_l2_2d(wmap, (kb_begin + i) * 128, wrow + w_half_row);
         }
         FP8Q_TRACE_AT(p, kTrPreloaded);
     }
@@ -302,7 +339,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
             long long issued = 0;
             for (int tile = cluster_id; tile < p.num_tiles; tile += num_clusters) {
                 int a_t, b_t;
-                tile_coords(tile, a_tiles, b_tiles, p.group, a_t, b_t);
+                coords(tile, a_t, b_t);
                 const int m_tile = SWAP ? b_t : a_t;
                 const int a_row = a_t * 128;
                 const int b_row = b_t * BN;
@@ -320,7 +357,11 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
                         if (!mbar_wait(&empty[stage], phase ^ 1u, abort, p.status)) { ok = false; break; }
                         mbar_arrive_expect_tx(&full[stage], C::kStageTx);
                         tma_load_2d(sA + stage * C::kABytes, &tm_a, &full[stage], kb * 128, a_row, pol_a);
-                        tma_load_2d(sB + stage * C::kBBytes, &tm_b, &full[stage], kb * 128, b_row, pol_b);
+                        if (pair)
+                            tma_load_2d_mc(sB + stage * C::kBBytes + w_half_off, &tm_b, &full[stage], kb * 128,
+                                           b_row + w_half_row, 3, pol_b);
+                        else
+                            tma_load_2d(sB + stage * C::kBBytes, &tm_b, &full[stage], kb * 128, b_row, pol_b);
                     }
                     if (BLOCKWISE)
                         tma_load_2d(sSA + stage * C::kSASlotFloats, &tm_sa, &full[stage], m_tile * C::kTokTile, kb,
@@ -339,6 +380,11 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
             const long long first = issued > STAGES ? issued - STAGES : 0;
             for (long long j = first; j < issued; ++j)
                 mbar_wait_drain(&full[j % STAGES], static_cast<uint32_t>((j / STAGES) & 1), p.status);
+            // Paired: the partner's MMA commits arrive on this CTA's empty
+            // barriers; every one of them must have landed before exit.
+            if (pair)
+                for (long long j = first; j < issued; ++j)
+                    mbar_wait_drain(&empty[j % STAGES], static_cast<uint32_t>((j / STAGES) & 1), p.status);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------
@@ -369,7 +415,8 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
                         umma_e4m3(d, umma_desc_sw128(a_addr + k * 32), umma_desc_sw128(b_addr + k * 32), C::kIdesc,
                                   acc);
                     }
-                    umma_commit(&empty[stage]);
+                    if (pair) umma_commit_mc(&empty[stage], 3);
+                    else umma_commit(&empty[stage]);
                     if (BLOCKWISE) {
                         umma_commit(&tfull[slot]);
                         slot ^= 1u;
@@ -405,7 +452,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
 
         for (int tile = cluster_id; tile < p.num_tiles; tile += num_clusters) {
             int a_t, b_t;
-            tile_coords(tile, a_tiles, b_tiles, p.group, a_t, b_t);
+            coords(tile, a_t, b_t);
             const int m0 = (SWAP ? b_t : a_t) * C::kTokTile;
             const int n0 = (SWAP ? a_t : b_t) * C::kColTile;
             // Row-wise (per thread) values.
@@ -623,7 +670,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
             const int r_lo = 4 * (32 * rank / split), r_hi = 4 * (32 * (rank + 1) / split);
             const int quads = (r_hi - r_lo) >> 2;
             int a_t, b_t;
-            tile_coords(cluster_id, a_tiles, b_tiles, p.group, a_t, b_t);
+            coords(cluster_id, a_t, b_t);
             const int m0 = (SWAP ? b_t : a_t) * C::kTokTile;
             const int n0 = (SWAP ? a_t : b_t) * C::kColTile;
             OutT *out = static_cast<OutT *>(p.out);
@@ -658,6 +705,9 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
 
     tc_fence_before();
     __syncthreads();
+    // Paired: neither CTA may exit while the other can still multicast into
+    // its shared memory or arrive on its barriers.
+    if (pair) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::kTmemCols);

@@ -33,7 +33,9 @@ cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigne
     // Operand maps: e4m3 rows of K bytes, boxes of 128 (K) x rows.
     CUtensorMap tm_w, tm_x, tm_sa;
     const int tok_box = C::kTokTile;
-    const int wrow_box = SWAP ? 128 : BN;
+    const bool pair = !SWAP && l.pair;
+    // Paired tiles: each CTA loads half of the weight rows of the tile.
+    const int wrow_box = SWAP ? 128 : (pair ? BN / 2 : BN);
     if (!make_tmap_2d(&tm_w, pr.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(pr.K),
                       static_cast<uint64_t>(pr.N), static_cast<uint64_t>(pr.ldw), 128, wrow_box, true))
         return cudaErrorInvalidValue;
@@ -58,8 +60,13 @@ cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigne
     a.num_kb = static_cast<int>((pr.K + 127) / 128);
     a.m_tiles = static_cast<int>((pr.M + C::kTokTile - 1) / C::kTokTile);
     a.n_tiles = static_cast<int>((pr.N + C::kColTile - 1) / C::kColTile);
-    a.num_tiles = a.m_tiles * a.n_tiles;
-    a.split = l.split;
+    a.pair = pair ? 1 : 0;
+    a.num_tiles = (pair ? (a.m_tiles + 1) / 2 : a.m_tiles) * a.n_tiles;
+    a.split = pair ? 1 : l.split;
+    // Non-swapped tiles with more weight tiles than token tiles group the
+    // weight tiles (each weight tile is then fetched by few concurrent CTAs
+    // while the smaller activation matrix stays in L2).
+    a.raster_b = (!SWAP && pr.N > pr.M) ? 1 : 0;
     a.group = SWAP ? a.n_tiles : 8;
     if (a.group < 1) a.group = 1;
     a.a_scale = pr.a_scale;
@@ -82,9 +89,10 @@ cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigne
     attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attrs[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
-    if (l.split > 1) {
+    const int csize = pair ? 2 : l.split;
+    if (csize > 1) {
         attrs[na].id = cudaLaunchAttributeClusterDimension;
-        attrs[na].val.clusterDim.x = static_cast<unsigned>(l.split);
+        attrs[na].val.clusterDim.x = static_cast<unsigned>(csize);
         attrs[na].val.clusterDim.y = 1;
         attrs[na].val.clusterDim.z = 1;
         ++na;

@@ -24,6 +24,7 @@ struct GemmLaunch {
     int split;         // K-split count = cluster size
     int grid;          // CTAs
     int stages;        // pipeline depth the instantiation uses
+    bool pair;         // non-swapped, split 1: 2-CTA clusters share each weight slice
 };
 
 struct GemmProblem {

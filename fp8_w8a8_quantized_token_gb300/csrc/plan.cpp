@@ -128,7 +128,17 @@ void plan_finish(int64_t M, int64_t N, int64_t K, int num_sms, fp8q_plan *pl)
     if (split > num_kb) split = num_kb;
     if (split < 1) split = 1;
     pl->split_k = static_cast<int32_t>(split);
-    if (split > 1) {
+    // Pairs of CTAs on adjacent token tiles share each weight slice
+    // (multicast) whenever there are two token tiles to pair.
+    static const bool no_pair = getenv("FP8Q_NO_PAIR") != nullptr && getenv("FP8Q_NO_PAIR")[0] == '1';
+    const int64_t m_tiles = (M + pl->tile_m - 1) / pl->tile_m;
+    pl->pair = (!pl->swap_ab && split == 1 && m_tiles >= 2 && !no_pair) ? 1 : 0;
+    if (pl->pair) {
+        const int64_t pairs = ((m_tiles + 1) / 2) * ((N + pl->tile_n - 1) / pl->tile_n);
+        const int64_t max_pairs = num_sms / 2 > 0 ? num_sms / 2 : 1;
+        pl->grid = static_cast<int32_t>(2 * (pairs < max_pairs ? pairs : max_pairs));
+        pl->persistent = pairs > max_pairs ? 1 : 0;
+    } else if (split > 1) {
         pl->grid = static_cast<int32_t>(tiles * split);
         pl->persistent = 0;
     } else {
@@ -165,9 +175,9 @@ extern "C" fp8q_status fp8q_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t b
         static std::set<std::tuple<int64_t, int64_t, int64_t, int>> seen;
         std::lock_guard<std::mutex> g(mu);
         if (seen.insert(std::make_tuple(M, N, K, blockwise)).second)
-            fprintf(stderr, "fp8q plan M=%lld N=%lld K=%lld %s: swap_ab=%d mma_n=%d split_k=%d grid=%d%s\n",
+            fprintf(stderr, "fp8q plan M=%lld N=%lld K=%lld %s: swap_ab=%d mma_n=%d split_k=%d pair=%d grid=%d%s\n",
                     static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K),
-                    blockwise ? "blockwise" : "channelwise", pl.swap_ab, pl.mma_n, pl.split_k, pl.grid,
+                    blockwise ? "blockwise" : "channelwise", pl.swap_ab, pl.mma_n, pl.split_k, pl.pair, pl.grid,
                     pl.from_table ? " (table)" : "");
     }
     *plan = pl;

@@ -258,6 +258,9 @@ typedef struct {
     int32_t grid;       /* CTAs launched */
     int32_t persistent; /* 1: CTAs loop over several tiles */
     int32_t from_table; /* 1: taken from the compiled-in table */
+    int32_t pair;       /* 1: CTA pairs (2-CTA clusters) on adjacent token tiles
+                           share each weight slice by multicast (non-swapped,
+                           split_k 1, at least two token tiles) */
 } fp8q_plan;
 
 FP8Q_API fp8q_status fp8q_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t blockwise, int32_t num_sms,

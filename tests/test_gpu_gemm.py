@@ -70,6 +70,32 @@ def test_channelwise_default_plan(dev, M):
     assert_gemm_close(out_values(out), ref, f"M={M}")
 
 
+@pytest.mark.parametrize("M,N,K", [
+    (2048, 2560, 512),    # 80 tile pairs: more than one pair per two SMs (persistent pairs)
+    (1000, 768, 1040),    # 8 token tiles, ragged M and K
+    (300, 512, 256),      # 3 token tiles: the last pair's second tile is empty
+])
+def test_channelwise_paired_tiles(dev, schedule, M, N, K):
+    """Non-swapped 128 x 256 tiles in 2-CTA clusters that share each weight
+    slice by multicast, compared on sampled outputs."""
+    fq.fp8q_set_plan_override(0, 256, 1)
+    assert fq.fp8q_gemm_plan(M, N, K)["pair"] == 1
+    x = synthetic.activations(M, K, seed=M + 1, outliers=True)
+    w = synthetic.weights(N, K, seed=M + 1)
+    b = synthetic.bias(N, seed=M + 1)
+    xq, xs, rq, rs = quant_both_per_token(x, dev)
+    wq, ws, rwq, rws = quant_both_per_token(w, dev)
+    out = fq.fp8q_scaled_mm_channelwise(xq, wq, xs, ws, bias=b.to(dev))
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(M)
+    ms, ns = rng.integers(0, M, 20000), rng.integers(0, N, 20000)
+    ms[:N] = M - 1                     # the whole last row (the last pair's ragged tile)
+    ns[:N] = np.arange(N)
+    ref = ref_values(oracle.gemm_channelwise_at(rq, rwq, rs, rws, ms, ns, bias=b))
+    assert_gemm_close(out_values(out)[ms, ns], ref, f"paired {M}x{N}x{K}")
+    assert fq.fp8q_device_status() == fq.FP8Q_OK
+
+
 def test_channelwise_fp16_output(dev):
     out, ref = channelwise_case(dev, 40, 256, 512, bias=True, out_dtype=torch.float16)
     assert out.dtype == torch.float16
@@ -118,6 +144,18 @@ def test_blockwise_every_schedule(dev, schedule, swap, mma_n, split):
     for M in (3, 70, 260):
         out, ctx = blockwise_case(dev, M, 384, 1024, seed=M, bias=True)
         assert_gemm_close(out_values(out), blockwise_ref(ctx, M), f"sched {swap},{mma_n},{split} M={M}")
+
+
+def test_blockwise_paired_tiles(dev, schedule):
+    fq.fp8q_set_plan_override(0, 256, 1)
+    M, N, K = 1100, 768, 1024
+    assert fq.fp8q_gemm_plan(M, N, K, blockwise=True)["pair"] == 1
+    out, ctx = blockwise_case(dev, M, N, K, seed=21, bias=True)
+    _, _, b, rq, rs, rwq, rws = ctx
+    rng = np.random.default_rng(21)
+    ms, ns = rng.integers(0, M, 20000), rng.integers(0, N, 20000)
+    ref = ref_values(oracle.gemm_blockwise_at(rq, rwq, rs, rws, ms, ns, bias=b))
+    assert_gemm_close(out_values(out)[ms, ns], ref, "blockwise paired")
 
 
 @pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 13, 16, 31, 64, 256])

@@ -59,6 +59,57 @@ def test_per_token_special_rows(dev):
     quant_both_per_token(x.to(torch.bfloat16), dev)
 
 
+def _tie_rows(K):
+    """Rows whose quotients x / s land exactly on midpoints between
+    neighbouring E4M3 values (ties, resolved to the even code), or one bf16
+    step beside them.  Each row's first element fixes amax = 448 * s, so
+    s is exact; s has at most 3 significant bits and a midpoint 5, so every
+    s * midpoint is a bf16 value,
+    but 1 / s is not a power of two, so x * (1 / s) can miss the tie by an
+    ulp -- where only the division gives the right code."""
+    codes = np.arange(0x08, 0x7E, dtype=np.uint8)             # positive normal E4M3 values
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    mids = (vals[:-1] + vals[1:]) / 2
+    rows = []
+    for s in (1.5, 1.25, 1.75, 0.375, 3.0 * 2.0 ** -7, 1.25 * 2.0 ** 5, 1.75 * 2.0 ** -9):
+        x = np.concatenate([[448.0 * s], s * mids, -s * mids])
+        row = torch.zeros(K, dtype=torch.float64)
+        row[:x.size] = torch.from_numpy(x)
+        exact = row.to(torch.bfloat16)
+        assert torch.equal(exact.double(), row), "a tie value is not a bf16 value"
+        rows.append(exact)
+        bump = exact.view(torch.int16).clone()
+        bump[1:x.size] += 1                                     # one bf16 step off each tie
+        rows.append(bump.view(torch.bfloat16))
+    return torch.stack(rows)
+
+
+def test_quotients_on_e4m3_rounding_midpoints(dev):
+    x = _tie_rows(256)
+    quant_both_per_token(x, dev)
+    quant_both_group(x, dev, 128)
+
+
+def test_every_bf16_significand_under_many_scales(dev):
+    """Rows with scales over a wide exponent range; every row holds values
+    of all 128 bf16 significands, both signs, at many exponents below its
+    amax (and signed zeros), so each quotient pattern meets many scales."""
+    rng = np.random.default_rng(77)
+    M, K = 1024, 2048
+    amax_exp = rng.integers(-30, 30, M)
+    amax = (1.0 + rng.integers(0, 128, M) / 128.0) * 2.0 ** amax_exp
+    sig = np.tile(np.arange(128), K // 128)[None, :] + np.zeros((M, 1), dtype=np.int64)
+    exp = amax_exp[:, None] - rng.integers(1, 24, (M, K))
+    vals = (1.0 + sig / 128.0) * 2.0 ** exp
+    vals *= np.where(rng.random((M, K)) < 0.5, -1.0, 1.0)
+    vals[:, 0] = amax
+    vals[:, 1] = -0.0
+    x = torch.from_numpy(vals).to(torch.bfloat16)
+    assert torch.equal(x.double().abs().amax(dim=1), torch.from_numpy(amax))
+    quant_both_per_token(x, dev)
+    quant_both_group(x, dev, 128)
+
+
 def test_per_token_m0_is_noop(dev):
     x = torch.empty((0, 64), dtype=torch.bfloat16, device=dev)
     xq, xs = fq.fp8q_quant_per_token(x)

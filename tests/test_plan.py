@@ -43,7 +43,15 @@ def test_plans_are_launchable(num_sms):
         tiles = -(-M // p["tile_m"]) * -(-N // p["tile_n"])
         num_kb = -(-K // 128)
         assert 1 <= p["split_k"] <= min(8, num_kb)
-        if p["split_k"] > 1:
+        m_tiles = -(-M // p["tile_m"])
+        assert p["pair"] == int(not p["swap_ab"] and p["split_k"] == 1 and m_tiles >= 2)
+        if p["pair"]:
+            # 2-CTA clusters over pairs of token tiles (an odd last tile pairs
+            # with an empty one), at most one pair per two SMs
+            pairs = -(-m_tiles // 2) * -(-N // p["tile_n"])
+            assert p["grid"] == 2 * min(pairs, num_sms // 2)
+            assert p["persistent"] == int(pairs > num_sms // 2)
+        elif p["split_k"] > 1:
             assert p["grid"] == tiles * p["split_k"] and not p["persistent"]
         else:
             assert p["grid"] == min(tiles, num_sms)
