@@ -51,6 +51,7 @@ fp8q_status run_gemm(GemmProblem p, cudaStream_t st)
     l.grid = pl.grid;
     l.stages = pl.stages;
     l.pair = pl.pair != 0;
+    l.two_sm = pl.two_sm != 0;
     const cudaError_t e = p.blockwise ? launch_gemm_blockwise(p, l, status, st)
                                       : launch_gemm_channelwise(p, l, status, st);
     if (e == cudaSuccess) note_launch_writes(st, p.out, static_cast<size_t>(p.M) * p.N * 2);

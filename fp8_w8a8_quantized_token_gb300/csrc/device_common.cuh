@@ -146,6 +146,20 @@ __device__ __forceinline__ void tma_load_2d_mc(void *dst, const CUtensorMap *map
         : "memory");
 }
 
+// Load issued by either CTA of a CTA pair feeding a 2-CTA MMA: the tile
+// lands in the issuing CTA's shared memory, its complete_tx goes to the
+// mbarrier at `bar_cluster` (a shared::cluster address, here always the
+// barrier of the pair's even CTA, which issues the MMA).
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, uint32_t bar_cluster,
+                                                 int32_t c0, int32_t c1, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "l"(policy)
+        : "memory");
+}
+
 // Prefetch one tile of a tensor map into L2 (no shared-memory destination,
 // no completion tracking).  L2 is the point of coherence for device memory,
 // so a prefetch can never make a later load observe stale data.
@@ -177,6 +191,25 @@ __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols)
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
                  "r"(ncols)
                  : "memory");
+}
+
+// The same for a CTA pair (.cta_group::2): one warp of EACH CTA of the pair
+// executes it; both CTAs receive the same column address.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
 __device__ __forceinline__ void tmem_relinquish()
@@ -229,6 +262,47 @@ __device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint
         "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// 2-CTA MMA (.cta_group::2, M = 256): issued by one thread of the pair's
+// even CTA.  A: 128 rows in each CTA's shared memory at the descriptor's
+// address (even CTA rows 0-127, odd CTA rows 128-255); B: N/2 rows in each
+// CTA (even CTA columns 0 .. N/2-1); D: rows 0-127 in the even CTA's TMEM,
+// rows 128-255 in the odd CTA's, at the same column address.
+__device__ __forceinline__ void umma_e4m3_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Commits for 2-CTA MMAs: arrive once on `bar` (in this CTA), or on the
+// mbarrier at `bar`'s offset in every CTA of `cta_mask`, when every
+// tcgen05.mma.cta_group::2 issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit_pair(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_pair_mc(uint64_t *bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster (shared::cluster
+// address from dsmem_map), releasing this thread's prior accesses.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread

@@ -38,6 +38,15 @@
 // after both CTAs' MMAs have consumed it (each MMA commit arrives on both
 // CTAs' empty barriers).
 //
+// 2-CTA MMA (TWO_SM, non-swapped channelwise).  The same CTA pairs compute
+// a 256-token x BN tile with tcgen05.mma.cta_group::2 (M = 256) issued by
+// the even CTA: each CTA stages only its own 128 tokens and its half of the
+// BN weight rows (no duplicate copy of the weights in either CTA), all of a
+// slot's loads complete on the even CTA's full barrier, and the even CTA's
+// commits arrive on both CTAs' empty and accumulator barriers.  Each CTA's
+// TMEM holds its own 128 accumulator rows; both epilogues release the even
+// CTA's accumulator slot.
+//
 // Split-K.  split > 1 launches thread-block clusters of `split` CTAs that
 // share one output tile and take consecutive ranges of K blocks; each CTA
 // writes its fp32 partial tile to its own shared memory, and after a
@@ -93,7 +102,7 @@ enum TracePhase {
     } while (0)
 #endif
 
-template <bool SWAP, int BN, int STAGES, bool BLOCKWISE>
+template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, bool TWO_SM = false>
 struct GemmCfg {
     static constexpr int kEpiWarps = BN > 128 ? 8 : 4;
     static constexpr int kColGroups = kEpiWarps / 4;
@@ -103,12 +112,14 @@ struct GemmCfg {
     static constexpr int kTokTile = SWAP ? BN : 128;     // tokens per tile
     static constexpr int kColTile = SWAP ? 128 : BN;     // output columns per tile
     static constexpr uint32_t kABytes = 128u * 128u;
-    static constexpr uint32_t kBBytes = static_cast<uint32_t>(BN) * 128u;
+    // TWO_SM: each CTA of the pair holds BN/2 weight rows.
+    static constexpr uint32_t kBBytes = static_cast<uint32_t>(TWO_SM ? BN / 2 : BN) * 128u;
     static constexpr uint32_t kSABytes = BLOCKWISE ? static_cast<uint32_t>(kTokTile) * 4u : 0u;  // TMA box
     // Scale slots are 128-byte aligned (TMA destination alignment).
     static constexpr uint32_t kSASlot = BLOCKWISE ? (kSABytes + 127u) / 128u * 128u : 0u;
     static constexpr int kSASlotFloats = static_cast<int>(kSASlot / 4u);
-    static constexpr uint32_t kStageTx = kABytes + kBBytes + kSABytes;
+    // Bytes one ring slot's full barrier waits for (TWO_SM: both CTAs' loads).
+    static constexpr uint32_t kStageTx = TWO_SM ? 2u * (kABytes + kBBytes) : kABytes + kBBytes + kSABytes;
     static constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32u : static_cast<uint32_t>(2 * BN);
     static constexpr uint32_t kOffA = 0;
     static constexpr uint32_t kOffB = kOffA + STAGES * kABytes;
@@ -129,7 +140,8 @@ struct GemmCfg {
     static constexpr uint32_t kOffCol = (kOffMisc + 16 + 15) / 16 * 16;  // staged column scale, bias
     static constexpr uint32_t kSmemBytes = kOffCol + 2u * BN * 4u + 1024u;  // + alignment slack
     static constexpr uint32_t kRedBytes = 128u * BN * 4u;
-    static constexpr uint32_t kIdesc = idesc_e4m3_f32<128, BN>();
+    static constexpr uint32_t kIdesc = idesc_e4m3_f32<TWO_SM ? 256 : 128, BN>();
+    static_assert(!TWO_SM || (!SWAP && !BLOCKWISE && BN == 256), "2-CTA MMA: non-swapped channelwise 256");
     static_assert(kRedBytes <= kOffSA, "the split-K partial tile must fit in the stage ring");
     static_assert(!kPush || 128u * kPartStride * 4u <= kOffSA, "the staged partial tile must fit in the ring");
     static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
@@ -186,12 +198,12 @@ __device__ __forceinline__ void store_out(OutT *out, long long idx, float v)
     out[idx] = to_out<OutT>(v);
 }
 
-template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT>
-__global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads, 1)
+template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT, bool TWO_SM = false>
+__global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sa, const GemmArgs p)
 {
-    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE>;
+    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sA = smem + C::kOffA;
@@ -214,7 +226,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = p.split;
-    const bool pair = !SWAP && p.pair != 0;   // then split == 1
+    const bool pair = !SWAP && (TWO_SM || p.pair != 0);   // then split == 1
     const int csize = pair ? 2 : split;       // CTAs per cluster
     const int rank = csize > 1 ? static_cast<int>(cluster_ctarank()) : 0;
     const int krank = pair ? 0 : rank;        // position along K
@@ -231,19 +243,23 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
         tile_order(tile, a_tiles, b_tiles, p.group, p.raster_b, a_t, b_t);
         if (pair) a_t = 2 * a_t + rank;
     };
-    // Paired: this CTA's half of the weight slice (rows and ring offset).
+    // Paired: this CTA's half of the weight slice (rows and ring offset;
+    // TWO_SM rings hold only that half).
     constexpr int kHalfRows = BN / 2;
     const int w_half_row = pair ? rank * kHalfRows : 0;
-    const uint32_t w_half_off = pair ? static_cast<uint32_t>(rank) * kHalfRows * 128u : 0u;
+    const uint32_t w_half_off = (pair && !TWO_SM) ? static_cast<uint32_t>(rank) * kHalfRows * 128u : 0u;
+    const bool leader = rank == 0;  // TWO_SM: the CTA that issues the MMAs
+    // TWO_SM: a ring slot's full barrier in the even CTA (shared::cluster).
+    auto lead_full = [&](int stage) { return dsmem_map(smem_u32(&full[stage]), 0u); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], (BLOCKWISE ? C::kEpiWarps : 0) + (pair ? 2 : 1));
+            mbar_init(&empty[s], (BLOCKWISE ? C::kEpiWarps : 0) + ((pair && !TWO_SM) ? 2 : 1));
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], C::kEpiWarps);
+            mbar_init(&tempty[i], TWO_SM ? 2 * C::kEpiWarps : C::kEpiWarps);
         }
         mbar_init(drain, 1);
         mbar_init(recv_full, 1);
@@ -299,6 +315,12 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
             const uint64_t pol_w = SWAP ? policy_evict_first() : policy_evict_normal();
             npre = p.preload ? (nkb < STAGES ? nkb : STAGES) : 0;
             for (int i = 0; i < npre; ++i) {
+                if (TWO_SM) {
+                    if (leader) mbar_arrive_expect_tx(&full[i], C::kStageTx);
+                    tma_load_2d_pair(wbuf + i * wbytes, wmap, lead_full(i), (kb_begin + i) * 128, wrow + w_half_row,
+                                     pol_w);
+                    continue;
+                }
                 mbar_arrive_expect_tx(&full[i], C::kStageTx);
                 if (pair)
                     tma_load_2d_mc(wbuf + i * wbytes + w_half_off, wmap, &full[i], (kb_begin + i) * 128,
@@ -312,8 +334,13 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
         FP8Q_TRACE_AT(p, kTrPreloaded);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_holder, C::kTmemCols);
-        tmem_relinquish();
+        if (TWO_SM) {
+            tmem_alloc_pair(tmem_holder, C::kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_holder, C::kTmemCols);
+            tmem_relinquish();
+        }
         if (lane == 0) FP8Q_TRACE_AT(p, kTrTmemAlloc);
     }
     tc_fence_before();
@@ -347,7 +374,15 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
                 for (int i = 0; i < nkb; ++i) {
                     const int kb = kb_begin + i;
                     if (issued == 0) FP8Q_TRACE_AT(p, kTrFirstTma);
-                    if (issued < npre) {
+                    if (TWO_SM) {
+                        if (issued >= npre) {
+                            if (!mbar_wait(&empty[stage], phase ^ 1u, abort, p.status)) { ok = false; break; }
+                            if (leader) mbar_arrive_expect_tx(&full[stage], C::kStageTx);
+                            tma_load_2d_pair(sB + stage * C::kBBytes, &tm_b, lead_full(stage), kb * 128,
+                                             b_row + w_half_row, pol_b);
+                        }
+                        tma_load_2d_pair(sA + stage * C::kABytes, &tm_a, lead_full(stage), kb * 128, a_row, pol_a);
+                    } else if (issued < npre) {
                         // Weight slice already in flight; barrier armed.
                         if (SWAP)
                             tma_load_2d(sB + stage * C::kBBytes, &tm_b, &full[stage], kb * 128, b_row, pol_b);
@@ -378,8 +413,10 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
             // phase cannot complete, so the wait only ends on the timeout.
             if (issued < npre) issued = npre;
             const long long first = issued > STAGES ? issued - STAGES : 0;
-            for (long long j = first; j < issued; ++j)
-                mbar_wait_drain(&full[j % STAGES], static_cast<uint32_t>((j / STAGES) & 1), p.status);
+            // (TWO_SM: only the even CTA's full barriers are used.)
+            if (!TWO_SM || leader)
+                for (long long j = first; j < issued; ++j)
+                    mbar_wait_drain(&full[j % STAGES], static_cast<uint32_t>((j / STAGES) & 1), p.status);
             // Paired: the partner's MMA commits arrive on this CTA's empty
             // barriers; every one of them must have landed before exit.
             if (pair)
@@ -390,7 +427,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
         // ------------------------------------------------------------------
         // MMA issuer (one thread)
         // ------------------------------------------------------------------
-        if (lane == 0) {
+        if (lane == 0 && (!TWO_SM || leader)) {
             uint32_t stage = 0, phase = 0, slot = 0, tphase = 0;
             bool ok = true;
             for (int tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
@@ -412,10 +449,15 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const uint32_t acc = BLOCKWISE ? (k > 0) : (i > 0 || k > 0);
-                        umma_e4m3(d, umma_desc_sw128(a_addr + k * 32), umma_desc_sw128(b_addr + k * 32), C::kIdesc,
-                                  acc);
+                        if (TWO_SM)
+                            umma_e4m3_pair(d, umma_desc_sw128(a_addr + k * 32), umma_desc_sw128(b_addr + k * 32),
+                                           C::kIdesc, acc);
+                        else
+                            umma_e4m3(d, umma_desc_sw128(a_addr + k * 32), umma_desc_sw128(b_addr + k * 32),
+                                      C::kIdesc, acc);
                     }
-                    if (pair) umma_commit_mc(&empty[stage], 3);
+                    if (TWO_SM) umma_commit_pair_mc(&empty[stage], 3);
+                    else if (pair) umma_commit_mc(&empty[stage], 3);
                     else umma_commit(&empty[stage]);
                     if (BLOCKWISE) {
                         umma_commit(&tfull[slot]);
@@ -426,15 +468,25 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
                 }
                 if (!ok) break;
                 if (!BLOCKWISE) {
-                    umma_commit(&tfull[slot]);
+                    if (TWO_SM) umma_commit_pair_mc(&tfull[slot], 3);
+                    else umma_commit(&tfull[slot]);
                     slot ^= 1u;
                     if (slot == 0) tphase ^= 1u;
                 }
             }
             FP8Q_TRACE_AT(p, kTrLastCommit);
             // Every MMA this thread issued has finished before TMEM is freed.
-            umma_commit(drain);
+            if (TWO_SM) umma_commit_pair(drain);
+            else umma_commit(drain);
             mbar_wait_drain(drain, 0, p.status);
+            // TWO_SM: the other CTA's epilogue releases arrive on this CTA's
+            // accumulator barriers; all of them must have landed before exit.
+            if (TWO_SM)
+                for (int i = 0; i < 2; ++i) {
+                    mbar_wait_drain(&tempty[slot], tphase ^ 1u, p.status);
+                    slot ^= 1u;
+                    if (slot == 0) tphase ^= 1u;
+                }
         }
         __syncwarp();
     } else {
@@ -535,7 +587,10 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
                     }
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&tempty[slot]);
+                    if (lane == 0) {
+                        if (TWO_SM && !leader) mbar_arrive_cluster(dsmem_map(smem_u32(&tempty[slot]), 0u));
+                        else mbar_arrive(&tempty[slot]);
+                    }
                     slot ^= 1u;
                     if (slot == 0) tphase ^= 1u;
                 }
@@ -710,7 +765,8 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE>::kThreads
     if (pair) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, C::kTmemCols);
+        if (TWO_SM) tmem_dealloc_pair(tmem_base, C::kTmemCols);
+        else tmem_dealloc(tmem_base, C::kTmemCols);
         if (lane == 0) FP8Q_TRACE_AT(p, kTrExit);
     }
 }

@@ -13,11 +13,11 @@ namespace fp8q {
 
 constexpr int kMaxDevices = 64;
 
-template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT>
+template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT, bool TWO_SM = false>
 cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigned *status, cudaStream_t st)
 {
-    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE>;
-    auto kernel = fp8_gemm_kernel<SWAP, BN, STAGES, BLOCKWISE, OutT>;
+    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>;
+    auto kernel = fp8_gemm_kernel<SWAP, BN, STAGES, BLOCKWISE, OutT, TWO_SM>;
 
     static std::atomic<uint64_t> attr_done[kMaxDevices / 64 + 1];
     int dev = 0;
@@ -33,7 +33,7 @@ cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigne
     // Operand maps: e4m3 rows of K bytes, boxes of 128 (K) x rows.
     CUtensorMap tm_w, tm_x, tm_sa;
     const int tok_box = C::kTokTile;
-    const bool pair = !SWAP && l.pair;
+    const bool pair = !SWAP && (TWO_SM || l.pair);
     // Paired tiles: each CTA loads half of the weight rows of the tile.
     const int wrow_box = SWAP ? 128 : (pair ? BN / 2 : BN);
     if (!make_tmap_2d(&tm_w, pr.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(pr.K),

@@ -25,6 +25,7 @@ struct GemmLaunch {
     int grid;          // CTAs
     int stages;        // pipeline depth the instantiation uses
     bool pair;         // non-swapped, split 1: 2-CTA clusters share each weight slice
+    bool two_sm;       // pair computing 256-token tiles with 2-CTA MMAs (channelwise)
 };
 
 struct GemmProblem {
@@ -57,6 +58,10 @@ constexpr int stages_for(bool swap_ab, int mma_n)
 {
     return swap_ab ? (mma_n == 16 ? 5 : mma_n == 32 ? 4 : mma_n == 64 ? 7 : 4) : 4;
 }
+
+// Ring depth of the 2-CTA MMA instantiation (each slot: 16 KB of tokens +
+// 16 KB, the CTA's half, of weight rows).
+constexpr int kTwoSmStages = 6;
 
 // True if an instantiation exists for (swap_ab, mma_n).
 constexpr bool gemm_shape_supported(bool swap_ab, int mma_n)

@@ -117,7 +117,7 @@ bool table_plan(int64_t M, int64_t N, int64_t K, int blockwise, fp8q_plan *pl)
 }  // namespace
 
 // Tile sizes, grid and persistence for a chosen (swap_ab, mma_n, split_k).
-void plan_finish(int64_t M, int64_t N, int64_t K, int num_sms, fp8q_plan *pl)
+void plan_finish(int64_t M, int64_t N, int64_t K, int blockwise, int num_sms, fp8q_plan *pl)
 {
     pl->tile_m = pl->swap_ab ? pl->mma_n : 128;
     pl->tile_n = pl->swap_ab ? 128 : pl->mma_n;
@@ -145,7 +145,11 @@ void plan_finish(int64_t M, int64_t N, int64_t K, int num_sms, fp8q_plan *pl)
         pl->grid = static_cast<int32_t>(tiles < num_sms ? tiles : num_sms);
         pl->persistent = tiles > num_sms ? 1 : 0;
     }
-    pl->stages = stages_for(pl->swap_ab != 0, pl->mma_n);
+    // Channelwise pairs use 2-CTA MMAs (FP8Q_NO_2SM=1 keeps the multicast
+    // pairs, for comparison).
+    static const bool no_2sm = getenv("FP8Q_NO_2SM") != nullptr && getenv("FP8Q_NO_2SM")[0] == '1';
+    pl->two_sm = (pl->pair && !blockwise && pl->mma_n == 256 && !no_2sm) ? 1 : 0;
+    pl->stages = pl->two_sm ? kTwoSmStages : stages_for(pl->swap_ab != 0, pl->mma_n);
 }
 
 }  // namespace fp8q
@@ -168,7 +172,7 @@ extern "C" fp8q_status fp8q_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t b
         generic_rule(M, N, K, num_sms, &pl);
         pl.from_table = 0;
     }
-    plan_finish(M, N, K, num_sms, &pl);
+    plan_finish(M, N, K, blockwise ? 1 : 0, num_sms, &pl);
     static const bool log = getenv("FP8Q_LOG") != nullptr && getenv("FP8Q_LOG")[0] == '1';
     if (log) {
         static std::mutex mu;

@@ -23,6 +23,8 @@ WARMUP = 2
 CASES = {
     "prefill_oproj": ("channelwise", 8192, 4096, 4096),
     "prefill_gateup": ("channelwise", 8192, 24576, 4096),
+    "mid_oproj": ("channelwise", 1024, 4096, 4096),
+    "mid_oproj_512": ("channelwise", 512, 4096, 4096),
     "decode_oproj": ("channelwise", 16, 4096, 4096),
     "decode_down": ("channelwise", 1, 4096, 12288),
     "blockwise_prefill": ("blockwise", 8192, 24576, 3072),

@@ -261,6 +261,10 @@ typedef struct {
     int32_t pair;       /* 1: CTA pairs (2-CTA clusters) on adjacent token tiles
                            share each weight slice by multicast (non-swapped,
                            split_k 1, at least two token tiles) */
+    int32_t two_sm;     /* 1: each CTA pair computes a 256-token x 256-column
+                           tile with 2-CTA MMAs (tcgen05 cta_group::2), each
+                           CTA staging only its half of the weights
+                           (channelwise pairs) */
 } fp8q_plan;
 
 FP8Q_API fp8q_status fp8q_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t blockwise, int32_t num_sms,

@@ -76,10 +76,12 @@ def test_channelwise_default_plan(dev, M):
     (300, 512, 256),      # 3 token tiles: the last pair's second tile is empty
 ])
 def test_channelwise_paired_tiles(dev, schedule, M, N, K):
-    """Non-swapped 128 x 256 tiles in 2-CTA clusters that share each weight
-    slice by multicast, compared on sampled outputs."""
+    """Non-swapped tiles computed by CTA pairs with 2-CTA MMAs (256 tokens x
+    256 columns per pair, each CTA staging half of the weight slice),
+    compared on sampled outputs."""
     fq.fp8q_set_plan_override(0, 256, 1)
-    assert fq.fp8q_gemm_plan(M, N, K)["pair"] == 1
+    plan = fq.fp8q_gemm_plan(M, N, K)
+    assert plan["pair"] == 1 and plan["two_sm"] == 1
     x = synthetic.activations(M, K, seed=M + 1, outliers=True)
     w = synthetic.weights(N, K, seed=M + 1)
     b = synthetic.bias(N, seed=M + 1)
@@ -147,9 +149,11 @@ def test_blockwise_every_schedule(dev, schedule, swap, mma_n, split):
 
 
 def test_blockwise_paired_tiles(dev, schedule):
+    """Blockwise pairs share each weight slice by TMA multicast."""
     fq.fp8q_set_plan_override(0, 256, 1)
     M, N, K = 1100, 768, 1024
-    assert fq.fp8q_gemm_plan(M, N, K, blockwise=True)["pair"] == 1
+    plan = fq.fp8q_gemm_plan(M, N, K, blockwise=True)
+    assert plan["pair"] == 1 and plan["two_sm"] == 0
     out, ctx = blockwise_case(dev, M, N, K, seed=21, bias=True)
     _, _, b, rq, rs, rwq, rws = ctx
     rng = np.random.default_rng(21)

@@ -56,7 +56,11 @@ def test_plans_are_launchable(num_sms):
         else:
             assert p["grid"] == min(tiles, num_sms)
             assert p["persistent"] == int(tiles > num_sms)
-        assert p["stages"] * stage_bytes(p["swap_ab"], p["mma_n"], bw) + 4096 <= SMEM_LIMIT
+        # channelwise pairs of 128 x 256 tiles use 2-CTA MMAs: each CTA stages
+        # 128 token rows and its 128 of the 256 weight rows per K slice
+        assert p["two_sm"] == int(p["pair"] and not bw and p["mma_n"] == 256)
+        per_stage = 2 * 128 * 128 if p["two_sm"] else stage_bytes(p["swap_ab"], p["mma_n"], bw)
+        assert p["stages"] * per_stage + 4096 <= SMEM_LIMIT
 
 
 def test_decode_sizes_put_weights_on_the_mma_m_side():
