@@ -160,6 +160,16 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *m
         : "memory");
 }
 
+// Store a box of a tensor map from shared memory (bulk async-group of the
+// issuing thread).  Parts of the box outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int32_t c0, int32_t c1)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(src)), "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 // Prefetch one tile of a tensor map into L2 (no shared-memory destination,
 // no completion tracking).  L2 is the point of coherence for device memory,
 // so a prefetch can never make a later load observe stale data.
@@ -404,6 +414,10 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 // Wait until the source side of every committed bulk copy of this thread
 // has been read (its shared memory may then be reused or released).
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Wait until every committed bulk copy of this thread has completed
+// (writes performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Make this thread's generic-proxy shared-memory writes visible to later
 // async-proxy (bulk copy / TMA) reads.

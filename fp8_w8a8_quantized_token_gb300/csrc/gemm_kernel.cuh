@@ -138,7 +138,13 @@ struct GemmCfg {
     static constexpr uint32_t kNumBars = 2 * STAGES + 6;  // full, empty, tfull[2], tempty[2], drain, recv
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr uint32_t kOffCol = (kOffMisc + 16 + 15) / 16 * 16;  // staged column scale, bias
-    static constexpr uint32_t kSmemBytes = kOffCol + 2u * BN * 4u + 1024u;  // + alignment slack
+    // Non-swapped tiles store their output through one 2 KB staging buffer
+    // per epilogue warp (32 rows x 32 columns of 2-byte values) and TMA.
+    static constexpr bool kTmaStore = !SWAP;
+    static constexpr uint32_t kStageBufBytes = 2048;
+    static constexpr uint32_t kOffStage = (kOffCol + 2u * BN * 4u + 1023u) / 1024u * 1024u;
+    static constexpr uint32_t kSmemBytes =
+        (kTmaStore ? kOffStage + kEpiWarps * kStageBufBytes : kOffCol + 2u * BN * 4u) + 1024u;  // + alignment slack
     static constexpr uint32_t kRedBytes = 128u * BN * 4u;
     static constexpr uint32_t kIdesc = idesc_e4m3_f32<TWO_SM ? 256 : 128, BN>();
     static_assert(!TWO_SM || (!SWAP && !BLOCKWISE && BN == 256), "2-CTA MMA: non-swapped channelwise 256");
@@ -201,7 +207,8 @@ __device__ __forceinline__ void store_out(OutT *out, long long idx, float v)
 template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT, bool TWO_SM = false>
 __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                    const __grid_constant__ CUtensorMap tm_sa, const GemmArgs p)
+                    const __grid_constant__ CUtensorMap tm_sa, const __grid_constant__ CUtensorMap tm_out,
+                    const GemmArgs p)
 {
     using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>;
     extern __shared__ uint8_t smem_raw[];
@@ -298,6 +305,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
         tma_prefetch_map(&tm_a);
         tma_prefetch_map(&tm_b);
         if (BLOCKWISE) tma_prefetch_map(&tm_sa);
+        if (C::kTmaStore) tma_prefetch_map(&tm_out);
         // Every kernel of the library triggers its dependents only after
         // its own dependency wait, so the only kernel that may still run
         // now is the immediate predecessor; the host clears p.preload when
@@ -615,6 +623,47 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
                             }
                         }
                     }
+                } else if (C::kTmaStore) {
+                    // Each warp converts 32 columns of its 32 rows at a time
+                    // into its staging buffer -- 64-byte rows, 64-byte TMA
+                    // swizzle: 16-byte unit u of row r sits at unit
+                    // u ^ ((r >> 1) & 3), so the eight rows a quarter-warp
+                    // writes hit distinct banks -- and one lane stores the
+                    // 32 x 32 box with TMA, which clips rows >= M and
+                    // columns >= N.
+                    uint8_t *sbuf = smem + C::kOffStage + static_cast<uint32_t>(ew) * C::kStageBufBytes;
+                    const int ybox = m0 + quarter * 32;
+#pragma unroll
+                    for (int ch = 0; ch < C::kCols / 32; ++ch) {
+                        const int cb = col0 + ch * 32;
+                        uint32_t w[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int c = cb + 2 * e;
+                            const float y0 = BLOCKWISE ? acc[ch * 32 + 2 * e] + sColBias[c]
+                                                       : fmaf(acc[ch * 32 + 2 * e] * row_scale, sColScale[c], sColBias[c]);
+                            const float y1 = BLOCKWISE ? acc[ch * 32 + 2 * e + 1] + sColBias[c + 1]
+                                                       : fmaf(acc[ch * 32 + 2 * e + 1] * row_scale, sColScale[c + 1],
+                                                              sColBias[c + 1]);
+                            const OutT lo = to_out<OutT>(y0), hi = to_out<OutT>(y1);
+                            w[e] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(&lo)) |
+                                   (static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(&hi)) << 16);
+                        }
+                        // The previous box stored from this buffer must have
+                        // been read out first.
+                        if (lane == 0) bulk_wait_read();
+                        __syncwarp();
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            *reinterpret_cast<uint4 *>(sbuf + lane * 64 + 16 * (u ^ ((lane >> 1) & 3))) =
+                                make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0 && ybox < p.M && n0 + cb < p.N) {
+                            tma_store_2d(&tm_out, sbuf, n0 + cb, ybox);
+                            bulk_commit();
+                        }
+                    }
                 } else if (rm < p.M) {
                     OutT *orow = out + static_cast<long long>(rm) * p.ldo;
 #pragma unroll
@@ -714,6 +763,8 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
             }
             if (warp == 2 && lane == 0) FP8Q_TRACE_AT(p, kTrEpiDone);
         }
+        // Output boxes stored with TMA are complete before the CTA exits.
+        if (C::kTmaStore && lane == 0) bulk_wait_all();
     }
 
     if (split > 1 && !C::kPush) {

@@ -37,17 +37,27 @@ cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigne
     // Paired tiles: each CTA loads half of the weight rows of the tile.
     const int wrow_box = SWAP ? 128 : (pair ? BN / 2 : BN);
     if (!make_tmap_2d(&tm_w, pr.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(pr.K),
-                      static_cast<uint64_t>(pr.N), static_cast<uint64_t>(pr.ldw), 128, wrow_box, true))
+                      static_cast<uint64_t>(pr.N), static_cast<uint64_t>(pr.ldw), 128, wrow_box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     if (!make_tmap_2d(&tm_x, pr.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(pr.K),
-                      static_cast<uint64_t>(pr.M), static_cast<uint64_t>(pr.K), 128, tok_box, true))
+                      static_cast<uint64_t>(pr.M), static_cast<uint64_t>(pr.K), 128, tok_box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    // Output (non-swapped tiles): 2-byte values [M, N], row stride N, boxes
+    // of 32 x 32 with the 64-byte swizzle of the epilogue's staging buffers.
+    CUtensorMap tm_out = tm_x;
+    if (C::kTmaStore &&
+        !make_tmap_2d(&tm_out, pr.out, CU_TENSOR_MAP_DATA_TYPE_UINT16, static_cast<uint64_t>(pr.N),
+                      static_cast<uint64_t>(pr.M), static_cast<uint64_t>(pr.N) * 2u, 32, 32,
+                      CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     if (BLOCKWISE) {
         // Column-major activation scales: K/128 columns of m_pad floats; only
         // the first M entries of each column are real (the rest read as 0).
         if (!make_tmap_2d(&tm_sa, pr.a_scale, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, static_cast<uint64_t>(pr.M),
                           static_cast<uint64_t>(pr.K / 128), static_cast<uint64_t>(pr.m_pad) * 4u, tok_box, 1,
-                          false))
+                          CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     } else {
         tm_sa = tm_x;  // unused
@@ -102,7 +112,7 @@ cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigne
     // A operand: the 128-row side of the MMA; B operand: the BN-row side.
     const CUtensorMap &tm_a = SWAP ? tm_w : tm_x;
     const CUtensorMap &tm_b = SWAP ? tm_x : tm_w;
-    return cudaLaunchKernelEx(&cfg, kernel, tm_a, tm_b, tm_sa, a);
+    return cudaLaunchKernelEx(&cfg, kernel, tm_a, tm_b, tm_sa, tm_out, a);
 }
 
 }  // namespace fp8q

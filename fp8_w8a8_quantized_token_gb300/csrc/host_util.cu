@@ -51,7 +51,7 @@ std::atomic<int> g_sms[kMaxDev];
 }  // namespace
 
 bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, uint64_t cols, uint64_t rows,
-                  uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows, bool swizzle128)
+                  uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle)
 {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return false;
@@ -60,8 +60,7 @@ bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

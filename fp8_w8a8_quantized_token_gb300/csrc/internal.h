@@ -71,10 +71,10 @@ constexpr bool gemm_shape_supported(bool swap_ab, int mma_n)
 
 // ---- tensor maps (host_util.cu) ------------------------------------------------
 // 2-D tensor map over a row-major matrix of `rows` x `cols` elements with a
-// row stride of `row_bytes`, box = box_cols x box_rows, optional 128-byte
-// swizzle.  Returns false if the driver rejects it.
+// row stride of `row_bytes`, box = box_cols x box_rows, the given shared-
+// memory swizzle.  Returns false if the driver rejects it.
 bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, uint64_t cols, uint64_t rows,
-                  uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows, bool swizzle128);
+                  uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle);
 
 // ---- device status word (host_util.cu) --------------------------------------
 unsigned *device_status_ptr();   // of the current device, or null
