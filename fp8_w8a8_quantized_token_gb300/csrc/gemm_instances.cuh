@@ -20,8 +20,8 @@ cudaError_t dispatch_gemm(const GemmProblem &p, const GemmLaunch &l, unsigned *s
         }
     }
     if (l.mma_n == 256) {
-        if (!BLOCKWISE && l.pair && l.two_sm)
-            return launch_gemm_inst<false, 256, kTwoSmStages, false, OutT, true>(p, l, status, st);
+        if constexpr (!BLOCKWISE)
+            if (l.pair && l.two_sm) return launch_gemm_inst<false, 256, kTwoSmStages, false, OutT, true>(p, l, status, st);
         return launch_gemm_inst<false, 256, stages_for(false, 256), BLOCKWISE, OutT>(p, l, status, st);
     }
     return cudaErrorInvalidValue;

@@ -145,11 +145,10 @@ struct GemmCfg {
     static constexpr uint32_t kOffStage = (kOffCol + 2u * BN * 4u + 1023u) / 1024u * 1024u;
     static constexpr uint32_t kSmemBytes =
         (kTmaStore ? kOffStage + kEpiWarps * kStageBufBytes : kOffCol + 2u * BN * 4u) + 1024u;  // + alignment slack
-    static constexpr uint32_t kRedBytes = 128u * BN * 4u;
+    static constexpr uint32_t kRedBytes = 128u * (BN + 4) * 4u;  // padded partial tile
     static constexpr uint32_t kIdesc = idesc_e4m3_f32<TWO_SM ? 256 : 128, BN>();
     static_assert(!TWO_SM || (!SWAP && !BLOCKWISE && BN == 256), "2-CTA MMA: non-swapped channelwise 256");
     static_assert(kRedBytes <= kOffSA, "the split-K partial tile must fit in the stage ring");
-    static_assert(!kPush || 128u * kPartStride * 4u <= kOffSA, "the staged partial tile must fit in the ring");
     static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
     static_assert(kCols % 32 == 0 || kCols == 16, "epilogue column chunking");
@@ -202,6 +201,39 @@ template <typename OutT>
 __device__ __forceinline__ void store_out(OutT *out, long long idx, float v)
 {
     out[idx] = to_out<OutT>(v);
+}
+
+// Two outputs converted and packed into one 32-bit word (lo first).
+template <typename OutT>
+__device__ __forceinline__ uint32_t pack_out2(float lo, float hi)
+{
+    const OutT a = to_out<OutT>(lo), b = to_out<OutT>(hi);
+    return static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(&a)) |
+           (static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(&b)) << 16);
+}
+
+// One warp stores a 32-row x 32-column box of 2-byte outputs (lane = row,
+// w = its 32 packed values) through its 2 KB staging buffer: 64-byte rows,
+// 64-byte TMA swizzle -- 16-byte unit u of row r sits at unit
+// u ^ ((r >> 1) & 3), so the eight rows a quarter-warp writes hit distinct
+// banks -- then lane 0 stores the box at (column x, row y) with TMA, which
+// clips rows and columns outside the tensor.  The previous box stored from
+// the buffer must have been read out before it is overwritten.
+__device__ __forceinline__ void store_box_tma(const CUtensorMap *tm_out, uint8_t *sbuf, int lane,
+                                              const uint32_t (&w)[16], int x, int y, bool any_inside)
+{
+    if (lane == 0) bulk_wait_read();
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+        *reinterpret_cast<uint4 *>(sbuf + lane * 64 + 16 * (u ^ ((lane >> 1) & 3))) =
+            make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && any_inside) {
+        tma_store_2d(tm_out, sbuf, x, y);
+        bulk_commit();
+    }
 }
 
 template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT, bool TWO_SM = false>
@@ -259,7 +291,22 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
     // TWO_SM: a ring slot's full barrier in the even CTA (shared::cluster).
     auto lead_full = [&](int stage) { return dsmem_map(smem_u32(&full[stage]), 0u); };
 
+    // Prologue.  Thread 0 initialises the barriers while warp 1 allocates the
+    // TMEM accumulators; one block barrier publishes both.
     if (threadIdx.x == 0) {
+        FP8Q_TRACE_AT(p, kTrEntry);
+#ifdef FP8Q_TRACE
+        if (p.trace != nullptr && blockIdx.x < 4096) {
+            unsigned smid;
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+            p.trace[blockIdx.x * kTraceSlots + kTrSmid] = smid;
+            p.trace[blockIdx.x * kTraceSlots + kTrRank] = static_cast<unsigned long long>(rank);
+        }
+#endif
+        tma_prefetch_map(&tm_a);
+        tma_prefetch_map(&tm_b);
+        if (BLOCKWISE) tma_prefetch_map(&tm_sa);
+        if (C::kTmaStore) tma_prefetch_map(&tm_out);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], (BLOCKWISE ? C::kEpiWarps : 0) + ((pair && !TWO_SM) ? 2 : 1));
@@ -279,33 +326,31 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
             mbar_arrive_expect_tx(recv_full, static_cast<uint32_t>((split - 1) * my_rows * C::kPartStride * 4));
         }
     }
-    // Weight slices of the first tile issued before the dependency wait.
-    int npre = 0;
-    if (threadIdx.x == 0) {
-        FP8Q_TRACE_AT(p, kTrEntry);
-#ifdef FP8Q_TRACE
-        if (p.trace != nullptr && blockIdx.x < 4096) {
-            unsigned smid;
-            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-            p.trace[blockIdx.x * kTraceSlots + kTrSmid] = smid;
-            p.trace[blockIdx.x * kTraceSlots + kTrRank] = static_cast<unsigned long long>(rank);
+    if (warp == 1) {
+        if (TWO_SM) {
+            tmem_alloc_pair(tmem_holder, C::kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_holder, C::kTmemCols);
+            tmem_relinquish();
         }
-#endif
+        if (lane == 0) FP8Q_TRACE_AT(p, kTrTmemAlloc);
     }
-    // Barriers must be initialised before the early weight loads below (in
-    // both CTAs of a pair: each multicasts into the other).
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    // Barriers must be initialised before the early weight loads below (in
+    // both CTAs of a pair: each loads into, or signals, the other).
     if (pair) cluster_sync();
     // Push reduction: every CTA's receive barrier must be initialised and
     // armed before any CTA of the cluster may push into it.  Arrive now,
     // wait just before the dependency wait (the latency overlaps the rest of
     // the prologue).
     if (C::kPush && split > 1) cluster_arrive_relaxed();
+    // Weight slices of the first tile issued before the dependency wait.
+    int npre = 0;
     if (warp == 0 && lane == 0) {
-        tma_prefetch_map(&tm_a);
-        tma_prefetch_map(&tm_b);
-        if (BLOCKWISE) tma_prefetch_map(&tm_sa);
-        if (C::kTmaStore) tma_prefetch_map(&tm_out);
         // Every kernel of the library triggers its dependents only after
         // its own dependency wait, so the only kernel that may still run
         // now is the immediate predecessor; the host clears p.preload when
@@ -341,20 +386,6 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
         }
         FP8Q_TRACE_AT(p, kTrPreloaded);
     }
-    if (warp == 1) {
-        if (TWO_SM) {
-            tmem_alloc_pair(tmem_holder, C::kTmemCols);
-            tmem_relinquish_pair();
-        } else {
-            tmem_alloc(tmem_holder, C::kTmemCols);
-            tmem_relinquish();
-        }
-        if (lane == 0) FP8Q_TRACE_AT(p, kTrTmemAlloc);
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_holder;
     if (C::kPush && split > 1) cluster_wait();
     if (threadIdx.x == 0) FP8Q_TRACE_AT(p, kTrPrologue);
     // Everything below may read the previous kernel's output (activations,
@@ -585,13 +616,39 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
                     tc_fence_after();
                     if (warp == 2 && lane == 0) FP8Q_TRACE_AT(p, kTrEpiFull);
                     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + slot * BN + col0;
+                    // TWO_SM tiles (never split along K) go straight from TMEM
+                    // to the output; the others keep the whole row in
+                    // registers for the stores or the split-K exchange below.
+                    if constexpr (TWO_SM) {
+                        // 32 accumulator columns at a time: TMEM -> scale,
+                        // bias, convert -> staging buffer -> TMA store.
+                        uint8_t *sbuf = smem + C::kOffStage + static_cast<uint32_t>(ew) * C::kStageBufBytes;
+                        const int ybox = m0 + quarter * 32;
+#pragma unroll 1
+                        for (int ch = 0; ch < C::kCols / 32; ++ch) {
+                            uint32_t r[32];
+                            tmem_ld16(taddr + ch * 32, *reinterpret_cast<uint32_t(*)[16]>(r));
+                            tmem_ld16(taddr + ch * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+                            tmem_ld_wait();
+                            const int cb = col0 + ch * 32;
+                            uint32_t w[16];
 #pragma unroll
-                    for (int c = 0; c < C::kCols; c += 16) {
-                        uint32_t r[16];
-                        tmem_ld16(taddr + c, r);
+                            for (int e = 0; e < 16; ++e)
+                                w[e] = pack_out2<OutT>(
+                                    fmaf(__uint_as_float(r[2 * e]) * row_scale, sColScale[cb + 2 * e], sColBias[cb + 2 * e]),
+                                    fmaf(__uint_as_float(r[2 * e + 1]) * row_scale, sColScale[cb + 2 * e + 1],
+                                         sColBias[cb + 2 * e + 1]));
+                            store_box_tma(&tm_out, sbuf, lane, w, n0 + cb, ybox, ybox < p.M && n0 + cb < p.N);
+                        }
+                    } else if constexpr (!TWO_SM) {
+                        // All column loads in flight at once, then one wait.
+                        uint32_t r[C::kCols];
+#pragma unroll
+                        for (int c = 0; c < C::kCols; c += 16)
+                            tmem_ld16(taddr + c, *reinterpret_cast<uint32_t(*)[16]>(r + c));
                         tmem_ld_wait();
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) acc[c + j] = __uint_as_float(r[j]);
+                        for (int j = 0; j < C::kCols; ++j) acc[j] = __uint_as_float(r[j]);
                     }
                     tc_fence_before();
                     __syncwarp();
@@ -609,7 +666,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
             // and the output below is skipped).
             if (!named_barrier_and(1, C::kEpiThreads, ok && !*abort)) continue;
 
-            if (split == 1) {
+            if (TWO_SM || split == 1) {
                 // Scale, add bias, convert, store.
                 if (SWAP) {
                     if (rn < p.N) {
@@ -624,44 +681,25 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
                         }
                     }
                 } else if (C::kTmaStore) {
-                    // Each warp converts 32 columns of its 32 rows at a time
-                    // into its staging buffer -- 64-byte rows, 64-byte TMA
-                    // swizzle: 16-byte unit u of row r sits at unit
-                    // u ^ ((r >> 1) & 3), so the eight rows a quarter-warp
-                    // writes hit distinct banks -- and one lane stores the
-                    // 32 x 32 box with TMA, which clips rows >= M and
-                    // columns >= N.
-                    uint8_t *sbuf = smem + C::kOffStage + static_cast<uint32_t>(ew) * C::kStageBufBytes;
-                    const int ybox = m0 + quarter * 32;
+                    // From the row in registers (TWO_SM tiles were stored
+                    // straight from TMEM above), 32 columns at a time.
+                    if constexpr (!TWO_SM) {
+                        uint8_t *sbuf = smem + C::kOffStage + static_cast<uint32_t>(ew) * C::kStageBufBytes;
+                        const int ybox = m0 + quarter * 32;
 #pragma unroll
-                    for (int ch = 0; ch < C::kCols / 32; ++ch) {
-                        const int cb = col0 + ch * 32;
-                        uint32_t w[16];
+                        for (int ch = 0; ch < C::kCols / 32; ++ch) {
+                            const int cb = col0 + ch * 32;
+                            uint32_t w[16];
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int c = cb + 2 * e;
-                            const float y0 = BLOCKWISE ? acc[ch * 32 + 2 * e] + sColBias[c]
-                                                       : fmaf(acc[ch * 32 + 2 * e] * row_scale, sColScale[c], sColBias[c]);
-                            const float y1 = BLOCKWISE ? acc[ch * 32 + 2 * e + 1] + sColBias[c + 1]
-                                                       : fmaf(acc[ch * 32 + 2 * e + 1] * row_scale, sColScale[c + 1],
-                                                              sColBias[c + 1]);
-                            const OutT lo = to_out<OutT>(y0), hi = to_out<OutT>(y1);
-                            w[e] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(&lo)) |
-                                   (static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(&hi)) << 16);
-                        }
-                        // The previous box stored from this buffer must have
-                        // been read out first.
-                        if (lane == 0) bulk_wait_read();
-                        __syncwarp();
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            *reinterpret_cast<uint4 *>(sbuf + lane * 64 + 16 * (u ^ ((lane >> 1) & 3))) =
-                                make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0 && ybox < p.M && n0 + cb < p.N) {
-                            tma_store_2d(&tm_out, sbuf, n0 + cb, ybox);
-                            bulk_commit();
+                            for (int e = 0; e < 16; ++e) {
+                                const int j = ch * 32 + 2 * e, c = cb + 2 * e;
+                                w[e] = BLOCKWISE
+                                           ? pack_out2<OutT>(acc[j] + sColBias[c], acc[j + 1] + sColBias[c + 1])
+                                           : pack_out2<OutT>(fmaf(acc[j] * row_scale, sColScale[c], sColBias[c]),
+                                                             fmaf(acc[j + 1] * row_scale, sColScale[c + 1],
+                                                                  sColBias[c + 1]));
+                            }
+                            store_box_tma(&tm_out, sbuf, lane, w, n0 + cb, ybox, ybox < p.M && n0 + cb < p.N);
                         }
                     }
                 } else if (rm < p.M) {
@@ -755,11 +793,15 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
                 // before it may exit.
                 if (etid == 0) bulk_wait_read();
             } else {
-                // Split-K, pull: publish this CTA's partial tile (the ring is
-                // idle: every copy was consumed and every MMA has completed).
+                // Split-K, pull: publish this CTA's partial tile row-major
+                // with padded rows (the ring is idle: every copy was consumed
+                // and every MMA has completed).
+                constexpr int SP = C::kPartStride;
                 named_barrier_sync(1, C::kEpiThreads);
 #pragma unroll
-                for (int j = 0; j < C::kCols; ++j) sRed[(col0 + j) * 128 + row] = acc[j];
+                for (int j = 0; j < C::kCols; j += 4)
+                    *reinterpret_cast<float4 *>(sRed + row * SP + col0 + j) =
+                        make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
             }
             if (warp == 2 && lane == 0) FP8Q_TRACE_AT(p, kTrEpiDone);
         }
@@ -767,46 +809,60 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
         if (C::kTmaStore && lane == 0) bulk_wait_all();
     }
 
-    if (split > 1 && !C::kPush) {
-        cluster_sync();
-        if (threadIdx.x == 64) FP8Q_TRACE_AT(p, kTrCluster1);
-        if (warp >= 2 && !*abort) {
-            // Reduce rows [r_lo, r_hi) (whole groups of 4) over the cluster.
-            const int etid = threadIdx.x - 64;
-            const int r_lo = 4 * (32 * rank / split), r_hi = 4 * (32 * (rank + 1) / split);
-            const int quads = (r_hi - r_lo) >> 2;
-            int a_t, b_t;
-            coords(cluster_id, a_t, b_t);
-            const int m0 = (SWAP ? b_t : a_t) * C::kTokTile;
-            const int n0 = (SWAP ? a_t : b_t) * C::kColTile;
-            OutT *out = static_cast<OutT *>(p.out);
-            const uint32_t red_base = smem_u32(sRed);
-            for (int item = etid; item < BN * quads; item += C::kEpiThreads) {
-                const int c = item / quads;
-                const int r = r_lo + 4 * (item - c * quads);
-                const uint32_t off = static_cast<uint32_t>((c * 128 + r) * 4);
-                float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int q = 0; q < split; ++q) {
-                    const float4 v = dsmem_ld_f4(dsmem_map(red_base + off, static_cast<uint32_t>(q)));
-                    s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
-                }
-                const float sv[4] = {s.x, s.y, s.z, s.w};
+    if constexpr (!C::kPush) {
+        if (split > 1) {
+            cluster_sync();
+            if (threadIdx.x == 64) FP8Q_TRACE_AT(p, kTrCluster1);
+            if (warp >= 2 && !*abort) {
+                // Reduce rows [r_lo, r_hi) of the (non-swapped) tile over
+                // the cluster in rank order.  Items are (row, 4-column
+                // group) with the columns fastest, so a warp's DSMEM reads
+                // and its 8-byte output stores are contiguous.
+                constexpr int SP = C::kPartStride;
+                constexpr int G = BN / 4;
+                const int etid = threadIdx.x - 64;
+                const int r_lo = 4 * (32 * rank / split), r_hi = 4 * (32 * (rank + 1) / split);
+                int a_t, b_t;
+                coords(cluster_id, a_t, b_t);
+                const int m0 = a_t * C::kTokTile;
+                const int n0 = b_t * C::kColTile;
+                OutT *out = static_cast<OutT *>(p.out);
+                const uint32_t red_base = smem_u32(sRed);
+                for (int item = etid; item < (r_hi - r_lo) * G; item += C::kEpiThreads) {
+                    const int rr = item / G;
+                    const int c4 = item - rr * G;
+                    const int r = r_lo + rr;
+                    const uint32_t off = static_cast<uint32_t>((r * SP + c4 * 4) * 4);
+                    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int q = 0; q < split; ++q) {
+                        const float4 v = dsmem_ld_f4(dsmem_map(red_base + off, static_cast<uint32_t>(q)));
+                        sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+                    }
+                    const int m = m0 + r, n = n0 + 4 * c4;
+                    if (m >= p.M || n >= p.N) continue;
+                    const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+                    const float am = BLOCKWISE ? 1.0f : __ldg(p.a_scale + m);
+                    float y[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int m = SWAP ? m0 + c : m0 + r + e;
-                    const int n = SWAP ? n0 + r + e : n0 + c;
-                    if (m < p.M && n < p.N) {
-                        float y = sv[e];
-                        if (!BLOCKWISE) y *= __ldg(p.a_scale + m) * __ldg(p.w_scale + n);
-                        if (p.bias != nullptr) y += __bfloat162float(p.bias[n]);
-                        store_out(out, static_cast<long long>(m) * p.ldo + n, y);
+                    for (int e = 0; e < 4; ++e) {
+                        const bool in = n + e < p.N;
+                        const float bv = (p.bias != nullptr && in) ? __bfloat162float(p.bias[n + e]) : 0.0f;
+                        y[e] = BLOCKWISE ? sv[e] + bv : fmaf(sv[e] * am, in ? __ldg(p.w_scale + n + e) : 0.0f, bv);
+                    }
+                    OutT *o = out + static_cast<long long>(m) * p.ldo + n;
+                    if (n + 4 <= p.N) {
+                        *reinterpret_cast<uint2 *>(o) = make_uint2(pack_out2<OutT>(y[0], y[1]), pack_out2<OutT>(y[2], y[3]));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (n + e < p.N) o[e] = to_out<OutT>(y[e]);
                     }
                 }
             }
+            if (threadIdx.x == 64) FP8Q_TRACE_AT(p, kTrReduced);
+            cluster_sync();
+            if (threadIdx.x == 64) FP8Q_TRACE_AT(p, kTrCluster2);
         }
-        if (threadIdx.x == 64) FP8Q_TRACE_AT(p, kTrReduced);
-        cluster_sync();
-        if (threadIdx.x == 64) FP8Q_TRACE_AT(p, kTrCluster2);
     }
 
     tc_fence_before();
