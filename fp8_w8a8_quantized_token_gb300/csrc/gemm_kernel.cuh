@@ -589,15 +589,22 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
                     const float *sa = sSA + estage * C::kSASlotFloats;
                     const float srow = SWAP ? 0.0f : sa[row] * swk;
                     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + slot * BN + col0;
+                    // Promotion, 32 columns per TMEM wait, two columns per
+                    // packed FMA (each lane a correctly rounded fmaf).
 #pragma unroll
-                    for (int c = 0; c < C::kCols; c += 16) {
-                        uint32_t r[16];
-                        tmem_ld16(taddr + c, r);
+                    for (int c = 0; c < C::kCols; c += 32) {
+                        uint32_t r[32];
+                        tmem_ld16(taddr + c, *reinterpret_cast<uint32_t(*)[16]>(r));
+                        if (c + 16 < C::kCols) tmem_ld16(taddr + c + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
                         tmem_ld_wait();
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float s = SWAP ? sa[col0 + c + j] * swk : srow;
-                            acc[c + j] = fmaf(__uint_as_float(r[j]), s, acc[c + j]);
+                        for (int j = 0; j < 32 && c + j < C::kCols; j += 2) {
+                            const float2 s2 = SWAP ? make_float2(sa[col0 + c + j] * swk, sa[col0 + c + j + 1] * swk)
+                                                   : make_float2(srow, srow);
+                            const float2 t = __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                                                        s2, make_float2(acc[c + j], acc[c + j + 1]));
+                            acc[c + j] = t.x;
+                            acc[c + j + 1] = t.y;
                         }
                     }
                     tc_fence_before();

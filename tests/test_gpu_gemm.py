@@ -149,7 +149,9 @@ def test_blockwise_every_schedule(dev, schedule, swap, mma_n, split):
 
 
 def test_blockwise_paired_tiles(dev, schedule):
-    """Blockwise pairs share each weight slice by TMA multicast."""
+    """Blockwise pairs share each weight slice by TMA multicast (each CTA
+    runs its own MMAs: the per-K-block promotion hands the accumulator back
+    to the MMA every K block, which a 2-CTA MMA would couple across SMs)."""
     fq.fp8q_set_plan_override(0, 256, 1)
     M, N, K = 1100, 768, 1024
     plan = fq.fp8q_gemm_plan(M, N, K, blockwise=True)
@@ -247,3 +249,44 @@ def test_weights_rewritten_right_before_the_gemm(dev, order):
         rwq, rws = oracle.quant_weight_per_channel(ws_cpu[i])
         ref = ref_values(oracle.gemm_channelwise(rq, rwq, rs, rws, threads=THREADS))
         assert_gemm_close(out_values(outs[i]), ref, f"iteration {i}")
+
+
+MULTICAST_PAIR_SCRIPT = r"""
+import numpy as np, torch, sys
+sys.path.insert(0, %r)
+sys.path.insert(0, %r)
+import fp8_w8a8_quantized_token_gb300 as fq, oracle, synthetic
+from gpu_util import assert_gemm_close, out_values, quant_both_group, quant_both_per_token, ref_values, u8
+dev = torch.device("cuda", 0)
+fq.fp8q_set_plan_override(0, 256, 1)
+M, N, K = 700, 512, 1024
+assert fq.fp8q_gemm_plan(M, N, K)["two_sm"] == 0 and fq.fp8q_gemm_plan(M, N, K)["pair"] == 1
+x = synthetic.activations(M, K, seed=5, outliers=True)
+w = synthetic.weights(N, K, seed=5)
+xq, xs, rq, rs = quant_both_per_token(x, dev)
+wq, ws, rwq, rws = quant_both_per_token(w, dev)
+out = fq.fp8q_scaled_mm_channelwise(xq, wq, xs, ws)
+torch.cuda.synchronize()
+assert_gemm_close(out_values(out), ref_values(oracle.gemm_channelwise(rq, rwq, rs, rws)), "multicast pairs")
+gq, gs, grq, grs = quant_both_group(x, dev, 128)
+bwq, bws = fq.fp8q_quant_weight_block128(w.to(dev))
+out = fq.fp8q_scaled_mm_blockwise(gq, bwq, gs, bws, M=M)
+torch.cuda.synchronize()
+rwq, rws = oracle.quant_weight_blocks(w, 128, 128)
+assert_gemm_close(out_values(out), ref_values(oracle.gemm_blockwise(grq, rwq, grs, rws, M)), "blockwise multicast pairs")
+assert fq.fp8q_device_status() == fq.FP8Q_OK
+print("multicast pairs ok")
+"""
+
+
+def test_multicast_pairs_without_two_cta_mma(dev):
+    """FP8Q_NO_2SM=1 (read at start-up, so in a child process): channelwise
+    pairs share each weight slice by TMA multicast instead of 2-CTA MMAs."""
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    script = MULTICAST_PAIR_SCRIPT % (os.path.dirname(here), here)
+    r = subprocess.run([sys.executable, "-c", script], capture_output=True, text=True, timeout=600,
+                       env=dict(os.environ, FP8Q_NO_2SM="1"))
+    assert r.returncode == 0 and "multicast pairs ok" in r.stdout, r.stdout + r.stderr
