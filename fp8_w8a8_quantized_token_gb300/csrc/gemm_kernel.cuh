@@ -574,6 +574,9 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
             float acc[C::kCols];
             bool ok = true;
             if (BLOCKWISE) {
+                // TMEM columns per wait: 16 where the accumulator row is long
+                // (keeps the 128-float row and the loop state in registers).
+                constexpr int kPromoteCols = C::kCols >= 128 ? 16 : 32;
 #pragma unroll
                 for (int j = 0; j < C::kCols; ++j) acc[j] = 0.0f;
                 const int wblk = SWAP ? a_t : (n0 >> 7) + cgroup;  // 128-row weight block
@@ -589,16 +592,17 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
                     const float *sa = sSA + estage * C::kSASlotFloats;
                     const float srow = SWAP ? 0.0f : sa[row] * swk;
                     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + slot * BN + col0;
-                    // Promotion, 32 columns per TMEM wait, two columns per
-                    // packed FMA (each lane a correctly rounded fmaf).
+                    // Promotion, two columns per packed FMA (each lane a
+                    // correctly rounded fmaf).
 #pragma unroll
-                    for (int c = 0; c < C::kCols; c += 32) {
-                        uint32_t r[32];
+                    for (int c = 0; c < C::kCols; c += kPromoteCols) {
+                        uint32_t r[kPromoteCols];
                         tmem_ld16(taddr + c, *reinterpret_cast<uint32_t(*)[16]>(r));
-                        if (c + 16 < C::kCols) tmem_ld16(taddr + c + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+                        if (kPromoteCols == 32 && c + 16 < C::kCols)
+                            tmem_ld16(taddr + c + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
                         tmem_ld_wait();
 #pragma unroll
-                        for (int j = 0; j < 32 && c + j < C::kCols; j += 2) {
+                        for (int j = 0; j < kPromoteCols && c + j < C::kCols; j += 2) {
                             const float2 s2 = SWAP ? make_float2(sa[col0 + c + j] * swk, sa[col0 + c + j + 1] * swk)
                                                    : make_float2(srow, srow);
                             const float2 t = __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
