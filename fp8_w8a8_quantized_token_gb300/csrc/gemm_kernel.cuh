@@ -203,13 +203,43 @@ __device__ __forceinline__ void store_out(OutT *out, long long idx, float v)
     out[idx] = to_out<OutT>(v);
 }
 
-// Two outputs converted and packed into one 32-bit word (lo first).
+// Two outputs converted (round to nearest even) and packed into one 32-bit
+// word, lo in the low half: one paired conversion instruction.
 template <typename OutT>
-__device__ __forceinline__ uint32_t pack_out2(float lo, float hi)
+__device__ __forceinline__ uint32_t pack_out2(float lo, float hi);
+template <>
+__device__ __forceinline__ uint32_t pack_out2<__nv_bfloat16>(float lo, float hi)
 {
-    const OutT a = to_out<OutT>(lo), b = to_out<OutT>(hi);
-    return static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(&a)) |
-           (static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(&b)) << 16);
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+template <>
+__device__ __forceinline__ uint32_t pack_out2<__half>(float lo, float hi)
+{
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// Channelwise output of 32 consecutive columns of one row: y = acc * a_scale
+// * w_scale + bias, as (acc * a_scale) rounded, then one fma -- the scalar
+// order -- two columns per packed instruction; scales and bias read four at a
+// time from shared memory (16-byte aligned).
+template <typename OutT>
+__device__ __forceinline__ void convert32_channelwise(const float *acc, float row_scale, const float *col_scale,
+                                                      const float *col_bias, uint32_t (&w)[16])
+{
+    const float2 rs = make_float2(row_scale, row_scale);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 sc = *reinterpret_cast<const float4 *>(col_scale + 4 * q);
+        const float4 bi = *reinterpret_cast<const float4 *>(col_bias + 4 * q);
+        const float2 p0 = __fmul2_rn(make_float2(acc[4 * q], acc[4 * q + 1]), rs);
+        const float2 p1 = __fmul2_rn(make_float2(acc[4 * q + 2], acc[4 * q + 3]), rs);
+        const float2 y0 = __ffma2_rn(p0, make_float2(sc.x, sc.y), make_float2(bi.x, bi.y));
+        const float2 y1 = __ffma2_rn(p1, make_float2(sc.z, sc.w), make_float2(bi.z, bi.w));
+        w[2 * q] = pack_out2<OutT>(y0.x, y0.y);
+        w[2 * q + 1] = pack_out2<OutT>(y1.x, y1.y);
+    }
 }
 
 // One warp stores a 32-row x 32-column box of 2-byte outputs (lane = row,
@@ -643,12 +673,8 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
                             tmem_ld_wait();
                             const int cb = col0 + ch * 32;
                             uint32_t w[16];
-#pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                w[e] = pack_out2<OutT>(
-                                    fmaf(__uint_as_float(r[2 * e]) * row_scale, sColScale[cb + 2 * e], sColBias[cb + 2 * e]),
-                                    fmaf(__uint_as_float(r[2 * e + 1]) * row_scale, sColScale[cb + 2 * e + 1],
-                                         sColBias[cb + 2 * e + 1]));
+                            convert32_channelwise<OutT>(reinterpret_cast<const float *>(r), row_scale, sColScale + cb,
+                                                        sColBias + cb, w);
                             store_box_tma(&tm_out, sbuf, lane, w, n0 + cb, ybox, ybox < p.M && n0 + cb < p.N);
                         }
                     } else if constexpr (!TWO_SM) {
@@ -816,8 +842,9 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
             }
             if (warp == 2 && lane == 0) FP8Q_TRACE_AT(p, kTrEpiDone);
         }
-        // Output boxes stored with TMA are complete before the CTA exits.
-        if (C::kTmaStore && lane == 0) bulk_wait_all();
+        // The staging buffers must have been read out by the TMA unit before
+        // the CTA exits (the stores themselves complete with the grid).
+        if (C::kTmaStore && lane == 0) bulk_wait_read();
     }
 
     if constexpr (!C::kPush) {
