@@ -42,6 +42,7 @@ EXPORTED = (
     "fp8q_gemm_plan",
     "fp8q_set_plan_override",
     "fp8q_device_status",
+    "fp8q_selftest_wait_timeout",
     "fp8q_status_str",
     "fp8q_version",
 )
@@ -87,6 +88,7 @@ def load_library(path: str | None = None):
         "fp8q_linear_channelwise_noalloc": [P, P, I64, P, P, P, I64, I64, I64, ctypes.c_int, P],
         "fp8q_gemm_plan": [I64, I64, I64, I32, I32, ctypes.POINTER(Plan)],
         "fp8q_device_status": [P, I32],
+        "fp8q_selftest_wait_timeout": [P],
         "fp8q_set_plan_override": [I32, I32, I32],
     }
     for name, args in sig.items():
@@ -373,6 +375,14 @@ def fp8q_device_status(reset: bool = True, device=None) -> int:
     L = load_library()
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     return int(L.fp8q_device_status(_stream(device), int(bool(reset))))
+
+
+def fp8q_selftest_wait_timeout(device=None) -> None:
+    """Enqueue the diagnostics kernel whose bounded pipeline wait runs out
+    (about 2 s); fp8q_device_status() then reports FP8Q_ERR_TIMEOUT."""
+    L = load_library()
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    _check("fp8q_selftest_wait_timeout", L.fp8q_selftest_wait_timeout(_stream(device)))
 
 
 def fp8q_version() -> int:

@@ -417,6 +417,12 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
         FP8Q_TRACE_AT(p, kTrPreloaded);
     }
     if (C::kPush && split > 1) cluster_wait();
+    // The producer's cache policies, made before the dependency wait.
+    uint64_t pol_a = 0, pol_b = 0;
+    if (warp == 0 && lane == 0) {
+        pol_a = SWAP ? policy_evict_first() : policy_evict_normal();
+        pol_b = SWAP ? policy_evict_last() : policy_evict_normal();
+    }
     if (threadIdx.x == 0) FP8Q_TRACE_AT(p, kTrPrologue);
     // Everything below may read the previous kernel's output (activations,
     // scales) or overwrite buffers it reads (out).
@@ -429,8 +435,6 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
         // TMA producer
         // ------------------------------------------------------------------
         if (lane == 0) {
-            const uint64_t pol_a = SWAP ? policy_evict_first() : policy_evict_normal();
-            const uint64_t pol_b = SWAP ? policy_evict_last() : policy_evict_normal();
             uint32_t stage = 0, phase = 0;
             long long issued = 0;
             for (int tile = cluster_id; tile < p.num_tiles; tile += num_clusters) {

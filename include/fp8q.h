@@ -284,6 +284,14 @@ FP8Q_API fp8q_status fp8q_set_plan_override(int32_t swap_ab, int32_t mma_n, int3
  * Synchronizes `stream`.  reset != 0 clears the word afterwards. */
 FP8Q_API fp8q_status fp8q_device_status(void *stream, int32_t reset);
 
+/* Diagnostics (the pages have no counterpart): enqueue a one-warp kernel
+ * whose pipeline wait can never complete.  The bounded wait the GEMM uses
+ * gives up after its time limit (about 2 s), records FP8Q_ERR_TIMEOUT in
+ * the device status word and the kernel returns: nothing hangs and the
+ * context stays usable.  Read (and reset) the word with fp8q_device_status.
+ * Returns FP8Q_OK if the kernel was enqueued, ERR_CUDA otherwise. */
+FP8Q_API fp8q_status fp8q_selftest_wait_timeout(void *stream);
+
 /* Human-readable name of a status code (static string). */
 FP8Q_API const char *fp8q_status_str(fp8q_status status);
 
