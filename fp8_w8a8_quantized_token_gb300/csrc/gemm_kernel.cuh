@@ -107,7 +107,18 @@ struct GemmCfg {
     static constexpr int kEpiWarps = BN > 128 ? 8 : 4;
     static constexpr int kColGroups = kEpiWarps / 4;
     static constexpr int kCols = BN / kColGroups;  // TMEM columns per epilogue thread
-    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    // MMA-issuing warps.  A tcgen05.mma occupies its issuing thread for
+    // about 140 cycles whatever its N, while the tensor pipe completes a
+    // 128 x N x 32 MMA in about N/256 of that: channelwise tiles narrower
+    // than 256 columns spread each K block's four MMAs over 2 warps, each
+    // accumulating into its own TMEM columns; the epilogue adds the two
+    // accumulators.  (More issuers would add warps: 2 CTAs of 7 warps still
+    // fit one SM's register file, which lets the next launch's CTAs load
+    // their weights while this launch's CTAs finish.)
+    static constexpr int kIssuers = (BLOCKWISE || TWO_SM || BN >= 256) ? 1 : 2;
+    static constexpr int kSlotCols = kIssuers * BN;  // TMEM columns per accumulator slot
+    static constexpr int kEpiWarp0 = 1 + kIssuers;   // first epilogue warp
+    static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
     static constexpr int kEpiThreads = 32 * kEpiWarps;
     static constexpr int kTokTile = SWAP ? BN : 128;     // tokens per tile
     static constexpr int kColTile = SWAP ? 128 : BN;     // output columns per tile
@@ -120,7 +131,9 @@ struct GemmCfg {
     static constexpr int kSASlotFloats = static_cast<int>(kSASlot / 4u);
     // Bytes one ring slot's full barrier waits for (TWO_SM: both CTAs' loads).
     static constexpr uint32_t kStageTx = TWO_SM ? 2u * (kABytes + kBBytes) : kABytes + kBBytes + kSABytes;
-    static constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32u : static_cast<uint32_t>(2 * BN);
+    // Two accumulator slots, allocated as a power of two >= 32 columns.
+    static constexpr uint32_t kTmemCols = 2 * kSlotCols <= 32 ? 32u : 2 * kSlotCols <= 64 ? 64u
+                                        : 2 * kSlotCols <= 128 ? 128u : 2 * kSlotCols <= 256 ? 256u : 512u;
     static constexpr uint32_t kOffA = 0;
     static constexpr uint32_t kOffB = kOffA + STAGES * kABytes;
     static constexpr uint32_t kOffSA = kOffB + STAGES * kBBytes;
@@ -152,6 +165,7 @@ struct GemmCfg {
     static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
     static_assert(kCols % 32 == 0 || kCols == 16, "epilogue column chunking");
+    static_assert(2 * kSlotCols <= 512, "TMEM columns");
 };
 
 // Waits that only give up on the time limit (used while draining).
@@ -339,13 +353,13 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
         if (C::kTmaStore) tma_prefetch_map(&tm_out);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], (BLOCKWISE ? C::kEpiWarps : 0) + ((pair && !TWO_SM) ? 2 : 1));
+            mbar_init(&empty[s], (BLOCKWISE ? C::kEpiWarps : 0) + ((pair && !TWO_SM) ? 2 : C::kIssuers));
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&tfull[i], 1);
+            mbar_init(&tfull[i], C::kIssuers);
             mbar_init(&tempty[i], TWO_SM ? 2 * C::kEpiWarps : C::kEpiWarps);
         }
-        mbar_init(drain, 1);
+        mbar_init(drain, C::kIssuers);
         mbar_init(recv_full, 1);
         *abort = 0;
         fence_mbar_init();
@@ -496,10 +510,12 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
                 for (long long j = first; j < issued; ++j)
                     mbar_wait_drain(&empty[j % STAGES], static_cast<uint32_t>((j / STAGES) & 1), p.status);
         }
-    } else if (warp == 1) {
+    } else if (warp <= C::kIssuers) {
         // ------------------------------------------------------------------
-        // MMA issuer (one thread)
+        // MMA issuers (one thread per issuing warp; issuer j takes the K
+        // steps k of every K block with k % kIssuers == j)
         // ------------------------------------------------------------------
+        const int issuer = warp - 1;
         if (lane == 0 && (!TWO_SM || leader)) {
             uint32_t stage = 0, phase = 0, slot = 0, tphase = 0;
             bool ok = true;
@@ -515,13 +531,14 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
                     }
                     if (!mbar_wait(&full[stage], phase, abort, p.status)) { ok = false; break; }
                     tc_fence_after();
-                    if (tile == cluster_id && i == 0) FP8Q_TRACE_AT(p, kTrFirstMma);
+                    if (tile == cluster_id && i == 0 && issuer == 0) FP8Q_TRACE_AT(p, kTrFirstMma);
                     const uint32_t a_addr = smem_u32(sA + stage * C::kABytes);
                     const uint32_t b_addr = smem_u32(sB + stage * C::kBBytes);
-                    const uint32_t d = tmem_base + slot * BN;
+                    const uint32_t d = tmem_base + slot * C::kSlotCols + static_cast<uint32_t>(issuer * BN);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const uint32_t acc = BLOCKWISE ? (k > 0) : (i > 0 || k > 0);
+                        if (C::kIssuers > 1 && k % C::kIssuers != issuer) continue;
+                        const uint32_t acc = BLOCKWISE ? (k > 0) : (i > 0 || k >= C::kIssuers);
                         if (TWO_SM)
                             umma_e4m3_pair(d, umma_desc_sw128(a_addr + k * 32), umma_desc_sw128(b_addr + k * 32),
                                            C::kIdesc, acc);
@@ -547,7 +564,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
                     if (slot == 0) tphase ^= 1u;
                 }
             }
-            FP8Q_TRACE_AT(p, kTrLastCommit);
+            if (issuer == 0) FP8Q_TRACE_AT(p, kTrLastCommit);
             // Every MMA this thread issued has finished before TMEM is freed.
             if (TWO_SM) umma_commit_pair(drain);
             else umma_commit(drain);
@@ -566,12 +583,12 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
         // ------------------------------------------------------------------
         // Epilogue warps
         // ------------------------------------------------------------------
-        const int ew = warp - 2;
+        const int ew = warp - C::kEpiWarp0;
         const int quarter = warp & 3;          // TMEM lanes this warp may access
         const int cgroup = ew >> 2;            // column group
         const int row = quarter * 32 + lane;   // TMEM lane = accumulator row
         const int col0 = cgroup * C::kCols;
-        const int etid = threadIdx.x - 64;
+        const int etid = threadIdx.x - 32 * C::kEpiWarp0;
         OutT *out = static_cast<OutT *>(p.out);
         uint32_t slot = 0, tphase = 0, estage = 0, ephase = 0;
 
@@ -625,7 +642,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
                     const float swk = __ldg(sw_row + kb);
                     const float *sa = sSA + estage * C::kSASlotFloats;
                     const float srow = SWAP ? 0.0f : sa[row] * swk;
-                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + slot * BN + col0;
+                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + slot * C::kSlotCols + col0;
                     // Promotion, two columns per packed FMA (each lane a
                     // correctly rounded fmaf).
 #pragma unroll
@@ -659,16 +676,21 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
                 ok = __all_sync(0xffffffffu, mbar_wait(&tfull[slot], tphase, abort, p.status));
                 if (ok) {
                     tc_fence_after();
-                    if (warp == 2 && lane == 0) FP8Q_TRACE_AT(p, kTrEpiFull);
-                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + slot * BN + col0;
-                    // TWO_SM tiles (never split along K) go straight from TMEM
-                    // to the output; the others keep the whole row in
-                    // registers for the stores or the split-K exchange below.
-                    if constexpr (TWO_SM) {
+                    if (ew == 0 && lane == 0) FP8Q_TRACE_AT(p, kTrEpiFull);
+                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + slot * C::kSlotCols + col0;
+                    // Non-swapped channelwise tiles go straight from TMEM to
+                    // the output (or, split along K, to the partial tile);
+                    // swapped tiles keep the whole row in registers for the
+                    // stores or the split-K exchange below.
+                    if constexpr (!SWAP) {
                         // 32 accumulator columns at a time: TMEM -> scale,
-                        // bias, convert -> staging buffer -> TMA store.
+                        // bias, convert -> staging buffer -> TMA store; split
+                        // along K: TMEM -> this row of the partial tile, kept
+                        // row-major with padded rows in the ring (idle: every
+                        // copy was consumed and every MMA has completed).
                         uint8_t *sbuf = smem + C::kOffStage + static_cast<uint32_t>(ew) * C::kStageBufBytes;
                         const int ybox = m0 + quarter * 32;
+                        const bool partial = !TWO_SM && split > 1;
 #pragma unroll 1
                         for (int ch = 0; ch < C::kCols / 32; ++ch) {
                             uint32_t r[32];
@@ -676,20 +698,52 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
                             tmem_ld16(taddr + ch * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
                             tmem_ld_wait();
                             const int cb = col0 + ch * 32;
-                            uint32_t w[16];
-                            convert32_channelwise<OutT>(reinterpret_cast<const float *>(r), row_scale, sColScale + cb,
-                                                        sColBias + cb, w);
-                            store_box_tma(&tm_out, sbuf, lane, w, n0 + cb, ybox, ybox < p.M && n0 + cb < p.N);
+                            if (partial) {
+                                float *dst = sRed + row * C::kPartStride + cb;
+#pragma unroll
+                                for (int j = 0; j < 32; j += 4)
+                                    *reinterpret_cast<float4 *>(dst + j) =
+                                        make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                                    __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+                            } else {
+                                uint32_t w[16];
+                                convert32_channelwise<OutT>(reinterpret_cast<const float *>(r), row_scale,
+                                                            sColScale + cb, sColBias + cb, w);
+                                store_box_tma(&tm_out, sbuf, lane, w, n0 + cb, ybox, ybox < p.M && n0 + cb < p.N);
+                            }
                         }
-                    } else if constexpr (!TWO_SM) {
-                        // All column loads in flight at once, then one wait.
-                        uint32_t r[C::kCols];
+                    } else {
+                        if constexpr (C::kIssuers == 1) {
+                            // All column loads in flight at once, then one wait.
+                            uint32_t r[C::kCols];
 #pragma unroll
-                        for (int c = 0; c < C::kCols; c += 16)
-                            tmem_ld16(taddr + c, *reinterpret_cast<uint32_t(*)[16]>(r + c));
-                        tmem_ld_wait();
+                            for (int c = 0; c < C::kCols; c += 16)
+                                tmem_ld16(taddr + c, *reinterpret_cast<uint32_t(*)[16]>(r + c));
+                            tmem_ld_wait();
 #pragma unroll
-                        for (int j = 0; j < C::kCols; ++j) acc[j] = __uint_as_float(r[j]);
+                            for (int j = 0; j < C::kCols; ++j) acc[j] = __uint_as_float(r[j]);
+                        } else {
+                            // Up to 32 columns of every issuer's accumulator
+                            // in flight, then one wait; added in issuer order.
+                            constexpr int kChunk = C::kCols < 32 ? C::kCols : 32;
+#pragma unroll
+                            for (int c = 0; c < C::kCols; c += kChunk) {
+                                uint32_t r[C::kIssuers][kChunk];
+#pragma unroll
+                                for (int a = 0; a < C::kIssuers; ++a)
+#pragma unroll
+                                    for (int h = 0; h < kChunk; h += 16)
+                                        tmem_ld16(taddr + a * BN + c + h, *reinterpret_cast<uint32_t(*)[16]>(r[a] + h));
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int j = 0; j < kChunk; ++j) {
+                                    float v = __uint_as_float(r[0][j]);
+#pragma unroll
+                                    for (int a = 1; a < C::kIssuers; ++a) v += __uint_as_float(r[a][j]);
+                                    acc[c + j] = v;
+                                }
+                            }
+                        }
                     }
                     tc_fence_before();
                     __syncwarp();
@@ -707,7 +761,9 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
             // and the output below is skipped).
             if (!named_barrier_and(1, C::kEpiThreads, ok && !*abort)) continue;
 
-            if (TWO_SM || split == 1) {
+            if (!SWAP && !BLOCKWISE) {
+                // Stored (or published as a partial tile) above.
+            } else if (split == 1) {
                 // Scale, add bias, convert, store.
                 if (SWAP) {
                     if (rn < p.N) {
@@ -722,9 +778,8 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
                         }
                     }
                 } else if (C::kTmaStore) {
-                    // From the row in registers (TWO_SM tiles were stored
-                    // straight from TMEM above), 32 columns at a time.
-                    if constexpr (!TWO_SM) {
+                    // From the promoted row in registers, 32 columns at a time.
+                    if constexpr (BLOCKWISE) {
                         uint8_t *sbuf = smem + C::kOffStage + static_cast<uint32_t>(ew) * C::kStageBufBytes;
                         const int ybox = m0 + quarter * 32;
 #pragma unroll
@@ -844,7 +899,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
                     *reinterpret_cast<float4 *>(sRed + row * SP + col0 + j) =
                         make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
             }
-            if (warp == 2 && lane == 0) FP8Q_TRACE_AT(p, kTrEpiDone);
+            if (ew == 0 && lane == 0) FP8Q_TRACE_AT(p, kTrEpiDone);
         }
         // The staging buffers must have been read out by the TMA unit before
         // the CTA exits (the stores themselves complete with the grid).
@@ -854,34 +909,38 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
     if constexpr (!C::kPush) {
         if (split > 1) {
             cluster_sync();
-            if (threadIdx.x == 64) FP8Q_TRACE_AT(p, kTrCluster1);
-            if (warp >= 2 && !*abort) {
-                // Reduce rows [r_lo, r_hi) of the (non-swapped) tile over
-                // the cluster in rank order.  Items are (row, 4-column
-                // group) with the columns fastest, so a warp's DSMEM reads
-                // and its 8-byte output stores are contiguous.
+            if (threadIdx.x == 32 * C::kEpiWarp0) FP8Q_TRACE_AT(p, kTrCluster1);
+            if (warp >= C::kEpiWarp0 && !*abort) {
+                // Reduce the tile's valid rows over the cluster in rank
+                // order.  Items are (row, 4-column group) with the columns
+                // fastest, so a warp's DSMEM reads and its 8-byte output
+                // stores are contiguous; each rank takes an equal share of
+                // the items (a share of the columns when the tile holds few
+                // tokens).
                 constexpr int SP = C::kPartStride;
                 constexpr int G = BN / 4;
-                const int etid = threadIdx.x - 64;
-                const int r_lo = 4 * (32 * rank / split), r_hi = 4 * (32 * (rank + 1) / split);
+                const int etid = threadIdx.x - 32 * C::kEpiWarp0;
                 int a_t, b_t;
                 coords(cluster_id, a_t, b_t);
                 const int m0 = a_t * C::kTokTile;
                 const int n0 = b_t * C::kColTile;
+                const int rows = p.M - m0 < C::kTokTile ? p.M - m0 : C::kTokTile;
+                const int items = rows * G;
+                const int i_lo = static_cast<int>(static_cast<long long>(items) * rank / split);
+                const int i_hi = static_cast<int>(static_cast<long long>(items) * (rank + 1) / split);
                 OutT *out = static_cast<OutT *>(p.out);
                 const uint32_t red_base = smem_u32(sRed);
-                for (int item = etid; item < (r_hi - r_lo) * G; item += C::kEpiThreads) {
-                    const int rr = item / G;
-                    const int c4 = item - rr * G;
-                    const int r = r_lo + rr;
+                for (int item = i_lo + etid; item < i_hi; item += C::kEpiThreads) {
+                    const int r = item / G;
+                    const int c4 = item - r * G;
+                    const int m = m0 + r, n = n0 + 4 * c4;
+                    if (n >= p.N) continue;
                     const uint32_t off = static_cast<uint32_t>((r * SP + c4 * 4) * 4);
                     float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
                     for (int q = 0; q < split; ++q) {
                         const float4 v = dsmem_ld_f4(dsmem_map(red_base + off, static_cast<uint32_t>(q)));
                         sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
                     }
-                    const int m = m0 + r, n = n0 + 4 * c4;
-                    if (m >= p.M || n >= p.N) continue;
                     const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
                     const float am = BLOCKWISE ? 1.0f : __ldg(p.a_scale + m);
                     float y[4];
@@ -901,9 +960,9 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
                     }
                 }
             }
-            if (threadIdx.x == 64) FP8Q_TRACE_AT(p, kTrReduced);
+            if (threadIdx.x == 32 * C::kEpiWarp0) FP8Q_TRACE_AT(p, kTrReduced);
             cluster_sync();
-            if (threadIdx.x == 64) FP8Q_TRACE_AT(p, kTrCluster2);
+            if (threadIdx.x == 32 * C::kEpiWarp0) FP8Q_TRACE_AT(p, kTrCluster2);
         }
     }
 

@@ -45,8 +45,9 @@ def candidates(M: int):
         if M > 1024:
             continue
         c += [(1, mn, s) for s in SPLITS]
-    if M >= 64:
-        c += [(0, 256, s) for s in (1, 2, 4)]
+    # Weights on the MMA's N side: half the MMA instructions of 128-row
+    # weight tiles (a tcgen05.mma costs the same whatever its N).
+    c += [(0, 256, s) for s in ((1, 2, 4) if M > 1024 else SPLITS)]
     return c
 
 
