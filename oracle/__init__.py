@@ -64,6 +64,11 @@ def lib():
             L.fp8q_oracle_quant_per_token.argtypes = [P, I64, I64, F32, P, P, I64, I64]
             L.fp8q_oracle_quant_group_row_padded.argtypes = [P, I64, I64, I64, F32, I64, P, P, I64, I64]
             L.fp8q_oracle_quant_weight_blocks.argtypes = [P, I64, I64, I64, I64, I64, F32, P, P]
+            L.fp8q_oracle_quant_static.argtypes = [P, I64, I64, F32, P, I64, I64]
+            L.fp8q_oracle_quant_group_row_padded_ex.argtypes = [P, I64, I64, I64, F32, INT, INT, I64, P, P, I64, I64]
+            L.fp8q_oracle_exp_f32_array.argtypes = [P, P, I64]
+            L.fp8q_oracle_silu_mul_array.argtypes = [P, P, P, I64]
+            L.fp8q_oracle_pow2_ceil_array.argtypes = [P, P, I64]
             L.fp8q_oracle_gemm_channelwise.argtypes = [P, I64, P, I64, P, P, P, I64, I64, INT, P, I64, P, I64, I64]
             L.fp8q_oracle_gemm_blockwise.argtypes = [P, I64, P, I64, P, I64, P, P, I64, I64, INT, P, I64, P, I64, I64]
             L.fp8q_oracle_gemm_channelwise_at.argtypes = [P, I64, P, I64, P, P, P, I64, INT, P, P, I64, P]
@@ -181,6 +186,64 @@ def quant_group_row_padded(x, group_size: int = 128, eps: float = 1e-10, row_ali
     _run_rows(lambda r0, r1: L.fp8q_oracle_quant_group_row_padded(
         _ptr(xb), K, K, group_size, eps, m_pad, _ptr(xq), _ptr(xs), r0, r1), M, threads)
     return xq, xs
+
+
+def quant_group_row_padded_ex(x, group_size: int = 128, eps: float = 1e-10, row_alignment: int = 4,
+                              scale_ue8m0: bool = False, fuse_silu_and_mul: bool = False,
+                              xq_init: int = 0, xs_init: float = 0.0, threads: int = 1):
+    """The group quantizer with its options.  fuse_silu_and_mul: x is bf16
+    [M, 2K] and the quantized [M, K] values are silu(x[:, :K]) * x[:, K:] in
+    fp32; scale_ue8m0: scales rounded up to powers of two.  Returns (uint8
+    x_q [m_pad, K], fp32 x_s storage [K/g, m_pad])."""
+    xb = _bits16(x)
+    M, W = xb.shape
+    K = W // 2 if fuse_silu_and_mul else W
+    assert K % group_size == 0 and (not fuse_silu_and_mul or W == 2 * K)
+    m_pad = (M + row_alignment - 1) // row_alignment * row_alignment
+    xq = np.full((m_pad, K), xq_init, dtype=np.uint8)
+    xs = np.full((K // group_size, m_pad), xs_init, dtype=np.float32)
+    L = lib()
+    _run_rows(lambda r0, r1: L.fp8q_oracle_quant_group_row_padded_ex(
+        _ptr(xb), K, W, group_size, eps, int(scale_ue8m0), int(fuse_silu_and_mul), m_pad, _ptr(xq), _ptr(xs),
+        r0, r1), M, threads)
+    return xq, xs
+
+
+def quant_static(x, scale: float, threads: int = 1):
+    """Static per-tensor quantization: bf16 [M, K] and one fp32 scale ->
+    uint8 codes [M, K]."""
+    xb = _bits16(x)
+    M, K = xb.shape
+    xq = np.zeros((M, K), dtype=np.uint8)
+    L = lib()
+    s = float(np.float32(scale))
+    _run_rows(lambda r0, r1: L.fp8q_oracle_quant_static(_ptr(xb), K, K, s, _ptr(xq), r0, r1), M, threads)
+    return xq
+
+
+def exp_f32(t) -> np.ndarray:
+    """The quantizer's fully specified fp32 exp (elementwise)."""
+    t = np.ascontiguousarray(t, dtype=np.float32)
+    out = np.empty_like(t)
+    lib().fp8q_oracle_exp_f32_array(_ptr(t), _ptr(out), t.size)
+    return out
+
+
+def silu_mul(a, b) -> np.ndarray:
+    """silu(a) * b in fp32, as the fused group quantizer computes it."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    b = np.ascontiguousarray(b, dtype=np.float32)
+    out = np.empty_like(a)
+    lib().fp8q_oracle_silu_mul_array(_ptr(a), _ptr(b), _ptr(out), a.size)
+    return out
+
+
+def pow2_ceil(s) -> np.ndarray:
+    """fp32 scales rounded up to powers of two (UE8M0 scales)."""
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    out = np.empty_like(s)
+    lib().fp8q_oracle_pow2_ceil_array(_ptr(s), _ptr(out), s.size)
+    return out
 
 
 def quant_weight_blocks(w, block_n: int, block_k: int, eps: float = 1e-10):

@@ -32,6 +32,7 @@
  * fp32 division below must be the IEEE-754 correctly rounded one, and no
  * multiply-add may be contracted).
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -235,6 +236,136 @@ void fp8q_oracle_quant_weight_blocks(const uint16_t *w, int64_t N, int64_t K, in
                 quant_run(w + n * ldw + k0, k1 - k0, s, wq + n * K + k0);
         }
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Variants of the quantizers                                                */
+/* ------------------------------------------------------------------------ */
+
+/* Static per-tensor quantization of rows [r0, r1): one given fp32 scale s
+ * for the whole tensor (the static quant kernel _static_quant_fp8 named in
+ * [PR31340] "Implementation breakdown"), q = cast_e4m3(clamp(x / s)). */
+void fp8q_oracle_quant_static(const uint16_t *x, int64_t K, int64_t ldx, float s, uint8_t *xq,
+                              int64_t r0, int64_t r1)
+{
+    for (int64_t r = r0; r < r1; ++r) quant_run(x + r * ldx, K, s, xq + r * K);
+}
+
+/* The scale rounded up to a power of two, so that it is exactly an 8-bit
+ * exponent (UE8M0; the scale_ue8m0 flag of the group quantizer in [PR27896]
+ * "Key source snippets"): the smallest power of two >= s among the normal
+ * fp32 numbers, i.e. 2^ceil(log2 s) for a normal s and 2^-126 below that;
+ * +inf stays +inf.  frexp gives s = f * 2^e with f in [0.5, 1): s is itself
+ * a power of two exactly when f == 0.5. */
+static float pow2_ceil(float s)
+{
+    if (!(s >= FLT_MIN)) return FLT_MIN;
+    if (isinf(s)) return s;
+    int e;
+    double f = frexp((double)s, &e);
+    if (f == 0.5) return s;
+    return (float)ldexp(1.0, e); /* +inf if e == 128 */
+}
+
+/* exp(t) in fp32, fully specified by its sequence of IEEE fp32 operations
+ * (no library exp): the range reduction of Cody and Waite ("Software Manual
+ * for the Elementary Functions", 1980), done with fused multiply-adds,
+ *   n = rint(RN(t * log2 e)),  r = t - n*ln2_hi - n*ln2_lo  (two FMAs),
+ * where ln2_hi is ln 2 rounded to fp32 and ln2_lo the fp32 rounding of the
+ * remainder, then exp(r) from its Taylor series to degree 7 (coefficients
+ * 1/k! rounded to fp32, Horner's rule with FMAs; |r| <= ln2/2 makes the
+ * truncation error below 1e-8 relative), times 2^n (exact).  t > 88 gives
+ * +inf; t < -32 gives 0 (then exp(t) < 2^-46 cannot change 1 + exp(t) in
+ * fp32, the only use made of it). */
+static float exp_f32(float t)
+{
+    if (t > 88.0f) return INFINITY;
+    if (t < -32.0f) return 0.0f;
+    const float log2e = 0x1.715476p+0f, ln2_hi = 0x1.62e430p-1f, ln2_lo = -0x1.05c610p-29f;
+    const float c7 = 0x1.a01a02p-13f, c6 = 0x1.6c16c2p-10f, c5 = 0x1.111112p-7f, c4 = 0x1.555556p-5f,
+                c3 = 0x1.555556p-3f, c2 = 0x1.0p-1f;
+    float prod = t * log2e;
+    float n = rintf(prod);
+    float r = fmaf(-n, ln2_hi, t);
+    r = fmaf(-n, ln2_lo, r);
+    float p = c7;
+    p = fmaf(p, r, c6);
+    p = fmaf(p, r, c5);
+    p = fmaf(p, r, c4);
+    p = fmaf(p, r, c3);
+    p = fmaf(p, r, c2);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    return p * ldexpf(1.0f, (int)n);
+}
+
+/* silu(a) * b in fp32: silu(a) = a / (1 + exp(-a)) (IEEE fp32 add and
+ * division, exp as above), then one fp32 multiply -- the fuse_silu_and_mul
+ * input of the group quantizer ([PR27896] "Key source snippets"): the
+ * quantized row is silu(gate) * up, gate the first and up the second half
+ * of the input row, with no rounding to bf16 in between. */
+static float silu_mul(float a, float b)
+{
+    float den = 1.0f + exp_f32(-a);
+    float silu = a / den;
+    return silu * b;
+}
+
+void fp8q_oracle_exp_f32_array(const float *t, float *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = exp_f32(t[i]);
+}
+
+void fp8q_oracle_silu_mul_array(const float *a, const float *b, float *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = silu_mul(a[i], b[i]);
+}
+
+void fp8q_oracle_pow2_ceil_array(const float *s, float *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = pow2_ceil(s[i]);
+}
+
+/* The row-padded per-token-group quantizer with its two options ([PR27896]
+ * "Key source snippets": the scale_ue8m0 and fuse_silu_and_mul arguments of
+ * sgl_per_token_group_quant_8bit):
+ *   silu_and_mul: x rows hold 2K values; the quantized values are
+ *                 y[k] = silu(x[k]) * x[K + k] in fp32 (silu_mul above);
+ *                 otherwise y[k] = x[k].
+ *   ue8m0:        the group scale max(amax|y|, eps) / 448 is rounded up to a
+ *                 power of two (pow2_ceil) before use.
+ * q = cast_e4m3(clamp(y / s)), y / s an fp32 division; layout as in
+ * fp8q_oracle_quant_group_row_padded (x_s[j * m_pad + r]). */
+void fp8q_oracle_quant_group_row_padded_ex(const uint16_t *x, int64_t K, int64_t ldx, int64_t g, float eps,
+                                           int ue8m0, int silu_and_mul, int64_t m_pad, uint8_t *xq,
+                                           float *xs, int64_t r0, int64_t r1)
+{
+    float *y = (float *)malloc((size_t)g * sizeof(float));
+    if (y == NULL) abort();
+    int64_t groups = K / g;
+    for (int64_t r = r0; r < r1; ++r) {
+        const uint16_t *xr = x + r * ldx;
+        for (int64_t j = 0; j < groups; ++j) {
+            float amax = 0.0f;
+            for (int64_t i = 0; i < g; ++i) {
+                int64_t k = j * g + i;
+                y[i] = silu_and_mul ? silu_mul(fp8q_oracle_bf16_to_f32(xr[k]), fp8q_oracle_bf16_to_f32(xr[K + k]))
+                                    : fp8q_oracle_bf16_to_f32(xr[k]);
+                float a = fabsf(y[i]);
+                if (a > amax) amax = a;
+            }
+            float s = (amax > eps ? amax : eps) / 448.0f;
+            if (ue8m0) s = pow2_ceil(s);
+            xs[j * m_pad + r] = s;
+            for (int64_t i = 0; i < g; ++i) {
+                float v = y[i] / s;
+                if (v > 448.0f) v = 448.0f;
+                if (v < -448.0f) v = -448.0f;
+                xq[r * K + j * g + i] = fp8q_oracle_e4m3_encode(v);
+            }
+        }
+    }
+    free(y);
 }
 
 /* ------------------------------------------------------------------------ */
