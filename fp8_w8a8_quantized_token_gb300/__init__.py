@@ -33,6 +33,8 @@ NOALLOC_MAX_CODES, NOALLOC_MAX_ROWS = 16 * 1024 * 1024, 16384
 EXPORTED = (
     "fp8q_quant_per_token",
     "fp8q_quant_per_token_group_row_padded",
+    "fp8q_quant_per_token_group_row_padded_ex",
+    "fp8q_quant_static_per_tensor",
     "fp8q_quant_weight_block128",
     "fp8q_scaled_mm_channelwise",
     "fp8q_scaled_mm_blockwise",
@@ -80,6 +82,8 @@ def load_library(path: str | None = None):
     sig = {
         "fp8q_quant_per_token": [P, I64, I64, I64, P, P, F32, P],
         "fp8q_quant_per_token_group_row_padded": [P, I64, I64, I64, I32, F32, I32, P, P, I64, P],
+        "fp8q_quant_per_token_group_row_padded_ex": [P, I64, I64, I64, I32, F32, I32, I32, P, P, I64, P],
+        "fp8q_quant_static_per_tensor": [P, I64, I64, I64, P, P, P, P],
         "fp8q_quant_weight_block128": [P, I64, I64, P, P, F32, P],
         "fp8q_scaled_mm_channelwise": [P, P, I64, P, P, P, P, I64, I64, I64, ctypes.c_int, P],
         "fp8q_scaled_mm_blockwise": [P, P, P, P, P, P, I64, I64, I64, I64, ctypes.c_int, P],
@@ -166,19 +170,31 @@ def fp8q_quant_per_token(x: torch.Tensor, eps: float = 1e-10, xq: torch.Tensor |
     return xq, x_scale
 
 
+FP8Q_QUANT_SCALE_UE8M0 = 1
+FP8Q_QUANT_SILU_AND_MUL = 2
+
+
 def fp8q_quant_per_token_group_row_padded(x: torch.Tensor, group_size: int = 128, eps: float = 1e-10,
                                           row_alignment: int = 4, xq: torch.Tensor | None = None,
-                                          x_scale_storage: torch.Tensor | None = None):
+                                          x_scale_storage: torch.Tensor | None = None,
+                                          scale_ue8m0: bool = False, fuse_silu_and_mul: bool = False):
     """bf16 [M, K] -> (x_q e4m3 [m_pad, K], x_s fp32 (m_pad, K/g) column-major view).
 
     As on the row-padding page: m_pad = ceil_align(M, row_alignment), x_s is a
     (K/g, m_pad) allocation viewed transposed (stride(0) == 1); rows >= M of
-    both buffers are left as allocated (never written)."""
+    both buffers are left as allocated (never written).  scale_ue8m0 rounds
+    every scale up to a power of two; fuse_silu_and_mul takes x as [M, 2K]
+    and quantizes silu(x[:, :K]) * x[:, K:] (computed in fp32)."""
     L = load_library()
     _need(x, torch.bfloat16, "x")
     if x.dim() != 2 or x.stride(1) != 1:
         raise ValueError("x must be 2-D with contiguous rows")
     M, K = x.shape
+    if fuse_silu_and_mul:
+        if K % 2 != 0:
+            raise ValueError("fuse_silu_and_mul needs an even last dimension (gate, up)")
+        K //= 2
+    flags = (FP8Q_QUANT_SCALE_UE8M0 if scale_ue8m0 else 0) | (FP8Q_QUANT_SILU_AND_MUL if fuse_silu_and_mul else 0)
     if K % group_size != 0:
         raise ValueError("the last dimension of x must be divisible by group_size")
     m_pad = ceil_align(M, row_alignment)
@@ -193,10 +209,41 @@ def fp8q_quant_per_token_group_row_padded(x: torch.Tensor, group_size: int = 128
         raise ValueError("xq must be a contiguous [m_pad, K] buffer")
     if tuple(x_scale_storage.shape) != (K // group_size, m_pad) or not x_scale_storage.is_contiguous():
         raise ValueError("x_scale_storage must be a contiguous [K/g, m_pad] buffer")
-    _check("fp8q_quant_per_token_group_row_padded",
-           L.fp8q_quant_per_token_group_row_padded(_ptr(x), M, K, x.stride(0), group_size, eps, row_alignment,
-                                                   _ptr(xq), _ptr(x_scale_storage), m_pad, _stream(x.device)))
+    if flags == 0:
+        _check("fp8q_quant_per_token_group_row_padded",
+               L.fp8q_quant_per_token_group_row_padded(_ptr(x), M, K, x.stride(0), group_size, eps, row_alignment,
+                                                       _ptr(xq), _ptr(x_scale_storage), m_pad, _stream(x.device)))
+    else:
+        _check("fp8q_quant_per_token_group_row_padded_ex",
+               L.fp8q_quant_per_token_group_row_padded_ex(_ptr(x), M, K, x.stride(0), group_size, eps,
+                                                          row_alignment, flags, _ptr(xq), _ptr(x_scale_storage),
+                                                          m_pad, _stream(x.device)))
     return xq, x_scale_storage.transpose(0, 1)
+
+
+def fp8q_quant_static_per_tensor(x: torch.Tensor, scale: torch.Tensor, xq: torch.Tensor | None = None,
+                                 repeat_scale: bool = False):
+    """Static per-tensor quantization: bf16 [M, K] and a one-element fp32
+    device tensor s -> (x_q e4m3 [M, K], the scale repeated to fp32 [M] if
+    repeat_scale else None).  x_q = e4m3(x / s), saturating."""
+    L = load_library()
+    _need(x, torch.bfloat16, "x")
+    _need(scale, torch.float32, "scale", x.device)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with contiguous rows")
+    if scale.numel() != 1:
+        raise ValueError("scale must hold exactly one value")
+    M, K = x.shape
+    if xq is None:
+        xq = torch.empty((M, K), dtype=E4M3, device=x.device)
+    _need(xq, E4M3, "xq", x.device)
+    if tuple(xq.shape) != (M, K) or not xq.is_contiguous():
+        raise ValueError("xq must be a contiguous [M, K] buffer")
+    rep = torch.empty(M, dtype=torch.float32, device=x.device) if repeat_scale else None
+    _check("fp8q_quant_static_per_tensor",
+           L.fp8q_quant_static_per_tensor(_ptr(x), M, K, x.stride(0), _ptr(scale), _ptr(xq),
+                                          None if rep is None else _ptr(rep), _stream(x.device)))
+    return xq, rep
 
 
 def fp8q_quant_weight_block128(w: torch.Tensor, eps: float = 1e-10):

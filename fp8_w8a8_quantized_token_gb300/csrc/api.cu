@@ -91,6 +91,45 @@ fp8q_status fp8q_quant_per_token_group_row_padded(const void *x, int64_t M, int6
     return from_cuda(e);
 }
 
+fp8q_status fp8q_quant_per_token_group_row_padded_ex(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                                     int32_t group_size, float eps, int32_t row_alignment,
+                                                     int32_t flags, void *xq, float *x_scale, int64_t m_pad,
+                                                     void *stream)
+{
+    if ((flags & ~(FP8Q_QUANT_SCALE_UE8M0 | FP8Q_QUANT_SILU_AND_MUL)) != 0) return FP8Q_ERR_INVALID_ARG;
+    const bool silu = (flags & FP8Q_QUANT_SILU_AND_MUL) != 0;
+    if (group_size != 16 && group_size != 32 && group_size != 64 && group_size != 128) {
+        if (group_size <= 0) return FP8Q_ERR_INVALID_ARG;
+        return FP8Q_ERR_UNSUPPORTED;
+    }
+    if (row_alignment <= 0 || m_pad < M || m_pad % row_alignment != 0 || m_pad > kMaxDim)
+        return FP8Q_ERR_INVALID_ARG;
+    if (K > 0 && K % group_size != 0) return FP8Q_ERR_INVALID_ARG;
+    // The fused input row holds 2K values (gate, then up).
+    if (silu && (K > kMaxDim / 2 || ldx < 2 * K)) return FP8Q_ERR_INVALID_ARG;
+    const fp8q_status s = check_quant_common(x, M, K, ldx, xq, x_scale, eps);
+    if (s != FP8Q_OK || M == 0) return s;
+    const cudaError_t e = launch_quant_group(x, M, K, ldx, group_size, xq, x_scale, m_pad, eps, current_device_sms(),
+                                             as_stream(stream), (flags & FP8Q_QUANT_SCALE_UE8M0) != 0, silu);
+    if (e == cudaSuccess) note_launch_writes(as_stream(stream), xq, static_cast<size_t>(M) * K);
+    return from_cuda(e);
+}
+
+fp8q_status fp8q_quant_static_per_tensor(const void *x, int64_t M, int64_t K, int64_t ldx, const float *scale,
+                                         void *xq, float *x_scale_rep, void *stream)
+{
+    if (M < 0 || K <= 0 || M > kMaxDim || K > kMaxDim) return FP8Q_ERR_INVALID_ARG;
+    if (K % 16 != 0 || ldx < K || ldx % 8 != 0) return FP8Q_ERR_INVALID_ARG;
+    if (M == 0) return FP8Q_OK;
+    if (x == nullptr || xq == nullptr || scale == nullptr) return FP8Q_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xq) || !aligned4(scale) || !aligned4(x_scale_rep))
+        return FP8Q_ERR_INVALID_ARG;
+    const cudaError_t e = launch_quant_static(x, M, K, ldx, scale, xq, x_scale_rep, current_device_sms(),
+                                              as_stream(stream));
+    if (e == cudaSuccess) note_launch_writes(as_stream(stream), xq, static_cast<size_t>(M) * K);
+    return from_cuda(e);
+}
+
 fp8q_status fp8q_quant_weight_block128(const void *w, int64_t N, int64_t K, void *wq, float *w_scale, float eps,
                                        void *stream)
 {

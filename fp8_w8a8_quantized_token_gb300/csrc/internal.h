@@ -12,7 +12,10 @@ namespace fp8q {
 cudaError_t launch_quant_per_token(const void *x, int64_t M, int64_t K, int64_t ldx, void *xq, float *xs, float eps,
                                    cudaStream_t st);
 cudaError_t launch_quant_group(const void *x, int64_t M, int64_t K, int64_t ldx, int group, void *xq, float *xs,
-                               int64_t m_pad, float eps, int num_sms, cudaStream_t st);
+                               int64_t m_pad, float eps, int num_sms, cudaStream_t st, bool ue8m0 = false,
+                               bool silu_and_mul = false);
+cudaError_t launch_quant_static(const void *x, int64_t M, int64_t K, int64_t ldx, const float *scale, void *xq,
+                                float *xs_rep, int num_sms, cudaStream_t st);
 cudaError_t launch_quant_weight_block128(const void *w, int64_t N, int64_t K, void *wq, float *ws, float eps,
                                          cudaStream_t st);
 

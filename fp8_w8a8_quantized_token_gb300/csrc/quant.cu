@@ -109,6 +109,56 @@ __device__ __forceinline__ uint4 quant_chunk(const Chunk16 &c, float s)
 
 __device__ __forceinline__ float scale_of(float amax, float eps) { return fmaxf(amax, eps) / 448.0f; }
 
+// The scale rounded up to a power of two (an exact 8-bit exponent, UE8M0:
+// the scale_ue8m0 option of the group quantizer on the row-padding page,
+// key source snippets): clear the fp32 mantissa and, if it was not zero,
+// step the exponent up; zero and subnormal scales become 2^-126, the
+// smallest normal power of two; +inf stays.
+__device__ __forceinline__ float pow2_ceil(float s)
+{
+    uint32_t b = __float_as_uint(s);
+    if (b < 0x00800000u) return __uint_as_float(0x00800000u);
+    if (b & 0x007FFFFFu) b = (b & 0x7F800000u) + 0x00800000u;
+    return __uint_as_float(b);
+}
+
+// exp(t) in fp32 as a fixed sequence of IEEE fp32 operations (no library
+// exp): Cody and Waite's range reduction (W. J. Cody, W. Waite, "Software
+// Manual for the Elementary Functions", 1980) with fused multiply-adds --
+// n = rint(t * log2 e), r = t - n*ln2_hi - n*ln2_lo, ln2_hi = ln 2 rounded
+// to fp32 and ln2_lo the fp32 rounding of the rest -- then the Taylor
+// series of exp(r) to degree 7 (coefficients 1/k! rounded to fp32, Horner's
+// rule with FMAs) and the exact scaling by 2^n.  t > 88: +inf; t < -32: 0
+// (exp(t) < 2^-46 cannot change 1 + exp(t), its only use).  Explicit
+// __f*_rn intrinsics keep the compiler from contracting or reordering.
+__device__ __forceinline__ float exp_fixed(float t)
+{
+    if (t > 88.0f) return __uint_as_float(0x7F800000u);
+    if (t < -32.0f) return 0.0f;
+    const float n = rintf(__fmul_rn(t, 0x1.715476p+0f));
+    float r = __fmaf_rn(-n, 0x1.62e430p-1f, t);
+    r = __fmaf_rn(-n, -0x1.05c610p-29f, r);
+    float p = 0x1.a01a02p-13f;
+    p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);
+    p = __fmaf_rn(p, r, 0x1.111112p-7f);
+    p = __fmaf_rn(p, r, 0x1.555556p-5f);
+    p = __fmaf_rn(p, r, 0x1.555556p-3f);
+    p = __fmaf_rn(p, r, 0.5f);
+    p = __fmaf_rn(p, r, 1.0f);
+    p = __fmaf_rn(p, r, 1.0f);
+    return __fmul_rn(p, __int_as_float((static_cast<int>(n) + 127) << 23));
+}
+
+// silu(a) * b in fp32: a / (1 + exp(-a)) (IEEE add and division), times b
+// -- the fuse_silu_and_mul input of the group quantizer (row-padding page,
+// key source snippets): gate a from the first half of the row, up b from
+// the second, no rounding to bf16 in between.
+__device__ __forceinline__ float silu_mul(float a, float b)
+{
+    const float den = __fadd_rn(1.0f, exp_fixed(-a));
+    return __fmul_rn(__fdiv_rn(a, den), b);
+}
+
 // Programmatic dependent launch: each quantizer first waits for the
 // previous kernel in the stream (so every earlier kernel has completed), then
 // lets the next kernel launch.  When any kernel of this library starts, at
@@ -198,7 +248,15 @@ __global__ void __launch_bounds__(1024) quant_per_token_two_pass_kernel(const __
 // left to right, so loads and stores are fully coalesced; the scale of
 // (row r, group j) goes to xs[j * m_pad + r].
 // ---------------------------------------------------------------------------
-template <int TPG>
+//
+// Options (the scale_ue8m0 and fuse_silu_and_mul arguments of the group
+// quantizer on the row-padding page): UE8M0 rounds each scale up to a power
+// of two; SILU reads rows of 2K values and quantizes y = silu(x[k]) *
+// x[K + k] (fp32), dividing with the IEEE division (y is a general fp32
+// value, outside the bf16 numerators the quotient() shortcut is checked
+// for).
+// ---------------------------------------------------------------------------
+template <int TPG, bool UE8M0, bool SILU>
 __global__ void __launch_bounds__(256) quant_group_kernel(const __nv_bfloat16 *__restrict__ x, int64_t ldx,
                                                           uint8_t *__restrict__ xq, float *__restrict__ xs,
                                                           int64_t M, int K, int64_t m_pad, float eps)
@@ -213,18 +271,66 @@ __global__ void __launch_bounds__(256) quant_group_kernel(const __nv_bfloat16 *_
         const int64_t row = active ? t / chunks_per_row : 0;
         const int ci = active ? static_cast<int>(t - row * chunks_per_row) : 0;
         Chunk16 c;
+        float y[SILU ? 16 : 1];
         float m = 0.0f;
         if (active) {
             c = load_chunk(x + row * ldx + (ci << 4));
-            m = chunk_amax(c, 0.0f);
+            if constexpr (SILU) {
+                const Chunk16 u = load_chunk(x + row * ldx + K + (ci << 4));
+                const uint32_t gw[8] = {c.lo.x, c.lo.y, c.lo.z, c.lo.w, c.hi.x, c.hi.y, c.hi.z, c.hi.w};
+                const uint32_t uw[8] = {u.lo.x, u.lo.y, u.lo.z, u.lo.w, u.hi.x, u.hi.y, u.hi.z, u.hi.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    y[2 * i] = silu_mul(bf_lo(gw[i]), bf_lo(uw[i]));
+                    y[2 * i + 1] = silu_mul(bf_hi(gw[i]), bf_hi(uw[i]));
+                    m = fmaxf(m, fmaxf(fabsf(y[2 * i]), fabsf(y[2 * i + 1])));
+                }
+            } else {
+                m = chunk_amax(c, 0.0f);
+            }
         }
 #pragma unroll
         for (int o = TPG >> 1; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (active) {
-            const float s = scale_of(m, eps);
-            *reinterpret_cast<uint4 *>(xq + row * static_cast<int64_t>(K) + (ci << 4)) = quant_chunk(c, s);
+            float s = scale_of(m, eps);
+            if (UE8M0) s = pow2_ceil(s);
+            uint4 q;
+            if constexpr (SILU) {
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    w[i] = cvt_e4m3x2(__fdiv_rn(y[4 * i], s), __fdiv_rn(y[4 * i + 1], s)) |
+                           (cvt_e4m3x2(__fdiv_rn(y[4 * i + 2], s), __fdiv_rn(y[4 * i + 3], s)) << 16);
+                q = make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
+                q = quant_chunk(c, s);
+            }
+            *reinterpret_cast<uint4 *>(xq + row * static_cast<int64_t>(K) + (ci << 4)) = q;
             if ((ci & (TPG - 1)) == 0) xs[static_cast<int64_t>(ci / TPG) * m_pad + row] = s;
         }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Static per-tensor quantization (one precomputed scale, read from device
+// memory): a grid-stride stream over the 16-element chunks of x; the first
+// chunk of each row also writes the repeated per-token scale if asked.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) quant_static_kernel(const __nv_bfloat16 *__restrict__ x, int64_t ldx,
+                                                           uint8_t *__restrict__ xq, const float *__restrict__ scale,
+                                                           float *__restrict__ xs_rep, int64_t M, int K)
+{
+    pdl_enter();
+    const float s = __ldg(scale);
+    const int chunks_per_row = K >> 4;
+    const int64_t total = M * chunks_per_row;
+    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total;
+         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t row = t / chunks_per_row;
+        const int ci = static_cast<int>(t - row * chunks_per_row);
+        *reinterpret_cast<uint4 *>(xq + row * static_cast<int64_t>(K) + (ci << 4)) =
+            quant_chunk(load_chunk(x + row * ldx + (ci << 4)), s);
+        if (xs_rep != nullptr && ci == 0) xs_rep[row] = s;
     }
 }
 
@@ -317,24 +423,53 @@ cudaError_t launch_quant_per_token(const void *x, int64_t M, int64_t K, int64_t 
     }
 }
 
-cudaError_t launch_quant_group(const void *x, int64_t M, int64_t K, int64_t ldx, int group, void *xq, float *xs,
-                               int64_t m_pad, float eps, int num_sms, cudaStream_t st)
+namespace {
+
+// Grid of a grid-stride quantizer over M * K / 16 chunks (256 threads).
+dim3 stream_grid(int64_t M, int64_t K, int num_sms)
 {
     const int64_t total = M * (K >> 4);
-    const int threads = 256;
-    int64_t blocks = (total + threads - 1) / threads;
+    int64_t blocks = (total + 255) / 256;
     const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 148) * 64;
     if (blocks > cap) blocks = cap;
+    return dim3(static_cast<unsigned>(blocks));
+}
+
+template <bool UE8M0, bool SILU>
+cudaError_t launch_group(const void *x, int64_t M, int64_t K, int64_t ldx, int group, void *xq, float *xs,
+                         int64_t m_pad, float eps, int num_sms, cudaStream_t st)
+{
     const auto *xb = static_cast<const __nv_bfloat16 *>(x);
     auto *q = static_cast<uint8_t *>(xq);
-    const dim3 g(static_cast<unsigned>(blocks)), b(threads);
+    const dim3 g = stream_grid(M, K, num_sms), b(256);
     const int k = static_cast<int>(K);
     switch (group) {
-        case 16: return launch_pdl(quant_group_kernel<1>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps);
-        case 32: return launch_pdl(quant_group_kernel<2>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps);
-        case 64: return launch_pdl(quant_group_kernel<4>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps);
-        default: return launch_pdl(quant_group_kernel<8>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps);
+        case 16: return launch_pdl(quant_group_kernel<1, UE8M0, SILU>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps);
+        case 32: return launch_pdl(quant_group_kernel<2, UE8M0, SILU>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps);
+        case 64: return launch_pdl(quant_group_kernel<4, UE8M0, SILU>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps);
+        default: return launch_pdl(quant_group_kernel<8, UE8M0, SILU>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps);
     }
+}
+
+}  // namespace
+
+cudaError_t launch_quant_group(const void *x, int64_t M, int64_t K, int64_t ldx, int group, void *xq, float *xs,
+                               int64_t m_pad, float eps, int num_sms, cudaStream_t st, bool ue8m0,
+                               bool silu_and_mul)
+{
+    if (silu_and_mul)
+        return ue8m0 ? launch_group<true, true>(x, M, K, ldx, group, xq, xs, m_pad, eps, num_sms, st)
+                     : launch_group<false, true>(x, M, K, ldx, group, xq, xs, m_pad, eps, num_sms, st);
+    return ue8m0 ? launch_group<true, false>(x, M, K, ldx, group, xq, xs, m_pad, eps, num_sms, st)
+                 : launch_group<false, false>(x, M, K, ldx, group, xq, xs, m_pad, eps, num_sms, st);
+}
+
+cudaError_t launch_quant_static(const void *x, int64_t M, int64_t K, int64_t ldx, const float *scale, void *xq,
+                                float *xs_rep, int num_sms, cudaStream_t st)
+{
+    return launch_pdl(quant_static_kernel, stream_grid(M, K, num_sms), dim3(256), st,
+                      static_cast<const __nv_bfloat16 *>(x), ldx, static_cast<uint8_t *>(xq), scale, xs_rep, M,
+                      static_cast<int>(K));
 }
 
 cudaError_t launch_quant_weight_block128(const void *w, int64_t N, int64_t K, void *wq, float *ws, float eps,

@@ -129,6 +129,54 @@ FP8Q_API fp8q_status fp8q_quant_per_token_group_row_padded(const void *x, int64_
                                                   float *x_scale, int64_t m_pad, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * fp8q_quant_per_token_group_row_padded_ex -- the group quantizer above
+ * with the two options its kernel takes in [PR27896] "Key source snippets"
+ * (the scale_ue8m0 and fuse_silu_and_mul arguments, passed as False
+ * there); `flags` is a bitwise OR of:
+ *   FP8Q_QUANT_SCALE_UE8M0  each group scale max(amax, eps) / 448 is
+ *       rounded up to a power of two before use (an exact 8-bit exponent):
+ *       the smallest normal fp32 power of two >= the scale (2^-126 for
+ *       smaller scales).  x / s is then exact before the E4M3 rounding.
+ *   FP8Q_QUANT_SILU_AND_MUL  x is bf16 [M, 2K] (row stride ldx >= 2K): the
+ *       quantized values are y[m,k] = silu(x[m,k]) * x[m,K+k], computed in
+ *       fp32 with no rounding in between, silu(a) = a / (1 + exp(-a)) with
+ *       IEEE fp32 add and division and exp the library's fixed fp32
+ *       sequence (Cody-Waite reduction with FMAs, degree-7 Taylor series,
+ *       within 2 ulp of exp; exp(t) = +inf for t > 88 and 0 for t < -32).
+ *       The amax, scale and y / s (IEEE division) follow as above; xq is
+ *       [m_pad, K].
+ * flags == 0 is exactly fp8q_quant_per_token_group_row_padded.
+ * Errors     : as above; INVALID_ARG for unknown flag bits or, with
+ *              SILU_AND_MUL, ldx < 2K.
+ * ------------------------------------------------------------------------- */
+#define FP8Q_QUANT_SCALE_UE8M0 1
+#define FP8Q_QUANT_SILU_AND_MUL 2
+FP8Q_API fp8q_status fp8q_quant_per_token_group_row_padded_ex(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                                     int32_t group_size, float eps,
+                                                     int32_t row_alignment, int32_t flags, void *xq,
+                                                     float *x_scale, int64_t m_pad, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * fp8q_quant_static_per_tensor -- static per-tensor quantization with one
+ * precomputed scale (the _static_quant_fp8 kernel named in [PR31340]
+ * "Implementation breakdown"):
+ *   xq[m,k] = e4m3_rne_satfinite(x[m,k] / s)        (fp32 quotient)
+ *   x_scale_rep[m] = s  for m < M, if x_scale_rep != NULL (the per-token
+ *   scale vector fp8q_scaled_mm_channelwise takes).
+ * x           : bf16 [M, K], row stride ldx >= K (ldx % 8 == 0), 16-byte aligned.
+ * scale       : DEVICE pointer to one fp32 s, read by the kernel (so it may be
+ *               produced by an earlier kernel on the stream); s must be > 0
+ *               and finite -- other values give unspecified codes, no error.
+ * xq          : e4m3 [M, K], row stride K (K % 16 == 0), 16-byte aligned.
+ * x_scale_rep : fp32 [M] or NULL.
+ * Errors      : INVALID_ARG for M < 0, K <= 0, K % 16, ldx < K, ldx % 8,
+ *               null or misaligned pointers.
+ * ------------------------------------------------------------------------- */
+FP8Q_API fp8q_status fp8q_quant_static_per_tensor(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                         const float *scale, void *xq, float *x_scale_rep,
+                                         void *stream);
+
+/* ---------------------------------------------------------------------------
  * fp8q_quant_weight_block128 -- weight preparation for the blockwise GEMM
  * (one fp32 scale per 128 x 128 block, same scale and cast rule as the
  * activations).  Not on the per-call hot path: weights are quantized once.
