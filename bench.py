@@ -465,6 +465,51 @@ def main():
     roof["share_of_step"] = round(dom["us"] / (quant_total + gemm_total), 3)
     roof["peak_source"] = peaks["source"]
 
+    # ---- quantizer variants (static per-tensor; group-128 with power-of-two
+    # scales; silu_and_mul-fused group-128) at a decode and a prefill size
+    # (the prefill inputs and outputs exceed L2): 8 back-to-back launches per
+    # graph, algorithmic bytes (bf16 in, e4m3 + fp32 scales out) over the
+    # CUDA-event duration, against the HBM peak.
+    variants = []
+    vK, vKm = 4096, 12288          # hidden size; MLP intermediate (silu input 2 x 12288)
+    s_dev = torch.tensor([0.02], dtype=torch.float32, device=dev)
+    for vM in (16, 16384):
+        xv = synthetic.activations(vM, vK, outliers=True).to(dev)
+        xm = synthetic.activations(vM, 2 * vKm, outliers=True).to(dev)
+        m_pad = (vM + 3) // 4 * 4
+        q_s = torch.empty((vM, vK), dtype=fq.E4M3, device=dev)
+        rep = torch.empty(vM, dtype=torch.float32, device=dev)
+        q_g = torch.empty((m_pad, vK), dtype=fq.E4M3, device=dev)
+        s_g = torch.empty((vK // 128, m_pad), dtype=torch.float32, device=dev)
+        q_m = torch.empty((m_pad, vKm), dtype=fq.E4M3, device=dev)
+        s_m = torch.empty((vKm // 128, m_pad), dtype=torch.float32, device=dev)
+        cases = [
+            ("static_per_tensor", vK, vM * vK * 3 + vM * 4,
+             lambda sp: L.fp8q_quant_static_per_tensor(P(xv.data_ptr()), vM, vK, vK, P(s_dev.data_ptr()),
+                                                        P(q_s.data_ptr()), P(rep.data_ptr()), sp)),
+            ("group128_ue8m0", vK, vM * vK * 3 + vM * (vK // 128) * 4,
+             lambda sp: L.fp8q_quant_per_token_group_row_padded_ex(P(xv.data_ptr()), vM, vK, vK, 128, 1e-10, 4, 1,
+                                                                   P(q_g.data_ptr()), P(s_g.data_ptr()), m_pad, sp)),
+            ("silu_mul_group128", vKm, vM * vKm * 5 + vM * (vKm // 128) * 4,
+             lambda sp: L.fp8q_quant_per_token_group_row_padded_ex(P(xm.data_ptr()), vM, vKm, 2 * vKm, 128, 1e-10,
+                                                                   4, 2, P(q_m.data_ptr()), P(s_m.data_ptr()),
+                                                                   m_pad, sp)),
+            ("silu_mul_group128_ue8m0", vKm, vM * vKm * 5 + vM * (vKm // 128) * 4,
+             lambda sp: L.fp8q_quant_per_token_group_row_padded_ex(P(xm.data_ptr()), vM, vKm, 2 * vKm, 128, 1e-10,
+                                                                   4, 3, P(q_m.data_ptr()), P(s_m.data_ptr()),
+                                                                   m_pad, sp)),
+        ]
+        for name, kk, nbytes, fn in cases:
+            def body_v(st, fn=fn):
+                for _ in range(reps):
+                    if fn(P(st.cuda_stream)) != 0:
+                        raise RuntimeError(f"{name} failed")
+            us = time_graph(body_v, reps)
+            gbs = nbytes / (us * 1e-6) / 1e9
+            variants.append({"kernel": name, "M": vM, "K": kk, "us": round(us, 3), "gbs": round(gbs, 1),
+                             "hbm_frac": round(gbs / peaks["hbm_gbs"], 3)})
+        del xv, xm
+
     # ---- end to end through the C ABI with host buffers --------------------
     h2d = sum(p["x"].numel() * 2 for p in problems)
     d2h = sum(p["out"].numel() * 2 for p in problems)
@@ -520,7 +565,7 @@ def main():
                           "8 back-to-back launches of each problem's kernel (GEMMs over rotating weight copies)",
                 "clocks": clk.summary(),
                 "kernel_time_us": {"quant": round(quant_total, 2), "gemm": round(gemm_total, 2)},
-                "sweep": sweep}
+                "sweep": sweep, "quant_variants": variants}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

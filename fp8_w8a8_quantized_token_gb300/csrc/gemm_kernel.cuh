@@ -107,14 +107,17 @@ struct GemmCfg {
     static constexpr int kEpiWarps = BN > 128 ? 8 : 4;
     static constexpr int kColGroups = kEpiWarps / 4;
     static constexpr int kCols = BN / kColGroups;  // TMEM columns per epilogue thread
-    // MMA-issuing warps.  A tcgen05.mma occupies its issuing thread for
-    // about 140 cycles whatever its N, while the tensor pipe completes a
-    // 128 x N x 32 MMA in about N/256 of that: channelwise tiles narrower
-    // than 256 columns spread each K block's four MMAs over 2 warps, each
-    // accumulating into its own TMEM columns; the epilogue adds the two
-    // accumulators.  (More issuers would add warps: 2 CTAs of 7 warps still
-    // fit one SM's register file, which lets the next launch's CTAs load
-    // their weights while this launch's CTAs finish.)
+    // MMA-issuing warps.  Measured on GB300: one issuing thread completes a
+    // 128 x N x 32 MMA chain no faster than about one MMA per 27 ns whatever
+    // N (up to 64), while the tensor pipe needs only about N/256 of 66 ns
+    // for it; a second issuing warp with its own accumulator overlaps the
+    // first (about 1.4x at N = 16; no gain at N >= 128, where the pipe is
+    // the limit).  Channelwise tiles narrower than 256 columns therefore
+    // spread each K block's four MMAs over 2 warps, each accumulating into
+    // its own TMEM columns; the epilogue adds the two accumulators.  (More
+    // issuers would add warps: 2 CTAs of 7 warps still fit one SM's register
+    // file, which lets the next launch's CTAs load their weights while this
+    // launch's CTAs finish.)
     static constexpr int kIssuers = (BLOCKWISE || TWO_SM || BN >= 256) ? 1 : 2;
     static constexpr int kSlotCols = kIssuers * BN;  // TMEM columns per accumulator slot
     static constexpr int kEpiWarp0 = 1 + kIssuers;   // first epilogue warp

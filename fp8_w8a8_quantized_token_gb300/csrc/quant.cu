@@ -64,8 +64,9 @@ __device__ __forceinline__ float chunk_amax(const Chunk16 &c, float m)
 // of x and every fp32 significand of s (2^30 pairs, at several exponent
 // offsets): no difference.  The result carries the sign of x, as x / s
 // does for s > 0 (this keeps -0 for x = -0).  The kernels use it only for
-// finite s (quant_chunk); where the quotient would be subnormal in fp32,
-// x / s is below 2^-11 and both round to a signed zero in E4M3.
+// normal finite s (the reciprocal is then a normal number); where the
+// quotient would be subnormal in fp32, x / s is below 2^-11 and both round
+// to a signed zero in E4M3.
 __device__ __forceinline__ float quotient(float x, float s, float r)
 {
     const float q0 = x * r;
@@ -91,14 +92,16 @@ __device__ __forceinline__ uint32_t quant4_div(uint32_t w0, uint32_t w1, float s
 __device__ __forceinline__ uint4 quant_chunk(const Chunk16 &c, float s)
 {
     uint4 q;
-    if (s <= 3.0e38f) {
+    if (s >= 0x1p-126f && s <= 3.0e38f) {
         const float r = 1.0f / s;
         q.x = quant4(c.lo.x, c.lo.y, s, r);
         q.y = quant4(c.lo.z, c.lo.w, s, r);
         q.z = quant4(c.hi.x, c.hi.y, s, r);
         q.w = quant4(c.hi.z, c.hi.w, s, r);
     } else {
-        // Infinite scale (an infinite input): x / inf = +-0, inf / inf = NaN.
+        // Infinite scale (an infinite input): x / inf = +-0, inf / inf = NaN;
+        // a zero or subnormal scale (an eps below 448 * 2^-126): the IEEE
+        // division as well (its reciprocal would overflow).
         q.x = quant4_div(c.lo.x, c.lo.y, s);
         q.y = quant4_div(c.lo.z, c.lo.w, s);
         q.z = quant4_div(c.hi.x, c.hi.y, s);
@@ -254,7 +257,8 @@ __global__ void __launch_bounds__(1024) quant_per_token_two_pass_kernel(const __
 // of two; SILU reads rows of 2K values and quantizes y = silu(x[k]) *
 // x[K + k] (fp32), dividing with the IEEE division (y is a general fp32
 // value, outside the bf16 numerators the quotient() shortcut is checked
-// for).
+// for; measured, the shortcut does not speed this kernel up: it is bound by
+// the ~38 fp32 instructions per element of exp, silu and quantization).
 // ---------------------------------------------------------------------------
 template <int TPG, bool UE8M0, bool SILU>
 __global__ void __launch_bounds__(256) quant_group_kernel(const __nv_bfloat16 *__restrict__ x, int64_t ldx,

@@ -163,3 +163,19 @@ def test_weight_per_channel_quant_is_per_token_quant_of_rows(dev):
     torch.cuda.synchronize()
     rq, rs = oracle.quant_weight_per_channel(w)
     assert np.array_equal(u8(wq), rq) and np.array_equal(ws.cpu().numpy(), rs)
+
+
+def test_tiny_eps_zero_and_subnormal_scales(dev):
+    """eps so small that max(amax, eps) / 448 is zero or subnormal in fp32:
+    the kernels divide with the IEEE division there, as the oracle does."""
+    x = torch.zeros((4, 256), dtype=torch.float32)
+    x[1, 7] = 1e-40                    # subnormal scale
+    x[2, :3] = torch.tensor([3e-39, -2e-38, 5e-40])
+    x[3] = torch.linspace(-1, 1, 256)
+    x = x.to(torch.bfloat16)
+    for eps in (1e-44, 1e-41):
+        q, s = fq.fp8q_quant_per_token(x.to(dev), eps=eps)
+        torch.cuda.synchronize()
+        rq, rs = oracle.quant_per_token(x, eps=eps)
+        assert np.array_equal(u8(q), rq)
+        assert np.array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
