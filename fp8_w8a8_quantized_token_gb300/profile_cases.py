@@ -31,6 +31,8 @@ CASES = {
     "blockwise_decode": ("blockwise", 16, 4096, 7168),
     "quant_token": ("quant_token", 8192, 0, 4096),
     "quant_group": ("quant_group", 8192, 0, 12288),
+    "quant_silu_group": ("quant_silu_group", 4096, 0, 12288),   # input [4096, 2 x 12288]
+    "quant_static": ("quant_static", 16384, 0, 4096),
 }
 
 
@@ -44,6 +46,16 @@ def run(case: str, dev) -> None:
     if kind == "quant_group":
         for _ in range(WARMUP + 1):
             fq.fp8q_quant_per_token_group_row_padded(x, 128)
+        return
+    if kind == "quant_silu_group":
+        xm = synthetic.activations(M, 2 * K, outliers=True).to(dev)
+        for _ in range(WARMUP + 1):
+            fq.fp8q_quant_per_token_group_row_padded(xm, 128, scale_ue8m0=True, fuse_silu_and_mul=True)
+        return
+    if kind == "quant_static":
+        s = torch.tensor([0.02], dtype=torch.float32, device=dev)
+        for _ in range(WARMUP + 1):
+            fq.fp8q_quant_static_per_tensor(x, s)
         return
     w = synthetic.weights(N, K).to(dev)
     if kind == "channelwise":
