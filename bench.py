@@ -510,6 +510,44 @@ def main():
                              "hbm_frac": round(gbs / peaks["hbm_gbs"], 3)})
         del xv, xm
 
+    # ---- quantization fused into the blockwise GEMM (one kernel) against the
+    # two-kernel blockwise linear, at decode sizes of the blockwise decode
+    # layer (N = 4096, K = 7168): 8 back-to-back launches per graph over
+    # rotating weight copies (> L2), CUDA events.
+    fused = []
+    fN, fK = 4096, 7168
+    fw = synthetic.weights(fN, fK).to(dev)
+    fwq0, fws = fq.fp8q_quant_weight_block128(fw)
+    del fw
+    fcopies = [fwq0] + [fwq0.clone() for _ in range(reps - 1)]
+    for fM in (1, 16):
+        fx = synthetic.activations(fM, fK, outliers=True).to(dev)
+        fm_pad = (fM + 3) // 4 * 4
+        fxq = torch.empty((fm_pad, fK), dtype=fq.E4M3, device=dev)
+        fxs = torch.empty((fK // 128, fm_pad), dtype=torch.float32, device=dev)
+        fout = torch.empty((fM, fN), dtype=torch.bfloat16, device=dev)
+
+        def body_fused(st, fx=fx, fM=fM, fout=fout):
+            for r in range(reps):
+                if L.fp8q_linear_blockwise_fused(P(fx.data_ptr()), fK, P(fcopies[r].data_ptr()), P(fws.data_ptr()),
+                                                 None, P(fout.data_ptr()), fM, fN, fK, 0, P(st.cuda_stream)) != 0:
+                    raise RuntimeError("fused linear failed")
+
+        def body_two(st, fx=fx, fM=fM, fout=fout, fxq=fxq, fxs=fxs, fm_pad=fm_pad):
+            for r in range(reps):
+                if L.fp8q_linear_blockwise(P(fx.data_ptr()), P(fcopies[r].data_ptr()), P(fws.data_ptr()), None,
+                                           P(fout.data_ptr()), fM, fN, fK, P(fxq.data_ptr()), P(fxs.data_ptr()),
+                                           fm_pad, 0, P(st.cuda_stream)) != 0:
+                    raise RuntimeError("linear failed")
+
+        fu = time_graph(body_fused, reps)
+        tu = time_graph(body_two, reps)
+        fb = gemm_bytes(fM, fN, fK, True)
+        fused.append({"M": fM, "N": fN, "K": fK, "fused_us": round(fu, 3), "two_kernel_us": round(tu, 3),
+                      "fused_hbm_frac": round(fb / (fu * 1e-6) / 1e9 / peaks["hbm_gbs"], 3),
+                      "two_kernel_hbm_frac": round(fb / (tu * 1e-6) / 1e9 / peaks["hbm_gbs"], 3)})
+    del fcopies
+
     # ---- end to end through the C ABI with host buffers --------------------
     h2d = sum(p["x"].numel() * 2 for p in problems)
     d2h = sum(p["out"].numel() * 2 for p in problems)
@@ -565,7 +603,7 @@ def main():
                           "8 back-to-back launches of each problem's kernel (GEMMs over rotating weight copies)",
                 "clocks": clk.summary(),
                 "kernel_time_us": {"quant": round(quant_total, 2), "gemm": round(gemm_total, 2)},
-                "sweep": sweep, "quant_variants": variants}
+                "sweep": sweep, "quant_variants": variants, "fused_quant_linear": fused}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

@@ -41,6 +41,7 @@ EXPORTED = (
     "fp8q_linear_channelwise",
     "fp8q_linear_blockwise",
     "fp8q_linear_channelwise_noalloc",
+    "fp8q_linear_blockwise_fused",
     "fp8q_gemm_plan",
     "fp8q_set_plan_override",
     "fp8q_device_status",
@@ -90,6 +91,7 @@ def load_library(path: str | None = None):
         "fp8q_linear_channelwise": [P, P, I64, P, P, P, I64, I64, I64, P, P, ctypes.c_int, P],
         "fp8q_linear_blockwise": [P, P, P, P, P, I64, I64, I64, P, P, I64, ctypes.c_int, P],
         "fp8q_linear_channelwise_noalloc": [P, P, I64, P, P, P, I64, I64, I64, ctypes.c_int, P],
+        "fp8q_linear_blockwise_fused": [P, I64, P, P, P, P, I64, I64, I64, ctypes.c_int, P],
         "fp8q_gemm_plan": [I64, I64, I64, I32, I32, ctypes.POINTER(Plan)],
         "fp8q_device_status": [P, I32],
         "fp8q_selftest_wait_timeout": [P],
@@ -367,6 +369,29 @@ def fp8q_linear_blockwise(x: torch.Tensor, w: torch.Tensor, w_scale: torch.Tenso
     _check("fp8q_linear_blockwise",
            L.fp8q_linear_blockwise(_ptr(x), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(out), M, N, K, _ptr(xq),
                                    _ptr(xs), m_pad, _out_code(out_dtype), _stream(x.device)))
+    return out
+
+
+def fp8q_linear_blockwise_fused(x: torch.Tensor, w: torch.Tensor, w_scale: torch.Tensor, bias=None,
+                                out_dtype=torch.bfloat16):
+    """The blockwise linear layer in one kernel: group-128 quantization of
+    the bf16 activations inside the GEMM (decode sizes whose schedule is the
+    16-token tile; otherwise FP8Q_ERR_UNSUPPORTED).  Bit-identical to
+    fp8q_linear_blockwise on the same schedule."""
+    L = load_library()
+    _need(x, torch.bfloat16, "x")
+    _need(w, E4M3, "w", x.device)
+    _need(w_scale, torch.float32, "w_scale", x.device)
+    if bias is not None:
+        _need(bias, torch.bfloat16, "bias", x.device)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with contiguous rows")
+    M, K = x.shape
+    N = w.shape[0]
+    out = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    _check("fp8q_linear_blockwise_fused",
+           L.fp8q_linear_blockwise_fused(_ptr(x), x.stride(0), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(out), M, N,
+                                         K, _out_code(out_dtype), _stream(x.device)))
     return out
 
 

@@ -3,6 +3,7 @@
 // fp8q_device_status, which exists to synchronize), no exceptions.
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stdlib.h>
 #include <stdint.h>
 
 #include "../../include/fp8q.h"
@@ -158,11 +159,13 @@ fp8q_status fp8q_scaled_mm_channelwise(const void *a, const void *b, int64_t ldb
     if (bias != nullptr && (reinterpret_cast<uintptr_t>(bias) & 1u)) return FP8Q_ERR_INVALID_ARG;
     GemmProblem p;
     p.M = M; p.N = N; p.K = K; p.m_pad = M;
-    p.a = a; p.w = b; p.ldw = ldb;
+    p.a = a; p.lda = K; p.w = b; p.ldw = ldb;
     p.a_scale = a_scale; p.w_scale = b_scale; p.bias = bias; p.out = out;
     p.out_fp16 = out_dtype == FP8Q_OUT_FP16;
     p.blockwise = false;
     p.preload = false;
+    p.fused_quant = false;
+    p.eps = 0.0f;
     return run_gemm(p, as_stream(stream));
 }
 
@@ -182,11 +185,13 @@ fp8q_status fp8q_scaled_mm_blockwise(const void *a, const void *w, const float *
     if (bias != nullptr && (reinterpret_cast<uintptr_t>(bias) & 1u)) return FP8Q_ERR_INVALID_ARG;
     GemmProblem p;
     p.M = M; p.N = N; p.K = K; p.m_pad = m_pad;
-    p.a = a; p.w = w; p.ldw = K;
+    p.a = a; p.lda = K; p.w = w; p.ldw = K;
     p.a_scale = a_scale; p.w_scale = w_scale; p.bias = bias; p.out = out;
     p.out_fp16 = out_dtype == FP8Q_OUT_FP16;
     p.blockwise = true;
     p.preload = false;
+    p.fused_quant = false;
+    p.eps = 0.0f;
     return run_gemm(p, as_stream(stream));
 }
 
@@ -221,9 +226,38 @@ fp8q_status fp8q_linear_blockwise(const void *x, const void *w, const float *w_s
     if (w == nullptr || w_scale == nullptr || out == nullptr || !aligned16(w) || !aligned16(out) ||
         !aligned16(xs) || !aligned4(w_scale))
         return FP8Q_ERR_INVALID_ARG;
+    if (bias != nullptr && (reinterpret_cast<uintptr_t>(bias) & 1u)) return FP8Q_ERR_INVALID_ARG;
     s = fp8q_quant_per_token_group_row_padded(x, M, K, K, 128, 1e-10f, 4, xq, xs, m_pad, stream);
     if (s != FP8Q_OK) return s;
     return fp8q_scaled_mm_blockwise(xq, w, xs, w_scale, bias, out, M, m_pad, N, K, out_dtype, stream);
+}
+
+fp8q_status fp8q_linear_blockwise_fused(const void *x, int64_t ldx, const void *w, const float *w_scale,
+                                        const void *bias, void *out, int64_t M, int64_t N, int64_t K,
+                                        fp8q_out_dtype out_dtype, void *stream)
+{
+    if (M < 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return FP8Q_ERR_INVALID_ARG;
+    if (out_dtype != FP8Q_OUT_BF16 && out_dtype != FP8Q_OUT_FP16) return FP8Q_ERR_UNSUPPORTED;
+    if (N % 128 != 0 || K % 128 != 0) return FP8Q_ERR_UNSUPPORTED;
+    if (ldx < K || ldx % 8 != 0 || ldx > kMaxDim) return FP8Q_ERR_INVALID_ARG;
+    if (M == 0) return FP8Q_OK;
+    if (x == nullptr || w == nullptr || w_scale == nullptr || out == nullptr) return FP8Q_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(out) || !aligned4(w_scale)) return FP8Q_ERR_INVALID_ARG;
+    if (bias != nullptr && (reinterpret_cast<uintptr_t>(bias) & 1u)) return FP8Q_ERR_INVALID_ARG;
+    fp8q_plan pl;
+    const fp8q_status s = fp8q_gemm_plan(M, N, K, 1, 0, &pl);
+    if (s != FP8Q_OK) return s;
+    if (!pl.swap_ab || pl.mma_n != 16) return FP8Q_ERR_UNSUPPORTED;
+    GemmProblem p;
+    p.M = M; p.N = N; p.K = K; p.m_pad = M;
+    p.a = x; p.lda = ldx; p.w = w; p.ldw = K;
+    p.a_scale = nullptr; p.w_scale = w_scale; p.bias = bias; p.out = out;
+    p.out_fp16 = out_dtype == FP8Q_OUT_FP16;
+    p.blockwise = true;
+    p.preload = false;
+    p.fused_quant = true;
+    p.eps = 1e-10f;
+    return run_gemm(p, as_stream(stream));
 }
 
 fp8q_status fp8q_device_status(void *stream, int32_t reset)

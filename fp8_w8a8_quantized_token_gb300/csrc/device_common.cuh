@@ -102,6 +102,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
 }
 
 // ---------------------------------------------------------------------------
+// cp.async: 16-byte asynchronous global -> shared copies (not via the TMA
+// unit), tracked per thread in commit groups.  src_bytes < 16 zero-fills the
+// rest of the 16 bytes (0: no global read at all).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Wait until at most N of this thread's most recent commit groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // TMA (tensor maps live in kernel parameter space as __grid_constant__)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map)

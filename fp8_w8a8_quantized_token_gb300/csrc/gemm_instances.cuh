@@ -10,6 +10,13 @@ namespace fp8q {
 template <bool BLOCKWISE, typename OutT>
 cudaError_t dispatch_gemm(const GemmProblem &p, const GemmLaunch &l, unsigned *status, cudaStream_t st)
 {
+    if (p.fused_quant) {
+        // Quantization fused into the GEMM: blockwise 16-token decode tiles.
+        if constexpr (BLOCKWISE)
+            if (l.swap_ab && l.mma_n == 16)
+                return launch_gemm_inst<true, 16, kFusedQuantStages, true, OutT, false, true>(p, l, status, st);
+        return cudaErrorInvalidValue;
+    }
     if (l.swap_ab) {
         switch (l.mma_n) {
             case 16: return launch_gemm_inst<true, 16, stages_for(true, 16), BLOCKWISE, OutT>(p, l, status, st);

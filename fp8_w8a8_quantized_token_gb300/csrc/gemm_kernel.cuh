@@ -60,6 +60,7 @@
 #pragma once
 
 #include "device_common.cuh"
+#include "quant_common.cuh"
 
 namespace fp8q {
 
@@ -81,6 +82,9 @@ struct GemmArgs {
     unsigned long long *trace;  // per-CTA phase timestamps (trace builds only), or null
     int prefetch_kb;            // weight K blocks per CTA prefetched into L2 before the dependency wait
     int preload;                // 1: load the first tile's weight slices before the dependency wait
+    float eps;                  // fused quantization: the amax floor of the group scales
+    const __nv_bfloat16 *x;     // fused quantization: bf16 activations [M, K]
+    long long ldx;              //   and their row stride (elements)
 };
 
 // Phase timestamps of a trace build (-DFP8Q_TRACE): kTraceSlots 64-bit
@@ -102,7 +106,7 @@ enum TracePhase {
     } while (0)
 #endif
 
-template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, bool TWO_SM = false>
+template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, bool TWO_SM = false, bool FQ = false>
 struct GemmCfg {
     static constexpr int kEpiWarps = BN > 128 ? 8 : 4;
     static constexpr int kColGroups = kEpiWarps / 4;
@@ -121,7 +125,10 @@ struct GemmCfg {
     static constexpr int kIssuers = (BLOCKWISE || TWO_SM || BN >= 256) ? 1 : 2;
     static constexpr int kSlotCols = kIssuers * BN;  // TMEM columns per accumulator slot
     static constexpr int kEpiWarp0 = 1 + kIssuers;   // first epilogue warp
-    static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+    // FQ: two warps after the epilogue warps quantize the activation tiles.
+    static constexpr int kQuantWarps = FQ ? 2 : 0;
+    static constexpr int kQuantWarp0 = kEpiWarp0 + kEpiWarps;
+    static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps + kQuantWarps);
     static constexpr int kEpiThreads = 32 * kEpiWarps;
     static constexpr int kTokTile = SWAP ? BN : 128;     // tokens per tile
     static constexpr int kColTile = SWAP ? 128 : BN;     // output columns per tile
@@ -133,7 +140,14 @@ struct GemmCfg {
     static constexpr uint32_t kSASlot = BLOCKWISE ? (kSABytes + 127u) / 128u * 128u : 0u;
     static constexpr int kSASlotFloats = static_cast<int>(kSASlot / 4u);
     // Bytes one ring slot's full barrier waits for (TWO_SM: both CTAs' loads).
-    static constexpr uint32_t kStageTx = TWO_SM ? 2u * (kABytes + kBBytes) : kABytes + kBBytes + kSABytes;
+    // Fused quantization (FQ; blockwise, swapped 16-token tiles): the
+    // producer loads only the weight slices; two quantizing warps copy the
+    // bf16 activation tiles (BN rows x 128 columns) into a staging ring of
+    // their own and turn them into the ring's B tiles and scale slots.
+    static constexpr int kXStages = FQ ? STAGES : 0;
+    static constexpr uint32_t kXBytes = FQ ? static_cast<uint32_t>(BN) * 256u : 0u;
+    static constexpr uint32_t kStageTx = TWO_SM ? 2u * (kABytes + kBBytes)
+                                                : (FQ ? kABytes : kABytes + kBBytes + kSABytes);
     // Two accumulator slots, allocated as a power of two >= 32 columns.
     static constexpr uint32_t kTmemCols = 2 * kSlotCols <= 32 ? 32u : 2 * kSlotCols <= 64 ? 64u
                                         : 2 * kSlotCols <= 128 ? 128u : 2 * kSlotCols <= 256 ? 256u : 512u;
@@ -150,7 +164,8 @@ struct GemmCfg {
     static constexpr int kPartStride = BN + 4;
     static constexpr uint32_t kRecvBytes = kPush ? 144u * kPartStride * 4u : 0u;
     static constexpr uint32_t kOffRecv = kOffSA + STAGES * kSASlot;
-    static constexpr uint32_t kOffBar = kOffRecv + kRecvBytes;
+    static constexpr uint32_t kOffX = (kOffRecv + kRecvBytes + 127u) / 128u * 128u;
+    static constexpr uint32_t kOffBar = kOffX + kXStages * kXBytes;
     static constexpr uint32_t kNumBars = 2 * STAGES + 6;  // full, empty, tfull[2], tempty[2], drain, recv
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr uint32_t kOffCol = (kOffMisc + 16 + 15) / 16 * 16;  // staged column scale, bias
@@ -169,6 +184,7 @@ struct GemmCfg {
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
     static_assert(kCols % 32 == 0 || kCols == 16, "epilogue column chunking");
     static_assert(2 * kSlotCols <= 512, "TMEM columns");
+    static_assert(!FQ || (BLOCKWISE && SWAP && BN == 16 && !TWO_SM), "fused quantization: blockwise 16-token tiles");
 };
 
 // Waits that only give up on the time limit (used while draining).
@@ -283,13 +299,13 @@ __device__ __forceinline__ void store_box_tma(const CUtensorMap *tm_out, uint8_t
     }
 }
 
-template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT, bool TWO_SM = false>
-__global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::kThreads, 1)
+template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT, bool TWO_SM = false, bool FQ = false>
+__global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sa, const __grid_constant__ CUtensorMap tm_out,
                     const GemmArgs p)
 {
-    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>;
+    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sA = smem + C::kOffA;
@@ -301,6 +317,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
     uint64_t *recv_full = drain + 1;
+    uint8_t *sX = smem + C::kOffX;              // FQ: bf16 activation tiles
     float *sRecv = reinterpret_cast<float *>(smem + C::kOffRecv);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
@@ -355,7 +372,8 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
         if (BLOCKWISE) tma_prefetch_map(&tm_sa);
         if (C::kTmaStore) tma_prefetch_map(&tm_out);
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
+            // FQ: the quantizing warps' arrivals publish the B tile.
+            mbar_init(&full[s], 1 + C::kQuantWarps);
             mbar_init(&empty[s], (BLOCKWISE ? C::kEpiWarps : 0) + ((pair && !TWO_SM) ? 2 : C::kIssuers));
         }
         for (int i = 0; i < 2; ++i) {
@@ -364,6 +382,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
         }
         mbar_init(drain, C::kIssuers);
         mbar_init(recv_full, 1);
+
         *abort = 0;
         fence_mbar_init();
         if (C::kPush && split > 1) {
@@ -474,7 +493,9 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
                         tma_load_2d_pair(sA + stage * C::kABytes, &tm_a, lead_full(stage), kb * 128, a_row, pol_a);
                     } else if (issued < npre) {
                         // Weight slice already in flight; barrier armed.
-                        if (SWAP)
+                        if (FQ) {
+                            // (the activation tile is the epilogue warps' work)
+                        } else if (SWAP)
                             tma_load_2d(sB + stage * C::kBBytes, &tm_b, &full[stage], kb * 128, b_row, pol_b);
                         else
                             tma_load_2d(sA + stage * C::kABytes, &tm_a, &full[stage], kb * 128, a_row, pol_a);
@@ -482,13 +503,14 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
                         if (!mbar_wait(&empty[stage], phase ^ 1u, abort, p.status)) { ok = false; break; }
                         mbar_arrive_expect_tx(&full[stage], C::kStageTx);
                         tma_load_2d(sA + stage * C::kABytes, &tm_a, &full[stage], kb * 128, a_row, pol_a);
-                        if (pair)
+                        if (FQ) {
+                        } else if (pair)
                             tma_load_2d_mc(sB + stage * C::kBBytes + w_half_off, &tm_b, &full[stage], kb * 128,
                                            b_row + w_half_row, 3, pol_b);
                         else
                             tma_load_2d(sB + stage * C::kBBytes, &tm_b, &full[stage], kb * 128, b_row, pol_b);
                     }
-                    if (BLOCKWISE)
+                    if (BLOCKWISE && !FQ)
                         tma_load_2d(sSA + stage * C::kSASlotFloats, &tm_sa, &full[stage], m_tile * C::kTokTile, kb,
                                     pol_b);
                     ++issued;
@@ -580,6 +602,83 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
                     slot ^= 1u;
                     if (slot == 0) tphase ^= 1u;
                 }
+        }
+        __syncwarp();
+    } else if (FQ && warp >= C::kQuantWarp0) {
+        // ------------------------------------------------------------------
+        // Quantizing warps (FQ): this CTA's K blocks g = 0, 1, ... (its tiles
+        // in order, nkb blocks each).  Each thread owns two 16-element chunks
+        // of every block (rows t0 and t0 + 8, chunk c) and copies them itself
+        // into staging slot g % kXStages with cp.async (16-byte global ->
+        // shared copies, zero-filled past row M; not the TMA unit, whose
+        // queue holds the weight tiles), kXStages blocks ahead, one commit
+        // group per block.  Once ring stage g % STAGES is free (the empty
+        // barrier the producer waits on: the block STAGES earlier was
+        // consumed by its MMA and promoted), it quantizes them with the
+        // standalone quantizer's arithmetic (quant_common.cuh) -- the row's
+        // group scale from the 8 lanes holding that row -- writes the E4M3
+        // codes into the 128-byte-swizzled B tile (16-byte unit c of row t
+        // at c ^ (t & 7), as the TMA would) and the scale into the stage's
+        // scale slot, and publishes the tile (proxy fence, arrive on full).
+        // Each thread reads only the bytes it copied: no barrier between the
+        // two warps.
+        // ------------------------------------------------------------------
+        if constexpr (FQ) {
+            const int qt = threadIdx.x - 32 * C::kQuantWarp0;  // 0 .. 63
+            const int t0 = qt >> 3, c = qt & 7;                 // rows t0 and t0 + 8, chunk c
+            const long long total =
+                cluster_id < p.num_tiles
+                    ? static_cast<long long>((p.num_tiles - 1 - cluster_id) / num_clusters + 1) * nkb
+                    : 0;
+            // Copy this thread's part of block g into its staging slot (an
+            // empty commit group past the last block keeps the count uniform).
+            auto copy_x = [&](long long g) {
+                if (g < total) {
+                    int a_q, b_q;
+                    coords(cluster_id + static_cast<int>(g / nkb) * num_clusters, a_q, b_q);
+                    const int k0 = (kb_begin + static_cast<int>(g % nkb)) * 128 + c * 16;
+                    uint8_t *slot = sX + static_cast<int>(g % C::kXStages) * C::kXBytes;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int t = t0 + 8 * h;
+                        const int m = b_q * BN + t;
+                        const bool in = m < p.M;
+                        const __nv_bfloat16 *src = p.x + (in ? static_cast<long long>(m) * p.ldx + k0 : 0);
+                        const uint32_t dst = smem_u32(slot + t * 256 + c * 32);
+                        cp_async_16(dst, src, in ? 16u : 0u);
+                        cp_async_16(dst + 16, src + 8, in ? 16u : 0u);
+                    }
+                }
+                cp_async_commit();
+            };
+            for (int u = 0; u < C::kXStages; ++u) copy_x(u);
+            uint32_t stage = 0, phase = 0;
+            for (long long g = 0; g < total; ++g) {
+                cp_async_wait_group<C::kXStages - 1>();   // block g's copies have landed
+                const bool got = mbar_wait(&empty[stage], phase ^ 1u, abort, p.status);
+                if (!__all_sync(0xffffffffu, got)) break;
+                const uint8_t *xs = sX + static_cast<int>(g % C::kXStages) * C::kXBytes;
+                uint8_t *bt = sB + stage * C::kBBytes;
+                float *sa = sSA + stage * C::kSASlotFloats;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int t = t0 + 8 * h;
+                    const Chunk16 v = load_chunk_smem(xs + t * 256 + c * 32);
+                    float m = chunk_amax(v, 0.0f);
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                    const float sc = scale_of(m, p.eps);
+                    *reinterpret_cast<uint4 *>(bt + t * 128 + ((c ^ (t & 7)) << 4)) = quant_chunk(v, sc);
+                    if (c == 0) sa[t] = sc;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[stage]);
+                copy_x(g + C::kXStages);                 // refill the slot just read (by this thread)
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+            cp_async_wait_all();   // no copy may still be writing when the CTA exits
         }
         __syncwarp();
     } else {
@@ -907,6 +1006,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>::
         // The staging buffers must have been read out by the TMA unit before
         // the CTA exits (the stores themselves complete with the grid).
         if (C::kTmaStore && lane == 0) bulk_wait_read();
+
     }
 
     if constexpr (!C::kPush) {

@@ -13,11 +13,11 @@ namespace fp8q {
 
 constexpr int kMaxDevices = 64;
 
-template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT, bool TWO_SM = false>
+template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT, bool TWO_SM = false, bool FQ = false>
 cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigned *status, cudaStream_t st)
 {
-    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM>;
-    auto kernel = fp8_gemm_kernel<SWAP, BN, STAGES, BLOCKWISE, OutT, TWO_SM>;
+    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ>;
+    auto kernel = fp8_gemm_kernel<SWAP, BN, STAGES, BLOCKWISE, OutT, TWO_SM, FQ>;
 
     static std::atomic<uint64_t> attr_done[kMaxDevices / 64 + 1];
     int dev = 0;
@@ -40,9 +40,13 @@ cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigne
                       static_cast<uint64_t>(pr.N), static_cast<uint64_t>(pr.ldw), 128, wrow_box,
                       CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    if (!make_tmap_2d(&tm_x, pr.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(pr.K),
-                      static_cast<uint64_t>(pr.M), static_cast<uint64_t>(pr.K), 128, tok_box,
-                      CU_TENSOR_MAP_SWIZZLE_128B))
+    // FQ: the bf16 activations are copied by the kernel's quantizing warps
+    // (GemmArgs::x); the activation map slot holds the weight map, unused.
+    if (FQ)
+        tm_x = tm_w;
+    else if (!make_tmap_2d(&tm_x, pr.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(pr.K),
+                           static_cast<uint64_t>(pr.M), static_cast<uint64_t>(pr.K), 128, tok_box,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     // Output (non-swapped tiles): 2-byte values [M, N], row stride N, boxes
     // of 32 x 32 with the 64-byte swizzle of the epilogue's staging buffers.
@@ -52,7 +56,7 @@ cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigne
                       static_cast<uint64_t>(pr.M), static_cast<uint64_t>(pr.N) * 2u, 32, 32,
                       CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
-    if (BLOCKWISE) {
+    if (BLOCKWISE && !FQ) {
         // Column-major activation scales: K/128 columns of m_pad floats; only
         // the first M entries of each column are real (the rest read as 0).
         if (!make_tmap_2d(&tm_sa, pr.a_scale, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, static_cast<uint64_t>(pr.M),
@@ -88,6 +92,9 @@ cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigne
     a.trace = trace_buffer();
     a.prefetch_kb = prefetch_kblocks();
     a.preload = pr.preload ? 1 : 0;
+    a.eps = pr.eps;
+    a.x = FQ ? static_cast<const __nv_bfloat16 *>(pr.a) : nullptr;
+    a.ldx = pr.lda;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(l.grid));

@@ -34,7 +34,8 @@ struct GemmLaunch {
 struct GemmProblem {
     int64_t M, N, K;
     int64_t m_pad;          // blockwise: leading dimension of the scale columns
-    const void *a;          // e4m3 activations, row stride K
+    const void *a;          // e4m3 activations, row stride K (fused_quant: bf16, row stride lda)
+    int64_t lda;            // fused_quant: row stride of the bf16 activations (elements)
     const void *w;          // e4m3 weights [N, K] with row stride ldw
     int64_t ldw;
     const float *a_scale;   // channelwise [M]; blockwise column-major [K/128][m_pad]
@@ -44,6 +45,8 @@ struct GemmProblem {
     bool out_fp16;
     bool blockwise;
     bool preload;           // weights may be read before the dependency wait
+    bool fused_quant;       // blockwise: a is bf16, quantized inside the GEMM (group 128, eps)
+    float eps;              // fused_quant: amax floor of the group scales
 };
 
 // Launchers return cudaSuccess or the launch error; a tensor map the driver
@@ -61,6 +64,11 @@ constexpr int stages_for(bool swap_ab, int mma_n)
 {
     return swap_ab ? (mma_n == 16 ? 5 : mma_n == 32 ? 4 : mma_n == 64 ? 7 : 4) : 4;
 }
+
+// Ring depth of the fused-quantization instantiation (blockwise, 16-token
+// tiles): 4 slots of 16 KB + 2 KB plus a 4-slot bf16 staging ring of 4 KB
+// keep it near 100 KB, so two CTAs still fit on one SM.
+constexpr int kFusedQuantStages = 4;
 
 // Ring depth of the 2-CTA MMA instantiation (each slot: 16 KB of tokens +
 // 16 KB, the CTA's half, of weight rows).

@@ -248,6 +248,29 @@ FP8Q_API fp8q_status fp8q_linear_blockwise(const void *x, const void *w, const f
                                   void *stream);
 
 /* ---------------------------------------------------------------------------
+ * fp8q_linear_blockwise_fused -- the blockwise linear layer in ONE kernel:
+ * the row-padded group-128 quantization of fp8q_linear_blockwise is done
+ * inside the GEMM, on the activation tiles it consumes (the quantization
+ * "optionally fused" into the GEMM; group scales are local to each 128-wide
+ * K block, so every CTA quantizes exactly the blocks it multiplies).  Codes
+ * and scales are those of fp8q_quant_per_token_group_row_padded (g = 128,
+ * eps = 1e-10), so the output is bit-identical to fp8q_linear_blockwise on
+ * the same schedule.
+ * Available where the planner's schedule is the 16-token swapped tile
+ * (decode sizes, M <= 16 on the compiled table's shapes); other problems
+ * return FP8Q_ERR_UNSUPPORTED.  Measured on GB300 it is SLOWER than the
+ * two-kernel fp8q_linear_blockwise on back-to-back layers (the activation
+ * reads issued after the dependency wait queue behind the weight stream),
+ * so fp8q_linear_blockwise does not use it; it is for callers that want a
+ * single launch per layer.
+ * x   : bf16 [M, K], row stride ldx >= K (ldx % 8 == 0), 16-byte aligned.
+ * w, w_scale, bias, out, out_dtype: as fp8q_linear_blockwise.  No scratch.
+ * ------------------------------------------------------------------------- */
+FP8Q_API fp8q_status fp8q_linear_blockwise_fused(const void *x, int64_t ldx, const void *w, const float *w_scale,
+                                        const void *bias, void *out, int64_t M, int64_t N, int64_t K,
+                                        fp8q_out_dtype out_dtype, void *stream);
+
+/* ---------------------------------------------------------------------------
  * fp8q_linear_channelwise_noalloc -- the pages have no counterpart: this is
  * an addition of this library for callers that cannot allocate.
  *
