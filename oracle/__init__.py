@@ -71,6 +71,7 @@ def lib():
             L.fp8q_oracle_pow2_ceil_array.argtypes = [P, P, I64]
             L.fp8q_oracle_gemm_channelwise.argtypes = [P, I64, P, I64, P, P, P, I64, I64, INT, P, I64, P, I64, I64]
             L.fp8q_oracle_gemm_blockwise.argtypes = [P, I64, P, I64, P, I64, P, P, I64, I64, INT, P, I64, P, I64, I64]
+            L.fp8q_oracle_gemm_w8a16.argtypes = [P, I64, P, I64, P, P, I64, I64, INT, P, I64, P, I64, I64]
             L.fp8q_oracle_gemm_channelwise_at.argtypes = [P, I64, P, I64, P, P, P, I64, INT, P, P, I64, P]
             L.fp8q_oracle_gemm_blockwise_at.argtypes = [P, I64, P, I64, P, I64, P, P, I64, INT, P, P, I64, P]
             _lib = L
@@ -282,6 +283,23 @@ def gemm_channelwise(a, b, sa, sb, bias=None, out_fp16: bool = False, threads: i
     _run_rows(lambda r0, r1: L.fp8q_oracle_gemm_channelwise(
         _ptr(a8), K, _ptr(b8), K, _ptr(sa_), _ptr(sb_), _ptr(bb), N, K, int(out_fp16),
         _ptr(out), N, _ptr(yd), r0, r1), M, threads)
+    return (out, yd) if return_double else out
+
+
+def gemm_w8a16(x, w, ws, bias=None, out_fp16: bool = False, threads: int = 1, return_double: bool = False):
+    """Weight-only FP8: x bf16 [M, K], w uint8 E4M3 [N, K], ws fp32 [N],
+    bias bf16 [N] or None -> out bits uint16 [M, N]."""
+    xb, w8 = _bits16(x), _u8(w)
+    M, K = xb.shape
+    N = w8.shape[0]
+    ws_ = _f32(ws)
+    bb = None if bias is None else _bits16(bias)
+    out = np.zeros((M, N), dtype=np.uint16)
+    yd = np.zeros((M, N), dtype=np.float64) if return_double else None
+    L = lib()
+    _run_rows(lambda r0, r1: L.fp8q_oracle_gemm_w8a16(
+        _ptr(xb), K, _ptr(w8), K, _ptr(ws_), _ptr(bb), N, K, int(out_fp16), _ptr(out), N, _ptr(yd), r0, r1),
+        M, threads)
     return (out, yd) if return_double else out
 
 

@@ -420,6 +420,38 @@ void fp8q_oracle_gemm_channelwise(const uint8_t *a, int64_t lda, const uint8_t *
  *   P_kb    = sum_{k in block kb} dec(a[m, k]) * dec(w[n, k])   (exact)
  * The bias is added after the GEMM in the reference wrapper; here it joins
  * y before the single rounding.  Rows [r0, r1). */
+/* Weight-only FP8 linear (W8A16; the Marlin linear of [PR31340]
+ * "Implementation breakdown" and "Key source snippets",
+ * apply_fp8_marlin_linear(input, weight, weight_scale, ..., bias): weight-only,
+ * no input scale), rows [r0, r1):
+ *   out[m, n] = round(sum_k x[m, k] * dec(w[n, k]) * ws[n] + bias[n])
+ * x bf16 [M, K] (row stride ldx), w e4m3 [N, K] (row stride ldw), ws fp32 [N]
+ * (a per-tensor scale is the case of equal entries).  Evaluated in double:
+ * each product of a bf16 and an E4M3 value (8 + 4 significant bits) is
+ * exact; the sum's rounding error is at most K * 2^-53 relative to the
+ * largest partial sum, ~1e-12 for K <= 16384; one final rounding. */
+void fp8q_oracle_gemm_w8a16(const uint16_t *x, int64_t ldx, const uint8_t *w, int64_t ldw, const float *ws,
+                            const uint16_t *bias, int64_t N, int64_t K, int out_fp16, uint16_t *out,
+                            int64_t ldo, double *yd, int64_t r0, int64_t r1)
+{
+    double t[256];
+    decode_table(t);
+    double *xrow = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+    for (int64_t m = r0; m < r1; ++m) {
+        for (int64_t k = 0; k < K; ++k) xrow[k] = (double)fp8q_oracle_bf16_to_f32(x[m * ldx + k]);
+        for (int64_t n = 0; n < N; ++n) {
+            const uint8_t *wr = w + n * ldw;
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) acc += xrow[k] * t[wr[k]];
+            double y = acc * (double)ws[n];
+            if (bias) y += (double)fp8q_oracle_bf16_to_f32(bias[n]);
+            out[m * ldo + n] = round_out(y, out_fp16);
+            if (yd) yd[m * ldo + n] = y;
+        }
+    }
+    free(xrow);
+}
+
 void fp8q_oracle_gemm_blockwise(const uint8_t *a, int64_t lda, const uint8_t *w, int64_t ldw,
                                 const float *sa, int64_t m_pad, const float *sw,
                                 const uint16_t *bias, int64_t N, int64_t K, int out_fp16,
