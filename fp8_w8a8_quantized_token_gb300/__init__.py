@@ -42,6 +42,7 @@ EXPORTED = (
     "fp8q_linear_blockwise",
     "fp8q_linear_channelwise_noalloc",
     "fp8q_linear_blockwise_fused",
+    "fp8q_scaled_mm_w8a16",
     "fp8q_gemm_plan",
     "fp8q_set_plan_override",
     "fp8q_device_status",
@@ -92,6 +93,7 @@ def load_library(path: str | None = None):
         "fp8q_linear_blockwise": [P, P, P, P, P, I64, I64, I64, P, P, I64, ctypes.c_int, P],
         "fp8q_linear_channelwise_noalloc": [P, P, I64, P, P, P, I64, I64, I64, ctypes.c_int, P],
         "fp8q_linear_blockwise_fused": [P, I64, P, P, P, P, I64, I64, I64, ctypes.c_int, P],
+        "fp8q_scaled_mm_w8a16": [P, I64, P, I64, P, P, P, I64, I64, I64, ctypes.c_int, P],
         "fp8q_gemm_plan": [I64, I64, I64, I32, I32, ctypes.POINTER(Plan)],
         "fp8q_device_status": [P, I32],
         "fp8q_selftest_wait_timeout": [P],
@@ -392,6 +394,28 @@ def fp8q_linear_blockwise_fused(x: torch.Tensor, w: torch.Tensor, w_scale: torch
     _check("fp8q_linear_blockwise_fused",
            L.fp8q_linear_blockwise_fused(_ptr(x), x.stride(0), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(out), M, N,
                                          K, _out_code(out_dtype), _stream(x.device)))
+    return out
+
+
+def fp8q_scaled_mm_w8a16(x: torch.Tensor, w: torch.Tensor, w_scale: torch.Tensor, bias=None,
+                         out_dtype=torch.bfloat16, out: torch.Tensor | None = None):
+    """Weight-only FP8 linear: bf16 x [M, K] @ (e4m3 w [N, K] * w_scale[N]).T
+    (+ bias) -> [M, N], fp32 accumulation, no activation quantization."""
+    L = load_library()
+    _need(x, torch.bfloat16, "x")
+    _need(w, E4M3, "w", x.device)
+    _need(w_scale, torch.float32, "w_scale", x.device)
+    if bias is not None:
+        _need(bias, torch.bfloat16, "bias", x.device)
+    if x.dim() != 2 or x.stride(1) != 1 or w.dim() != 2 or w.stride(1) != 1:
+        raise ValueError("x and w must be 2-D with contiguous rows")
+    M, K = x.shape
+    N = w.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    _check("fp8q_scaled_mm_w8a16",
+           L.fp8q_scaled_mm_w8a16(_ptr(x), x.stride(0), _ptr(w), w.stride(0), _ptr(w_scale), _ptr(bias), _ptr(out),
+                                  M, N, K, _out_code(out.dtype), _stream(x.device)))
     return out
 
 

@@ -35,14 +35,11 @@ fp8q_status check_quant_common(const void *x, int64_t M, int64_t K, int64_t ldx,
     return FP8Q_OK;
 }
 
-fp8q_status run_gemm(GemmProblem p, cudaStream_t st)
+fp8q_status launch_planned(GemmProblem p, const fp8q_plan &pl, cudaStream_t st)
 {
     // Weight bytes the kernel may read before waiting for its predecessor.
     const size_t wbytes = static_cast<size_t>(p.N - 1) * static_cast<size_t>(p.ldw) + static_cast<size_t>(p.K);
     p.preload = !last_launch_writes_overlap(st, p.w, wbytes);
-    fp8q_plan pl;
-    const fp8q_status s = fp8q_gemm_plan(p.M, p.N, p.K, p.blockwise ? 1 : 0, 0, &pl);
-    if (s != FP8Q_OK) return s;
     unsigned *status = device_status_ptr();
     if (status == nullptr) return FP8Q_ERR_CUDA;
     GemmLaunch l;
@@ -59,7 +56,19 @@ fp8q_status run_gemm(GemmProblem p, cudaStream_t st)
     return from_cuda(e);
 }
 
+fp8q_status run_gemm(const GemmProblem &p, cudaStream_t st)
+{
+    fp8q_plan pl;
+    const fp8q_status s = fp8q_gemm_plan(p.M, p.N, p.K, p.blockwise ? 1 : 0, 0, &pl);
+    if (s != FP8Q_OK) return s;
+    return launch_planned(p, pl, st);
+}
+
 }  // namespace
+
+namespace fp8q {
+void plan_finish(int64_t M, int64_t N, int64_t K, int blockwise, int num_sms, fp8q_plan *pl);
+}
 
 extern "C" {
 
@@ -165,6 +174,7 @@ fp8q_status fp8q_scaled_mm_channelwise(const void *a, const void *b, int64_t ldb
     p.blockwise = false;
     p.preload = false;
     p.fused_quant = false;
+    p.w16 = false;
     p.eps = 0.0f;
     return run_gemm(p, as_stream(stream));
 }
@@ -191,6 +201,7 @@ fp8q_status fp8q_scaled_mm_blockwise(const void *a, const void *w, const float *
     p.blockwise = true;
     p.preload = false;
     p.fused_quant = false;
+    p.w16 = false;
     p.eps = 0.0f;
     return run_gemm(p, as_stream(stream));
 }
@@ -256,8 +267,46 @@ fp8q_status fp8q_linear_blockwise_fused(const void *x, int64_t ldx, const void *
     p.blockwise = true;
     p.preload = false;
     p.fused_quant = true;
+    p.w16 = false;
     p.eps = 1e-10f;
     return run_gemm(p, as_stream(stream));
+}
+
+fp8q_status fp8q_scaled_mm_w8a16(const void *x, int64_t ldx, const void *w, int64_t ldw, const float *w_scale,
+                                 const void *bias, void *out, int64_t M, int64_t N, int64_t K,
+                                 fp8q_out_dtype out_dtype, void *stream)
+{
+    if (M < 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return FP8Q_ERR_INVALID_ARG;
+    if (out_dtype != FP8Q_OUT_BF16 && out_dtype != FP8Q_OUT_FP16) return FP8Q_ERR_UNSUPPORTED;
+    if (K % 16 != 0 || ldx < K || ldx % 8 != 0 || ldw < K || ldw % 16 != 0 || N % 8 != 0)
+        return FP8Q_ERR_INVALID_ARG;
+    if (M == 0) return FP8Q_OK;
+    if (x == nullptr || w == nullptr || w_scale == nullptr || out == nullptr) return FP8Q_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(out) || !aligned4(w_scale)) return FP8Q_ERR_INVALID_ARG;
+    if (bias != nullptr && (reinterpret_cast<uintptr_t>(bias) & 1u)) return FP8Q_ERR_INVALID_ARG;
+    const int num_sms = current_device_sms();
+    if (num_sms <= 0) return FP8Q_ERR_CUDA;
+    // Schedule: 128 weight rows x 16 (M <= 16) or 32 tokens per tile; K split
+    // across a cluster of 2, 4 or 8 while the tiles cannot fill the GPU.
+    fp8q_plan pl = {};
+    pl.swap_ab = 1;
+    pl.mma_n = M <= 16 ? 16 : 32;
+    const int64_t tiles = ((M + pl.mma_n - 1) / pl.mma_n) * ((N + 127) / 128);
+    int split = 1;
+    while (split < 8 && tiles * split * 2 <= num_sms) split *= 2;
+    pl.split_k = split;
+    plan_finish(M, N, K, 0, num_sms, &pl);
+    GemmProblem p;
+    p.M = M; p.N = N; p.K = K; p.m_pad = M;
+    p.a = x; p.lda = ldx; p.w = w; p.ldw = ldw;
+    p.a_scale = nullptr; p.w_scale = w_scale; p.bias = bias; p.out = out;
+    p.out_fp16 = out_dtype == FP8Q_OUT_FP16;
+    p.blockwise = false;
+    p.preload = false;
+    p.fused_quant = false;
+    p.w16 = true;
+    p.eps = 0.0f;
+    return launch_planned(p, pl, as_stream(stream));
 }
 
 fp8q_status fp8q_device_status(void *stream, int32_t reset)

@@ -285,6 +285,42 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32()
            | (static_cast<uint32_t>(M >> 4) << 24);// M / 16
 }
 
+// Instruction descriptor of tcgen05.mma.kind::f16: D = F32, A = B = BF16
+// (format code 1), both K-major, shape M x N.
+template <int M, int N>
+__host__ __device__ constexpr uint32_t idesc_bf16_f32()
+{
+    return (1u << 4)                               // D format: F32
+           | (1u << 7) | (1u << 10)                // A, B format: BF16
+           | (0u << 15) | (0u << 16)               // A, B K-major
+           | (static_cast<uint32_t>(N >> 3) << 17) // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);// M / 16
+}
+
+// bf16 x bf16 -> fp32 MMA, K = 16 per instruction.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Two E4M3 bytes (lo in the low byte) -> two bf16 (lo in the low half):
+// exact (E4M3 -> f16 by the conversion instruction, f16 -> bf16 through
+// fp32; every E4M3 value is representable in both).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t v)
+{
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+    return *reinterpret_cast<const uint32_t *>(&b);
+}
+
 __device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate)
 {

@@ -10,6 +10,16 @@ namespace fp8q {
 template <bool BLOCKWISE, typename OutT>
 cudaError_t dispatch_gemm(const GemmProblem &p, const GemmLaunch &l, unsigned *status, cudaStream_t st)
 {
+    if (p.w16) {
+        // Weight-only FP8 (bf16 activations): swapped 16- or 32-token tiles.
+        if constexpr (!BLOCKWISE) {
+            if (l.swap_ab && l.mma_n == 16)
+                return launch_gemm_inst<true, 16, kW16Stages, false, OutT, false, false, true>(p, l, status, st);
+            if (l.swap_ab && l.mma_n == 32)
+                return launch_gemm_inst<true, 32, kW16Stages, false, OutT, false, false, true>(p, l, status, st);
+        }
+        return cudaErrorInvalidValue;
+    }
     if (p.fused_quant) {
         // Quantization fused into the GEMM: blockwise 16-token decode tiles.
         if constexpr (BLOCKWISE)

@@ -106,7 +106,7 @@ enum TracePhase {
     } while (0)
 #endif
 
-template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, bool TWO_SM = false, bool FQ = false>
+template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, bool TWO_SM = false, bool FQ = false, bool W16 = false>
 struct GemmCfg {
     static constexpr int kEpiWarps = BN > 128 ? 8 : 4;
     static constexpr int kColGroups = kEpiWarps / 4;
@@ -128,13 +128,25 @@ struct GemmCfg {
     // FQ: two warps after the epilogue warps quantize the activation tiles.
     static constexpr int kQuantWarps = FQ ? 2 : 0;
     static constexpr int kQuantWarp0 = kEpiWarp0 + kEpiWarps;
-    static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps + kQuantWarps);
+    // W16 (weight-only FP8, bf16 activations; swapped channelwise tiles):
+    // four warps after the epilogue warps convert each landed E4M3 weight
+    // tile to bf16 (exact) for kind::f16 MMAs.
+    static constexpr int kConvWarps = W16 ? 4 : 0;
+    static constexpr int kConvWarp0 = kQuantWarp0 + kQuantWarps;
+    static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps + kQuantWarps + kConvWarps);
+    // K steps of one 128-wide K block: 4 MMAs of K = 32 (E4M3) or, W16, 8
+    // of K = 16 (bf16).
+    static constexpr int kKSteps = W16 ? 8 : 4;
     static constexpr int kEpiThreads = 32 * kEpiWarps;
     static constexpr int kTokTile = SWAP ? BN : 128;     // tokens per tile
     static constexpr int kColTile = SWAP ? 128 : BN;     // output columns per tile
-    static constexpr uint32_t kABytes = 128u * 128u;
+    // A operand slot: 128 rows x 128 K of E4M3, or (W16) of bf16 as two
+    // 64-column halves of 16 KB (128-byte rows each, 128-byte swizzle).
+    static constexpr uint32_t kABytes = W16 ? 2u * 128u * 128u : 128u * 128u;
+    static constexpr uint32_t kLBytes = W16 ? 128u * 128u : 0u;  // W16: E4M3 weight landing slot
     // TWO_SM: each CTA of the pair holds BN/2 weight rows.
-    static constexpr uint32_t kBBytes = static_cast<uint32_t>(TWO_SM ? BN / 2 : BN) * 128u;
+    // (W16: bf16 activations, two 64-column halves of BN x 128 bytes.)
+    static constexpr uint32_t kBBytes = static_cast<uint32_t>(TWO_SM ? BN / 2 : BN) * (W16 ? 256u : 128u);
     static constexpr uint32_t kSABytes = BLOCKWISE ? static_cast<uint32_t>(kTokTile) * 4u : 0u;  // TMA box
     // Scale slots are 128-byte aligned (TMA destination alignment).
     static constexpr uint32_t kSASlot = BLOCKWISE ? (kSABytes + 127u) / 128u * 128u : 0u;
@@ -147,7 +159,7 @@ struct GemmCfg {
     static constexpr int kXStages = FQ ? STAGES : 0;
     static constexpr uint32_t kXBytes = FQ ? static_cast<uint32_t>(BN) * 256u : 0u;
     static constexpr uint32_t kStageTx = TWO_SM ? 2u * (kABytes + kBBytes)
-                                                : (FQ ? kABytes : kABytes + kBBytes + kSABytes);
+                                                : (FQ ? kABytes : (W16 ? kLBytes : kABytes + kBBytes + kSABytes));
     // Two accumulator slots, allocated as a power of two >= 32 columns.
     static constexpr uint32_t kTmemCols = 2 * kSlotCols <= 32 ? 32u : 2 * kSlotCols <= 64 ? 64u
                                         : 2 * kSlotCols <= 128 ? 128u : 2 * kSlotCols <= 256 ? 256u : 512u;
@@ -165,8 +177,10 @@ struct GemmCfg {
     static constexpr uint32_t kRecvBytes = kPush ? 144u * kPartStride * 4u : 0u;
     static constexpr uint32_t kOffRecv = kOffSA + STAGES * kSASlot;
     static constexpr uint32_t kOffX = (kOffRecv + kRecvBytes + 127u) / 128u * 128u;
-    static constexpr uint32_t kOffBar = kOffX + kXStages * kXBytes;
-    static constexpr uint32_t kNumBars = 2 * STAGES + 6;  // full, empty, tfull[2], tempty[2], drain, recv
+    static constexpr uint32_t kOffL = (kOffX + kXStages * kXBytes + 1023u) / 1024u * 1024u;  // W16 landing ring
+    static constexpr uint32_t kOffBar = kOffL + STAGES * kLBytes;
+    // full, empty, tfull[2], tempty[2], drain, recv (+ W16: lfull[STAGES])
+    static constexpr uint32_t kNumBars = 2 * STAGES + 6 + (W16 ? STAGES : 0);
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr uint32_t kOffCol = (kOffMisc + 16 + 15) / 16 * 16;  // staged column scale, bias
     // Non-swapped tiles store their output through one 2 KB staging buffer
@@ -177,7 +191,7 @@ struct GemmCfg {
     static constexpr uint32_t kSmemBytes =
         (kTmaStore ? kOffStage + kEpiWarps * kStageBufBytes : kOffCol + 2u * BN * 4u) + 1024u;  // + alignment slack
     static constexpr uint32_t kRedBytes = 128u * (BN + 4) * 4u;  // padded partial tile
-    static constexpr uint32_t kIdesc = idesc_e4m3_f32<TWO_SM ? 256 : 128, BN>();
+    static constexpr uint32_t kIdesc = W16 ? idesc_bf16_f32<128, BN>() : idesc_e4m3_f32<TWO_SM ? 256 : 128, BN>();
     static_assert(!TWO_SM || (!SWAP && !BLOCKWISE && BN == 256), "2-CTA MMA: non-swapped channelwise 256");
     static_assert(kRedBytes <= kOffSA, "the split-K partial tile must fit in the stage ring");
     static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
@@ -185,6 +199,7 @@ struct GemmCfg {
     static_assert(kCols % 32 == 0 || kCols == 16, "epilogue column chunking");
     static_assert(2 * kSlotCols <= 512, "TMEM columns");
     static_assert(!FQ || (BLOCKWISE && SWAP && BN == 16 && !TWO_SM), "fused quantization: blockwise 16-token tiles");
+    static_assert(!W16 || (!BLOCKWISE && SWAP && !TWO_SM && !FQ && BN <= 32), "W16: swapped channelwise tiles");
 };
 
 // Waits that only give up on the time limit (used while draining).
@@ -299,13 +314,14 @@ __device__ __forceinline__ void store_box_tma(const CUtensorMap *tm_out, uint8_t
     }
 }
 
-template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT, bool TWO_SM = false, bool FQ = false>
-__global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ>::kThreads, 1)
+template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT, bool TWO_SM = false, bool FQ = false,
+          bool W16 = false>
+__global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ, W16>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sa, const __grid_constant__ CUtensorMap tm_out,
                     const GemmArgs p)
 {
-    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ>;
+    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ, W16>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sA = smem + C::kOffA;
@@ -318,6 +334,8 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
     uint64_t *drain = tempty + 2;
     uint64_t *recv_full = drain + 1;
     uint8_t *sX = smem + C::kOffX;              // FQ: bf16 activation tiles
+    uint8_t *sL = smem + C::kOffL;              // W16: E4M3 weight landing slots
+    uint64_t *lfull = recv_full + 1;            // W16: weight slot landed
     float *sRecv = reinterpret_cast<float *>(smem + C::kOffRecv);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
@@ -372,8 +390,10 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
         if (BLOCKWISE) tma_prefetch_map(&tm_sa);
         if (C::kTmaStore) tma_prefetch_map(&tm_out);
         for (int s = 0; s < STAGES; ++s) {
-            // FQ: the quantizing warps' arrivals publish the B tile.
-            mbar_init(&full[s], 1 + C::kQuantWarps);
+            // FQ: the quantizing warps' arrivals publish the B tile; W16: the
+            // converting warps' arrivals publish the bf16 A tile.
+            mbar_init(&full[s], 1 + C::kQuantWarps + C::kConvWarps);
+            if (W16) mbar_init(&lfull[s], 1);
             mbar_init(&empty[s], (BLOCKWISE ? C::kEpiWarps : 0) + ((pair && !TWO_SM) ? 2 : C::kIssuers));
         }
         for (int i = 0; i < 2; ++i) {
@@ -429,8 +449,10 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
             coords(cluster_id, a_t, b_t);
             const CUtensorMap *wmap = SWAP ? &tm_a : &tm_b;
             const int wrow = SWAP ? a_t * 128 : b_t * BN;
-            uint8_t *wbuf = SWAP ? sA : sB;
-            const uint32_t wbytes = SWAP ? C::kABytes : C::kBBytes;
+            // (W16: the E4M3 weight slices land in their own slots.)
+            uint8_t *wbuf = W16 ? sL : (SWAP ? sA : sB);
+            const uint32_t wbytes = W16 ? C::kLBytes : (SWAP ? C::kABytes : C::kBBytes);
+            uint64_t *wbar = W16 ? lfull : full;
             const uint64_t pol_w = SWAP ? policy_evict_first() : policy_evict_normal();
             npre = p.preload ? (nkb < STAGES ? nkb : STAGES) : 0;
             for (int i = 0; i < npre; ++i) {
@@ -440,12 +462,12 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                                      pol_w);
                     continue;
                 }
-                mbar_arrive_expect_tx(&full[i], C::kStageTx);
+                mbar_arrive_expect_tx(&wbar[i], C::kStageTx);
                 if (pair)
                     tma_load_2d_mc(wbuf + i * wbytes + w_half_off, wmap, &full[i], (kb_begin + i) * 128,
                                    wrow + w_half_row, 3, pol_w);
                 else
-                    tma_load_2d(wbuf + i * wbytes, wmap, &full[i], (kb_begin + i) * 128, wrow, pol_w);
+                    tma_load_2d(wbuf + i * wbytes, wmap, &wbar[i], (kb_begin + i) * 128, wrow, pol_w);
             }
             const int pf = nkb < p.prefetch_kb ? nkb : p.prefetch_kb;
             for (int i = npre; i < pf; ++i) tma_prefetch_l2_2d(wmap, (kb_begin + i) * 128, wrow + w_half_row);
@@ -491,6 +513,20 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                                              b_row + w_half_row, pol_b);
                         }
                         tma_load_2d_pair(sA + stage * C::kABytes, &tm_a, lead_full(stage), kb * 128, a_row, pol_a);
+                    } else if (W16) {
+                        // E4M3 weight slice into its landing slot (for the
+                        // converting warps), bf16 activation slice as two
+                        // 64-column halves into the B slot.
+                        if (issued >= npre) {
+                            if (!mbar_wait(&empty[stage], phase ^ 1u, abort, p.status)) { ok = false; break; }
+                            mbar_arrive_expect_tx(&lfull[stage], C::kLBytes);
+                            tma_load_2d(sL + stage * C::kLBytes, &tm_a, &lfull[stage], kb * 128, a_row, pol_a);
+                        }
+                        mbar_arrive_expect_tx(&full[stage], C::kBBytes);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            tma_load_2d(sB + stage * C::kBBytes + h * (BN * 128), &tm_b, &full[stage], kb * 128 + 64 * h,
+                                        b_row, pol_b);
                     } else if (issued < npre) {
                         // Weight slice already in flight; barrier armed.
                         if (FQ) {
@@ -529,6 +565,9 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
             if (!TWO_SM || leader)
                 for (long long j = first; j < issued; ++j)
                     mbar_wait_drain(&full[j % STAGES], static_cast<uint32_t>((j / STAGES) & 1), p.status);
+            if (W16)
+                for (long long j = first; j < issued; ++j)
+                    mbar_wait_drain(&lfull[j % STAGES], static_cast<uint32_t>((j / STAGES) & 1), p.status);
             // Paired: the partner's MMA commits arrive on this CTA's empty
             // barriers; every one of them must have landed before exit.
             if (pair)
@@ -561,15 +600,22 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                     const uint32_t b_addr = smem_u32(sB + stage * C::kBBytes);
                     const uint32_t d = tmem_base + slot * C::kSlotCols + static_cast<uint32_t>(issuer * BN);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
+                    for (int k = 0; k < C::kKSteps; ++k) {
                         if (C::kIssuers > 1 && k % C::kIssuers != issuer) continue;
                         const uint32_t acc = BLOCKWISE ? (k > 0) : (i > 0 || k >= C::kIssuers);
-                        if (TWO_SM)
+                        if (TWO_SM) {
                             umma_e4m3_pair(d, umma_desc_sw128(a_addr + k * 32), umma_desc_sw128(b_addr + k * 32),
                                            C::kIdesc, acc);
-                        else
+                        } else if (W16) {
+                            // K step k (16 bf16 = 32 bytes) lies in 64-column
+                            // half k / 4 of each operand slot.
+                            const uint32_t ao = static_cast<uint32_t>((k >> 2) * 16384 + (k & 3) * 32);
+                            const uint32_t bo = static_cast<uint32_t>((k >> 2) * (BN * 128) + (k & 3) * 32);
+                            umma_bf16(d, umma_desc_sw128(a_addr + ao), umma_desc_sw128(b_addr + bo), C::kIdesc, acc);
+                        } else {
                             umma_e4m3(d, umma_desc_sw128(a_addr + k * 32), umma_desc_sw128(b_addr + k * 32),
                                       C::kIdesc, acc);
+                        }
                     }
                     if (TWO_SM) umma_commit_pair_mc(&empty[stage], 3);
                     else if (pair) umma_commit_mc(&empty[stage], 3);
@@ -681,6 +727,54 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
             cp_async_wait_all();   // no copy may still be writing when the CTA exits
         }
         __syncwarp();
+    } else if (W16 && warp >= C::kConvWarp0) {
+        // ------------------------------------------------------------------
+        // Converting warps (W16): once block g's E4M3 weight slice has landed
+        // (128 rows x 128 bytes, 128-byte swizzled by the TMA), convert it
+        // to bf16 -- exact: every E4M3 value is a bf16 value -- into the A
+        // slot of its ring stage: two 64-column halves of 128-byte rows, the
+        // same 128-byte swizzle.  A landed 16-byte unit at position pu of row
+        // r holds K bytes 16 * (pu ^ (r & 7)) ..; they become bf16 units
+        // 2 * (that & 3) and + 1 of half (that >> 2), placed at their
+        // swizzled positions.  The slot is free: the landing load of block g
+        // was issued after the block STAGES earlier left the stage.
+        // ------------------------------------------------------------------
+        if constexpr (W16) {
+            const int ct = threadIdx.x - 32 * C::kConvWarp0;  // 0 .. 127
+            const long long total =
+                cluster_id < p.num_tiles
+                    ? static_cast<long long>((p.num_tiles - 1 - cluster_id) / num_clusters + 1) * nkb
+                    : 0;
+            uint32_t stage = 0, phase = 0;
+            for (long long g = 0; g < total; ++g) {
+                const bool got = mbar_wait(&lfull[stage], phase, abort, p.status);
+                if (!__all_sync(0xffffffffu, got)) break;
+                const uint8_t *ls = sL + stage * C::kLBytes;
+                uint8_t *as = sA + stage * C::kABytes;
+#pragma unroll 2
+                for (int u = ct; u < 1024; u += 128) {
+                    const int r = u >> 3, pu = u & 7;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(ls + r * 128 + pu * 16);
+                    const int lu = pu ^ (r & 7);
+                    const int lb = (lu & 3) * 2;
+                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                    uint32_t o[8];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        o[2 * q] = e4m3x2_to_bf16x2(static_cast<uint16_t>(wv[q] & 0xFFFFu));
+                        o[2 * q + 1] = e4m3x2_to_bf16x2(static_cast<uint16_t>(wv[q] >> 16));
+                    }
+                    uint8_t *row = as + (lu >> 2) * 16384 + r * 128;
+                    *reinterpret_cast<uint4 *>(row + ((lb ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4 *>(row + (((lb + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[stage]);
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        __syncwarp();
     } else {
         // ------------------------------------------------------------------
         // Epilogue warps
@@ -714,7 +808,8 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
             for (int c = etid; c < BN; c += C::kEpiThreads) {
                 if (SWAP) {
                     const int m = m0 + c;
-                    sColScale[c] = (!BLOCKWISE && m < p.M) ? __ldg(p.a_scale + m) : 0.0f;
+                    // (W16: no activation scale)
+                    sColScale[c] = (!BLOCKWISE && m < p.M) ? (W16 ? 1.0f : __ldg(p.a_scale + m)) : 0.0f;
                     sColBias[c] = 0.0f;
                 } else {
                     const int n = n0 + c;

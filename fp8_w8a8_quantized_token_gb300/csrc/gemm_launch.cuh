@@ -13,11 +13,12 @@ namespace fp8q {
 
 constexpr int kMaxDevices = 64;
 
-template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT, bool TWO_SM = false, bool FQ = false>
+template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT, bool TWO_SM = false, bool FQ = false,
+          bool W16 = false>
 cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigned *status, cudaStream_t st)
 {
-    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ>;
-    auto kernel = fp8_gemm_kernel<SWAP, BN, STAGES, BLOCKWISE, OutT, TWO_SM, FQ>;
+    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ, W16>;
+    auto kernel = fp8_gemm_kernel<SWAP, BN, STAGES, BLOCKWISE, OutT, TWO_SM, FQ, W16>;
 
     static std::atomic<uint64_t> attr_done[kMaxDevices / 64 + 1];
     int dev = 0;
@@ -42,9 +43,16 @@ cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigne
         return cudaErrorInvalidValue;
     // FQ: the bf16 activations are copied by the kernel's quantizing warps
     // (GemmArgs::x); the activation map slot holds the weight map, unused.
+    // W16: bf16 activations [M, K] with row stride lda, boxes of 64 columns
+    // (128 bytes) x the tile's tokens, 128-byte swizzle: two per K block.
     if (FQ)
         tm_x = tm_w;
-    else if (!make_tmap_2d(&tm_x, pr.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(pr.K),
+    else if (W16) {
+        if (!make_tmap_2d(&tm_x, pr.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<uint64_t>(pr.K),
+                          static_cast<uint64_t>(pr.M), static_cast<uint64_t>(pr.lda) * 2u, 64, tok_box,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    } else if (!make_tmap_2d(&tm_x, pr.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(pr.K),
                            static_cast<uint64_t>(pr.M), static_cast<uint64_t>(pr.K), 128, tok_box,
                            CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;

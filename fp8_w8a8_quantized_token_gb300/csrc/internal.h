@@ -46,6 +46,7 @@ struct GemmProblem {
     bool blockwise;
     bool preload;           // weights may be read before the dependency wait
     bool fused_quant;       // blockwise: a is bf16, quantized inside the GEMM (group 128, eps)
+    bool w16;               // channelwise weight-only FP8: a is bf16 (row stride lda), no a_scale
     float eps;              // fused_quant: amax floor of the group scales
 };
 
@@ -69,6 +70,11 @@ constexpr int stages_for(bool swap_ab, int mma_n)
 // tiles): 4 slots of 16 KB + 2 KB plus a 4-slot bf16 staging ring of 4 KB
 // keep it near 100 KB, so two CTAs still fit on one SM.
 constexpr int kFusedQuantStages = 4;
+
+// Ring depth of the weight-only FP8 (W16) instantiations: a slot holds the
+// E4M3 weight landing tile (16 KB), its bf16 conversion (32 KB) and the
+// bf16 activation tile (BN x 256 bytes).
+constexpr int kW16Stages = 3;
 
 // Ring depth of the 2-CTA MMA instantiation (each slot: 16 KB of tokens +
 // 16 KB, the CTA's half, of weight rows).

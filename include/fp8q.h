@@ -248,6 +248,29 @@ FP8Q_API fp8q_status fp8q_linear_blockwise(const void *x, const void *w, const f
                                   void *stream);
 
 /* ---------------------------------------------------------------------------
+ * fp8q_scaled_mm_w8a16 -- weight-only FP8 linear (W8A16): bf16 activations
+ * against E4M3 weights with one fp32 scale per output channel, the
+ * weight-only linear of [PR31340] "Implementation breakdown" / "Key source
+ * snippets" (apply_fp8_marlin_linear(input, weight, weight_scale, ...,
+ * bias): no input scale):
+ *   out[m,n] = round(sum_k x[m,k] * e4m3(w[n,k]) * w_scale[n] + bias[n])
+ * computed as fp32-accumulated bf16 x bf16 MMAs on the weights converted
+ * exactly to bf16 in shared memory (tcgen05.mma kind::f16); a per-tensor
+ * weight scale is the case of equal entries.  Tiles of 128 weight rows x
+ * 16 (M <= 16) or 32 tokens, K split across a cluster while the tiles do
+ * not fill the GPU: the decode regime the weight-only format is for (any M
+ * works; larger M simply takes more token tiles).
+ * x       : bf16 [M, K], row stride ldx >= K (ldx % 8 == 0), 16-byte aligned.
+ * w       : e4m3 [N, K] row-major, row stride ldw >= K (ldw % 16 == 0).
+ * w_scale : fp32 [N].  bias: bf16 [N] or NULL.  out: [M, N] (row stride N).
+ * Errors  : INVALID_ARG for M < 0, N, K <= 0, K % 16, N % 8, bad strides,
+ *           null or misaligned pointers; UNSUPPORTED for other out_dtype.
+ * ------------------------------------------------------------------------- */
+FP8Q_API fp8q_status fp8q_scaled_mm_w8a16(const void *x, int64_t ldx, const void *w, int64_t ldw,
+                                 const float *w_scale, const void *bias, void *out, int64_t M,
+                                 int64_t N, int64_t K, fp8q_out_dtype out_dtype, void *stream);
+
+/* ---------------------------------------------------------------------------
  * fp8q_linear_blockwise_fused -- the blockwise linear layer in ONE kernel:
  * the row-padded group-128 quantization of fp8q_linear_blockwise is done
  * inside the GEMM, on the activation tiles it consumes (the quantization
