@@ -548,6 +548,43 @@ def main():
                       "two_kernel_hbm_frac": round(fb / (tu * 1e-6) / 1e9 / peaks["hbm_gbs"], 3)})
     del fcopies
 
+    # ---- weight-only FP8 (W8A16: bf16 activations, no quantizer) against the
+    # W8A8 linear (quantizer + GEMM) at decode sizes: 8 back-to-back launches
+    # per graph over rotating weight copies (> L2), CUDA events; algorithmic
+    # bytes of W8A16 = N*K (E4M3 weights) + 2*M*K + 2*M*N + 4*N.
+    w16 = []
+    for (wl, wN, wK) in (("o_proj", 4096, 4096), ("gate_up", 24576, 4096)):
+        ww = synthetic.weights(wN, wK).to(dev)
+        wwq0, wws = fq.fp8q_quant_per_token(ww)
+        del ww
+        wcp = [wwq0] + [wwq0.clone() for _ in range(reps - 1)]
+        for wM in (1, 16):
+            wx = synthetic.activations(wM, wK, outliers=True).to(dev)
+            wxq = torch.empty((wM, wK), dtype=fq.E4M3, device=dev)
+            wxs = torch.empty((wM,), dtype=torch.float32, device=dev)
+            wout = torch.empty((wM, wN), dtype=torch.bfloat16, device=dev)
+
+            def body_w16(st, wx=wx, wM=wM, wout=wout, wcp=wcp, wN=wN, wK=wK):
+                for r in range(reps):
+                    if L.fp8q_scaled_mm_w8a16(P(wx.data_ptr()), wK, P(wcp[r].data_ptr()), wK, P(wws.data_ptr()),
+                                              None, P(wout.data_ptr()), wM, wN, wK, 0, P(st.cuda_stream)) != 0:
+                        raise RuntimeError("w8a16 failed")
+
+            def body_w8(st, wx=wx, wM=wM, wout=wout, wcp=wcp, wN=wN, wK=wK, wxq=wxq, wxs=wxs):
+                for r in range(reps):
+                    if L.fp8q_linear_channelwise(P(wx.data_ptr()), P(wcp[r].data_ptr()), wK, P(wws.data_ptr()),
+                                                 None, P(wout.data_ptr()), wM, wN, wK, P(wxq.data_ptr()),
+                                                 P(wxs.data_ptr()), 0, P(st.cuda_stream)) != 0:
+                        raise RuntimeError("linear failed")
+
+            u16 = time_graph(body_w16, reps)
+            u8 = time_graph(body_w8, reps)
+            wb = wN * wK + 2 * wM * wK + 2 * wM * wN + 4 * wN
+            w16.append({"shape": wl, "M": wM, "N": wN, "K": wK, "w8a16_us": round(u16, 3),
+                        "w8a8_linear_us": round(u8, 3),
+                        "w8a16_hbm_frac": round(wb / (u16 * 1e-6) / 1e9 / peaks["hbm_gbs"], 3)})
+        del wcp
+
     # ---- end to end through the C ABI with host buffers --------------------
     h2d = sum(p["x"].numel() * 2 for p in problems)
     d2h = sum(p["out"].numel() * 2 for p in problems)
@@ -630,7 +667,7 @@ def main():
                           "8 back-to-back launches of each problem's kernel (GEMMs over rotating weight copies)",
                 "clocks": clk.summary(),
                 "kernel_time_us": {"quant": round(quant_total, 2), "gemm": round(gemm_total, 2)},
-                "sweep": sweep, "quant_variants": variants, "fused_quant_linear": fused}
+                "sweep": sweep, "quant_variants": variants, "fused_quant_linear": fused, "w8a16": w16}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

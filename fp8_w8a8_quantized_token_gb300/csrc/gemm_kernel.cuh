@@ -129,9 +129,10 @@ struct GemmCfg {
     static constexpr int kQuantWarps = FQ ? 2 : 0;
     static constexpr int kQuantWarp0 = kEpiWarp0 + kEpiWarps;
     // W16 (weight-only FP8, bf16 activations; swapped channelwise tiles):
-    // four warps after the epilogue warps convert each landed E4M3 weight
-    // tile to bf16 (exact) for kind::f16 MMAs.
-    static constexpr int kConvWarps = W16 ? 4 : 0;
+    // eight warps after the epilogue warps (two per SM sub-partition, so one
+    // hides the other's latency) convert each landed E4M3 weight tile to
+    // bf16 (exact) for kind::f16 MMAs.
+    static constexpr int kConvWarps = W16 ? 8 : 0;
     static constexpr int kConvWarp0 = kQuantWarp0 + kQuantWarps;
     static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps + kQuantWarps + kConvWarps);
     // K steps of one 128-wide K block: 4 MMAs of K = 32 (E4M3) or, W16, 8
@@ -143,10 +144,17 @@ struct GemmCfg {
     // A operand slot: 128 rows x 128 K of E4M3, or (W16) of bf16 as two
     // 64-column halves of 16 KB (128-byte rows each, 128-byte swizzle).
     static constexpr uint32_t kABytes = W16 ? 2u * 128u * 128u : 128u * 128u;
-    static constexpr uint32_t kLBytes = W16 ? 128u * 128u : 0u;  // W16: E4M3 weight landing slot
+    // W16: a landing ring, deeper than the MMA ring, of slots holding one K
+    // block's E4M3 weight tile (16 KB, converted by the converting warps) and
+    // its bf16 activation tile (two 64-column halves of BN x 128 bytes, read
+    // by the MMA in place).
+    static constexpr uint32_t kLBytes = W16 ? 128u * 128u : 0u;
+    static constexpr uint32_t kXBBytes = W16 ? static_cast<uint32_t>(BN) * 256u : 0u;
+    static constexpr uint32_t kLSlotBytes = kLBytes + kXBBytes;
+    static constexpr int kLStages = W16 ? (BN == 16 ? 6 : 5) : 0;
     // TWO_SM: each CTA of the pair holds BN/2 weight rows.
-    // (W16: bf16 activations, two 64-column halves of BN x 128 bytes.)
-    static constexpr uint32_t kBBytes = static_cast<uint32_t>(TWO_SM ? BN / 2 : BN) * (W16 ? 256u : 128u);
+    // (W16: none; the activation tiles stay in the landing ring.)
+    static constexpr uint32_t kBBytes = W16 ? 0u : static_cast<uint32_t>(TWO_SM ? BN / 2 : BN) * 128u;
     static constexpr uint32_t kSABytes = BLOCKWISE ? static_cast<uint32_t>(kTokTile) * 4u : 0u;  // TMA box
     // Scale slots are 128-byte aligned (TMA destination alignment).
     static constexpr uint32_t kSASlot = BLOCKWISE ? (kSABytes + 127u) / 128u * 128u : 0u;
@@ -159,7 +167,7 @@ struct GemmCfg {
     static constexpr int kXStages = FQ ? STAGES : 0;
     static constexpr uint32_t kXBytes = FQ ? static_cast<uint32_t>(BN) * 256u : 0u;
     static constexpr uint32_t kStageTx = TWO_SM ? 2u * (kABytes + kBBytes)
-                                                : (FQ ? kABytes : (W16 ? kLBytes : kABytes + kBBytes + kSABytes));
+                                                : (FQ ? kABytes : (W16 ? kLSlotBytes : kABytes + kBBytes + kSABytes));
     // Two accumulator slots, allocated as a power of two >= 32 columns.
     static constexpr uint32_t kTmemCols = 2 * kSlotCols <= 32 ? 32u : 2 * kSlotCols <= 64 ? 64u
                                         : 2 * kSlotCols <= 128 ? 128u : 2 * kSlotCols <= 256 ? 256u : 512u;
@@ -178,9 +186,9 @@ struct GemmCfg {
     static constexpr uint32_t kOffRecv = kOffSA + STAGES * kSASlot;
     static constexpr uint32_t kOffX = (kOffRecv + kRecvBytes + 127u) / 128u * 128u;
     static constexpr uint32_t kOffL = (kOffX + kXStages * kXBytes + 1023u) / 1024u * 1024u;  // W16 landing ring
-    static constexpr uint32_t kOffBar = kOffL + STAGES * kLBytes;
-    // full, empty, tfull[2], tempty[2], drain, recv (+ W16: lfull[STAGES])
-    static constexpr uint32_t kNumBars = 2 * STAGES + 6 + (W16 ? STAGES : 0);
+    static constexpr uint32_t kOffBar = kOffL + kLStages * kLSlotBytes;
+    // full, empty, tfull[2], tempty[2], drain, recv (+ W16: lfull, lempty[kLStages])
+    static constexpr uint32_t kNumBars = 2 * STAGES + 6 + 2 * kLStages;
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr uint32_t kOffCol = (kOffMisc + 16 + 15) / 16 * 16;  // staged column scale, bias
     // Non-swapped tiles store their output through one 2 KB staging buffer
@@ -335,7 +343,9 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
     uint64_t *recv_full = drain + 1;
     uint8_t *sX = smem + C::kOffX;              // FQ: bf16 activation tiles
     uint8_t *sL = smem + C::kOffL;              // W16: E4M3 weight landing slots
-    uint64_t *lfull = recv_full + 1;            // W16: weight slot landed
+    uint64_t *lfull = recv_full + 1;            // W16: landing slot filled
+    uint64_t *lempty = lfull + C::kLStages;     // W16: landing slot read (converters + MMAs)
+    constexpr int kLS = C::kLStages > 0 ? C::kLStages : 1;  // (non-W16 builds never use the landing ring)
     float *sRecv = reinterpret_cast<float *>(smem + C::kOffRecv);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
@@ -391,9 +401,8 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
         if (C::kTmaStore) tma_prefetch_map(&tm_out);
         for (int s = 0; s < STAGES; ++s) {
             // FQ: the quantizing warps' arrivals publish the B tile; W16: the
-            // converting warps' arrivals publish the bf16 A tile.
-            mbar_init(&full[s], 1 + C::kQuantWarps + C::kConvWarps);
-            if (W16) mbar_init(&lfull[s], 1);
+            // converting warps' arrivals alone publish the bf16 A tile.
+            mbar_init(&full[s], W16 ? C::kConvWarps : 1 + C::kQuantWarps);
             mbar_init(&empty[s], (BLOCKWISE ? C::kEpiWarps : 0) + ((pair && !TWO_SM) ? 2 : C::kIssuers));
         }
         for (int i = 0; i < 2; ++i) {
@@ -402,6 +411,10 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
         }
         mbar_init(drain, C::kIssuers);
         mbar_init(recv_full, 1);
+        for (int j = 0; j < C::kLStages; ++j) {
+            mbar_init(&lfull[j], 1);
+            mbar_init(&lempty[j], C::kConvWarps + C::kIssuers);
+        }
 
         *abort = 0;
         fence_mbar_init();
@@ -451,10 +464,11 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
             const int wrow = SWAP ? a_t * 128 : b_t * BN;
             // (W16: the E4M3 weight slices land in their own slots.)
             uint8_t *wbuf = W16 ? sL : (SWAP ? sA : sB);
-            const uint32_t wbytes = W16 ? C::kLBytes : (SWAP ? C::kABytes : C::kBBytes);
+            const uint32_t wbytes = W16 ? C::kLSlotBytes : (SWAP ? C::kABytes : C::kBBytes);
             uint64_t *wbar = W16 ? lfull : full;
+            const int ring = W16 ? C::kLStages : STAGES;
             const uint64_t pol_w = SWAP ? policy_evict_first() : policy_evict_normal();
-            npre = p.preload ? (nkb < STAGES ? nkb : STAGES) : 0;
+            npre = p.preload ? (nkb < ring ? nkb : ring) : 0;
             for (int i = 0; i < npre; ++i) {
                 if (TWO_SM) {
                     if (leader) mbar_arrive_expect_tx(&full[i], C::kStageTx);
@@ -514,19 +528,22 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                         }
                         tma_load_2d_pair(sA + stage * C::kABytes, &tm_a, lead_full(stage), kb * 128, a_row, pol_a);
                     } else if (W16) {
-                        // E4M3 weight slice into its landing slot (for the
-                        // converting warps), bf16 activation slice as two
-                        // 64-column halves into the B slot.
+                        // Block `issued` into landing slot j: its E4M3 weight
+                        // tile (already in flight if preloaded; for the
+                        // converting warps) and its bf16 activation tile as
+                        // two 64-column halves (read by the MMA in place).
+                        const int j = static_cast<int>(issued % kLS);
+                        uint8_t *slot = sL + j * C::kLSlotBytes;
                         if (issued >= npre) {
-                            if (!mbar_wait(&empty[stage], phase ^ 1u, abort, p.status)) { ok = false; break; }
-                            mbar_arrive_expect_tx(&lfull[stage], C::kLBytes);
-                            tma_load_2d(sL + stage * C::kLBytes, &tm_a, &lfull[stage], kb * 128, a_row, pol_a);
+                            const uint32_t lph = static_cast<uint32_t>((issued / kLS) & 1);
+                            if (!mbar_wait(&lempty[j], lph ^ 1u, abort, p.status)) { ok = false; break; }
+                            mbar_arrive_expect_tx(&lfull[j], C::kStageTx);
+                            tma_load_2d(slot, &tm_a, &lfull[j], kb * 128, a_row, pol_a);
                         }
-                        mbar_arrive_expect_tx(&full[stage], C::kBBytes);
 #pragma unroll
                         for (int h = 0; h < 2; ++h)
-                            tma_load_2d(sB + stage * C::kBBytes + h * (BN * 128), &tm_b, &full[stage], kb * 128 + 64 * h,
-                                        b_row, pol_b);
+                            tma_load_2d(slot + C::kLBytes + h * (BN * 128), &tm_b, &lfull[j], kb * 128 + 64 * h, b_row,
+                                        pol_b);
                     } else if (issued < npre) {
                         // Weight slice already in flight; barrier armed.
                         if (FQ) {
@@ -562,12 +579,15 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
             if (issued < npre) issued = npre;
             const long long first = issued > STAGES ? issued - STAGES : 0;
             // (TWO_SM: only the even CTA's full barriers are used.)
-            if (!TWO_SM || leader)
+            // (W16: the copies go to the landing ring.)
+            if (W16) {
+                const long long lfirst = issued > kLS ? issued - kLS : 0;
+                for (long long j = lfirst; j < issued; ++j)
+                    mbar_wait_drain(&lfull[j % kLS], static_cast<uint32_t>((j / kLS) & 1), p.status);
+            } else if (!TWO_SM || leader) {
                 for (long long j = first; j < issued; ++j)
                     mbar_wait_drain(&full[j % STAGES], static_cast<uint32_t>((j / STAGES) & 1), p.status);
-            if (W16)
-                for (long long j = first; j < issued; ++j)
-                    mbar_wait_drain(&lfull[j % STAGES], static_cast<uint32_t>((j / STAGES) & 1), p.status);
+            }
             // Paired: the partner's MMA commits arrive on this CTA's empty
             // barriers; every one of them must have landed before exit.
             if (pair)
@@ -582,6 +602,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
         const int issuer = warp - 1;
         if (lane == 0 && (!TWO_SM || leader)) {
             uint32_t stage = 0, phase = 0, slot = 0, tphase = 0;
+            long long gm = 0;  // W16: K blocks consumed so far (landing slot gm % kLStages)
             bool ok = true;
             for (int tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
                 if (!BLOCKWISE) {
@@ -597,7 +618,9 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                     tc_fence_after();
                     if (tile == cluster_id && i == 0 && issuer == 0) FP8Q_TRACE_AT(p, kTrFirstMma);
                     const uint32_t a_addr = smem_u32(sA + stage * C::kABytes);
-                    const uint32_t b_addr = smem_u32(sB + stage * C::kBBytes);
+                    const int lj = W16 ? static_cast<int>(gm % kLS) : 0;
+                    const uint32_t b_addr =
+                        W16 ? smem_u32(sL + lj * C::kLSlotBytes + C::kLBytes) : smem_u32(sB + stage * C::kBBytes);
                     const uint32_t d = tmem_base + slot * C::kSlotCols + static_cast<uint32_t>(issuer * BN);
 #pragma unroll
                     for (int k = 0; k < C::kKSteps; ++k) {
@@ -620,6 +643,10 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                     if (TWO_SM) umma_commit_pair_mc(&empty[stage], 3);
                     else if (pair) umma_commit_mc(&empty[stage], 3);
                     else umma_commit(&empty[stage]);
+                    if (W16) {
+                        umma_commit(&lempty[lj]);   // the activation tile was read in place
+                        ++gm;
+                    }
                     if (BLOCKWISE) {
                         umma_commit(&tfull[slot]);
                         slot ^= 1u;
@@ -729,40 +756,50 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
         __syncwarp();
     } else if (W16 && warp >= C::kConvWarp0) {
         // ------------------------------------------------------------------
-        // Converting warps (W16): once block g's E4M3 weight slice has landed
-        // (128 rows x 128 bytes, 128-byte swizzled by the TMA), convert it
-        // to bf16 -- exact: every E4M3 value is a bf16 value -- into the A
-        // slot of its ring stage: two 64-column halves of 128-byte rows, the
-        // same 128-byte swizzle.  A landed 16-byte unit at position pu of row
-        // r holds K bytes 16 * (pu ^ (r & 7)) ..; they become bf16 units
-        // 2 * (that & 3) and + 1 of half (that >> 2), placed at their
-        // swizzled positions.  The slot is free: the landing load of block g
-        // was issued after the block STAGES earlier left the stage.
+        // Converting warps (W16): once block g's tiles have landed (slot
+        // g % kLStages of the landing ring) and the A slot of its ring stage
+        // has been read by the MMA STAGES blocks earlier, convert the E4M3
+        // weight tile (128 rows x 128 bytes, 128-byte swizzled by the TMA) to
+        // bf16 -- exact: every E4M3 value is a bf16 value -- into that A slot:
+        // two 64-column halves of 128-byte rows, the same swizzle.  A landed
+        // 16-byte unit at position pu of row r holds K bytes 16 * (pu ^ (r &
+        // 7)) ..; they become bf16 units 2 * (that & 3) and + 1 of half
+        // (that >> 2), placed at their swizzled positions.
         // ------------------------------------------------------------------
         if constexpr (W16) {
-            const int ct = threadIdx.x - 32 * C::kConvWarp0;  // 0 .. 127
+            const int ct = threadIdx.x - 32 * C::kConvWarp0;  // 0 .. 32 * kConvWarps - 1
+            constexpr int kUnits = 1024 / (32 * C::kConvWarps);  // 16-byte landed units per thread
             const long long total =
                 cluster_id < p.num_tiles
                     ? static_cast<long long>((p.num_tiles - 1 - cluster_id) / num_clusters + 1) * nkb
                     : 0;
             uint32_t stage = 0, phase = 0;
             for (long long g = 0; g < total; ++g) {
-                const bool got = mbar_wait(&lfull[stage], phase, abort, p.status);
+                const int j = static_cast<int>(g % kLS);
+                bool got = mbar_wait(&lfull[j], static_cast<uint32_t>((g / kLS) & 1), abort, p.status);
+                got = got && mbar_wait(&empty[stage], phase ^ 1u, abort, p.status);   // A slot read by its MMA
                 if (!__all_sync(0xffffffffu, got)) break;
-                const uint8_t *ls = sL + stage * C::kLBytes;
+                const uint8_t *ls = sL + j * C::kLSlotBytes;
                 uint8_t *as = sA + stage * C::kABytes;
-#pragma unroll 2
-                for (int u = ct; u < 1024; u += 128) {
+                uint4 vin[kUnits];
+#pragma unroll
+                for (int q = 0; q < kUnits; ++q) {
+                    const int u = ct + q * 32 * C::kConvWarps;
+                    vin[q] = *reinterpret_cast<const uint4 *>(ls + (u >> 3) * 128 + (u & 7) * 16);
+                }
+#pragma unroll
+                for (int q = 0; q < kUnits; ++q) {
+                    const int u = ct + q * 32 * C::kConvWarps;
                     const int r = u >> 3, pu = u & 7;
-                    const uint4 v = *reinterpret_cast<const uint4 *>(ls + r * 128 + pu * 16);
+                    const uint4 v = vin[q];
                     const int lu = pu ^ (r & 7);
                     const int lb = (lu & 3) * 2;
                     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
                     uint32_t o[8];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        o[2 * q] = e4m3x2_to_bf16x2(static_cast<uint16_t>(wv[q] & 0xFFFFu));
-                        o[2 * q + 1] = e4m3x2_to_bf16x2(static_cast<uint16_t>(wv[q] >> 16));
+                    for (int e = 0; e < 4; ++e) {
+                        o[2 * e] = e4m3x2_to_bf16x2(static_cast<uint16_t>(wv[e] & 0xFFFFu));
+                        o[2 * e + 1] = e4m3x2_to_bf16x2(static_cast<uint16_t>(wv[e] >> 16));
                     }
                     uint8_t *row = as + (lu >> 2) * 16384 + r * 128;
                     *reinterpret_cast<uint4 *>(row + ((lb ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -770,7 +807,10 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&full[stage]);
+                if (lane == 0) {
+                    mbar_arrive(&full[stage]);
+                    mbar_arrive(&lempty[j]);   // the weight tile is converted
+                }
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }

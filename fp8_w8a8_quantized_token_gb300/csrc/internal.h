@@ -71,10 +71,10 @@ constexpr int stages_for(bool swap_ab, int mma_n)
 // keep it near 100 KB, so two CTAs still fit on one SM.
 constexpr int kFusedQuantStages = 4;
 
-// Ring depth of the weight-only FP8 (W16) instantiations: a slot holds the
-// E4M3 weight landing tile (16 KB), its bf16 conversion (32 KB) and the
-// bf16 activation tile (BN x 256 bytes).
-constexpr int kW16Stages = 3;
+// Depth of the bf16 weight ring of the weight-only FP8 (W16) instantiations
+// (32 KB slots); the E4M3 weight and bf16 activation tiles stream through a
+// deeper landing ring of their own (gemm_kernel.cuh).
+constexpr int kW16Stages = 2;
 
 // Ring depth of the 2-CTA MMA instantiation (each slot: 16 KB of tokens +
 // 16 KB, the CTA's half, of weight rows).
