@@ -867,7 +867,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                 constexpr int kPromoteCols = C::kCols >= 128 ? 16 : 32;
 #pragma unroll
                 for (int j = 0; j < C::kCols; ++j) acc[j] = 0.0f;
-                const int wblk = SWAP ? a_t : (n0 >> 7) + cgroup;  // 128-row weight block
+                const int wblk = SWAP ? a_t : (n0 + col0) >> 7;  // 128-row weight block of these columns
                 const float *sw_row = p.w_scale + static_cast<long long>(wblk) * p.num_kb;
                 for (int i = 0; i < nkb; ++i) {
                     const int kb = kb_begin + i;
