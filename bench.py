@@ -394,17 +394,22 @@ def main():
     # copies (> L2 in total), timed with CUDA events on the launching stream.
     reps = 8
 
-    def time_graph(body, n_launch):
+    def time_graph(body, n_launch, repeats=5):
+        """Microseconds per launch: the median over `repeats` measurements,
+        each kernel_replays graph replays (>= 100 back-to-back launches)."""
         g = capture(body)
-        e0, e1 = mk(), mk()
         g.replay()
         torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(args.kernel_replays):
-            g.replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) * 1e3 / (args.kernel_replays * n_launch)
+        samples = []
+        for _ in range(repeats):
+            e0, e1 = mk(), mk()
+            e0.record(stream)
+            for _ in range(args.kernel_replays):
+                g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            samples.append(e0.elapsed_time(e1) * 1e3 / (args.kernel_replays * n_launch))
+        return statistics.median(samples)
 
     g_us, q_us = [], []
     for i, p in enumerate(problems):
@@ -663,8 +668,9 @@ def main():
                            "M": ms, "l2": l2note, "parallelism": f"replicas x{world}" if world > 1 else "single"},
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": 2 * len(problems) * args.steps,
-                "timing": "K replays of a CUDA graph holding one step; per-kernel durations from graphs of "
-                          "8 back-to-back launches of each problem's kernel (GEMMs over rotating weight copies)",
+                "timing": "K replays of a CUDA graph holding one step; per-kernel durations: median of 5 "
+                          f"measurements, each {args.kernel_replays} replays of a graph of 8 back-to-back "
+                          "launches of the problem's kernel (GEMMs over rotating weight copies)",
                 "clocks": clk.summary(),
                 "kernel_time_us": {"quant": round(quant_total, 2), "gemm": round(gemm_total, 2)},
                 "sweep": sweep, "quant_variants": variants, "fused_quant_linear": fused, "w8a16": w16}
