@@ -1,7 +1,7 @@
 // plan.cpp -- GEMM schedule selection (host only).
 //
-// A compiled-in table keyed by (N, K, scheme) holds the schedules the
-// build's own sweep on GB300 found fastest at a set of M values; a problem
+// A compiled-in table keyed by (N, K, scheme) holds the schedules that
+// tune.py's sweep on GB300 found fastest at a set of M values; a problem
 // takes the entry of the nearest M, ties going to the smaller M (the
 // nearest-M rule of get_w8a8_channelwise_fp8_config on the "Tune FP8 GEMM
 // Triton tiles on L40S and enable by default" page, key source snippets,

@@ -77,7 +77,7 @@ extern "C" {
 typedef enum {
     FP8Q_OK = 0,
     FP8Q_ERR_INVALID_ARG = 1, /* null pointer, bad size, stride or alignment */
-    FP8Q_ERR_UNSUPPORTED = 2, /* a shape or option this build does not implement */
+    FP8Q_ERR_UNSUPPORTED = 2, /* a shape or option the library does not implement */
     FP8Q_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
     FP8Q_ERR_TIMEOUT = 4      /* a device-side pipeline wait ran out of time */
 } fp8q_status;

@@ -93,8 +93,9 @@ def load_table():
 
 
 def test_table_lookup_is_nearest_m_with_ties_to_the_smaller_m():
-    """The rule of get_w8a8_channelwise_fp8_config: configs[min(keys, key=|k - M|)]
-    with keys scanned in ascending order, so a tie goes to the smaller key."""
+    """The rule of get_w8a8_channelwise_fp8_config: the entry of the key
+    nearest to M, keys scanned in ascending order, so a tie goes to the
+    smaller key."""
     rows = load_table()
     assert rows, "the sweep table is empty"
     by_shape = {}
