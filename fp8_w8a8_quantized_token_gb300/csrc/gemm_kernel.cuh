@@ -144,17 +144,18 @@ struct GemmCfg {
     // A operand slot: 128 rows x 128 K of E4M3, or (W16) of bf16 as two
     // 64-column halves of 16 KB (128-byte rows each, 128-byte swizzle).
     static constexpr uint32_t kABytes = W16 ? 2u * 128u * 128u : 128u * 128u;
-    // W16: a landing ring, deeper than the MMA ring, of slots holding one K
-    // block's E4M3 weight tile (16 KB, converted by the converting warps) and
-    // its bf16 activation tile (two 64-column halves of BN x 128 bytes, read
-    // by the MMA in place).
+    // W16: a landing ring of slots holding one K block's E4M3 weight tile
+    // (16 KB) and its bf16 activation tile (two 64-column halves of BN x 128
+    // bytes).  The converting warps empty a slot as soon as they have turned
+    // the weights into the A tile and copied the activations into the B
+    // tile of an MMA ring stage, so the landing slots never wait for MMAs.
     static constexpr uint32_t kLBytes = W16 ? 128u * 128u : 0u;
     static constexpr uint32_t kXBBytes = W16 ? static_cast<uint32_t>(BN) * 256u : 0u;
     static constexpr uint32_t kLSlotBytes = kLBytes + kXBBytes;
-    static constexpr int kLStages = W16 ? (BN == 16 ? 6 : 5) : 0;
-    // TWO_SM: each CTA of the pair holds BN/2 weight rows.
-    // (W16: none; the activation tiles stay in the landing ring.)
-    static constexpr uint32_t kBBytes = W16 ? 0u : static_cast<uint32_t>(TWO_SM ? BN / 2 : BN) * 128u;
+    static constexpr int kLStages = W16 ? 5 : 0;
+    // TWO_SM: each CTA of the pair holds BN/2 weight rows.  W16: the bf16
+    // activation tile copied out of the landing slot.
+    static constexpr uint32_t kBBytes = W16 ? kXBBytes : static_cast<uint32_t>(TWO_SM ? BN / 2 : BN) * 128u;
     static constexpr uint32_t kSABytes = BLOCKWISE ? static_cast<uint32_t>(kTokTile) * 4u : 0u;  // TMA box
     // Scale slots are 128-byte aligned (TMA destination alignment).
     static constexpr uint32_t kSASlot = BLOCKWISE ? (kSABytes + 127u) / 128u * 128u : 0u;
@@ -344,7 +345,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
     uint8_t *sX = smem + C::kOffX;              // FQ: bf16 activation tiles
     uint8_t *sL = smem + C::kOffL;              // W16: E4M3 weight landing slots
     uint64_t *lfull = recv_full + 1;            // W16: landing slot filled
-    uint64_t *lempty = lfull + C::kLStages;     // W16: landing slot read (converters + MMAs)
+    uint64_t *lempty = lfull + C::kLStages;     // W16: landing slot read by the converting warps
     constexpr int kLS = C::kLStages > 0 ? C::kLStages : 1;  // (non-W16 builds never use the landing ring)
     float *sRecv = reinterpret_cast<float *>(smem + C::kOffRecv);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
@@ -413,7 +414,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
         mbar_init(recv_full, 1);
         for (int j = 0; j < C::kLStages; ++j) {
             mbar_init(&lfull[j], 1);
-            mbar_init(&lempty[j], C::kConvWarps + C::kIssuers);
+            mbar_init(&lempty[j], C::kConvWarps);
         }
 
         *abort = 0;
@@ -529,9 +530,9 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                         tma_load_2d_pair(sA + stage * C::kABytes, &tm_a, lead_full(stage), kb * 128, a_row, pol_a);
                     } else if (W16) {
                         // Block `issued` into landing slot j: its E4M3 weight
-                        // tile (already in flight if preloaded; for the
-                        // converting warps) and its bf16 activation tile as
-                        // two 64-column halves (read by the MMA in place).
+                        // tile (already in flight if preloaded) and its bf16
+                        // activation tile as two 64-column halves, both for
+                        // the converting warps.
                         const int j = static_cast<int>(issued % kLS);
                         uint8_t *slot = sL + j * C::kLSlotBytes;
                         if (issued >= npre) {
@@ -602,7 +603,6 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
         const int issuer = warp - 1;
         if (lane == 0 && (!TWO_SM || leader)) {
             uint32_t stage = 0, phase = 0, slot = 0, tphase = 0;
-            long long gm = 0;  // W16: K blocks consumed so far (landing slot gm % kLStages)
             bool ok = true;
             for (int tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
                 if (!BLOCKWISE) {
@@ -618,9 +618,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                     tc_fence_after();
                     if (tile == cluster_id && i == 0 && issuer == 0) FP8Q_TRACE_AT(p, kTrFirstMma);
                     const uint32_t a_addr = smem_u32(sA + stage * C::kABytes);
-                    const int lj = W16 ? static_cast<int>(gm % kLS) : 0;
-                    const uint32_t b_addr =
-                        W16 ? smem_u32(sL + lj * C::kLSlotBytes + C::kLBytes) : smem_u32(sB + stage * C::kBBytes);
+                    const uint32_t b_addr = smem_u32(sB + stage * C::kBBytes);
                     const uint32_t d = tmem_base + slot * C::kSlotCols + static_cast<uint32_t>(issuer * BN);
 #pragma unroll
                     for (int k = 0; k < C::kKSteps; ++k) {
@@ -643,10 +641,6 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                     if (TWO_SM) umma_commit_pair_mc(&empty[stage], 3);
                     else if (pair) umma_commit_mc(&empty[stage], 3);
                     else umma_commit(&empty[stage]);
-                    if (W16) {
-                        umma_commit(&lempty[lj]);   // the activation tile was read in place
-                        ++gm;
-                    }
                     if (BLOCKWISE) {
                         umma_commit(&tfull[slot]);
                         slot ^= 1u;
@@ -764,11 +758,16 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
         // two 64-column halves of 128-byte rows, the same swizzle.  A landed
         // 16-byte unit at position pu of row r holds K bytes 16 * (pu ^ (r &
         // 7)) ..; they become bf16 units 2 * (that & 3) and + 1 of half
-        // (that >> 2), placed at their swizzled positions.
+        // (that >> 2), placed at their swizzled positions.  The bf16
+        // activation tile is copied unchanged into the stage's B slot (both
+        // 1024-byte aligned, so the swizzle carries over), and the landing
+        // slot is free again.
         // ------------------------------------------------------------------
         if constexpr (W16) {
             const int ct = threadIdx.x - 32 * C::kConvWarp0;  // 0 .. 32 * kConvWarps - 1
             constexpr int kUnits = 1024 / (32 * C::kConvWarps);  // 16-byte landed units per thread
+            constexpr int kXUnits = static_cast<int>(C::kXBBytes / 16u) / (32 * C::kConvWarps);  // activation units
+            static_assert(static_cast<int>(C::kXBBytes / 16u) % (32 * C::kConvWarps) == 0, "activation units");
             const long long total =
                 cluster_id < p.num_tiles
                     ? static_cast<long long>((p.num_tiles - 1 - cluster_id) / num_clusters + 1) * nkb
@@ -781,35 +780,48 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                 if (!__all_sync(0xffffffffu, got)) break;
                 const uint8_t *ls = sL + j * C::kLSlotBytes;
                 uint8_t *as = sA + stage * C::kABytes;
-                uint4 vin[kUnits];
+                uint4 vin[kUnits], xin[kXUnits];
 #pragma unroll
                 for (int q = 0; q < kUnits; ++q) {
                     const int u = ct + q * 32 * C::kConvWarps;
                     vin[q] = *reinterpret_cast<const uint4 *>(ls + (u >> 3) * 128 + (u & 7) * 16);
                 }
 #pragma unroll
+                for (int q = 0; q < kXUnits; ++q)
+                    xin[q] = *reinterpret_cast<const uint4 *>(ls + C::kLBytes + (ct + q * 32 * C::kConvWarps) * 16);
+#pragma unroll
+                for (int q = 0; q < kXUnits; ++q)
+                    *reinterpret_cast<uint4 *>(sB + stage * C::kBBytes + (ct + q * 32 * C::kConvWarps) * 16) = xin[q];
+#pragma unroll
                 for (int q = 0; q < kUnits; ++q) {
                     const int u = ct + q * 32 * C::kConvWarps;
                     const int r = u >> 3, pu = u & 7;
                     const uint4 v = vin[q];
                     const int lu = pu ^ (r & 7);
+                    const int hi = lu >> 2;                // 64-column half of the A tile
                     const int lb = (lu & 3) * 2;
-                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                    // The eight lanes of a row (one 16-byte store phase) hold
+                    // units lu and lu ^ 4 in pairs, whose bf16 units lie at the
+                    // same positions of the two halves: the upper-half lanes
+                    // store their second 8 bytes' bf16 unit first, so each
+                    // store hits eight distinct positions (no bank conflict).
+                    const uint32_t wv[4] = {hi ? v.z : v.x, hi ? v.w : v.y, hi ? v.x : v.z, hi ? v.y : v.w};
                     uint32_t o[8];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         o[2 * e] = e4m3x2_to_bf16x2(static_cast<uint16_t>(wv[e] & 0xFFFFu));
                         o[2 * e + 1] = e4m3x2_to_bf16x2(static_cast<uint16_t>(wv[e] >> 16));
                     }
-                    uint8_t *row = as + (lu >> 2) * 16384 + r * 128;
-                    *reinterpret_cast<uint4 *>(row + ((lb ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-                    *reinterpret_cast<uint4 *>(row + (((lb + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+                    uint8_t *row = as + hi * 16384 + r * 128;
+                    *reinterpret_cast<uint4 *>(row + (((lb + hi) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4 *>(row + (((lb + 1 - hi) ^ (r & 7)) << 4)) =
+                        make_uint4(o[4], o[5], o[6], o[7]);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&full[stage]);
-                    mbar_arrive(&lempty[j]);   // the weight tile is converted
+                    mbar_arrive(&lempty[j]);   // both tiles are out of the landing slot
                 }
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }

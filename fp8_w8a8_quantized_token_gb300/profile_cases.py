@@ -33,6 +33,7 @@ CASES = {
     "quant_group": ("quant_group", 8192, 0, 12288),
     "quant_silu_group": ("quant_silu_group", 4096, 0, 12288),   # input [4096, 2 x 12288]
     "quant_static": ("quant_static", 16384, 0, 4096),
+    "w8a16_gateup": ("w8a16", 1, 24576, 4096),
 }
 
 
@@ -58,7 +59,12 @@ def run(case: str, dev) -> None:
             fq.fp8q_quant_static_per_tensor(x, s)
         return
     w = synthetic.weights(N, K).to(dev)
-    if kind == "channelwise":
+    if kind == "w8a16":
+        wq, ws = fq.fp8q_quant_per_token(w)
+        torch.cuda.synchronize()
+        for _ in range(WARMUP + 1):
+            fq.fp8q_scaled_mm_w8a16(x, wq, ws)
+    elif kind == "channelwise":
         wq, ws = fq.fp8q_quant_per_token(w)
         xq, xs = fq.fp8q_quant_per_token(x)
         torch.cuda.synchronize()

@@ -53,6 +53,30 @@ def test_w8a16_bias_fp16_and_long_k(dev):
     _case(dev, 3, 1024, 7168, bias=True, seed=4)
 
 
+@pytest.mark.parametrize("M", [16, 32])
+def test_w8a16_every_e4m3_code_converts_exactly(dev, M):
+    """One-hot activation rows pick single weights: with unit weight scales,
+    out[m, n] = w[n, m] exactly (an E4M3 value is a bf16 value), so every
+    finite code, subnormals and both zeros included, must come out as the
+    oracle's decode of it -- an exhaustive check of the on-chip E4M3 -> bf16
+    conversion on the 16- and 32-token tiles."""
+    N, K = 128, 256
+    rng = np.random.default_rng(11)
+    codes = rng.integers(0, 256, (N, K)).astype(np.uint8)
+    codes[:, :M] = ((np.arange(N)[:, None] * M + np.arange(M)[None, :]) & 0xFF).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x00                # the two NaN codes are outside the contract
+    assert np.unique(codes[:, :M]).size == 254
+    x = torch.zeros((M, K), dtype=torch.bfloat16)
+    x[torch.arange(M), torch.arange(M)] = 1.0
+    wq = torch.from_numpy(codes).to(dev).view(fq.E4M3)
+    ws = torch.ones(N, dtype=torch.float32, device=dev)
+    out = fq.fp8q_scaled_mm_w8a16(x.to(dev), wq, ws)
+    torch.cuda.synchronize()
+    want = oracle.e4m3_decode(codes[:, :M]).reshape(N, M).T
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert np.array_equal(got, want)
+
+
 def test_w8a16_strided_input_and_m0(dev):
     M, N, K, ldx = 9, 512, 1024, 1536
     big = synthetic.activations(M, ldx, outliers=True, seed=5)
