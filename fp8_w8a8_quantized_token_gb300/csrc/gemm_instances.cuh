@@ -14,9 +14,9 @@ cudaError_t dispatch_gemm(const GemmProblem &p, const GemmLaunch &l, unsigned *s
         // Weight-only FP8 (bf16 activations): swapped 16- or 32-token tiles.
         if constexpr (!BLOCKWISE) {
             if (l.swap_ab && l.mma_n == 16)
-                return launch_gemm_inst<true, 16, w16_stages(16), false, OutT, false, false, true>(p, l, status, st);
+                return launch_gemm_inst<true, 16, kW16Stages, false, OutT, false, false, true>(p, l, status, st);
             if (l.swap_ab && l.mma_n == 32)
-                return launch_gemm_inst<true, 32, w16_stages(32), false, OutT, false, false, true>(p, l, status, st);
+                return launch_gemm_inst<true, 32, kW16Stages, false, OutT, false, false, true>(p, l, status, st);
         }
         return cudaErrorInvalidValue;
     }

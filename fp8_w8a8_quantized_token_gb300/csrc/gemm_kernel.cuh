@@ -141,9 +141,10 @@ struct GemmCfg {
     static constexpr int kEpiThreads = 32 * kEpiWarps;
     static constexpr int kTokTile = SWAP ? BN : 128;     // tokens per tile
     static constexpr int kColTile = SWAP ? 128 : BN;     // output columns per tile
-    // A operand slot: 128 rows x 128 K of E4M3, or (W16) of bf16 as two
-    // 64-column halves of 16 KB (128-byte rows each, 128-byte swizzle).
-    static constexpr uint32_t kABytes = W16 ? 2u * 128u * 128u : 128u * 128u;
+    // A operand slot: 128 rows x 128 K of E4M3.  (W16: none; the bf16 A
+    // tiles are in tensor memory, kATmemCols columns per ring stage from
+    // column kATmemCol0, after the two accumulator slots.)
+    static constexpr uint32_t kABytes = W16 ? 0u : 128u * 128u;
     // W16: a landing ring of slots holding one K block's E4M3 weight tile
     // (16 KB) and its bf16 activation tile (two 64-column halves of BN x 128
     // bytes).  The converting warps empty a slot as soon as they have turned
@@ -152,7 +153,7 @@ struct GemmCfg {
     static constexpr uint32_t kLBytes = W16 ? 128u * 128u : 0u;
     static constexpr uint32_t kXBBytes = W16 ? static_cast<uint32_t>(BN) * 256u : 0u;
     static constexpr uint32_t kLSlotBytes = kLBytes + kXBBytes;
-    static constexpr int kLStages = W16 ? 5 : 0;
+    static constexpr int kLStages = W16 ? (BN == 16 ? 8 : 7) : 0;
     // TWO_SM: each CTA of the pair holds BN/2 weight rows.  W16: the bf16
     // activation tile copied out of the landing slot.
     static constexpr uint32_t kBBytes = W16 ? kXBBytes : static_cast<uint32_t>(TWO_SM ? BN / 2 : BN) * 128u;
@@ -169,9 +170,13 @@ struct GemmCfg {
     static constexpr uint32_t kXBytes = FQ ? static_cast<uint32_t>(BN) * 256u : 0u;
     static constexpr uint32_t kStageTx = TWO_SM ? 2u * (kABytes + kBBytes)
                                                 : (FQ ? kABytes : (W16 ? kLSlotBytes : kABytes + kBBytes + kSABytes));
-    // Two accumulator slots, allocated as a power of two >= 32 columns.
-    static constexpr uint32_t kTmemCols = 2 * kSlotCols <= 32 ? 32u : 2 * kSlotCols <= 64 ? 64u
-                                        : 2 * kSlotCols <= 128 ? 128u : 2 * kSlotCols <= 256 ? 256u : 512u;
+    // Two accumulator slots (+ W16: the bf16 A tiles of the ring stages, 128
+    // K values = 64 columns each), allocated as a power of two >= 32 columns.
+    static constexpr uint32_t kATmemCol0 = 2u * kSlotCols;
+    static constexpr uint32_t kATmemCols = 64u;
+    static constexpr uint32_t kTmemNeed = kATmemCol0 + (W16 ? STAGES * kATmemCols : 0u);
+    static constexpr uint32_t kTmemCols = kTmemNeed <= 32 ? 32u : kTmemNeed <= 64 ? 64u
+                                        : kTmemNeed <= 128 ? 128u : kTmemNeed <= 256 ? 256u : 512u;
     static constexpr uint32_t kOffA = 0;
     static constexpr uint32_t kOffB = kOffA + STAGES * kABytes;
     static constexpr uint32_t kOffSA = kOffB + STAGES * kBBytes;
@@ -209,6 +214,7 @@ struct GemmCfg {
     static_assert(2 * kSlotCols <= 512, "TMEM columns");
     static_assert(!FQ || (BLOCKWISE && SWAP && BN == 16 && !TWO_SM), "fused quantization: blockwise 16-token tiles");
     static_assert(!W16 || (!BLOCKWISE && SWAP && !TWO_SM && !FQ && BN <= 32), "W16: swapped channelwise tiles");
+    static_assert(kTmemNeed <= 512, "tensor memory budget exceeded");
 };
 
 // Waits that only give up on the time limit (used while draining).
@@ -628,11 +634,13 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                             umma_e4m3_pair(d, umma_desc_sw128(a_addr + k * 32), umma_desc_sw128(b_addr + k * 32),
                                            C::kIdesc, acc);
                         } else if (W16) {
-                            // K step k (16 bf16 = 32 bytes) lies in 64-column
-                            // half k / 4 of each operand slot.
-                            const uint32_t ao = static_cast<uint32_t>((k >> 2) * 16384 + (k & 3) * 32);
+                            // K step k (16 bf16): TMEM columns 8k .. 8k + 7 of
+                            // the stage's A tile; 32 bytes in 64-column half
+                            // k / 4 of the B slot.
+                            const uint32_t at = tmem_base + C::kATmemCol0 + stage * C::kATmemCols +
+                                                static_cast<uint32_t>(k * 8);
                             const uint32_t bo = static_cast<uint32_t>((k >> 2) * (BN * 128) + (k & 3) * 32);
-                            umma_bf16(d, umma_desc_sw128(a_addr + ao), umma_desc_sw128(b_addr + bo), C::kIdesc, acc);
+                            umma_bf16_tmem_a(d, at, umma_desc_sw128(b_addr + bo), C::kIdesc, acc);
                         } else {
                             umma_e4m3(d, umma_desc_sw128(a_addr + k * 32), umma_desc_sw128(b_addr + k * 32),
                                       C::kIdesc, acc);
@@ -751,23 +759,28 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
     } else if (W16 && warp >= C::kConvWarp0) {
         // ------------------------------------------------------------------
         // Converting warps (W16): once block g's tiles have landed (slot
-        // g % kLStages of the landing ring) and the A slot of its ring stage
-        // has been read by the MMA STAGES blocks earlier, convert the E4M3
-        // weight tile (128 rows x 128 bytes, 128-byte swizzled by the TMA) to
-        // bf16 -- exact: every E4M3 value is a bf16 value -- into that A slot:
-        // two 64-column halves of 128-byte rows, the same swizzle.  A landed
-        // 16-byte unit at position pu of row r holds K bytes 16 * (pu ^ (r &
-        // 7)) ..; they become bf16 units 2 * (that & 3) and + 1 of half
-        // (that >> 2), placed at their swizzled positions.  The bf16
-        // activation tile is copied unchanged into the stage's B slot (both
-        // 1024-byte aligned, so the swizzle carries over), and the landing
-        // slot is free again.
+        // g % kLStages of the landing ring) and the A tile of its ring stage
+        // has been read by the MMAs STAGES blocks earlier, convert the E4M3
+        // weight tile (128 rows x 128 bytes, 128-byte swizzled by the TMA:
+        // logical 16-byte unit L of row m at position L ^ (m & 7)) to bf16 --
+        // exact: every E4M3 value is a bf16 value -- into that stage's A tile
+        // in tensor memory.  Weight row m is TMEM lane m, so warp w (lanes
+        // 32 (w % 4) ..) converts rows 32 (w % 4) + lane, the first four
+        // warps K 0..63 of the block, the next four K 64..127: each thread
+        // one row's 64 bytes into 32 columns.  The bf16 activation tile is
+        // copied unchanged into the stage's B slot (both 1024-byte aligned,
+        // so the swizzle carries over), and the landing slot is free again.
         // ------------------------------------------------------------------
         if constexpr (W16) {
+            static_assert(C::kConvWarps == 8, "two warps per TMEM lane quarter");
             const int ct = threadIdx.x - 32 * C::kConvWarp0;  // 0 .. 32 * kConvWarps - 1
-            constexpr int kUnits = 1024 / (32 * C::kConvWarps);  // 16-byte landed units per thread
+            const int quarter = warp & 3;                      // TMEM lanes this warp may access
+            const int khalf = (warp - C::kConvWarp0) >> 2;     // K half of the block
+            const int m = quarter * 32 + lane;                 // weight row of the tile = TMEM lane
             constexpr int kXUnits = static_cast<int>(C::kXBBytes / 16u) / (32 * C::kConvWarps);  // activation units
             static_assert(static_cast<int>(C::kXBBytes / 16u) % (32 * C::kConvWarps) == 0, "activation units");
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + C::kATmemCol0 +
+                                   static_cast<uint32_t>(khalf * 32);
             const long long total =
                 cluster_id < p.num_tiles
                     ? static_cast<long long>((p.num_tiles - 1 - cluster_id) / num_clusters + 1) * nkb
@@ -776,47 +789,37 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
             for (long long g = 0; g < total; ++g) {
                 const int j = static_cast<int>(g % kLS);
                 bool got = mbar_wait(&lfull[j], static_cast<uint32_t>((g / kLS) & 1), abort, p.status);
-                got = got && mbar_wait(&empty[stage], phase ^ 1u, abort, p.status);   // A slot read by its MMA
+                got = got && mbar_wait(&empty[stage], phase ^ 1u, abort, p.status);   // A tile read by its MMAs
                 if (!__all_sync(0xffffffffu, got)) break;
+                tc_fence_after();
                 const uint8_t *ls = sL + j * C::kLSlotBytes;
-                uint8_t *as = sA + stage * C::kABytes;
-                uint4 vin[kUnits], xin[kXUnits];
+                uint4 vin[4], xin[kXUnits];
+                // Units 4 khalf .. 4 khalf + 3 of row m: the eight rows of a
+                // store phase hit eight distinct positions (no bank conflict).
 #pragma unroll
-                for (int q = 0; q < kUnits; ++q) {
-                    const int u = ct + q * 32 * C::kConvWarps;
-                    vin[q] = *reinterpret_cast<const uint4 *>(ls + (u >> 3) * 128 + (u & 7) * 16);
-                }
+                for (int i = 0; i < 4; ++i)
+                    vin[i] = *reinterpret_cast<const uint4 *>(ls + m * 128 + (((4 * khalf + i) ^ (m & 7)) << 4));
 #pragma unroll
                 for (int q = 0; q < kXUnits; ++q)
                     xin[q] = *reinterpret_cast<const uint4 *>(ls + C::kLBytes + (ct + q * 32 * C::kConvWarps) * 16);
 #pragma unroll
                 for (int q = 0; q < kXUnits; ++q)
                     *reinterpret_cast<uint4 *>(sB + stage * C::kBBytes + (ct + q * 32 * C::kConvWarps) * 16) = xin[q];
+                // Column 8 i + 2 e (+ 1) holds K 16 i + 4 e .. + 1 (+ 2 .. + 3)
+                // of this half: two bf16 per column, the lower K in the low half.
+                uint32_t o[32];
 #pragma unroll
-                for (int q = 0; q < kUnits; ++q) {
-                    const int u = ct + q * 32 * C::kConvWarps;
-                    const int r = u >> 3, pu = u & 7;
-                    const uint4 v = vin[q];
-                    const int lu = pu ^ (r & 7);
-                    const int hi = lu >> 2;                // 64-column half of the A tile
-                    const int lb = (lu & 3) * 2;
-                    // The eight lanes of a row (one 16-byte store phase) hold
-                    // units lu and lu ^ 4 in pairs, whose bf16 units lie at the
-                    // same positions of the two halves: the upper-half lanes
-                    // store their second 8 bytes' bf16 unit first, so each
-                    // store hits eight distinct positions (no bank conflict).
-                    const uint32_t wv[4] = {hi ? v.z : v.x, hi ? v.w : v.y, hi ? v.x : v.z, hi ? v.y : v.w};
-                    uint32_t o[8];
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t wv[4] = {vin[i].x, vin[i].y, vin[i].z, vin[i].w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        o[2 * e] = e4m3x2_to_bf16x2(static_cast<uint16_t>(wv[e] & 0xFFFFu));
-                        o[2 * e + 1] = e4m3x2_to_bf16x2(static_cast<uint16_t>(wv[e] >> 16));
+                        o[8 * i + 2 * e] = e4m3x2_to_bf16x2(static_cast<uint16_t>(wv[e] & 0xFFFFu));
+                        o[8 * i + 2 * e + 1] = e4m3x2_to_bf16x2(static_cast<uint16_t>(wv[e] >> 16));
                     }
-                    uint8_t *row = as + hi * 16384 + r * 128;
-                    *reinterpret_cast<uint4 *>(row + (((lb + hi) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-                    *reinterpret_cast<uint4 *>(row + (((lb + 1 - hi) ^ (r & 7)) << 4)) =
-                        make_uint4(o[4], o[5], o[6], o[7]);
                 }
+                tmem_st32(t_row + stage * C::kATmemCols, o);
+                tmem_st_wait();
+                tc_fence_before();
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {

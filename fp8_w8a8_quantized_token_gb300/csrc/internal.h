@@ -71,12 +71,11 @@ constexpr int stages_for(bool swap_ab, int mma_n)
 // keep it near 100 KB, so two CTAs still fit on one SM.
 constexpr int kFusedQuantStages = 4;
 
-// Depth of the MMA ring of the weight-only FP8 (W16) instantiations (32 KB
-// bf16 weight tile + the token tile's bf16 activations per stage): three at
-// 16 tokens, two at 32, where a third no longer fits beside the landing ring
-// through which the E4M3 weight and bf16 activation tiles stream
-// (gemm_kernel.cuh).
-constexpr int w16_stages(int bn) { return bn == 16 ? 3 : 2; }
+// Depth of the MMA ring of the weight-only FP8 (W16) instantiations: per
+// stage a bf16 A tile in tensor memory (64 columns) and the token tile's bf16
+// activations in shared memory; the E4M3 weight and bf16 activation tiles
+// stream through a deeper landing ring of their own (gemm_kernel.cuh).
+constexpr int kW16Stages = 3;
 
 // Ring depth of the 2-CTA MMA instantiation (each slot: 16 KB of tokens +
 // 16 KB, the CTA's half, of weight rows).
