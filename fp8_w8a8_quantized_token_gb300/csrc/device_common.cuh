@@ -297,18 +297,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32()
            | (static_cast<uint32_t>(M >> 4) << 24);// M / 16
 }
 
-// bf16 x bf16 -> fp32 MMA, K = 16 per instruction.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // bf16 x bf16 -> fp32 MMA, K = 16 per instruction, with A read from tensor
 // memory: row m of A in TMEM lane m (lanes 0..127), K along the columns, two
 // bf16 per 32-bit column (the lower K in the low half): 8 columns per
