@@ -31,6 +31,24 @@ def test_small_integer_lattice_is_exact():
     assert np.array_equal(got, _round_bf16(ref.astype(np.float64)))
 
 
+def test_one_hot_rows_read_every_finite_code():
+    """One-hot activation rows pick single weights: with unit scales,
+    out[m, n] is the weight code w[n, m] decoded, for all 254 finite codes
+    (subnormals and both zeros included), against torch's own float8_e4m3fn
+    conversion (independent of the oracle's codec)."""
+    M, N, K = 16, 128, 256
+    rng = np.random.default_rng(12)
+    codes = rng.integers(0, 256, (N, K)).astype(np.uint8)
+    codes[:, :M] = ((np.arange(N)[:, None] * M + np.arange(M)[None, :]) & 0xFF).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x00
+    assert np.unique(codes[:, :M]).size == 254
+    x = torch.zeros((M, K), dtype=torch.bfloat16)
+    x[torch.arange(M), torch.arange(M)] = 1.0
+    out = oracle.gemm_w8a16(x, codes, np.ones(N, np.float32))
+    want = torch.from_numpy(codes[:, :M].copy()).view(torch.float8_e4m3fn).float().numpy().T
+    assert np.array_equal(oracle.bf16_bits_to_float(out), want)
+
+
 def test_against_float64_matmul_of_decoded_operands():
     M, N, K = 7, 48, 384
     x = synthetic.activations(M, K, outliers=True, seed=12)
