@@ -255,8 +255,8 @@ FP8Q_API fp8q_status fp8q_linear_blockwise(const void *x, const void *w, const f
  * bias): no input scale):
  *   out[m,n] = round(sum_k x[m,k] * e4m3(w[n,k]) * w_scale[n] + bias[n])
  * computed as fp32-accumulated bf16 x bf16 MMAs on the weights converted
- * exactly to bf16 in shared memory (tcgen05.mma kind::f16); a per-tensor
- * weight scale is the case of equal entries.  Tiles of 128 weight rows x
+ * exactly to bf16 into tensor memory (tcgen05.mma kind::f16, A operand in
+ * TMEM); a per-tensor weight scale is the case of equal entries.  Tiles of 128 weight rows x
  * 16 (M <= 16) or 32 tokens, K split across a cluster while the tiles do
  * not fill the GPU: the decode regime the weight-only format is for (any M
  * works; larger M simply takes more token tiles).
