@@ -111,3 +111,53 @@ def test_plan_override_validation(lib):
     p = fq.fp8q_gemm_plan(7, 4096, 4096, num_sms=148)
     assert (p["swap_ab"], p["mma_n"], p["split_k"], p["from_table"]) == (1, 32, 3, 0)
     assert lib.fp8q_set_plan_override(-1, 0, 0) == fq.FP8Q_OK
+
+
+def test_variant_entry_points_reject_invalid_arguments_before_any_cuda_call(lib):
+    """The variant, linear and weight-only entry points validate every
+    argument first: each case below fails (or, M = 0, succeeds as a no-op)
+    without touching the device, so it runs without a GPU."""
+    P = ctypes.c_void_p
+    fake, odd = P(0x1000), P(0x1001)   # never dereferenced
+    E = fq.FP8Q_ERR_INVALID_ARG
+    U = fq.FP8Q_ERR_UNSUPPORTED
+    g = lib.fp8q_quant_per_token_group_row_padded_ex
+    assert g(fake, 4, 256, 256, 128, 1e-10, 4, 8, fake, fake, 4, None) == E          # unknown flag bit
+    assert g(fake, 4, 256, 256, 48, 1e-10, 4, 0, fake, fake, 4, None) == U           # group size 48
+    assert g(fake, 4, 256, 256, 0, 1e-10, 4, 0, fake, fake, 4, None) == E            # group size 0
+    assert g(fake, 4, 256, 256, 128, 1e-10, 4, 2, fake, fake, 4, None) == E          # silu: ldx < 2K
+    assert g(fake, 5, 256, 256, 128, 1e-10, 4, 1, fake, fake, 6, None) == E          # m_pad % alignment
+    assert g(None, 0, 256, 512, 64, 1e-10, 4, 3, None, None, 0, None) == fq.FP8Q_OK  # M = 0
+    s = lib.fp8q_quant_static_per_tensor
+    assert s(fake, 4, 24, 24, fake, fake, None, None) == E                           # K % 16
+    assert s(fake, 4, 32, 16, fake, fake, None, None) == E                           # ldx < K
+    assert s(fake, 4, 32, 32, None, fake, None, None) == E                           # no scale
+    assert s(P(0x1008), 4, 32, 32, fake, fake, None, None) == E                      # x not 16-byte aligned
+    assert s(None, 0, 32, 32, None, None, None, None) == fq.FP8Q_OK                  # M = 0
+    wb = lib.fp8q_quant_weight_block128
+    assert wb(fake, 200, 256, fake, fake, 1e-10, None) == U                          # N % 128
+    assert wb(fake, 256, 256, fake, fake, 0.0, None) == E                            # eps
+    lc = lib.fp8q_linear_channelwise
+    assert lc(fake, fake, 64, fake, None, fake, 4, 64, 64, fake, fake, 7, None) == U  # output type
+    assert lc(fake, fake, 64, fake, None, fake, 4, 60, 64, fake, fake, 0, None) == E  # N % 8
+    assert lc(None, None, 64, None, None, None, 0, 64, 64, None, None, 0, None) == fq.FP8Q_OK
+    lb = lib.fp8q_linear_blockwise
+    assert lb(fake, fake, fake, None, fake, 4, 200, 256, fake, fake, 4, 0, None) == U  # N % 128
+    assert lb(fake, fake, fake, None, fake, 5, 256, 256, fake, fake, 6, 0, None) == E  # m_pad % 4
+    assert lb(fake, fake, fake, odd, fake, 4, 256, 256, fake, fake, 4, 0, None) == E   # odd bias address
+    fu = lib.fp8q_linear_blockwise_fused
+    assert fu(fake, 256, fake, fake, None, fake, 4, 200, 256, 0, None) == U           # N % 128
+    assert fu(fake, 128, fake, fake, None, fake, 4, 256, 256, 0, None) == E           # ldx < K
+    assert fu(fake, 256, fake, fake, odd, fake, 4, 256, 256, 0, None) == E            # odd bias address
+    assert fu(None, 256, None, None, None, None, 0, 256, 256, 0, None) == fq.FP8Q_OK  # M = 0
+    w16 = lib.fp8q_scaled_mm_w8a16
+    assert w16(fake, 40, fake, 48, fake, None, fake, 4, 64, 40, 0, None) == E         # K % 16
+    assert w16(fake, 64, fake, 72, fake, None, fake, 4, 64, 64, 0, None) == E         # ldw % 16
+    assert w16(fake, 64, fake, 64, fake, None, fake, 4, 60, 64, 0, None) == E         # N % 8
+    assert w16(fake, 64, fake, 64, fake, None, fake, 4, 64, 64, 5, None) == U         # output type
+    assert w16(fake, 64, None, 64, fake, None, fake, 4, 64, 64, 0, None) == E         # no weights
+    assert w16(fake, 64, fake, 64, fake, odd, fake, 4, 64, 64, 0, None) == E          # odd bias address
+    assert w16(None, 64, None, 64, None, None, None, 0, 64, 64, 0, None) == fq.FP8Q_OK
+    na = lib.fp8q_linear_channelwise_noalloc
+    assert na(fake, fake, 64, fake, None, fake, 4, 64, 0, 0, None) == E               # K <= 0
+    assert na(None, None, 64, None, None, None, 0, 64, 64, 0, None) == fq.FP8Q_OK     # M = 0
