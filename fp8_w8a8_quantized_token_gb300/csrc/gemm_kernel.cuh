@@ -129,9 +129,9 @@ struct GemmCfg {
     static constexpr int kQuantWarps = FQ ? 2 : 0;
     static constexpr int kQuantWarp0 = kEpiWarp0 + kEpiWarps;
     // W16 (weight-only FP8, bf16 activations; swapped channelwise tiles):
-    // eight warps after the epilogue warps (two per SM sub-partition, so one
-    // hides the other's latency) convert each landed E4M3 weight tile to
-    // bf16 (exact) for kind::f16 MMAs.
+    // eight warps after the epilogue warps (two per TMEM lane quarter, one
+    // per 64-wide K half of a block) convert each landed E4M3 weight tile to
+    // bf16 (exact) into tensor memory, the A operand of kind::f16 MMAs.
     static constexpr int kConvWarps = W16 ? 8 : 0;
     static constexpr int kConvWarp0 = kQuantWarp0 + kQuantWarps;
     static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps + kQuantWarps + kConvWarps);
@@ -408,7 +408,8 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
         if (C::kTmaStore) tma_prefetch_map(&tm_out);
         for (int s = 0; s < STAGES; ++s) {
             // FQ: the quantizing warps' arrivals publish the B tile; W16: the
-            // converting warps' arrivals alone publish the bf16 A tile.
+            // converting warps' arrivals alone publish the stage (its bf16 A
+            // tile in tensor memory and its activation B tile).
             mbar_init(&full[s], W16 ? C::kConvWarps : 1 + C::kQuantWarps);
             mbar_init(&empty[s], (BLOCKWISE ? C::kEpiWarps : 0) + ((pair && !TWO_SM) ? 2 : C::kIssuers));
         }
