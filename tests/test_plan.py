@@ -121,3 +121,22 @@ def test_shapes_without_rows_use_the_generic_rule():
     assert p["split_k"] in (1, 2, 4, 8)
     p = fq.fp8q_gemm_plan(4000, 8000, 1024, num_sms=148)
     assert p["from_table"] == 0 and (p["swap_ab"], p["mma_n"], p["split_k"]) == (0, 256, 1)
+
+
+def test_tuner_only_proposes_schedules_the_library_accepts(lib):
+    """tune.py's candidate schedules for every swept (shape, M) are ones the
+    plan override accepts and that fp8q_gemm_plan then launches as a
+    supported instantiation; the non-swapped 256 tile is always among them."""
+    from fp8_w8a8_quantized_token_gb300 import tune
+    try:
+        for label, (N, K, bw, ms) in tune.SHAPES.items():
+            for M in ms:
+                cands = tune.candidates(M)
+                assert any(c[:2] == (0, 256) for c in cands), (label, M)
+                for c in cands:
+                    assert (c[0], c[1]) in SUPPORTED and c[2] in tune.SPLITS, (label, M, c)
+                    assert lib.fp8q_set_plan_override(*c) == fq.FP8Q_OK
+                    plan = fq.fp8q_gemm_plan(M, N, K, bool(bw), num_sms=152)
+                    assert (plan["swap_ab"], plan["mma_n"]) == (c[0], c[1]), (label, M, c, plan)
+    finally:
+        lib.fp8q_set_plan_override(-1, 0, 0)
