@@ -1,13 +1,22 @@
 """Benchmark of the FP8 W8A8 linear layer on GB300.
 
-One step = one pass of the whole hot path over one batch: for every M of the
-sweep, per-token quantization of the bf16 activations followed by the scaled
-FP8 GEMM.  The default workload is the channelwise o_proj linear (N = K =
-4096) over M in {1, 2, 4, ..., 8192}; ``--workload`` selects the other
-linear shapes for measurement runs.
+One pass of the hot path = for every M of the sweep, per-token quantization
+of the bf16 activations followed by the scaled FP8 GEMM (the public linear
+entry point, with its split-K workspace).  The default workload is the
+channelwise o_proj linear (N = K = 4096) over M in {1, 2, 4, ..., 8192};
+``--workload`` selects the other linear shapes for measurement runs.  A
+timed step replays the pass enough times that the timed region lasts at
+least a second whatever --steps is (so the clock sampler running during it
+has samples); the line states the passes per step.
+
+After the headline, the same per-M measurement runs on the other
+configurations (tiny layer, Qwen3-8B-shaped set, blockwise decode and
+blockwise prefill) and each gets a compact block in the line.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
-instead, on a bounded sample of the same workload.
+instead, on a bounded sample of the same workload.  ``--profile-case NAME``
+runs one small fixed case of one kernel (for an Nsight Compute capture) and
+prints nothing else.
 """
 from __future__ import annotations
 
@@ -28,10 +37,31 @@ METRIC = "FP8 W8A8 GEMM TFLOP/s & GB/s vs M (1-8192) and % of roofline"
 UNIT = "TFLOP/s"
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
-# kernel, keyed by (scheme, swap_ab, mma_n), averaged over that kernel's
-# launches in the ncu launch list of this benchmark (profiles/
-# launches_oproj_sweep.md).  A key is dropped whenever its kernel changes.
-DOMINANT_TRAFFIC_BYTES = {("channelwise", 0, 256): 32.86e6}
+# kernel, keyed by (scheme, swap_ab, mma_n), from a one-kernel Nsight
+# Compute capture of its profiling case (--profile-case), scaled to the
+# bench launch by the units it processes where the case is smaller.  A key
+# is dropped whenever its kernel changes.
+DOMINANT_TRAFFIC_BYTES = {}
+
+# Small fixed cases for Nsight Compute captures: name -> (kind, M, N, K).
+PROFILE_CASES = {
+    "prefill_oproj": ("channelwise", 8192, 4096, 4096),
+    "prefill_gateup": ("channelwise", 8192, 24576, 4096),
+    "mid_oproj_256": ("channelwise", 256, 4096, 4096),
+    "mid_oproj_512": ("channelwise", 512, 4096, 4096),
+    "mid_oproj_1024": ("channelwise", 1024, 4096, 4096),
+    "decode_oproj": ("channelwise", 16, 4096, 4096),
+    "decode_down": ("channelwise", 1, 4096, 12288),
+    "blockwise_prefill": ("blockwise", 8192, 24576, 3072),
+    "blockwise_prefill_down": ("blockwise", 8192, 3072, 12288),
+    "blockwise_decode": ("blockwise", 16, 4096, 7168),
+    "quant_token": ("quant_token", 8192, 0, 4096),
+    "quant_group": ("quant_group", 8192, 0, 12288),
+    "quant_silu_group": ("quant_silu_group", 4096, 0, 12288),
+    "quant_static": ("quant_static", 16384, 0, 4096),
+    "w8a16_gateup": ("w8a16", 1, 24576, 4096),
+}
+PROFILE_WARMUP = 2
 
 WORKLOADS = {
     # name: (list of (label, N, K, blockwise), M sweep, outliers)
@@ -232,14 +262,247 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------
+# profiling cases (one kernel, few launches, for Nsight Compute)
+# ---------------------------------------------------------------------------
+
+def run_profile_case(name: str) -> int:
+    """PROFILE_WARMUP + 1 launches of the case's kernel on one stream (inputs
+    prepared first); capture the last with ncu -k regex:<kernel> -s <n> -c 1."""
+    import torch
+
+    import __graft_entry__
+    import fp8_w8a8_quantized_token_gb300 as fq
+    import synthetic
+    if name not in PROFILE_CASES:
+        print("cases:", ", ".join(PROFILE_CASES))
+        return 2
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    kind, M, N, K = PROFILE_CASES[name]
+    x = synthetic.activations(M, K, outliers=True).to(dev)
+    n = PROFILE_WARMUP + 1
+    if kind == "quant_token":
+        for _ in range(n):
+            fq.fp8q_quant_per_token(x)
+    elif kind == "quant_group":
+        for _ in range(n):
+            fq.fp8q_quant_per_token_group_row_padded(x, 128)
+    elif kind == "quant_silu_group":
+        xm = synthetic.activations(M, 2 * K, outliers=True).to(dev)
+        for _ in range(n):
+            fq.fp8q_quant_per_token_group_row_padded(xm, 128, scale_ue8m0=True, fuse_silu_and_mul=True)
+    elif kind == "quant_static":
+        sc = torch.tensor([0.02], dtype=torch.float32, device=dev)
+        for _ in range(n):
+            fq.fp8q_quant_static_per_tensor(x, sc)
+    else:
+        w = synthetic.weights(N, K).to(dev)
+        if kind == "w8a16":
+            wq, ws = fq.fp8q_quant_per_token(w)
+            torch.cuda.synchronize()
+            for _ in range(n):
+                fq.fp8q_scaled_mm_w8a16(x, wq, ws)
+        elif kind == "channelwise":
+            wq, ws = fq.fp8q_quant_per_token(w)
+            xq, xs = fq.fp8q_quant_per_token(x)
+            work = torch.empty(max(1, fq.fp8q_workspace_bytes(M, N, K)), dtype=torch.uint8, device=dev)
+            torch.cuda.synchronize()
+            for _ in range(n):
+                fq.fp8q_scaled_mm_channelwise(xq, wq, xs, ws, workspace=work)
+        else:
+            wq, ws = fq.fp8q_quant_weight_block128(w)
+            xq, xsv = fq.fp8q_quant_per_token_group_row_padded(x, 128)
+            work = torch.empty(max(1, fq.fp8q_workspace_bytes(M, N, K, True)), dtype=torch.uint8, device=dev)
+            torch.cuda.synchronize()
+            for _ in range(n):
+                fq.fp8q_scaled_mm_blockwise(xq, wq, xsv, ws, M=M, workspace=work)
+    torch.cuda.synchronize()
+    assert fq.fp8q_device_status() == fq.FP8Q_OK
+    return 0
+
+
+# ---------------------------------------------------------------------------
 # the CUDA path
 # ---------------------------------------------------------------------------
+
+class Gpu:
+    """Device-side state shared by the measurements: the library, ctypes
+    launchers of the public entry points, graph capture and timing."""
+
+    def __init__(self, dev, L, fq, torch, kernel_replays):
+        import ctypes
+        self.dev, self.L, self.fq, self.torch = dev, L, fq, torch
+        self.P = ctypes.c_void_p
+        self.kernel_replays = kernel_replays
+        self.stream = torch.cuda.current_stream(dev)
+
+    def ptr(self, t):
+        return None if t is None else self.P(t.data_ptr())
+
+    def linear(self, p, sp, wq=None):
+        """The public linear entry point: quantize, then GEMM (two kernels)."""
+        L, P = self.L, self.ptr
+        wq = p["wq"] if wq is None else wq
+        if p["bw"]:
+            st = L.fp8q_linear_blockwise(P(p["x"]), P(wq), P(p["ws"]), None, P(p["out"]), p["M"], p["N"], p["K"],
+                                         P(p["xq"]), P(p["xs"]), p["m_pad"], 0, P(p["work"]), p["work_bytes"], sp)
+        else:
+            st = L.fp8q_linear_channelwise(P(p["x"]), P(wq), p["K"], P(p["ws"]), None, P(p["out"]), p["M"],
+                                           p["N"], p["K"], P(p["xq"]), P(p["xs"]), 0, P(p["work"]), p["work_bytes"],
+                                           sp)
+        if st != 0:
+            raise RuntimeError(f"linear failed: {self.fq.status_str(st)}")
+
+    def gemm(self, p, wq, sp, workspace=True):
+        L, P = self.L, self.ptr
+        work, nbytes = (p["work"], p["work_bytes"]) if workspace else (None, 0)
+        if p["bw"]:
+            st = L.fp8q_scaled_mm_blockwise(P(p["xq"]), P(wq), P(p["xs"]), P(p["ws"]), None, P(p["out"]), p["M"],
+                                            p["m_pad"], p["N"], p["K"], 0, P(work), nbytes, sp)
+        else:
+            st = L.fp8q_scaled_mm_channelwise(P(p["xq"]), P(wq), p["K"], P(p["xs"]), P(p["ws"]), None,
+                                              P(p["out"]), p["M"], p["N"], p["K"], 0, P(work), nbytes, sp)
+        if st != 0:
+            raise RuntimeError(f"gemm failed: {self.fq.status_str(st)}")
+
+    def quant(self, p, sp):
+        L, P = self.L, self.ptr
+        if p["bw"]:
+            st = L.fp8q_quant_per_token_group_row_padded(P(p["x"]), p["M"], p["K"], p["K"], 128, 1e-10, 4,
+                                                         P(p["xq"]), P(p["xs"]), p["m_pad"], sp)
+        else:
+            st = L.fp8q_quant_per_token(P(p["x"]), p["M"], p["K"], p["K"], P(p["xq"]), P(p["xs"]), 1e-10, sp)
+        if st != 0:
+            raise RuntimeError(f"quant failed: {self.fq.status_str(st)}")
+
+    def capture(self, body):
+        """A CUDA graph of body(stream): the library's launches are captured
+        like any other stream work (one eager run first sets kernel
+        attributes outside the capture)."""
+        torch = self.torch
+        side = torch.cuda.Stream(self.dev)
+        side.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(side):
+            body(side)
+        side.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            body(side)
+        torch.cuda.synchronize()
+        return g
+
+    def event(self):
+        return self.torch.cuda.Event(enable_timing=True)
+
+    def time_graph(self, body, n_launch, repeats=5):
+        """Microseconds per launch: the median over `repeats` measurements,
+        each kernel_replays graph replays of body's n_launch launches."""
+        torch = self.torch
+        g = self.capture(body)
+        g.replay()
+        torch.cuda.synchronize()
+        samples = []
+        for _ in range(repeats):
+            e0, e1 = self.event(), self.event()
+            e0.record(self.stream)
+            for _ in range(self.kernel_replays):
+                g.replay()
+            e1.record(self.stream)
+            torch.cuda.synchronize()
+            samples.append(e0.elapsed_time(e1) * 1e3 / (self.kernel_replays * n_launch))
+        return statistics.median(samples)
+
+
+REPS = 8   # back-to-back launches per timing graph
+
+
+def build_problems(gpu, workload):
+    """Inputs resident in HBM for every (shape, M) of a workload: rotating
+    weight copies (more than twice L2 of weight bytes), activations,
+    quantized buffers, outputs and each problem's split-K workspace."""
+    import synthetic
+    fq, torch, dev = gpu.fq, gpu.torch, gpu.dev
+    shapes, ms, outliers = WORKLOADS[workload]
+    problems, wcopies, wbytes_total = [], {}, 0
+    for (label, N, K, bw) in shapes:
+        w = synthetic.weights(N, K)
+        wbytes = N * K
+        copies = max(2, math.ceil(2 * L2_BYTES / wbytes))
+        copies = min(copies, max(len(ms), REPS))
+        wdev = w.to(dev)
+        wq0, ws0 = fq.fp8q_quant_weight_block128(wdev) if bw else fq.fp8q_quant_per_token(wdev)
+        del wdev, w
+        wqs = [wq0] + [wq0.clone() for _ in range(copies - 1)]
+        wcopies[label] = wqs
+        wbytes_total += wbytes * copies
+        xall = synthetic.activations(max(ms), K, outliers=outliers)
+        for i, M in enumerate(ms):
+            x = xall[:M].contiguous().to(dev)
+            m_pad = (M + 3) // 4 * 4
+            if bw:
+                xq = torch.empty((m_pad, K), dtype=fq.E4M3, device=dev)
+                xs = torch.empty((K // 128, m_pad), dtype=torch.float32, device=dev)
+            else:
+                xq = torch.empty((M, K), dtype=fq.E4M3, device=dev)
+                xs = torch.empty((M,), dtype=torch.float32, device=dev)
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            plan = fq.fp8q_gemm_plan(M, N, K, bw)
+            need = fq.fp8q_workspace_bytes(M, N, K, bw)
+            work = torch.empty(need, dtype=torch.uint8, device=dev) if need else None
+            problems.append(dict(label=label, N=N, K=K, bw=bw, M=M, m_pad=m_pad, x=x, xq=xq, xs=xs, out=out,
+                                 wq=wqs[i % copies], ws=ws0, plan=plan, work=work, work_bytes=need,
+                                 copies=wqs))
+    torch.cuda.synchronize()
+    return problems, wbytes_total
+
+
+def plan_str(pl):
+    return f"{'swap' if pl['swap_ab'] else 'noswap'}{pl['mma_n']}x{pl['split_k']}"
+
+
+def measure_sweep(gpu, problems, peaks, with_quant=True):
+    """Per problem: the GEMM (REPS back-to-back launches over rotating weight
+    copies, > L2 in total) and its quantizer, each the median of 5 timed
+    measurements; K-split schedules are also timed without the workspace
+    (partials exchanged in distributed shared memory)."""
+    out = []
+    for i, p in enumerate(problems):
+        copies = p["copies"]
+
+        def body_g(st, p=p, copies=copies, i=i, ws=True):
+            for r in range(REPS):
+                gpu.gemm(p, copies[(i + r) % len(copies)], gpu.P(st.cuda_stream), workspace=ws)
+
+        def body_q(st, p=p):
+            for _ in range(REPS):
+                gpu.quant(p, gpu.P(st.cuda_stream))
+
+        gu = gpu.time_graph(body_g, REPS)
+        fl = 2 * p["M"] * p["N"] * p["K"]
+        by = gemm_bytes(p["M"], p["N"], p["K"], p["bw"])
+        t_fp8, t_hbm = fl / (peaks["fp8_tflops"] * 1e12), by / (peaks["hbm_gbs"] * 1e9)
+        e = {"shape": p["label"], "M": p["M"], "N": p["N"], "K": p["K"], "gemm_us": round(gu, 3),
+             "tflops": round(fl / (gu * 1e-6) / 1e12, 2), "gbs": round(by / (gu * 1e-6) / 1e9, 1),
+             "roofline_frac": round(max(t_fp8, t_hbm) / (gu * 1e-6), 3),
+             "bound": "tensor" if t_fp8 > t_hbm else "hbm", "plan": plan_str(p["plan"])}
+        if p["work"] is not None:
+            gd = gpu.time_graph(lambda st, b=body_g: b(st, ws=False), REPS)
+            e["gemm_us_dsmem_exchange"] = round(gd, 3)
+        if with_quant:
+            qu = gpu.time_graph(body_q, REPS)
+            qb = quant_bytes(p["M"], p["K"], p["bw"])
+            e["quant_us"] = round(qu, 3)
+            e["quant_gbs"] = round(qb / (qu * 1e-6) / 1e9, 1)
+        out.append(e)
+    return out
+
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="fp8q", choices=["fp8q", "reference"])
     ap.add_argument("--workload", default="oproj_sweep", choices=sorted(WORKLOADS))
     ap.add_argument("--ref-rows", type=int, default=2, help="oracle rows per M in the reference arm")
@@ -247,12 +510,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--kernel-replays", type=int, default=20)
+    ap.add_argument("--min-timed-s", type=float, default=1.0,
+                    help="replay the pass within each step so the timed region lasts at least this long")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other configurations' blocks")
+    ap.add_argument("--profile-case", default=None, help="run one small profiling case and exit")
     args = ap.parse_args()
+    if args.profile_case:
+        return run_profile_case(args.profile_case)
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
         return run_reference(args)
 
-    import numpy as np
     import torch
     import torch.distributed as dist
 
@@ -273,176 +541,56 @@ def main():
         dist.barrier()
     L = fq.load_library()
     peaks = load_peaks()
+    gpu = Gpu(dev, L, fq, torch, args.kernel_replays)
+    P = gpu.P
 
     shapes, ms, outliers = WORKLOADS[args.workload]
-    # ---- inputs resident in HBM -------------------------------------------
-    problems = []
-    wcopies = {}
-    wbytes_total = 0
-    for (label, N, K, bw) in shapes:
-        w = synthetic.weights(N, K)
-        wbytes = N * K
-        copies = max(2, math.ceil(2 * L2_BYTES / wbytes))  # rotate > 2x L2 of weight bytes
-        copies = min(copies, len(ms))  # one copy per M at most
-        wdev = w.to(dev)
-        if bw:
-            wq0, ws0 = fq.fp8q_quant_weight_block128(wdev)
-        else:
-            wq0, ws0 = fq.fp8q_quant_per_token(wdev)
-        wqs = [wq0] + [wq0.clone() for _ in range(copies - 1)]
-        wcopies[label] = wqs
-        wbytes_total += wbytes * copies
-        for i, M in enumerate(ms):
-            x = synthetic.activations(M, K, outliers=outliers).to(dev)
-            m_pad = (M + 3) // 4 * 4
-            if bw:
-                xq = torch.empty((m_pad, K), dtype=fq.E4M3, device=dev)
-                xs = torch.empty((K // 128, m_pad), dtype=torch.float32, device=dev)
-            else:
-                xq = torch.empty((M, K), dtype=fq.E4M3, device=dev)
-                xs = torch.empty((M,), dtype=torch.float32, device=dev)
-            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-            plan = fq.fp8q_gemm_plan(M, N, K, bw)
-            problems.append(dict(label=label, N=N, K=K, bw=bw, M=M, m_pad=m_pad, x=x, xq=xq, xs=xs, out=out,
-                                 wq=wqs[i % copies], ws=ws0, plan=plan))
-    del w
-    torch.cuda.synchronize()
-
-    import ctypes
-    P = ctypes.c_void_p
-
-    def launch(p, sp):
-        """The public linear entry point: quantize, then GEMM (two kernels)."""
-        if p["bw"]:
-            st = L.fp8q_linear_blockwise(P(p["x"].data_ptr()), P(p["wq"].data_ptr()), P(p["ws"].data_ptr()), None,
-                                         P(p["out"].data_ptr()), p["M"], p["N"], p["K"], P(p["xq"].data_ptr()),
-                                         P(p["xs"].data_ptr()), p["m_pad"], 0, sp)
-        else:
-            st = L.fp8q_linear_channelwise(P(p["x"].data_ptr()), P(p["wq"].data_ptr()), p["K"],
-                                           P(p["ws"].data_ptr()), None, P(p["out"].data_ptr()), p["M"], p["N"],
-                                           p["K"], P(p["xq"].data_ptr()), P(p["xs"].data_ptr()), 0, sp)
-        if st != 0:
-            raise RuntimeError(f"linear failed: {fq.status_str(st)}")
-
-    def launch_gemm(p, wq, sp):
-        if p["bw"]:
-            st = L.fp8q_scaled_mm_blockwise(P(p["xq"].data_ptr()), P(wq.data_ptr()), P(p["xs"].data_ptr()),
-                                            P(p["ws"].data_ptr()), None, P(p["out"].data_ptr()), p["M"], p["m_pad"],
-                                            p["N"], p["K"], 0, sp)
-        else:
-            st = L.fp8q_scaled_mm_channelwise(P(p["xq"].data_ptr()), P(wq.data_ptr()), p["K"],
-                                              P(p["xs"].data_ptr()), P(p["ws"].data_ptr()), None,
-                                              P(p["out"].data_ptr()), p["M"], p["N"], p["K"], 0, sp)
-        if st != 0:
-            raise RuntimeError(f"gemm failed: {fq.status_str(st)}")
-
-    def launch_quant(p, sp):
-        if p["bw"]:
-            st = L.fp8q_quant_per_token_group_row_padded(P(p["x"].data_ptr()), p["M"], p["K"], p["K"], 128, 1e-10, 4,
-                                                         P(p["xq"].data_ptr()), P(p["xs"].data_ptr()), p["m_pad"], sp)
-        else:
-            st = L.fp8q_quant_per_token(P(p["x"].data_ptr()), p["M"], p["K"], p["K"], P(p["xq"].data_ptr()),
-                                        P(p["xs"].data_ptr()), 1e-10, sp)
-        if st != 0:
-            raise RuntimeError(f"quant failed: {fq.status_str(st)}")
-
-    def capture(body):
-        """A CUDA graph of body(stream): the library's launches are captured
-        like any other stream work (one eager run first sets kernel
-        attributes outside the capture)."""
-        side = torch.cuda.Stream(dev)
-        side.wait_stream(torch.cuda.current_stream(dev))
-        with torch.cuda.stream(side):
-            body(side)
-        side.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=side):
-            body(side)
-        torch.cuda.synchronize()
-        return g
+    problems, wbytes_total = build_problems(gpu, args.workload)
 
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
 
-    def mk():
-        return torch.cuda.Event(enable_timing=True)
+    stream = gpu.stream
 
-    stream = torch.cuda.current_stream(dev)
-
-    # ---- one step = every problem's quant + GEMM, captured as one graph ----
-    step_graph = capture(lambda st: [launch(p, P(st.cuda_stream)) for p in problems])
+    # ---- one pass = every problem's linear layer (quant + GEMM), one graph;
+    # a timed step replays it `passes` times (timed region >= min_timed_s).
+    step_graph = gpu.capture(lambda st: [gpu.linear(p, P(st.cuda_stream)) for p in problems])
     for _ in range(args.warmup):
         step_graph.replay()
     barrier()
-    start, end = mk(), mk()
+    e0, e1 = gpu.event(), gpu.event()
+    e0.record(stream)
+    for _ in range(3):
+        step_graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    pass_ms = e0.elapsed_time(e1) / 3
+    passes = max(1, math.ceil(args.min_timed_s * 1e3 / (args.steps * pass_ms)))
+    passes = int(reduce_max_over_ranks(float(passes), world, dev))
+    start, end = gpu.event(), gpu.event()
     with ClockSampler(local) as clk:
         barrier()
         start.record(stream)
         for _ in range(args.steps):
-            step_graph.replay()
+            for _ in range(passes):
+                step_graph.replay()
         end.record(stream)
         barrier()
     elapsed_ms = reduce_max_over_ranks(start.elapsed_time(end), world, dev)
     ms_per_step = elapsed_ms / args.steps
-    flops_step = sum(2 * p["M"] * p["N"] * p["K"] for p in problems)
+    flops_pass = sum(2 * p["M"] * p["N"] * p["K"] for p in problems)
+    flops_step = flops_pass * passes
     value = aggregate_value(flops_step, world, ms_per_step)
 
-    # ---- per-kernel durations: each problem's GEMM (and quantizer) launched
-    # REPS times back to back in a graph, the GEMM over rotating weight
-    # copies (> L2 in total), timed with CUDA events on the launching stream.
-    reps = 8
-
-    def time_graph(body, n_launch, repeats=5):
-        """Microseconds per launch: the median over `repeats` measurements,
-        each kernel_replays graph replays (>= 100 back-to-back launches)."""
-        g = capture(body)
-        g.replay()
-        torch.cuda.synchronize()
-        samples = []
-        for _ in range(repeats):
-            e0, e1 = mk(), mk()
-            e0.record(stream)
-            for _ in range(args.kernel_replays):
-                g.replay()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            samples.append(e0.elapsed_time(e1) * 1e3 / (args.kernel_replays * n_launch))
-        return statistics.median(samples)
-
-    g_us, q_us = [], []
-    for i, p in enumerate(problems):
-        copies = wcopies[p["label"]]
-
-        def body_g(st, p=p, copies=copies, i=i):
-            for r in range(reps):
-                launch_gemm(p, copies[(i + r) % len(copies)], P(st.cuda_stream))
-
-        def body_q(st, p=p):
-            for _ in range(reps):
-                launch_quant(p, P(st.cuda_stream))
-
-        g_us.append(time_graph(body_g, reps))
-        q_us.append(time_graph(body_q, reps))
-
-    sweep = []
-    for p, qu, gu in zip(problems, q_us, g_us):
-        fl = 2 * p["M"] * p["N"] * p["K"]
-        by = gemm_bytes(p["M"], p["N"], p["K"], p["bw"])
-        t_roof = max(fl / (peaks["fp8_tflops"] * 1e12), by / (peaks["hbm_gbs"] * 1e9))
-        qb = quant_bytes(p["M"], p["K"], p["bw"])
-        pl = p["plan"]
-        sweep.append({"shape": p["label"], "M": p["M"], "N": p["N"], "K": p["K"], "gemm_us": round(gu, 3),
-                      "tflops": round(fl / (gu * 1e-6) / 1e12, 2), "gbs": round(by / (gu * 1e-6) / 1e9, 1),
-                      "roofline_frac": round(t_roof / (gu * 1e-6), 3),
-                      "bound": "tensor" if fl / (peaks["fp8_tflops"] * 1e12) > by / (peaks["hbm_gbs"] * 1e9)
-                      else "hbm",
-                      "quant_us": round(qu, 3), "quant_gbs": round(qb / (qu * 1e-6) / 1e9, 1),
-                      "plan": f"{'swap' if pl['swap_ab'] else 'noswap'}{pl['mma_n']}x{pl['split_k']}"})
+    # ---- per-kernel durations of the headline workload
+    sweep = measure_sweep(gpu, problems, peaks)
+    g_us = [e["gemm_us"] for e in sweep]
+    q_us = [e["quant_us"] for e in sweep]
 
     # dominant kernel = the GEMM instantiation (scheme, swap, mma_n) with the
-    # largest total time per step
+    # largest total time per pass
     groups = {}
     for p, gu in zip(problems, g_us):
         pl = p["plan"]
@@ -452,8 +600,7 @@ def main():
         g["flops"] += 2 * p["M"] * p["N"] * p["K"]
         g["bytes"] += gemm_bytes(p["M"], p["N"], p["K"], p["bw"])
         g["n"] += 1
-    quant_total = sum(q_us)
-    gemm_total = sum(g_us)
+    quant_total, gemm_total = sum(q_us), sum(g_us)
     dom_key, dom = max(groups.items(), key=lambda kv: kv[1]["us"])
     tensor_bound = dom["flops"] / (peaks["fp8_tflops"] * 1e12) > dom["bytes"] / (peaks["hbm_gbs"] * 1e9)
     if tensor_bound:
@@ -464,17 +611,131 @@ def main():
         achieved = dom["bytes"] / (dom["us"] * 1e-6) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": round(peaks["hbm_gbs"], 1),
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 3)}
-    roof["traffic"] = DOMINANT_TRAFFIC_BYTES.get(dom_key) if DOMINANT_TRAFFIC_BYTES else None
+    roof["traffic"] = DOMINANT_TRAFFIC_BYTES.get(dom_key)
     roof["kernel"] = (f"fp8_gemm_kernel<{'swap' if dom_key[1] else 'noswap'}, mma_n={dom_key[2]}, {dom_key[0]}> "
-                      f"({dom['n']} launches/step; achieved = their FLOPs / their summed durations)")
-    roof["share_of_step"] = round(dom["us"] / (quant_total + gemm_total), 3)
+                      f"({dom['n']} launches/pass; achieved = their FLOPs / their summed durations)")
+    roof["share_of_pass"] = round(dom["us"] / (quant_total + gemm_total), 3)
     roof["peak_source"] = peaks["source"]
 
-    # ---- quantizer variants (static per-tensor; group-128 with power-of-two
-    # scales; silu_and_mul-fused group-128) at a decode and a prefill size
-    # (the prefill inputs and outputs exceed L2): 8 back-to-back launches per
-    # graph, algorithmic bytes (bf16 in, e4m3 + fp32 scales out) over the
-    # CUDA-event duration, against the HBM peak.
+    # ---- the other configurations: the same per-M measurement, compact
+    configs = {}
+    if not args.no_configs and rank == 0:
+        for wl in ("tiny", "qwen3_8b", "blockwise_decode", "blockwise_prefill"):
+            if wl == args.workload:
+                continue
+            probs, _ = build_problems(gpu, wl)
+            entries = measure_sweep(gpu, probs, peaks)
+            configs[wl] = {"workload": WORKLOAD_DESC[wl], "per_m": [
+                [e["shape"], e["M"], e["gemm_us"], e["tflops"], e["gbs"], e["roofline_frac"], e["plan"],
+                 e.get("gemm_us_dsmem_exchange"), e["quant_us"]] for e in entries],
+                "columns": ["shape", "M", "gemm_us", "tflops", "gbs", "roofline_frac", "plan",
+                            "gemm_us_dsmem_exchange", "quant_us"]}
+            del probs
+            torch.cuda.empty_cache()
+
+    variants = measure_quant_variants(gpu, peaks, synthetic) if rank == 0 and not args.no_configs else []
+    fused = measure_fused(gpu, peaks, synthetic) if rank == 0 and not args.no_configs else []
+    w16 = measure_w8a16(gpu, peaks, synthetic) if rank == 0 and not args.no_configs else []
+
+    # ---- end to end through the C ABI with host buffers --------------------
+    h2d = sum(p["x"].numel() * 2 for p in problems)
+    d2h = sum(p["out"].numel() * 2 for p in problems)
+    hx = [p["x"].cpu().pin_memory() for p in problems]
+    ho = [torch.empty(p["out"].shape, dtype=torch.bfloat16).pin_memory() for p in problems]
+
+    # Three streams: every M's activations go up on s_in, its linear layer
+    # runs on the capturing stream once its upload is done, its output comes
+    # back on s_out once its layer is done -- uploads, layers and downloads of
+    # different M overlap, as a serving pipeline would run them.
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def e2e_body(st):
+        cur = torch.cuda.current_stream(dev)
+        s_in.wait_stream(cur)
+        s_out.wait_stream(cur)
+        ev_in, ev_c = [], []
+        with torch.cuda.stream(s_in):
+            for p, hxi in zip(problems, hx):
+                p["x"].copy_(hxi, non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(s_in)
+                ev_in.append(e)
+        for p, e in zip(problems, ev_in):
+            cur.wait_event(e)
+            gpu.linear(p, P(cur.cuda_stream))
+            e2 = torch.cuda.Event()
+            e2.record(cur)
+            ev_c.append(e2)
+        with torch.cuda.stream(s_out):
+            for p, hoi, e2 in zip(problems, ho, ev_c):
+                s_out.wait_event(e2)
+                hoi.copy_(p["out"], non_blocking=True)
+        cur.wait_stream(s_in)
+        cur.wait_stream(s_out)
+
+    e2e_graph = gpu.capture(e2e_body)
+    for _ in range(3):
+        e2e_graph.replay()
+    barrier()
+    e0, e1 = gpu.event(), gpu.event()
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_graph.replay()
+    e1.record(stream)
+    barrier()
+    e2e_ms = reduce_max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
+    e2e = {"value": round(aggregate_value(flops_pass, world, e2e_ms), 2), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+           "how": "CUDA graph per pass over three streams: pinned-host->device copy of each M's "
+                  "activations, the linear entry point (quant + GEMM) once that copy is done, "
+                  "device->pinned-host copy of its output once the layer is done; copies and layers "
+                  "of different M overlap; one pass per step"}
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline:
+            rows = args.cpu_rows
+            threads = os.cpu_count() or 1
+            cp = build_oracle_problems(args.workload, rows)
+            t0 = time.perf_counter()
+            fl = oracle_sample_step(cp, rows, threads)
+            dt = time.perf_counter() - t0
+            cpu = {"value": round(fl / dt / 1e12, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+                   "sample": f"quant + exact GEMM on the first min(M, {rows}) rows of every M ({dt:.1f} s)"}
+        l2note = (f"inputs larger than L2 per pass: {len(set(id(p['wq']) for p in problems))} rotating "
+                  f"weight copies ({wbytes_total / 2**20:.0f} MiB) + "
+                  f"{sum(p['x'].numel() * 2 for p in problems) / 2**20:.0f} MiB activations")
+        line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate)",
+                "data": "synthetic",
+                "config": {"workload": WORKLOAD_DESC[args.workload], "shapes": [s[:3] for s in shapes],
+                           "M": ms, "l2": l2note, "passes_per_step": passes,
+                           "parallelism": f"replicas x{world}" if world > 1 else "single"},
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": 2 * len(problems) * args.steps * passes,
+                "timing": f"K steps of {passes} replays each of a CUDA graph holding one pass (timed region "
+                          f"{elapsed_ms / 1e3:.2f} s); per-kernel durations: median of 5 measurements, each "
+                          f"{args.kernel_replays} replays of a graph of {REPS} back-to-back launches of the "
+                          "problem's kernel (GEMMs over rotating weight copies, with their split-K workspace)",
+                "clocks": clk.summary(),
+                "kernel_time_us": {"quant": round(quant_total, 2), "gemm": round(gemm_total, 2)},
+                "sweep": sweep, "configs": configs, "quant_variants": variants, "fused_quant_linear": fused,
+                "w8a16": w16}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_quant_variants(gpu, peaks, synthetic):
+    """Static per-tensor; group-128 with power-of-two scales; silu_and_mul-
+    fused group-128, at a decode and a prefill size (the prefill inputs and
+    outputs exceed L2): algorithmic bytes (bf16 in, e4m3 + fp32 scales out)
+    over the CUDA-event duration, against the HBM peak."""
+    torch, fq, dev, P, L = gpu.torch, gpu.fq, gpu.dev, gpu.P, gpu.L
     variants = []
     vK, vKm = 4096, 12288          # hidden size; MLP intermediate (silu input 2 x 12288)
     s_dev = torch.tensor([0.02], dtype=torch.float32, device=dev)
@@ -505,180 +766,105 @@ def main():
                                                                    m_pad, sp)),
         ]
         for name, kk, nbytes, fn in cases:
-            def body_v(st, fn=fn):
-                for _ in range(reps):
+            def body_v(st, fn=fn, name=name):
+                for _ in range(REPS):
                     if fn(P(st.cuda_stream)) != 0:
                         raise RuntimeError(f"{name} failed")
-            us = time_graph(body_v, reps)
+            us = gpu.time_graph(body_v, REPS)
             gbs = nbytes / (us * 1e-6) / 1e9
             variants.append({"kernel": name, "M": vM, "K": kk, "us": round(us, 3), "gbs": round(gbs, 1),
                              "hbm_frac": round(gbs / peaks["hbm_gbs"], 3)})
         del xv, xm
+    return variants
 
-    # ---- quantization fused into the blockwise GEMM (one kernel) against the
-    # two-kernel blockwise linear, at decode sizes of the blockwise decode
-    # layer (N = 4096, K = 7168): 8 back-to-back launches per graph over
-    # rotating weight copies (> L2), CUDA events.
+
+def measure_fused(gpu, peaks, synthetic):
+    """Quantization fused into the blockwise GEMM (one kernel) against the
+    two-kernel blockwise linear, at decode sizes of the blockwise decode
+    layer (N = 4096, K = 7168): back-to-back launches over rotating weight
+    copies (> L2), CUDA events."""
+    torch, fq, dev, P, L = gpu.torch, gpu.fq, gpu.dev, gpu.P, gpu.L
     fused = []
     fN, fK = 4096, 7168
     fw = synthetic.weights(fN, fK).to(dev)
     fwq0, fws = fq.fp8q_quant_weight_block128(fw)
     del fw
-    fcopies = [fwq0] + [fwq0.clone() for _ in range(reps - 1)]
+    fcopies = [fwq0] + [fwq0.clone() for _ in range(REPS - 1)]
     for fM in (1, 16):
         fx = synthetic.activations(fM, fK, outliers=True).to(dev)
         fm_pad = (fM + 3) // 4 * 4
         fxq = torch.empty((fm_pad, fK), dtype=fq.E4M3, device=dev)
         fxs = torch.empty((fK // 128, fm_pad), dtype=torch.float32, device=dev)
         fout = torch.empty((fM, fN), dtype=torch.bfloat16, device=dev)
+        need = fq.fp8q_workspace_bytes(fM, fN, fK, True)
+        work = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
 
         def body_fused(st, fx=fx, fM=fM, fout=fout):
-            for r in range(reps):
+            for r in range(REPS):
                 if L.fp8q_linear_blockwise_fused(P(fx.data_ptr()), fK, P(fcopies[r].data_ptr()), P(fws.data_ptr()),
                                                  None, P(fout.data_ptr()), fM, fN, fK, 0, P(st.cuda_stream)) != 0:
                     raise RuntimeError("fused linear failed")
 
-        def body_two(st, fx=fx, fM=fM, fout=fout, fxq=fxq, fxs=fxs, fm_pad=fm_pad):
-            for r in range(reps):
+        def body_two(st, fx=fx, fM=fM, fout=fout, fxq=fxq, fxs=fxs, fm_pad=fm_pad, work=work, need=need):
+            for r in range(REPS):
                 if L.fp8q_linear_blockwise(P(fx.data_ptr()), P(fcopies[r].data_ptr()), P(fws.data_ptr()), None,
                                            P(fout.data_ptr()), fM, fN, fK, P(fxq.data_ptr()), P(fxs.data_ptr()),
-                                           fm_pad, 0, P(st.cuda_stream)) != 0:
+                                           fm_pad, 0, P(work.data_ptr()), need, P(st.cuda_stream)) != 0:
                     raise RuntimeError("linear failed")
 
-        fu = time_graph(body_fused, reps)
-        tu = time_graph(body_two, reps)
+        fu = gpu.time_graph(body_fused, REPS)
+        tu = gpu.time_graph(body_two, REPS)
         fb = gemm_bytes(fM, fN, fK, True)
         fused.append({"M": fM, "N": fN, "K": fK, "fused_us": round(fu, 3), "two_kernel_us": round(tu, 3),
                       "fused_hbm_frac": round(fb / (fu * 1e-6) / 1e9 / peaks["hbm_gbs"], 3),
                       "two_kernel_hbm_frac": round(fb / (tu * 1e-6) / 1e9 / peaks["hbm_gbs"], 3)})
     del fcopies
+    return fused
 
-    # ---- weight-only FP8 (W8A16: bf16 activations, no quantizer) against the
-    # W8A8 linear (quantizer + GEMM) at decode sizes: 8 back-to-back launches
-    # per graph over rotating weight copies (> L2), CUDA events; algorithmic
-    # bytes of W8A16 = N*K (E4M3 weights) + 2*M*K + 2*M*N + 4*N.
+
+def measure_w8a16(gpu, peaks, synthetic):
+    """Weight-only FP8 (W8A16: bf16 activations, no quantizer) against the
+    W8A8 linear (quantizer + GEMM) at decode sizes: back-to-back launches
+    over rotating weight copies (> L2), CUDA events; algorithmic bytes of
+    W8A16 = N*K (E4M3 weights) + 2*M*K + 2*M*N + 4*N."""
+    torch, fq, dev, P, L = gpu.torch, gpu.fq, gpu.dev, gpu.P, gpu.L
     w16 = []
     for (wl, wN, wK) in (("o_proj", 4096, 4096), ("gate_up", 24576, 4096)):
         ww = synthetic.weights(wN, wK).to(dev)
         wwq0, wws = fq.fp8q_quant_per_token(ww)
         del ww
-        wcp = [wwq0] + [wwq0.clone() for _ in range(reps - 1)]
+        wcp = [wwq0] + [wwq0.clone() for _ in range(REPS - 1)]
         for wM in (1, 16):
             wx = synthetic.activations(wM, wK, outliers=True).to(dev)
             wxq = torch.empty((wM, wK), dtype=fq.E4M3, device=dev)
             wxs = torch.empty((wM,), dtype=torch.float32, device=dev)
             wout = torch.empty((wM, wN), dtype=torch.bfloat16, device=dev)
+            need = fq.fp8q_workspace_bytes(wM, wN, wK)
+            work = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
 
             def body_w16(st, wx=wx, wM=wM, wout=wout, wcp=wcp, wN=wN, wK=wK):
-                for r in range(reps):
+                for r in range(REPS):
                     if L.fp8q_scaled_mm_w8a16(P(wx.data_ptr()), wK, P(wcp[r].data_ptr()), wK, P(wws.data_ptr()),
                                               None, P(wout.data_ptr()), wM, wN, wK, 0, P(st.cuda_stream)) != 0:
                         raise RuntimeError("w8a16 failed")
 
-            def body_w8(st, wx=wx, wM=wM, wout=wout, wcp=wcp, wN=wN, wK=wK, wxq=wxq, wxs=wxs):
-                for r in range(reps):
+            def body_w8(st, wx=wx, wM=wM, wout=wout, wcp=wcp, wN=wN, wK=wK, wxq=wxq, wxs=wxs, work=work,
+                        need=need):
+                for r in range(REPS):
                     if L.fp8q_linear_channelwise(P(wx.data_ptr()), P(wcp[r].data_ptr()), wK, P(wws.data_ptr()),
                                                  None, P(wout.data_ptr()), wM, wN, wK, P(wxq.data_ptr()),
-                                                 P(wxs.data_ptr()), 0, P(st.cuda_stream)) != 0:
+                                                 P(wxs.data_ptr()), 0, P(work.data_ptr()), need,
+                                                 P(st.cuda_stream)) != 0:
                         raise RuntimeError("linear failed")
 
-            u16 = time_graph(body_w16, reps)
-            u8 = time_graph(body_w8, reps)
+            u16 = gpu.time_graph(body_w16, REPS)
+            u8 = gpu.time_graph(body_w8, REPS)
             wb = wN * wK + 2 * wM * wK + 2 * wM * wN + 4 * wN
             w16.append({"shape": wl, "M": wM, "N": wN, "K": wK, "w8a16_us": round(u16, 3),
                         "w8a8_linear_us": round(u8, 3),
                         "w8a16_hbm_frac": round(wb / (u16 * 1e-6) / 1e9 / peaks["hbm_gbs"], 3)})
         del wcp
-
-    # ---- end to end through the C ABI with host buffers --------------------
-    h2d = sum(p["x"].numel() * 2 for p in problems)
-    d2h = sum(p["out"].numel() * 2 for p in problems)
-    hx = [p["x"].cpu().pin_memory() for p in problems]
-    ho = [torch.empty(p["out"].shape, dtype=torch.bfloat16).pin_memory() for p in problems]
-
-    # Three streams: every M's activations go up on s_in, its linear layer
-    # runs on the capturing stream once its upload is done, its output comes
-    # back on s_out once its layer is done -- uploads, layers and downloads of
-    # different M overlap, as a serving pipeline would run them.  (Spreading
-    # the copies over four streams per direction measured slower.)
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-
-    def e2e_body(st):
-        cur = torch.cuda.current_stream(dev)
-        s_in.wait_stream(cur)
-        s_out.wait_stream(cur)
-        ev_in, ev_c = [], []
-        with torch.cuda.stream(s_in):
-            for p, hxi in zip(problems, hx):
-                p["x"].copy_(hxi, non_blocking=True)
-                e = torch.cuda.Event()
-                e.record(s_in)
-                ev_in.append(e)
-        for p, e in zip(problems, ev_in):
-            cur.wait_event(e)
-            launch(p, P(cur.cuda_stream))
-            e2 = torch.cuda.Event()
-            e2.record(cur)
-            ev_c.append(e2)
-        with torch.cuda.stream(s_out):
-            for p, hoi, e2 in zip(problems, ho, ev_c):
-                s_out.wait_event(e2)
-                hoi.copy_(p["out"], non_blocking=True)
-        cur.wait_stream(s_in)
-        cur.wait_stream(s_out)
-
-    e2e_graph = capture(e2e_body)
-    for _ in range(3):
-        e2e_graph.replay()
-    barrier()
-    e0, e1 = mk(), mk()
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_graph.replay()
-    e1.record(stream)
-    barrier()
-    e2e_ms = reduce_max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
-    e2e = {"value": round(aggregate_value(flops_step, world, e2e_ms), 2), "unit": UNIT,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-           "how": "CUDA graph per step over three streams: pinned-host->device copy of each M's "
-                  "activations, the linear entry point (quant + GEMM) once that copy is done, "
-                  "device->pinned-host copy of its output once the layer is done; copies and layers "
-                  "of different M overlap"}
-
-    line = None
-    if rank == 0:
-        cpu = None
-        if not args.no_cpu_baseline:
-            rows = args.cpu_rows
-            threads = os.cpu_count() or 1
-            cp = build_oracle_problems(args.workload, rows)
-            t0 = time.perf_counter()
-            fl = oracle_sample_step(cp, rows, threads)
-            dt = time.perf_counter() - t0
-            cpu = {"value": round(fl / dt / 1e12, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
-                   "sample": f"quant + exact GEMM on the first min(M, {rows}) rows of every M ({dt:.1f} s)"}
-        l2note = (f"inputs larger than L2 per step: {len(set(id(p['wq']) for p in problems))} rotating "
-                  f"weight copies ({wbytes_total / 2**20:.0f} MiB) + {sum(p['x'].numel() * 2 for p in problems) / 2**20:.0f}"
-                  f" MiB activations per step")
-        line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate)",
-                "data": "synthetic",
-                "config": {"workload": WORKLOAD_DESC[args.workload], "shapes": [s[:3] for s in shapes],
-                           "M": ms, "l2": l2note, "parallelism": f"replicas x{world}" if world > 1 else "single"},
-                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": 2 * len(problems) * args.steps,
-                "timing": "K replays of a CUDA graph holding one step; per-kernel durations: median of 5 "
-                          f"measurements, each {args.kernel_replays} replays of a graph of 8 back-to-back "
-                          "launches of the problem's kernel (GEMMs over rotating weight copies)",
-                "clocks": clk.summary(),
-                "kernel_time_us": {"quant": round(quant_total, 2), "gemm": round(gemm_total, 2)},
-                "sweep": sweep, "quant_variants": variants, "fused_quant_linear": fused, "w8a16": w16}
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.barrier()
-        dist.destroy_process_group()
-    return 0
+    return w16
 
 
 if __name__ == "__main__":

@@ -44,6 +44,7 @@ EXPORTED = (
     "fp8q_linear_blockwise_fused",
     "fp8q_scaled_mm_w8a16",
     "fp8q_gemm_plan",
+    "fp8q_workspace_bytes",
     "fp8q_set_plan_override",
     "fp8q_device_status",
     "fp8q_selftest_wait_timeout",
@@ -80,17 +81,17 @@ def load_library(path: str | None = None):
         raise RuntimeError(f"libfp8q.so not found at {path}: run __graft_entry__.build() "
                            "(or python fp8_w8a8_quantized_token_gb300/build.py) first")
     L = ctypes.CDLL(path)
-    P, I64, I32, F32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+    P, I64, I32, F32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
     sig = {
         "fp8q_quant_per_token": [P, I64, I64, I64, P, P, F32, P],
         "fp8q_quant_per_token_group_row_padded": [P, I64, I64, I64, I32, F32, I32, P, P, I64, P],
         "fp8q_quant_per_token_group_row_padded_ex": [P, I64, I64, I64, I32, F32, I32, I32, P, P, I64, P],
         "fp8q_quant_static_per_tensor": [P, I64, I64, I64, P, P, P, P],
         "fp8q_quant_weight_block128": [P, I64, I64, P, P, F32, P],
-        "fp8q_scaled_mm_channelwise": [P, P, I64, P, P, P, P, I64, I64, I64, ctypes.c_int, P],
-        "fp8q_scaled_mm_blockwise": [P, P, P, P, P, P, I64, I64, I64, I64, ctypes.c_int, P],
-        "fp8q_linear_channelwise": [P, P, I64, P, P, P, I64, I64, I64, P, P, ctypes.c_int, P],
-        "fp8q_linear_blockwise": [P, P, P, P, P, I64, I64, I64, P, P, I64, ctypes.c_int, P],
+        "fp8q_scaled_mm_channelwise": [P, P, I64, P, P, P, P, I64, I64, I64, ctypes.c_int, P, SZ, P],
+        "fp8q_scaled_mm_blockwise": [P, P, P, P, P, P, I64, I64, I64, I64, ctypes.c_int, P, SZ, P],
+        "fp8q_linear_channelwise": [P, P, I64, P, P, P, I64, I64, I64, P, P, ctypes.c_int, P, SZ, P],
+        "fp8q_linear_blockwise": [P, P, P, P, P, I64, I64, I64, P, P, I64, ctypes.c_int, P, SZ, P],
         "fp8q_linear_channelwise_noalloc": [P, P, I64, P, P, P, I64, I64, I64, ctypes.c_int, P],
         "fp8q_linear_blockwise_fused": [P, I64, P, P, P, P, I64, I64, I64, ctypes.c_int, P],
         "fp8q_scaled_mm_w8a16": [P, I64, P, I64, P, P, P, I64, I64, I64, ctypes.c_int, P],
@@ -107,6 +108,8 @@ def load_library(path: str | None = None):
     L.fp8q_status_str.restype = ctypes.c_char_p
     L.fp8q_version.argtypes = []
     L.fp8q_version.restype = ctypes.c_int32
+    L.fp8q_workspace_bytes.argtypes = [I64, I64, I64, I32]
+    L.fp8q_workspace_bytes.restype = SZ
     _lib = L
     return L
 
@@ -126,6 +129,34 @@ def _ptr(t: torch.Tensor | None):
 
 def _stream(device: torch.device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _on(device: torch.device):
+    """Make the tensors' device current for the C call: the library reads
+    the current device for its per-device state (status word, SM count,
+    kernel attributes, the no-alloc array's address)."""
+    return torch.cuda.device(device)
+
+
+def _workspace(workspace, M: int, N: int, K: int, blockwise: bool, device: torch.device):
+    """(pointer, bytes) of the split-K workspace: "auto" allocates what the
+    planned schedule uses (nothing if it does not split K), None passes none
+    (partials then go through distributed shared memory), a uint8 CUDA
+    tensor is used as given."""
+    if workspace is None:
+        return None, 0
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError('workspace must be "auto", None or a uint8 CUDA tensor')
+        with _on(device):
+            nbytes = int(load_library().fp8q_workspace_bytes(M, N, K, int(bool(blockwise))))
+        if nbytes == 0:
+            return None, 0
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    _need(workspace, torch.uint8, "workspace", device)
+    if not workspace.is_contiguous():
+        raise ValueError("workspace must be contiguous")
+    return _ptr(workspace), workspace.numel()
 
 
 def _need(t: torch.Tensor, dtype, name: str, device=None):
@@ -169,8 +200,9 @@ def fp8q_quant_per_token(x: torch.Tensor, eps: float = 1e-10, xq: torch.Tensor |
     _need(x_scale, torch.float32, "x_scale", x.device)
     if tuple(xq.shape) != (M, K) or not xq.is_contiguous() or x_scale.numel() < M:
         raise ValueError("xq must be a contiguous [M, K] buffer and x_scale hold M floats")
-    _check("fp8q_quant_per_token",
-           L.fp8q_quant_per_token(_ptr(x), M, K, x.stride(0), _ptr(xq), _ptr(x_scale), eps, _stream(x.device)))
+    with _on(x.device):
+        _check("fp8q_quant_per_token",
+               L.fp8q_quant_per_token(_ptr(x), M, K, x.stride(0), _ptr(xq), _ptr(x_scale), eps, _stream(x.device)))
     return xq, x_scale
 
 
@@ -214,14 +246,16 @@ def fp8q_quant_per_token_group_row_padded(x: torch.Tensor, group_size: int = 128
     if tuple(x_scale_storage.shape) != (K // group_size, m_pad) or not x_scale_storage.is_contiguous():
         raise ValueError("x_scale_storage must be a contiguous [K/g, m_pad] buffer")
     if flags == 0:
-        _check("fp8q_quant_per_token_group_row_padded",
-               L.fp8q_quant_per_token_group_row_padded(_ptr(x), M, K, x.stride(0), group_size, eps, row_alignment,
-                                                       _ptr(xq), _ptr(x_scale_storage), m_pad, _stream(x.device)))
+        with _on(x.device):
+            _check("fp8q_quant_per_token_group_row_padded",
+                   L.fp8q_quant_per_token_group_row_padded(_ptr(x), M, K, x.stride(0), group_size, eps, row_alignment,
+                                                           _ptr(xq), _ptr(x_scale_storage), m_pad, _stream(x.device)))
     else:
-        _check("fp8q_quant_per_token_group_row_padded_ex",
-               L.fp8q_quant_per_token_group_row_padded_ex(_ptr(x), M, K, x.stride(0), group_size, eps,
-                                                          row_alignment, flags, _ptr(xq), _ptr(x_scale_storage),
-                                                          m_pad, _stream(x.device)))
+        with _on(x.device):
+            _check("fp8q_quant_per_token_group_row_padded_ex",
+                   L.fp8q_quant_per_token_group_row_padded_ex(_ptr(x), M, K, x.stride(0), group_size, eps,
+                                                              row_alignment, flags, _ptr(xq), _ptr(x_scale_storage),
+                                                              m_pad, _stream(x.device)))
     return xq, x_scale_storage.transpose(0, 1)
 
 
@@ -244,9 +278,10 @@ def fp8q_quant_static_per_tensor(x: torch.Tensor, scale: torch.Tensor, xq: torch
     if tuple(xq.shape) != (M, K) or not xq.is_contiguous():
         raise ValueError("xq must be a contiguous [M, K] buffer")
     rep = torch.empty(M, dtype=torch.float32, device=x.device) if repeat_scale else None
-    _check("fp8q_quant_static_per_tensor",
-           L.fp8q_quant_static_per_tensor(_ptr(x), M, K, x.stride(0), _ptr(scale), _ptr(xq),
-                                          None if rep is None else _ptr(rep), _stream(x.device)))
+    with _on(x.device):
+        _check("fp8q_quant_static_per_tensor",
+               L.fp8q_quant_static_per_tensor(_ptr(x), M, K, x.stride(0), _ptr(scale), _ptr(xq),
+                                              None if rep is None else _ptr(rep), _stream(x.device)))
     return xq, rep
 
 
@@ -259,8 +294,9 @@ def fp8q_quant_weight_block128(w: torch.Tensor, eps: float = 1e-10):
     N, K = w.shape
     wq = torch.empty((N, K), dtype=E4M3, device=w.device)
     ws = torch.empty((N // 128, K // 128), dtype=torch.float32, device=w.device)
-    _check("fp8q_quant_weight_block128",
-           L.fp8q_quant_weight_block128(_ptr(w), N, K, _ptr(wq), _ptr(ws), eps, _stream(w.device)))
+    with _on(w.device):
+        _check("fp8q_quant_weight_block128",
+               L.fp8q_quant_weight_block128(_ptr(w), N, K, _ptr(wq), _ptr(ws), eps, _stream(w.device)))
     return wq, ws
 
 
@@ -270,10 +306,10 @@ def fp8q_quant_weight_block128(w: torch.Tensor, eps: float = 1e-10):
 
 def fp8q_scaled_mm_channelwise(a: torch.Tensor, b: torch.Tensor, a_scale: torch.Tensor, b_scale: torch.Tensor,
                                bias: torch.Tensor | None = None, out_dtype=torch.bfloat16,
-                               out: torch.Tensor | None = None):
+                               out: torch.Tensor | None = None, workspace="auto"):
     """a e4m3 [M, K]; b e4m3 weight given as its [N, K] K-contiguous storage
     (logical [K, N] = b.T); a_scale fp32 [M]; b_scale fp32 [N]; bias bf16 [N].
-    Returns out [M, N] of out_dtype."""
+    Returns out [M, N] of out_dtype.  workspace: see _workspace."""
     L = load_library()
     _need(a, E4M3, "a")
     _need(b, E4M3, "b", a.device)
@@ -291,15 +327,17 @@ def fp8q_scaled_mm_channelwise(a: torch.Tensor, b: torch.Tensor, a_scale: torch.
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=a.device)
     _need(out, out_dtype, "out", a.device)
-    _check("fp8q_scaled_mm_channelwise",
-           L.fp8q_scaled_mm_channelwise(_ptr(a), _ptr(b), b.stride(0), _ptr(a_scale), _ptr(b_scale), _ptr(bias),
-                                        _ptr(out), M, N, K, code, _stream(a.device)))
+    ws, ws_bytes = _workspace(workspace, M, N, K, False, a.device)
+    with _on(a.device):
+        _check("fp8q_scaled_mm_channelwise",
+               L.fp8q_scaled_mm_channelwise(_ptr(a), _ptr(b), b.stride(0), _ptr(a_scale), _ptr(b_scale), _ptr(bias),
+                                            _ptr(out), M, N, K, code, ws, ws_bytes, _stream(a.device)))
     return out
 
 
 def fp8q_scaled_mm_blockwise(a: torch.Tensor, w: torch.Tensor, a_scale: torch.Tensor, w_scale: torch.Tensor,
                              M: int | None = None, bias: torch.Tensor | None = None, out_dtype=torch.bfloat16,
-                             out: torch.Tensor | None = None):
+                             out: torch.Tensor | None = None, workspace="auto"):
     """a e4m3 [m_pad, K] (row-padded); w e4m3 [N, K]; a_scale the (m_pad, K/128)
     column-major view (or its [K/128, m_pad] storage); w_scale fp32 [N/128, K/128].
     Returns out [M, N] (M defaults to m_pad)."""
@@ -322,14 +360,16 @@ def fp8q_scaled_mm_blockwise(a: torch.Tensor, w: torch.Tensor, a_scale: torch.Te
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=a.device)
     _need(out, out_dtype, "out", a.device)
-    _check("fp8q_scaled_mm_blockwise",
-           L.fp8q_scaled_mm_blockwise(_ptr(a), _ptr(w), _ptr(storage), _ptr(w_scale), _ptr(bias), _ptr(out),
-                                      M, m_pad, N, K, code, _stream(a.device)))
+    ws, ws_bytes = _workspace(workspace, M, N, K, True, a.device)
+    with _on(a.device):
+        _check("fp8q_scaled_mm_blockwise",
+               L.fp8q_scaled_mm_blockwise(_ptr(a), _ptr(w), _ptr(storage), _ptr(w_scale), _ptr(bias), _ptr(out),
+                                          M, m_pad, N, K, code, ws, ws_bytes, _stream(a.device)))
     return out
 
 
 def fp8q_linear_channelwise(x: torch.Tensor, b: torch.Tensor, b_scale: torch.Tensor, bias=None,
-                            out_dtype=torch.bfloat16):
+                            out_dtype=torch.bfloat16, workspace="auto"):
     """Per-token quantization of x followed by the channelwise GEMM."""
     L = load_library()
     _need(x, torch.bfloat16, "x")
@@ -344,14 +384,17 @@ def fp8q_linear_channelwise(x: torch.Tensor, b: torch.Tensor, b_scale: torch.Ten
     xq = torch.empty((M, K), dtype=E4M3, device=x.device)
     xs = torch.empty((M,), dtype=torch.float32, device=x.device)
     out = torch.empty((M, N), dtype=out_dtype, device=x.device)
-    _check("fp8q_linear_channelwise",
-           L.fp8q_linear_channelwise(_ptr(x), _ptr(b), b.stride(0), _ptr(b_scale), _ptr(bias), _ptr(out), M, N, K,
-                                     _ptr(xq), _ptr(xs), _out_code(out_dtype), _stream(x.device)))
+    ws, ws_bytes = _workspace(workspace, M, N, K, False, x.device)
+    with _on(x.device):
+        _check("fp8q_linear_channelwise",
+               L.fp8q_linear_channelwise(_ptr(x), _ptr(b), b.stride(0), _ptr(b_scale), _ptr(bias), _ptr(out), M, N,
+                                         K, _ptr(xq), _ptr(xs), _out_code(out_dtype), ws, ws_bytes,
+                                         _stream(x.device)))
     return out
 
 
 def fp8q_linear_blockwise(x: torch.Tensor, w: torch.Tensor, w_scale: torch.Tensor, bias=None,
-                          out_dtype=torch.bfloat16):
+                          out_dtype=torch.bfloat16, workspace="auto"):
     """Row-padded group quantization of x followed by the blockwise GEMM; the
     output has exactly M rows (the padded rows are never materialised)."""
     L = load_library()
@@ -368,9 +411,11 @@ def fp8q_linear_blockwise(x: torch.Tensor, w: torch.Tensor, w_scale: torch.Tenso
     xq = torch.empty((m_pad, K), dtype=E4M3, device=x.device)
     xs = torch.empty((K // 128, m_pad), dtype=torch.float32, device=x.device)
     out = torch.empty((M, N), dtype=out_dtype, device=x.device)
-    _check("fp8q_linear_blockwise",
-           L.fp8q_linear_blockwise(_ptr(x), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(out), M, N, K, _ptr(xq),
-                                   _ptr(xs), m_pad, _out_code(out_dtype), _stream(x.device)))
+    ws, ws_bytes = _workspace(workspace, M, N, K, True, x.device)
+    with _on(x.device):
+        _check("fp8q_linear_blockwise",
+               L.fp8q_linear_blockwise(_ptr(x), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(out), M, N, K, _ptr(xq),
+                                       _ptr(xs), m_pad, _out_code(out_dtype), ws, ws_bytes, _stream(x.device)))
     return out
 
 
@@ -391,9 +436,10 @@ def fp8q_linear_blockwise_fused(x: torch.Tensor, w: torch.Tensor, w_scale: torch
     M, K = x.shape
     N = w.shape[0]
     out = torch.empty((M, N), dtype=out_dtype, device=x.device)
-    _check("fp8q_linear_blockwise_fused",
-           L.fp8q_linear_blockwise_fused(_ptr(x), x.stride(0), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(out), M, N,
-                                         K, _out_code(out_dtype), _stream(x.device)))
+    with _on(x.device):
+        _check("fp8q_linear_blockwise_fused",
+               L.fp8q_linear_blockwise_fused(_ptr(x), x.stride(0), _ptr(w), _ptr(w_scale), _ptr(bias), _ptr(out), M, N,
+                                             K, _out_code(out_dtype), _stream(x.device)))
     return out
 
 
@@ -413,9 +459,10 @@ def fp8q_scaled_mm_w8a16(x: torch.Tensor, w: torch.Tensor, w_scale: torch.Tensor
     N = w.shape[0]
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=x.device)
-    _check("fp8q_scaled_mm_w8a16",
-           L.fp8q_scaled_mm_w8a16(_ptr(x), x.stride(0), _ptr(w), w.stride(0), _ptr(w_scale), _ptr(bias), _ptr(out),
-                                  M, N, K, _out_code(out.dtype), _stream(x.device)))
+    with _on(x.device):
+        _check("fp8q_scaled_mm_w8a16",
+               L.fp8q_scaled_mm_w8a16(_ptr(x), x.stride(0), _ptr(w), w.stride(0), _ptr(w_scale), _ptr(bias), _ptr(out),
+                                      M, N, K, _out_code(out.dtype), _stream(x.device)))
     return out
 
 
@@ -446,9 +493,10 @@ def fp8q_linear_channelwise_noalloc(x: torch.Tensor, b: torch.Tensor, b_scale: t
     _need(out, out_dtype, "out", x.device)
     if tuple(out.shape) != (M, N) or not out.is_contiguous():
         raise ValueError("out must be a contiguous [M, N] tensor")
-    _check("fp8q_linear_channelwise_noalloc",
-           L.fp8q_linear_channelwise_noalloc(_ptr(x), _ptr(b), b.stride(0), _ptr(b_scale), _ptr(bias), _ptr(out),
-                                             M, N, K, _out_code(out_dtype), _stream(x.device)))
+    with _on(x.device):
+        _check("fp8q_linear_channelwise_noalloc",
+               L.fp8q_linear_channelwise_noalloc(_ptr(x), _ptr(b), b.stride(0), _ptr(b_scale), _ptr(bias), _ptr(out),
+                                                 M, N, K, _out_code(out_dtype), _stream(x.device)))
     return out
 
 
@@ -458,6 +506,14 @@ def fp8q_gemm_plan(M: int, N: int, K: int, blockwise: bool = False, num_sms: int
     p = Plan()
     _check("fp8q_gemm_plan", L.fp8q_gemm_plan(M, N, K, int(bool(blockwise)), num_sms, ctypes.byref(p)))
     return p.as_dict()
+
+
+def fp8q_workspace_bytes(M: int, N: int, K: int, blockwise: bool = False, device=None) -> int:
+    """Bytes of split-K workspace the planned GEMM uses on `device` (default:
+    the current device); 0 if its schedule does not split K."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with _on(device):
+        return int(load_library().fp8q_workspace_bytes(M, N, K, int(bool(blockwise))))
 
 
 def fp8q_set_plan_override(swap_ab: int, mma_n: int = 0, split_k: int = 1) -> None:
@@ -470,7 +526,8 @@ def fp8q_device_status(reset: bool = True, device=None) -> int:
     (FP8Q_OK, or FP8Q_ERR_TIMEOUT if a GEMM gave up on a pipeline wait)."""
     L = load_library()
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
-    return int(L.fp8q_device_status(_stream(device), int(bool(reset))))
+    with _on(device):
+        return int(L.fp8q_device_status(_stream(device), int(bool(reset))))
 
 
 def fp8q_selftest_wait_timeout(device=None) -> None:
@@ -478,7 +535,8 @@ def fp8q_selftest_wait_timeout(device=None) -> None:
     (about 2 s); fp8q_device_status() then reports FP8Q_ERR_TIMEOUT."""
     L = load_library()
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
-    _check("fp8q_selftest_wait_timeout", L.fp8q_selftest_wait_timeout(_stream(device)))
+    with _on(device):
+        _check("fp8q_selftest_wait_timeout", L.fp8q_selftest_wait_timeout(_stream(device)))
 
 
 def fp8q_version() -> int:

@@ -155,8 +155,10 @@ fp8q_status fp8q_quant_weight_block128(const void *w, int64_t N, int64_t K, void
 
 fp8q_status fp8q_scaled_mm_channelwise(const void *a, const void *b, int64_t ldb, const float *a_scale,
                                        const float *b_scale, const void *bias, void *out, int64_t M, int64_t N,
-                                       int64_t K, fp8q_out_dtype out_dtype, void *stream)
+                                       int64_t K, fp8q_out_dtype out_dtype, void *workspace, size_t workspace_bytes,
+                                       void *stream)
 {
+    if (workspace != nullptr && !aligned16(workspace)) return FP8Q_ERR_INVALID_ARG;
     if (M < 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return FP8Q_ERR_INVALID_ARG;
     if (out_dtype != FP8Q_OUT_BF16 && out_dtype != FP8Q_OUT_FP16) return FP8Q_ERR_UNSUPPORTED;
     if (K % 16 != 0 || ldb < K || ldb % 16 != 0 || N % 8 != 0) return FP8Q_ERR_INVALID_ARG;
@@ -176,13 +178,17 @@ fp8q_status fp8q_scaled_mm_channelwise(const void *a, const void *b, int64_t ldb
     p.fused_quant = false;
     p.w16 = false;
     p.eps = 0.0f;
+    p.ws = workspace;
+    p.ws_bytes = workspace_bytes;
     return run_gemm(p, as_stream(stream));
 }
 
 fp8q_status fp8q_scaled_mm_blockwise(const void *a, const void *w, const float *a_scale, const float *w_scale,
                                      const void *bias, void *out, int64_t M, int64_t m_pad, int64_t N, int64_t K,
-                                     fp8q_out_dtype out_dtype, void *stream)
+                                     fp8q_out_dtype out_dtype, void *workspace, size_t workspace_bytes,
+                                     void *stream)
 {
+    if (workspace != nullptr && !aligned16(workspace)) return FP8Q_ERR_INVALID_ARG;
     if (M < 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return FP8Q_ERR_INVALID_ARG;
     if (out_dtype != FP8Q_OUT_BF16 && out_dtype != FP8Q_OUT_FP16) return FP8Q_ERR_UNSUPPORTED;
     if (N % 128 != 0 || K % 128 != 0) return FP8Q_ERR_UNSUPPORTED;
@@ -203,13 +209,16 @@ fp8q_status fp8q_scaled_mm_blockwise(const void *a, const void *w, const float *
     p.fused_quant = false;
     p.w16 = false;
     p.eps = 0.0f;
+    p.ws = workspace;
+    p.ws_bytes = workspace_bytes;
     return run_gemm(p, as_stream(stream));
 }
 
 fp8q_status fp8q_linear_channelwise(const void *x, const void *b, int64_t ldb, const float *b_scale, const void *bias,
                                     void *out, int64_t M, int64_t N, int64_t K, void *xq, float *xs,
-                                    fp8q_out_dtype out_dtype, void *stream)
+                                    fp8q_out_dtype out_dtype, void *workspace, size_t workspace_bytes, void *stream)
 {
+    if (workspace != nullptr && !aligned16(workspace)) return FP8Q_ERR_INVALID_ARG;
     // Validate the GEMM's arguments before enqueueing the quantizer so that
     // an error leaves nothing enqueued.
     if (M < 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return FP8Q_ERR_INVALID_ARG;
@@ -221,13 +230,15 @@ fp8q_status fp8q_linear_channelwise(const void *x, const void *b, int64_t ldb, c
         return FP8Q_ERR_INVALID_ARG;
     s = fp8q_quant_per_token(x, M, K, K, xq, xs, 1e-10f, stream);
     if (s != FP8Q_OK) return s;
-    return fp8q_scaled_mm_channelwise(xq, b, ldb, xs, b_scale, bias, out, M, N, K, out_dtype, stream);
+    return fp8q_scaled_mm_channelwise(xq, b, ldb, xs, b_scale, bias, out, M, N, K, out_dtype, workspace,
+                                      workspace_bytes, stream);
 }
 
 fp8q_status fp8q_linear_blockwise(const void *x, const void *w, const float *w_scale, const void *bias, void *out,
                                   int64_t M, int64_t N, int64_t K, void *xq, float *xs, int64_t m_pad,
-                                  fp8q_out_dtype out_dtype, void *stream)
+                                  fp8q_out_dtype out_dtype, void *workspace, size_t workspace_bytes, void *stream)
 {
+    if (workspace != nullptr && !aligned16(workspace)) return FP8Q_ERR_INVALID_ARG;
     if (M < 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return FP8Q_ERR_INVALID_ARG;
     if (out_dtype != FP8Q_OUT_BF16 && out_dtype != FP8Q_OUT_FP16) return FP8Q_ERR_UNSUPPORTED;
     if (N % 128 != 0 || K % 128 != 0) return FP8Q_ERR_UNSUPPORTED;
@@ -240,7 +251,8 @@ fp8q_status fp8q_linear_blockwise(const void *x, const void *w, const float *w_s
     if (bias != nullptr && (reinterpret_cast<uintptr_t>(bias) & 1u)) return FP8Q_ERR_INVALID_ARG;
     s = fp8q_quant_per_token_group_row_padded(x, M, K, K, 128, 1e-10f, 4, xq, xs, m_pad, stream);
     if (s != FP8Q_OK) return s;
-    return fp8q_scaled_mm_blockwise(xq, w, xs, w_scale, bias, out, M, m_pad, N, K, out_dtype, stream);
+    return fp8q_scaled_mm_blockwise(xq, w, xs, w_scale, bias, out, M, m_pad, N, K, out_dtype, workspace,
+                                    workspace_bytes, stream);
 }
 
 fp8q_status fp8q_linear_blockwise_fused(const void *x, int64_t ldx, const void *w, const float *w_scale,
@@ -269,6 +281,8 @@ fp8q_status fp8q_linear_blockwise_fused(const void *x, int64_t ldx, const void *
     p.fused_quant = true;
     p.w16 = false;
     p.eps = 1e-10f;
+    p.ws = nullptr;
+    p.ws_bytes = 0;
     return run_gemm(p, as_stream(stream));
 }
 
@@ -306,6 +320,8 @@ fp8q_status fp8q_scaled_mm_w8a16(const void *x, int64_t ldx, const void *w, int6
     p.fused_quant = false;
     p.w16 = true;
     p.eps = 0.0f;
+    p.ws = nullptr;
+    p.ws_bytes = 0;
     return launch_planned(p, pl, as_stream(stream));
 }
 
@@ -329,6 +345,6 @@ const char *fp8q_status_str(fp8q_status status)
     }
 }
 
-int32_t fp8q_version(void) { return (1 << 16) | 0; }
+int32_t fp8q_version(void) { return (2 << 16) | 0; }
 
 }  // extern "C"

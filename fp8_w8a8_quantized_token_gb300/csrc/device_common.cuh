@@ -155,19 +155,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
-// As tma_load_2d, but the tile lands at the same shared-memory offset in
-// every CTA of the cluster named in `cta_mask`, and each of them receives
-// the complete_tx on its own mbarrier at `bar`'s offset.
-__device__ __forceinline__ void tma_load_2d_mc(void *dst, const CUtensorMap *map, uint64_t *bar, int32_t c0,
-                                               int32_t c1, uint16_t cta_mask, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(cta_mask), "l"(policy)
-        : "memory");
-}
-
 // Load issued by either CTA of a CTA pair feeding a 2-CTA MMA: the tile
 // lands in the issuing CTA's shared memory, its complete_tx goes to the
 // mbarrier at `bar_cluster` (a shared::cluster address, here always the
@@ -405,17 +392,6 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
-}
-
-// As umma_commit, arriving on the mbarrier at `bar`'s offset in every CTA of
-// the cluster named in `cta_mask`.
-__device__ __forceinline__ void umma_commit_mc(uint64_t *bar, uint16_t cta_mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
 }
 
 // 32 lanes x 16 consecutive 32-bit columns: thread i of the warp gets lane

@@ -31,28 +31,33 @@
 //   SWAP = false (prefill M):      A = 128 tokens, B = BN weight rows;
 //                 TMEM lane = token m, TMEM column = output column n.
 //
-// Paired tiles (non-swapped, split 1).  Two CTAs of a 2-CTA cluster take
-// the token tiles 2t and 2t+1 against the same BN weight rows; each loads
-// half of the weight slice and multicasts it into both CTAs' rings, so
-// every weight byte leaves L2 once per pair.  A ring slot is refilled only
-// after both CTAs' MMAs have consumed it (each MMA commit arrives on both
-// CTAs' empty barriers).
-//
-// 2-CTA MMA (TWO_SM, non-swapped channelwise).  The same CTA pairs compute
-// a 256-token x BN tile with tcgen05.mma.cta_group::2 (M = 256) issued by
-// the even CTA: each CTA stages only its own 128 tokens and its half of the
-// BN weight rows (no duplicate copy of the weights in either CTA), all of a
-// slot's loads complete on the even CTA's full barrier, and the even CTA's
-// commits arrive on both CTAs' empty and accumulator barriers.  Each CTA's
-// TMEM holds its own 128 accumulator rows; both epilogues release the even
-// CTA's accumulator slot.
+// 2-CTA MMA (TWO_SM, non-swapped channelwise, split 1).  Two CTAs of a
+// 2-CTA cluster ("a pair") take the token tiles 2t and 2t+1 against the
+// same BN weight rows and compute the 256-token x BN tile with
+// tcgen05.mma.cta_group::2 (M = 256) issued by the even CTA: each CTA loads
+// (plain TMA into its own shared memory) only its own 128 tokens and its
+// half of the BN weight rows, so every weight byte leaves L2 once per pair
+// and neither CTA holds a duplicate copy.  All of a slot's loads complete on
+// the even CTA's full barrier, and the even CTA's commits arrive on both
+// CTAs' empty and accumulator barriers.  Each CTA's TMEM holds its own 128
+// accumulator rows; both epilogues release the even CTA's accumulator slot.
 //
 // Split-K.  split > 1 launches thread-block clusters of `split` CTAs that
-// share one output tile and take consecutive ranges of K blocks; each CTA
-// writes its fp32 partial tile to its own shared memory, and after a
-// cluster barrier every CTA sums a slice of rows over all CTAs of the
-// cluster in rank order (distributed shared memory), so the result is
-// deterministic and needs no global workspace.
+// share one output tile and take consecutive ranges of K blocks.  Each CTA
+// stages its fp32 partial tile in its own (then idle) shared-memory ring;
+// the tile's outputs are divided among the ranks, and each rank sums its
+// share over all ranks' partials in rank order (deterministic).  The
+// partials of the other ranks reach the owner in one of two ways:
+//   * a caller-provided global workspace (GemmArgs::ws): each CTA writes the
+//     parts of its partial tile that other ranks own into its own slot
+//     (coalesced stores that stay in L2), one cluster barrier publishes
+//     them, and each owner reads its share of every slot;
+//   * no workspace: through distributed shared memory (the non-swapped
+//     orientation pulls its share from every CTA after a cluster barrier,
+//     the swapped orientation pushes each rank's rows into that rank's
+//     receive buffer with bulk copies).
+// Both ways add the same values in the same order, so they give identical
+// results.
 //
 // Every mbarrier wait is bounded (device_common.cuh); a wait that runs out
 // records a timeout in the status word and all roles wind down, waiting
@@ -72,7 +77,7 @@ struct GemmArgs {
     int split;             // CTAs per cluster along K
     int group;             // tile rasterisation group
     int raster_b;          // 1: groups of B-operand tiles sweep the A tiles (else the reverse)
-    int pair;              // 1: paired tiles (non-swapped, split 1): num_tiles counts tile pairs
+    int pair;              // 1: 2-CTA MMA pairs (TWO_SM): num_tiles counts tile pairs
     const float *a_scale;
     const float *w_scale;
     const __nv_bfloat16 *bias;
@@ -85,6 +90,7 @@ struct GemmArgs {
     float eps;                  // fused quantization: the amax floor of the group scales
     const __nv_bfloat16 *x;     // fused quantization: bf16 activations [M, K]
     long long ldx;              //   and their row stride (elements)
+    float *ws;                  // split-K workspace: split slots of 128 x BN floats per cluster, or null
 };
 
 // Phase timestamps of a trace build (-DFP8Q_TRACE): kTraceSlots 64-bit
@@ -329,6 +335,111 @@ __device__ __forceinline__ void store_box_tma(const CUtensorMap *tm_out, uint8_t
     }
 }
 
+// Split-K reduction through the global workspace (every thread of the CTA
+// calls it; the cluster barrier inside needs all of them).  The partial
+// tile of this CTA is in sRed, row r (TMEM lane: a token of a non-swapped
+// tile, an output column of a swapped one) at sRed[r * kPartStride], its
+// BN columns contiguous.  Items are 4-column groups of the tile's valid
+// rows, numbered in the order the owner stores its outputs: non-swapped
+// (r, c4) with c4 fastest (consecutive threads, consecutive output
+// columns of one token); swapped (c4, r) with r fastest (consecutive
+// threads, consecutive output columns n0 + r).  Rank q owns the items
+// [items * q / split, items * (q + 1) / split).  A slot holds one rank's
+// partial in item order (float4 per item), so the copy into the slot and
+// the owner's reads are both contiguous.
+template <typename C, typename OutT, bool BLOCKWISE, bool SWAP, typename Coords>
+__device__ __forceinline__ void reduce_split_workspace(const GemmArgs &p, const float *sRed, const float *sColScale,
+                                                       int rank, int cluster_id, int warp, volatile int *abort,
+                                                       Coords coords)
+{
+    constexpr int SP = C::kPartStride;
+    constexpr int BN = C::kPartStride - 4;   // columns of the partial tile (the MMA N extent)
+    constexpr int G = BN / 4;
+    constexpr long long kSlotFloats = 128LL * BN;
+    const int split = p.split;
+    const bool epi = warp >= C::kEpiWarp0 && warp < C::kEpiWarp0 + C::kEpiWarps;
+    const int etid = threadIdx.x - 32 * C::kEpiWarp0;
+    int a_t, b_t;
+    coords(cluster_id, a_t, b_t);
+    const int m0 = (SWAP ? b_t : a_t) * C::kTokTile;
+    const int n0 = (SWAP ? a_t : b_t) * C::kColTile;
+    // Valid rows of the partial tile.
+    const int rows = SWAP ? min(128, p.N - n0) : min(128, p.M - m0);
+    const int items = rows * G;
+    auto item_rc = [&](int item, int &r, int &c4) {
+        if (SWAP) { c4 = item / rows; r = item - c4 * rows; }
+        else { r = item / G; c4 = item - r * G; }
+    };
+    const int i_lo = static_cast<int>(static_cast<long long>(items) * rank / split);
+    const int i_hi = static_cast<int>(static_cast<long long>(items) * (rank + 1) / split);
+    float4 *slots = reinterpret_cast<float4 *>(p.ws + static_cast<long long>(cluster_id) * split * kSlotFloats);
+    if (epi) {
+        // The whole partial tile is in shared memory.
+        named_barrier_sync(1, C::kEpiThreads);
+        if (!*abort) {
+            // The items other ranks own, into this rank's slot.
+            float4 *mine = slots + static_cast<long long>(rank) * (kSlotFloats / 4);
+            for (int item = etid; item < items; item += C::kEpiThreads) {
+                if (item >= i_lo && item < i_hi) continue;
+                int r, c4;
+                item_rc(item, r, c4);
+                __stcg(mine + item, *reinterpret_cast<const float4 *>(sRed + r * SP + 4 * c4));
+            }
+        }
+        __threadfence();
+    }
+    // Publishes every rank's slot to the cluster (release / acquire).
+    cluster_sync();
+    if (!epi || *abort) return;
+    OutT *out = static_cast<OutT *>(p.out);
+    for (int item = i_lo + etid; item < i_hi; item += C::kEpiThreads) {
+        int r, c4;
+        item_rc(item, r, c4);
+        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < split; ++q) {
+            const float4 v = q == rank ? *reinterpret_cast<const float4 *>(sRed + r * SP + 4 * c4)
+                                       : __ldcg(slots + static_cast<long long>(q) * (kSlotFloats / 4) + item);
+            sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+        }
+        const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+        if (SWAP) {
+            // Output column n0 + r; tokens m0 + 4 c4 .. + 3 (scales staged
+            // in sColScale by the epilogue).
+            const int n = n0 + r;
+            const float wsc = BLOCKWISE ? 1.0f : __ldg(p.w_scale + n);
+            const float bv = p.bias != nullptr ? __bfloat162float(p.bias[n]) : 0.0f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int m = m0 + c4 * 4 + e;
+                if (m < p.M) {
+                    const float y = BLOCKWISE ? sv[e] + bv : fmaf(sv[e] * wsc, sColScale[c4 * 4 + e], bv);
+                    out[static_cast<long long>(m) * p.ldo + n] = to_out<OutT>(y);
+                }
+            }
+        } else {
+            // Token m0 + r; output columns n0 + 4 c4 .. + 3.
+            const int m = m0 + r, n = n0 + 4 * c4;
+            if (n >= p.N) continue;
+            const float am = BLOCKWISE ? 1.0f : __ldg(p.a_scale + m);
+            float y[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const bool in = n + e < p.N;
+                const float bv = (p.bias != nullptr && in) ? __bfloat162float(p.bias[n + e]) : 0.0f;
+                y[e] = BLOCKWISE ? sv[e] + bv : fmaf(sv[e] * am, in ? __ldg(p.w_scale + n + e) : 0.0f, bv);
+            }
+            OutT *o = out + static_cast<long long>(m) * p.ldo + n;
+            if (n + 4 <= p.N) {
+                *reinterpret_cast<uint2 *>(o) = make_uint2(pack_out2<OutT>(y[0], y[1]), pack_out2<OutT>(y[2], y[3]));
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (n + e < p.N) o[e] = to_out<OutT>(y[e]);
+            }
+        }
+    }
+}
+
 template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT, bool TWO_SM = false, bool FQ = false,
           bool W16 = false>
 __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ, W16>::kThreads, 1)
@@ -364,7 +475,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = p.split;
-    const bool pair = !SWAP && (TWO_SM || p.pair != 0);   // then split == 1
+    const bool pair = TWO_SM;                 // (then non-swapped, split == 1)
     const int csize = pair ? 2 : split;       // CTAs per cluster
     const int rank = csize > 1 ? static_cast<int>(cluster_ctarank()) : 0;
     const int krank = pair ? 0 : rank;        // position along K
@@ -381,11 +492,10 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
         tile_order(tile, a_tiles, b_tiles, p.group, p.raster_b, a_t, b_t);
         if (pair) a_t = 2 * a_t + rank;
     };
-    // Paired: this CTA's half of the weight slice (rows and ring offset;
-    // TWO_SM rings hold only that half).
+    // Paired: this CTA's half of the weight rows (its ring holds only that
+    // half).
     constexpr int kHalfRows = BN / 2;
     const int w_half_row = pair ? rank * kHalfRows : 0;
-    const uint32_t w_half_off = (pair && !TWO_SM) ? static_cast<uint32_t>(rank) * kHalfRows * 128u : 0u;
     const bool leader = rank == 0;  // TWO_SM: the CTA that issues the MMAs
     // TWO_SM: a ring slot's full barrier in the even CTA (shared::cluster).
     auto lead_full = [&](int stage) { return dsmem_map(smem_u32(&full[stage]), 0u); };
@@ -411,7 +521,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
             // converting warps' arrivals alone publish the stage (its bf16 A
             // tile in tensor memory and its activation B tile).
             mbar_init(&full[s], W16 ? C::kConvWarps : 1 + C::kQuantWarps);
-            mbar_init(&empty[s], (BLOCKWISE ? C::kEpiWarps : 0) + ((pair && !TWO_SM) ? 2 : C::kIssuers));
+            mbar_init(&empty[s], (BLOCKWISE ? C::kEpiWarps : 0) + C::kIssuers);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], C::kIssuers);
@@ -426,7 +536,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
 
         *abort = 0;
         fence_mbar_init();
-        if (C::kPush && split > 1) {
+        if (C::kPush && split > 1 && p.ws == nullptr) {
             // Expect the partial rows this CTA owns from every other rank
             // (armed before the cluster barrier below, so before any push).
             const int my_rows = 4 * (32 * (rank + 1) / split) - 4 * (32 * rank / split);
@@ -454,7 +564,8 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
     // armed before any CTA of the cluster may push into it.  Arrive now,
     // wait just before the dependency wait (the latency overlaps the rest of
     // the prologue).
-    if (C::kPush && split > 1) cluster_arrive_relaxed();
+    const bool push = C::kPush && split > 1 && p.ws == nullptr;   // DSMEM push reduction
+    if (push) cluster_arrive_relaxed();
     // Weight slices of the first tile issued before the dependency wait.
     int npre = 0;
     if (warp == 0 && lane == 0) {
@@ -485,18 +596,14 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                     continue;
                 }
                 mbar_arrive_expect_tx(&wbar[i], C::kStageTx);
-                if (pair)
-                    tma_load_2d_mc(wbuf + i * wbytes + w_half_off, wmap, &full[i], (kb_begin + i) * 128,
-                                   wrow + w_half_row, 3, pol_w);
-                else
-                    tma_load_2d(wbuf + i * wbytes, wmap, &wbar[i], (kb_begin + i) * 128, wrow, pol_w);
+                tma_load_2d(wbuf + i * wbytes, wmap, &wbar[i], (kb_begin + i) * 128, wrow, pol_w);
             }
             const int pf = nkb < p.prefetch_kb ? nkb : p.prefetch_kb;
             for (int i = npre; i < pf; ++i) tma_prefetch_l2_2d(wmap, (kb_begin + i) * 128, wrow + w_half_row);
         }
         FP8Q_TRACE_AT(p, kTrPreloaded);
     }
-    if (C::kPush && split > 1) cluster_wait();
+    if (push) cluster_wait();
     // The producer's cache policies, made before the dependency wait.
     uint64_t pol_a = 0, pol_b = 0;
     if (warp == 0 && lane == 0) {
@@ -564,12 +671,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                         if (!mbar_wait(&empty[stage], phase ^ 1u, abort, p.status)) { ok = false; break; }
                         mbar_arrive_expect_tx(&full[stage], C::kStageTx);
                         tma_load_2d(sA + stage * C::kABytes, &tm_a, &full[stage], kb * 128, a_row, pol_a);
-                        if (FQ) {
-                        } else if (pair)
-                            tma_load_2d_mc(sB + stage * C::kBBytes + w_half_off, &tm_b, &full[stage], kb * 128,
-                                           b_row + w_half_row, 3, pol_b);
-                        else
-                            tma_load_2d(sB + stage * C::kBBytes, &tm_b, &full[stage], kb * 128, b_row, pol_b);
+                        if (!FQ) tma_load_2d(sB + stage * C::kBBytes, &tm_b, &full[stage], kb * 128, b_row, pol_b);
                     }
                     if (BLOCKWISE && !FQ)
                         tma_load_2d(sSA + stage * C::kSASlotFloats, &tm_sa, &full[stage], m_tile * C::kTokTile, kb,
@@ -648,7 +750,6 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                         }
                     }
                     if (TWO_SM) umma_commit_pair_mc(&empty[stage], 3);
-                    else if (pair) umma_commit_mc(&empty[stage], 3);
                     else umma_commit(&empty[stage]);
                     if (BLOCKWISE) {
                         umma_commit(&tfull[slot]);
@@ -1080,7 +1181,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                         }
                     }
                 }
-            } else if (C::kPush) {
+            } else if (push) {
                 // Split-K, push: stage the partial tile row-major in the idle
                 // ring, push each other rank's rows into its receive buffer
                 // (bulk DSMEM copies completing on its mbarrier), then the
@@ -1142,9 +1243,9 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                 // before it may exit.
                 if (etid == 0) bulk_wait_read();
             } else {
-                // Split-K, pull: publish this CTA's partial tile row-major
-                // with padded rows (the ring is idle: every copy was consumed
-                // and every MMA has completed).
+                // Split-K, pull or workspace: publish this CTA's partial tile
+                // row-major with padded rows (the ring is idle: every copy was
+                // consumed and every MMA has completed).
                 constexpr int SP = C::kPartStride;
                 named_barrier_sync(1, C::kEpiThreads);
 #pragma unroll
@@ -1160,7 +1261,10 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
 
     }
 
-    if constexpr (!C::kPush) {
+    if (split > 1 && p.ws != nullptr) {
+        reduce_split_workspace<C, OutT, BLOCKWISE, SWAP>(p, sRed, sColScale, rank, cluster_id, warp, abort,
+                                                        [&](int tile, int &a_t, int &b_t) { coords(tile, a_t, b_t); });
+    } else if constexpr (!C::kPush) {
         if (split > 1) {
             cluster_sync();
             if (threadIdx.x == 32 * C::kEpiWarp0) FP8Q_TRACE_AT(p, kTrCluster1);
@@ -1222,8 +1326,9 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
 
     tc_fence_before();
     __syncthreads();
-    // Paired: neither CTA may exit while the other can still multicast into
-    // its shared memory or arrive on its barriers.
+    // Paired: neither CTA may exit while the other can still load into its
+    // shared memory (the odd CTA's loads signal the even CTA's barriers) or
+    // arrive on its barriers.
     if (pair) cluster_sync();
     if (warp == 1) {
         tc_fence_after();

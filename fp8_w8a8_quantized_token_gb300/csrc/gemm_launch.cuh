@@ -34,7 +34,7 @@ cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigne
     // Operand maps: e4m3 rows of K bytes, boxes of 128 (K) x rows.
     CUtensorMap tm_w, tm_x, tm_sa;
     const int tok_box = C::kTokTile;
-    const bool pair = !SWAP && (TWO_SM || l.pair);
+    const bool pair = TWO_SM;   // 2-CTA MMA pairs (non-swapped channelwise, split 1)
     // Paired tiles: each CTA loads half of the weight rows of the tile.
     const int wrow_box = SWAP ? 128 : (pair ? BN / 2 : BN);
     if (!make_tmap_2d(&tm_w, pr.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(pr.K),
@@ -103,6 +103,10 @@ cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigne
     a.eps = pr.eps;
     a.x = FQ ? static_cast<const __nv_bfloat16 *>(pr.a) : nullptr;
     a.ldx = pr.lda;
+    // Split-K partials go through the workspace when the caller gave one
+    // large enough for this schedule (one 128 x BN slot per CTA).
+    const size_t ws_need = static_cast<size_t>(a.num_tiles) * static_cast<size_t>(a.split) * 128u * BN * 4u;
+    a.ws = (a.split > 1 && pr.ws != nullptr && pr.ws_bytes >= ws_need) ? static_cast<float *>(pr.ws) : nullptr;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(l.grid));

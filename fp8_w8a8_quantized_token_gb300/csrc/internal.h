@@ -27,8 +27,8 @@ struct GemmLaunch {
     int split;         // K-split count = cluster size
     int grid;          // CTAs
     int stages;        // pipeline depth the instantiation uses
-    bool pair;         // non-swapped, split 1: 2-CTA clusters share each weight slice
-    bool two_sm;       // pair computing 256-token tiles with 2-CTA MMAs (channelwise)
+    bool pair;         // non-swapped channelwise, split 1: 2-CTA clusters on adjacent token tiles
+    bool two_sm;       // the pair computes 256-token tiles with 2-CTA MMAs (always with pair)
 };
 
 struct GemmProblem {
@@ -48,7 +48,13 @@ struct GemmProblem {
     bool fused_quant;       // blockwise: a is bf16, quantized inside the GEMM (group 128, eps)
     bool w16;               // channelwise weight-only FP8: a is bf16 (row stride lda), no a_scale
     float eps;              // fused_quant: amax floor of the group scales
+    void *ws;               // split-K workspace (16-byte aligned) or null
+    size_t ws_bytes;        // its size; smaller than the schedule needs = not used
 };
+
+// Bytes of split-K workspace a schedule uses (0 when K is not split): one
+// slot of 128 x mma_n fp32 partial sums per CTA.
+size_t plan_workspace_bytes(int64_t M, int64_t N, int swap_ab, int mma_n, int split_k);
 
 // Launchers return cudaSuccess or the launch error; a tensor map the driver
 // rejects is reported as cudaErrorInvalidValue.

@@ -70,7 +70,7 @@ extern "C" fp8q_status fp8q_linear_channelwise_noalloc(const void *x, const void
     using namespace fp8q;
     if (M < 0 || K <= 0) return FP8Q_ERR_INVALID_ARG;
     if (M == 0) return fp8q_linear_channelwise(x, b, ldb, b_scale, bias, out, M, N, K, nullptr, nullptr, out_dtype,
-                                               stream);
+                                               nullptr, 0, stream);
     // Beyond the array's capacity: refused before any CUDA call.
     if (M > kNoAllocMaxRows || K > kNoAllocMaxCodes || M * K > kNoAllocMaxCodes) return FP8Q_ERR_UNSUPPORTED;
     uint8_t *scratch = scratch_address();
@@ -78,5 +78,5 @@ extern "C" fp8q_status fp8q_linear_channelwise_noalloc(const void *x, const void
     // Nothing in the array needs clearing: the quantizer writes every code
     // and scale the GEMM then reads, whatever an earlier call left there.
     return fp8q_linear_channelwise(x, b, ldb, b_scale, bias, out, M, N, K, scratch,
-                                   reinterpret_cast<float *>(scratch + kScaleOffset), out_dtype, stream);
+                                   reinterpret_cast<float *>(scratch + kScaleOffset), out_dtype, nullptr, 0, stream);
 }

@@ -116,6 +116,14 @@ bool table_plan(int64_t M, int64_t N, int64_t K, int blockwise, fp8q_plan *pl)
 
 }  // namespace
 
+size_t plan_workspace_bytes(int64_t M, int64_t N, int swap_ab, int mma_n, int split_k)
+{
+    if (split_k <= 1) return 0;
+    const int64_t tile_m = swap_ab ? mma_n : 128, tile_n = swap_ab ? 128 : mma_n;
+    const int64_t tiles = ((M + tile_m - 1) / tile_m) * ((N + tile_n - 1) / tile_n);
+    return static_cast<size_t>(tiles) * static_cast<size_t>(split_k) * 128u * static_cast<size_t>(mma_n) * 4u;
+}
+
 // Tile sizes, grid and persistence for a chosen (swap_ab, mma_n, split_k).
 void plan_finish(int64_t M, int64_t N, int64_t K, int blockwise, int num_sms, fp8q_plan *pl)
 {
@@ -128,11 +136,15 @@ void plan_finish(int64_t M, int64_t N, int64_t K, int blockwise, int num_sms, fp
     if (split > num_kb) split = num_kb;
     if (split < 1) split = 1;
     pl->split_k = static_cast<int32_t>(split);
-    // Pairs of CTAs on adjacent token tiles share each weight slice
-    // (multicast) whenever there are two token tiles to pair.
+    // Channelwise 256-column tiles on adjacent token tiles run as CTA pairs
+    // with 2-CTA MMAs (256 tokens x 256 columns per pair, each CTA loading
+    // half of the weight rows) whenever there are two token tiles to pair.
+    // Blockwise tiles stay single: their per-K-block promotion hands each
+    // accumulator slot back to the MMA every K block, which a 2-CTA MMA would
+    // couple across both CTAs' epilogues.  FP8Q_NO_PAIR=1 turns pairs off.
     static const bool no_pair = getenv("FP8Q_NO_PAIR") != nullptr && getenv("FP8Q_NO_PAIR")[0] == '1';
     const int64_t m_tiles = (M + pl->tile_m - 1) / pl->tile_m;
-    pl->pair = (!pl->swap_ab && split == 1 && m_tiles >= 2 && !no_pair) ? 1 : 0;
+    pl->pair = (!pl->swap_ab && !blockwise && pl->mma_n == 256 && split == 1 && m_tiles >= 2 && !no_pair) ? 1 : 0;
     if (pl->pair) {
         const int64_t pairs = ((m_tiles + 1) / 2) * ((N + pl->tile_n - 1) / pl->tile_n);
         const int64_t max_pairs = num_sms / 2 > 0 ? num_sms / 2 : 1;
@@ -145,10 +157,7 @@ void plan_finish(int64_t M, int64_t N, int64_t K, int blockwise, int num_sms, fp
         pl->grid = static_cast<int32_t>(tiles < num_sms ? tiles : num_sms);
         pl->persistent = tiles > num_sms ? 1 : 0;
     }
-    // Channelwise pairs use 2-CTA MMAs (FP8Q_NO_2SM=1 keeps the multicast
-    // pairs, for comparison).
-    static const bool no_2sm = getenv("FP8Q_NO_2SM") != nullptr && getenv("FP8Q_NO_2SM")[0] == '1';
-    pl->two_sm = (pl->pair && !blockwise && pl->mma_n == 256 && !no_2sm) ? 1 : 0;
+    pl->two_sm = pl->pair;
     pl->stages = pl->two_sm ? kTwoSmStages : stages_for(pl->swap_ab != 0, pl->mma_n);
 }
 
@@ -186,6 +195,14 @@ extern "C" fp8q_status fp8q_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t b
     }
     *plan = pl;
     return FP8Q_OK;
+}
+
+extern "C" size_t fp8q_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t blockwise)
+{
+    using namespace fp8q;
+    fp8q_plan pl;
+    if (M <= 0 || fp8q_gemm_plan(M, N, K, blockwise, 0, &pl) != FP8Q_OK) return 0;
+    return plan_workspace_bytes(M, N, pl.swap_ab, pl.mma_n, pl.split_k);
 }
 
 extern "C" fp8q_status fp8q_set_plan_override(int32_t swap_ab, int32_t mma_n, int32_t split_k)

@@ -2,7 +2,8 @@
 
 For every linear shape of the benchmark workloads and a grid of M values,
 each candidate schedule (operand orientation, MMA N extent, K-split) is
-timed on the GPU -- 8 back-to-back launches over rotating weight copies
+timed on the GPU with the split-K workspace it uses -- 8 back-to-back
+launches over rotating weight copies
 (more than twice L2 in total) captured in a CUDA graph, replayed 10 times,
 CUDA events on the launching stream -- and the fastest one becomes the
 table row for that (N, K, scheme, M).  Run on a GB300:
@@ -85,19 +86,28 @@ def main():
                 (xq, xs), m_pad = fq.fp8q_quant_per_token(x), M
             out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
 
+            work = None
+
             def gemm(wqi, sp):
+                wp, wn = (None, 0) if work is None else (P(work.data_ptr()), work.numel())
                 if bw:
                     st = L.fp8q_scaled_mm_blockwise(P(xq.data_ptr()), P(wqi.data_ptr()), P(xs.data_ptr()),
-                                                    P(ws.data_ptr()), None, P(out.data_ptr()), M, m_pad, N, K, 0, sp)
+                                                    P(ws.data_ptr()), None, P(out.data_ptr()), M, m_pad, N, K, 0,
+                                                    wp, wn, sp)
                 else:
                     st = L.fp8q_scaled_mm_channelwise(P(xq.data_ptr()), P(wqi.data_ptr()), K, P(xs.data_ptr()),
-                                                      P(ws.data_ptr()), None, P(out.data_ptr()), M, N, K, 0, sp)
+                                                      P(ws.data_ptr()), None, P(out.data_ptr()), M, N, K, 0, wp,
+                                                      wn, sp)
                 if st != 0:
                     raise RuntimeError(fq.status_str(st))
 
             timed = []
             for cand in candidates(M):
                 fq.fp8q_set_plan_override(*cand)
+                # Each candidate with the split-K workspace it uses (as the
+                # library's callers pass it).
+                need = fq.fp8q_workspace_bytes(M, N, K, bool(bw))
+                work = torch.empty(need, dtype=torch.uint8, device=dev) if need else None
                 side = torch.cuda.Stream()
                 with torch.cuda.stream(side):
                     for i in range(2):

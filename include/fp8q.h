@@ -198,12 +198,18 @@ FP8Q_API fp8q_status fp8q_quant_weight_block128(const void *w, int64_t N, int64_
  *           ldb >= K, ldb % 16 == 0.
  * a_scale : fp32 [M]; b_scale : fp32 [N]; bias : bf16 [N] or NULL.
  * out     : [M, N] row-major (ld = N) of out_dtype (N % 8 == 0).
- * Errors  : INVALID_ARG / UNSUPPORTED as above.
+ * workspace, workspace_bytes : optional DEVICE scratch for the split-K
+ *           partial sums (see fp8q_workspace_bytes); NULL / 0 or too small
+ *           for the schedule: the partials are exchanged in distributed
+ *           shared memory instead.  Same result either way.
+ * Errors  : INVALID_ARG / UNSUPPORTED as above; INVALID_ARG for a
+ *           workspace that is not 16-byte aligned.
  * ------------------------------------------------------------------------- */
 FP8Q_API fp8q_status fp8q_scaled_mm_channelwise(const void *a, const void *b, int64_t ldb,
                                        const float *a_scale, const float *b_scale,
                                        const void *bias, void *out, int64_t M, int64_t N,
-                                       int64_t K, fp8q_out_dtype out_dtype, void *stream);
+                                       int64_t K, fp8q_out_dtype out_dtype, void *workspace,
+                                       size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
  * fp8q_scaled_mm_blockwise -- [PR27896] "Key source snippets",
@@ -221,13 +227,39 @@ FP8Q_API fp8q_status fp8q_scaled_mm_channelwise(const void *a, const void *b, in
  * bias    : bf16 [N] or NULL.   out : [M, N] row-major of out_dtype.
  * m_pad   : >= M and a multiple of 4 (keeps each scale column 16-byte
  *           aligned for the Tensor Memory Accelerator).
+ * workspace, workspace_bytes : as fp8q_scaled_mm_channelwise.
  * Errors  : UNSUPPORTED when N or K is not a multiple of 128 (the pages
  *           fall back to another kernel there; this library refuses).
  * ------------------------------------------------------------------------- */
 FP8Q_API fp8q_status fp8q_scaled_mm_blockwise(const void *a, const void *w, const float *a_scale,
                                      const float *w_scale, const void *bias, void *out,
                                      int64_t M, int64_t m_pad, int64_t N, int64_t K,
-                                     fp8q_out_dtype out_dtype, void *stream);
+                                     fp8q_out_dtype out_dtype, void *workspace,
+                                     size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * fp8q_workspace_bytes -- the split-K workspace of the GEMM the library
+ * would launch for (M, N, K, blockwise) on the CURRENT device (the
+ * schedule depends on its SM count and on any plan override in force).
+ * 0 when that schedule does not split K (then no workspace is used).
+ * The scratch argument of the GEMM calls on the pages' interface (the
+ * fp8_scaled_mm / fp8_blockwise_scaled_mm callers own all device memory).
+ *
+ * With K split over a cluster of s CTAs, each CTA computes an fp32 partial
+ * tile over its range of K blocks.  Given a workspace of at least this
+ * size, every CTA writes the parts of its partial tile that other CTAs of
+ * its cluster own into its own slot (one slot of 128 x mma_n floats per
+ * CTA: tiles * s * 128 * mma_n * 4 bytes), a cluster barrier publishes
+ * them, and each CTA adds up its share of the outputs over all s partials
+ * in a fixed order.  The slots are traffic through L2, which is faster
+ * than the distributed-shared-memory exchange used without a workspace,
+ * and gives the same result.  Nothing in the workspace has to be
+ * initialised, and its contents are undefined after the call.  Calls that
+ * can run concurrently on the GPU need separate workspaces; calls in
+ * order on one stream can share one.
+ * Returns 0 as well for invalid sizes (M <= 0, N <= 0, K <= 0).
+ * ------------------------------------------------------------------------- */
+FP8Q_API size_t fp8q_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t blockwise);
 
 /* ---------------------------------------------------------------------------
  * Linear-layer compositions (two launches each, no padding copies):
@@ -237,15 +269,17 @@ FP8Q_API fp8q_status fp8q_scaled_mm_blockwise(const void *a, const void *w, cons
  *   m_pad = ceil(M/4)*4 or a larger multiple of 4 -- the row-padded
  *   pipeline of [PR27896] "Implementation breakdown" (quantizer writes the
  *   GEMM's final layout; output sliced to M rows).
+ * workspace, workspace_bytes : passed to the GEMM (fp8q_workspace_bytes).
  * ------------------------------------------------------------------------- */
 FP8Q_API fp8q_status fp8q_linear_channelwise(const void *x, const void *b, int64_t ldb,
                                     const float *b_scale, const void *bias, void *out,
                                     int64_t M, int64_t N, int64_t K, void *xq, float *xs,
-                                    fp8q_out_dtype out_dtype, void *stream);
+                                    fp8q_out_dtype out_dtype, void *workspace,
+                                    size_t workspace_bytes, void *stream);
 FP8Q_API fp8q_status fp8q_linear_blockwise(const void *x, const void *w, const float *w_scale,
                                   const void *bias, void *out, int64_t M, int64_t N, int64_t K,
                                   void *xq, float *xs, int64_t m_pad, fp8q_out_dtype out_dtype,
-                                  void *stream);
+                                  void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
  * fp8q_scaled_mm_w8a16 -- weight-only FP8 linear (W8A16): bf16 activations
@@ -298,7 +332,8 @@ FP8Q_API fp8q_status fp8q_linear_blockwise_fused(const void *x, int64_t ldx, con
  * an addition of this library for callers that cannot allocate.
  *
  * Same computation, arguments and errors as fp8q_linear_channelwise, minus
- * the scratch buffers xq and xs: the E4M3 codes and per-token scales live
+ * the scratch buffers xq and xs and the workspace (K splits exchange their
+ * partial sums in distributed shared memory): the E4M3 codes and per-token scales live
  * in a fixed array inside the library (a file-scope __device__ array of
  * FP8Q_NOALLOC_MAX_CODES + 4 * FP8Q_NOALLOC_MAX_ROWS bytes = 16 MiB + 64 KiB,
  * held on every GPU that loads the library until the process exits).
@@ -314,7 +349,12 @@ FP8Q_API fp8q_status fp8q_linear_blockwise_fused(const void *x, int64_t ldx, con
  * Set-up  : the first call on each device looks up the array's device
  *           address (cudaGetSymbolAddress, with that device current) and
  *           caches it; make that first call before any stream capture.
- *           A failed look-up returns FP8Q_ERR_CUDA.
+ *           A failed look-up returns FP8Q_ERR_CUDA.  The device is the
+ *           CURRENT device: make the device of x, out and stream current
+ *           before the call.  The cached address belongs to the device's
+ *           primary context; after cudaDeviceReset on that device it is no
+ *           longer valid, so do not call this entry point in a process that
+ *           has reset the device after its first call.
  * Sharing : every call on a device uses the same array, which keeps the
  *           last call's contents (nothing in it needs to start at zero:
  *           the quantizer writes every code and scale the GEMM reads).
@@ -333,7 +373,8 @@ FP8Q_API fp8q_status fp8q_linear_channelwise_noalloc(const void *x, const void *
  * Tile selection (host only, no GPU needed).  The GEMM schedule for a
  * problem: which operand sits on the MMA's 128-row side, the MMA N extent,
  * the K-split count (CTAs of one thread-block cluster that share a tile and
- * reduce their partial sums in distributed shared memory), pipeline depth
+ * add up their partial sums through the workspace or distributed shared
+ * memory), pipeline depth
  * and grid size.  The choice comes from a compiled-in table keyed by
  * (N, K, scheme) with nearest-M lookup, ties to the smaller M, as in
  * get_w8a8_channelwise_fp8_config of [PR34331] "Key source snippets";
@@ -353,12 +394,12 @@ typedef struct {
     int32_t persistent; /* 1: CTAs loop over several tiles */
     int32_t from_table; /* 1: taken from the compiled-in table */
     int32_t pair;       /* 1: CTA pairs (2-CTA clusters) on adjacent token tiles
-                           share each weight slice by multicast (non-swapped,
-                           split_k 1, at least two token tiles) */
+                           (non-swapped channelwise, split_k 1, at least two
+                           token tiles) */
     int32_t two_sm;     /* 1: each CTA pair computes a 256-token x 256-column
                            tile with 2-CTA MMAs (tcgen05 cta_group::2), each
-                           CTA staging only its half of the weights
-                           (channelwise pairs) */
+                           CTA loading only its half of the weight rows
+                           (always equal to pair) */
 } fp8q_plan;
 
 FP8Q_API fp8q_status fp8q_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t blockwise, int32_t num_sms,

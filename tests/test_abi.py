@@ -54,7 +54,7 @@ def test_status_strings_and_version(lib):
     assert fq.status_str(0) == "FP8Q_OK"
     assert fq.status_str(4) == "FP8Q_ERR_TIMEOUT"
     assert fq.status_str(99) == "FP8Q_UNKNOWN_STATUS"
-    assert fq.fp8q_version() >> 16 == 1
+    assert fq.fp8q_version() >> 16 == 2
 
 
 def test_invalid_arguments_are_rejected_before_any_cuda_call(lib):
@@ -80,27 +80,36 @@ def test_invalid_arguments_are_rejected_before_any_cuda_call(lib):
     assert lib.fp8q_quant_per_token_group_row_padded(fake, 4, 192, 192, 128, 1e-10, 4, fake, fake, 4,
                                                      None) == fq.FP8Q_ERR_INVALID_ARG
     # blockwise needs N, K multiples of 128 (the reference falls back; we refuse)
-    assert lib.fp8q_scaled_mm_blockwise(fake, fake, fake, fake, None, fake, 4, 4, 200, 256, 0,
+    assert lib.fp8q_scaled_mm_blockwise(fake, fake, fake, fake, None, fake, 4, 4, 200, 256, 0, None, 0,
                                         None) == fq.FP8Q_ERR_UNSUPPORTED
-    assert lib.fp8q_scaled_mm_blockwise(fake, fake, fake, fake, None, fake, 4, 4, 256, 200, 0,
+    assert lib.fp8q_scaled_mm_blockwise(fake, fake, fake, fake, None, fake, 4, 4, 256, 200, 0, None, 0,
                                         None) == fq.FP8Q_ERR_UNSUPPORTED
-    assert lib.fp8q_scaled_mm_blockwise(fake, fake, fake, fake, None, fake, 5, 6, 256, 256, 0,
+    assert lib.fp8q_scaled_mm_blockwise(fake, fake, fake, fake, None, fake, 5, 6, 256, 256, 0, None, 0,
                                         None) == fq.FP8Q_ERR_INVALID_ARG
     # channelwise: K % 16, ldb < K, N % 8, unknown output type, misaligned pointer
-    assert lib.fp8q_scaled_mm_channelwise(fake, fake, 40, fake, fake, None, fake, 4, 64, 40, 0,
+    assert lib.fp8q_scaled_mm_channelwise(fake, fake, 40, fake, fake, None, fake, 4, 64, 40, 0, None, 0,
                                           None) == fq.FP8Q_ERR_INVALID_ARG
-    assert lib.fp8q_scaled_mm_channelwise(fake, fake, 32, fake, fake, None, fake, 4, 64, 64, 0,
+    assert lib.fp8q_scaled_mm_channelwise(fake, fake, 32, fake, fake, None, fake, 4, 64, 64, 0, None, 0,
                                           None) == fq.FP8Q_ERR_INVALID_ARG
-    assert lib.fp8q_scaled_mm_channelwise(fake, fake, 64, fake, fake, None, fake, 4, 60, 64, 0,
+    assert lib.fp8q_scaled_mm_channelwise(fake, fake, 64, fake, fake, None, fake, 4, 60, 64, 0, None, 0,
                                           None) == fq.FP8Q_ERR_INVALID_ARG
-    assert lib.fp8q_scaled_mm_channelwise(fake, fake, 64, fake, fake, None, fake, 4, 64, 64, 7,
+    assert lib.fp8q_scaled_mm_channelwise(fake, fake, 64, fake, fake, None, fake, 4, 64, 64, 7, None, 0,
                                           None) == fq.FP8Q_ERR_UNSUPPORTED
-    assert lib.fp8q_scaled_mm_channelwise(P(0x1008), fake, 64, fake, fake, None, fake, 4, 64, 64, 0,
+    assert lib.fp8q_scaled_mm_channelwise(P(0x1008), fake, 64, fake, fake, None, fake, 4, 64, 64, 0, None, 0,
                                           None) == fq.FP8Q_ERR_INVALID_ARG
     # null pointers
-    assert lib.fp8q_scaled_mm_channelwise(None, fake, 64, fake, fake, None, fake, 4, 64, 64, 0,
+    assert lib.fp8q_scaled_mm_channelwise(None, fake, 64, fake, fake, None, fake, 4, 64, 64, 0, None, 0,
                                           None) == fq.FP8Q_ERR_INVALID_ARG
-    assert lib.fp8q_scaled_mm_channelwise(None, None, 64, None, None, None, None, 0, 64, 64, 0, None) == fq.FP8Q_OK
+    assert lib.fp8q_scaled_mm_channelwise(None, None, 64, None, None, None, None, 0, 64, 64, 0, None, 0,
+                                          None) == fq.FP8Q_OK
+    # a workspace that is not 16-byte aligned
+    assert lib.fp8q_scaled_mm_channelwise(fake, fake, 64, fake, fake, None, fake, 4, 64, 64, 0, P(0x1004), 4096,
+                                          None) == fq.FP8Q_ERR_INVALID_ARG
+    assert lib.fp8q_scaled_mm_blockwise(fake, fake, fake, fake, None, fake, 4, 4, 256, 256, 0, P(0x1008), 4096,
+                                        None) == fq.FP8Q_ERR_INVALID_ARG
+    # invalid sizes need no workspace
+    for M, N, K in ((0, 64, 64), (-1, 64, 64), (4, 0, 64), (4, 64, 0)):
+        assert lib.fp8q_workspace_bytes(M, N, K, 0) == 0
 
 
 def test_plan_override_validation(lib):
@@ -138,13 +147,13 @@ def test_variant_entry_points_reject_invalid_arguments_before_any_cuda_call(lib)
     assert wb(fake, 200, 256, fake, fake, 1e-10, None) == U                          # N % 128
     assert wb(fake, 256, 256, fake, fake, 0.0, None) == E                            # eps
     lc = lib.fp8q_linear_channelwise
-    assert lc(fake, fake, 64, fake, None, fake, 4, 64, 64, fake, fake, 7, None) == U  # output type
-    assert lc(fake, fake, 64, fake, None, fake, 4, 60, 64, fake, fake, 0, None) == E  # N % 8
-    assert lc(None, None, 64, None, None, None, 0, 64, 64, None, None, 0, None) == fq.FP8Q_OK
+    assert lc(fake, fake, 64, fake, None, fake, 4, 64, 64, fake, fake, 7, None, 0, None) == U  # output type
+    assert lc(fake, fake, 64, fake, None, fake, 4, 60, 64, fake, fake, 0, None, 0, None) == E  # N % 8
+    assert lc(None, None, 64, None, None, None, 0, 64, 64, None, None, 0, None, 0, None) == fq.FP8Q_OK
     lb = lib.fp8q_linear_blockwise
-    assert lb(fake, fake, fake, None, fake, 4, 200, 256, fake, fake, 4, 0, None) == U  # N % 128
-    assert lb(fake, fake, fake, None, fake, 5, 256, 256, fake, fake, 6, 0, None) == E  # m_pad % 4
-    assert lb(fake, fake, fake, odd, fake, 4, 256, 256, fake, fake, 4, 0, None) == E   # odd bias address
+    assert lb(fake, fake, fake, None, fake, 4, 200, 256, fake, fake, 4, 0, None, 0, None) == U  # N % 128
+    assert lb(fake, fake, fake, None, fake, 5, 256, 256, fake, fake, 6, 0, None, 0, None) == E  # m_pad % 4
+    assert lb(fake, fake, fake, odd, fake, 4, 256, 256, fake, fake, 4, 0, None, 0, None) == E   # odd bias address
     fu = lib.fp8q_linear_blockwise_fused
     assert fu(fake, 256, fake, fake, None, fake, 4, 200, 256, 0, None) == U           # N % 128
     assert fu(fake, 128, fake, fake, None, fake, 4, 256, 256, 0, None) == E           # ldx < K

@@ -44,7 +44,8 @@ def test_plans_are_launchable(num_sms):
         num_kb = -(-K // 128)
         assert 1 <= p["split_k"] <= min(8, num_kb)
         m_tiles = -(-M // p["tile_m"])
-        assert p["pair"] == int(not p["swap_ab"] and p["split_k"] == 1 and m_tiles >= 2)
+        # channelwise 256-column tiles pair up (blockwise tiles never do)
+        assert p["pair"] == int(not bw and not p["swap_ab"] and p["split_k"] == 1 and m_tiles >= 2)
         if p["pair"]:
             # 2-CTA clusters over pairs of token tiles (an odd last tile pairs
             # with an empty one), at most one pair per two SMs
@@ -58,7 +59,7 @@ def test_plans_are_launchable(num_sms):
             assert p["persistent"] == int(tiles > num_sms)
         # channelwise pairs of 128 x 256 tiles use 2-CTA MMAs: each CTA stages
         # 128 token rows and its 128 of the 256 weight rows per K slice
-        assert p["two_sm"] == int(p["pair"] and not bw and p["mma_n"] == 256)
+        assert p["two_sm"] == p["pair"]
         per_stage = 2 * 128 * 128 if p["two_sm"] else stage_bytes(p["swap_ab"], p["mma_n"], bw)
         assert p["stages"] * per_stage + 4096 <= SMEM_LIMIT
 

@@ -6,9 +6,12 @@ caller buffers.
 
 The GPU test calls it through the C ABI twice in a row, on different shapes
 (the second smaller, so the array still holds the first call's larger
-contents), and compares each result with fp8q_linear_channelwise run on
-caller-allocated buffers, within the GEMM tolerance of the parity tests.
-This file is named to be collected last."""
+contents; the second on a stream other than the current one), and compares
+each result with fp8q_linear_channelwise run on caller-allocated buffers
+without a workspace.  Both run the same kernels on the same schedule with
+the same split-K exchange, so the outputs must be identical bit for bit;
+the oracle's GEMM tolerance is checked as well.  This file is named to be
+collected last."""
 import ctypes
 
 import pytest
@@ -48,17 +51,30 @@ def test_noalloc_linear_matches_the_allocating_entry_point_on_two_calls():
     torch.cuda.set_device(dev)
     fq.fp8q_set_plan_override(-1)
     lib = fq.load_library()
-    stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    side = torch.cuda.Stream(dev)
     for call, (M, N, K, bias) in enumerate([(300, 512, 4096, True), (7, 384, 1024, False)]):
         x, wq, ws, b = _layer(dev, M, N, K, seed=60 + call, bias=bias)
         out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=dev)
+        # the second call on a stream that is not the current one
+        s = torch.cuda.current_stream(dev) if call == 0 else side
+        s.wait_stream(torch.cuda.current_stream(dev))
         st = lib.fp8q_linear_channelwise_noalloc(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(wq.data_ptr()),
                                                  K, ctypes.c_void_p(ws.data_ptr()),
                                                  None if b is None else ctypes.c_void_p(b.data_ptr()),
                                                  ctypes.c_void_p(out.data_ptr()), M, N, K, fq.FP8Q_OUT_BF16,
-                                                 stream)
+                                                 ctypes.c_void_p(s.cuda_stream))
         assert st == fq.FP8Q_OK, fq.status_str(st)
-        ref = fq.fp8q_linear_channelwise(x, wq, ws, bias=b)
+        s.synchronize()
+        ref = fq.fp8q_linear_channelwise(x, wq, ws, bias=b, workspace=None)
         torch.cuda.synchronize()
-        assert_gemm_close(out_values(out), out_values(ref), f"no-alloc call {call + 1} ({M}x{N}x{K})")
+        assert torch.equal(out, ref), f"no-alloc call {call + 1} ({M}x{N}x{K}) differs from the allocating call"
+        assert_gemm_close(out_values(out), oracle_linear(x, wq, ws, b), f"no-alloc call {call + 1} ({M}x{N}x{K})")
     assert fq.fp8q_device_status() == fq.FP8Q_OK
+
+
+def oracle_linear(x, wq, ws, b):
+    import oracle
+    from gpu_util import THREADS, ref_values, u8
+    rq, rs = oracle.quant_per_token(x.cpu(), threads=THREADS)
+    return ref_values(oracle.gemm_channelwise(rq, u8(wq), rs, ws.cpu().numpy(), bias=None if b is None else b.cpu(),
+                                              threads=THREADS))
