@@ -351,7 +351,14 @@ def fp8q_scaled_mm_blockwise(a: torch.Tensor, w: torch.Tensor, a_scale: torch.Te
     m_pad, K = a.shape
     N = w.shape[0]
     M = m_pad if M is None else int(M)
-    storage = a_scale.transpose(0, 1) if a_scale.shape == (m_pad, K // 128) else a_scale
+    # The (m_pad, K/128) column-major view (stride(0) == 1) or its [K/128,
+    # m_pad] contiguous storage; decided by the strides, since the two have
+    # the same shape when K/128 == m_pad.
+    if a_scale.dim() == 2 and tuple(a_scale.shape) == (m_pad, K // 128) and a_scale.stride(0) == 1 \
+            and (a_scale.stride(1) == m_pad or K // 128 == 1):
+        storage = a_scale.transpose(0, 1)
+    else:
+        storage = a_scale
     if tuple(storage.shape) != (K // 128, m_pad) or not storage.is_contiguous():
         raise ValueError("a_scale must be the column-major (m_pad, K/128) scales of the row-padded quantizer")
     if not a.is_contiguous() or not w.is_contiguous() or not w_scale.is_contiguous():

@@ -190,6 +190,14 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32
                  : "memory");
 }
 
+// Drop the 128-byte L2 line at `p` (128-byte aligned) without writing it
+// back: its contents become undefined.  For scratch data that no one will
+// read again.
+__device__ __forceinline__ void discard_l2_line(const void *p)
+{
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch: a kernel launched with the programmatic
 // stream-serialization attribute may start while the previous kernel in the

@@ -344,9 +344,14 @@ __device__ __forceinline__ void store_box_tma(const CUtensorMap *tm_out, uint8_t
 // (r, c4) with c4 fastest (consecutive threads, consecutive output
 // columns of one token); swapped (c4, r) with r fastest (consecutive
 // threads, consecutive output columns n0 + r).  Rank q owns the items
-// [items * q / split, items * (q + 1) / split).  A slot holds one rank's
-// partial in item order (float4 per item), so the copy into the slot and
-// the owner's reads are both contiguous.
+// [b(q), b(q + 1)), b(q) = items * q / split rounded down to a multiple of
+// 8 (one 128-byte line of float4 items; b(split) = items).  A slot holds
+// one rank's partial in item order, so the copy into the slot and the
+// owner's reads are both contiguous, and every line of a slot is read by
+// exactly one CTA: the owner discards each whole line it has read from L2
+// (its contents are dead), so the slots are never written back to HBM.
+// The owner issues the loads of kBatch items per thread from every slot
+// before adding any of them, so L2 latency is paid once per batch.
 template <typename C, typename OutT, bool BLOCKWISE, bool SWAP, typename Coords>
 __device__ __forceinline__ void reduce_split_workspace(const GemmArgs &p, const float *sRed, const float *sColScale,
                                                        int rank, int cluster_id, int warp, volatile int *abort,
@@ -355,10 +360,13 @@ __device__ __forceinline__ void reduce_split_workspace(const GemmArgs &p, const 
     constexpr int SP = C::kPartStride;
     constexpr int BN = C::kPartStride - 4;   // columns of the partial tile (the MMA N extent)
     constexpr int G = BN / 4;
-    constexpr long long kSlotFloats = 128LL * BN;
+    constexpr long long kSlotItems = 128LL * BN / 4;
+    constexpr int kMaxSplit = 8;
+    constexpr int kBatch = 2;
     const int split = p.split;
     const bool epi = warp >= C::kEpiWarp0 && warp < C::kEpiWarp0 + C::kEpiWarps;
     const int etid = threadIdx.x - 32 * C::kEpiWarp0;
+    const int lane = threadIdx.x & 31;
     int a_t, b_t;
     coords(cluster_id, a_t, b_t);
     const int m0 = (SWAP ? b_t : a_t) * C::kTokTile;
@@ -370,15 +378,17 @@ __device__ __forceinline__ void reduce_split_workspace(const GemmArgs &p, const 
         if (SWAP) { c4 = item / rows; r = item - c4 * rows; }
         else { r = item / G; c4 = item - r * G; }
     };
-    const int i_lo = static_cast<int>(static_cast<long long>(items) * rank / split);
-    const int i_hi = static_cast<int>(static_cast<long long>(items) * (rank + 1) / split);
-    float4 *slots = reinterpret_cast<float4 *>(p.ws + static_cast<long long>(cluster_id) * split * kSlotFloats);
+    auto bound = [&](int q) {
+        return q >= split ? items : static_cast<int>(static_cast<long long>(items) * q / split) & ~7;
+    };
+    const int i_lo = bound(rank), i_hi = bound(rank + 1);
+    float4 *slots = reinterpret_cast<float4 *>(p.ws) + static_cast<long long>(cluster_id) * split * kSlotItems;
     if (epi) {
         // The whole partial tile is in shared memory.
         named_barrier_sync(1, C::kEpiThreads);
         if (!*abort) {
             // The items other ranks own, into this rank's slot.
-            float4 *mine = slots + static_cast<long long>(rank) * (kSlotFloats / 4);
+            float4 *mine = slots + static_cast<long long>(rank) * kSlotItems;
             for (int item = etid; item < items; item += C::kEpiThreads) {
                 if (item >= i_lo && item < i_hi) continue;
                 int r, c4;
@@ -386,58 +396,100 @@ __device__ __forceinline__ void reduce_split_workspace(const GemmArgs &p, const 
                 __stcg(mine + item, *reinterpret_cast<const float4 *>(sRed + r * SP + 4 * c4));
             }
         }
-        __threadfence();
     }
-    // Publishes every rank's slot to the cluster (release / acquire).
+    // Publishes every rank's slot to the cluster (release / acquire at
+    // cluster scope orders the global stores above before the loads below).
     cluster_sync();
+    if (threadIdx.x == 32 * C::kEpiWarp0) FP8Q_TRACE_AT(p, kTrCluster1);
     if (!epi || *abort) return;
     OutT *out = static_cast<OutT *>(p.out);
-    for (int item = i_lo + etid; item < i_hi; item += C::kEpiThreads) {
-        int r, c4;
-        item_rc(item, r, c4);
-        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int q = 0; q < split; ++q) {
-            const float4 v = q == rank ? *reinterpret_cast<const float4 *>(sRed + r * SP + 4 * c4)
-                                       : __ldcg(slots + static_cast<long long>(q) * (kSlotFloats / 4) + item);
-            sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
-        }
-        const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
-        if (SWAP) {
-            // Output column n0 + r; tokens m0 + 4 c4 .. + 3 (scales staged
-            // in sColScale by the epilogue).
-            const int n = n0 + r;
-            const float wsc = BLOCKWISE ? 1.0f : __ldg(p.w_scale + n);
-            const float bv = p.bias != nullptr ? __bfloat162float(p.bias[n]) : 0.0f;
+    // Lines may be discarded only if the workspace is 128-byte aligned.
+    const bool may_discard = (reinterpret_cast<uintptr_t>(p.ws) & 127u) == 0;
+    // The loop runs per warp (wbase is the same for all its lanes: the line
+    // discards below synchronise the warp); items past i_hi are skipped.
+    for (int wbase = i_lo + (etid - lane); wbase < i_hi; wbase += kBatch * C::kEpiThreads) {
+        const int base = wbase + lane;
+        float4 v[kMaxSplit][kBatch];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int m = m0 + c4 * 4 + e;
-                if (m < p.M) {
-                    const float y = BLOCKWISE ? sv[e] + bv : fmaf(sv[e] * wsc, sColScale[c4 * 4 + e], bv);
-                    out[static_cast<long long>(m) * p.ldo + n] = to_out<OutT>(y);
+        for (int q = 0; q < kMaxSplit; ++q) {
+            if (q >= split) break;
+#pragma unroll
+            for (int bt = 0; bt < kBatch; ++bt) {
+                const int item = base + bt * C::kEpiThreads;
+                if (item >= i_hi) continue;
+                if (q == rank) {
+                    int r, c4;
+                    item_rc(item, r, c4);
+                    v[q][bt] = *reinterpret_cast<const float4 *>(sRed + r * SP + 4 * c4);
+                } else {
+                    v[q][bt] = __ldcg(slots + static_cast<long long>(q) * kSlotItems + item);
                 }
             }
-        } else {
-            // Token m0 + r; output columns n0 + 4 c4 .. + 3.
-            const int m = m0 + r, n = n0 + 4 * c4;
-            if (n >= p.N) continue;
-            const float am = BLOCKWISE ? 1.0f : __ldg(p.a_scale + m);
-            float y[4];
+        }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const bool in = n + e < p.N;
-                const float bv = (p.bias != nullptr && in) ? __bfloat162float(p.bias[n + e]) : 0.0f;
-                y[e] = BLOCKWISE ? sv[e] + bv : fmaf(sv[e] * am, in ? __ldg(p.w_scale + n + e) : 0.0f, bv);
+        for (int bt = 0; bt < kBatch; ++bt) {
+            const int item = base + bt * C::kEpiThreads;
+            if (item >= i_hi) continue;
+            float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < kMaxSplit; ++q) {
+                if (q >= split) break;
+                sum.x += v[q][bt].x; sum.y += v[q][bt].y; sum.z += v[q][bt].z; sum.w += v[q][bt].w;
             }
-            OutT *o = out + static_cast<long long>(m) * p.ldo + n;
-            if (n + 4 <= p.N) {
-                *reinterpret_cast<uint2 *>(o) = make_uint2(pack_out2<OutT>(y[0], y[1]), pack_out2<OutT>(y[2], y[3]));
-            } else {
+            int r, c4;
+            item_rc(item, r, c4);
+            const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+            if (SWAP) {
+                // Output column n0 + r; tokens m0 + 4 c4 .. + 3 (scales
+                // staged in sColScale by the epilogue).
+                const int n = n0 + r;
+                const float wsc = BLOCKWISE ? 1.0f : __ldg(p.w_scale + n);
+                const float bv = p.bias != nullptr ? __bfloat162float(p.bias[n]) : 0.0f;
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (n + e < p.N) o[e] = to_out<OutT>(y[e]);
+                for (int e = 0; e < 4; ++e) {
+                    const int m = m0 + c4 * 4 + e;
+                    if (m < p.M) {
+                        const float y = BLOCKWISE ? sv[e] + bv : fmaf(sv[e] * wsc, sColScale[c4 * 4 + e], bv);
+                        out[static_cast<long long>(m) * p.ldo + n] = to_out<OutT>(y);
+                    }
+                }
+            } else {
+                // Token m0 + r; output columns n0 + 4 c4 .. + 3.
+                const int m = m0 + r, n = n0 + 4 * c4;
+                if (n < p.N) {
+                    const float am = BLOCKWISE ? 1.0f : __ldg(p.a_scale + m);
+                    float y[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const bool in = n + e < p.N;
+                        const float bv = (p.bias != nullptr && in) ? __bfloat162float(p.bias[n + e]) : 0.0f;
+                        y[e] = BLOCKWISE ? sv[e] + bv : fmaf(sv[e] * am, in ? __ldg(p.w_scale + n + e) : 0.0f, bv);
+                    }
+                    OutT *o = out + static_cast<long long>(m) * p.ldo + n;
+                    if (n + 4 <= p.N) {
+                        *reinterpret_cast<uint2 *>(o) = make_uint2(pack_out2<OutT>(y[0], y[1]), pack_out2<OutT>(y[2], y[3]));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (n + e < p.N) o[e] = to_out<OutT>(y[e]);
+                    }
+                }
+            }
+        }
+        // Every line whose 8 items this warp has now read (all lanes: the
+        // values were used above) is dead in every other rank's slot.
+        __syncwarp();
+        if (may_discard) {
+#pragma unroll
+            for (int bt = 0; bt < kBatch; ++bt) {
+                const int item = base + bt * C::kEpiThreads;
+                if ((item & 7) != 0 || item + 8 > i_hi) continue;
+                for (int q = 0; q < split; ++q)
+                    if (q != rank) discard_l2_line(slots + static_cast<long long>(q) * kSlotItems + item);
             }
         }
     }
+    if (threadIdx.x == 32 * C::kEpiWarp0) FP8Q_TRACE_AT(p, kTrReduced);
 }
 
 template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT, bool TWO_SM = false, bool FQ = false,

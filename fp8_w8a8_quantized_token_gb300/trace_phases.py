@@ -7,7 +7,9 @@ Builds ``libfp8q_trace.so`` (the library with the GEMM's per-CTA
 quantization + the channelwise GEMM three times as warm-up, then once more
 after clearing the trace buffer, and prints for every phase the minimum,
 median and maximum time (microseconds after the earliest CTA entry) over
-the launch's CTAs.  Inputs are the seeded synthetic tensors.  Needs a GPU.
+the launch's CTAs.  Schedules that split K are traced twice: with the
+split-K workspace and without it (partials exchanged in distributed shared
+memory).  Inputs are the seeded synthetic tensors.  Needs a GPU.
 """
 from __future__ import annotations
 
@@ -34,18 +36,18 @@ PHASES = ["entry", "prologue done", "dependency wait passed", "first TMA issued"
 SLOTS_PER_CTA = 16
 
 
-def trace_launch(L, dev, M: int, N: int, K: int):
+def trace_launch(L, dev, M: int, N: int, K: int, workspace="auto"):
     x = synthetic.activations(M, K, outliers=True).to(dev)
     wq, ws = fq.fp8q_quant_per_token(synthetic.weights(N, K).to(dev))
     plan = fq.fp8q_gemm_plan(M, N, K)
     for _ in range(3):
         xq, xs = fq.fp8q_quant_per_token(x)
-        fq.fp8q_scaled_mm_channelwise(xq, wq, xs, ws)
+        fq.fp8q_scaled_mm_channelwise(xq, wq, xs, ws, workspace=workspace)
     torch.cuda.synchronize()
     if L.fp8q_trace_clear() != 0:
         raise RuntimeError("fp8q_trace_clear failed")
     xq, xs = fq.fp8q_quant_per_token(x)
-    fq.fp8q_scaled_mm_channelwise(xq, wq, xs, ws)
+    fq.fp8q_scaled_mm_channelwise(xq, wq, xs, ws, workspace=workspace)
     torch.cuda.synchronize()
     buf = (ctypes.c_ulonglong * (4096 * SLOTS_PER_CTA))()
     if L.fp8q_trace_read(ctypes.addressof(buf), 4096 * SLOTS_PER_CTA) != 0:
@@ -64,18 +66,26 @@ def main(argv) -> int:
     torch.cuda.set_device(dev)
     for spec in argv:
         M, N, K = (int(v) for v in spec.split("x"))
-        plan, t = trace_launch(L, dev, M, N, K)
-        t0 = t[:, 0].min()
-        print(f"== M={M} N={N} K={K} plan={plan}")
-        for i, name in enumerate(PHASES):
-            col = t[:, i]
-            hit = col > 0
-            if not hit.any():
-                continue
-            rel = (col[hit] - t0) / 1000.0
-            print(f"  {name:>38}: min {rel.min():7.2f}  median {np.median(rel):7.2f}  max {rel.max():7.2f} us"
-                  f"  ({int(hit.sum())} CTAs)")
+        split = fq.fp8q_gemm_plan(M, N, K)["split_k"] > 1
+        for workspace in (("auto", None) if split else ("auto",)):
+            trace_one(L, dev, M, N, K, workspace)
     return 0
+
+
+def trace_one(L, dev, M, N, K, workspace):
+    plan, t = trace_launch(L, dev, M, N, K, workspace)
+    t0 = t[:, 0].min()
+    exchange = "" if plan["split_k"] == 1 else (" (split-K workspace)" if workspace else
+                                                " (split-K exchange in distributed shared memory)")
+    print(f"== M={M} N={N} K={K} plan={plan}{exchange}")
+    for i, name in enumerate(PHASES):
+        col = t[:, i]
+        hit = col > 0
+        if not hit.any():
+            continue
+        rel = (col[hit] - t0) / 1000.0
+        print(f"  {name:>38}: min {rel.min():7.2f}  median {np.median(rel):7.2f}  max {rel.max():7.2f} us"
+              f"  ({int(hit.sum())} CTAs)")
 
 
 if __name__ == "__main__":
