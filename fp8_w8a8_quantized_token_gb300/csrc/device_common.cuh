@@ -190,6 +190,34 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32
                  : "memory");
 }
 
+// Bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned)
+// from this CTA's shared memory to global memory, in the issuing thread's
+// bulk async-group.
+__device__ __forceinline__ void bulk_store_global(void *dst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned)
+// from global memory into this CTA's shared memory; completion is signalled
+// to the mbarrier `bar` (complete_tx).
+__device__ __forceinline__ void bulk_load_global(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Order this thread's async-proxy (bulk copy) accesses to global memory
+// with its generic-proxy accesses (both directions).
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Drop the 128-byte L2 line at `p` (128-byte aligned) without writing it
 // back: its contents become undefined.  For scratch data that no one will
 // read again.

@@ -199,8 +199,18 @@ struct GemmCfg {
     static constexpr uint32_t kOffX = (kOffRecv + kRecvBytes + 127u) / 128u * 128u;
     static constexpr uint32_t kOffL = (kOffX + kXStages * kXBytes + 1023u) / 1024u * 1024u;  // W16 landing ring
     static constexpr uint32_t kOffBar = kOffL + kLStages * kLSlotBytes;
-    // full, empty, tfull[2], tempty[2], drain, recv (+ W16: lfull, lempty[kLStages])
-    static constexpr uint32_t kNumBars = 2 * STAGES + 6 + 2 * kLStages;
+    // Split-K exchange through the global workspace: only for partial tiles
+    // of 64 KB and more (non-swapped 256-column tiles, swapped 128-token
+    // tiles); smaller ones exchange faster in distributed shared memory.
+    // The owner's remote partial rows land (bulk copies, padded rows) in the
+    // idle ring after the partial tile, double-buffered in chunks, each chunk
+    // completing on its own single-use barrier.
+    static constexpr bool kWsExchange = !FQ && !W16 && (!SWAP || BN >= 128);
+    static constexpr int kWsBars = 8;
+    static constexpr uint32_t kOffLand = (128u * kPartStride * 4u + 127u) / 128u * 128u;
+    static constexpr uint32_t kLandBytes = kOffX > kOffLand ? kOffX - kOffLand : 0u;
+    // full, empty, tfull[2], tempty[2], drain, recv (+ W16: lfull, lempty[kLStages]), workspace chunks
+    static constexpr uint32_t kNumBars = 2 * STAGES + 6 + 2 * kLStages + kWsBars;
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr uint32_t kOffCol = (kOffMisc + 16 + 15) / 16 * 16;  // staged column scale, bias
     // Non-swapped tiles store their output through one 2 KB staging buffer
@@ -337,156 +347,160 @@ __device__ __forceinline__ void store_box_tma(const CUtensorMap *tm_out, uint8_t
 
 // Split-K reduction through the global workspace (every thread of the CTA
 // calls it; the cluster barrier inside needs all of them).  The partial
-// tile of this CTA is in sRed, row r (TMEM lane: a token of a non-swapped
-// tile, an output column of a swapped one) at sRed[r * kPartStride], its
-// BN columns contiguous.  Items are 4-column groups of the tile's valid
-// rows, numbered in the order the owner stores its outputs: non-swapped
-// (r, c4) with c4 fastest (consecutive threads, consecutive output
-// columns of one token); swapped (c4, r) with r fastest (consecutive
-// threads, consecutive output columns n0 + r).  Rank q owns the items
-// [b(q), b(q + 1)), b(q) = items * q / split rounded down to a multiple of
-// 8 (one 128-byte line of float4 items; b(split) = items).  A slot holds
-// one rank's partial in item order, so the copy into the slot and the
-// owner's reads are both contiguous, and every line of a slot is read by
-// exactly one CTA: the owner discards each whole line it has read from L2
-// (its contents are dead), so the slots are never written back to HBM.
-// The owner issues the loads of kBatch items per thread from every slot
-// before adding any of them, so L2 latency is paid once per batch.
-template <typename C, typename OutT, bool BLOCKWISE, bool SWAP, typename Coords>
-__device__ __forceinline__ void reduce_split_workspace(const GemmArgs &p, const float *sRed, const float *sColScale,
-                                                       int rank, int cluster_id, int warp, volatile int *abort,
-                                                       Coords coords)
+// tile of this CTA is in shared memory, row r (TMEM lane: a token of a
+// non-swapped tile, an output column of a swapped one) at r * kPartStride
+// floats, its BN columns contiguous.  Rank q of the cluster owns the rows
+// [rows * q / split, rows * (q + 1) / split) of the tile's valid rows.
+//   1. Every rank writes the rows it does not own into its own slot of the
+//      workspace (one slot of 128 x BN floats, rows dense), one bulk copy
+//      per row, and waits for the copies to complete.
+//   2. A cluster barrier publishes the slots.
+//   3. The owner bulk-loads its rows from every other rank's slot, in
+//      chunks of rows, double-buffered in the idle ring after its partial
+//      tile (padded rows, so both item orders read shared memory without
+//      bank conflicts), adds each item over the ranks in rank order and
+//      stores the outputs; the slot lines it has loaded are dead and are
+//      discarded from L2 (never written back to HBM).
+// Items are 4-column groups, numbered in the order the owner stores its
+// outputs: non-swapped (r, c4) with c4 fastest (consecutive threads,
+// consecutive output columns of one token), swapped (c4, r) with r fastest
+// (consecutive threads, consecutive output columns n0 + r).
+// Called once per CTA and kept out of line: its registers do not add to
+// the main loop's.
+template <typename C, typename OutT, bool BLOCKWISE, bool SWAP>
+__device__ __noinline__ void reduce_split_workspace(const GemmArgs &p, uint8_t *smem, const float *sColScale,
+                                                    uint64_t *ws_bar, int rank, int cluster_id, int warp,
+                                                    volatile int *abort, int m0, int n0)
 {
     constexpr int SP = C::kPartStride;
     constexpr int BN = C::kPartStride - 4;   // columns of the partial tile (the MMA N extent)
     constexpr int G = BN / 4;
-    constexpr long long kSlotItems = 128LL * BN / 4;
-    constexpr int kMaxSplit = 8;
-    constexpr int kBatch = 2;
+    constexpr uint32_t kRowBytes = BN * 4u;
+    constexpr long long kSlotFloats = 128LL * BN;
+    const float *sRed = reinterpret_cast<const float *>(smem);
+    float *land = reinterpret_cast<float *>(smem + C::kOffLand);
     const int split = p.split;
     const bool epi = warp >= C::kEpiWarp0 && warp < C::kEpiWarp0 + C::kEpiWarps;
+    const bool lead_warp = warp == C::kEpiWarp0;   // issues the bulk copies
     const int etid = threadIdx.x - 32 * C::kEpiWarp0;
     const int lane = threadIdx.x & 31;
-    int a_t, b_t;
-    coords(cluster_id, a_t, b_t);
-    const int m0 = (SWAP ? b_t : a_t) * C::kTokTile;
-    const int n0 = (SWAP ? a_t : b_t) * C::kColTile;
-    // Valid rows of the partial tile.
+    // Valid rows of the partial tile and this rank's share of them.
     const int rows = SWAP ? min(128, p.N - n0) : min(128, p.M - m0);
-    const int items = rows * G;
-    auto item_rc = [&](int item, int &r, int &c4) {
-        if (SWAP) { c4 = item / rows; r = item - c4 * rows; }
-        else { r = item / G; c4 = item - r * G; }
-    };
-    auto bound = [&](int q) {
-        return q >= split ? items : static_cast<int>(static_cast<long long>(items) * q / split) & ~7;
-    };
-    const int i_lo = bound(rank), i_hi = bound(rank + 1);
-    float4 *slots = reinterpret_cast<float4 *>(p.ws) + static_cast<long long>(cluster_id) * split * kSlotItems;
+    const int lo = rows * rank / split, hi = rows * (rank + 1) / split;
+    // Chunk rows: two buffers of (split - 1) x cr padded rows fit the
+    // landing area (the host checks that the chunks fit kWsBars barriers).
+    const int cr = static_cast<int>(C::kLandBytes / (2u * static_cast<uint32_t>(split - 1) * SP * 4u));
+    const int nchunks = hi > lo ? (hi - lo + cr - 1) / cr : 0;
+    float *slots = p.ws + static_cast<long long>(cluster_id) * split * kSlotFloats;
     if (epi) {
-        // The whole partial tile is in shared memory.
+        // This thread's partial-tile writes, before the bulk copies read them.
+        fence_proxy_async_smem();
         named_barrier_sync(1, C::kEpiThreads);
-        if (!*abort) {
-            // The items other ranks own, into this rank's slot.
-            float4 *mine = slots + static_cast<long long>(rank) * kSlotItems;
-            for (int item = etid; item < items; item += C::kEpiThreads) {
-                if (item >= i_lo && item < i_hi) continue;
-                int r, c4;
-                item_rc(item, r, c4);
-                __stcg(mine + item, *reinterpret_cast<const float4 *>(sRed + r * SP + 4 * c4));
-            }
+        if (lead_warp && !*abort) {
+            float *mine = slots + static_cast<long long>(rank) * kSlotFloats;
+            for (int r = lane; r < rows; r += 32)
+                if (r < lo || r >= hi) bulk_store_global(mine + r * BN, sRed + r * SP, kRowBytes);
+            bulk_commit();
+            bulk_wait_all();
+            fence_proxy_async_global();
         }
     }
-    // Publishes every rank's slot to the cluster (release / acquire at
-    // cluster scope orders the global stores above before the loads below).
+    // Publishes every rank's slot to the cluster (release / acquire).
     cluster_sync();
     if (threadIdx.x == 32 * C::kEpiWarp0) FP8Q_TRACE_AT(p, kTrCluster1);
     if (!epi || *abort) return;
-    OutT *out = static_cast<OutT *>(p.out);
-    // Lines may be discarded only if the workspace is 128-byte aligned.
-    const bool may_discard = (reinterpret_cast<uintptr_t>(p.ws) & 127u) == 0;
-    // The loop runs per warp (wbase is the same for all its lanes: the line
-    // discards below synchronise the warp); items past i_hi are skipped.
-    for (int wbase = i_lo + (etid - lane); wbase < i_hi; wbase += kBatch * C::kEpiThreads) {
-        const int base = wbase + lane;
-        float4 v[kMaxSplit][kBatch];
-#pragma unroll
-        for (int q = 0; q < kMaxSplit; ++q) {
-            if (q >= split) break;
-#pragma unroll
-            for (int bt = 0; bt < kBatch; ++bt) {
-                const int item = base + bt * C::kEpiThreads;
-                if (item >= i_hi) continue;
-                if (q == rank) {
-                    int r, c4;
-                    item_rc(item, r, c4);
-                    v[q][bt] = *reinterpret_cast<const float4 *>(sRed + r * SP + 4 * c4);
-                } else {
-                    v[q][bt] = __ldcg(slots + static_cast<long long>(q) * kSlotItems + item);
-                }
-            }
+    auto issue = [&](int c) {   // the lead warp, all lanes
+        const int r0 = lo + c * cr, nr = min(cr, hi - r0);
+        float *buf = land + (c & 1) * (split - 1) * cr * SP;
+        if (lane == 0) mbar_arrive_expect_tx(&ws_bar[c], static_cast<uint32_t>((split - 1) * nr) * kRowBytes);
+        __syncwarp();
+        for (int t = lane; t < (split - 1) * nr; t += 32) {
+            const int j = t / nr, rr = t - j * nr;
+            const int q = j < rank ? j : j + 1;
+            bulk_load_global(buf + (j * cr + rr) * SP, slots + q * kSlotFloats + static_cast<long long>(r0 + rr) * BN,
+                             kRowBytes, &ws_bar[c]);
         }
-#pragma unroll
-        for (int bt = 0; bt < kBatch; ++bt) {
-            const int item = base + bt * C::kEpiThreads;
-            if (item >= i_hi) continue;
-            float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int q = 0; q < kMaxSplit; ++q) {
-                if (q >= split) break;
-                sum.x += v[q][bt].x; sum.y += v[q][bt].y; sum.z += v[q][bt].z; sum.w += v[q][bt].w;
-            }
-            int r, c4;
-            item_rc(item, r, c4);
-            const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
-            if (SWAP) {
-                // Output column n0 + r; tokens m0 + 4 c4 .. + 3 (scales
-                // staged in sColScale by the epilogue).
-                const int n = n0 + r;
-                const float wsc = BLOCKWISE ? 1.0f : __ldg(p.w_scale + n);
-                const float bv = p.bias != nullptr ? __bfloat162float(p.bias[n]) : 0.0f;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int m = m0 + c4 * 4 + e;
-                    if (m < p.M) {
-                        const float y = BLOCKWISE ? sv[e] + bv : fmaf(sv[e] * wsc, sColScale[c4 * 4 + e], bv);
-                        out[static_cast<long long>(m) * p.ldo + n] = to_out<OutT>(y);
-                    }
+    };
+    if (lead_warp) {
+        fence_proxy_async_global();   // after the barrier's acquire, before the bulk reads
+        for (int c = 0; c < 2 && c < nchunks; ++c) issue(c);
+    }
+    const bool may_discard = (reinterpret_cast<uintptr_t>(p.ws) & 127u) == 0;
+    OutT *out = static_cast<OutT *>(p.out);
+    for (int c = 0; c < nchunks; ++c) {
+        const bool got = mbar_wait(&ws_bar[c], 0, abort, p.status);
+        const bool ok = named_barrier_and(1, C::kEpiThreads, got);
+        const int r0 = lo + c * cr, nr = min(cr, hi - r0);
+        const float *buf = land + (c & 1) * (split - 1) * cr * SP;
+        if (ok) {
+            for (int i = etid; i < nr * G; i += C::kEpiThreads) {
+                int rr, c4;
+                if (SWAP) { c4 = i / nr; rr = i - c4 * nr; }
+                else { rr = i / G; c4 = i - rr * G; }
+                const int r = r0 + rr;
+                float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int q = 0; q < split; ++q) {
+                    const float *src = q == rank ? sRed + r * SP : buf + ((q < rank ? q : q - 1) * cr + rr) * SP;
+                    const float4 v = *reinterpret_cast<const float4 *>(src + 4 * c4);
+                    sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
                 }
-            } else {
-                // Token m0 + r; output columns n0 + 4 c4 .. + 3.
-                const int m = m0 + r, n = n0 + 4 * c4;
-                if (n < p.N) {
-                    const float am = BLOCKWISE ? 1.0f : __ldg(p.a_scale + m);
-                    float y[4];
+                const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+                if (SWAP) {
+                    // Output column n0 + r; tokens m0 + 4 c4 .. + 3 (scales
+                    // staged in sColScale by the epilogue).
+                    const int n = n0 + r;
+                    const float wsc = BLOCKWISE ? 1.0f : __ldg(p.w_scale + n);
+                    const float bv = p.bias != nullptr ? __bfloat162float(p.bias[n]) : 0.0f;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const bool in = n + e < p.N;
-                        const float bv = (p.bias != nullptr && in) ? __bfloat162float(p.bias[n + e]) : 0.0f;
-                        y[e] = BLOCKWISE ? sv[e] + bv : fmaf(sv[e] * am, in ? __ldg(p.w_scale + n + e) : 0.0f, bv);
+                        const int m = m0 + c4 * 4 + e;
+                        if (m < p.M) {
+                            const float y = BLOCKWISE ? sv[e] + bv : fmaf(sv[e] * wsc, sColScale[c4 * 4 + e], bv);
+                            out[static_cast<long long>(m) * p.ldo + n] = to_out<OutT>(y);
+                        }
                     }
-                    OutT *o = out + static_cast<long long>(m) * p.ldo + n;
-                    if (n + 4 <= p.N) {
-                        *reinterpret_cast<uint2 *>(o) = make_uint2(pack_out2<OutT>(y[0], y[1]), pack_out2<OutT>(y[2], y[3]));
-                    } else {
+                } else {
+                    // Token m0 + r; output columns n0 + 4 c4 .. + 3.
+                    const int m = m0 + r, n = n0 + 4 * c4;
+                    if (n < p.N) {
+                        const float am = BLOCKWISE ? 1.0f : __ldg(p.a_scale + m);
+                        float y[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (n + e < p.N) o[e] = to_out<OutT>(y[e]);
+                        for (int e = 0; e < 4; ++e) {
+                            const bool in = n + e < p.N;
+                            const float bv = (p.bias != nullptr && in) ? __bfloat162float(p.bias[n + e]) : 0.0f;
+                            y[e] = BLOCKWISE ? sv[e] + bv : fmaf(sv[e] * am, in ? __ldg(p.w_scale + n + e) : 0.0f, bv);
+                        }
+                        OutT *o = out + static_cast<long long>(m) * p.ldo + n;
+                        if (n + 4 <= p.N) {
+                            *reinterpret_cast<uint2 *>(o) =
+                                make_uint2(pack_out2<OutT>(y[0], y[1]), pack_out2<OutT>(y[2], y[3]));
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if (n + e < p.N) o[e] = to_out<OutT>(y[e]);
+                        }
                     }
                 }
             }
         }
-        // Every line whose 8 items this warp has now read (all lanes: the
-        // values were used above) is dead in every other rank's slot.
-        __syncwarp();
-        if (may_discard) {
-#pragma unroll
-            for (int bt = 0; bt < kBatch; ++bt) {
-                const int item = base + bt * C::kEpiThreads;
-                if ((item & 7) != 0 || item + 8 > i_hi) continue;
-                for (int q = 0; q < split; ++q)
-                    if (q != rank) discard_l2_line(slots + static_cast<long long>(q) * kSlotItems + item);
+        // This thread's reads of the buffer, before the next bulk copies
+        // overwrite it.
+        fence_proxy_async_smem();
+        named_barrier_sync(1, C::kEpiThreads);
+        if (lead_warp && ok) {
+            // The chunk's rows in the other ranks' slots are dead.
+            if (may_discard) {
+                constexpr int kLinesPerRow = static_cast<int>(kRowBytes / 128u);
+                for (int t = lane; t < (split - 1) * nr * kLinesPerRow; t += 32) {
+                    const int j = t / (nr * kLinesPerRow), l = t - j * (nr * kLinesPerRow);
+                    const int q = j < rank ? j : j + 1;
+                    discard_l2_line(reinterpret_cast<const uint8_t *>(slots + q * kSlotFloats +
+                                                                      static_cast<long long>(r0) * BN) +
+                                    128 * l);
+                }
             }
+            if (c + 2 < nchunks) issue(c + 2);
         }
     }
     if (threadIdx.x == 32 * C::kEpiWarp0) FP8Q_TRACE_AT(p, kTrReduced);
@@ -515,6 +529,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
     uint8_t *sL = smem + C::kOffL;              // W16: E4M3 weight landing slots
     uint64_t *lfull = recv_full + 1;            // W16: landing slot filled
     uint64_t *lempty = lfull + C::kLStages;     // W16: landing slot read by the converting warps
+    uint64_t *ws_bar = lempty + C::kLStages;    // split-K workspace exchange: chunk landed
     constexpr int kLS = C::kLStages > 0 ? C::kLStages : 1;  // (non-W16 builds never use the landing ring)
     float *sRecv = reinterpret_cast<float *>(smem + C::kOffRecv);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
@@ -585,6 +600,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
             mbar_init(&lfull[j], 1);
             mbar_init(&lempty[j], C::kConvWarps);
         }
+        for (int c = 0; c < C::kWsBars; ++c) mbar_init(&ws_bar[c], 1);
 
         *abort = 0;
         fence_mbar_init();
@@ -1313,11 +1329,20 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
 
     }
 
-    if (split > 1 && p.ws != nullptr) {
-        reduce_split_workspace<C, OutT, BLOCKWISE, SWAP>(p, sRed, sColScale, rank, cluster_id, warp, abort,
-                                                        [&](int tile, int &a_t, int &b_t) { coords(tile, a_t, b_t); });
-    } else if constexpr (!C::kPush) {
-        if (split > 1) {
+    bool exchanged = false;   // split-K partials reduced through the workspace
+    if constexpr (C::kWsExchange) {
+        if (split > 1 && p.ws != nullptr) {
+            // (split > 1: one tile per cluster, tile index = cluster index)
+            int a_t, b_t;
+            coords(cluster_id, a_t, b_t);
+            reduce_split_workspace<C, OutT, BLOCKWISE, SWAP>(p, smem, sColScale, ws_bar, rank, cluster_id, warp,
+                                                             abort, (SWAP ? b_t : a_t) * C::kTokTile,
+                                                             (SWAP ? a_t : b_t) * C::kColTile);
+            exchanged = true;
+        }
+    }
+    if constexpr (!C::kPush) {
+        if (split > 1 && !exchanged) {
             cluster_sync();
             if (threadIdx.x == 32 * C::kEpiWarp0) FP8Q_TRACE_AT(p, kTrCluster1);
             if (warp >= C::kEpiWarp0 && !*abort) {

@@ -103,10 +103,18 @@ cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigne
     a.eps = pr.eps;
     a.x = FQ ? static_cast<const __nv_bfloat16 *>(pr.a) : nullptr;
     a.ldx = pr.lda;
-    // Split-K partials go through the workspace when the caller gave one
-    // large enough for this schedule (one 128 x BN slot per CTA).
+    // Split-K partials go through the workspace when the instantiation
+    // exchanges that way and the caller gave a workspace large enough for
+    // this schedule (one 128 x BN slot per CTA); the owner's rows arrive in
+    // at most kWsBars chunks.
     const size_t ws_need = static_cast<size_t>(a.num_tiles) * static_cast<size_t>(a.split) * 128u * BN * 4u;
-    a.ws = (a.split > 1 && pr.ws != nullptr && pr.ws_bytes >= ws_need) ? static_cast<float *>(pr.ws) : nullptr;
+    bool use_ws = C::kWsExchange && a.split > 1 && pr.ws != nullptr && pr.ws_bytes >= ws_need;
+    if (use_ws) {
+        const uint32_t cr = C::kLandBytes / (2u * static_cast<uint32_t>(a.split - 1) * C::kPartStride * 4u);
+        const uint32_t owned = (128u + static_cast<uint32_t>(a.split) - 1u) / static_cast<uint32_t>(a.split);
+        use_ws = cr >= 1 && (owned + cr - 1) / cr <= static_cast<uint32_t>(C::kWsBars);
+    }
+    a.ws = use_ws ? static_cast<float *>(pr.ws) : nullptr;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(l.grid));

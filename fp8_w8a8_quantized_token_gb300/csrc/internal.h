@@ -52,8 +52,9 @@ struct GemmProblem {
     size_t ws_bytes;        // its size; smaller than the schedule needs = not used
 };
 
-// Bytes of split-K workspace a schedule uses (0 when K is not split): one
-// slot of 128 x mma_n fp32 partial sums per CTA.
+// Bytes of split-K workspace a schedule uses (0 when K is not split or the
+// partial tiles are smaller than 128 x 128 floats): one slot of 128 x mma_n
+// fp32 partial sums per CTA.
 size_t plan_workspace_bytes(int64_t M, int64_t N, int swap_ab, int mma_n, int split_k);
 
 // Launchers return cudaSuccess or the launch error; a tensor map the driver
