@@ -45,6 +45,9 @@ DOMINANT_TRAFFIC_BYTES = {}
 
 # Small fixed cases for Nsight Compute captures: name -> (kind, M, N, K).
 PROFILE_CASES = {
+    # the dominant kernel of the o_proj sweep: its six launches (M = 512 ..
+    # 8192), once each after the warm-up round
+    "oproj_prefill_group": ("channelwise_group", (512, 1024, 2048, 4096, 8192), 4096, 4096),
     "prefill_oproj": ("channelwise", 8192, 4096, 4096),
     "prefill_gateup": ("channelwise", 8192, 24576, 4096),
     "mid_oproj_256": ("channelwise", 256, 4096, 4096),
@@ -280,8 +283,25 @@ def run_profile_case(name: str) -> int:
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     kind, M, N, K = PROFILE_CASES[name]
-    x = synthetic.activations(M, K, outliers=True).to(dev)
     n = PROFILE_WARMUP + 1
+    if kind == "channelwise_group":
+        # PROFILE_WARMUP rounds over all M, then one more: capture the last
+        # len(M) launches (-s PROFILE_WARMUP * len(M) -c len(M)).
+        w = synthetic.weights(N, K).to(dev)
+        wq, ws = fq.fp8q_quant_per_token(w)
+        xall = synthetic.activations(max(M), K, outliers=True).to(dev)
+        cases = []
+        for m in M:
+            xq, xs = fq.fp8q_quant_per_token(xall[:m])
+            cases.append((xq, xs))
+        torch.cuda.synchronize()
+        for _ in range(n):
+            for xq, xs in cases:
+                fq.fp8q_scaled_mm_channelwise(xq, wq, xs, ws)
+        torch.cuda.synchronize()
+        assert fq.fp8q_device_status() == fq.FP8Q_OK
+        return 0
+    x = synthetic.activations(M, K, outliers=True).to(dev)
     if kind == "quant_token":
         for _ in range(n):
             fq.fp8q_quant_per_token(x)

@@ -320,15 +320,23 @@ cudaError_t launch_per_token(const void *x, int64_t M, int K, int64_t ldx, void 
 
 }  // namespace
 
+// Row count from which per-token quantization is bandwidth-bound rather
+// than latency-bound (several rows per SM).
+constexpr int64_t kManyRows = 1024;
+
 cudaError_t launch_quant_per_token(const void *x, int64_t M, int64_t K, int64_t ldx, void *xq, float *xs, float eps,
                                    cudaStream_t st)
 {
     const int chunks = static_cast<int>(K >> 4);
-    // One 16-element chunk per thread where possible (short dependent
-    // chains: decode-size M runs one CTA per row and is latency-bound), in
-    // whole warps, at most 1024 threads; rows longer than 4 chunks per
+    // Decode-size M (latency-bound, one CTA per row): one 16-element chunk
+    // per thread where possible, the shortest dependent chain.  Many rows
+    // (bandwidth-bound): four chunks per thread, so each thread keeps 128
+    // bytes of loads in flight and an SM holds several times more bytes in
+    // flight than with one chunk per thread (its thread count is the limit).
+    // Whole warps, at most 1024 threads; rows longer than 4 chunks per
     // thread take the two-pass kernel.
-    int threads = (chunks + 31) / 32 * 32;
+    const int per_thread = M >= kManyRows ? 4 : 1;
+    int threads = (chunks + 32 * per_thread - 1) / (32 * per_thread) * 32;
     if (threads > 1024) threads = 1024;
     const int vpt = (chunks + threads - 1) / threads;
     switch (vpt) {

@@ -26,6 +26,9 @@ def dev():
     (1, 4096, True), (7, 4096, True), (300, 4096, True),
     (33, 12288, True), (5, 16, False), (64, 7168, False), (3, 3072, True),
     (2, 65552, False),       # longer than the register-cached path: two-pass kernel
+    # many rows: the four-chunks-per-thread configuration, whole and ragged
+    # last thread (K = 4112: 257 chunks over 96 threads)
+    (1024, 4096, True), (1500, 4112, True), (1031, 12288, False), (1024, 48, False),
 ])
 def test_per_token_bit_exact(dev, M, K, outliers):
     x = synthetic.activations(M, K, seed=M * 7 + K, outliers=outliers)
