@@ -108,7 +108,8 @@ cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigne
     // this schedule (one 128 x BN slot per CTA); the owner's rows arrive in
     // at most kWsBars chunks.
     const size_t ws_need = static_cast<size_t>(a.num_tiles) * static_cast<size_t>(a.split) * 128u * BN * 4u;
-    bool use_ws = C::kWsExchange && a.split > 1 && pr.ws != nullptr && pr.ws_bytes >= ws_need;
+    bool use_ws = C::kWsExchange && a.split > 1 && pr.ws != nullptr && pr.ws_bytes >= ws_need &&
+                  workspace_exchange_enabled();
     if (use_ws) {
         const uint32_t cr = C::kLandBytes / (2u * static_cast<uint32_t>(a.split - 1) * C::kPartStride * 4u);
         const uint32_t owned = (128u + static_cast<uint32_t>(a.split) - 1u) / static_cast<uint32_t>(a.split);

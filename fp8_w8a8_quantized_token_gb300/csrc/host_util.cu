@@ -100,6 +100,15 @@ int prefetch_kblocks()
     return v;
 }
 
+bool workspace_exchange_enabled()
+{
+    static const bool v = [] {
+        const char *s = getenv("FP8Q_WORKSPACE_EXCHANGE");
+        return s != nullptr && s[0] == '1';
+    }();
+    return v;
+}
+
 namespace {
 struct LaunchRecord {
     cudaStream_t stream;

@@ -108,6 +108,13 @@ unsigned long long *trace_buffer();
 // Weight K blocks each GEMM CTA prefetches into L2 before its dependency
 // wait (default 16; FP8Q_PREFETCH_KB overrides it at start-up, 0 disables).
 int prefetch_kblocks();
+// Split-K partial sums through the caller's workspace (global memory)
+// instead of distributed shared memory: off unless FP8Q_WORKSPACE_EXCHANGE=1
+// at start-up.  On the GB300s measured, reading partials that other SMs of
+// the cluster have just written through global memory moved 10-30 GB/s per
+// SM, below the distributed-shared-memory exchange at every schedule, so by
+// default the library asks for no workspace and ignores one passed to it.
+bool workspace_exchange_enabled();
 
 // Per-stream record of the byte range the library's most recent launch on
 // that stream writes.  With programmatic dependent launch, that launch is the

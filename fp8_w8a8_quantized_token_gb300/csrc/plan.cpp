@@ -119,8 +119,8 @@ bool table_plan(int64_t M, int64_t N, int64_t K, int blockwise, fp8q_plan *pl)
 size_t plan_workspace_bytes(int64_t M, int64_t N, int swap_ab, int mma_n, int split_k)
 {
     // Only partial tiles of 64 KB and more (128 x 128 floats) go through the
-    // workspace; smaller ones exchange faster in distributed shared memory.
-    if (split_k <= 1 || (swap_ab && mma_n < 128)) return 0;
+    // workspace, and only when the workspace exchange is enabled.
+    if (split_k <= 1 || (swap_ab && mma_n < 128) || !workspace_exchange_enabled()) return 0;
     const int64_t tile_m = swap_ab ? mma_n : 128, tile_n = swap_ab ? 128 : mma_n;
     const int64_t tiles = ((M + tile_m - 1) / tile_m) * ((N + tile_n - 1) / tile_n);
     return static_cast<size_t>(tiles) * static_cast<size_t>(split_k) * 128u * static_cast<size_t>(mma_n) * 4u;

@@ -5,7 +5,7 @@
 //   s = max(amax(|x| over the group), eps) / 448
 //   q = cvt.rn.satfinite.e4m3(x / s)
 // The correctly rounded quotient x / s is formed with Markstein's
-// FMA-based correction (quotient() in quant_common.cuh, shared with the
+// FMA-based correction (quotient2() in quant_common.cuh, shared with the
 // GEMM's fused quantization) rather than one IEEE division per element.
 // Per-token groups are whole rows ("qinput"/"x_scale" of the channelwise
 // path, "Tune FP8 GEMM Triton tiles on L40S..." page, key source snippets);
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(1024) quant_per_token_two_pass_kernel(const __
 // quantizer on the row-padding page): UE8M0 rounds each scale up to a power
 // of two; SILU reads rows of 2K values and quantizes y = silu(x[k]) *
 // x[K + k] (fp32), dividing with the IEEE division (y is a general fp32
-// value, outside the bf16 numerators the quotient() shortcut is checked
+// value, outside the bf16 numerators the quotient2() shortcut is checked
 // for; measured, the shortcut does not speed this kernel up: it is bound by
 // the ~38 fp32 instructions per element of exp, silu and quantization).
 // ---------------------------------------------------------------------------

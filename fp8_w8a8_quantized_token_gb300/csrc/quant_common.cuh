@@ -28,43 +28,50 @@ __device__ __forceinline__ Chunk16 load_chunk(const __nv_bfloat16 *p)
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__device__ __forceinline__ float amax_word(uint32_t w, float m)
-{
-    return fmaxf(m, fmaxf(fabsf(bf_lo(w)), fabsf(bf_hi(w))));
-}
+__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t w) { return *reinterpret_cast<const __nv_bfloat162 *>(&w); }
 
+// max(m, |x|) over the 16 values, on packed bf16 pairs: |x| and the max of
+// bf16 values are exact in bf16 (the result is one of the inputs), and the
+// packed max, like fmaxf, returns the other operand when one is NaN.
 __device__ __forceinline__ float chunk_amax(const Chunk16 &c, float m)
 {
-    m = amax_word(c.lo.x, m); m = amax_word(c.lo.y, m); m = amax_word(c.lo.z, m); m = amax_word(c.lo.w, m);
-    m = amax_word(c.hi.x, m); m = amax_word(c.hi.y, m); m = amax_word(c.hi.z, m); m = amax_word(c.hi.w, m);
-    return m;
+    __nv_bfloat162 a = __hmax2(__habs2(as_bf2(c.lo.x)), __habs2(as_bf2(c.lo.y)));
+    a = __hmax2(a, __hmax2(__habs2(as_bf2(c.lo.z)), __habs2(as_bf2(c.lo.w))));
+    __nv_bfloat162 b = __hmax2(__habs2(as_bf2(c.hi.x)), __habs2(as_bf2(c.hi.y)));
+    b = __hmax2(b, __hmax2(__habs2(as_bf2(c.hi.z)), __habs2(as_bf2(c.hi.w))));
+    a = __hmax2(a, b);
+    return fmaxf(m, fmaxf(__low2float(a), __high2float(a)));
 }
 
-// The IEEE quotient RN(x / s), given r = RN(1 / s), by Markstein's
-// correction (P. Markstein, "Computation of elementary functions on the IBM
-// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with
-// q0 = RN(x * r), the remainder x - q0 * s is exact in one FMA, and
-// RN(q0 + remainder * r) is the correctly rounded quotient.  Checked
+// The IEEE quotients RN(x / s) of a pair, given r = RN(1 / s), by
+// Markstein's correction (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990): with q0 = RN(x * r), the remainder x - q0 * s is exact in one FMA,
+// and RN(q0 + remainder * r) is the correctly rounded quotient.  Checked
 // exhaustively against the division on this GPU for every bf16 significand
 // of x and every fp32 significand of s (2^30 pairs, at several exponent
 // offsets): no difference.  The result carries the sign of x, as x / s
 // does for s > 0 (this keeps -0 for x = -0).  The kernels use it only for
 // normal finite s (the reciprocal is then a normal number); where the
 // quotient would be subnormal in fp32, x / s is below 2^-11 and both round
-// to a signed zero in E4M3.
-__device__ __forceinline__ float quotient(float x, float s, float r)
+// to a signed zero in E4M3.  Packed fp32x2 operations: each lane is the
+// correctly rounded scalar operation (fma(q0, -s, x) is fma(-q0, s, x)
+// exactly), two quotients per instruction.
+__device__ __forceinline__ float2 quotient2(float2 x, float s, float r)
 {
-    const float q0 = x * r;
-    const float rem = fmaf(-q0, s, x);
-    return copysignf(fmaf(rem, r, q0), x);
+    const float2 r2 = make_float2(r, r);
+    const float2 q0 = __fmul2_rn(x, r2);
+    const float2 rem = __ffma2_rn(q0, make_float2(-s, -s), x);
+    const float2 q = __ffma2_rn(rem, r2, q0);
+    return make_float2(copysignf(q.x, x.x), copysignf(q.y, x.y));
 }
 
 // Four bf16 (two words) / s -> four E4M3 bytes packed little-endian.
 __device__ __forceinline__ uint32_t quant4(uint32_t w0, uint32_t w1, float s, float r)
 {
-    const uint32_t a = cvt_e4m3x2(quotient(bf_lo(w0), s, r), quotient(bf_hi(w0), s, r));
-    const uint32_t b = cvt_e4m3x2(quotient(bf_lo(w1), s, r), quotient(bf_hi(w1), s, r));
-    return a | (b << 16);
+    const float2 q0 = quotient2(make_float2(bf_lo(w0), bf_hi(w0)), s, r);
+    const float2 q1 = quotient2(make_float2(bf_lo(w1), bf_hi(w1)), s, r);
+    return cvt_e4m3x2(q0.x, q0.y) | (cvt_e4m3x2(q1.x, q1.y) << 16);
 }
 
 __device__ __forceinline__ uint32_t quant4_div(uint32_t w0, uint32_t w1, float s)

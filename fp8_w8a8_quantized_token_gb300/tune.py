@@ -131,7 +131,7 @@ def main():
             best_us, best = timed[0]
             rows.append((N, K, bw, M, *best))
             print(json.dumps({"shape": label, "M": M, "best_us": round(best_us, 2), "best": best,
-                              "next": [(round(u, 2), c) for u, c in timed[1:4]]}), flush=True)
+                              "all": [(round(u, 2), c) for u, c in timed[1:]]}), flush=True)
     with open(args.out, "w") as f:
         f.write("// Generated by fp8_w8a8_quantized_token_gb300/tune.py on a GB300: the fastest measured\n")
         f.write("// schedule per shape and M.  Row: {N, K, blockwise, M, swap_ab, mma_n, split_k},\n")

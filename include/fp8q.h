@@ -199,9 +199,10 @@ FP8Q_API fp8q_status fp8q_quant_weight_block128(const void *w, int64_t N, int64_
  * a_scale : fp32 [M]; b_scale : fp32 [N]; bias : bf16 [N] or NULL.
  * out     : [M, N] row-major (ld = N) of out_dtype (N % 8 == 0).
  * workspace, workspace_bytes : optional DEVICE scratch for the split-K
- *           partial sums (see fp8q_workspace_bytes); NULL / 0 or too small
- *           for the schedule: the partials are exchanged in distributed
- *           shared memory instead.  Same result either way.
+ *           partial sums (see fp8q_workspace_bytes); NULL / 0, too small for
+ *           the schedule, or the workspace exchange not enabled: the
+ *           partials are exchanged in distributed shared memory instead.
+ *           Same result either way.
  * Errors  : INVALID_ARG / UNSUPPORTED as above; INVALID_ARG for a
  *           workspace that is not 16-byte aligned.
  * ------------------------------------------------------------------------- */
@@ -246,17 +247,23 @@ FP8Q_API fp8q_status fp8q_scaled_mm_blockwise(const void *a, const void *w, cons
  * fp8_scaled_mm / fp8_blockwise_scaled_mm callers own all device memory).
  *
  * With K split over a cluster of s CTAs, each CTA computes an fp32 partial
- * tile over its range of K blocks.  Given a workspace of at least this
- * size, every CTA writes the parts of its partial tile that other CTAs of
- * its cluster own into its own slot (one slot of 128 x mma_n floats per
- * CTA: tiles * s * 128 * mma_n * 4 bytes), a cluster barrier publishes
- * them, and each CTA adds up its share of the outputs over all s partials
- * in a fixed order.  The slots are traffic through L2, which is faster
- * than the distributed-shared-memory exchange used without a workspace,
- * and gives the same result.  Nothing in the workspace has to be
- * initialised, and its contents are undefined after the call.  Calls that
- * can run concurrently on the GPU need separate workspaces; calls in
- * order on one stream can share one.
+ * tile over its range of K blocks, and each CTA adds up its share of the
+ * tile's outputs over all s partials in a fixed order.  The other CTAs'
+ * partials reach it in one of two ways, with identical results:
+ *   - through distributed shared memory (the default);
+ *   - through this workspace (one slot of 128 x mma_n floats per CTA:
+ *     tiles * s * 128 * mma_n * 4 bytes): every CTA bulk-copies the rows
+ *     other CTAs own into its slot, a cluster barrier publishes them, and
+ *     each CTA bulk-loads its rows from the other slots.  Used only for
+ *     partial tiles of 128 x 128 floats or more, and only when the process
+ *     starts with FP8Q_WORKSPACE_EXCHANGE=1: on the GB300s this library was
+ *     measured on, it was slower than the distributed-shared-memory
+ *     exchange at every schedule (partials just written by other SMs came
+ *     back through global memory at 10-30 GB/s per SM).
+ * So by default this returns 0 and the GEMMs ignore a workspace.  Nothing
+ * in the workspace has to be initialised, and its contents are undefined
+ * after the call.  Calls that can run concurrently on the GPU need
+ * separate workspaces; calls in order on one stream can share one.
  * Returns 0 as well for invalid sizes (M <= 0, N <= 0, K <= 0).
  * ------------------------------------------------------------------------- */
 FP8Q_API size_t fp8q_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t blockwise);

@@ -67,49 +67,30 @@ def test_channelwise_every_schedule(dev, schedule, swap, mma_n, split):
 SPLIT_SCHEDULES = [s for s in SCHEDULES if s[2] > 1]
 
 
-@pytest.mark.parametrize("blockwise", [False, True])
-@pytest.mark.parametrize("swap,mma_n,split", SPLIT_SCHEDULES)
-def test_split_k_workspace_equals_dsmem_exchange(dev, schedule, swap, mma_n, split, blockwise):
-    """K split over a cluster: the partial sums exchanged through the
-    caller's global workspace (schedules with partial tiles of 128 x 128
-    floats or more) and through distributed shared memory are added in the
-    same order, so the outputs are identical; a workspace one slot short of
-    what the schedule needs is not used (identical again); smaller partial
-    tiles need no workspace; and the result matches the oracle.  Two M per
-    schedule: one tile row, and a ragged multi-tile problem."""
-    fq.fp8q_set_plan_override(swap, mma_n, split)
-    for M in (5, 300):
-        if blockwise:
-            N, K = 384, 1024
-            out, ctx = blockwise_case(dev, M, N, K, seed=M + 7, bias=True)
-            _, _, b, rq, rs, rwq, rws = ctx
-            xq, xs, _, _ = quant_both_group(synthetic.activations(M, K, seed=M + 7, outliers=True), dev, 128)
-            wq, ws = fq.fp8q_quant_weight_block128(synthetic.weights(N, K, seed=M + 7).to(dev))
+def test_split_k_requests_no_workspace_by_default(dev, schedule):
+    """Without FP8Q_WORKSPACE_EXCHANGE=1 the K-split partials are exchanged in
+    distributed shared memory: no schedule asks for a workspace."""
+    for swap, mma_n, split in SPLIT_SCHEDULES:
+        fq.fp8q_set_plan_override(swap, mma_n, split)
+        for bw in (False, True):
+            assert fq.fp8q_workspace_bytes(300, 384, 1024, bw) == 0
 
-            def run(workspace):
-                return fq.fp8q_scaled_mm_blockwise(xq, wq, xs, ws, M=M, bias=b.to(dev), workspace=workspace)
-            ref = blockwise_ref(ctx, M)
-        else:
-            N, K = 392, 1040
-            x = synthetic.activations(M, K, seed=M + 7, outliers=True)
-            w = synthetic.weights(N, K, seed=M + 7)
-            b = synthetic.bias(N, seed=M + 7)
-            xq, xs, rq, rs = quant_both_per_token(x, dev)
-            wq, ws, rwq, rws = quant_both_per_token(w, dev)
 
-            def run(workspace):
-                return fq.fp8q_scaled_mm_channelwise(xq, wq, xs, ws, bias=b.to(dev), workspace=workspace)
-            ref = ref_values(oracle.gemm_channelwise(rq, rwq, rs, rws, bias=b, threads=THREADS))
-        need = fq.fp8q_workspace_bytes(M, N, K, blockwise)
-        assert (need > 0) == (swap == 0 or mma_n >= 128)
-        out_ws, out_dsmem = run("auto"), run(None)
-        out_short = run(torch.empty(need - 128 * mma_n * 4, dtype=torch.uint8, device=dev)) if need else out_dsmem
-        torch.cuda.synchronize()
-        what = f"{'blockwise' if blockwise else 'channelwise'} sched {swap},{mma_n},{split} M={M}"
-        assert torch.equal(out_ws, out_dsmem), what
-        assert torch.equal(out_short, out_dsmem), what
-        assert_gemm_close(out_values(out_ws), ref, what)
-    assert fq.fp8q_device_status() == fq.FP8Q_OK
+def test_split_k_workspace_exchange_equals_dsmem_exchange(dev):
+    """With FP8Q_WORKSPACE_EXCHANGE=1 (read at start-up, so in a child
+    process): for every K-split schedule, the partial sums exchanged through
+    the caller's global workspace (partial tiles of 128 x 128 floats or
+    more) and through distributed shared memory are added in the same
+    order, so the outputs are identical; a workspace one slot short is not
+    used; smaller partial tiles ask for none; and the result matches the
+    oracle (tests/ws_exchange_check.py)."""
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    r = subprocess.run([sys.executable, os.path.join(here, "ws_exchange_check.py")], capture_output=True, text=True,
+                       timeout=900, env=dict(os.environ, FP8Q_WORKSPACE_EXCHANGE="1"))
+    assert r.returncode == 0 and "workspace exchange ok" in r.stdout, r.stdout[-3000:] + r.stderr[-3000:]
 
 
 @pytest.mark.parametrize("M", [1, 2, 5, 16, 33, 64, 100, 128, 129, 256, 300, 512])
