@@ -37,11 +37,12 @@ METRIC = "FP8 W8A8 GEMM TFLOP/s & GB/s vs M (1-8192) and % of roofline"
 UNIT = "TFLOP/s"
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
-# kernel, keyed by (scheme, swap_ab, mma_n), from a one-kernel Nsight
-# Compute capture of its profiling case (--profile-case), scaled to the
-# bench launch by the units it processes where the case is smaller.  A key
-# is dropped whenever its kernel changes.
-DOMINANT_TRAFFIC_BYTES = {}
+# kernel, keyed by (scheme, swap_ab, mma_n, 2-CTA pairs), from a one-kernel
+# Nsight Compute capture of its profiling case (--profile-case): for the
+# o_proj sweep, the 2-CTA prefill kernel's five launches M = 512 .. 8192 of
+# "oproj_prefill_group", averaged (profiles/traffic_oproj_prefill_group.md).
+# A key is dropped whenever its kernel changes.
+DOMINANT_TRAFFIC_BYTES = {("channelwise", 0, 256, 1): 35.74e6}
 
 # Small fixed cases for Nsight Compute captures: name -> (kind, M, N, K).
 PROFILE_CASES = {
@@ -614,7 +615,7 @@ def main():
     groups = {}
     for p, gu in zip(problems, g_us):
         pl = p["plan"]
-        key = ("blockwise" if p["bw"] else "channelwise", pl["swap_ab"], pl["mma_n"])
+        key = ("blockwise" if p["bw"] else "channelwise", pl["swap_ab"], pl["mma_n"], pl["two_sm"])
         g = groups.setdefault(key, {"us": 0.0, "flops": 0, "bytes": 0, "n": 0})
         g["us"] += gu
         g["flops"] += 2 * p["M"] * p["N"] * p["K"]
@@ -632,8 +633,9 @@ def main():
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": round(peaks["hbm_gbs"], 1),
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 3)}
     roof["traffic"] = DOMINANT_TRAFFIC_BYTES.get(dom_key)
-    roof["kernel"] = (f"fp8_gemm_kernel<{'swap' if dom_key[1] else 'noswap'}, mma_n={dom_key[2]}, {dom_key[0]}> "
-                      f"({dom['n']} launches/pass; achieved = their FLOPs / their summed durations)")
+    roof["kernel"] = (f"fp8_gemm_kernel<{'swap' if dom_key[1] else 'noswap'}, mma_n={dom_key[2]}, {dom_key[0]}"
+                      f"{', 2-CTA pairs' if dom_key[3] else ''}> ({dom['n']} launches/pass; achieved = their FLOPs "
+                      "/ their summed durations)")
     roof["share_of_pass"] = round(dom["us"] / (quant_total + gemm_total), 3)
     roof["peak_source"] = peaks["source"]
 
