@@ -130,7 +130,22 @@ struct GemmCfg {
     // launch's CTAs finish.)
     static constexpr int kIssuers = (BLOCKWISE || TWO_SM || BN >= 256) ? 1 : 2;
     static constexpr int kSlotCols = kIssuers * BN;  // TMEM columns per accumulator slot
-    static constexpr int kEpiWarp0 = 1 + kIssuers;   // first epilogue warp
+    // Register split (blockwise 256-column tiles): each epilogue thread
+    // promotes 128 accumulator columns every K block, in rounds of (TMEM
+    // load, wait, packed FMAs) whose latencies add up; with 10 warps, three
+    // share a sub-partition and cap a thread at 168 registers, which allows
+    // only 16 columns per round (8 rounds per K block, longer than the
+    // block's MMA).  Instead the CTA runs 12 warps: warpgroup 0 = producer,
+    // MMA issuer and two idle warps; warpgroups 1 and 2 = the eight epilogue
+    // warps.  Launched at kLaunchRegs registers per thread, warpgroup 0 gives
+    // registers back (setmaxnreg.dec to kLowRegs) and the epilogue warpgroups
+    // take them (setmaxnreg.inc to kHighRegs), enough for 64 columns per
+    // round.  kLowRegs * 128 + kHighRegs * 256 == kLaunchRegs * kThreads, and
+    // the host checks the kernel's register count before it launches.
+    static constexpr bool kRegSplit = BLOCKWISE && !SWAP && BN == 256 && !TWO_SM && !FQ && !W16;
+    static constexpr int kIdleWarps = kRegSplit ? 2 : 0;
+    static constexpr int kLaunchRegs = 168, kLowRegs = 72, kHighRegs = 216;
+    static constexpr int kEpiWarp0 = 1 + kIssuers + kIdleWarps;   // first epilogue warp
     // FQ: two warps after the epilogue warps quantize the activation tiles.
     static constexpr int kQuantWarps = FQ ? 2 : 0;
     static constexpr int kQuantWarp0 = kEpiWarp0 + kEpiWarps;
@@ -141,6 +156,9 @@ struct GemmCfg {
     static constexpr int kConvWarps = W16 ? 8 : 0;
     static constexpr int kConvWarp0 = kQuantWarp0 + kQuantWarps;
     static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps + kQuantWarps + kConvWarps);
+    static_assert(!kRegSplit || (kThreads == 384 && kEpiWarp0 == 4 && kEpiWarps == 8 &&
+                                 kLowRegs * 128 + kHighRegs * 256 == kLaunchRegs * kThreads),
+                  "register split: warpgroup 0 low, warpgroups 1-2 high, same total as at launch");
     // K steps of one 128-wide K block: 4 MMAs of K = 32 (E4M3) or, W16, 8
     // of K = 16 (bf16).
     static constexpr int kKSteps = W16 ? 8 : 4;
@@ -684,6 +702,10 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
     pdl_wait();
     pdl_trigger();
     if (threadIdx.x == 0) FP8Q_TRACE_AT(p, kTrPdlWait);
+    if constexpr (C::kRegSplit) {
+        if (warp < 4) setmaxnreg_dec<C::kLowRegs>();
+        else setmaxnreg_inc<C::kHighRegs>();
+    }
 
     if (warp == 0) {
         // ------------------------------------------------------------------
@@ -1000,6 +1022,8 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
             }
         }
         __syncwarp();
+    } else if (warp < C::kEpiWarp0) {
+        // Idle warps of the register split's warpgroup 0.
     } else {
         // ------------------------------------------------------------------
         // Epilogue warps
@@ -1048,8 +1072,9 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
             bool ok = true;
             if (BLOCKWISE) {
                 // TMEM columns per wait: 16 where the accumulator row is long
-                // (keeps the 128-float row and the loop state in registers).
-                constexpr int kPromoteCols = C::kCols >= 128 ? 16 : 32;
+                // (keeps the 128-float row and the loop state in registers),
+                // 64 with the register split.
+                constexpr int kPromoteCols = C::kRegSplit ? 64 : C::kCols >= 128 ? 16 : 32;
 #pragma unroll
                 for (int j = 0; j < C::kCols; ++j) acc[j] = 0.0f;
                 const int wblk = SWAP ? a_t : (n0 + col0) >> 7;  // 128-row weight block of these columns
@@ -1070,9 +1095,9 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
 #pragma unroll
                     for (int c = 0; c < C::kCols; c += kPromoteCols) {
                         uint32_t r[kPromoteCols];
-                        tmem_ld16(taddr + c, *reinterpret_cast<uint32_t(*)[16]>(r));
-                        if (kPromoteCols == 32 && c + 16 < C::kCols)
-                            tmem_ld16(taddr + c + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+#pragma unroll
+                        for (int h = 0; h < kPromoteCols; h += 16)
+                            if (c + h < C::kCols) tmem_ld16(taddr + c + h, *reinterpret_cast<uint32_t(*)[16]>(r + h));
                         tmem_ld_wait();
 #pragma unroll
                         for (int j = 0; j < kPromoteCols && c + j < C::kCols; j += 2) {

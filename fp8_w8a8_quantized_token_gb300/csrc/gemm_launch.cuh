@@ -28,6 +28,15 @@ cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigne
     if (!(attr_done[dev >> 6].load(std::memory_order_acquire) & bit)) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmemBytes));
         if (e != cudaSuccess) return e;
+        if constexpr (C::kRegSplit) {
+            // The register split hands exactly the launch allocation between
+            // the warpgroups; with any other per-thread count its
+            // setmaxnreg.inc could never be satisfied, so refuse to launch.
+            cudaFuncAttributes fa;
+            e = cudaFuncGetAttributes(&fa, kernel);
+            if (e != cudaSuccess) return e;
+            if (fa.numRegs != C::kLaunchRegs) return cudaErrorInvalidKernelImage;
+        }
         attr_done[dev >> 6].fetch_or(bit, std::memory_order_acq_rel);
     }
 
