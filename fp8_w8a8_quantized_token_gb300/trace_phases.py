@@ -10,6 +10,15 @@ median and maximum time (microseconds after the earliest CTA entry) over
 the launch's CTAs.  Schedules that split K are traced twice: with the
 split-K workspace and without it (partials exchanged in distributed shared
 memory).  Inputs are the seeded synthetic tensors.  Needs a GPU.
+
+    python -m fp8_w8a8_quantized_token_gb300.trace_phases --back-to-back MxNxK
+
+traces the steady state instead: four GEMM launches over four weight copies
+(the inputs quantized beforehand) captured in one CUDA graph, replayed
+three times as warm-up and once more after clearing the buffer; it prints
+each launch's phase medians (microseconds after the graph's first CTA
+entry) and, for launches 2-4, the gap from the previous launch's last CTA
+exit to this launch's dependency release.
 """
 from __future__ import annotations
 
@@ -56,10 +65,66 @@ def trace_launch(L, dev, M: int, N: int, K: int, workspace="auto"):
     return plan, t
 
 
+def back_to_back(L, dev, M: int, N: int, K: int):
+    x = synthetic.activations(M, K, outliers=True).to(dev)
+    xq, xs = fq.fp8q_quant_per_token(x)
+    wq0, ws = fq.fp8q_quant_per_token(synthetic.weights(N, K).to(dev))
+    copies = [wq0] + [wq0.clone() for _ in range(3)]
+    outs = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(4)]
+    plan = fq.fp8q_gemm_plan(M, N, K)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        for i in range(4):
+            fq.fp8q_scaled_mm_channelwise(xq, copies[i], xs, ws, out=outs[i], workspace=None)
+    side.synchronize()
+    if L.fp8q_trace_clear() != 0:   # capture writes launch i to block i
+        raise RuntimeError("fp8q_trace_clear failed")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for i in range(4):
+            fq.fp8q_scaled_mm_channelwise(xq, copies[i], xs, ws, out=outs[i], workspace=None)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    if L.fp8q_trace_clear() != 0:
+        raise RuntimeError("fp8q_trace_clear failed")
+    g.replay()
+    torch.cuda.synchronize()
+    n = 4 * 4096 * SLOTS_PER_CTA
+    buf = (ctypes.c_ulonglong * n)()
+    if L.fp8q_trace_read(ctypes.addressof(buf), n) != 0:
+        raise RuntimeError("fp8q_trace_read failed")
+    t = np.frombuffer(buf, dtype=np.uint64).reshape(4, 4096, SLOTS_PER_CTA)[:, :plan["grid"]].astype(np.int64)
+    t0 = t[0, :, 0].min()
+    print(f"== back to back: M={M} N={N} K={K} plan={plan}")
+    cols = [("entry", 0), ("release", 2), ("first MMA", 4), ("last MMA", 5), ("stored", 7), ("exit", 11)]
+    print("  launch " + "".join(f"{c:>12}" for c, _ in cols) + "   gap(prev exit -> release)")
+    for i in range(4):
+        med = [np.median(t[i, :, j][t[i, :, j] > 0] - t0) / 1000.0 for _, j in cols]
+        gap = ""
+        if i > 0:
+            prev_exit = t[i - 1, :, 11].max() - t0
+            rel = t[i, :, 2][t[i, :, 2] > 0] - t0
+            gap = f"   {(rel.min() - prev_exit) / 1000.0:6.2f} .. {(np.median(rel) - prev_exit) / 1000.0:6.2f} us"
+        print(f"  {i + 1:6d} " + "".join(f"{v:12.2f}" for v in med) + gap)
+    per_launch = (t[3, :, 11].max() - t[0, :, 11].max()) / 3000.0
+    print(f"  launch period (last exit to last exit): {per_launch:.2f} us")
+
+
 def main(argv) -> int:
     if not argv:
         print(__doc__)
         return 2
+    if argv[0] == "--back-to-back":
+        L = fq.load_library(fbuild.build(trace=True))
+        L.fp8q_trace_read.argtypes = [ctypes.c_void_p, ctypes.c_int]
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        for spec in argv[1:]:
+            back_to_back(L, dev, *(int(v) for v in spec.split("x")))
+        return 0
     L = fq.load_library(fbuild.build(trace=True))
     L.fp8q_trace_read.argtypes = [ctypes.c_void_p, ctypes.c_int]
     dev = torch.device("cuda", 0)
