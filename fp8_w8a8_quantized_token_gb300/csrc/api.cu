@@ -50,7 +50,6 @@ fp8q_status launch_planned(GemmProblem p, const fp8q_plan &pl, cudaStream_t st)
     l.stages = pl.stages;
     l.pair = pl.pair != 0;
     l.two_sm = pl.two_sm != 0;
-    l.tmem_staged = pl.tmem_staged != 0;
     const cudaError_t e = p.blockwise ? launch_gemm_blockwise(p, l, status, st)
                                       : launch_gemm_channelwise(p, l, status, st);
     if (e == cudaSuccess) note_launch_writes(st, p.out, static_cast<size_t>(p.M) * p.N * 2);
@@ -311,7 +310,6 @@ fp8q_status fp8q_scaled_mm_w8a16(const void *x, int64_t ldx, const void *w, int6
     while (split < 8 && tiles * split * 2 <= num_sms) split *= 2;
     pl.split_k = split;
     plan_finish(M, N, K, 0, num_sms, &pl);
-    pl.tmem_staged = 0;   // (the weight-only kernel converts its weights itself)
     GemmProblem p;
     p.M = M; p.N = N; p.K = K; p.m_pad = M;
     p.a = x; p.lda = ldx; p.w = w; p.ldw = ldw;

@@ -383,21 +383,6 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t v)
     return *reinterpret_cast<const uint32_t *>(&b);
 }
 
-// E4M3 x E4M3 -> fp32 MMA, K = 32 per instruction, with A read from tensor
-// memory: row m of A in TMEM lane m, K along the columns, four E4M3 values
-// per 32-bit column (the lower K in the lower byte): 8 columns per
-// instruction.  B from shared memory (descriptor).
-__device__ __forceinline__ void umma_e4m3_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                                 uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 __device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate)
 {

@@ -28,12 +28,6 @@ cudaError_t dispatch_gemm(const GemmProblem &p, const GemmLaunch &l, unsigned *s
         return cudaErrorInvalidValue;
     }
     if (l.swap_ab) {
-        // Weights staged in tensor memory before the dependency wait
-        // (channelwise 16-token decode tiles; the planner decides).
-        if constexpr (!BLOCKWISE)
-            if (l.tmem_staged && l.mma_n == 16)
-                return launch_gemm_inst<true, 16, kTmemStagedStages, false, OutT, false, false, false, true>(p, l,
-                                                                                                           status, st);
         switch (l.mma_n) {
             case 16: return launch_gemm_inst<true, 16, stages_for(true, 16), BLOCKWISE, OutT>(p, l, status, st);
             case 32: return launch_gemm_inst<true, 32, stages_for(true, 32), BLOCKWISE, OutT>(p, l, status, st);

@@ -112,8 +112,7 @@ enum TracePhase {
     } while (0)
 #endif
 
-template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, bool TWO_SM = false, bool FQ = false, bool W16 = false,
-          bool TS = false>
+template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, bool TWO_SM = false, bool FQ = false, bool W16 = false>
 struct GemmCfg {
     static constexpr int kEpiWarps = BN > 128 ? 8 : 4;
     static constexpr int kColGroups = kEpiWarps / 4;
@@ -193,36 +192,18 @@ struct GemmCfg {
     // their own and turn them into the ring's B tiles and scale slots.
     static constexpr int kXStages = FQ ? STAGES : 0;
     static constexpr uint32_t kXBytes = FQ ? static_cast<uint32_t>(BN) * 256u : 0u;
-    // Weights staged in tensor memory (TS; channelwise swapped 16-token
-    // decode tiles with K split, one tile per CTA).  Before the dependency
-    // wait, the producer streams the CTA's weight K blocks through the ring
-    // (A tiles only) and the epilogue warps, idle until the accumulator is
-    // ready, copy each landed tile into tensor memory (32 columns per K
-    // block: row m in lane m, 4 E4M3 values per column, the lower K in the
-    // lower byte) and free the ring slot; K blocks beyond kTW stay in their
-    // ring slot.  Every weight byte of the CTA is on chip when the
-    // dependency wait returns.  The activation tiles of all K blocks then
-    // load into kNB slots of their own, and the MMAs read A from tensor
-    // memory (or the ring) and B from those slots.  The tensor memory holds
-    // one accumulator slot (one tile per CTA) and kTW weight blocks: 256
-    // columns, so two CTAs (the running launch's and the next one's) still
-    // share an SM's tensor memory.
-    static constexpr int kTW = TS ? 7 : 0;
-    static constexpr int kNB = TS ? kTW + STAGES : 0;   // K blocks per CTA the variant takes
-    static constexpr uint32_t kTWCol0 = kSlotCols;      // weight blocks after accumulator slot 0
-    static constexpr int kBSlots = TS ? kNB : STAGES;
     static constexpr uint32_t kStageTx = TWO_SM ? 2u * (kABytes + kBBytes)
-                                                : (FQ || TS ? kABytes : (W16 ? kLSlotBytes : kABytes + kBBytes + kSABytes));
+                                                : (FQ ? kABytes : (W16 ? kLSlotBytes : kABytes + kBBytes + kSABytes));
     // Two accumulator slots (+ W16: the bf16 A tiles of the ring stages, 128
     // K values = 64 columns each), allocated as a power of two >= 32 columns.
     static constexpr uint32_t kATmemCol0 = 2u * kSlotCols;
     static constexpr uint32_t kATmemCols = 64u;
-    static constexpr uint32_t kTmemNeed = TS ? kTWCol0 + kTW * 32u : kATmemCol0 + (W16 ? STAGES * kATmemCols : 0u);
+    static constexpr uint32_t kTmemNeed = kATmemCol0 + (W16 ? STAGES * kATmemCols : 0u);
     static constexpr uint32_t kTmemCols = kTmemNeed <= 32 ? 32u : kTmemNeed <= 64 ? 64u
                                         : kTmemNeed <= 128 ? 128u : kTmemNeed <= 256 ? 256u : 512u;
     static constexpr uint32_t kOffA = 0;
     static constexpr uint32_t kOffB = kOffA + STAGES * kABytes;
-    static constexpr uint32_t kOffSA = kOffB + kBSlots * kBBytes;
+    static constexpr uint32_t kOffSA = kOffB + STAGES * kBBytes;
     // Split-K with the swapped (decode) orientation pushes partial rows into
     // the owning CTA's receive buffer: slots for every source rank, each of
     // up to 4*ceil(32/split) rows of BN floats (at most 144 rows in total).
@@ -247,8 +228,7 @@ struct GemmCfg {
     static constexpr uint32_t kOffLand = (128u * kPartStride * 4u + 127u) / 128u * 128u;
     static constexpr uint32_t kLandBytes = kOffX > kOffLand ? kOffX - kOffLand : 0u;
     // full, empty, tfull[2], tempty[2], drain, recv (+ W16: lfull, lempty[kLStages]), workspace chunks
-    // (+ TS: tready[kTW], bfull[kNB])
-    static constexpr uint32_t kNumBars = 2 * STAGES + 6 + 2 * kLStages + kWsBars + kTW + kNB;
+    static constexpr uint32_t kNumBars = 2 * STAGES + 6 + 2 * kLStages + kWsBars;
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr uint32_t kOffCol = (kOffMisc + 16 + 15) / 16 * 16;  // staged column scale, bias
     // Non-swapped tiles store their output through one 2 KB staging buffer
@@ -269,8 +249,6 @@ struct GemmCfg {
     static_assert(!FQ || (BLOCKWISE && SWAP && BN == 16 && !TWO_SM), "fused quantization: blockwise 16-token tiles");
     static_assert(!W16 || (!BLOCKWISE && SWAP && !TWO_SM && !FQ && BN <= 32), "W16: swapped channelwise tiles");
     static_assert(kTmemNeed <= 512, "tensor memory budget exceeded");
-    static_assert(!TS || (SWAP && BN == 16 && !BLOCKWISE && !TWO_SM && !FQ && !W16 && kTmemNeed == 256),
-                  "weights in tensor memory: channelwise swapped 16-token tiles, 256 columns");
 };
 
 // Waits that only give up on the time limit (used while draining).
@@ -547,13 +525,13 @@ __device__ __noinline__ void reduce_split_workspace(const GemmArgs &p, uint8_t *
 }
 
 template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT, bool TWO_SM = false, bool FQ = false,
-          bool W16 = false, bool TS = false>
-__global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ, W16, TS>::kThreads, 1)
+          bool W16 = false>
+__global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ, W16>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sa, const __grid_constant__ CUtensorMap tm_out,
                     const GemmArgs p)
 {
-    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ, W16, TS>;
+    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ, W16>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sA = smem + C::kOffA;
@@ -570,8 +548,6 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
     uint64_t *lfull = recv_full + 1;            // W16: landing slot filled
     uint64_t *lempty = lfull + C::kLStages;     // W16: landing slot read by the converting warps
     uint64_t *ws_bar = lempty + C::kLStages;    // split-K workspace exchange: chunk landed
-    uint64_t *tready = ws_bar + C::kWsBars;     // TS: weight block i in tensor memory
-    uint64_t *bfull = tready + C::kTW;          // TS: activation tile of K block i landed
     constexpr int kLS = C::kLStages > 0 ? C::kLStages : 1;  // (non-W16 builds never use the landing ring)
     float *sRecv = reinterpret_cast<float *>(smem + C::kOffRecv);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
@@ -630,9 +606,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
             // converting warps' arrivals alone publish the stage (its bf16 A
             // tile in tensor memory and its activation B tile).
             mbar_init(&full[s], W16 ? C::kConvWarps : 1 + C::kQuantWarps);
-            // (TS: a ring slot is freed by the epilogue warps that copied its
-            // weights into tensor memory.)
-            mbar_init(&empty[s], TS ? C::kEpiWarps : (BLOCKWISE ? C::kEpiWarps : 0) + C::kIssuers);
+            mbar_init(&empty[s], (BLOCKWISE ? C::kEpiWarps : 0) + C::kIssuers);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], C::kIssuers);
@@ -645,8 +619,6 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
             mbar_init(&lempty[j], C::kConvWarps);
         }
         for (int c = 0; c < C::kWsBars; ++c) mbar_init(&ws_bar[c], 1);
-        for (int j = 0; j < C::kTW; ++j) mbar_init(&tready[j], C::kEpiWarps);
-        for (int j = 0; j < C::kNB; ++j) mbar_init(&bfull[j], 1);
 
         *abort = 0;
         fence_mbar_init();
@@ -682,7 +654,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
     if (push) cluster_arrive_relaxed();
     // Weight slices of the first tile issued before the dependency wait.
     int npre = 0;
-    if (!TS && warp == 0 && lane == 0) {
+    if (warp == 0 && lane == 0) {
         // Every kernel of the library triggers its dependents only after
         // its own dependency wait, so the only kernel that may still run
         // now is the immediate predecessor; the host clears p.preload when
@@ -725,65 +697,10 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
         pol_b = SWAP ? policy_evict_last() : policy_evict_normal();
     }
     if (threadIdx.x == 0) FP8Q_TRACE_AT(p, kTrPrologue);
-    // TS: the weight phase (producer: every weight K block through the ring;
-    // epilogue warps: the first kTW of them into tensor memory), before the
-    // dependency wait unless the previous launch writes the weights.
-    int ts_issued = 0;   // weight loads the producer issued (TS)
-    auto ts_weights = [&]() {
-        if constexpr (TS) {
-            if (cluster_id >= p.num_tiles) return;
-            if (warp == 0) {
-                if (lane == 0) {
-                    int a_t, b_t;
-                    coords(cluster_id, a_t, b_t);
-                    const uint64_t pol_w = policy_evict_first();
-                    for (int i = 0; i < nkb; ++i) {
-                        const int s = i % STAGES, u = i / STAGES;
-                        if (u > 0 && !mbar_wait(&empty[s], static_cast<uint32_t>((u - 1) & 1), abort, p.status)) break;
-                        mbar_arrive_expect_tx(&full[s], C::kABytes);
-                        tma_load_2d(sA + s * C::kABytes, &tm_a, &full[s], (kb_begin + i) * 128, a_t * 128, pol_w);
-                        ++ts_issued;
-                    }
-                }
-                __syncwarp();
-            } else if (warp >= C::kEpiWarp0 && warp < C::kEpiWarp0 + C::kEpiWarps) {
-                const int quarter = warp & 3;
-                const int m = quarter * 32 + lane;   // weight row of the tile = TMEM lane
-                const int nt = nkb < C::kTW ? nkb : C::kTW;
-                for (int i = 0; i < nt; ++i) {
-                    const int s = i % STAGES, u = i / STAGES;
-                    const bool got = mbar_wait(&full[s], static_cast<uint32_t>(u & 1), abort, p.status);
-                    if (!__all_sync(0xffffffffu, got)) break;
-                    // Row m's 128 bytes: 16-byte unit q at position q ^ (m & 7)
-                    // (the TMA's 128-byte swizzle); word w of unit q holds
-                    // K = 16 q + 4 w .. + 3, lowest K in the lowest byte.
-                    const uint8_t *row = sA + s * C::kABytes + m * 128;
-                    uint32_t o[32];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const uint4 v = *reinterpret_cast<const uint4 *>(row + ((q ^ (m & 7)) << 4));
-                        o[4 * q] = v.x; o[4 * q + 1] = v.y; o[4 * q + 2] = v.z; o[4 * q + 3] = v.w;
-                    }
-                    tmem_st32(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + C::kTWCol0 +
-                                  static_cast<uint32_t>(i * 32),
-                              o);
-                    tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(&tready[i]);
-                        mbar_arrive(&empty[s]);
-                    }
-                }
-            }
-        }
-    };
-    if (TS && p.preload) ts_weights();
     // Everything below may read the previous kernel's output (activations,
     // scales) or overwrite buffers it reads (out).
     pdl_wait();
     pdl_trigger();
-    if (TS && !p.preload) ts_weights();
     if (threadIdx.x == 0) FP8Q_TRACE_AT(p, kTrPdlWait);
     if constexpr (C::kRegSplit) {
         if (warp < 4) setmaxnreg_dec<C::kLowRegs>();
@@ -794,23 +711,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
         // ------------------------------------------------------------------
         // TMA producer
         // ------------------------------------------------------------------
-        if constexpr (TS) {
-            // The activation tiles of the CTA's K blocks into slots of their
-            // own, then drain: every copy into this CTA has landed before exit.
-            if (lane == 0 && cluster_id < p.num_tiles) {
-                int a_t, b_t;
-                coords(cluster_id, a_t, b_t);
-                for (int i = 0; i < nkb; ++i) {
-                    mbar_arrive_expect_tx(&bfull[i], C::kBBytes);
-                    tma_load_2d(sB + i * C::kBBytes, &tm_b, &bfull[i], (kb_begin + i) * 128, b_t * BN, pol_b);
-                }
-                for (int i = 0; i < nkb; ++i) mbar_wait_drain(&bfull[i], 0, p.status);
-                for (int st = 0; st < STAGES && st < ts_issued; ++st) {
-                    const int last = st + ((ts_issued - 1 - st) / STAGES) * STAGES;   // last block loaded into slot st
-                    mbar_wait_drain(&full[st], static_cast<uint32_t>((last / STAGES) & 1), p.status);
-                }
-            }
-        } else if (lane == 0) {
+        if (lane == 0) {
             uint32_t stage = 0, phase = 0;
             long long issued = 0;
             for (int tile = cluster_id; tile < p.num_tiles; tile += num_clusters) {
@@ -899,42 +800,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
         // steps k of every K block with k % kIssuers == j)
         // ------------------------------------------------------------------
         const int issuer = warp - 1;
-        if constexpr (TS) {
-            // K block i: A from tensor memory (i < kTW) or its ring slot, B
-            // from activation slot i; this issuer's K steps into its own
-            // accumulator columns of slot 0.
-            if (lane == 0 && cluster_id < p.num_tiles) {
-                bool ok = true;
-                for (int i = 0; i < nkb && ok; ++i) {
-                    const bool in_tmem = i < C::kTW;
-                    ok = mbar_wait(&bfull[i], 0, abort, p.status) &&
-                         (in_tmem ? mbar_wait(&tready[i], 0, abort, p.status)
-                                  : mbar_wait(&full[i % STAGES], static_cast<uint32_t>((i / STAGES) & 1), abort,
-                                              p.status));
-                    if (!ok) break;
-                    tc_fence_after();
-                    if (i == 0 && issuer == 0) FP8Q_TRACE_AT(p, kTrFirstMma);
-                    const uint32_t b_addr = smem_u32(sB + i * C::kBBytes);
-                    const uint32_t a_addr = smem_u32(sA + (i % STAGES) * C::kABytes);
-                    const uint32_t d = tmem_base + static_cast<uint32_t>(issuer * BN);
-#pragma unroll
-                    for (int k = 0; k < C::kKSteps; ++k) {
-                        if (C::kIssuers > 1 && k % C::kIssuers != issuer) continue;
-                        const uint32_t acc = (i > 0 || k >= C::kIssuers) ? 1u : 0u;
-                        if (in_tmem)
-                            umma_e4m3_tmem_a(d, tmem_base + C::kTWCol0 + static_cast<uint32_t>(i * 32 + k * 8),
-                                             umma_desc_sw128(b_addr + k * 32), C::kIdesc, acc);
-                        else
-                            umma_e4m3(d, umma_desc_sw128(a_addr + k * 32), umma_desc_sw128(b_addr + k * 32),
-                                      C::kIdesc, acc);
-                    }
-                }
-                if (ok) umma_commit(&tfull[0]);
-                if (issuer == 0) FP8Q_TRACE_AT(p, kTrLastCommit);
-                umma_commit(drain);
-                mbar_wait_drain(drain, 0, p.status);
-            }
-        } else if (lane == 0 && (!TWO_SM || leader)) {
+        if (lane == 0 && (!TWO_SM || leader)) {
             uint32_t stage = 0, phase = 0, slot = 0, tphase = 0;
             bool ok = true;
             for (int tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {

@@ -14,11 +14,11 @@ namespace fp8q {
 constexpr int kMaxDevices = 64;
 
 template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT, bool TWO_SM = false, bool FQ = false,
-          bool W16 = false, bool TS = false>
+          bool W16 = false>
 cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigned *status, cudaStream_t st)
 {
-    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ, W16, TS>;
-    auto kernel = fp8_gemm_kernel<SWAP, BN, STAGES, BLOCKWISE, OutT, TWO_SM, FQ, W16, TS>;
+    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ, W16>;
+    auto kernel = fp8_gemm_kernel<SWAP, BN, STAGES, BLOCKWISE, OutT, TWO_SM, FQ, W16>;
 
     static std::atomic<uint64_t> attr_done[kMaxDevices / 64 + 1];
     int dev = 0;

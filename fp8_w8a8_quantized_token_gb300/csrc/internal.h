@@ -29,7 +29,6 @@ struct GemmLaunch {
     int stages;        // pipeline depth the instantiation uses
     bool pair;         // non-swapped channelwise, split 1: 2-CTA clusters on adjacent token tiles
     bool two_sm;       // the pair computes 256-token tiles with 2-CTA MMAs (always with pair)
-    bool tmem_staged;  // channelwise 16-token decode tiles with the weights staged in tensor memory
 };
 
 struct GemmProblem {
@@ -88,13 +87,6 @@ constexpr int kW16Stages = 3;
 // Ring depth of the 2-CTA MMA instantiation (each slot: 16 KB of tokens +
 // 16 KB, the CTA's half, of weight rows).
 constexpr int kTwoSmStages = 6;
-
-// Weights staged in tensor memory (16-token decode tiles): a ring of 4
-// weight slots carries the CTA's K blocks into 7 tensor-memory blocks (the
-// K blocks past the 7th stay in their ring slot), so a CTA takes at most
-// 7 + 4 K blocks.
-constexpr int kTmemStagedStages = 4;
-constexpr int kTmemStagedMaxKb = 7 + kTmemStagedStages;
 
 // True if an instantiation exists for (swap_ab, mma_n).
 constexpr bool gemm_shape_supported(bool swap_ab, int mma_n)

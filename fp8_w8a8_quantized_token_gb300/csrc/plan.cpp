@@ -160,15 +160,7 @@ void plan_finish(int64_t M, int64_t N, int64_t K, int blockwise, int num_sms, fp
         pl->persistent = tiles > num_sms ? 1 : 0;
     }
     pl->two_sm = pl->pair;
-    // Channelwise 16-token decode tiles with one tile per CTA and at most
-    // kTmemStagedMaxKb K blocks per CTA stage their weights in tensor memory
-    // before the dependency wait (FP8Q_NO_TMEM_STAGING=1 turns this off).
-    static const bool no_ts = getenv("FP8Q_NO_TMEM_STAGING") != nullptr && getenv("FP8Q_NO_TMEM_STAGING")[0] == '1';
-    const int64_t kb_per_cta = (num_kb + split - 1) / split;
-    pl->tmem_staged = (!blockwise && pl->swap_ab && pl->mma_n == 16 && !pl->persistent &&
-                       kb_per_cta <= kTmemStagedMaxKb && !no_ts) ? 1 : 0;
-    pl->stages = pl->two_sm ? kTwoSmStages
-                            : (pl->tmem_staged ? kTmemStagedStages : stages_for(pl->swap_ab != 0, pl->mma_n));
+    pl->stages = pl->two_sm ? kTwoSmStages : stages_for(pl->swap_ab != 0, pl->mma_n);
 }
 
 }  // namespace fp8q

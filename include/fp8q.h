@@ -407,10 +407,6 @@ typedef struct {
                            tile with 2-CTA MMAs (tcgen05 cta_group::2), each
                            CTA loading only its half of the weight rows
                            (always equal to pair) */
-    int32_t tmem_staged; /* 1: channelwise 16-token decode tiles whose CTAs
-                           copy all their weight K blocks into tensor memory
-                           (and the ring) before waiting for the previous
-                           kernel; the MMAs read the weights from there */
 } fp8q_plan;
 
 FP8Q_API fp8q_status fp8q_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t blockwise, int32_t num_sms,

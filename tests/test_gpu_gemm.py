@@ -93,69 +93,6 @@ def test_split_k_workspace_exchange_equals_dsmem_exchange(dev):
     assert r.returncode == 0 and "workspace exchange ok" in r.stdout, r.stdout[-3000:] + r.stderr[-3000:]
 
 
-# Decode tiles with the weights staged in tensor memory: K blocks per CTA
-# 1, 7 (the tensor-memory capacity), 8 and 11 (7 in tensor memory, the rest
-# read from the ring), ragged N (392) and a ragged last K block (K % 128).
-TMEM_STAGED = [(1, 4096 // 32, 1), (13, 7 * 128, 1), (16, 8 * 128 - 48, 1), (5, 11 * 128, 1), (16, 4 * 11 * 128, 4),
-               (40, 2 * 7 * 128 + 16, 2)]
-
-
-@pytest.mark.parametrize("M,K,split", TMEM_STAGED)
-def test_tmem_staged_decode_tiles(dev, schedule, M, K, split):
-    fq.fp8q_set_plan_override(1, 16, split)
-    N = 392
-    plan = fq.fp8q_gemm_plan(M, N, K)
-    assert plan["tmem_staged"] == 1 and plan["split_k"] == split
-    out, ref = channelwise_case(dev, M, N, K, seed=M + K, bias=True)
-    assert_gemm_close(out_values(out), ref, f"tmem-staged M={M} K={K} split={split}")
-    assert fq.fp8q_device_status() == fq.FP8Q_OK
-
-
-TMEM_STAGING_OFF_SCRIPT = r"""
-import sys, torch
-sys.path.insert(0, %r)
-sys.path.insert(0, %r)
-import fp8_w8a8_quantized_token_gb300 as fq, synthetic
-dev = torch.device("cuda", 0)
-outs = {}
-for (M, K, split) in %r:
-    fq.fp8q_set_plan_override(1, 16, split)
-    assert fq.fp8q_gemm_plan(M, 392, K)["tmem_staged"] == 0
-    x = synthetic.activations(M, K, seed=M + K, outliers=True)
-    w = synthetic.weights(392, K, seed=M + K)
-    xq, xs = fq.fp8q_quant_per_token(x.to(dev))
-    wq, ws = fq.fp8q_quant_per_token(w.to(dev))
-    outs[(M, K, split)] = fq.fp8q_scaled_mm_channelwise(xq, wq, xs, ws).cpu()
-torch.save(outs, %r)
-print("staging off ok")
-"""
-
-
-def test_tmem_staged_equals_ring_only_decode(dev, schedule, tmp_path):
-    """The MMAs read the same weights from tensor memory as from the ring, in
-    the same order: outputs bit-identical to a process started with
-    FP8Q_NO_TMEM_STAGING=1 (read at start-up)."""
-    import os
-    import subprocess
-    import sys
-    here = os.path.dirname(os.path.abspath(__file__))
-    path = str(tmp_path / "ring_only.pt")
-    script = TMEM_STAGING_OFF_SCRIPT % (os.path.dirname(here), here, TMEM_STAGED, path)
-    r = subprocess.run([sys.executable, "-c", script], capture_output=True, text=True, timeout=600,
-                       env=dict(os.environ, FP8Q_NO_TMEM_STAGING="1"))
-    assert r.returncode == 0 and "staging off ok" in r.stdout, r.stdout + r.stderr
-    ring_only = torch.load(path)
-    for (M, K, split), ref in ring_only.items():
-        fq.fp8q_set_plan_override(1, 16, split)
-        assert fq.fp8q_gemm_plan(M, 392, K)["tmem_staged"] == 1
-        x = synthetic.activations(M, K, seed=M + K, outliers=True)
-        w = synthetic.weights(392, K, seed=M + K)
-        xq, xs = fq.fp8q_quant_per_token(x.to(dev))
-        wq, ws = fq.fp8q_quant_per_token(w.to(dev))
-        out = fq.fp8q_scaled_mm_channelwise(xq, wq, xs, ws).cpu()
-        assert torch.equal(out, ref), (M, K, split)
-
-
 @pytest.mark.parametrize("M", [1, 2, 5, 16, 33, 64, 100, 128, 129, 256, 300, 512])
 def test_channelwise_default_plan(dev, M):
     out, ref = channelwise_case(dev, M, 384, 1024, seed=M)
