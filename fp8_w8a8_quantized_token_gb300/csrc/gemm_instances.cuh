@@ -1,6 +1,7 @@
 // gemm_instances.cuh -- the instantiations a translation unit provides:
-// swapped (decode) tiles of 16/32/64/128 tokens and non-swapped (prefill)
-// tiles of 128 tokens x 256 output columns, bf16 or fp16 output.
+// swapped (decode) tiles of 16/32/64/128 tokens and non-swapped tiles of
+// 128 tokens x 256 output columns (prefill; 2-CTA pairs for channelwise)
+// or 128 / 64 / 32 columns (mid-size M), bf16 or fp16 output.
 #pragma once
 
 #include "gemm_launch.cuh"
@@ -36,12 +37,18 @@ cudaError_t dispatch_gemm(const GemmProblem &p, const GemmLaunch &l, unsigned *s
             default: return cudaErrorInvalidValue;
         }
     }
-    if (l.mma_n == 256) {
-        if constexpr (!BLOCKWISE)
-            if (l.pair && l.two_sm) return launch_gemm_inst<false, 256, kTwoSmStages, false, OutT, true>(p, l, status, st);
-        return launch_gemm_inst<false, 256, stages_for(false, 256), BLOCKWISE, OutT>(p, l, status, st);
+    switch (l.mma_n) {
+        case 256:
+            if constexpr (!BLOCKWISE)
+                if (l.pair && l.two_sm)
+                    return launch_gemm_inst<false, 256, kTwoSmStages, false, OutT, true>(p, l, status, st);
+            return launch_gemm_inst<false, 256, stages_for(false, 256), BLOCKWISE, OutT>(p, l, status, st);
+        // Narrow weight tiles: mid-size M with one tile per CTA and no K split.
+        case 128: return launch_gemm_inst<false, 128, stages_for(false, 128), BLOCKWISE, OutT>(p, l, status, st);
+        case 64: return launch_gemm_inst<false, 64, stages_for(false, 64), BLOCKWISE, OutT>(p, l, status, st);
+        case 32: return launch_gemm_inst<false, 32, stages_for(false, 32), BLOCKWISE, OutT>(p, l, status, st);
+        default: return cudaErrorInvalidValue;
     }
-    return cudaErrorInvalidValue;
 }
 
 }  // namespace fp8q

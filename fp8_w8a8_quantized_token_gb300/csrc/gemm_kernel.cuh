@@ -1143,7 +1143,20 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                             uint32_t r[32];
                             tmem_ld16(taddr + ch * 32, *reinterpret_cast<uint32_t(*)[16]>(r));
                             tmem_ld16(taddr + ch * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
-                            tmem_ld_wait();
+                            if constexpr (C::kIssuers > 1) {
+                                // Tiles narrower than 256 columns: the second
+                                // issuer's accumulator (BN columns on), added
+                                // in issuer order.
+                                uint32_t r2[32];
+                                tmem_ld16(taddr + BN + ch * 32, *reinterpret_cast<uint32_t(*)[16]>(r2));
+                                tmem_ld16(taddr + BN + ch * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(r2 + 16));
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
+                            } else {
+                                tmem_ld_wait();
+                            }
                             const int cb = col0 + ch * 32;
                             if (partial) {
                                 float *dst = sRed + row * C::kPartStride + cb;

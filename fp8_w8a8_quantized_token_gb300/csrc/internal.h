@@ -70,7 +70,8 @@ cudaError_t launch_gemm_blockwise(const GemmProblem &p, const GemmLaunch &l, uns
 // prefetch) on SMs still running the previous layer's tail.
 constexpr int stages_for(bool swap_ab, int mma_n)
 {
-    return swap_ab ? (mma_n == 16 ? 5 : mma_n == 32 ? 4 : mma_n == 64 ? 7 : 4) : 4;
+    return swap_ab ? (mma_n == 16 ? 5 : mma_n == 32 ? 4 : mma_n == 64 ? 7 : 4)
+                   : (mma_n == 256 ? 4 : mma_n == 128 ? 6 : 8);
 }
 
 // Ring depth of the fused-quantization instantiation (blockwise, 16-token
@@ -91,7 +92,8 @@ constexpr int kTwoSmStages = 6;
 // True if an instantiation exists for (swap_ab, mma_n).
 constexpr bool gemm_shape_supported(bool swap_ab, int mma_n)
 {
-    return swap_ab ? (mma_n == 16 || mma_n == 32 || mma_n == 64 || mma_n == 128) : (mma_n == 256);
+    return swap_ab ? (mma_n == 16 || mma_n == 32 || mma_n == 64 || mma_n == 128)
+                   : (mma_n == 32 || mma_n == 64 || mma_n == 128 || mma_n == 256);
 }
 
 // ---- tensor maps (host_util.cu) ------------------------------------------------

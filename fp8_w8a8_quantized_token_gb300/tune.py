@@ -49,6 +49,10 @@ def candidates(M: int):
     # Weights on the MMA's N side: half the MMA instructions of 128-row
     # weight tiles (a tcgen05.mma costs the same whatever its N).
     c += [(0, 256, s) for s in ((1, 2, 4) if M > 1024 else SPLITS)]
+    # Narrow weight tiles (mid-size M: enough tiles for every SM without a
+    # K split).
+    if 64 <= M <= 2048:
+        c += [(0, n, s) for n in (32, 64, 128) for s in (1, 2)]
     return c
 
 

@@ -414,7 +414,7 @@ FP8Q_API fp8q_status fp8q_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t blo
 
 /* Force the schedule of every following GEMM in this process (for tests
  * and tuning sweeps): swap_ab in {0, 1} with an mma_n that has a kernel
- * instantiation (swapped: 16, 32, 64, 128; non-swapped: 256) and
+ * instantiation (swapped: 16, 32, 64, 128; non-swapped: 32, 64, 128, 256) and
  * split_k >= 1 (clamped to 8 and to the number of 128-wide K blocks).
  * swap_ab < 0 removes the override.  Errors: INVALID_ARG for a
  * combination without an instantiation.  Not thread-safe with concurrent

@@ -114,7 +114,7 @@ def test_invalid_arguments_are_rejected_before_any_cuda_call(lib):
 
 def test_plan_override_validation(lib):
     assert lib.fp8q_set_plan_override(1, 48, 1) == fq.FP8Q_ERR_INVALID_ARG
-    assert lib.fp8q_set_plan_override(0, 128, 1) == fq.FP8Q_ERR_INVALID_ARG
+    assert lib.fp8q_set_plan_override(0, 16, 1) == fq.FP8Q_ERR_INVALID_ARG
     assert lib.fp8q_set_plan_override(1, 32, 0) == fq.FP8Q_ERR_INVALID_ARG
     assert lib.fp8q_set_plan_override(1, 32, 3) == fq.FP8Q_OK
     p = fq.fp8q_gemm_plan(7, 4096, 4096, num_sms=148)

@@ -18,7 +18,8 @@ from gpu_util import (THREADS, assert_gemm_close, out_values, quant_both_group, 
 pytestmark = pytest.mark.gpu
 
 SCHEDULES = [(1, 16, 1), (1, 16, 3), (1, 16, 5), (1, 32, 2), (1, 32, 8), (1, 64, 1), (1, 64, 4), (1, 64, 7),
-             (1, 128, 1), (1, 128, 2), (1, 128, 6), (0, 256, 1), (0, 256, 2), (0, 256, 5)]
+             (1, 128, 1), (1, 128, 2), (1, 128, 6), (0, 256, 1), (0, 256, 2), (0, 256, 5),
+             (0, 128, 1), (0, 128, 3), (0, 64, 1), (0, 64, 2), (0, 32, 1), (0, 32, 4)]
 
 
 @pytest.fixture(scope="module")

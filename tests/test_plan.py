@@ -9,7 +9,7 @@ import pytest
 import fp8_w8a8_quantized_token_gb300 as fq
 from fp8_w8a8_quantized_token_gb300 import build as fbuild
 
-SUPPORTED = {(1, 16), (1, 32), (1, 64), (1, 128), (0, 256)}
+SUPPORTED = {(1, 16), (1, 32), (1, 64), (1, 128), (0, 32), (0, 64), (0, 128), (0, 256)}
 SMEM_LIMIT = 232448
 
 
