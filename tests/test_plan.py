@@ -44,8 +44,9 @@ def test_plans_are_launchable(num_sms):
         num_kb = -(-K // 128)
         assert 1 <= p["split_k"] <= min(8, num_kb)
         m_tiles = -(-M // p["tile_m"])
-        # channelwise 256-column tiles pair up (blockwise tiles never do)
-        assert p["pair"] == int(not bw and not p["swap_ab"] and p["split_k"] == 1 and m_tiles >= 2)
+        # channelwise 256-column tiles pair up (blockwise and narrower tiles never do)
+        assert p["pair"] == int(not bw and not p["swap_ab"] and p["mma_n"] == 256 and p["split_k"] == 1
+                                and m_tiles >= 2)
         if p["pair"]:
             # 2-CTA clusters over pairs of token tiles (an odd last tile pairs
             # with an empty one), at most one pair per two SMs
