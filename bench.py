@@ -53,6 +53,7 @@ PROFILE_CASES = {
     "prefill_gateup": ("channelwise", 8192, 24576, 4096),
     "mid_oproj_256": ("channelwise", 256, 4096, 4096),
     "mid_oproj_512": ("channelwise", 512, 4096, 4096),
+    "mid_qkv_128": ("channelwise", 128, 6144, 4096),
     "mid_oproj_1024": ("channelwise", 1024, 4096, 4096),
     "decode_oproj": ("channelwise", 16, 4096, 4096),
     "decode_down": ("channelwise", 1, 4096, 12288),
