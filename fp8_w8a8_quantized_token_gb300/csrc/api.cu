@@ -77,7 +77,9 @@ fp8q_status fp8q_quant_per_token(const void *x, int64_t M, int64_t K, int64_t ld
 {
     const fp8q_status s = check_quant_common(x, M, K, ldx, xq, x_scale, eps);
     if (s != FP8Q_OK || M == 0) return s;
-    const cudaError_t e = launch_quant_per_token(x, M, K, ldx, xq, x_scale, eps, as_stream(stream));
+    unsigned *status = device_status_ptr();
+    if (status == nullptr) return FP8Q_ERR_CUDA;
+    const cudaError_t e = launch_quant_per_token(x, M, K, ldx, xq, x_scale, eps, status, as_stream(stream));
     if (e == cudaSuccess) note_launch_writes(as_stream(stream), xq, static_cast<size_t>(M) * K);
     return from_cuda(e);
 }

@@ -101,6 +101,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// Waits that only give up on the time limit (used while draining copies in
+// flight before a CTA exits, after an abort as well).
+__device__ __forceinline__ void mbar_wait_drain(uint64_t *bar, uint32_t parity, unsigned *status)
+{
+    const uint32_t a = smem_u32(bar);
+    const unsigned long long t0 = globaltimer_ns();
+    while (!mbar_try_wait(a, parity)) {
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            atomicOr(status, kStatusTimeout);
+            return;
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // cp.async: 16-byte asynchronous global -> shared copies (not via the TMA
 // unit), tracked per thread in commit groups.  src_bytes < 16 zero-fills the
@@ -209,6 +223,17 @@ __device__ __forceinline__ void bulk_load_global(void *dst, const void *src, uin
                      smem_u32(dst)),
                  "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
+}
+
+// bulk_load_global with an L2 cache policy (createpolicy) for the source.
+__device__ __forceinline__ void bulk_load_global_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                                      uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
 }
 
 // Order this thread's async-proxy (bulk copy) accesses to global memory

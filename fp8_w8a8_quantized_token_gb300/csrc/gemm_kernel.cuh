@@ -251,19 +251,6 @@ struct GemmCfg {
     static_assert(kTmemNeed <= 512, "tensor memory budget exceeded");
 };
 
-// Waits that only give up on the time limit (used while draining).
-__device__ __forceinline__ void mbar_wait_drain(uint64_t *bar, uint32_t parity, unsigned *status)
-{
-    const uint32_t a = smem_u32(bar);
-    const unsigned long long t0 = globaltimer_ns();
-    while (!mbar_try_wait(a, parity)) {
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-            atomicOr(status, kStatusTimeout);
-            return;
-        }
-    }
-}
-
 __device__ __forceinline__ uint64_t policy_evict_normal()
 {
     uint64_t p;

@@ -9,8 +9,10 @@
 namespace fp8q {
 
 // ---- quantizers (quant.cu) ------------------------------------------------
+// `status`: the device status word, where the many-row kernel's bounded
+// wait records a timeout.
 cudaError_t launch_quant_per_token(const void *x, int64_t M, int64_t K, int64_t ldx, void *xq, float *xs, float eps,
-                                   cudaStream_t st);
+                                   unsigned *status, cudaStream_t st);
 cudaError_t launch_quant_group(const void *x, int64_t M, int64_t K, int64_t ldx, int group, void *xq, float *xs,
                                int64_t m_pad, float eps, int num_sms, cudaStream_t st, bool ue8m0 = false,
                                bool silu_and_mul = false);

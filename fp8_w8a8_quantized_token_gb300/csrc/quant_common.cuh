@@ -104,6 +104,25 @@ __device__ __forceinline__ uint4 quant_chunk(const Chunk16 &c, float s)
 
 __device__ __forceinline__ float scale_of(float amax, float eps) { return fmaxf(amax, eps) / 448.0f; }
 
+// The same operations on 8-value units (one 16-byte word of bf16): the
+// running max of |x| kept as a bf16 pair (exact, NaN-ignoring as above), and
+// the codes of 8 values for a scale s with r = RN(1 / s), or, where s is not
+// a normal finite number, by the IEEE division (as quant_chunk does).
+__device__ __forceinline__ __nv_bfloat162 unit_amax2(const uint4 &v, __nv_bfloat162 acc)
+{
+    const __nv_bfloat162 a = __hmax2(__habs2(as_bf2(v.x)), __habs2(as_bf2(v.y)));
+    const __nv_bfloat162 b = __hmax2(__habs2(as_bf2(v.z)), __habs2(as_bf2(v.w)));
+    return __hmax2(acc, __hmax2(a, b));
+}
+
+__device__ __forceinline__ bool scale_has_reciprocal(float s) { return s >= 0x1p-126f && s <= 3.0e38f; }
+
+__device__ __forceinline__ uint2 quant_unit8(const uint4 &v, float s, float r, bool recip)
+{
+    if (recip) return make_uint2(quant4(v.x, v.y, s, r), quant4(v.z, v.w, s, r));
+    return make_uint2(quant4_div(v.x, v.y, s), quant4_div(v.z, v.w, s));
+}
+
 // 16 consecutive bf16 values from shared memory (16-byte aligned).
 __device__ __forceinline__ Chunk16 load_chunk_smem(const void *p)
 {

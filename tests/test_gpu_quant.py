@@ -29,6 +29,13 @@ def dev():
     # many rows: the four-chunks-per-thread configuration, whole and ragged
     # last thread (K = 4112: 257 chunks over 96 threads)
     (1024, 4096, True), (1500, 4112, True), (1031, 12288, False), (1024, 48, False),
+    # 4096 rows and more: one bulk copy of each row into shared memory; 64
+    # threads of 8 units at K = 4096, ragged unit counts (K = 4112: 514 units
+    # over 96 threads; K = 48: 6 units, one warp), 256 threads at the longest
+    # bulk row (K = 16384), and the next longer row back on the
+    # four-chunks-per-thread kernel (K = 16400)
+    (4096, 4096, True), (4099, 4112, True), (4100, 48, False), (4096, 7168, True), (4096, 16384, False),
+    (4096, 16400, False),
 ])
 def test_per_token_bit_exact(dev, M, K, outliers):
     x = synthetic.activations(M, K, seed=M * 7 + K, outliers=outliers)
@@ -48,6 +55,29 @@ def test_per_token_strided_input_and_no_overrun(dev):
     assert np.array_equal(u8(xq)[:M], rq)
     assert np.array_equal(xs.cpu().numpy()[:M], rs)
     assert np.all(u8(xq)[M] == 0x5A) and np.all(xs.cpu().numpy()[M:] == -1.0)
+
+
+def test_many_rows_strided_input_and_no_overrun(dev):
+    """Many-row quantization of a strided input (the per-token kernel's bulk
+    row copies start at row * ldx); rows and scales beyond M are never
+    written (per-token and group-128)."""
+    M, K, ldx = 4100, 1024, 1536
+    big = synthetic.activations(M, ldx, seed=13, outliers=True)
+    x_gpu = big.to(dev)[:, :K]
+    xq = torch.empty((M + 1, K), dtype=fq.E4M3, device=dev)
+    xq.view(torch.uint8).fill_(0x5A)
+    xs = torch.full((M + 4,), -1.0, dtype=torch.float32, device=dev)
+    fq.fp8q_quant_per_token(x_gpu, xq=xq[:M], x_scale=xs)
+    torch.cuda.synchronize()
+    rq, rs = oracle.quant_per_token(big[:, :K].contiguous(), threads=THREADS)
+    assert np.array_equal(u8(xq)[:M], rq)
+    assert np.array_equal(xs.cpu().numpy()[:M], rs)
+    assert np.all(u8(xq)[M] == 0x5A) and np.all(xs.cpu().numpy()[M:] == -1.0)
+    gq, gsv = fq.fp8q_quant_per_token_group_row_padded(x_gpu, 128)
+    torch.cuda.synchronize()
+    rq, rs = oracle.quant_group_row_padded(big[:, :K].contiguous(), 128, threads=THREADS)
+    assert np.array_equal(u8(gq)[:M], rq[:M])
+    assert np.array_equal(gsv.transpose(0, 1).cpu().numpy()[:, :M], rs[:, :M])
 
 
 def test_per_token_special_rows(dev):
@@ -93,12 +123,36 @@ def test_quotients_on_e4m3_rounding_midpoints(dev):
     quant_both_group(x, dev, 128)
 
 
+def test_special_tie_and_tiny_scale_rows_in_many_row_launches(dev):
+    """The special rows, the midpoint rows and rows with zero or subnormal
+    scales, repeated into launches of 4096 rows and more, so that the
+    many-row (bulk copy) kernel quantizes them too."""
+    special = torch.zeros((8, 256), dtype=torch.float32)
+    special[1, 3] = 1e-12
+    special[2] = torch.linspace(-448, 448, 256)
+    special[3, :] = -0.0
+    special[4, 0] = 3e38
+    special[4, 1:] = -torch.linspace(1, 2, 255)
+    special[5] = torch.tensor([(-1) ** i * 2.0 ** (-(i % 20)) for i in range(256)])
+    special[6, 7] = 1e-40
+    special[7, :3] = torch.tensor([3e-39, -2e-38, 5e-40])
+    rows = torch.cat([special.to(torch.bfloat16), _tie_rows(256)])
+    x = rows.repeat((4100 + rows.shape[0] - 1) // rows.shape[0], 1)[:4100].contiguous()
+    quant_both_per_token(x, dev)
+    for eps in (1e-44, 1e-41):
+        q, sc = fq.fp8q_quant_per_token(x.to(dev), eps=eps)
+        torch.cuda.synchronize()
+        rq, rs = oracle.quant_per_token(x, eps=eps, threads=THREADS)
+        assert np.array_equal(u8(q), rq)
+        assert np.array_equal(sc.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+
+
 def test_every_bf16_significand_under_many_scales(dev):
     """Rows with scales over a wide exponent range; every row holds values
     of all 128 bf16 significands, both signs, at many exponents below its
     amax (and signed zeros), so each quotient pattern meets many scales."""
     rng = np.random.default_rng(77)
-    M, K = 1024, 2048
+    M, K = 4096, 2048   # the many-row per-token kernel
     amax_exp = rng.integers(-30, 30, M)
     amax = (1.0 + rng.integers(0, 128, M) / 128.0) * 2.0 ** amax_exp
     sig = np.tile(np.arange(128), K // 128)[None, :] + np.zeros((M, 1), dtype=np.int64)

@@ -61,6 +61,23 @@ def test_group_variants_bit_exact(dev, g, ue8m0, silu, M, K):
     _group_both(x, dev, g, ue8m0, silu)
 
 
+@pytest.mark.parametrize("g", [16, 32, 64, 128])
+@pytest.mark.parametrize("ue8m0", [False, True])
+def test_group_many_rows_bit_exact(dev, g, ue8m0):
+    """Every group size and scale format at many rows (K = 3200, not a
+    multiple of the 256-thread grid stride), padding rows (row_alignment 8)
+    left untouched."""
+    M, K = 1100, 3200
+    x = synthetic.activations(M, K, outliers=True, seed=g * 3 + ue8m0)
+    _group_both(x, dev, g, ue8m0, False, row_alignment=8)
+
+
+def test_group_many_rows_short_rows(dev):
+    """K = 48 with g = 16: six units per row, three groups, 26 idle lanes."""
+    x = synthetic.activations(1030, 48, outliers=True, seed=5)
+    _group_both(x, dev, 16, False, False)
+
+
 def test_silu_every_bf16_gate_value(dev):
     """All 63488 finite bf16 gate values (up = 1): with groups of 16 the
     scales expose max|silu(gate)| of every group bit-exactly, the codes the
