@@ -330,14 +330,14 @@ def run_profile_case(name: str) -> int:
         elif kind == "channelwise":
             wq, ws = fq.fp8q_quant_per_token(w)
             xq, xs = fq.fp8q_quant_per_token(x)
-            work = torch.empty(max(1, fq.fp8q_workspace_bytes(M, N, K)), dtype=torch.uint8, device=dev)
+            work = torch.zeros(max(1, fq.fp8q_workspace_bytes(M, N, K)), dtype=torch.uint8, device=dev)
             torch.cuda.synchronize()
             for _ in range(n):
                 fq.fp8q_scaled_mm_channelwise(xq, wq, xs, ws, workspace=work)
         else:
             wq, ws = fq.fp8q_quant_weight_block128(w)
             xq, xsv = fq.fp8q_quant_per_token_group_row_padded(x, 128)
-            work = torch.empty(max(1, fq.fp8q_workspace_bytes(M, N, K, True)), dtype=torch.uint8, device=dev)
+            work = torch.zeros(max(1, fq.fp8q_workspace_bytes(M, N, K, True)), dtype=torch.uint8, device=dev)
             torch.cuda.synchronize()
             for _ in range(n):
                 fq.fp8q_scaled_mm_blockwise(xq, wq, xsv, ws, M=M, workspace=work)
@@ -477,7 +477,7 @@ def build_problems(gpu, workload):
             out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             plan = fq.fp8q_gemm_plan(M, N, K, bw)
             need = fq.fp8q_workspace_bytes(M, N, K, bw)
-            work = torch.empty(need, dtype=torch.uint8, device=dev) if need else None
+            work = torch.zeros(need, dtype=torch.uint8, device=dev) if need else None
             problems.append(dict(label=label, N=N, K=K, bw=bw, M=M, m_pad=m_pad, x=x, xcopies=xcopies, xq=xq,
                                  xs=xs, out=out,
                                  wq=wqs[i % copies], ws=ws0, plan=plan, work=work, work_bytes=need,
@@ -832,7 +832,7 @@ def measure_fused(gpu, peaks, synthetic):
         fxs = torch.empty((fK // 128, fm_pad), dtype=torch.float32, device=dev)
         fout = torch.empty((fM, fN), dtype=torch.bfloat16, device=dev)
         need = fq.fp8q_workspace_bytes(fM, fN, fK, True)
-        work = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        work = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
 
         def body_fused(st, fx=fx, fM=fM, fout=fout):
             for r in range(REPS):
@@ -875,7 +875,7 @@ def measure_w8a16(gpu, peaks, synthetic):
             wxs = torch.empty((wM,), dtype=torch.float32, device=dev)
             wout = torch.empty((wM, wN), dtype=torch.bfloat16, device=dev)
             need = fq.fp8q_workspace_bytes(wM, wN, wK)
-            work = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+            work = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
 
             def body_w16(st, wx=wx, wM=wM, wout=wout, wcp=wcp, wN=wN, wK=wK):
                 for r in range(REPS):

@@ -62,7 +62,7 @@ class Fp8qError(RuntimeError):
 class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("swap_ab", "mma_n", "tile_m", "tile_n", "split_k", "stages", "grid", "persistent", "from_table",
-                 "pair", "two_sm")]
+                 "pair", "two_sm", "stream_k")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -140,9 +140,11 @@ def _on(device: torch.device):
 
 def _workspace(workspace, M: int, N: int, K: int, blockwise: bool, device: torch.device):
     """(pointer, bytes) of the split-K workspace: "auto" allocates what the
-    planned schedule uses (nothing if it does not split K), None passes none
-    (partials then go through distributed shared memory), a uint8 CUDA
-    tensor is used as given."""
+    planned schedule uses (nothing if it does not split K), zero-filled as
+    stream-K schedules require; None passes none (K-split partials then go
+    through distributed shared memory, and stream-K schedules run split
+    along K instead); a uint8 CUDA tensor is used as given (for stream-K it
+    must have been zero-filled once: the GEMM leaves it that way)."""
     if workspace is None:
         return None, 0
     if isinstance(workspace, str):
@@ -152,7 +154,7 @@ def _workspace(workspace, M: int, N: int, K: int, blockwise: bool, device: torch
             nbytes = int(load_library().fp8q_workspace_bytes(M, N, K, int(bool(blockwise))))
         if nbytes == 0:
             return None, 0
-        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=device)
     _need(workspace, torch.uint8, "workspace", device)
     if not workspace.is_contiguous():
         raise ValueError("workspace must be contiguous")

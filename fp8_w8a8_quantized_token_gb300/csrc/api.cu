@@ -42,14 +42,21 @@ fp8q_status launch_planned(GemmProblem p, const fp8q_plan &pl, cudaStream_t st)
     p.preload = !last_launch_writes_overlap(st, p.w, wbytes);
     unsigned *status = device_status_ptr();
     if (status == nullptr) return FP8Q_ERR_CUDA;
+    // Stream-K needs its workspace and exists only for the plain E4M3
+    // kernels; otherwise the same tiles run split along K.
+    fp8q_plan plan = pl;
+    if (plan.stream_k && (p.fused_quant || p.w16 || p.ws == nullptr ||
+                          p.ws_bytes < stream_k_workspace_bytes(plan.grid, plan.mma_n)))
+        plan_without_stream_k(p.M, p.N, p.K, p.blockwise ? 1 : 0, current_device_sms(), &plan);
     GemmLaunch l;
-    l.swap_ab = pl.swap_ab != 0;
-    l.mma_n = pl.mma_n;
-    l.split = pl.split_k;
-    l.grid = pl.grid;
-    l.stages = pl.stages;
-    l.pair = pl.pair != 0;
-    l.two_sm = pl.two_sm != 0;
+    l.swap_ab = plan.swap_ab != 0;
+    l.mma_n = plan.mma_n;
+    l.split = plan.split_k;
+    l.grid = plan.grid;
+    l.stages = plan.stages;
+    l.pair = plan.pair != 0;
+    l.two_sm = plan.two_sm != 0;
+    l.stream_k = plan.stream_k != 0;
     const cudaError_t e = p.blockwise ? launch_gemm_blockwise(p, l, status, st)
                                       : launch_gemm_channelwise(p, l, status, st);
     if (e == cudaSuccess) note_launch_writes(st, p.out, static_cast<size_t>(p.M) * p.N * 2);
@@ -347,6 +354,6 @@ const char *fp8q_status_str(fp8q_status status)
     }
 }
 
-int32_t fp8q_version(void) { return (2 << 16) | 0; }
+int32_t fp8q_version(void) { return (2 << 16) | 1; }
 
 }  // extern "C"

@@ -115,6 +115,45 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t *bar, uint32_t parity, 
     }
 }
 
+// Flags in global memory shared between CTAs of one grid.
+__device__ __forceinline__ void st_release_gpu_u32(unsigned *p, unsigned v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_gpu_u32(unsigned *p, unsigned v)
+{
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu_u32(const unsigned *p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait until *flag != 0 (acquire).  Gives up like mbar_wait: after
+// kWaitTimeoutNs, or as soon as *abort is raised; on giving up it raises
+// *abort, records the timeout in *status and returns false.
+__device__ __forceinline__ bool flag_wait_acquire(const unsigned *flag, volatile int *abort, unsigned *status)
+{
+    if (ld_acquire_gpu_u32(flag) != 0u) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        __nanosleep(32);
+        if (ld_acquire_gpu_u32(flag) != 0u) return true;
+        if ((i & 15u) == 0u) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+                *abort = 1;
+                atomicOr(status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // cp.async: 16-byte asynchronous global -> shared copies (not via the TMA
 // unit), tracked per thread in commit groups.  src_bytes < 16 zero-fills the

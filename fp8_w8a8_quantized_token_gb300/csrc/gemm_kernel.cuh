@@ -59,6 +59,22 @@
 // Both ways add the same values in the same order, so they give identical
 // results.
 //
+// Stream-K (swapped channelwise or blockwise tiles, p.stream_k).  The
+// (tile, K block) pairs are numbered tile-major, T = num_tiles * num_kb of
+// them, and CTA c of G takes the pairs [c*T/G, (c+1)*T/G): every CTA streams
+// the same number of weight blocks whatever the tile count.  A CTA's range
+// is cut at tile boundaries into work units (tile, K blocks [kb0, kb1)); a
+// unit covering the whole tile is stored as usual.  Only a CTA's first unit
+// can start inside a tile: it writes its fp32 partial tile (raw MMA sums;
+// blockwise: the promoted sums) to its workspace slot and publishes it with
+// a release store of its flag.  The unit holding the tile's first K block
+// (the last unit of its CTA, which therefore reaches the tile after the
+// other CTAs have published theirs) waits for the flags of the following
+// CTAs whose ranges start inside the tile (acquire loads, bounded), adds
+// their partials in increasing K order (a fixed order: deterministic),
+// clears the flags for the next launch and stores the tile.  Waits only go
+// to higher CTA indices, so they cannot form a cycle.
+//
 // Every mbarrier wait is bounded (device_common.cuh); a wait that runs out
 // records a timeout in the status word and all roles wind down, waiting
 // (bounded) for their in-flight TMA copies and MMAs before TMEM is freed.
@@ -90,7 +106,10 @@ struct GemmArgs {
     float eps;                  // fused quantization: the amax floor of the group scales
     const __nv_bfloat16 *x;     // fused quantization: bf16 activations [M, K]
     long long ldx;              //   and their row stride (elements)
-    float *ws;                  // split-K workspace: split slots of 128 x BN floats per cluster, or null
+    float *ws;                  // split-K workspace: split slots of 128 x BN floats per cluster, or null;
+                                //   stream-K: one slot of 128 x BN floats per CTA
+    int stream_k;               // 1: stream-K (swapped tiles, one CTA per cluster, see below)
+    unsigned *sk_flags;         // stream-K: one flag per CTA after the slots, 1 = its partial is published
 };
 
 // Phase timestamps of a trace build (-DFP8Q_TRACE): kTraceSlots 64-bit
@@ -129,6 +148,11 @@ struct GemmCfg {
     // file, which lets the next launch's CTAs load their weights while this
     // launch's CTAs finish.)
     static constexpr int kIssuers = (BLOCKWISE || TWO_SM || BN >= 256) ? 1 : 2;
+    // Stream-K: swapped E4M3 tiles of 16 and 32 tokens (not the fused-
+    // quantization or weight-only variants, whose extra warps walk tiles on
+    // their own; wider tiles hold rows of 64 or 128 floats per thread, and the
+    // hand-over code would cost them registers they do not have).
+    static constexpr bool kStreamK = SWAP && BN <= 32 && !TWO_SM && !FQ && !W16;
     static constexpr int kSlotCols = kIssuers * BN;  // TMEM columns per accumulator slot
     // Register split (blockwise 256-column tiles): each epilogue thread
     // promotes 128 accumulator columns every K block, in rounds of (TMEM
@@ -571,6 +595,31 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
     const bool leader = rank == 0;  // TWO_SM: the CTA that issues the MMAs
     // TWO_SM: a ring slot's full barrier in the even CTA (shared::cluster).
     auto lead_full = [&](int stage) { return dsmem_map(smem_u32(&full[stage]), 0u); };
+    // Work units (tile, K blocks [kb0, kb1)), walked in the same order by
+    // every role: the cluster's tiles over this rank's K range, or (stream-K)
+    // this CTA's range of (tile, K block) pairs cut at tile boundaries.
+    const bool sk = C::kStreamK && p.stream_k != 0;
+    const long long sk_total = static_cast<long long>(p.num_tiles) * p.num_kb;
+    const long long sk_g0 = sk ? sk_total * blockIdx.x / gridDim.x : 0;
+    const long long sk_g1 = sk ? sk_total * (blockIdx.x + 1) / gridDim.x : 0;
+    const long long unit_first = sk ? sk_g0 : static_cast<long long>(cluster_id);
+    auto next_unit = [&](long long &cur, int &tile, int &kb0, int &kb1) -> bool {
+        if (sk) {
+            if (cur >= sk_g1) return false;
+            tile = static_cast<int>(cur / p.num_kb);
+            kb0 = static_cast<int>(cur - static_cast<long long>(tile) * p.num_kb);
+            const long long left = sk_g1 - cur;
+            kb1 = left < p.num_kb - kb0 ? kb0 + static_cast<int>(left) : p.num_kb;
+            cur += kb1 - kb0;
+            return true;
+        }
+        if (cur >= p.num_tiles) return false;
+        tile = static_cast<int>(cur);
+        kb0 = kb_begin;
+        kb1 = kb_end;
+        cur += num_clusters;
+        return true;
+    };
 
     // Prologue.  Thread 0 initialises the barriers while warp 1 allocates the
     // TMEM accumulators; one block barrier publishes both.
@@ -649,9 +698,12 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
         // slices stream into the ring right away and the activation slices
         // follow after pdl_wait().  Further weight slices of the first tile
         // are prefetched into L2 (always safe: L2 is the coherence point).
-        if (cluster_id < p.num_tiles) {
+        long long cur0 = unit_first;
+        int t0, u0_kb0, u0_kb1;
+        if (next_unit(cur0, t0, u0_kb0, u0_kb1)) {
+            const int u0_nkb = u0_kb1 - u0_kb0;
             int a_t, b_t;
-            coords(cluster_id, a_t, b_t);
+            coords(t0, a_t, b_t);
             const CUtensorMap *wmap = SWAP ? &tm_a : &tm_b;
             const int wrow = SWAP ? a_t * 128 : b_t * BN;
             // (W16: the E4M3 weight slices land in their own slots.)
@@ -660,19 +712,41 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
             uint64_t *wbar = W16 ? lfull : full;
             const int ring = W16 ? C::kLStages : STAGES;
             const uint64_t pol_w = SWAP ? policy_evict_first() : policy_evict_normal();
-            npre = p.preload ? (nkb < ring ? nkb : ring) : 0;
+            npre = p.preload ? (u0_nkb < ring ? u0_nkb : ring) : 0;
             for (int i = 0; i < npre; ++i) {
                 if (TWO_SM) {
                     if (leader) mbar_arrive_expect_tx(&full[i], C::kStageTx);
-                    tma_load_2d_pair(wbuf + i * wbytes, wmap, lead_full(i), (kb_begin + i) * 128, wrow + w_half_row,
+                    tma_load_2d_pair(wbuf + i * wbytes, wmap, lead_full(i), (u0_kb0 + i) * 128, wrow + w_half_row,
                                      pol_w);
                     continue;
                 }
                 mbar_arrive_expect_tx(&wbar[i], C::kStageTx);
-                tma_load_2d(wbuf + i * wbytes, wmap, &wbar[i], (kb_begin + i) * 128, wrow, pol_w);
+                tma_load_2d(wbuf + i * wbytes, wmap, &wbar[i], (u0_kb0 + i) * 128, wrow, pol_w);
             }
-            const int pf = nkb < p.prefetch_kb ? nkb : p.prefetch_kb;
-            for (int i = npre; i < pf; ++i) tma_prefetch_l2_2d(wmap, (kb_begin + i) * 128, wrow + w_half_row);
+            const int pf = u0_nkb < p.prefetch_kb ? u0_nkb : p.prefetch_kb;
+            for (int i = npre; i < pf; ++i) tma_prefetch_l2_2d(wmap, (u0_kb0 + i) * 128, wrow + w_half_row);
+            if (sk) {
+                // Stream-K: a CTA's first unit may be a few K blocks only
+                // (the tail of a tile); the ring and the L2 prefetch go on
+                // into the following units, in the order the producer
+                // issues them (issued < npre: weight slice already loaded).
+                int n = u0_nkb;   // blocks walked so far
+                auto more = [&]() { return (p.preload && npre == n && npre < ring) || n < p.prefetch_kb; };
+                int tn, kn0, kn1;
+                while (more() && next_unit(cur0, tn, kn0, kn1)) {
+                    coords(tn, a_t, b_t);
+                    const int wr = a_t * 128;   // (swapped tiles: the weights are the A operand)
+                    for (int kb = kn0; kb < kn1 && more(); ++kb, ++n) {
+                        if (p.preload && npre == n && npre < ring) {
+                            mbar_arrive_expect_tx(&wbar[npre], C::kStageTx);
+                            tma_load_2d(wbuf + npre * wbytes, wmap, &wbar[npre], kb * 128, wr, pol_w);
+                            ++npre;
+                        } else if (n < p.prefetch_kb) {
+                            tma_prefetch_l2_2d(wmap, kb * 128, wr);
+                        }
+                    }
+                }
+            }
         }
         FP8Q_TRACE_AT(p, kTrPreloaded);
     }
@@ -701,15 +775,16 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
             long long issued = 0;
-            for (int tile = cluster_id; tile < p.num_tiles; tile += num_clusters) {
+            long long cur = unit_first;
+            int tile, ukb0, ukb1;
+            while (next_unit(cur, tile, ukb0, ukb1)) {
                 int a_t, b_t;
                 coords(tile, a_t, b_t);
                 const int m_tile = SWAP ? b_t : a_t;
                 const int a_row = a_t * 128;
                 const int b_row = b_t * BN;
                 bool ok = true;
-                for (int i = 0; i < nkb; ++i) {
-                    const int kb = kb_begin + i;
+                for (int kb = ukb0; kb < ukb1; ++kb) {
                     if (issued == 0) FP8Q_TRACE_AT(p, kTrFirstTma);
                     if (TWO_SM) {
                         if (issued >= npre) {
@@ -790,19 +865,23 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
         if (lane == 0 && (!TWO_SM || leader)) {
             uint32_t stage = 0, phase = 0, slot = 0, tphase = 0;
             bool ok = true;
-            for (int tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
+            bool first_unit = true;
+            long long cur = unit_first;
+            int tile, ukb0, ukb1;
+            while (ok && next_unit(cur, tile, ukb0, ukb1)) {
                 if (!BLOCKWISE) {
                     if (!mbar_wait(&tempty[slot], tphase ^ 1u, abort, p.status)) { ok = false; break; }
                     tc_fence_after();
                 }
-                for (int i = 0; i < nkb; ++i) {
+                const int unkb = ukb1 - ukb0;
+                for (int i = 0; i < unkb; ++i) {
                     if (BLOCKWISE) {
                         if (!mbar_wait(&tempty[slot], tphase ^ 1u, abort, p.status)) { ok = false; break; }
                         tc_fence_after();
                     }
                     if (!mbar_wait(&full[stage], phase, abort, p.status)) { ok = false; break; }
                     tc_fence_after();
-                    if (tile == cluster_id && i == 0 && issuer == 0) FP8Q_TRACE_AT(p, kTrFirstMma);
+                    if (first_unit && i == 0 && issuer == 0) FP8Q_TRACE_AT(p, kTrFirstMma);
                     const uint32_t a_addr = smem_u32(sA + stage * C::kABytes);
                     const uint32_t b_addr = smem_u32(sB + stage * C::kBBytes);
                     const uint32_t d = tmem_base + slot * C::kSlotCols + static_cast<uint32_t>(issuer * BN);
@@ -842,6 +921,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                     slot ^= 1u;
                     if (slot == 0) tphase ^= 1u;
                 }
+                first_unit = false;
             }
             if (issuer == 0) FP8Q_TRACE_AT(p, kTrLastCommit);
             // Every MMA this thread issued has finished before TMEM is freed.
@@ -1024,7 +1104,9 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
         OutT *out = static_cast<OutT *>(p.out);
         uint32_t slot = 0, tphase = 0, estage = 0, ephase = 0;
 
-        for (int tile = cluster_id; tile < p.num_tiles; tile += num_clusters) {
+        long long cur = unit_first;
+        int tile, ukb0, ukb1;
+        while (next_unit(cur, tile, ukb0, ukb1)) {
             int a_t, b_t;
             coords(tile, a_t, b_t);
             const int m0 = (SWAP ? b_t : a_t) * C::kTokTile;
@@ -1066,8 +1148,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                 for (int j = 0; j < C::kCols; ++j) acc[j] = 0.0f;
                 const int wblk = SWAP ? a_t : (n0 + col0) >> 7;  // 128-row weight block of these columns
                 const float *sw_row = p.w_scale + static_cast<long long>(wblk) * p.num_kb;
-                for (int i = 0; i < nkb; ++i) {
-                    const int kb = kb_begin + i;
+                for (int kb = ukb0; kb < ukb1; ++kb) {
                     // Warp-uniform outcome: the __syncwarp below needs every lane.
                     bool got = mbar_wait(&full[estage], ephase, abort, p.status);
                     got = got && mbar_wait(&tfull[slot], tphase, abort, p.status);
@@ -1207,6 +1288,71 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
             // decision (after a timeout every further wait fails at once
             // and the output below is skipped).
             if (!named_barrier_and(1, C::kEpiThreads, ok && !*abort)) continue;
+
+            if (sk && (ukb0 > 0 || ukb1 < p.num_kb)) {
+                // Stream-K unit that is part of a tile (only swapped tiles:
+                // the whole row is in registers, kCols == BN).
+                if constexpr (C::kStreamK) {
+                    if (ukb0 > 0) {
+                        // The CTA's leading unit: publish the partial tile
+                        // (row-major [128][BN] in this CTA's slot).
+                        float *dst = p.ws + static_cast<size_t>(blockIdx.x) * (128u * BN) + row * BN + col0;
+#pragma unroll
+                        for (int j = 0; j < C::kCols; j += 4)
+                            *reinterpret_cast<float4 *>(dst + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                        // The barrier orders every thread's stores before
+                        // thread 0's fence and release store (cumulative).
+                        named_barrier_sync(1, C::kEpiThreads);
+                        if (etid == 0) {
+                            __threadfence();
+                            st_release_gpu_u32(p.sk_flags + blockIdx.x, 1u);
+                            FP8Q_TRACE_AT(p, kTrCluster1);   // stream-K: partial published
+                        }
+                        continue;
+                    }
+                    // The unit holding the tile's first K block: add the
+                    // partials of the CTAs whose ranges start inside the
+                    // tile (the sources), in increasing K order.  Epilogue
+                    // thread q waits for source q's flag, so all the waits
+                    // overlap; the barrier then orders every thread's reads
+                    // after those acquires.
+                    const long long tile_end = static_cast<long long>(tile + 1) * p.num_kb;
+                    int nsrc = 0;
+                    while (blockIdx.x + 1 + nsrc < gridDim.x &&
+                           sk_total * (blockIdx.x + 1 + nsrc) / gridDim.x < tile_end)
+                        ++nsrc;
+                    bool seen = true;
+                    for (int q = etid; q < nsrc; q += C::kEpiThreads)
+                        seen = seen && flag_wait_acquire(p.sk_flags + blockIdx.x + 1 + q, abort, p.status);
+                    const bool got = named_barrier_and(1, C::kEpiThreads, seen);
+                    if (etid == 0) FP8Q_TRACE_AT(p, kTrReduced);   // stream-K: sources' flags seen
+                    if (got) {
+                        // (One source at a time: loading several sources' rows
+                        // before adding them overlaps their L2 round trips,
+                        // but the registers it takes would cost the decode
+                        // kernels their second CTA per SM.)
+                        const float *src = p.ws + static_cast<size_t>(blockIdx.x + 1) * (128u * BN) + row * BN + col0;
+#pragma unroll 1
+                        for (int q = 0; q < nsrc; ++q, src += 128 * BN) {
+#pragma unroll
+                            for (int j = 0; j < C::kCols; j += 4) {
+                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + j));
+                                acc[j] += v.x;
+                                acc[j + 1] += v.y;
+                                acc[j + 2] += v.z;
+                                acc[j + 3] += v.w;
+                            }
+                        }
+                        // Every thread has read the partials: clear their
+                        // flags for the next launch.
+                        named_barrier_sync(1, C::kEpiThreads);
+                        for (int q = etid; q < nsrc; q += C::kEpiThreads)
+                            st_relaxed_gpu_u32(p.sk_flags + blockIdx.x + 1 + q, 0u);
+                        if (etid == 0) FP8Q_TRACE_AT(p, kTrCluster2);   // stream-K: partials added
+                    }
+                    if (!got) continue;
+                }
+            }
 
             if (!SWAP && !BLOCKWISE) {
                 // Stored (or published as a partial tile) above.

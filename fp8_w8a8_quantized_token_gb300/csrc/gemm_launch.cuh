@@ -125,6 +125,16 @@ cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigne
         use_ws = cr >= 1 && (owned + cr - 1) / cr <= static_cast<uint32_t>(C::kWsBars);
     }
     a.ws = use_ws ? static_cast<float *>(pr.ws) : nullptr;
+    // Stream-K (the caller checked the workspace size): slots, then flags.
+    a.stream_k = 0;
+    a.sk_flags = nullptr;
+    if (l.stream_k) {
+        if (!C::kStreamK || l.split != 1 || pr.ws == nullptr) return cudaErrorInvalidValue;
+        a.stream_k = 1;
+        a.ws = static_cast<float *>(pr.ws);
+        a.sk_flags = reinterpret_cast<unsigned *>(static_cast<char *>(pr.ws) +
+                                                  static_cast<size_t>(l.grid) * 128u * BN * 4u);
+    }
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(l.grid));

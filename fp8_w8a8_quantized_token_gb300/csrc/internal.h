@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/fp8q.h"
+
 namespace fp8q {
 
 // ---- quantizers (quant.cu) ------------------------------------------------
@@ -31,6 +33,7 @@ struct GemmLaunch {
     int stages;        // pipeline depth the instantiation uses
     bool pair;         // non-swapped channelwise, split 1: 2-CTA clusters on adjacent token tiles
     bool two_sm;       // the pair computes 256-token tiles with 2-CTA MMAs (always with pair)
+    bool stream_k;     // swapped tiles: equal shares of (tile, K block) pairs per CTA, split 1
 };
 
 struct GemmProblem {
@@ -58,6 +61,14 @@ struct GemmProblem {
 // partial tiles are smaller than 128 x 128 floats): one slot of 128 x mma_n
 // fp32 partial sums per CTA.
 size_t plan_workspace_bytes(int64_t M, int64_t N, int swap_ab, int mma_n, int split_k);
+
+// Workspace of a stream-K launch of `grid` CTAs: one slot of 128 x mma_n
+// floats per CTA, then one 32-bit flag per CTA (zero between launches).
+size_t stream_k_workspace_bytes(int grid, int mma_n);
+
+// The K-split schedule of a stream-K plan's tiles (the generic rule's
+// split: 2, 4 or 8 while the CTAs fill at most half the SMs).
+void plan_without_stream_k(int64_t M, int64_t N, int64_t K, int blockwise, int num_sms, fp8q_plan *pl);
 
 // Launchers return cudaSuccess or the launch error; a tensor map the driver
 // rejects is reported as cudaErrorInvalidValue.

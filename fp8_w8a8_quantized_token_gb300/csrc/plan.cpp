@@ -30,7 +30,8 @@ struct TableEntry {
     int swap_ab, mma_n, split;
 };
 
-// Rows "{N, K, blockwise, M, swap_ab, mma_n, split}," from the sweep.
+// Rows "{N, K, blockwise, M, swap_ab, mma_n, split}," from the sweep
+// (split 0: stream-K).
 const TableEntry kTable[] = {
 #include "tile_table.inc"
     {0, 0, 0, 0, 0, 0, 0}};
@@ -126,13 +127,34 @@ size_t plan_workspace_bytes(int64_t M, int64_t N, int swap_ab, int mma_n, int sp
     return static_cast<size_t>(tiles) * static_cast<size_t>(split_k) * 128u * static_cast<size_t>(mma_n) * 4u;
 }
 
-// Tile sizes, grid and persistence for a chosen (swap_ab, mma_n, split_k).
+size_t stream_k_workspace_bytes(int grid, int mma_n)
+{
+    return static_cast<size_t>(grid) * (128u * static_cast<size_t>(mma_n) * 4u + 4u);
+}
+
+// Tile sizes, grid and persistence for a chosen (swap_ab, mma_n, split_k);
+// split_k 0 with swapped tiles asks for stream-K.
 void plan_finish(int64_t M, int64_t N, int64_t K, int blockwise, int num_sms, fp8q_plan *pl)
 {
     pl->tile_m = pl->swap_ab ? pl->mma_n : 128;
     pl->tile_n = pl->swap_ab ? 128 : pl->mma_n;
     const int64_t tiles = ((M + pl->tile_m - 1) / pl->tile_m) * ((N + pl->tile_n - 1) / pl->tile_n);
     const int64_t num_kb = (K + 127) / 128;
+    if (pl->swap_ab && pl->mma_n <= 32 && pl->split_k == 0) {
+        // Stream-K: at most one CTA per SM (every CTA must be resident for
+        // the partial hand-over) and at least one K block per CTA.
+        const int64_t total = tiles * num_kb;
+        const int64_t sms = num_sms > 0 ? num_sms : 1;
+        pl->stream_k = 1;
+        pl->split_k = 1;
+        pl->pair = 0;
+        pl->two_sm = 0;
+        pl->grid = static_cast<int32_t>(total < sms ? total : sms);
+        pl->persistent = 1;
+        pl->stages = stages_for(true, pl->mma_n);
+        return;
+    }
+    pl->stream_k = 0;
     int64_t split = pl->split_k;
     if (split > 8) split = 8;
     if (split > num_kb) split = num_kb;
@@ -163,6 +185,15 @@ void plan_finish(int64_t M, int64_t N, int64_t K, int blockwise, int num_sms, fp
     pl->stages = pl->two_sm ? kTwoSmStages : stages_for(pl->swap_ab != 0, pl->mma_n);
 }
 
+void plan_without_stream_k(int64_t M, int64_t N, int64_t K, int blockwise, int num_sms, fp8q_plan *pl)
+{
+    const int64_t tiles = ((M + pl->tile_m - 1) / pl->tile_m) * ((N + pl->tile_n - 1) / pl->tile_n);
+    int split = 1;
+    while (split < 8 && tiles * split * 2 <= num_sms) split *= 2;
+    pl->split_k = split;
+    plan_finish(M, N, K, blockwise, num_sms, pl);
+}
+
 }  // namespace fp8q
 
 extern "C" fp8q_status fp8q_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t blockwise, int32_t num_sms,
@@ -190,10 +221,11 @@ extern "C" fp8q_status fp8q_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t b
         static std::set<std::tuple<int64_t, int64_t, int64_t, int>> seen;
         std::lock_guard<std::mutex> g(mu);
         if (seen.insert(std::make_tuple(M, N, K, blockwise)).second)
-            fprintf(stderr, "fp8q plan M=%lld N=%lld K=%lld %s: swap_ab=%d mma_n=%d split_k=%d pair=%d grid=%d%s\n",
+            fprintf(stderr, "fp8q plan M=%lld N=%lld K=%lld %s: swap_ab=%d mma_n=%d split_k=%d pair=%d stream_k=%d "
+                    "grid=%d%s\n",
                     static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K),
-                    blockwise ? "blockwise" : "channelwise", pl.swap_ab, pl.mma_n, pl.split_k, pl.pair, pl.grid,
-                    pl.from_table ? " (table)" : "");
+                    blockwise ? "blockwise" : "channelwise", pl.swap_ab, pl.mma_n, pl.split_k, pl.pair, pl.stream_k,
+                    pl.grid, pl.from_table ? " (table)" : "");
     }
     *plan = pl;
     return FP8Q_OK;
@@ -204,6 +236,7 @@ extern "C" size_t fp8q_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t 
     using namespace fp8q;
     fp8q_plan pl;
     if (M <= 0 || fp8q_gemm_plan(M, N, K, blockwise, 0, &pl) != FP8Q_OK) return 0;
+    if (pl.stream_k) return stream_k_workspace_bytes(pl.grid, pl.mma_n);
     return plan_workspace_bytes(M, N, pl.swap_ab, pl.mma_n, pl.split_k);
 }
 
@@ -214,7 +247,9 @@ extern "C" fp8q_status fp8q_set_plan_override(int32_t swap_ab, int32_t mma_n, in
         g_ovr_swap.store(-1);
         return FP8Q_OK;
     }
-    if (swap_ab > 1 || !gemm_shape_supported(swap_ab != 0, mma_n) || split_k < 1) return FP8Q_ERR_INVALID_ARG;
+    if (swap_ab > 1 || !gemm_shape_supported(swap_ab != 0, mma_n) || split_k < 0 ||
+        (split_k == 0 && (swap_ab != 1 || mma_n > 32)))
+        return FP8Q_ERR_INVALID_ARG;
     g_ovr_n.store(mma_n);
     g_ovr_split.store(split_k);
     g_ovr_swap.store(swap_ab);

@@ -72,19 +72,23 @@ def back_to_back(L, dev, M: int, N: int, K: int):
     copies = [wq0] + [wq0.clone() for _ in range(3)]
     outs = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(4)]
     plan = fq.fp8q_gemm_plan(M, N, K)
+    # One zero-filled workspace for all launches where the schedule takes
+    # one (stream-K); K-split schedules exchange in distributed shared memory.
+    need = fq.fp8q_workspace_bytes(M, N, K) if plan.get("stream_k") else 0
+    work = torch.zeros(need, dtype=torch.uint8, device=dev) if need else None
     side = torch.cuda.Stream(dev)
     side.wait_stream(torch.cuda.current_stream(dev))
     torch.cuda.synchronize()
     with torch.cuda.stream(side):
         for i in range(4):
-            fq.fp8q_scaled_mm_channelwise(xq, copies[i], xs, ws, out=outs[i], workspace=None)
+            fq.fp8q_scaled_mm_channelwise(xq, copies[i], xs, ws, out=outs[i], workspace=work)
     side.synchronize()
     if L.fp8q_trace_clear() != 0:   # capture writes launch i to block i
         raise RuntimeError("fp8q_trace_clear failed")
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=side):
         for i in range(4):
-            fq.fp8q_scaled_mm_channelwise(xq, copies[i], xs, ws, out=outs[i], workspace=None)
+            fq.fp8q_scaled_mm_channelwise(xq, copies[i], xs, ws, out=outs[i], workspace=work)
     for _ in range(3):
         g.replay()
     torch.cuda.synchronize()
@@ -100,6 +104,10 @@ def back_to_back(L, dev, M: int, N: int, K: int):
     t0 = t[0, :, 0].min()
     print(f"== back to back: M={M} N={N} K={K} plan={plan}")
     cols = [("entry", 0), ("release", 2), ("first MMA", 4), ("last MMA", 5), ("stored", 7), ("exit", 11)]
+    if plan.get("stream_k"):
+        # (stream-K reuses the split-K slots: partial published, sources'
+        # flags seen by the tile's owner, partials added)
+        cols[4:4] = [("published", 8), ("flags seen", 9), ("added", 10)]
     print("  launch " + "".join(f"{c:>12}" for c, _ in cols) + "   gap(prev exit -> release)")
     for i in range(4):
         med = [np.median(t[i, :, j][t[i, :, j] > 0] - t0) / 1000.0 for _, j in cols]

@@ -1,7 +1,8 @@
 """Schedule sweep for the GEMM planner: writes ``csrc/tile_table.inc``.
 
 For every linear shape of the benchmark workloads and a grid of M values,
-each candidate schedule (operand orientation, MMA N extent, K-split) is
+each candidate schedule (operand orientation, MMA N extent, K-split or,
+for swapped tiles, stream-K) is
 timed on the GPU with the split-K workspace it uses -- 8 back-to-back
 launches over rotating weight copies
 (more than twice L2 in total) captured in a CUDA graph, replayed 10 times,
@@ -36,6 +37,7 @@ SHAPES = {
     "blk_3072x12288": (3072, 12288, 1, [1, 16, 64, 256, 1024, 8192]),
 }
 SPLITS = (1, 2, 4, 8)
+SWAP_SPLITS = (0,) + SPLITS   # 0: stream-K (16- and 32-token tiles)
 
 
 def candidates(M: int):
@@ -45,7 +47,7 @@ def candidates(M: int):
             continue
         if M > 1024:
             continue
-        c += [(1, mn, s) for s in SPLITS]
+        c += [(1, mn, s) for s in (SWAP_SPLITS if mn <= 32 else SPLITS)]
     # Weights on the MMA's N side: half the MMA instructions of 128-row
     # weight tiles (a tcgen05.mma costs the same whatever its N).
     c += [(0, 256, s) for s in ((1, 2, 4) if M > 1024 else SPLITS)]
@@ -111,7 +113,7 @@ def main():
                 # Each candidate with the split-K workspace it uses (as the
                 # library's callers pass it).
                 need = fq.fp8q_workspace_bytes(M, N, K, bool(bw))
-                work = torch.empty(need, dtype=torch.uint8, device=dev) if need else None
+                work = torch.zeros(need, dtype=torch.uint8, device=dev) if need else None
                 side = torch.cuda.Stream()
                 with torch.cuda.stream(side):
                     for i in range(2):

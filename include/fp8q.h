@@ -246,6 +246,15 @@ FP8Q_API fp8q_status fp8q_scaled_mm_blockwise(const void *a, const void *w, cons
  * The scratch argument of the GEMM calls on the pages' interface (the
  * fp8_scaled_mm / fp8_blockwise_scaled_mm callers own all device memory).
  *
+ * Stream-K schedules (fp8q_plan.stream_k; decode-size M): grid slots of
+ * 128 x mma_n floats, then grid 32-bit flags (grid * (512 * mma_n + 4)
+ * bytes).  Such a workspace MUST BE ZERO-FILLED before its first use
+ * (cudaMemset); every completed GEMM leaves its flags at zero again, so
+ * later calls (and CUDA-graph replays) need no further clearing.  After a
+ * call that reported FP8Q_ERR_TIMEOUT, zero it again.  A workspace that is
+ * NULL or smaller than this makes the GEMM fall back to a K-split schedule
+ * (correct, slower at these sizes).
+ *
  * With K split over a cluster of s CTAs, each CTA computes an fp32 partial
  * tile over its range of K blocks, and each CTA adds up its share of the
  * tile's outputs over all s partials in a fixed order.  The other CTAs'
@@ -260,9 +269,10 @@ FP8Q_API fp8q_status fp8q_scaled_mm_blockwise(const void *a, const void *w, cons
  *     measured on, it was slower than the distributed-shared-memory
  *     exchange at every schedule (partials just written by other SMs came
  *     back through global memory at 10-30 GB/s per SM).
- * So by default this returns 0 and the GEMMs ignore a workspace.  Nothing
- * in the workspace has to be initialised, and its contents are undefined
- * after the call.  Calls that can run concurrently on the GPU need
+ * So by default this returns 0 for K-split schedules and the GEMMs
+ * ignore a workspace there.  For K-split schedules nothing in the
+ * workspace has to be initialised, and its contents are undefined after
+ * the call.  Calls that can run concurrently on the GPU need
  * separate workspaces; calls in order on one stream can share one.
  * Returns 0 as well for invalid sizes (M <= 0, N <= 0, K <= 0).
  * ------------------------------------------------------------------------- */
@@ -407,6 +417,17 @@ typedef struct {
                            tile with 2-CTA MMAs (tcgen05 cta_group::2), each
                            CTA loading only its half of the weight rows
                            (always equal to pair) */
+    int32_t stream_k;   /* 1 (swapped tiles of 16 or 32 tokens; split_k 1,
+                           grid <= SMs):
+                           stream-K -- each CTA takes an equal share of the
+                           (tile, 128-wide K block) pairs in tile-major order,
+                           and a CTA whose share starts inside a tile hands
+                           its fp32 partial sums to the CTA holding that
+                           tile's first K block through the workspace (see
+                           fp8q_workspace_bytes, which then sizes it).
+                           Without that workspace, and in the fused and
+                           weight-only GEMMs, the GEMM runs a K-split
+                           schedule of the same tiles instead. */
 } fp8q_plan;
 
 FP8Q_API fp8q_status fp8q_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t blockwise, int32_t num_sms,
@@ -415,7 +436,9 @@ FP8Q_API fp8q_status fp8q_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t blo
 /* Force the schedule of every following GEMM in this process (for tests
  * and tuning sweeps): swap_ab in {0, 1} with an mma_n that has a kernel
  * instantiation (swapped: 16, 32, 64, 128; non-swapped: 32, 64, 128, 256) and
- * split_k >= 1 (clamped to 8 and to the number of 128-wide K blocks).
+ * split_k >= 1 (clamped to 8 and to the number of 128-wide K blocks), or
+ * split_k == 0 with swap_ab == 1 and mma_n 16 or 32 for stream-K
+ * (fp8q_plan.stream_k).
  * swap_ab < 0 removes the override.  Errors: INVALID_ARG for a
  * combination without an instantiation.  Not thread-safe with concurrent
  * GEMM calls. */

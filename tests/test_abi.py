@@ -54,7 +54,7 @@ def test_status_strings_and_version(lib):
     assert fq.status_str(0) == "FP8Q_OK"
     assert fq.status_str(4) == "FP8Q_ERR_TIMEOUT"
     assert fq.status_str(99) == "FP8Q_UNKNOWN_STATUS"
-    assert fq.fp8q_version() >> 16 == 2
+    assert fq.fp8q_version() == (2 << 16) | 1
 
 
 def test_invalid_arguments_are_rejected_before_any_cuda_call(lib):
@@ -115,7 +115,11 @@ def test_invalid_arguments_are_rejected_before_any_cuda_call(lib):
 def test_plan_override_validation(lib):
     assert lib.fp8q_set_plan_override(1, 48, 1) == fq.FP8Q_ERR_INVALID_ARG
     assert lib.fp8q_set_plan_override(0, 16, 1) == fq.FP8Q_ERR_INVALID_ARG
-    assert lib.fp8q_set_plan_override(1, 32, 0) == fq.FP8Q_ERR_INVALID_ARG
+    assert lib.fp8q_set_plan_override(1, 32, -1) == fq.FP8Q_ERR_INVALID_ARG
+    assert lib.fp8q_set_plan_override(0, 256, 0) == fq.FP8Q_ERR_INVALID_ARG   # stream-K: swapped tiles only
+    assert lib.fp8q_set_plan_override(1, 32, 0) == fq.FP8Q_OK
+    p = fq.fp8q_gemm_plan(7, 4096, 4096, num_sms=148)
+    assert (p["swap_ab"], p["mma_n"], p["split_k"], p["stream_k"]) == (1, 32, 1, 1)
     assert lib.fp8q_set_plan_override(1, 32, 3) == fq.FP8Q_OK
     p = fq.fp8q_gemm_plan(7, 4096, 4096, num_sms=148)
     assert (p["swap_ab"], p["mma_n"], p["split_k"], p["from_table"]) == (1, 32, 3, 0)

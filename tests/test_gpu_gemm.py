@@ -17,9 +17,13 @@ from gpu_util import (THREADS, assert_gemm_close, out_values, quant_both_group, 
 
 pytestmark = pytest.mark.gpu
 
+# (swap_ab, mma_n, split_k); split_k 0 = stream-K (swapped tiles).  On the
+# 392 x 1040 shapes below, M = 1 has 4 tiles x 9 K blocks = 36 pairs: 36
+# stream-K CTAs of one K block each, so every tile is split 9 ways.
 SCHEDULES = [(1, 16, 1), (1, 16, 3), (1, 16, 5), (1, 32, 2), (1, 32, 8), (1, 64, 1), (1, 64, 4), (1, 64, 7),
              (1, 128, 1), (1, 128, 2), (1, 128, 6), (0, 256, 1), (0, 256, 2), (0, 256, 5),
-             (0, 128, 1), (0, 128, 3), (0, 64, 1), (0, 64, 2), (0, 32, 1), (0, 32, 4)]
+             (0, 128, 1), (0, 128, 3), (0, 64, 1), (0, 64, 2), (0, 32, 1), (0, 32, 4),
+             (1, 16, 0), (1, 32, 0)]
 
 
 @pytest.fixture(scope="module")
@@ -38,14 +42,14 @@ def schedule():
     fq.fp8q_set_plan_override(-1)
 
 
-def channelwise_case(dev, M, N, K, seed=0, bias=False, outliers=True, out_dtype=torch.bfloat16):
+def channelwise_case(dev, M, N, K, seed=0, bias=False, outliers=True, out_dtype=torch.bfloat16, workspace="auto"):
     x = synthetic.activations(M, K, seed=seed, outliers=outliers)
     w = synthetic.weights(N, K, seed=seed)
     b = synthetic.bias(N, seed=seed) if bias else None
     xq, xs, rq, rs = quant_both_per_token(x, dev)
     wq, ws, rwq, rws = quant_both_per_token(w, dev)
     out = fq.fp8q_scaled_mm_channelwise(xq, wq, xs, ws, bias=None if b is None else b.to(dev),
-                                        out_dtype=out_dtype)
+                                        out_dtype=out_dtype, workspace=workspace)
     torch.cuda.synchronize()
     fp16 = out_dtype == torch.float16
     ref = ref_values(oracle.gemm_channelwise(rq, rwq, rs, rws, bias=b, out_fp16=fp16, threads=THREADS), fp16)
@@ -66,6 +70,82 @@ def test_channelwise_every_schedule(dev, schedule, swap, mma_n, split):
 
 
 SPLIT_SCHEDULES = [s for s in SCHEDULES if s[2] > 1]
+STREAM_K_SCHEDULES = [s for s in SCHEDULES if s[2] == 0]
+
+
+def _flags(work: torch.Tensor, grid: int) -> np.ndarray:
+    return work[work.numel() - 4 * grid:].view(torch.int32).cpu().numpy()
+
+
+@pytest.mark.parametrize("bw", [False, True])
+def test_stream_k_workspace_flags_and_repeats(dev, schedule, bw):
+    """Stream-K through a caller's zero-filled workspace: the plan asks for
+    grid * (512 * mma_n + 4) bytes; two calls in a row on different inputs
+    both match the oracle, repeating a call gives identical bits, and every
+    flag is back at zero after each call."""
+    fq.fp8q_set_plan_override(1, 16, 0)
+    M, N, K = 13, 1024, 2176          # 8 tiles x 17 K blocks = 136 pairs
+    plan = fq.fp8q_gemm_plan(M, N, K, blockwise=bw)
+    assert plan["stream_k"] == 1 and plan["split_k"] == 1
+    grid = plan["grid"]
+    need = fq.fp8q_workspace_bytes(M, N, K, bw)
+    assert need == grid * (512 * 16 + 4)
+    work = torch.zeros(need, dtype=torch.uint8, device=dev)
+    for seed in (1, 2):
+        if bw:
+            out, ctx = blockwise_case(dev, M, N, K, seed=seed, bias=True, workspace=work)
+            ref = blockwise_ref(ctx, M)
+        else:
+            out, ref = channelwise_case(dev, M, N, K, seed=seed, bias=True, workspace=work)
+        assert_gemm_close(out_values(out), ref, f"stream-K seed {seed}")
+        assert not _flags(work, grid).any(), "flags left set"
+        again = (blockwise_case(dev, M, N, K, seed=seed, bias=True, workspace=work)[0] if bw else
+                 channelwise_case(dev, M, N, K, seed=seed, bias=True, workspace=work)[0])
+        assert torch.equal(out, again), "stream-K result not deterministic"
+
+
+def test_stream_k_without_workspace_falls_back(dev, schedule):
+    """A stream-K plan called without a workspace runs the tiles split along
+    K instead (same oracle bar)."""
+    fq.fp8q_set_plan_override(1, 32, 0)
+    for M in (1, 20):
+        out, ref = channelwise_case(dev, M, 768, 3072, seed=M, workspace=None)
+        assert_gemm_close(out_values(out), ref, f"stream-K fallback M={M}")
+
+
+def test_stream_k_graph_replays(dev, schedule):
+    """CUDA-graph replays of a stream-K GEMM (same workspace every replay)
+    on inputs rewritten between replays: each replay matches the oracle, so
+    each launch leaves the flags ready for the next."""
+    fq.fp8q_set_plan_override(1, 16, 0)
+    M, N, K = 16, 2048, 4096
+    w = synthetic.weights(N, K, seed=5)
+    wq, ws, rwq, rws = quant_both_per_token(w, dev)
+    need = fq.fp8q_workspace_bytes(M, N, K)
+    work = torch.zeros(need, dtype=torch.uint8, device=dev)
+    xq = torch.empty((M, K), dtype=fq.E4M3, device=dev)
+    xs = torch.empty((M,), dtype=torch.float32, device=dev)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fq.fp8q_scaled_mm_channelwise(xq, wq, xs, ws, out=out, workspace=work)
+    side.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        fq.fp8q_scaled_mm_channelwise(xq, wq, xs, ws, out=out, workspace=work)
+    for seed in (11, 12, 13):
+        x = synthetic.activations(M, K, seed=seed, outliers=True)
+        q, s, rq, rs = quant_both_per_token(x, dev)
+        xq.copy_(q)
+        xs.copy_(s)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        ref = ref_values(oracle.gemm_channelwise(rq, rwq, rs, rws, threads=THREADS))
+        assert_gemm_close(out_values(out), ref, f"graph replay seed {seed}")
+    assert not _flags(work, fq.fp8q_gemm_plan(M, N, K)["grid"]).any()
+    assert fq.fp8q_device_status() == fq.FP8Q_OK
 
 
 def test_split_k_requests_no_workspace_by_default(dev, schedule):
@@ -150,7 +230,7 @@ def test_channelwise_strided_weight_and_output_canary(dev):
     assert torch.all(out_buf[M:] == 7.0)
 
 
-def blockwise_case(dev, M, N, K, seed=0, bias=False, outliers=True, garbage_padding=False):
+def blockwise_case(dev, M, N, K, seed=0, bias=False, outliers=True, garbage_padding=False, workspace="auto"):
     x = synthetic.activations(M, K, seed=seed, outliers=outliers)
     w = synthetic.weights(N, K, seed=seed)
     b = synthetic.bias(N, seed=seed) if bias else None
@@ -160,7 +240,8 @@ def blockwise_case(dev, M, N, K, seed=0, bias=False, outliers=True, garbage_padd
     torch.cuda.synchronize()
     rwq, rws = oracle.quant_weight_blocks(w, 128, 128)
     assert np.array_equal(u8(wq), rwq) and np.array_equal(ws.cpu().numpy(), rws)
-    out = fq.fp8q_scaled_mm_blockwise(xq, wq, xs, ws, M=M, bias=None if b is None else b.to(dev))
+    out = fq.fp8q_scaled_mm_blockwise(xq, wq, xs, ws, M=M, bias=None if b is None else b.to(dev),
+                                      workspace=workspace)
     torch.cuda.synchronize()
     return out, (x, w, b, rq, rs, rwq, rws)
 

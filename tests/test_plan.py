@@ -43,6 +43,13 @@ def test_plans_are_launchable(num_sms):
         tiles = -(-M // p["tile_m"]) * -(-N // p["tile_n"])
         num_kb = -(-K // 128)
         assert 1 <= p["split_k"] <= min(8, num_kb)
+        if p["stream_k"]:
+            # stream-K: swapped tiles, no clusters, one CTA per SM at most and
+            # at least one (tile, K block) pair per CTA
+            assert p["swap_ab"] == 1 and p["split_k"] == 1 and p["pair"] == 0 and p["persistent"] == 1
+            assert p["grid"] == min(tiles * num_kb, num_sms)
+            assert p["stages"] * stage_bytes(1, p["mma_n"], bw) + 4096 <= SMEM_LIMIT
+            continue
         m_tiles = -(-M // p["tile_m"])
         # channelwise 256-column tiles pair up (blockwise and narrower tiles never do)
         assert p["pair"] == int(not bw and not p["swap_ab"] and p["mma_n"] == 256 and p["split_k"] == 1
@@ -82,6 +89,26 @@ def test_override_forces_the_schedule_and_clamps_split():
         fq.fp8q_set_plan_override(-1)
 
 
+@pytest.mark.parametrize("num_sms", [148, 152])
+def test_stream_k_plans(num_sms):
+    """split_k 0 on swapped tiles asks for stream-K: split 1, no pairs, one
+    CTA per SM at most, at least one (tile, K block) pair per CTA."""
+    try:
+        fq.fp8q_set_plan_override(1, 16, 0)
+        p = fq.fp8q_gemm_plan(16, 24576, 4096, num_sms=num_sms)      # 192 tiles x 32 K blocks
+        assert (p["stream_k"], p["split_k"], p["pair"], p["grid"], p["persistent"]) == (1, 1, 0, num_sms, 1)
+        p = fq.fp8q_gemm_plan(1, 256, 512, num_sms=num_sms)          # 2 tiles x 4 K blocks = 8 pairs
+        assert (p["stream_k"], p["grid"]) == (1, 8)
+        fq.fp8q_set_plan_override(1, 32, 0)
+        p = fq.fp8q_gemm_plan(32, 4096, 12288, blockwise=True, num_sms=num_sms)
+        assert p["stream_k"] == 1 and p["mma_n"] == 32 and p["tile_m"] == 32
+        assert fq.load_library().fp8q_set_plan_override(1, 64, 0) == fq.FP8Q_ERR_INVALID_ARG
+        fq.fp8q_set_plan_override(1, 16, 4)
+        assert fq.fp8q_gemm_plan(16, 24576, 4096, num_sms=num_sms)["stream_k"] == 0
+    finally:
+        fq.fp8q_set_plan_override(-1)
+
+
 def load_table():
     import os
     import re
@@ -114,7 +141,11 @@ def test_table_lookup_is_nearest_m_with_ties_to_the_smaller_m():
             p = fq.fp8q_gemm_plan(M, N, K, bool(bw), num_sms=148)
             assert p["from_table"] == 1
             assert (p["swap_ab"], p["mma_n"]) == (swap, mma_n), (N, K, bw, M, best)
-            assert p["split_k"] == min(split, 8, -(-K // 128)), (N, K, bw, M, best)
+            if split == 0:   # stream-K row
+                assert p["stream_k"] == 1 and p["split_k"] == 1, (N, K, bw, M, best)
+            else:
+                assert p["stream_k"] == 0
+                assert p["split_k"] == min(split, 8, -(-K // 128)), (N, K, bw, M, best)
 
 
 def test_shapes_without_rows_use_the_generic_rule():
@@ -136,7 +167,8 @@ def test_tuner_only_proposes_schedules_the_library_accepts(lib):
                 cands = tune.candidates(M)
                 assert any(c[:2] == (0, 256) for c in cands), (label, M)
                 for c in cands:
-                    assert (c[0], c[1]) in SUPPORTED and c[2] in tune.SPLITS, (label, M, c)
+                    assert (c[0], c[1]) in SUPPORTED, (label, M, c)
+                    assert c[2] in (tune.SWAP_SPLITS if c[0] else tune.SPLITS), (label, M, c)
                     assert lib.fp8q_set_plan_override(*c) == fq.FP8Q_OK
                     plan = fq.fp8q_gemm_plan(M, N, K, bool(bw), num_sms=152)
                     assert (plan["swap_ab"], plan["mma_n"]) == (c[0], c[1]), (label, M, c, plan)
