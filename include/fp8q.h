@@ -354,6 +354,10 @@ FP8Q_API fp8q_status fp8q_linear_blockwise_fused(const void *x, int64_t ldx, con
  * in a fixed array inside the library (a file-scope __device__ array of
  * FP8Q_NOALLOC_MAX_CODES + 4 * FP8Q_NOALLOC_MAX_ROWS bytes = 16 MiB + 64 KiB,
  * held on every GPU that loads the library until the process exits).
+ * Where the planned schedule is stream-K (which needs a workspace), this
+ * entry runs the K-split schedule of the same tiles, as
+ * fp8q_linear_channelwise does without a workspace; the output can then
+ * differ in the last bits (fp32 summation order) from a call with one.
  * It is meant for callers that cannot call cudaMalloc: code whose device
  * memory is handed out entirely by a host framework's own pool (a plugin
  * given no workspace, an engine that budgets every byte up front), or a
