@@ -42,7 +42,7 @@ UNIT = "TFLOP/s"
 # o_proj sweep, the 2-CTA prefill kernel's four launches M = 1024 .. 8192 of
 # "oproj_prefill_group", averaged.  A key is dropped whenever its kernel
 # changes.
-DOMINANT_TRAFFIC_BYTES = {}
+DOMINANT_TRAFFIC_BYTES = {("channelwise", 0, 256, 1): 39.94e6}
 
 # Small fixed cases for Nsight Compute captures: name -> (kind, M, N, K).
 PROFILE_CASES = {
@@ -487,7 +487,8 @@ def build_problems(gpu, workload):
 
 
 def plan_str(pl):
-    return f"{'swap' if pl['swap_ab'] else 'noswap'}{pl['mma_n']}x{pl['split_k']}"
+    k = "streamK" if pl.get("stream_k") else pl["split_k"]
+    return f"{'swap' if pl['swap_ab'] else 'noswap'}{pl['mma_n']}x{k}"
 
 
 def measure_sweep(gpu, problems, peaks, with_quant=True):
