@@ -6,7 +6,8 @@ L40S" page, Motivation; the blockwise prefill layers of the row-padding
 page, Implementation breakdown):
   channelwise o_proj 4096x4096 at M in {512, 2048, 8192};
   channelwise qkv 6144x4096, down 4096x12288, gate_up 24576x4096 at
-  M in {128, 512, 2048, 8192};
+  M in {128, 512, 2048, 8192}, and gate_up at M in {1, 16} (the stream-K
+  schedule, with the zero-filled workspace the binding allocates);
   blockwise 24576x3072 and 3072x12288 at M = 8192.
 
 Per case:
@@ -53,6 +54,7 @@ CHANNELWISE = [
     ("qkv", 6144, 4096, 128), ("qkv", 6144, 4096, 512), ("qkv", 6144, 4096, 2048), ("qkv", 6144, 4096, 8192),
     ("down", 4096, 12288, 128), ("down", 4096, 12288, 512), ("down", 4096, 12288, 2048),
     ("down", 4096, 12288, 8192),
+    ("gate_up", 24576, 4096, 1), ("gate_up", 24576, 4096, 16),     # stream-K rows of the table
     ("gate_up", 24576, 4096, 128), ("gate_up", 24576, 4096, 512), ("gate_up", 24576, 4096, 2048),
     ("gate_up", 24576, 4096, 8192),
 ]
@@ -148,7 +150,8 @@ def test_channelwise_full_size_planner_schedule(dev, label, N, K, M):
     ms, ns = positions(M, N, seed=M + N)
     ref = ref_values(oracle.gemm_channelwise_at(rq, rwq, rs, rws, ms, ns))
     got = gathered(out, ms, ns)
-    sched = f"{'swap' if plan['swap_ab'] else 'noswap'}{plan['mma_n']}x{plan['split_k']}"
+    split = "streamK" if plan.get("stream_k") else plan["split_k"]
+    sched = f"{'swap' if plan['swap_ab'] else 'noswap'}{plan['mma_n']}x{split}"
     what = f"{label} M={M} ({sched})"
     assert_gemm_close(got, ref, what)
     S = ref_values(oracle.gemm_channelwise_at(rq & 0x7F, rwq & 0x7F, rs, rws, ms, ns))
