@@ -364,15 +364,16 @@ class Gpu:
     def ptr(self, t):
         return None if t is None else self.P(t.data_ptr())
 
-    def linear(self, p, sp, wq=None):
+    def linear(self, p, sp, wq=None, x=None):
         """The public linear entry point: quantize, then GEMM (two kernels)."""
         L, P = self.L, self.ptr
         wq = p["wq"] if wq is None else wq
+        x = p["x"] if x is None else x
         if p["bw"]:
-            st = L.fp8q_linear_blockwise(P(p["x"]), P(wq), P(p["ws"]), None, P(p["out"]), p["M"], p["N"], p["K"],
+            st = L.fp8q_linear_blockwise(P(x), P(wq), P(p["ws"]), None, P(p["out"]), p["M"], p["N"], p["K"],
                                          P(p["xq"]), P(p["xs"]), p["m_pad"], 0, P(p["work"]), p["work_bytes"], sp)
         else:
-            st = L.fp8q_linear_channelwise(P(p["x"]), P(wq), p["K"], P(p["ws"]), None, P(p["out"]), p["M"],
+            st = L.fp8q_linear_channelwise(P(x), P(wq), p["K"], P(p["ws"]), None, P(p["out"]), p["M"],
                                            p["N"], p["K"], P(p["xq"]), P(p["xs"]), 0, P(p["work"]), p["work_bytes"],
                                            sp)
         if st != 0:
@@ -493,9 +494,9 @@ def plan_str(pl):
 
 def measure_sweep(gpu, problems, peaks, with_quant=True):
     """Per problem: the GEMM (REPS back-to-back launches over rotating weight
-    copies, > L2 in total) and its quantizer (REPS launches over rotating
-    activation copies, > L2 in total), each the median of 5 timed
-    measurements; K-split schedules are also timed without the workspace
+    copies, > L2 in total), its quantizer (REPS launches over rotating
+    activation copies, > L2 in total) and the linear entry point that runs
+    both (over both rotations), each the median of 5 timed measurements; K-split schedules are also timed without the workspace
     (partials exchanged in distributed shared memory)."""
     out = []
     for i, p in enumerate(problems):
@@ -508,6 +509,11 @@ def measure_sweep(gpu, problems, peaks, with_quant=True):
         def body_q(st, p=p):
             for r in range(REPS):
                 gpu.quant(p, gpu.P(st.cuda_stream), x=p["xcopies"][r % len(p["xcopies"])])
+
+        def body_l(st, p=p, copies=copies, i=i):
+            for r in range(REPS):
+                gpu.linear(p, gpu.P(st.cuda_stream), wq=copies[(i + r) % len(copies)],
+                           x=p["xcopies"][r % len(p["xcopies"])])
 
         gu = gpu.time_graph(body_g, REPS)
         fl = 2 * p["M"] * p["N"] * p["K"]
@@ -525,6 +531,9 @@ def measure_sweep(gpu, problems, peaks, with_quant=True):
             qb = quant_bytes(p["M"], p["K"], p["bw"])
             e["quant_us"] = round(qu, 3)
             e["quant_gbs"] = round(qb / (qu * 1e-6) / 1e9, 1)
+            # The public linear entry point (quantizer + GEMM, back to back):
+            # what the quantizer adds on top of the GEMM at this M.
+            e["linear_us"] = round(gpu.time_graph(body_l, REPS), 3)
         out.append(e)
     return out
 
@@ -663,9 +672,9 @@ def main():
             entries = measure_sweep(gpu, probs, peaks)
             configs[wl] = {"workload": WORKLOAD_DESC[wl], "per_m": [
                 [e["shape"], e["M"], e["gemm_us"], e["tflops"], e["gbs"], e["roofline_frac"], e["plan"],
-                 e.get("gemm_us_dsmem_exchange"), e["quant_us"]] for e in entries],
+                 e.get("gemm_us_dsmem_exchange"), e["quant_us"], e["linear_us"]] for e in entries],
                 "columns": ["shape", "M", "gemm_us", "tflops", "gbs", "roofline_frac", "plan",
-                            "gemm_us_dsmem_exchange", "quant_us"]}
+                            "gemm_us_dsmem_exchange", "quant_us", "linear_us"]}
             del probs
             torch.cuda.empty_cache()
 
