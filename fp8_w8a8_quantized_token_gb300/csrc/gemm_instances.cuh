@@ -1,5 +1,6 @@
 // gemm_instances.cuh -- the instantiations a translation unit provides:
-// swapped (decode) tiles of 16/32/64/128 tokens and non-swapped tiles of
+// swapped (decode) tiles of 16/32/64/128 tokens (16 and 32 also as stream-K
+// instantiations with a deeper ring) and non-swapped tiles of
 // 128 tokens x 256 output columns (prefill; 2-CTA pairs for channelwise)
 // or 128 / 64 / 32 columns (mid-size M), bf16 or fp16 output.
 #pragma once
@@ -26,6 +27,14 @@ cudaError_t dispatch_gemm(const GemmProblem &p, const GemmLaunch &l, unsigned *s
         if constexpr (BLOCKWISE)
             if (l.swap_ab && l.mma_n == 16)
                 return launch_gemm_inst<true, 16, kFusedQuantStages, true, OutT, false, true>(p, l, status, st);
+        return cudaErrorInvalidValue;
+    }
+    if (l.swap_ab && l.stream_k) {
+        // Stream-K: one CTA per SM at most, a deeper ring.
+        if (l.mma_n == 16)
+            return launch_gemm_inst<true, 16, stream_k_stages(16), BLOCKWISE, OutT>(p, l, status, st);
+        if (l.mma_n == 32)
+            return launch_gemm_inst<true, 32, stream_k_stages(32), BLOCKWISE, OutT>(p, l, status, st);
         return cudaErrorInvalidValue;
     }
     if (l.swap_ab) {

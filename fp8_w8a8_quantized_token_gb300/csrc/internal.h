@@ -87,6 +87,13 @@ constexpr int stages_for(bool swap_ab, int mma_n)
                    : (mma_n == 256 ? 4 : mma_n == 128 ? 6 : 8);
 }
 
+// Ring depth of the stream-K instantiations (16- and 32-token tiles).  A
+// stream-K grid has at most one CTA per SM, so the ring can take the shared
+// memory two split-K CTAs would share: 10 slots of 16 KB + 2 KB, 9 of
+// 16 KB + 4 KB.  Measured on gate_up at M = 1: 21.5 us with the 5-slot ring
+// of the 16-token split-K instantiation, 19.0 us with 8 slots.
+constexpr int stream_k_stages(int mma_n) { return mma_n == 16 ? 10 : 9; }
+
 // Ring depth of the fused-quantization instantiation (blockwise, 16-token
 // tiles): 4 slots of 16 KB + 2 KB plus a 4-slot bf16 staging ring of 4 KB
 // keep it near 100 KB, so two CTAs still fit on one SM.

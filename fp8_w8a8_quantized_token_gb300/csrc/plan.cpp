@@ -151,7 +151,7 @@ void plan_finish(int64_t M, int64_t N, int64_t K, int blockwise, int num_sms, fp
         pl->two_sm = 0;
         pl->grid = static_cast<int32_t>(total < sms ? total : sms);
         pl->persistent = 1;
-        pl->stages = stages_for(true, pl->mma_n);
+        pl->stages = stream_k_stages(pl->mma_n);
         return;
     }
     pl->stream_k = 0;
