@@ -42,9 +42,11 @@ def _fused(x, wq, ws, bias, fp16, ldx=None):
 
 
 def _two_kernel(x, wq, ws, bias, fp16):
+    # No workspace, as the fused kernel takes none: where the plan is
+    # stream-K both then run the same K-split schedule of the same tiles.
     xq, xsv = fq.fp8q_quant_per_token_group_row_padded(x, 128)
     return fq.fp8q_scaled_mm_blockwise(xq, wq, xsv, ws, bias=bias, M=x.shape[0],
-                                       out_dtype=torch.float16 if fp16 else torch.bfloat16)
+                                       out_dtype=torch.float16 if fp16 else torch.bfloat16, workspace=None)
 
 
 @pytest.mark.parametrize("M,N,K,bias,fp16", [
