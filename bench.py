@@ -57,6 +57,7 @@ PROFILE_CASES = {
     "mid_oproj_1024": ("channelwise", 1024, 4096, 4096),
     "decode_oproj": ("channelwise", 16, 4096, 4096),
     "decode_down": ("channelwise", 1, 4096, 12288),
+    "decode_gateup": ("channelwise", 1, 24576, 4096),     # stream-K in the tuned table
     "blockwise_prefill": ("blockwise", 8192, 24576, 3072),
     "blockwise_prefill_down": ("blockwise", 8192, 3072, 12288),
     "blockwise_decode": ("blockwise", 16, 4096, 7168),
