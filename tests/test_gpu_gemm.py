@@ -105,12 +105,17 @@ def test_stream_k_workspace_flags_and_repeats(dev, schedule, bw):
 
 
 def test_stream_k_without_workspace_falls_back(dev, schedule):
-    """A stream-K plan called without a workspace runs the tiles split along
-    K instead (same oracle bar)."""
+    """A stream-K plan called without a workspace, or with one 4 bytes short
+    (one flag), runs the tiles split along K instead: the two give identical
+    bits, and both meet the oracle bar."""
     fq.fp8q_set_plan_override(1, 32, 0)
     for M in (1, 20):
         out, ref = channelwise_case(dev, M, 768, 3072, seed=M, workspace=None)
         assert_gemm_close(out_values(out), ref, f"stream-K fallback M={M}")
+        need = fq.fp8q_workspace_bytes(M, 768, 3072)
+        short = torch.zeros(need - 4, dtype=torch.uint8, device=dev)
+        out_short, _ = channelwise_case(dev, M, 768, 3072, seed=M, workspace=short)
+        assert torch.equal(out_short, out), "a short workspace did not fall back to the K-split schedule"
 
 
 def test_stream_k_graph_replays(dev, schedule):
