@@ -47,6 +47,7 @@ EXPORTED = (
     "fp8q_workspace_bytes",
     "fp8q_set_plan_override",
     "fp8q_device_status",
+    "fp8q_last_device_status",
     "fp8q_selftest_wait_timeout",
     "fp8q_status_str",
     "fp8q_version",
@@ -97,6 +98,7 @@ def load_library(path: str | None = None):
         "fp8q_scaled_mm_w8a16": [P, I64, P, I64, P, P, P, I64, I64, I64, ctypes.c_int, P],
         "fp8q_gemm_plan": [I64, I64, I64, I32, I32, ctypes.POINTER(Plan)],
         "fp8q_device_status": [P, I32],
+        "fp8q_last_device_status": [P],
         "fp8q_selftest_wait_timeout": [P],
         "fp8q_set_plan_override": [I32, I32, I32],
     }

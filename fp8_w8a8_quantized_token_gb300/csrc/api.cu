@@ -342,6 +342,8 @@ fp8q_status fp8q_device_status(void *stream, int32_t reset)
     return v == 0 ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
 
+fp8q_status fp8q_last_device_status(void *stream) { return fp8q_device_status(stream, 0); }
+
 const char *fp8q_status_str(fp8q_status status)
 {
     switch (status) {

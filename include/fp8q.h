@@ -453,6 +453,10 @@ FP8Q_API fp8q_status fp8q_set_plan_override(int32_t swap_ab, int32_t mma_n, int3
  * Synchronizes `stream`.  reset != 0 clears the word afterwards. */
 FP8Q_API fp8q_status fp8q_device_status(void *stream, int32_t reset);
 
+/* The same word read without clearing it: fp8q_device_status(stream, 0),
+ * under the name the boundary's design used. */
+FP8Q_API fp8q_status fp8q_last_device_status(void *stream);
+
 /* Diagnostics (the pages have no counterpart): enqueue a one-warp kernel
  * whose pipeline wait can never complete.  The bounded wait the GEMM uses
  * gives up after its time limit (about 2 s), records FP8Q_ERR_TIMEOUT in

@@ -1,6 +1,7 @@
 """Failure detection on the GPU without a GPU fault: a pipeline wait that can
 never complete gives up after its time limit, the device status word reports
 FP8Q_ERR_TIMEOUT, reading it resets it, and the context keeps working."""
+import ctypes
 import time
 
 import pytest
@@ -28,10 +29,14 @@ def test_stalled_wait_reports_timeout_and_the_context_survives(dev):
     assert fq.fp8q_device_status(reset=True) == fq.FP8Q_OK
     t0 = time.monotonic()
     fq.fp8q_selftest_wait_timeout()
-    status = fq.fp8q_device_status(reset=True)      # synchronizes the stream
+    L = fq.load_library()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    status = L.fp8q_last_device_status(stream)        # synchronizes the stream, keeps the word
     waited = time.monotonic() - t0
     assert status == fq.FP8Q_ERR_TIMEOUT
     assert 1.5 < waited < 60, waited                   # the 2 s limit, not a hang
+    assert L.fp8q_last_device_status(stream) == fq.FP8Q_ERR_TIMEOUT
+    assert fq.fp8q_device_status(reset=True) == fq.FP8Q_ERR_TIMEOUT
     assert fq.fp8q_device_status(reset=True) == fq.FP8Q_OK
 
     # the same context still computes correctly
