@@ -836,7 +836,7 @@ def measure_fused(gpu, peaks, synthetic):
     fwq0, fws = fq.fp8q_quant_weight_block128(fw)
     del fw
     fcopies = [fwq0] + [fwq0.clone() for _ in range(REPS - 1)]
-    for fM in (1, 16):
+    for fM in (1, 16, 32):
         fx = synthetic.activations(fM, fK, outliers=True).to(dev)
         fm_pad = (fM + 3) // 4 * 4
         fxq = torch.empty((fm_pad, fK), dtype=fq.E4M3, device=dev)

@@ -434,7 +434,7 @@ def fp8q_linear_blockwise_fused(x: torch.Tensor, w: torch.Tensor, w_scale: torch
                                 out_dtype=torch.bfloat16):
     """The blockwise linear layer in one kernel: group-128 quantization of
     the bf16 activations inside the GEMM (decode sizes whose schedule is the
-    16-token tile; otherwise FP8Q_ERR_UNSUPPORTED).  Bit-identical to
+    16- or 32-token tile; otherwise FP8Q_ERR_UNSUPPORTED).  Bit-identical to
     fp8q_linear_blockwise on the same schedule."""
     L = load_library()
     _need(x, torch.bfloat16, "x")

@@ -279,7 +279,7 @@ fp8q_status fp8q_linear_blockwise_fused(const void *x, int64_t ldx, const void *
     fp8q_plan pl;
     const fp8q_status s = fp8q_gemm_plan(M, N, K, 1, 0, &pl);
     if (s != FP8Q_OK) return s;
-    if (!pl.swap_ab || pl.mma_n != 16) return FP8Q_ERR_UNSUPPORTED;
+    if (!pl.swap_ab || (pl.mma_n != 16 && pl.mma_n != 32)) return FP8Q_ERR_UNSUPPORTED;
     GemmProblem p;
     p.M = M; p.N = N; p.K = K; p.m_pad = M;
     p.a = x; p.lda = ldx; p.w = w; p.ldw = K;

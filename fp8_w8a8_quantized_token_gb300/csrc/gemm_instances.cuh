@@ -23,10 +23,13 @@ cudaError_t dispatch_gemm(const GemmProblem &p, const GemmLaunch &l, unsigned *s
         return cudaErrorInvalidValue;
     }
     if (p.fused_quant) {
-        // Quantization fused into the GEMM: blockwise 16-token decode tiles.
+        // Quantization fused into the GEMM: blockwise 16- and 32-token decode tiles.
         if constexpr (BLOCKWISE)
             if (l.swap_ab && l.mma_n == 16)
                 return launch_gemm_inst<true, 16, kFusedQuantStages, true, OutT, false, true>(p, l, status, st);
+        if constexpr (BLOCKWISE)
+            if (l.swap_ab && l.mma_n == 32)
+                return launch_gemm_inst<true, 32, kFusedQuantStages32, true, OutT, false, true>(p, l, status, st);
         return cudaErrorInvalidValue;
     }
     if (l.swap_ab && l.stream_k) {

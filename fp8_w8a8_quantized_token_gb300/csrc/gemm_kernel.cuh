@@ -210,7 +210,7 @@ struct GemmCfg {
     static constexpr uint32_t kSASlot = BLOCKWISE ? (kSABytes + 127u) / 128u * 128u : 0u;
     static constexpr int kSASlotFloats = static_cast<int>(kSASlot / 4u);
     // Bytes one ring slot's full barrier waits for (TWO_SM: both CTAs' loads).
-    // Fused quantization (FQ; blockwise, swapped 16-token tiles): the
+    // Fused quantization (FQ; blockwise, swapped 16- or 32-token tiles): the
     // producer loads only the weight slices; two quantizing warps copy the
     // bf16 activation tiles (BN rows x 128 columns) into a staging ring of
     // their own and turn them into the ring's B tiles and scale slots.
@@ -270,7 +270,8 @@ struct GemmCfg {
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
     static_assert(kCols % 32 == 0 || kCols == 16, "epilogue column chunking");
     static_assert(2 * kSlotCols <= 512, "TMEM columns");
-    static_assert(!FQ || (BLOCKWISE && SWAP && BN == 16 && !TWO_SM), "fused quantization: blockwise 16-token tiles");
+    static_assert(!FQ || (BLOCKWISE && SWAP && (BN == 16 || BN == 32) && !TWO_SM),
+                  "fused quantization: blockwise 16- and 32-token tiles");
     static_assert(!W16 || (!BLOCKWISE && SWAP && !TWO_SM && !FQ && BN <= 32), "W16: swapped channelwise tiles");
     static_assert(kTmemNeed <= 512, "tensor memory budget exceeded");
 };
@@ -941,8 +942,8 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
     } else if (FQ && warp >= C::kQuantWarp0) {
         // ------------------------------------------------------------------
         // Quantizing warps (FQ): this CTA's K blocks g = 0, 1, ... (its tiles
-        // in order, nkb blocks each).  Each thread owns two 16-element chunks
-        // of every block (rows t0 and t0 + 8, chunk c) and copies them itself
+        // in order, nkb blocks each).  Each thread owns BN/8 16-element chunks
+        // of every block (rows t0, t0 + 8, ..., chunk c) and copies them itself
         // into staging slot g % kXStages with cp.async (16-byte global ->
         // shared copies, zero-filled past row M; not the TMA unit, whose
         // queue holds the weight tiles), kXStages blocks ahead, one commit
@@ -959,7 +960,8 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
         // ------------------------------------------------------------------
         if constexpr (FQ) {
             const int qt = threadIdx.x - 32 * C::kQuantWarp0;  // 0 .. 63
-            const int t0 = qt >> 3, c = qt & 7;                 // rows t0 and t0 + 8, chunk c
+            const int t0 = qt >> 3, c = qt & 7;                 // rows t0, t0 + 8, ..., chunk c
+            constexpr int kRowsPer = BN / 8;                    // rows of the tile per thread
             const long long total =
                 cluster_id < p.num_tiles
                     ? static_cast<long long>((p.num_tiles - 1 - cluster_id) / num_clusters + 1) * nkb
@@ -973,7 +975,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                     const int k0 = (kb_begin + static_cast<int>(g % nkb)) * 128 + c * 16;
                     uint8_t *slot = sX + static_cast<int>(g % C::kXStages) * C::kXBytes;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
+                    for (int h = 0; h < kRowsPer; ++h) {
                         const int t = t0 + 8 * h;
                         const int m = b_q * BN + t;
                         const bool in = m < p.M;
@@ -995,7 +997,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                 uint8_t *bt = sB + stage * C::kBBytes;
                 float *sa = sSA + stage * C::kSASlotFloats;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int h = 0; h < kRowsPer; ++h) {
                     const int t = t0 + 8 * h;
                     const Chunk16 v = load_chunk_smem(xs + t * 256 + c * 32);
                     float m = chunk_amax(v, 0.0f);

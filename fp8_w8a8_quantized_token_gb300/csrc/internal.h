@@ -98,6 +98,9 @@ constexpr int stream_k_stages(int mma_n) { return mma_n == 16 ? 10 : 9; }
 // tiles): 4 slots of 16 KB + 2 KB plus a 4-slot bf16 staging ring of 4 KB
 // keep it near 100 KB, so two CTAs still fit on one SM.
 constexpr int kFusedQuantStages = 4;
+// (32-token tiles: 3 slots of 16 KB + 4 KB and a 3-slot staging ring of 8 KB
+// keep the CTA near 105 KB as well.)
+constexpr int kFusedQuantStages32 = 3;
 
 // Depth of the MMA ring of the weight-only FP8 (W16) instantiations: per
 // stage a bf16 A tile in tensor memory (64 columns) and the token tile's bf16

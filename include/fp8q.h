@@ -330,9 +330,10 @@ FP8Q_API fp8q_status fp8q_scaled_mm_w8a16(const void *x, int64_t ldx, const void
  * and scales are those of fp8q_quant_per_token_group_row_padded (g = 128,
  * eps = 1e-10), so the output is bit-identical to fp8q_linear_blockwise on
  * the same schedule.
- * Available where the planner's schedule is the 16-token swapped tile
- * (decode sizes, M <= 16 on the compiled table's shapes); other problems
- * return FP8Q_ERR_UNSUPPORTED.  Measured on GB300 it is SLOWER than the
+ * Available where the planner's schedule is the 16- or 32-token swapped
+ * tile (decode sizes, M <= 32 on the compiled table's shapes); other
+ * problems return FP8Q_ERR_UNSUPPORTED.  A stream-K plan runs here as the
+ * same tiles split along K (no workspace is taken).  Measured on GB300 it is SLOWER than the
  * two-kernel fp8q_linear_blockwise on back-to-back layers (the activation
  * reads issued after the dependency wait queue behind the weight stream),
  * so fp8q_linear_blockwise does not use it; it is for callers that want a

@@ -1,4 +1,4 @@
-"""Quantization fused into the blockwise GEMM (decode, 16-token tiles):
+"""Quantization fused into the blockwise GEMM (decode, 16- and 32-token tiles):
 fp8q_linear_blockwise_fused quantizes the bf16 activation tiles inside the
 GEMM.  Its codes and scales are the standalone quantizer's, so its output
 must be bit-identical to the two-kernel path (group quantizer + blockwise
@@ -57,10 +57,18 @@ def _two_kernel(x, wq, ws, bias, fp16):
     (13, 24576, 3072, False, False),     # wide N
     (5, 256, 512, True, True),           # tiny: one K block per CTA
     (16, 512, 128, False, False),        # K = one block
+    # 32-token tiles (four rows per quantizing thread)
+    (32, 4096, 7168, False, False),
+    (31, 4096, 7168, True, True),        # ragged token tile
+    (19, 256, 512, True, False),         # 13 zero-filled token rows
+    (32, 512, 128, False, True),
+    (29, 512, 1024, True, False),
+    (25, 1024, 1024, False, False),
+    (32, 24576, 3072, True, False),      # stream-K plan: runs split along K
 ])
 def test_fused_equals_two_kernel_path_and_oracle(dev, M, N, K, bias, fp16):
     plan = fq.fp8q_gemm_plan(M, N, K, True)
-    assert plan["swap_ab"] == 1 and plan["mma_n"] == 16, plan
+    assert plan["swap_ab"] == 1 and plan["mma_n"] in (16, 32), plan
     x = synthetic.activations(M, K, outliers=True, seed=M * 3 + K).to(dev)
     w = synthetic.weights(N, K, seed=N + K).to(dev)
     wq, ws = fq.fp8q_quant_weight_block128(w)
@@ -104,7 +112,7 @@ def test_fused_strided_input_and_unsupported_schedule(dev):
     ref2 = _two_kernel(x.contiguous(), wq, ws, None, False)
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), ref2.view(torch.int16))
-    # a prefill size has no 16-token schedule: refused, nothing enqueued
+    # a prefill size has no 16- or 32-token schedule: refused, nothing enqueued
     xp = synthetic.activations(512, K, seed=83).to(dev)
     with pytest.raises(RuntimeError, match="UNSUPPORTED"):
         fq.fp8q_linear_blockwise_fused(xp, wq, ws)
