@@ -180,6 +180,12 @@ struct GemmCfg {
     static constexpr int kConvWarps = W16 ? 8 : 0;
     static constexpr int kConvWarp0 = kQuantWarp0 + kQuantWarps;
     static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps + kQuantWarps + kConvWarps);
+    // CTAs per SM the register allocation must allow.  The fused-quantization
+    // tiles run clusters of up to 8 CTAs along K: with one CTA per SM, few
+    // such clusters fit in a GPC at once (the 32-token tile at 139 registers
+    // took 48 us for blockwise 4096 x 7168 at M = 32, against 11.5 us for the
+    // two-kernel path), so they are held to two CTAs per SM.
+    static constexpr int kMinBlocks = FQ ? 2 : 1;
     static_assert(!kRegSplit || (kThreads == 384 && kEpiWarp0 == 4 && kEpiWarps == 8 &&
                                  kLowRegs * 128 + kHighRegs * 256 == kLaunchRegs * kThreads),
                   "register split: warpgroup 0 low, warpgroups 1-2 high, same total as at launch");
@@ -538,7 +544,8 @@ __device__ __noinline__ void reduce_split_workspace(const GemmArgs &p, uint8_t *
 
 template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT, bool TWO_SM = false, bool FQ = false,
           bool W16 = false>
-__global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ, W16>::kThreads, 1)
+__global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ, W16>::kThreads,
+                                  GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ, W16>::kMinBlocks)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sa, const __grid_constant__ CUtensorMap tm_out,
                     const GemmArgs p)

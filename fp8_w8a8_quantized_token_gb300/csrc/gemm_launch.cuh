@@ -107,7 +107,7 @@ cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigne
     a.ldo = pr.N;
     a.status = status;
     a.trace = trace_buffer();
-    a.prefetch_kb = prefetch_kblocks();
+    a.prefetch_kb = prefetch_kblocks(SWAP, BLOCKWISE, l.grid);
     a.preload = pr.preload ? 1 : 0;
     a.eps = pr.eps;
     a.x = FQ ? static_cast<const __nv_bfloat16 *>(pr.a) : nullptr;

@@ -91,13 +91,16 @@ unsigned long long *trace_buffer()
 #endif
 }
 
-int prefetch_kblocks()
+int prefetch_kblocks(bool swapped, bool blockwise, int grid)
 {
     static const int v = [] {
         const char *s = getenv("FP8Q_PREFETCH_KB");
-        return s != nullptr ? atoi(s) : 16;
+        return s != nullptr ? atoi(s) : -1;
     }();
-    return v;
+    if (v >= 0) return v;
+    if (!swapped) return 0;
+    if (!blockwise) return 16;
+    return 2 * static_cast<long long>(grid) <= 3 * static_cast<long long>(current_device_sms()) ? 16 : 0;
 }
 
 bool workspace_exchange_enabled()

@@ -131,8 +131,16 @@ unsigned *device_status_ptr();   // of the current device, or null
 // Per-CTA phase timestamps of a trace build (-DFP8Q_TRACE); null otherwise.
 unsigned long long *trace_buffer();
 // Weight K blocks each GEMM CTA prefetches into L2 before its dependency
-// wait (default 16; FP8Q_PREFETCH_KB overrides it at start-up, 0 disables).
-int prefetch_kblocks();
+// wait: 16 for swapped (decode) tiles -- blockwise ones only while the grid
+// is at most 1.5 CTAs per SM -- and none for non-swapped tiles;
+// FP8Q_PREFETCH_KB overrides the rule at start-up (0 disables).  Measured on
+// GB300 over rotating weight copies (more than L2), two interleaved runs
+// each: the prefetch shortens o_proj decode from 6.72 to 6.22 us (128 CTAs,
+// 8 K blocks each) and blockwise 3072 x 12288 decode from 11.1 to 10.55 us
+// (192 CTAs), but lengthens blockwise 4096 x 7168 decode (256 CTAs, 9.08 ->
+// 9.25 us) and every non-swapped size by 1-6 % (o_proj M = 512: 12.56 ->
+// 12.85 us; down M = 256: 19.9 -> 21.2 us).
+int prefetch_kblocks(bool swapped, bool blockwise, int grid);
 // Split-K partial sums through the caller's workspace (global memory)
 // instead of distributed shared memory: off unless FP8Q_WORKSPACE_EXCHANGE=1
 // at start-up.  On the GB300s measured, reading partials that other SMs of

@@ -5,7 +5,10 @@
 // takes the entry of the nearest M, ties going to the smaller M (the
 // nearest-M rule of get_w8a8_channelwise_fp8_config on the "Tune FP8 GEMM
 // Triton tiles on L40S and enable by default" page, key source snippets,
-// whose keys are scanned in ascending order).  Shapes without a table entry
+// whose keys are scanned in ascending order), except that a smaller-M row
+// whose token tile M outgrows is passed over for a larger-M row (the
+// schedules here fix the token tile, the page's configs only block sizes).
+// Shapes without a table entry
 // use the generic rule.  fp8q_set_plan_override (or FP8Q_PLAN="swap,mma_n,
 // split" at start-up) forces a schedule for tests and sweeps; FP8Q_LOG=1
 // prints each new choice once to stderr.
@@ -95,13 +98,31 @@ bool override_plan(fp8q_plan *pl)
     return true;
 }
 
+// Token tiles of a row's schedule at M tokens.
+int64_t token_tiles(const TableEntry &e, int64_t M)
+{
+    const int64_t tile_m = e.swap_ab ? e.mma_n : 128;
+    return (M + tile_m - 1) / tile_m;
+}
+
 bool table_plan(int64_t M, int64_t N, int64_t K, int blockwise, fp8q_plan *pl)
 {
+    // A row swept at a smaller M is not taken where M needs more token tiles
+    // than that row's M did (every weight tile would be read once more per
+    // extra token tile) while a row at a larger M exists: blockwise 4096 x
+    // 7168 at M = 17 ran 18.5 us on the M = 16 row's 16-token tiles and
+    // 11.5 us on the M = 32 row's 32-token tile.
+    bool larger = false;
+    for (int i = 0; i < kTableSize; ++i) {
+        const TableEntry &e = kTable[i];
+        if (e.N == N && e.K == K && e.blockwise == blockwise && e.M >= M) larger = true;
+    }
     const TableEntry *best = nullptr;
     int64_t best_d = 0;
     for (int i = 0; i < kTableSize; ++i) {
         const TableEntry &e = kTable[i];
         if (e.N != N || e.K != K || e.blockwise != blockwise) continue;
+        if (larger && e.M < M && token_tiles(e, M) > token_tiles(e, e.M)) continue;
         const int64_t d = e.M > M ? e.M - M : M - e.M;
         if (best == nullptr || d < best_d || (d == best_d && e.M < best->M)) {
             best = &e;

@@ -124,7 +124,8 @@ def load_table():
 def test_table_lookup_is_nearest_m_with_ties_to_the_smaller_m():
     """The rule of get_w8a8_channelwise_fp8_config: the entry of the key
     nearest to M, keys scanned in ascending order, so a tie goes to the
-    smaller key."""
+    smaller key -- among the keys whose schedule M does not push to more
+    token tiles than the key itself had (while a key >= M exists)."""
     rows = load_table()
     assert rows, "the sweep table is empty"
     by_shape = {}
@@ -135,8 +136,13 @@ def test_table_lookup_is_nearest_m_with_ties_to_the_smaller_m():
         keys = [m for m, _ in entries]
         table = dict(entries)
         probe = sorted(set(keys + [(a + b) // 2 for a, b in zip(keys, keys[1:])] + [k + 1 for k in keys] + [3, 10000]))
+        def tiles(k, m):
+            swap, mma_n, _ = table[k]
+            tm = mma_n if swap else 128
+            return -(-m // tm)
         for M in probe:
-            best = min(keys, key=lambda k: abs(k - M))   # Python's min keeps the first (smallest) on ties
+            ok = [k for k in keys if not (k < M and max(keys) >= M and tiles(k, M) > tiles(k, k))]
+            best = min(ok, key=lambda k: abs(k - M))   # Python's min keeps the first (smallest) on ties
             swap, mma_n, split = table[best]
             p = fq.fp8q_gemm_plan(M, N, K, bool(bw), num_sms=148)
             assert p["from_table"] == 1
