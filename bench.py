@@ -42,7 +42,7 @@ UNIT = "TFLOP/s"
 # o_proj sweep, the 2-CTA prefill kernel's four launches M = 1024 .. 8192 of
 # "oproj_prefill_group", averaged.  A key is dropped whenever its kernel
 # changes.
-DOMINANT_TRAFFIC_BYTES = {("channelwise", 0, 256, 1): 39.94e6}
+DOMINANT_TRAFFIC_BYTES = {("channelwise", 0, 256, 1): 39.99e6}
 
 # Small fixed cases for Nsight Compute captures: name -> (kind, M, N, K).
 PROFILE_CASES = {
