@@ -49,6 +49,7 @@ EXPORTED = (
     "fp8q_device_status",
     "fp8q_last_device_status",
     "fp8q_selftest_wait_timeout",
+    "fp8q_selftest_silu_mul",
     "fp8q_status_str",
     "fp8q_version",
 )
@@ -100,6 +101,7 @@ def load_library(path: str | None = None):
         "fp8q_device_status": [P, I32],
         "fp8q_last_device_status": [P],
         "fp8q_selftest_wait_timeout": [P],
+        "fp8q_selftest_silu_mul": [P, P, P, I64, P],
         "fp8q_set_plan_override": [I32, I32, I32],
     }
     for name, args in sig.items():

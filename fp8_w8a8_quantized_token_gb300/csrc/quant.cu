@@ -41,41 +41,20 @@ __device__ __forceinline__ float pow2_ceil(float s)
     return __uint_as_float(b);
 }
 
-// exp(t) in fp32 as a fixed sequence of IEEE fp32 operations (no library
-// exp): Cody and Waite's range reduction (W. J. Cody, W. Waite, "Software
-// Manual for the Elementary Functions", 1980) with fused multiply-adds --
-// n = rint(t * log2 e), r = t - n*ln2_hi - n*ln2_lo, ln2_hi = ln 2 rounded
-// to fp32 and ln2_lo the fp32 rounding of the rest -- then the Taylor
-// series of exp(r) to degree 7 (coefficients 1/k! rounded to fp32, Horner's
-// rule with FMAs) and the exact scaling by 2^n.  t > 88: +inf; t < -32: 0
-// (exp(t) < 2^-46 cannot change 1 + exp(t), its only use).  Explicit
-// __f*_rn intrinsics keep the compiler from contracting or reordering.
-__device__ __forceinline__ float exp_fixed(float t)
+// Quotients RN(y / s) of four fp32 values, for 2^-90 <= s <= 3e38 with
+// r = RN(1 / s): Markstein's correction (see quotient2 in quant_common.cuh)
+// gives the correctly rounded quotient whenever the remainder y - q0 * s is
+// exact, which holds while it is a normal number.  For |y / s| >= 2^-11 the
+// remainder is about 2^-24 |y| >= 2^-35 s >= 2^-125: normal.  Below 2^-11
+// a quotient off by an ulp still rounds to the same signed zero in E4M3 (the
+// smallest code is 2^-9).  Every y of the group is finite here: for finite
+// inputs y is finite or an overflow to +-inf, and an infinite y makes the
+// group's scale infinite, which takes the IEEE division instead.
+__device__ __forceinline__ uint32_t quant4_f32(const float *y, float s, float r)
 {
-    if (t > 88.0f) return __uint_as_float(0x7F800000u);
-    if (t < -32.0f) return 0.0f;
-    const float n = rintf(__fmul_rn(t, 0x1.715476p+0f));
-    float r = __fmaf_rn(-n, 0x1.62e430p-1f, t);
-    r = __fmaf_rn(-n, -0x1.05c610p-29f, r);
-    float p = 0x1.a01a02p-13f;
-    p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);
-    p = __fmaf_rn(p, r, 0x1.111112p-7f);
-    p = __fmaf_rn(p, r, 0x1.555556p-5f);
-    p = __fmaf_rn(p, r, 0x1.555556p-3f);
-    p = __fmaf_rn(p, r, 0.5f);
-    p = __fmaf_rn(p, r, 1.0f);
-    p = __fmaf_rn(p, r, 1.0f);
-    return __fmul_rn(p, __int_as_float((static_cast<int>(n) + 127) << 23));
-}
-
-// silu(a) * b in fp32: a / (1 + exp(-a)) (IEEE add and division), times b
-// -- the fuse_silu_and_mul input of the group quantizer (row-padding page,
-// key source snippets): gate a from the first half of the row, up b from
-// the second, no rounding to bf16 in between.
-__device__ __forceinline__ float silu_mul(float a, float b)
-{
-    const float den = __fadd_rn(1.0f, exp_fixed(-a));
-    return __fmul_rn(__fdiv_rn(a, den), b);
+    const float2 a = quotient2(make_float2(y[0], y[1]), s, r);
+    const float2 b = quotient2(make_float2(y[2], y[3]), s, r);
+    return cvt_e4m3x2(a.x, a.y) | (cvt_e4m3x2(b.x, b.y) << 16);
 }
 
 // Programmatic dependent launch: each quantizer first waits for the
@@ -171,10 +150,9 @@ __global__ void __launch_bounds__(1024) quant_per_token_two_pass_kernel(const __
 // Options (the scale_ue8m0 and fuse_silu_and_mul arguments of the group
 // quantizer on the row-padding page): UE8M0 rounds each scale up to a power
 // of two; SILU reads rows of 2K values and quantizes y = silu(x[k]) *
-// x[K + k] (fp32), dividing with the IEEE division (y is a general fp32
-// value, outside the bf16 numerators the quotient2() shortcut is checked
-// for; measured, the shortcut does not speed this kernel up: it is bound by
-// the ~38 fp32 instructions per element of exp, silu and quantization).
+// x[K + k] (fp32): exp, silu's add and product and the quotients by the
+// group scale run on fp32 pairs (the kernel is bound by its instruction
+// issue, not by HBM).
 // ---------------------------------------------------------------------------
 template <int TPG, bool UE8M0, bool SILU>
 __global__ void __launch_bounds__(256) quant_group_kernel(const __nv_bfloat16 *__restrict__ x, int64_t ldx,
@@ -210,9 +188,11 @@ __global__ void __launch_bounds__(256) quant_group_kernel(const __nv_bfloat16 *_
                 const uint32_t uw[8] = {u.lo.x, u.lo.y, u.lo.z, u.lo.w, u.hi.x, u.hi.y, u.hi.z, u.hi.w};
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    y[2 * i] = silu_mul(bf_lo(gw[i]), bf_lo(uw[i]));
-                    y[2 * i + 1] = silu_mul(bf_hi(gw[i]), bf_hi(uw[i]));
-                    m = fmaxf(m, fmaxf(fabsf(y[2 * i]), fabsf(y[2 * i + 1])));
+                    const float2 y2 = silu_mul2(make_float2(bf_lo(gw[i]), bf_hi(gw[i])),
+                                                make_float2(bf_lo(uw[i]), bf_hi(uw[i])));
+                    y[2 * i] = y2.x;
+                    y[2 * i + 1] = y2.y;
+                    m = fmaxf(m, fmaxf(fabsf(y2.x), fabsf(y2.y)));
                 }
             } else {
                 m = chunk_amax(c, 0.0f);
@@ -226,10 +206,16 @@ __global__ void __launch_bounds__(256) quant_group_kernel(const __nv_bfloat16 *_
             uint4 q;
             if constexpr (SILU) {
                 uint32_t w[4];
+                if (s >= 0x1p-90f && s <= 3.0e38f) {
+                    const float r = 1.0f / s;
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    w[i] = cvt_e4m3x2(__fdiv_rn(y[4 * i], s), __fdiv_rn(y[4 * i + 1], s)) |
-                           (cvt_e4m3x2(__fdiv_rn(y[4 * i + 2], s), __fdiv_rn(y[4 * i + 3], s)) << 16);
+                    for (int i = 0; i < 4; ++i) w[i] = quant4_f32(y + 4 * i, s, r);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        w[i] = cvt_e4m3x2(__fdiv_rn(y[4 * i], s), __fdiv_rn(y[4 * i + 1], s)) |
+                               (cvt_e4m3x2(__fdiv_rn(y[4 * i + 2], s), __fdiv_rn(y[4 * i + 3], s)) << 16);
+                }
                 q = make_uint4(w[0], w[1], w[2], w[3]);
             } else {
                 q = quant_chunk(c, s);

@@ -123,6 +123,62 @@ __device__ __forceinline__ uint2 quant_unit8(const uint4 &v, float s, float r, b
     return make_uint2(quant4_div(v.x, v.y, s), quant4_div(v.z, v.w, s));
 }
 
+// exp(t) in fp32 as a fixed sequence of IEEE fp32 operations (no library
+// exp): Cody and Waite's range reduction (W. J. Cody, W. Waite, "Software
+// Manual for the Elementary Functions", 1980) with fused multiply-adds --
+// n = rint(t * log2 e), r = t - n*ln2_hi - n*ln2_lo, ln2_hi = ln 2 rounded
+// to fp32 and ln2_lo the fp32 rounding of the rest -- then the Taylor
+// series of exp(r) to degree 7 (coefficients 1/k! rounded to fp32, Horner's
+// rule with FMAs) and the exact scaling by 2^n.  t > 88: +inf; t < -32: 0
+// (exp(t) < 2^-46 cannot change 1 + exp(t), its only use).
+// Two values at a time: the packed fp32x2 operations (__ffma2_rn,
+// __fmul2_rn, __fadd2_rn) round each lane exactly as the scalar operation
+// does.  n = rint(u) for u = t * log2 e is formed as (u + 1.5 * 2^23) -
+// 1.5 * 2^23, which rounds u to the nearest integer (ties to even) for
+// |u| < 2^22 -- all of [-32, 88] -- and leaves n + 127 in the low bits of
+// u + 1.5 * 2^23 for the exponent of 2^n.  fma(-n, c, x) is written
+// fma(n, -c, x) (the same exact product).  Lanes outside [-32, 88] are
+// computed and then replaced.
+__device__ __forceinline__ float2 exp_fixed2(float2 t)
+{
+    constexpr float kShift = 0x1.8p23f;
+    const float2 u = __fmul2_rn(t, make_float2(0x1.715476p+0f, 0x1.715476p+0f));
+    const float2 big = __fadd2_rn(u, make_float2(kShift, kShift));
+    const float2 n = __fadd2_rn(big, make_float2(-kShift, -kShift));
+    float2 r = __ffma2_rn(n, make_float2(-0x1.62e430p-1f, -0x1.62e430p-1f), t);
+    r = __ffma2_rn(n, make_float2(0x1.05c610p-29f, 0x1.05c610p-29f), r);
+    float2 p = make_float2(0x1.a01a02p-13f, 0x1.a01a02p-13f);
+    p = __ffma2_rn(p, r, make_float2(0x1.6c16c2p-10f, 0x1.6c16c2p-10f));
+    p = __ffma2_rn(p, r, make_float2(0x1.111112p-7f, 0x1.111112p-7f));
+    p = __ffma2_rn(p, r, make_float2(0x1.555556p-5f, 0x1.555556p-5f));
+    p = __ffma2_rn(p, r, make_float2(0x1.555556p-3f, 0x1.555556p-3f));
+    p = __ffma2_rn(p, r, make_float2(0.5f, 0.5f));
+    p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
+    p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
+    constexpr uint32_t kBias = 127u - 0x4B400000u;   // bits of 1.5 * 2^23 + n  ->  n + 127
+    const float2 scale = make_float2(__uint_as_float((__float_as_uint(big.x) + kBias) << 23),
+                                     __uint_as_float((__float_as_uint(big.y) + kBias) << 23));
+    float2 e = __fmul2_rn(p, scale);
+    if (t.x > 88.0f) e.x = __uint_as_float(0x7F800000u);
+    if (t.x < -32.0f) e.x = 0.0f;
+    if (t.y > 88.0f) e.y = __uint_as_float(0x7F800000u);
+    if (t.y < -32.0f) e.y = 0.0f;
+    return e;
+}
+
+// silu(a) * b in fp32 for two lanes: a / (1 + exp(-a)) (IEEE add and
+// division), times b -- the fuse_silu_and_mul input of the group quantizer
+// (row-padding page, key source snippets): gate a from the first half of
+// the row, up b from the second, no rounding to bf16 in between.  (A
+// division by the approximate reciprocal, one Newton step and Markstein's
+// correction matched the IEEE quotient on every finite bf16 gate but did
+// not make the kernel faster, so the IEEE division stays.)
+__device__ __forceinline__ float2 silu_mul2(float2 a, float2 b)
+{
+    const float2 den = __fadd2_rn(make_float2(1.0f, 1.0f), exp_fixed2(make_float2(-a.x, -a.y)));
+    return __fmul2_rn(make_float2(__fdiv_rn(a.x, den.x), __fdiv_rn(a.y, den.y)), b);
+}
+
 // 16 consecutive bf16 values from shared memory (16-byte aligned).
 __device__ __forceinline__ Chunk16 load_chunk_smem(const void *p)
 {

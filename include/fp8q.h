@@ -466,6 +466,19 @@ FP8Q_API fp8q_status fp8q_last_device_status(void *stream);
  * Returns FP8Q_OK if the kernel was enqueued, ERR_CUDA otherwise. */
 FP8Q_API fp8q_status fp8q_selftest_wait_timeout(void *stream);
 
+/* Diagnostics: out[i] = silu(a[i]) * b[i] in fp32 for i < n, computed by the
+ * device function of the silu_and_mul-fused group quantizer
+ * (FP8Q_QUANT_SILU_AND_MUL; the silu_and_mul input of the row-padding page,
+ * key source snippets): a / (1 + exp(-a)) with the library's fixed exp
+ * sequence and the correctly rounded fp32 add and quotient, then one fp32
+ * multiply by b.  Lets tests compare that arithmetic with a reference bit for
+ * bit rather than through 8-bit codes.
+ * a, b, out: device fp32 arrays of n elements (4-byte aligned); n >= 0
+ * (n = 0: nothing is enqueued).  Enqueued on `stream`, not synchronized.
+ * Errors: INVALID_ARG (n < 0 or above 2^40, a null pointer with n > 0),
+ * ERR_CUDA (launch failure). */
+FP8Q_API fp8q_status fp8q_selftest_silu_mul(const float *a, const float *b, float *out, int64_t n, void *stream);
+
 /* Human-readable name of a status code (static string). */
 FP8Q_API const char *fp8q_status_str(fp8q_status status);
 

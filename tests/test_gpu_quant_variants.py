@@ -97,6 +97,90 @@ def test_silu_every_bf16_gate_value(dev):
         _group_both(x, dev, 16, ue8m0, True, row_alignment=1)
 
 
+def _random_bf16_bits(rng, shape, exp_lo, exp_hi):
+    """bf16 values with uniform random sign and 7-bit significand and a
+    uniform exponent in [exp_lo, exp_hi] (biased)."""
+    sign = rng.integers(0, 2, shape, dtype=np.uint32) << 15
+    expo = rng.integers(exp_lo, exp_hi + 1, shape, dtype=np.uint32) << 7
+    frac = rng.integers(0, 128, shape, dtype=np.uint32)
+    return (sign | expo | frac).astype(np.uint16)
+
+
+@pytest.mark.parametrize("g", [16, 128])
+def test_silu_random_significands_bit_exact(dev, g):
+    """Gate and up values with random significands over 2^-20 .. 2^12, so
+    the fp32 products silu(gate) * up and their quotients by the group scale
+    take general 24-bit significands (the quantizer divides them with a
+    Markstein correction): codes and scales bit-exact against the oracle."""
+    rng = np.random.default_rng(g)
+    M, K = 512, 4096
+    gate = _random_bf16_bits(rng, (M, K), 127 - 20, 127 + 12)
+    up = _random_bf16_bits(rng, (M, K), 127 - 20, 127 + 12)
+    x = torch.from_numpy(np.concatenate([gate, up], axis=1).view(np.int16)).view(torch.bfloat16)
+    _group_both(x, dev, g, False, True)
+
+
+def test_silu_tiny_scales_take_the_division(dev):
+    """Groups whose scale is below 2^-90 (tiny values, eps 1e-38) quantize
+    with the IEEE division: bit-exact against the oracle as well."""
+    rng = np.random.default_rng(3)
+    M, K = 8, 256
+    gate = _random_bf16_bits(rng, (M, K), 1, 20)          # 2^-126 .. 2^-107
+    up = _random_bf16_bits(rng, (M, K), 127 - 4, 127 + 4)
+    gate[1] = _random_bf16_bits(rng, (K,), 127 - 60, 127 - 50)
+    x = torch.from_numpy(np.concatenate([gate, up], axis=1).view(np.int16)).view(torch.bfloat16)
+    m_pad = M
+    for g in (16, 128):
+        xq = torch.empty((m_pad, K), dtype=fq.E4M3, device=dev)
+        xs = torch.empty((K // g, m_pad), dtype=torch.float32, device=dev)
+        fq.fp8q_quant_per_token_group_row_padded(x.to(dev), g, eps=1e-38, row_alignment=1, xq=xq,
+                                                 x_scale_storage=xs, fuse_silu_and_mul=True)
+        torch.cuda.synchronize()
+        rq, rs = oracle.quant_group_row_padded_ex(x, g, eps=1e-38, row_alignment=1, fuse_silu_and_mul=True)
+        assert np.array_equal(u8(xq), rq)
+        assert np.array_equal(xs.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+        assert (xs.cpu().numpy()[:, 0] < 2.0 ** -90).all()
+
+
+def _device_silu(a, b, dev):
+    L = fq.load_library()
+    at = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
+    bt = torch.from_numpy(np.ascontiguousarray(b, dtype=np.float32)).to(dev)
+    out = torch.full_like(at, float("nan"))
+    st = L.fp8q_selftest_silu_mul(ctypes.c_void_p(at.data_ptr()), ctypes.c_void_p(bt.data_ptr()),
+                                  ctypes.c_void_p(out.data_ptr()), at.numel(),
+                                  ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == fq.FP8Q_OK, fq.status_str(st)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def test_silu_device_function_bit_exact(dev):
+    """The fused quantizer's silu(a) * b in fp32, bit for bit against the
+    oracle: every finite bf16 gate with b = 1 (the quotient a / (1 +
+    exp(-a)) depends on the gate alone, so this covers every quotient the
+    kernel can form), an odd count (the last thread's single element), and
+    two million random bf16 (gate, up) pairs."""
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    finite = (bits & 0x7F80) != 0x7F80
+    a = oracle.bf16_bits_to_float(bits[finite].astype(np.uint16)).astype(np.float32)
+    b = np.ones_like(a)
+    got = _device_silu(a, b, dev)
+    ref = oracle.silu_mul(a, b)
+    diff = np.flatnonzero(got.view(np.uint32) != ref.view(np.uint32))
+    assert diff.size == 0, (a[diff[:5]], got[diff[:5]], ref[diff[:5]])
+    got = _device_silu(a[:1001], b[:1001], dev)
+    assert np.array_equal(got.view(np.uint32), ref[:1001].view(np.uint32))
+    rng = np.random.default_rng(17)
+    n = 2_000_000
+    ga = oracle.bf16_bits_to_float(_random_bf16_bits(rng, (n,), 1, 254)).astype(np.float32)
+    ub = oracle.bf16_bits_to_float(_random_bf16_bits(rng, (n,), 127 - 30, 127 + 30)).astype(np.float32)
+    got = _device_silu(ga, ub, dev)
+    ref = oracle.silu_mul(ga, ub)
+    same = (got.view(np.uint32) == ref.view(np.uint32)) | (np.isnan(got) & np.isnan(ref))
+    assert same.all(), np.flatnonzero(~same)[:5]
+
+
 def test_silu_exp_range_ends(dev):
     K = 256
     vals = [0.0, -0.0, 1.0, -1.0, 17.0, 18.0, 25.0, 100.0, 1e30, 3e38, -3e38, -1e30, -100.0, -88.5, -88.0,
