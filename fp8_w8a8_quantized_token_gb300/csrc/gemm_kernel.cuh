@@ -131,7 +131,8 @@ enum TracePhase {
     } while (0)
 #endif
 
-template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, bool TWO_SM = false, bool FQ = false, bool W16 = false>
+template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, bool TWO_SM = false, bool FQ = false, bool W16 = false,
+          bool WIDE = false>
 struct GemmCfg {
     static constexpr int kEpiWarps = BN > 128 ? 8 : 4;
     static constexpr int kColGroups = kEpiWarps / 4;
@@ -189,16 +190,24 @@ struct GemmCfg {
     static_assert(!kRegSplit || (kThreads == 384 && kEpiWarp0 == 4 && kEpiWarps == 8 &&
                                  kLowRegs * 128 + kHighRegs * 256 == kLaunchRegs * kThreads),
                   "register split: warpgroup 0 low, warpgroups 1-2 high, same total as at launch");
-    // K steps of one 128-wide K block: 4 MMAs of K = 32 (E4M3) or, W16, 8
+    // WIDE (non-swapped channelwise single-CTA tiles, K a multiple of 128,
+    // no K split): each ring stage holds two consecutive 128-wide K blocks,
+    // loaded by one 3-D TMA box per operand.  Measured on GB300, the TMA
+    // issue of one thread costs ~85 ns per box whatever its size (16 or
+    // 32 KB) plus ~70 ns per stage, which paced the 128 x 64 tiles at
+    // ~290 ns per K block with or without their MMAs; two blocks per box
+    // halve both.
+    static constexpr int kSub = WIDE ? 2 : 1;            // K blocks per stage
+    // K steps of one stage: 4 MMAs of K = 32 per K block (E4M3) or, W16, 8
     // of K = 16 (bf16).
-    static constexpr int kKSteps = W16 ? 8 : 4;
+    static constexpr int kKSteps = W16 ? 8 : 4 * kSub;
     static constexpr int kEpiThreads = 32 * kEpiWarps;
     static constexpr int kTokTile = SWAP ? BN : 128;     // tokens per tile
     static constexpr int kColTile = SWAP ? 128 : BN;     // output columns per tile
     // A operand slot: 128 rows x 128 K of E4M3.  (W16: none; the bf16 A
     // tiles are in tensor memory, kATmemCols columns per ring stage from
     // column kATmemCol0, after the two accumulator slots.)
-    static constexpr uint32_t kABytes = W16 ? 0u : 128u * 128u;
+    static constexpr uint32_t kABytes = W16 ? 0u : 128u * 128u * kSub;
     // W16: a landing ring of slots holding one K block's E4M3 weight tile
     // (16 KB) and its bf16 activation tile (two 64-column halves of BN x 128
     // bytes).  The converting warps empty a slot as soon as they have turned
@@ -210,7 +219,7 @@ struct GemmCfg {
     static constexpr int kLStages = W16 ? (BN == 16 ? 8 : 7) : 0;
     // TWO_SM: each CTA of the pair holds BN/2 weight rows.  W16: the bf16
     // activation tile copied out of the landing slot.
-    static constexpr uint32_t kBBytes = W16 ? kXBBytes : static_cast<uint32_t>(TWO_SM ? BN / 2 : BN) * 128u;
+    static constexpr uint32_t kBBytes = W16 ? kXBBytes : static_cast<uint32_t>(TWO_SM ? BN / 2 : BN) * 128u * kSub;
     static constexpr uint32_t kSABytes = BLOCKWISE ? static_cast<uint32_t>(kTokTile) * 4u : 0u;  // TMA box
     // Scale slots are 128-byte aligned (TMA destination alignment).
     static constexpr uint32_t kSASlot = BLOCKWISE ? (kSABytes + 127u) / 128u * 128u : 0u;
@@ -279,6 +288,7 @@ struct GemmCfg {
     static_assert(!FQ || (BLOCKWISE && SWAP && (BN == 16 || BN == 32) && !TWO_SM),
                   "fused quantization: blockwise 16- and 32-token tiles");
     static_assert(!W16 || (!BLOCKWISE && SWAP && !TWO_SM && !FQ && BN <= 32), "W16: swapped channelwise tiles");
+    static_assert(!WIDE || (!SWAP && !BLOCKWISE && !TWO_SM && !FQ && !W16), "WIDE: non-swapped channelwise tiles");
     static_assert(kTmemNeed <= 512, "tensor memory budget exceeded");
 };
 
@@ -543,14 +553,14 @@ __device__ __noinline__ void reduce_split_workspace(const GemmArgs &p, uint8_t *
 }
 
 template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT, bool TWO_SM = false, bool FQ = false,
-          bool W16 = false>
-__global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ, W16>::kThreads,
-                                  GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ, W16>::kMinBlocks)
+          bool W16 = false, bool WIDE = false>
+__global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ, W16, WIDE>::kThreads,
+                                  GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ, W16, WIDE>::kMinBlocks)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sa, const __grid_constant__ CUtensorMap tm_out,
                     const GemmArgs p)
 {
-    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ, W16>;
+    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ, W16, WIDE>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sA = smem + C::kOffA;
@@ -720,7 +730,9 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
             uint64_t *wbar = W16 ? lfull : full;
             const int ring = W16 ? C::kLStages : STAGES;
             const uint64_t pol_w = SWAP ? policy_evict_first() : policy_evict_normal();
-            npre = p.preload ? (u0_nkb < ring ? u0_nkb : ring) : 0;
+            // (WIDE: stages of two K blocks.)
+            const int u0_nst = (u0_nkb + C::kSub - 1) / C::kSub;
+            npre = p.preload ? (u0_nst < ring ? u0_nst : ring) : 0;
             for (int i = 0; i < npre; ++i) {
                 if (TWO_SM) {
                     if (leader) mbar_arrive_expect_tx(&full[i], C::kStageTx);
@@ -729,9 +741,12 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                     continue;
                 }
                 mbar_arrive_expect_tx(&wbar[i], C::kStageTx);
-                tma_load_2d(wbuf + i * wbytes, wmap, &wbar[i], (u0_kb0 + i) * 128, wrow, pol_w);
+                if constexpr (WIDE)
+                    tma_load_3d(wbuf + i * wbytes, wmap, &wbar[i], 0, wrow, u0_kb0 + 2 * i, pol_w);
+                else
+                    tma_load_2d(wbuf + i * wbytes, wmap, &wbar[i], (u0_kb0 + i) * 128, wrow, pol_w);
             }
-            const int pf = u0_nkb < p.prefetch_kb ? u0_nkb : p.prefetch_kb;
+            const int pf = WIDE ? 0 : (u0_nkb < p.prefetch_kb ? u0_nkb : p.prefetch_kb);
             for (int i = npre; i < pf; ++i) tma_prefetch_l2_2d(wmap, (u0_kb0 + i) * 128, wrow + w_half_row);
             if (sk) {
                 // Stream-K: a CTA's first unit may be a few K blocks only
@@ -792,7 +807,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                 const int a_row = a_t * 128;
                 const int b_row = b_t * BN;
                 bool ok = true;
-                for (int kb = ukb0; kb < ukb1; ++kb) {
+                for (int kb = ukb0; kb < ukb1; kb += C::kSub) {
                     if (issued == 0) FP8Q_TRACE_AT(p, kTrFirstTma);
                     if (TWO_SM) {
                         if (issued >= npre) {
@@ -825,13 +840,21 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                             // (the activation tile is the epilogue warps' work)
                         } else if (SWAP)
                             tma_load_2d(sB + stage * C::kBBytes, &tm_b, &full[stage], kb * 128, b_row, pol_b);
+                        else if (WIDE)
+                            tma_load_3d(sA + stage * C::kABytes, &tm_a, &full[stage], 0, a_row, kb, pol_a);
                         else
                             tma_load_2d(sA + stage * C::kABytes, &tm_a, &full[stage], kb * 128, a_row, pol_a);
                     } else {
                         if (!mbar_wait(&empty[stage], phase ^ 1u, abort, p.status)) { ok = false; break; }
                         mbar_arrive_expect_tx(&full[stage], C::kStageTx);
-                        tma_load_2d(sA + stage * C::kABytes, &tm_a, &full[stage], kb * 128, a_row, pol_a);
-                        if (!FQ) tma_load_2d(sB + stage * C::kBBytes, &tm_b, &full[stage], kb * 128, b_row, pol_b);
+                        if constexpr (WIDE) {
+                            tma_load_3d(sA + stage * C::kABytes, &tm_a, &full[stage], 0, a_row, kb, pol_a);
+                            tma_load_3d(sB + stage * C::kBBytes, &tm_b, &full[stage], 0, b_row, kb, pol_b);
+                        } else {
+                            tma_load_2d(sA + stage * C::kABytes, &tm_a, &full[stage], kb * 128, a_row, pol_a);
+                            if (!FQ)
+                                tma_load_2d(sB + stage * C::kBBytes, &tm_b, &full[stage], kb * 128, b_row, pol_b);
+                        }
                     }
                     if (BLOCKWISE && !FQ)
                         tma_load_2d(sSA + stage * C::kSASlotFloats, &tm_sa, &full[stage], m_tile * C::kTokTile, kb,
@@ -881,7 +904,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                     if (!mbar_wait(&tempty[slot], tphase ^ 1u, abort, p.status)) { ok = false; break; }
                     tc_fence_after();
                 }
-                const int unkb = ukb1 - ukb0;
+                const int unkb = (ukb1 - ukb0 + C::kSub - 1) / C::kSub;   // ring stages of this unit
                 for (int i = 0; i < unkb; ++i) {
                     if (BLOCKWISE) {
                         if (!mbar_wait(&tempty[slot], tphase ^ 1u, abort, p.status)) { ok = false; break; }
@@ -909,8 +932,11 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                             const uint32_t bo = static_cast<uint32_t>((k >> 2) * (BN * 128) + (k & 3) * 32);
                             umma_bf16_tmem_a(d, at, umma_desc_sw128(b_addr + bo), C::kIdesc, acc);
                         } else {
-                            umma_e4m3(d, umma_desc_sw128(a_addr + k * 32), umma_desc_sw128(b_addr + k * 32),
-                                      C::kIdesc, acc);
+                            // (WIDE: K step k reads 32 bytes of K block k / 4 of the stage.)
+                            const uint32_t ao = static_cast<uint32_t>((k >> 2) * (128 * 128) + (k & 3) * 32);
+                            const uint32_t bo = static_cast<uint32_t>((k >> 2) * (BN * 128) + (k & 3) * 32);
+                            umma_e4m3(d, umma_desc_sw128(a_addr + ao), umma_desc_sw128(b_addr + bo), C::kIdesc,
+                                      acc);
                         }
                     }
                     if (TWO_SM) umma_commit_pair_mc(&empty[stage], 3);

@@ -14,11 +14,13 @@ namespace fp8q {
 constexpr int kMaxDevices = 64;
 
 template <bool SWAP, int BN, int STAGES, bool BLOCKWISE, typename OutT, bool TWO_SM = false, bool FQ = false,
-          bool W16 = false>
+          bool W16 = false, bool WIDE = false>
 cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigned *status, cudaStream_t st)
 {
-    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ, W16>;
-    auto kernel = fp8_gemm_kernel<SWAP, BN, STAGES, BLOCKWISE, OutT, TWO_SM, FQ, W16>;
+    using C = GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, FQ, W16, WIDE>;
+    auto kernel = fp8_gemm_kernel<SWAP, BN, STAGES, BLOCKWISE, OutT, TWO_SM, FQ, W16, WIDE>;
+    // Double-K-block stages: whole 128-wide K blocks, one CTA per tile along K.
+    if (WIDE && (pr.K % 128 != 0 || l.split != 1)) return cudaErrorInvalidValue;
 
     static std::atomic<uint64_t> attr_done[kMaxDevices / 64 + 1];
     int dev = 0;
@@ -46,9 +48,13 @@ cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigne
     const bool pair = TWO_SM;   // 2-CTA MMA pairs (non-swapped channelwise, split 1)
     // Paired tiles: each CTA loads half of the weight rows of the tile.
     const int wrow_box = SWAP ? 128 : (pair ? BN / 2 : BN);
-    if (!make_tmap_2d(&tm_w, pr.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(pr.K),
-                      static_cast<uint64_t>(pr.N), static_cast<uint64_t>(pr.ldw), 128, wrow_box,
-                      CU_TENSOR_MAP_SWIZZLE_128B))
+    if (WIDE) {
+        if (!make_tmap_3d_kblocks(&tm_w, pr.w, static_cast<uint64_t>(pr.K), static_cast<uint64_t>(pr.N),
+                                  static_cast<uint64_t>(pr.ldw), static_cast<uint32_t>(wrow_box)))
+            return cudaErrorInvalidValue;
+    } else if (!make_tmap_2d(&tm_w, pr.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(pr.K),
+                             static_cast<uint64_t>(pr.N), static_cast<uint64_t>(pr.ldw), 128, wrow_box,
+                             CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     // FQ: the bf16 activations are copied by the kernel's quantizing warps
     // (GemmArgs::x); the activation map slot holds the weight map, unused.
@@ -56,7 +62,11 @@ cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigne
     // (128 bytes) x the tile's tokens, 128-byte swizzle: two per K block.
     if (FQ)
         tm_x = tm_w;
-    else if (W16) {
+    else if (WIDE) {
+        if (!make_tmap_3d_kblocks(&tm_x, pr.a, static_cast<uint64_t>(pr.K), static_cast<uint64_t>(pr.M),
+                                  static_cast<uint64_t>(pr.K), static_cast<uint32_t>(tok_box)))
+            return cudaErrorInvalidValue;
+    } else if (W16) {
         if (!make_tmap_2d(&tm_x, pr.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<uint64_t>(pr.K),
                           static_cast<uint64_t>(pr.M), static_cast<uint64_t>(pr.lda) * 2u, 64, tok_box,
                           CU_TENSOR_MAP_SWIZZLE_128B))

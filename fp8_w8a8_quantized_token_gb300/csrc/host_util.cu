@@ -65,6 +65,21 @@ bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
     return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_3d_kblocks(CUtensorMap *map, const void *base, uint64_t K, uint64_t rows, uint64_t row_bytes,
+                          uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr || K % 128 != 0) return false;
+    const cuuint64_t dims[3] = {128, rows, K / 128};
+    const cuuint64_t strides[2] = {row_bytes, 128};
+    const cuuint32_t box[3] = {128, box_rows, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 unsigned *device_status_ptr()
 {
     int dev = 0;

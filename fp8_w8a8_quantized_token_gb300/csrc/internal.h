@@ -101,6 +101,9 @@ constexpr int kFusedQuantStages = 4;
 // (32-token tiles: 3 slots of 16 KB + 4 KB and a 3-slot staging ring of 8 KB
 // keep the CTA near 105 KB as well.)
 constexpr int kFusedQuantStages32 = 3;
+// Ring stages of the double-K-block (WIDE) narrow channelwise tiles: stages
+// of 32 KB of activations + BN x 256 bytes of weights, about 190 KB.
+constexpr int wide_stages(int mma_n) { return mma_n == 128 ? 3 : mma_n == 64 ? 4 : 5; }
 
 // Depth of the MMA ring of the weight-only FP8 (W16) instantiations: per
 // stage a bf16 A tile in tensor memory (64 columns) and the token tile's bf16
@@ -141,6 +144,14 @@ unsigned long long *trace_buffer();
 // 9.25 us) and every non-swapped size by 1-6 % (o_proj M = 512: 12.56 ->
 // 12.85 us; down M = 256: 19.9 -> 21.2 us).
 int prefetch_kblocks(bool swapped, bool blockwise, int grid);
+// E4M3 operand [rows, K] (K % 128 == 0, row stride row_bytes) as a 3-D
+// tensor (128 bytes, rows, K / 128) whose boxes of 128 bytes x box_rows x 2
+// hold two consecutive 128-wide K blocks (each 128-byte swizzled, one after
+// the other): the double-K-block stages of the non-swapped channelwise
+// tiles.  A box starting at the last K block of an odd count reads the
+// missing second block as zeros.
+bool make_tmap_3d_kblocks(CUtensorMap *map, const void *base, uint64_t K, uint64_t rows, uint64_t row_bytes,
+                          uint32_t box_rows);
 // Split-K partial sums through the caller's workspace (global memory)
 // instead of distributed shared memory: off unless FP8Q_WORKSPACE_EXCHANGE=1
 // at start-up.  On the GB300s measured, reading partials that other SMs of

@@ -235,6 +235,39 @@ def test_channelwise_strided_weight_and_output_canary(dev):
     assert torch.all(out_buf[M:] == 7.0)
 
 
+@pytest.mark.parametrize("mma_n", [32, 64, 128])
+@pytest.mark.parametrize("K", [384, 640, 1024])
+def test_channelwise_double_k_block_stages(dev, schedule, mma_n, K):
+    """Non-swapped channelwise tiles over whole 128-wide K blocks with K not
+    split take stages of two K blocks (one 3-D TMA box per operand); an odd
+    number of K blocks leaves the last stage's second block zero-filled."""
+    fq.fp8q_set_plan_override(0, mma_n, 1)
+    for M in (1, 70, 300):
+        out, ref = channelwise_case(dev, M, 392, K, seed=M + K, bias=True)
+        assert_gemm_close(out_values(out), ref, f"noswap{mma_n} K={K} M={M}")
+
+
+@pytest.mark.parametrize("mma_n", [32, 64, 128])
+def test_channelwise_double_k_block_strided_weight(dev, schedule, mma_n):
+    """The same stages with the weights' row stride above K (ldb = K + 128)
+    and an output canary row."""
+    fq.fp8q_set_plan_override(0, mma_n, 1)
+    M, N, K, ldb = 200, 264, 640, 768
+    x = synthetic.activations(M, K, seed=13)
+    w = synthetic.weights(N, K, seed=13)
+    xq, xs, rq, rs = quant_both_per_token(x, dev)
+    wq, ws = fq.fp8q_quant_per_token(w.to(dev))
+    wstore = torch.zeros((N, ldb), dtype=fq.E4M3, device=dev)
+    wstore[:, :K] = wq
+    wstore[:, K:].view(torch.uint8).fill_(0x7E)     # 448 past K: must never be read
+    out_buf = torch.full((M + 1, N), 7.0, dtype=torch.bfloat16, device=dev)
+    fq.fp8q_scaled_mm_channelwise(xq, wstore[:, :K], xs, ws, out=out_buf[:M])
+    torch.cuda.synchronize()
+    ref = ref_values(oracle.gemm_channelwise(rq, u8(wq), rs, ws.cpu().numpy()))
+    assert_gemm_close(out_values(out_buf[:M]), ref, f"noswap{mma_n} strided b")
+    assert torch.all(out_buf[M:] == 7.0)
+
+
 def blockwise_case(dev, M, N, K, seed=0, bias=False, outliers=True, garbage_padding=False, workspace="auto"):
     x = synthetic.activations(M, K, seed=seed, outliers=outliers)
     w = synthetic.weights(N, K, seed=seed)
