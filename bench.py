@@ -490,7 +490,8 @@ def build_problems(gpu, workload):
 
 def plan_str(pl):
     k = "streamK" if pl.get("stream_k") else pl["split_k"]
-    return f"{'swap' if pl['swap_ab'] else 'noswap'}{pl['mma_n']}x{k}"
+    wide = "w2" if pl.get("kb_per_stage", 1) == 2 else ""   # two K blocks per stage
+    return f"{'swap' if pl['swap_ab'] else 'noswap'}{pl['mma_n']}x{k}{wide}"
 
 
 def measure_sweep(gpu, problems, peaks, with_quant=True):

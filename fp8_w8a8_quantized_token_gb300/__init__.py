@@ -64,7 +64,7 @@ class Fp8qError(RuntimeError):
 class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("swap_ab", "mma_n", "tile_m", "tile_n", "split_k", "stages", "grid", "persistent", "from_table",
-                 "pair", "two_sm", "stream_k")]
+                 "pair", "two_sm", "stream_k", "kb_per_stage")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

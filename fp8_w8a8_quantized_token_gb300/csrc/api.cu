@@ -57,6 +57,7 @@ fp8q_status launch_planned(GemmProblem p, const fp8q_plan &pl, cudaStream_t st)
     l.pair = plan.pair != 0;
     l.two_sm = plan.two_sm != 0;
     l.stream_k = plan.stream_k != 0;
+    l.wide = plan.kb_per_stage == 2;
     const cudaError_t e = p.blockwise ? launch_gemm_blockwise(p, l, status, st)
                                       : launch_gemm_channelwise(p, l, status, st);
     if (e == cudaSuccess) note_launch_writes(st, p.out, static_cast<size_t>(p.M) * p.N * 2);
@@ -356,6 +357,6 @@ const char *fp8q_status_str(fp8q_status status)
     }
 }
 
-int32_t fp8q_version(void) { return (2 << 16) | 1; }
+int32_t fp8q_version(void) { return (2 << 16) | 2; }
 
 }  // extern "C"

@@ -52,7 +52,7 @@ cudaError_t dispatch_gemm(const GemmProblem &p, const GemmLaunch &l, unsigned *s
     if constexpr (!BLOCKWISE) {
         // Narrow channelwise tiles over whole 128-wide K blocks, K not split:
         // stages of two K blocks.
-        if (!l.pair && l.split == 1 && p.K % 128 == 0) {
+        if (l.wide) {
             switch (l.mma_n) {
                 case 128: return launch_gemm_inst<false, 128, wide_stages(128), false, OutT, false, false, false, true>(p, l, status, st);
                 case 64: return launch_gemm_inst<false, 64, wide_stages(64), false, OutT, false, false, false, true>(p, l, status, st);

@@ -81,6 +81,7 @@
 #pragma once
 
 #include "device_common.cuh"
+#include "internal.h"
 #include "quant_common.cuh"
 
 namespace fp8q {
@@ -110,6 +111,7 @@ struct GemmArgs {
                                 //   stream-K: one slot of 128 x BN floats per CTA
     int stream_k;               // 1: stream-K (swapped tiles, one CTA per cluster, see below)
     unsigned *sk_flags;         // stream-K: one flag per CTA after the slots, 1 = its partial is published
+    unsigned long long *trace_stages;  // trace builds: CTA 0's per-stage stamps (null otherwise)
 };
 
 // Phase timestamps of a trace build (-DFP8Q_TRACE): kTraceSlots 64-bit
@@ -125,7 +127,18 @@ enum TracePhase {
         if ((p).trace != nullptr && blockIdx.x < 4096)                                            \
             (p).trace[blockIdx.x * kTraceSlots + (phase)] = globaltimer_ns();                     \
     } while (0)
+// Per-ring-stage stamps of CTA 0 (stage k in issue order, k < kTraceStages):
+// event 0 loads issued, 1 MMA issuer 0 saw the stage full, 2 its commit
+// issued, 3 the producer began waiting for the stage to be empty.
+#define FP8Q_TRACE_STAGE(p, event, k)                                                             \
+    do {                                                                                          \
+        if ((p).trace_stages != nullptr && blockIdx.x == 0 && (k) < kTraceStages)                 \
+            (p).trace_stages[(k) * 4 + (event)] = globaltimer_ns();                               \
+    } while (0)
 #else
+#define FP8Q_TRACE_STAGE(p, event, k) \
+    do {                              \
+    } while (0)
 #define FP8Q_TRACE_AT(p, phase) \
     do {                        \
     } while (0)
@@ -845,6 +858,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                         else
                             tma_load_2d(sA + stage * C::kABytes, &tm_a, &full[stage], kb * 128, a_row, pol_a);
                     } else {
+                        FP8Q_TRACE_STAGE(p, 3, issued);
                         if (!mbar_wait(&empty[stage], phase ^ 1u, abort, p.status)) { ok = false; break; }
                         mbar_arrive_expect_tx(&full[stage], C::kStageTx);
                         if constexpr (WIDE) {
@@ -859,6 +873,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                     if (BLOCKWISE && !FQ)
                         tma_load_2d(sSA + stage * C::kSASlotFloats, &tm_sa, &full[stage], m_tile * C::kTokTile, kb,
                                     pol_b);
+                    FP8Q_TRACE_STAGE(p, 0, issued);
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -895,6 +910,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
         const int issuer = warp - 1;
         if (lane == 0 && (!TWO_SM || leader)) {
             uint32_t stage = 0, phase = 0, slot = 0, tphase = 0;
+            long long n_stages = 0;   // stages consumed (trace stamps)
             bool ok = true;
             bool first_unit = true;
             long long cur = unit_first;
@@ -912,6 +928,7 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                     }
                     if (!mbar_wait(&full[stage], phase, abort, p.status)) { ok = false; break; }
                     tc_fence_after();
+                    if (issuer == 0) FP8Q_TRACE_STAGE(p, 1, n_stages);
                     if (first_unit && i == 0 && issuer == 0) FP8Q_TRACE_AT(p, kTrFirstMma);
                     const uint32_t a_addr = smem_u32(sA + stage * C::kABytes);
                     const uint32_t b_addr = smem_u32(sB + stage * C::kBBytes);
@@ -941,6 +958,8 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
                     }
                     if (TWO_SM) umma_commit_pair_mc(&empty[stage], 3);
                     else umma_commit(&empty[stage]);
+                    if (issuer == 0) FP8Q_TRACE_STAGE(p, 2, n_stages);
+                    ++n_stages;
                     if (BLOCKWISE) {
                         umma_commit(&tfull[slot]);
                         slot ^= 1u;

@@ -116,7 +116,7 @@ cudaError_t launch_gemm_inst(const GemmProblem &pr, const GemmLaunch &l, unsigne
     a.out = pr.out;
     a.ldo = pr.N;
     a.status = status;
-    a.trace = trace_buffer();
+    a.trace = trace_buffer(&a.trace_stages);
     a.prefetch_kb = prefetch_kblocks(SWAP, BLOCKWISE, l.grid);
     a.preload = pr.preload ? 1 : 0;
     a.eps = pr.eps;

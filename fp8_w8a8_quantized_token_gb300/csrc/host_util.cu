@@ -18,8 +18,10 @@ __device__ unsigned g_status_word;
 
 #ifdef FP8Q_TRACE
 // Trace builds: 16 timestamps for each of the first 4096 CTAs of each of
-// the 4 most recent GEMM launches (launch i uses block i % 4).
+// the 4 most recent GEMM launches (launch i uses block i % 4), and 4 per
+// ring stage (the first 128) of each launch's CTA 0.
 __device__ unsigned long long g_trace_buf[4 * 4096 * 16];
+__device__ unsigned long long g_trace_stages[4 * kTraceStages * 4];
 std::atomic<unsigned> g_trace_launch{0};
 #endif
 
@@ -94,12 +96,15 @@ unsigned *device_status_ptr()
     return p;
 }
 
-unsigned long long *trace_buffer()
+unsigned long long *trace_buffer(unsigned long long **stages)
 {
+    *stages = nullptr;
 #ifdef FP8Q_TRACE
-    void *addr = nullptr;
+    void *addr = nullptr, *saddr = nullptr;
     if (cudaGetSymbolAddress(&addr, g_trace_buf) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&saddr, g_trace_stages) != cudaSuccess) return nullptr;
     const unsigned i = g_trace_launch.fetch_add(1) % 4u;
+    *stages = static_cast<unsigned long long *>(saddr) + static_cast<size_t>(i) * kTraceStages * 4;
     return static_cast<unsigned long long *>(addr) + static_cast<size_t>(i) * 4096 * 16;
 #else
     return nullptr;
@@ -195,11 +200,19 @@ extern "C" __attribute__((visibility("default"))) int fp8q_trace_read(unsigned l
     if (count > 4 * 4096 * 16) count = 4 * 4096 * 16;
     return cudaMemcpyFromSymbol(host, fp8q::g_trace_buf, sizeof(unsigned long long) * count) == cudaSuccess ? 0 : 3;
 }
+extern "C" __attribute__((visibility("default"))) int fp8q_trace_read_stages(unsigned long long *host, int count)
+{
+    if (count > 4 * fp8q::kTraceStages * 4) count = 4 * fp8q::kTraceStages * 4;
+    return cudaMemcpyFromSymbol(host, fp8q::g_trace_stages, sizeof(unsigned long long) * count) == cudaSuccess ? 0
+                                                                                                             : 3;
+}
 extern "C" __attribute__((visibility("default"))) int fp8q_trace_clear(void)
 {
-    void *addr = nullptr;
+    void *addr = nullptr, *saddr = nullptr;
     if (cudaGetSymbolAddress(&addr, fp8q::g_trace_buf) != cudaSuccess) return 3;
+    if (cudaGetSymbolAddress(&saddr, fp8q::g_trace_stages) != cudaSuccess) return 3;
     fp8q::g_trace_launch.store(0);
+    if (cudaMemset(saddr, 0, sizeof(unsigned long long) * 4 * fp8q::kTraceStages * 4) != cudaSuccess) return 3;
     return cudaMemset(addr, 0, sizeof(unsigned long long) * 4 * 4096 * 16) == cudaSuccess ? 0 : 3;
 }
 #endif

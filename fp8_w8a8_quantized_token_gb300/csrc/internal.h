@@ -34,6 +34,7 @@ struct GemmLaunch {
     bool pair;         // non-swapped channelwise, split 1: 2-CTA clusters on adjacent token tiles
     bool two_sm;       // the pair computes 256-token tiles with 2-CTA MMAs (always with pair)
     bool stream_k;     // swapped tiles: equal shares of (tile, K block) pairs per CTA, split 1
+    bool wide;         // non-swapped channelwise: stages of two K blocks (fp8q_plan::kb_per_stage 2)
 };
 
 struct GemmProblem {
@@ -131,8 +132,11 @@ bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
 
 // ---- device status word (host_util.cu) --------------------------------------
 unsigned *device_status_ptr();   // of the current device, or null
-// Per-CTA phase timestamps of a trace build (-DFP8Q_TRACE); null otherwise.
-unsigned long long *trace_buffer();
+// Per-CTA phase timestamps of a trace build (-DFP8Q_TRACE) and, through
+// *stages, the per-ring-stage stamps of the launch's CTA 0; null otherwise.
+unsigned long long *trace_buffer(unsigned long long **stages);
+// Ring stages of CTA 0 whose stamps a trace build keeps.
+constexpr int kTraceStages = 128;
 // Weight K blocks each GEMM CTA prefetches into L2 before its dependency
 // wait: 16 for swapped (decode) tiles -- blockwise ones only while the grid
 // is at most 1.5 CTAs per SM -- and none for non-swapped tiles;

@@ -157,6 +157,7 @@ size_t stream_k_workspace_bytes(int grid, int mma_n)
 // split_k 0 with swapped tiles asks for stream-K.
 void plan_finish(int64_t M, int64_t N, int64_t K, int blockwise, int num_sms, fp8q_plan *pl)
 {
+    pl->kb_per_stage = 1;
     pl->tile_m = pl->swap_ab ? pl->mma_n : 128;
     pl->tile_n = pl->swap_ab ? 128 : pl->mma_n;
     const int64_t tiles = ((M + pl->tile_m - 1) / pl->tile_m) * ((N + pl->tile_n - 1) / pl->tile_n);
@@ -204,6 +205,12 @@ void plan_finish(int64_t M, int64_t N, int64_t K, int blockwise, int num_sms, fp
     }
     pl->two_sm = pl->pair;
     pl->stages = pl->two_sm ? kTwoSmStages : stages_for(pl->swap_ab != 0, pl->mma_n);
+    // Narrow channelwise tiles over whole K blocks, K not split: stages of
+    // two K blocks.
+    if (!blockwise && !pl->swap_ab && !pl->pair && pl->split_k == 1 && K % 128 == 0 && pl->mma_n <= 128) {
+        pl->kb_per_stage = 2;
+        pl->stages = wide_stages(pl->mma_n);
+    }
 }
 
 void plan_without_stream_k(int64_t M, int64_t N, int64_t K, int blockwise, int num_sms, fp8q_plan *pl)

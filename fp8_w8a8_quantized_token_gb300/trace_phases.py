@@ -11,6 +11,13 @@ the launch's CTAs.  Schedules that split K are traced twice: with the
 split-K workspace and without it (partials exchanged in distributed shared
 memory).  Inputs are the seeded synthetic tensors.  Needs a GPU.
 
+    python -m fp8_w8a8_quantized_token_gb300.trace_phases --stages MxNxK [MxNxK ...]
+
+prints, for one launch (after the same warm-up), CTA 0's pipeline stages: when
+each stage's loads were issued, when MMA issuer 0 saw it full and issued its
+commit, and when the producer began waiting for a reused slot; then the
+median interval between consecutive "full" events.
+
     python -m fp8_w8a8_quantized_token_gb300.trace_phases --back-to-back MxNxK
 
 traces the steady state instead: four GEMM launches over four weight copies
@@ -63,6 +70,25 @@ def trace_launch(L, dev, M: int, N: int, K: int, workspace="auto"):
         raise RuntimeError("fp8q_trace_read failed")
     t = np.frombuffer(buf, dtype=np.uint64).reshape(4096, SLOTS_PER_CTA)[:plan["grid"]].astype(np.int64)
     return plan, t
+
+
+def stages(L, dev, M: int, N: int, K: int):
+    plan, t = trace_launch(L, dev, M, N, K)
+    n = 4 * 128 * 4
+    buf = (ctypes.c_ulonglong * n)()
+    if L.fp8q_trace_read_stages(ctypes.addressof(buf), n) != 0:
+        raise RuntimeError("fp8q_trace_read_stages failed")
+    s = np.frombuffer(buf, dtype=np.uint64).reshape(4, 128, 4)[0].astype(np.int64)
+    t0 = t[0, 0]   # CTA 0 entry
+    used = [k for k in range(128) if s[k, 1] > 0]
+    print(f"== stages of CTA 0: M={M} N={N} K={K} plan={plan}")
+    print("  stage   wait-empty    issued    full-seen    committed   (ns after CTA 0 entry)")
+    for k in used:
+        cells = [s[k, 3], s[k, 0], s[k, 1], s[k, 2]]
+        print(f"  {k:5d} " + "".join(f"{(c - t0) if c > 0 else -1:12d}" for c in cells))
+    full = s[used, 1]
+    if len(full) > 2:
+        print(f"  median full-to-full interval: {np.median(np.diff(full)):.0f} ns over {len(full)} stages")
 
 
 def back_to_back(L, dev, M: int, N: int, K: int):
@@ -125,6 +151,15 @@ def main(argv) -> int:
     if not argv:
         print(__doc__)
         return 2
+    if argv[0] == "--stages":
+        L = fq.load_library(fbuild.build(trace=True))
+        L.fp8q_trace_read.argtypes = [ctypes.c_void_p, ctypes.c_int]
+        L.fp8q_trace_read_stages.argtypes = [ctypes.c_void_p, ctypes.c_int]
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        for spec in argv[1:]:
+            stages(L, dev, *(int(v) for v in spec.split("x")))
+        return 0
     if argv[0] == "--back-to-back":
         L = fq.load_library(fbuild.build(trace=True))
         L.fp8q_trace_read.argtypes = [ctypes.c_void_p, ctypes.c_int]

@@ -433,6 +433,11 @@ typedef struct {
                            Without that workspace, and in the fused and
                            weight-only GEMMs, the GEMM runs a K-split
                            schedule of the same tiles instead. */
+    int32_t kb_per_stage; /* 128-wide K blocks per pipeline stage: 2 for the
+                           channelwise non-swapped tiles of 32, 64 or 128
+                           columns with split_k 1, no pair and K a multiple
+                           of 128 (one 3-D TMA box per operand and stage;
+                           `stages` then counts double stages), else 1 */
 } fp8q_plan;
 
 FP8Q_API fp8q_status fp8q_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t blockwise, int32_t num_sms,

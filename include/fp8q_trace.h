@@ -13,6 +13,12 @@
  * CTA's rank in its cluster.  Launch i after fp8q_trace_clear() writes
  * block i % 4 of 4096 * 16 slots.  Unreached phases keep their previous
  * contents.
+ *
+ * Each launch also stores, for CTA 0, four slots per pipeline ring stage
+ * (stages in issue order, the first 128): loads issued, MMA issuer 0 saw the
+ * stage full, its commit issued, and (stages that reuse a slot) the
+ * producer began waiting for the slot to be empty -- block i % 4 of 128 * 4
+ * slots of a second buffer, read with fp8q_trace_read_stages.
  */
 #ifndef FP8Q_TRACE_H_
 #define FP8Q_TRACE_H_
@@ -25,7 +31,11 @@ extern "C" {
  * host memory; synchronous.  Returns 0 (FP8Q_OK) or 3 (FP8Q_ERR_CUDA). */
 int fp8q_trace_read(unsigned long long *host, int count);
 
-/* Zero the trace buffer of the current device; synchronous. */
+/* Copy `count` (<= 4 * 512) per-stage slots (see above) to host memory;
+ * synchronous.  Returns 0 (FP8Q_OK) or 3 (FP8Q_ERR_CUDA). */
+int fp8q_trace_read_stages(unsigned long long *host, int count);
+
+/* Zero both trace buffers of the current device; synchronous. */
 int fp8q_trace_clear(void);
 
 #ifdef __cplusplus

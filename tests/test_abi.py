@@ -54,7 +54,7 @@ def test_status_strings_and_version(lib):
     assert fq.status_str(0) == "FP8Q_OK"
     assert fq.status_str(4) == "FP8Q_ERR_TIMEOUT"
     assert fq.status_str(99) == "FP8Q_UNKNOWN_STATUS"
-    assert fq.fp8q_version() == (2 << 16) | 1
+    assert fq.fp8q_version() == (2 << 16) | 2
 
 
 def test_invalid_arguments_are_rejected_before_any_cuda_call(lib):

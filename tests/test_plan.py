@@ -48,6 +48,7 @@ def test_plans_are_launchable(num_sms):
             # at least one (tile, K block) pair per CTA
             assert p["swap_ab"] == 1 and p["split_k"] == 1 and p["pair"] == 0 and p["persistent"] == 1
             assert p["grid"] == min(tiles * num_kb, num_sms)
+            assert p["kb_per_stage"] == 1
             assert p["stages"] * stage_bytes(1, p["mma_n"], bw) + 4096 <= SMEM_LIMIT
             continue
         m_tiles = -(-M // p["tile_m"])
@@ -68,8 +69,13 @@ def test_plans_are_launchable(num_sms):
         # channelwise pairs of 128 x 256 tiles use 2-CTA MMAs: each CTA stages
         # 128 token rows and its 128 of the 256 weight rows per K slice
         assert p["two_sm"] == p["pair"]
+        # narrow channelwise tiles over whole K blocks, K not split: two K
+        # blocks per stage
+        wide = (not bw and not p["swap_ab"] and not p["pair"] and p["split_k"] == 1 and K % 128 == 0
+                and p["mma_n"] <= 128)
+        assert p["kb_per_stage"] == (2 if wide else 1)
         per_stage = 2 * 128 * 128 if p["two_sm"] else stage_bytes(p["swap_ab"], p["mma_n"], bw)
-        assert p["stages"] * per_stage + 4096 <= SMEM_LIMIT
+        assert p["stages"] * per_stage * p["kb_per_stage"] + 4096 <= SMEM_LIMIT
 
 
 def test_decode_sizes_put_weights_on_the_mma_m_side():
