@@ -11,7 +11,7 @@ the launch's CTAs.  Schedules that split K are traced twice: with the
 split-K workspace and without it (partials exchanged in distributed shared
 memory).  Inputs are the seeded synthetic tensors.  Needs a GPU.
 
-    python -m fp8_w8a8_quantized_token_gb300.trace_phases --stages MxNxK [MxNxK ...]
+    python -m fp8_w8a8_quantized_token_gb300.trace_phases --stages [--blockwise] MxNxK [MxNxK ...]
 
 prints, for one launch (after the same warm-up), CTA 0's pipeline stages: when
 each stage's loads were issued, when MMA issuer 0 saw it full and issued its
@@ -52,18 +52,26 @@ PHASES = ["entry", "prologue done", "dependency wait passed", "first TMA issued"
 SLOTS_PER_CTA = 16
 
 
-def trace_launch(L, dev, M: int, N: int, K: int, workspace="auto"):
+def trace_launch(L, dev, M: int, N: int, K: int, workspace="auto", blockwise: bool = False):
     x = synthetic.activations(M, K, outliers=True).to(dev)
-    wq, ws = fq.fp8q_quant_per_token(synthetic.weights(N, K).to(dev))
-    plan = fq.fp8q_gemm_plan(M, N, K)
+    w = synthetic.weights(N, K).to(dev)
+    wq, ws = fq.fp8q_quant_weight_block128(w) if blockwise else fq.fp8q_quant_per_token(w)
+    plan = fq.fp8q_gemm_plan(M, N, K, blockwise)
+
+    def run():
+        if blockwise:
+            xq, xsv = fq.fp8q_quant_per_token_group_row_padded(x, 128)
+            fq.fp8q_scaled_mm_blockwise(xq, wq, xsv, ws, M=M, workspace=workspace)
+        else:
+            xq, xs = fq.fp8q_quant_per_token(x)
+            fq.fp8q_scaled_mm_channelwise(xq, wq, xs, ws, workspace=workspace)
+
     for _ in range(3):
-        xq, xs = fq.fp8q_quant_per_token(x)
-        fq.fp8q_scaled_mm_channelwise(xq, wq, xs, ws, workspace=workspace)
+        run()
     torch.cuda.synchronize()
     if L.fp8q_trace_clear() != 0:
         raise RuntimeError("fp8q_trace_clear failed")
-    xq, xs = fq.fp8q_quant_per_token(x)
-    fq.fp8q_scaled_mm_channelwise(xq, wq, xs, ws, workspace=workspace)
+    run()
     torch.cuda.synchronize()
     buf = (ctypes.c_ulonglong * (4096 * SLOTS_PER_CTA))()
     if L.fp8q_trace_read(ctypes.addressof(buf), 4096 * SLOTS_PER_CTA) != 0:
@@ -72,8 +80,8 @@ def trace_launch(L, dev, M: int, N: int, K: int, workspace="auto"):
     return plan, t
 
 
-def stages(L, dev, M: int, N: int, K: int):
-    plan, t = trace_launch(L, dev, M, N, K)
+def stages(L, dev, M: int, N: int, K: int, blockwise: bool = False):
+    plan, t = trace_launch(L, dev, M, N, K, blockwise=blockwise)
     n = 4 * 128 * 4
     buf = (ctypes.c_ulonglong * n)()
     if L.fp8q_trace_read_stages(ctypes.addressof(buf), n) != 0:
@@ -81,7 +89,7 @@ def stages(L, dev, M: int, N: int, K: int):
     s = np.frombuffer(buf, dtype=np.uint64).reshape(4, 128, 4)[0].astype(np.int64)
     t0 = t[0, 0]   # CTA 0 entry
     used = [k for k in range(128) if s[k, 1] > 0]
-    print(f"== stages of CTA 0: M={M} N={N} K={K} plan={plan}")
+    print(f"== stages of CTA 0: M={M} N={N} K={K} {'blockwise' if blockwise else 'channelwise'} plan={plan}")
     print("  stage   wait-empty    issued    full-seen    committed   (ns after CTA 0 entry)")
     for k in used:
         cells = [s[k, 3], s[k, 0], s[k, 1], s[k, 2]]
@@ -157,8 +165,10 @@ def main(argv) -> int:
         L.fp8q_trace_read_stages.argtypes = [ctypes.c_void_p, ctypes.c_int]
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
+        blockwise = "--blockwise" in argv
         for spec in argv[1:]:
-            stages(L, dev, *(int(v) for v in spec.split("x")))
+            if spec != "--blockwise":
+                stages(L, dev, *(int(v) for v in spec.split("x")), blockwise=blockwise)
         return 0
     if argv[0] == "--back-to-back":
         L = fq.load_library(fbuild.build(trace=True))
