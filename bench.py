@@ -42,6 +42,8 @@ UNIT = "TFLOP/s"
 # o_proj sweep, the 2-CTA prefill kernel's four launches M = 1024 .. 8192 of
 # "oproj_prefill_group", averaged.  A key is dropped whenever its kernel
 # changes.
+# e2e: layers with more rows run as calls on slices of this many rows.
+E2E_CHUNK = 2048
 DOMINANT_TRAFFIC_BYTES = {("channelwise", 0, 256, 1): 39.99e6}
 
 # Small fixed cases for Nsight Compute captures: name -> (kind, M, N, K).
@@ -551,6 +553,8 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=256, help="oracle rows per M for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-chunk", type=int, default=E2E_CHUNK,
+                    help="rows per linear call of the e2e pipeline for larger layers")
     ap.add_argument("--kernel-replays", type=int, default=20)
     ap.add_argument("--min-timed-s", type=float, default=1.0,
                     help="replay the pass within each step so the timed region lasts at least this long")
@@ -690,53 +694,88 @@ def main():
     hx = [p["x"].cpu().pin_memory() for p in problems]
     ho = [torch.empty(p["out"].shape, dtype=torch.bfloat16).pin_memory() for p in problems]
 
-    # Three streams: every M's activations go up on s_in, its linear layer
+    # Work items of the pipeline: every M as one call of the linear entry
+    # point, or (chunked) layers of more than E2E_CHUNK rows as calls on
+    # consecutive E2E_CHUNK-row slices (rows are independent: per-token
+    # scales, one output row per input row), so that a large layer's output
+    # starts coming back before its last rows are computed.  Each chunk has
+    # its own quantizer scratch and workspace.
+    def work_items(chunked):
+        items = []
+        for p, hxi, hoi in zip(problems, hx, ho):
+            if not chunked or p["M"] <= args.e2e_chunk:
+                items.append((p, hxi, hoi))
+                continue
+            for r0 in range(0, p["M"], args.e2e_chunk):
+                r1 = min(p["M"], r0 + args.e2e_chunk)
+                m = r1 - r0
+                m_pad = (m + 3) // 4 * 4
+                need = fq.fp8q_workspace_bytes(m, p["N"], p["K"], p["bw"])
+                c = dict(p, M=m, m_pad=m_pad, x=p["x"][r0:r1], out=p["out"][r0:r1],
+                         xq=torch.empty((m_pad if p["bw"] else m, p["K"]), dtype=fq.E4M3, device=dev),
+                         xs=(torch.empty((p["K"] // 128, m_pad), dtype=torch.float32, device=dev) if p["bw"]
+                             else torch.empty((m,), dtype=torch.float32, device=dev)),
+                         work=torch.zeros(need, dtype=torch.uint8, device=dev) if need else None,
+                         work_bytes=need)
+                items.append((c, hxi[r0:r1], hoi[r0:r1]))
+        return items
+
+    # Three streams: every item's activations go up on s_in, its linear layer
     # runs on the capturing stream once its upload is done, its output comes
     # back on s_out once its layer is done -- uploads, layers and downloads of
-    # different M overlap, as a serving pipeline would run them.
+    # different items overlap, as a serving pipeline would run them.
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def e2e_body(st):
-        cur = torch.cuda.current_stream(dev)
-        s_in.wait_stream(cur)
-        s_out.wait_stream(cur)
-        ev_in, ev_c = [], []
-        with torch.cuda.stream(s_in):
-            for p, hxi in zip(problems, hx):
-                p["x"].copy_(hxi, non_blocking=True)
-                e = torch.cuda.Event()
-                e.record(s_in)
-                ev_in.append(e)
-        for p, e in zip(problems, ev_in):
-            cur.wait_event(e)
-            gpu.linear(p, P(cur.cuda_stream))
-            e2 = torch.cuda.Event()
-            e2.record(cur)
-            ev_c.append(e2)
-        with torch.cuda.stream(s_out):
-            for p, hoi, e2 in zip(problems, ho, ev_c):
-                s_out.wait_event(e2)
-                hoi.copy_(p["out"], non_blocking=True)
-        cur.wait_stream(s_in)
-        cur.wait_stream(s_out)
+    def make_body(items):
+        def e2e_body(st):
+            cur = torch.cuda.current_stream(dev)
+            s_in.wait_stream(cur)
+            s_out.wait_stream(cur)
+            ev_in, ev_c = [], []
+            with torch.cuda.stream(s_in):
+                for p, hxi, _ in items:
+                    p["x"].copy_(hxi, non_blocking=True)
+                    e = torch.cuda.Event()
+                    e.record(s_in)
+                    ev_in.append(e)
+            for (p, _, _), e in zip(items, ev_in):
+                cur.wait_event(e)
+                gpu.linear(p, P(cur.cuda_stream))
+                e2 = torch.cuda.Event()
+                e2.record(cur)
+                ev_c.append(e2)
+            with torch.cuda.stream(s_out):
+                for (p, _, hoi), e2 in zip(items, ev_c):
+                    s_out.wait_event(e2)
+                    hoi.copy_(p["out"], non_blocking=True)
+            cur.wait_stream(s_in)
+            cur.wait_stream(s_out)
+        return e2e_body
 
-    e2e_graph = gpu.capture(e2e_body)
-    for _ in range(3):
-        e2e_graph.replay()
-    barrier()
-    e0, e1 = gpu.event(), gpu.event()
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_graph.replay()
-    e1.record(stream)
-    barrier()
-    e2e_ms = reduce_max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
+    def time_e2e(items):
+        graph = gpu.capture(make_body(items))
+        for _ in range(3):
+            graph.replay()
+        barrier()
+        e0, e1 = gpu.event(), gpu.event()
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            graph.replay()
+        e1.record(stream)
+        barrier()
+        return reduce_max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
+
+    e2e_ms_whole = time_e2e(work_items(False))
+    e2e_ms = time_e2e(work_items(True))
     e2e = {"value": round(aggregate_value(flops_pass, world, e2e_ms), 2), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-           "how": "CUDA graph per pass over three streams: pinned-host->device copy of each M's "
-                  "activations, the linear entry point (quant + GEMM) once that copy is done, "
-                  "device->pinned-host copy of its output once the layer is done; copies and layers "
-                  "of different M overlap; one pass per step"}
+           "how": f"CUDA graph per pass over three streams: pinned-host->device copy of each item's "
+                  f"activations, the linear entry point (quant + GEMM) once that copy is done, "
+                  f"device->pinned-host copy of its output once the layer is done; copies and layers "
+                  f"of different items overlap; an item is one M, layers above {args.e2e_chunk} rows split "
+                  f"into {args.e2e_chunk}-row calls; one pass per step",
+           "value_one_call_per_m": round(aggregate_value(flops_pass, world, e2e_ms_whole), 2),
+           "ms_per_step_one_call_per_m": round(e2e_ms_whole, 4)}
 
     line = None
     if rank == 0:
