@@ -920,7 +920,7 @@ def measure_w8a16(gpu, peaks, synthetic):
         wwq0, wws = fq.fp8q_quant_per_token(ww)
         del ww
         wcp = [wwq0] + [wwq0.clone() for _ in range(REPS - 1)]
-        for wM in (1, 16):
+        for wM in (1, 4, 16):
             wx = synthetic.activations(wM, wK, outliers=True).to(dev)
             wxq = torch.empty((wM, wK), dtype=fq.E4M3, device=dev)
             wxs = torch.empty((wM,), dtype=torch.float32, device=dev)

@@ -308,6 +308,10 @@ fp8q_status fp8q_scaled_mm_w8a16(const void *x, int64_t ldx, const void *w, int6
     if (x == nullptr || w == nullptr || w_scale == nullptr || out == nullptr) return FP8Q_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(w) || !aligned16(out) || !aligned4(w_scale)) return FP8Q_ERR_INVALID_ARG;
     if (bias != nullptr && (reinterpret_cast<uintptr_t>(bias) & 1u)) return FP8Q_ERR_INVALID_ARG;
+    // A few tokens: matrix-vector products on the CUDA cores.
+    if (M <= kW16GemvMaxM)
+        return from_cuda(launch_w8a16_gemv(x, ldx, w, ldw, w_scale, bias, out, M, N, K,
+                                           out_dtype == FP8Q_OUT_FP16, as_stream(stream)));
     const int num_sms = current_device_sms();
     if (num_sms <= 0) return FP8Q_ERR_CUDA;
     // Schedule: 128 weight rows x 16 (M <= 16) or 32 tokens per tile; K split

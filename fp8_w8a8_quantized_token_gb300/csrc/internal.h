@@ -102,6 +102,12 @@ constexpr int kFusedQuantStages = 4;
 // (32-token tiles: 3 slots of 16 KB + 4 KB and a 3-slot staging ring of 8 KB
 // keep the CTA near 105 KB as well.)
 constexpr int kFusedQuantStages32 = 3;
+// Weight-only FP8 for at most this many tokens runs as matrix-vector
+// products on the CUDA cores (w8a16_gemv.cu), above it on the tensor cores.
+constexpr int kW16GemvMaxM = 4;
+cudaError_t launch_w8a16_gemv(const void *x, int64_t ldx, const void *w, int64_t ldw, const float *w_scale,
+                              const void *bias, void *out, int64_t M, int64_t N, int64_t K, bool out_fp16,
+                              cudaStream_t st);
 // Ring stages of the double-K-block (WIDE) narrow channelwise tiles: stages
 // of 32 KB of activations + BN x 256 bytes of weights, about 190 KB.
 constexpr int wide_stages(int mma_n) { return mma_n == 128 ? 3 : mma_n == 64 ? 4 : 5; }

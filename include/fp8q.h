@@ -305,12 +305,14 @@ FP8Q_API fp8q_status fp8q_linear_blockwise(const void *x, const void *w, const f
  * snippets" (apply_fp8_marlin_linear(input, weight, weight_scale, ...,
  * bias): no input scale):
  *   out[m,n] = round(sum_k x[m,k] * e4m3(w[n,k]) * w_scale[n] + bias[n])
- * computed as fp32-accumulated bf16 x bf16 MMAs on the weights converted
- * exactly to bf16 into tensor memory (tcgen05.mma kind::f16, A operand in
- * TMEM); a per-tensor weight scale is the case of equal entries.  Tiles of 128 weight rows x
- * 16 (M <= 16) or 32 tokens, K split across a cluster while the tiles do
- * not fill the GPU: the decode regime the weight-only format is for (any M
- * works; larger M simply takes more token tiles).
+ * (a per-tensor weight scale is the case of equal entries).  M <= 4: matrix-
+ * vector products on the CUDA cores (weights decoded exactly to fp32 in
+ * registers, fp32 FMAs), the weight stream at HBM speed.  M > 4: fp32-
+ * accumulated bf16 x bf16 MMAs on the weights converted exactly to bf16 into
+ * tensor memory (tcgen05.mma kind::f16, A operand in TMEM), tiles of 128
+ * weight rows x 16 (M <= 16) or 32 tokens, K split across a cluster while
+ * the tiles do not fill the GPU (any M works; larger M simply takes more
+ * token tiles).
  * x       : bf16 [M, K], row stride ldx >= K (ldx % 8 == 0), 16-byte aligned.
  * w       : e4m3 [N, K] row-major, row stride ldw >= K (ldw % 16 == 0).
  * w_scale : fp32 [N].  bias: bf16 [N] or NULL.  out: [M, N] (row stride N).
