@@ -368,7 +368,8 @@ class Gpu:
         return None if t is None else self.P(t.data_ptr())
 
     def linear(self, p, sp, wq=None, x=None):
-        """The public linear entry point: quantize, then GEMM (two kernels)."""
+        """The public linear entry point: quantize, then GEMM (two kernels;
+        one fused launch for a single channelwise token with K <= 4096)."""
         L, P = self.L, self.ptr
         wq = p["wq"] if wq is None else wq
         x = p["x"] if x is None else x
@@ -770,13 +771,17 @@ def main():
     e2e = {"value": round(aggregate_value(flops_pass, world, e2e_ms), 2), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
            "how": f"CUDA graph per pass over three streams: pinned-host->device copy of each item's "
-                  f"activations, the linear entry point (quant + GEMM) once that copy is done, "
+                  f"activations, the linear entry point (quant + GEMM, or one fused launch for a single token) once that copy is done, "
                   f"device->pinned-host copy of its output once the layer is done; copies and layers "
                   f"of different items overlap; an item is one M, layers above {args.e2e_chunk} rows split "
                   f"into {args.e2e_chunk}-row calls; one pass per step",
            "value_one_call_per_m": round(aggregate_value(flops_pass, world, e2e_ms_whole), 2),
            "ms_per_step_one_call_per_m": round(e2e_ms_whole, 4)}
 
+    # Library kernels one pass launches: the blockwise linear is always two;
+    # the channelwise one says how many it takes for its (M, K).
+    launches_per_pass = sum(2 if p["bw"] else int(L.fp8q_linear_channelwise_launches(p["M"], p["K"]))
+                            for p in problems)
     line = None
     if rank == 0:
         cpu = None
@@ -800,7 +805,7 @@ def main():
                            "M": ms, "l2": l2note, "passes_per_step": passes,
                            "parallelism": f"replicas x{world}" if world > 1 else "single"},
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": 2 * len(problems) * args.steps * passes,
+                "gpu_launches": launches_per_pass * args.steps * passes,
                 "timing": f"K steps of {passes} replays each of a CUDA graph holding one pass (timed region "
                           f"{elapsed_ms / 1e3:.2f} s); per-kernel durations: median of 5 measurements, each "
                           f"{args.kernel_replays} replays of a graph of {REPS} back-to-back launches of the "

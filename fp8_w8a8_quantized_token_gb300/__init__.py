@@ -45,6 +45,7 @@ EXPORTED = (
     "fp8q_scaled_mm_w8a16",
     "fp8q_gemm_plan",
     "fp8q_workspace_bytes",
+    "fp8q_linear_channelwise_launches",
     "fp8q_set_plan_override",
     "fp8q_device_status",
     "fp8q_last_device_status",
@@ -114,6 +115,8 @@ def load_library(path: str | None = None):
     L.fp8q_version.restype = ctypes.c_int32
     L.fp8q_workspace_bytes.argtypes = [I64, I64, I64, I32]
     L.fp8q_workspace_bytes.restype = SZ
+    L.fp8q_linear_channelwise_launches.argtypes = [I64, I64]
+    L.fp8q_linear_channelwise_launches.restype = ctypes.c_int32
     _lib = L
     return L
 
@@ -527,6 +530,12 @@ def fp8q_workspace_bytes(M: int, N: int, K: int, blockwise: bool = False, device
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     with _on(device):
         return int(load_library().fp8q_workspace_bytes(M, N, K, int(bool(blockwise))))
+
+
+def fp8q_linear_channelwise_launches(M: int, K: int) -> int:
+    """Kernel launches fp8q_linear_channelwise makes for M tokens of K values
+    (1: the fused one-token form; 2: quantizer + GEMM; 0: nothing to do)."""
+    return int(load_library().fp8q_linear_channelwise_launches(M, K))
 
 
 def fp8q_set_plan_override(swap_ab: int, mma_n: int = 0, split_k: int = 1) -> None:

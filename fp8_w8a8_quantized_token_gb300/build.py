@@ -22,7 +22,7 @@ TRACE_LIB = os.path.join(HERE, "libfp8q_trace.so")
 OBJ_DIR = os.path.join(HERE, "_build")
 
 SOURCES = ["api.cu", "host_util.cu", "quant.cu", "gemm_channelwise.cu", "gemm_blockwise.cu", "plan.cpp",
-           "noalloc.cu", "selftest.cu", "w8a16_gemv.cu"]
+           "noalloc.cu", "selftest.cu", "w8a16_gemv.cu", "linear_gemv.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"]

@@ -88,7 +88,8 @@ fp8q_status fp8q_quant_per_token(const void *x, int64_t M, int64_t K, int64_t ld
     unsigned *status = device_status_ptr();
     if (status == nullptr) return FP8Q_ERR_CUDA;
     const cudaError_t e = launch_quant_per_token(x, M, K, ldx, xq, x_scale, eps, status, as_stream(stream));
-    if (e == cudaSuccess) note_launch_writes(as_stream(stream), xq, static_cast<size_t>(M) * K);
+    if (e == cudaSuccess)
+        note_launch_writes(as_stream(stream), xq, static_cast<size_t>(M) * K, x_scale, static_cast<size_t>(M) * 4);
     return from_cuda(e);
 }
 
@@ -107,7 +108,9 @@ fp8q_status fp8q_quant_per_token_group_row_padded(const void *x, int64_t M, int6
     if (s != FP8Q_OK || M == 0) return s;
     const cudaError_t e = launch_quant_group(x, M, K, ldx, group_size, xq, x_scale, m_pad, eps, current_device_sms(),
                                              as_stream(stream));
-    if (e == cudaSuccess) note_launch_writes(as_stream(stream), xq, static_cast<size_t>(M) * K);
+    if (e == cudaSuccess)
+        note_launch_writes(as_stream(stream), xq, static_cast<size_t>(M) * K, x_scale,
+                           static_cast<size_t>(K / group_size) * m_pad * 4);
     return from_cuda(e);
 }
 
@@ -131,7 +134,9 @@ fp8q_status fp8q_quant_per_token_group_row_padded_ex(const void *x, int64_t M, i
     if (s != FP8Q_OK || M == 0) return s;
     const cudaError_t e = launch_quant_group(x, M, K, ldx, group_size, xq, x_scale, m_pad, eps, current_device_sms(),
                                              as_stream(stream), (flags & FP8Q_QUANT_SCALE_UE8M0) != 0, silu);
-    if (e == cudaSuccess) note_launch_writes(as_stream(stream), xq, static_cast<size_t>(M) * K);
+    if (e == cudaSuccess)
+        note_launch_writes(as_stream(stream), xq, static_cast<size_t>(M) * K, x_scale,
+                           static_cast<size_t>(K / group_size) * m_pad * 4);
     return from_cuda(e);
 }
 
@@ -146,7 +151,9 @@ fp8q_status fp8q_quant_static_per_tensor(const void *x, int64_t M, int64_t K, in
         return FP8Q_ERR_INVALID_ARG;
     const cudaError_t e = launch_quant_static(x, M, K, ldx, scale, xq, x_scale_rep, current_device_sms(),
                                               as_stream(stream));
-    if (e == cudaSuccess) note_launch_writes(as_stream(stream), xq, static_cast<size_t>(M) * K);
+    if (e == cudaSuccess)
+        note_launch_writes(as_stream(stream), xq, static_cast<size_t>(M) * K, x_scale_rep,
+                           static_cast<size_t>(M) * 4);
     return from_cuda(e);
 }
 
@@ -159,7 +166,9 @@ fp8q_status fp8q_quant_weight_block128(const void *w, int64_t N, int64_t K, void
     if (w == nullptr || wq == nullptr || w_scale == nullptr) return FP8Q_ERR_INVALID_ARG;
     if (!aligned16(w) || !aligned16(wq) || !aligned4(w_scale)) return FP8Q_ERR_INVALID_ARG;
     const cudaError_t e = launch_quant_weight_block128(w, N, K, wq, w_scale, eps, as_stream(stream));
-    if (e == cudaSuccess) note_launch_writes(as_stream(stream), wq, static_cast<size_t>(N) * K);
+    if (e == cudaSuccess)
+        note_launch_writes(as_stream(stream), wq, static_cast<size_t>(N) * K, w_scale,
+                           static_cast<size_t>(N / 128) * (K / 128) * 4);
     return from_cuda(e);
 }
 
@@ -238,10 +247,23 @@ fp8q_status fp8q_linear_channelwise(const void *x, const void *b, int64_t ldb, c
     if (s != FP8Q_OK || M == 0) return s;
     if (b == nullptr || b_scale == nullptr || out == nullptr || !aligned16(b) || !aligned16(out) || !aligned4(b_scale))
         return FP8Q_ERR_INVALID_ARG;
+    if (bias != nullptr && (reinterpret_cast<uintptr_t>(bias) & 1u)) return FP8Q_ERR_INVALID_ARG;
+    // A few tokens: one launch, the quantization fused into matrix-vector
+    // products (unless a schedule override asks for the GEMM).
+    if (linear_gemv_fits(M, K) && !plan_override_active()) {
+        return from_cuda(launch_linear_pt_gemv(x, b, ldb, b_scale, bias, out, xq, xs, M, N, K, 1e-10f,
+                                               out_dtype == FP8Q_OUT_FP16, as_stream(stream)));
+    }
     s = fp8q_quant_per_token(x, M, K, K, xq, xs, 1e-10f, stream);
     if (s != FP8Q_OK) return s;
     return fp8q_scaled_mm_channelwise(xq, b, ldb, xs, b_scale, bias, out, M, N, K, out_dtype, workspace,
                                       workspace_bytes, stream);
+}
+
+int32_t fp8q_linear_channelwise_launches(int64_t M, int64_t K)
+{
+    if (M <= 0 || K <= 0) return 0;
+    return linear_gemv_fits(M, K) && !plan_override_active() ? 1 : 2;
 }
 
 fp8q_status fp8q_linear_blockwise(const void *x, const void *w, const float *w_scale, const void *bias, void *out,

@@ -133,26 +133,34 @@ bool workspace_exchange_enabled()
 }
 
 namespace {
+// The device ranges the last library launch on a stream writes (up to three).
 struct LaunchRecord {
     cudaStream_t stream;
-    uintptr_t lo, hi;
+    bool used;
+    uintptr_t lo[3], hi[3];
 };
 std::mutex g_launch_mu;
 LaunchRecord g_launches[64];
 int g_launch_next = 0;
 }  // namespace
 
-void note_launch_writes(cudaStream_t st, const void *base, size_t bytes)
+void note_launch_writes(cudaStream_t st, const void *base, size_t bytes, const void *base2, size_t bytes2,
+                        const void *base3, size_t bytes3)
 {
     std::lock_guard<std::mutex> g(g_launch_mu);
-    const uintptr_t lo = reinterpret_cast<uintptr_t>(base);
+    LaunchRecord rec = {st, true, {}, {}};
+    const void *bases[3] = {base, base2, base3};
+    const size_t sizes[3] = {bytes, bytes2, bytes3};
+    for (int i = 0; i < 3; ++i) {
+        rec.lo[i] = reinterpret_cast<uintptr_t>(bases[i]);
+        rec.hi[i] = bases[i] != nullptr ? rec.lo[i] + sizes[i] : 0;
+    }
     for (auto &r : g_launches)
-        if (r.stream == st && r.hi != 0) {
-            r.lo = lo;
-            r.hi = lo + bytes;
+        if (r.used && r.stream == st) {
+            r = rec;
             return;
         }
-    g_launches[g_launch_next] = {st, lo, lo + bytes};
+    g_launches[g_launch_next] = rec;
     g_launch_next = (g_launch_next + 1) % 64;
 }
 
@@ -161,7 +169,11 @@ bool last_launch_writes_overlap(cudaStream_t st, const void *base, size_t bytes)
     std::lock_guard<std::mutex> g(g_launch_mu);
     const uintptr_t lo = reinterpret_cast<uintptr_t>(base), hi = lo + bytes;
     for (const auto &r : g_launches)
-        if (r.stream == st && r.hi != 0) return r.lo < hi && lo < r.hi;
+        if (r.used && r.stream == st) {
+            for (int i = 0; i < 3; ++i)
+                if (r.lo[i] < hi && lo < r.hi[i]) return true;
+            return false;
+        }
     // No record for this stream (evicted or never seen): assume the worst.
     return true;
 }

@@ -103,11 +103,23 @@ constexpr int kFusedQuantStages = 4;
 // keep the CTA near 105 KB as well.)
 constexpr int kFusedQuantStages32 = 3;
 // Weight-only FP8 for at most this many tokens runs as matrix-vector
-// products on the CUDA cores (w8a16_gemv.cu), above it on the tensor cores.
-constexpr int kW16GemvMaxM = 4;
+// products on the CUDA cores (w8a16_gemv.cu), above it on the tensor cores
+// (with three or four tokens the CUDA-core kernel measured slower).
+constexpr int kW16GemvMaxM = 2;
 cudaError_t launch_w8a16_gemv(const void *x, int64_t ldx, const void *w, int64_t ldw, const float *w_scale,
                               const void *bias, void *out, int64_t M, int64_t N, int64_t K, bool out_fp16,
                               cudaStream_t st);
+// True while a schedule override (fp8q_set_plan_override / FP8Q_PLAN) is set.
+bool plan_override_active();
+// The channelwise W8A8 linear for one token with K <= 4096 (each warp of
+// the matrix-vector CTA then owns one 512-byte chunk of a row) runs as one
+// launch with the per-token quantization fused (linear_gemv.cu), unless a
+// schedule override is set.  Measured on GB300 it is faster there than the
+// quantizer + tensor-core GEMM, and slower with two tokens or longer rows.
+inline bool linear_gemv_fits(int64_t M, int64_t K) { return M == 1 && K <= 4096; }
+cudaError_t launch_linear_pt_gemv(const void *x, const void *w, int64_t ldw, const float *w_scale, const void *bias,
+                                  void *out, void *xq, float *xs, int64_t M, int64_t N, int64_t K, float eps,
+                                  bool out_fp16, cudaStream_t st);
 // Ring stages of the double-K-block (WIDE) narrow channelwise tiles: stages
 // of 32 KB of activations + BN x 256 bytes of weights, about 190 KB.
 constexpr int wide_stages(int mma_n) { return mma_n == 128 ? 3 : mma_n == 64 ? 4 : 5; }
@@ -170,12 +182,13 @@ bool make_tmap_3d_kblocks(CUtensorMap *map, const void *base, uint64_t K, uint64
 // default the library asks for no workspace and ignores one passed to it.
 bool workspace_exchange_enabled();
 
-// Per-stream record of the byte range the library's most recent launch on
-// that stream writes.  With programmatic dependent launch, that launch is the
+// Per-stream record of the byte ranges (up to three) the library's most
+// recent launch on that stream writes.  With programmatic dependent launch, that launch is the
 // only kernel that may still be running when the next one starts (every
 // kernel triggers its dependents only after its own dependency wait), so a
-// GEMM may read its weights early unless they overlap this range.
-void note_launch_writes(cudaStream_t st, const void *base, size_t bytes);
+// GEMM may read its weights early unless they overlap these ranges.
+void note_launch_writes(cudaStream_t st, const void *base, size_t bytes, const void *base2 = nullptr,
+                        size_t bytes2 = 0, const void *base3 = nullptr, size_t bytes3 = 0);
 bool last_launch_writes_overlap(cudaStream_t st, const void *base, size_t bytes);
 int current_device_sms();        // SM count of the current device (cached)
 

@@ -138,6 +138,12 @@ bool table_plan(int64_t M, int64_t N, int64_t K, int blockwise, fp8q_plan *pl)
 
 }  // namespace
 
+bool plan_override_active()
+{
+    fp8q_plan pl = {};
+    return override_plan(&pl);
+}
+
 size_t plan_workspace_bytes(int64_t M, int64_t N, int swap_ab, int mma_n, int split_k)
 {
     // Only partial tiles of 64 KB and more (128 x 128 floats) go through the

@@ -279,8 +279,16 @@ FP8Q_API fp8q_status fp8q_scaled_mm_blockwise(const void *a, const void *w, cons
 FP8Q_API size_t fp8q_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t blockwise);
 
 /* ---------------------------------------------------------------------------
- * Linear-layer compositions (two launches each, no padding copies):
- * quantize x into the caller's buffers, then run the GEMM on them.
+ * Linear-layer compositions (no padding copies): quantize x into the
+ * caller's buffers, then run the GEMM on them -- two launches, except:
+ * fp8q_linear_channelwise with ONE token and K <= 4096 (and no schedule
+ * override set) runs as one launch, the per-token quantization fused into a
+ * matrix-vector product on the CUDA cores (every CTA quantizes the row into
+ * its shared memory; CTA 0 also writes xq and xs, so they hold the same
+ * codes and scales as after the two launches).  Its sums are accumulated in
+ * another order than the tensor-core GEMM's, so its output is within the
+ * GEMM tolerance of the two-kernel result rather than bit-identical.
+ * fp8q_linear_channelwise_launches tells which form a call takes.
  * fp8q_linear_channelwise : xq e4m3 [M, K], xs fp32 [M].
  * fp8q_linear_blockwise   : xq e4m3 [m_pad, K], xs fp32 [K/128][m_pad],
  *   m_pad = ceil(M/4)*4 or a larger multiple of 4 -- the row-padded
@@ -297,6 +305,10 @@ FP8Q_API fp8q_status fp8q_linear_blockwise(const void *x, const void *w, const f
                                   const void *bias, void *out, int64_t M, int64_t N, int64_t K,
                                   void *xq, float *xs, int64_t m_pad, fp8q_out_dtype out_dtype,
                                   void *workspace, size_t workspace_bytes, void *stream);
+/* Kernel launches fp8q_linear_channelwise makes for M tokens of K values:
+ * 1 (the fused one-token form), 2 (quantizer + GEMM), or 0 for M <= 0 or
+ * K <= 0.  Host only; reads the schedule override. */
+FP8Q_API int32_t fp8q_linear_channelwise_launches(int64_t M, int64_t K);
 
 /* ---------------------------------------------------------------------------
  * fp8q_scaled_mm_w8a16 -- weight-only FP8 linear (W8A16): bf16 activations
@@ -305,9 +317,9 @@ FP8Q_API fp8q_status fp8q_linear_blockwise(const void *x, const void *w, const f
  * snippets" (apply_fp8_marlin_linear(input, weight, weight_scale, ...,
  * bias): no input scale):
  *   out[m,n] = round(sum_k x[m,k] * e4m3(w[n,k]) * w_scale[n] + bias[n])
- * (a per-tensor weight scale is the case of equal entries).  M <= 4: matrix-
+ * (a per-tensor weight scale is the case of equal entries).  M <= 2: matrix-
  * vector products on the CUDA cores (weights decoded exactly to fp32 in
- * registers, fp32 FMAs), the weight stream at HBM speed.  M > 4: fp32-
+ * registers, fp32 FMAs), the weight stream at HBM speed.  M > 2: fp32-
  * accumulated bf16 x bf16 MMAs on the weights converted exactly to bf16 into
  * tensor memory (tcgen05.mma kind::f16, A operand in TMEM), tiles of 128
  * weight rows x 16 (M <= 16) or 32 tokens, K split across a cluster while

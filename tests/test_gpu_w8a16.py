@@ -56,15 +56,17 @@ def test_w8a16_bias_fp16_and_long_k(dev):
 @pytest.mark.parametrize("M", [1, 2, 3, 4])
 @pytest.mark.parametrize("N,K", [(392, 1040), (8, 16), (4096, 4096), (264, 12288)])
 def test_w8a16_few_tokens_on_cuda_cores(dev, M, N, K):
-    """Up to four tokens: matrix-vector products on the CUDA cores (K not a
+    """One or two tokens: matrix-vector products on the CUDA cores (K not a
     multiple of the 512-byte chunk, one 16-element piece, N not a multiple of
-    a CTA's rows), with bias and fp16 output on every other case."""
+    a CTA's rows); three and four: the 16-token tensor-core tiles; bias and
+    fp16 output on every other case."""
     _case(dev, M, N, K, bias=(M % 2 == 1), fp16=(M == 2), seed=M)
 
 
 def test_w8a16_few_tokens_strided_operands(dev):
-    """Row strides above K for both the activations and the weights."""
-    M, N, K, ldx, ldw = 3, 520, 2064, 2080, 2112
+    """Row strides above K for both the activations and the weights (two
+    tokens: the CUDA-core path)."""
+    M, N, K, ldx, ldw = 2, 520, 2064, 2080, 2112
     big = synthetic.activations(M, ldx, outliers=True, seed=21)
     w = synthetic.weights(N, K, seed=22).to(dev)
     wq, ws = fq.fp8q_quant_per_token(w)
@@ -77,13 +79,13 @@ def test_w8a16_few_tokens_strided_operands(dev):
     assert_gemm_close(out_values(out), ref_values(ref), "w8a16 few tokens strided")
 
 
-@pytest.mark.parametrize("M", [4, 16, 32])
+@pytest.mark.parametrize("M", [2, 16, 32])
 def test_w8a16_every_e4m3_code_converts_exactly(dev, M):
     """One-hot activation rows pick single weights: with unit weight scales,
     out[m, n] = w[n, m] exactly (an E4M3 value is a bf16 value), so every
     finite code, subnormals and both zeros included, must come out as the
     oracle's decode of it -- an exhaustive check of the on-chip E4M3
-    conversion of the CUDA-core path (M = 4) and the 16- and 32-token
+    conversion of the CUDA-core path (M = 2) and the 16- and 32-token
     tiles."""
     N, K = 128, 256
     rng = np.random.default_rng(11)

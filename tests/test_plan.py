@@ -186,3 +186,21 @@ def test_tuner_only_proposes_schedules_the_library_accepts(lib):
                     assert (plan["swap_ab"], plan["mma_n"]) == (c[0], c[1]), (label, M, c, plan)
     finally:
         lib.fp8q_set_plan_override(-1, 0, 0)
+
+
+def test_linear_channelwise_launch_count(lib):
+    """One token with rows up to 4096 values: one fused launch; otherwise the
+    quantizer and the GEMM; nothing for empty problems; two again while a
+    schedule override asks for the GEMM."""
+    assert fq.fp8q_linear_channelwise_launches(1, 4096) == 1
+    assert fq.fp8q_linear_channelwise_launches(1, 16) == 1
+    assert fq.fp8q_linear_channelwise_launches(1, 4112) == 2
+    assert fq.fp8q_linear_channelwise_launches(1, 12288) == 2
+    assert fq.fp8q_linear_channelwise_launches(2, 4096) == 2
+    assert fq.fp8q_linear_channelwise_launches(8192, 4096) == 2
+    assert fq.fp8q_linear_channelwise_launches(0, 4096) == 0
+    lib.fp8q_set_plan_override(1, 16, 4)
+    try:
+        assert fq.fp8q_linear_channelwise_launches(1, 4096) == 2
+    finally:
+        lib.fp8q_set_plan_override(-1, 0, 0)
