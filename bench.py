@@ -68,6 +68,9 @@ PROFILE_CASES = {
     "quant_silu_group": ("quant_silu_group", 4096, 0, 12288),
     "quant_static": ("quant_static", 16384, 0, 4096),
     "w8a16_gateup": ("w8a16", 1, 24576, 4096),
+    # the one-token channelwise linear (quantization fused, one launch)
+    "linear1_oproj": ("linear1", 1, 4096, 4096),
+    "linear1_gateup": ("linear1", 1, 24576, 4096),
 }
 PROFILE_WARMUP = 2
 
@@ -330,6 +333,11 @@ def run_profile_case(name: str) -> int:
             torch.cuda.synchronize()
             for _ in range(n):
                 fq.fp8q_scaled_mm_w8a16(x, wq, ws)
+        elif kind == "linear1":
+            wq, ws = fq.fp8q_quant_per_token(w)
+            torch.cuda.synchronize()
+            for _ in range(n):
+                fq.fp8q_linear_channelwise(x, wq, ws)
         elif kind == "channelwise":
             wq, ws = fq.fp8q_quant_per_token(w)
             xq, xs = fq.fp8q_quant_per_token(x)
@@ -688,6 +696,7 @@ def main():
     variants = measure_quant_variants(gpu, peaks, synthetic) if rank == 0 and not args.no_configs else []
     fused = measure_fused(gpu, peaks, synthetic) if rank == 0 and not args.no_configs else []
     w16 = measure_w8a16(gpu, peaks, synthetic) if rank == 0 and not args.no_configs else []
+    one_tok = measure_linear_one_token(gpu, peaks, synthetic) if rank == 0 and not args.no_configs else []
 
     # ---- end to end through the C ABI with host buffers --------------------
     h2d = sum(p["x"].numel() * 2 for p in problems)
@@ -813,7 +822,7 @@ def main():
                 "clocks": clk.summary(),
                 "kernel_time_us": {"quant": round(quant_total, 2), "gemm": round(gemm_total, 2)},
                 "sweep": sweep, "configs": configs, "quant_variants": variants, "fused_quant_linear": fused,
-                "w8a16": w16}
+                "w8a16": w16, "linear_one_token": one_tok}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -925,7 +934,7 @@ def measure_w8a16(gpu, peaks, synthetic):
         wwq0, wws = fq.fp8q_quant_per_token(ww)
         del ww
         wcp = [wwq0] + [wwq0.clone() for _ in range(REPS - 1)]
-        for wM in (1, 4, 16):
+        for wM in (1, 2, 4, 16):
             wx = synthetic.activations(wM, wK, outliers=True).to(dev)
             wxq = torch.empty((wM, wK), dtype=fq.E4M3, device=dev)
             wxs = torch.empty((wM,), dtype=torch.float32, device=dev)
@@ -956,6 +965,52 @@ def measure_w8a16(gpu, peaks, synthetic):
                         "w8a16_hbm_frac": round(wb / (u16 * 1e-6) / 1e9 / peaks["hbm_gbs"], 3)})
         del wcp
     return w16
+
+
+def measure_linear_one_token(gpu, peaks, synthetic):
+    """The channelwise linear entry point at one and two tokens on the four
+    decode layers, as planned (one fused launch where
+    fp8q_linear_channelwise_launches says 1) and with the schedule override
+    set to the planner's own GEMM plan (which forces the quantizer + GEMM):
+    back-to-back launches over rotating weight copies (> L2), CUDA events;
+    algorithmic bytes N*K + 2*M*K + M*K + 4*M + 2*M*N + 4*N."""
+    torch, fq, dev, P, L = gpu.torch, gpu.fq, gpu.dev, gpu.P, gpu.L
+    rows = []
+    for (lab, N, K) in (("o_proj", 4096, 4096), ("qkv", 6144, 4096), ("down", 4096, 12288),
+                        ("gate_up", 24576, 4096)):
+        w = synthetic.weights(N, K).to(dev)
+        wq0, ws = fq.fp8q_quant_per_token(w)
+        del w
+        wcp = [wq0] + [wq0.clone() for _ in range(REPS - 1)]
+        for M in (1, 2):
+            x = synthetic.activations(M, K, outliers=True).to(dev)
+            xq = torch.empty((M, K), dtype=fq.E4M3, device=dev)
+            xs = torch.empty((M,), dtype=torch.float32, device=dev)
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            need = fq.fp8q_workspace_bytes(M, N, K)
+            work = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
+
+            def body(st, x=x, M=M, N=N, K=K, out=out, xq=xq, xs=xs, work=work, need=need, wcp=wcp):
+                for r in range(REPS):
+                    if L.fp8q_linear_channelwise(P(x.data_ptr()), P(wcp[r].data_ptr()), K, P(ws.data_ptr()), None,
+                                                 P(out.data_ptr()), M, N, K, P(xq.data_ptr()), P(xs.data_ptr()), 0,
+                                                 P(work.data_ptr()), need, P(st.cuda_stream)) != 0:
+                        raise RuntimeError("linear failed")
+
+            launches = int(L.fp8q_linear_channelwise_launches(M, K))
+            planned = gpu.time_graph(body, REPS)
+            plan = fq.fp8q_gemm_plan(M, N, K)
+            fq.fp8q_set_plan_override(plan["swap_ab"], plan["mma_n"], 0 if plan["stream_k"] else plan["split_k"])
+            try:
+                two = gpu.time_graph(body, REPS)
+            finally:
+                fq.fp8q_set_plan_override(-1)
+            b = N * K + 3 * M * K + 4 * M + 2 * M * N + 4 * N
+            rows.append({"shape": lab, "M": M, "N": N, "K": K, "launches": launches, "linear_us": round(planned, 3),
+                         "quant_plus_gemm_us": round(two, 3),
+                         "hbm_frac": round(b / (planned * 1e-6) / 1e9 / peaks["hbm_gbs"], 3)})
+        del wcp
+    return rows
 
 
 if __name__ == "__main__":
