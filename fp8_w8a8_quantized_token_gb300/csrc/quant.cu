@@ -73,13 +73,18 @@ __device__ __forceinline__ void pdl_enter()
 // read from HBM exactly once.  Rows longer than T*VPT chunks take the
 // two-pass kernel below.
 // ---------------------------------------------------------------------------
+//
+// With `early` set (the host found that the previous launch of the library
+// on this stream does not write x), the row is loaded, reduced and quantized
+// in registers before the dependency wait, so all of it overlaps the tail of
+// the previous kernel; only the stores of the codes and the scale wait.
 template <int VPT>
 __global__ void __launch_bounds__(1024) quant_per_token_kernel(const __nv_bfloat16 *__restrict__ x, int64_t ldx,
                                                                uint8_t *__restrict__ xq, float *__restrict__ xs,
-                                                               int K, float eps)
+                                                               int K, float eps, int early)
 {
     __shared__ float warp_max[32];
-    pdl_enter();
+    if (!early) pdl_enter();
     const int64_t row = blockIdx.x;
     const int chunks = K >> 4;
     const __nv_bfloat16 *xr = x + row * ldx;
@@ -104,12 +109,19 @@ __global__ void __launch_bounds__(1024) quant_per_token_kernel(const __nv_bfloat
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     }
     const float s = scale_of(m, eps);
+    // The codes of chunk v replace its first half (its registers are free).
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int ci = threadIdx.x + v * blockDim.x;
+        if (ci < chunks) c[v].lo = quant_chunk(c[v], s);
+    }
+    if (early) pdl_enter();
     if (threadIdx.x == 0) xs[row] = s;
     uint8_t *qr = xq + row * static_cast<int64_t>(K);
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         const int ci = threadIdx.x + v * blockDim.x;
-        if (ci < chunks) *reinterpret_cast<uint4 *>(qr + (ci << 4)) = quant_chunk(c[v], s);
+        if (ci < chunks) *reinterpret_cast<uint4 *>(qr + (ci << 4)) = c[v].lo;
     }
 }
 
@@ -157,9 +169,13 @@ __global__ void __launch_bounds__(1024) quant_per_token_two_pass_kernel(const __
 template <int TPG, bool UE8M0, bool SILU>
 __global__ void __launch_bounds__(256) quant_group_kernel(const __nv_bfloat16 *__restrict__ x, int64_t ldx,
                                                           uint8_t *__restrict__ xq, float *__restrict__ xs,
-                                                          int64_t M, int K, int64_t m_pad, float eps)
+                                                          int64_t M, int K, int64_t m_pad, float eps, int early)
 {
-    pdl_enter();
+    // With `early` (the previous launch of the library on this stream does
+    // not write x), each thread's first chunk is loaded and quantized before
+    // the dependency wait, which then comes right before its first store.
+    bool waited = !early;
+    if (!early) pdl_enter();
     const int chunks_per_row = K >> 4;
     const int64_t total = M * chunks_per_row;
     // (row, chunk) of chunk index t, advanced by the grid stride without a
@@ -220,10 +236,15 @@ __global__ void __launch_bounds__(256) quant_group_kernel(const __nv_bfloat16 *_
             } else {
                 q = quant_chunk(c, s);
             }
+            if (!waited) {
+                pdl_enter();
+                waited = true;
+            }
             *reinterpret_cast<uint4 *>(xq + row * static_cast<int64_t>(K) + (ci << 4)) = q;
             if ((ci & (TPG - 1)) == 0) xs[static_cast<int64_t>(ci / TPG) * m_pad + row] = s;
         }
     }
+    if (!waited) pdl_enter();   // threads without a chunk
 }
 
 // ---------------------------------------------------------------------------
@@ -394,10 +415,11 @@ cudaError_t launch_per_token_bulk(const void *x, int64_t M, int64_t K, int64_t l
 
 template <int VPT>
 cudaError_t launch_per_token(const void *x, int64_t M, int K, int64_t ldx, void *xq, float *xs, float eps, int threads,
-                             cudaStream_t st)
+                             bool early, cudaStream_t st)
 {
     return launch_pdl(quant_per_token_kernel<VPT>, dim3(static_cast<unsigned>(M)), dim3(threads), st,
-                      static_cast<const __nv_bfloat16 *>(x), ldx, static_cast<uint8_t *>(xq), xs, K, eps);
+                      static_cast<const __nv_bfloat16 *>(x), ldx, static_cast<uint8_t *>(xq), xs, K, eps,
+                      early ? 1 : 0);
 }
 
 }  // namespace
@@ -425,11 +447,15 @@ cudaError_t launch_quant_per_token(const void *x, int64_t M, int64_t K, int64_t 
     int threads = (chunks + 32 * per_thread - 1) / (32 * per_thread) * 32;
     if (threads > 1024) threads = 1024;
     const int vpt = (chunks + threads - 1) / threads;
+    // The rows may be read before the dependency wait unless the previous
+    // launch of the library on this stream writes them.
+    const size_t xbytes = (static_cast<size_t>(M - 1) * static_cast<size_t>(ldx) + static_cast<size_t>(K)) * 2u;
+    const bool early = !last_launch_writes_overlap(st, x, xbytes);
     switch (vpt) {
-        case 1: return launch_per_token<1>(x, M, static_cast<int>(K), ldx, xq, xs, eps, threads, st);
-        case 2: return launch_per_token<2>(x, M, static_cast<int>(K), ldx, xq, xs, eps, threads, st);
-        case 3: return launch_per_token<3>(x, M, static_cast<int>(K), ldx, xq, xs, eps, threads, st);
-        case 4: return launch_per_token<4>(x, M, static_cast<int>(K), ldx, xq, xs, eps, threads, st);
+        case 1: return launch_per_token<1>(x, M, static_cast<int>(K), ldx, xq, xs, eps, threads, early, st);
+        case 2: return launch_per_token<2>(x, M, static_cast<int>(K), ldx, xq, xs, eps, threads, early, st);
+        case 3: return launch_per_token<3>(x, M, static_cast<int>(K), ldx, xq, xs, eps, threads, early, st);
+        case 4: return launch_per_token<4>(x, M, static_cast<int>(K), ldx, xq, xs, eps, threads, early, st);
         default:
             return launch_pdl(quant_per_token_two_pass_kernel, dim3(static_cast<unsigned>(M)), dim3(1024), st,
                               static_cast<const __nv_bfloat16 *>(x), ldx, static_cast<uint8_t *>(xq), xs,
@@ -457,11 +483,16 @@ cudaError_t launch_group(const void *x, int64_t M, int64_t K, int64_t ldx, int g
     auto *q = static_cast<uint8_t *>(xq);
     const dim3 g = stream_grid(M, K, num_sms), b(256);
     const int k = static_cast<int>(K);
+    // The rows (2K values each with the silu input) may be read before the
+    // dependency wait unless the previous launch of the library writes them.
+    const size_t xbytes =
+        (static_cast<size_t>(M - 1) * static_cast<size_t>(ldx) + static_cast<size_t>(SILU ? 2 * K : K)) * 2u;
+    const int e = last_launch_writes_overlap(st, x, xbytes) ? 0 : 1;
     switch (group) {
-        case 16: return launch_pdl(quant_group_kernel<1, UE8M0, SILU>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps);
-        case 32: return launch_pdl(quant_group_kernel<2, UE8M0, SILU>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps);
-        case 64: return launch_pdl(quant_group_kernel<4, UE8M0, SILU>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps);
-        default: return launch_pdl(quant_group_kernel<8, UE8M0, SILU>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps);
+        case 16: return launch_pdl(quant_group_kernel<1, UE8M0, SILU>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps, e);
+        case 32: return launch_pdl(quant_group_kernel<2, UE8M0, SILU>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps, e);
+        case 64: return launch_pdl(quant_group_kernel<4, UE8M0, SILU>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps, e);
+        default: return launch_pdl(quant_group_kernel<8, UE8M0, SILU>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps, e);
     }
 }
 
