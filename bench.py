@@ -787,10 +787,10 @@ def main():
            "value_one_call_per_m": round(aggregate_value(flops_pass, world, e2e_ms_whole), 2),
            "ms_per_step_one_call_per_m": round(e2e_ms_whole, 4)}
 
-    # Library kernels one pass launches: the blockwise linear is always two;
-    # the channelwise one says how many it takes for its (M, K).
-    launches_per_pass = sum(2 if p["bw"] else int(L.fp8q_linear_channelwise_launches(p["M"], p["K"]))
-                            for p in problems)
+    # Library kernels one pass launches: each linear entry point says how
+    # many it takes for its (M, K).
+    launches_per_pass = sum(int(L.fp8q_linear_blockwise_launches(p["M"], p["K"]) if p["bw"]
+                                else L.fp8q_linear_channelwise_launches(p["M"], p["K"])) for p in problems)
     line = None
     if rank == 0:
         cpu = None
@@ -880,9 +880,10 @@ def measure_quant_variants(gpu, peaks, synthetic):
 
 def measure_fused(gpu, peaks, synthetic):
     """Quantization fused into the blockwise GEMM (one kernel) against the
-    two-kernel blockwise linear, at decode sizes of the blockwise decode
-    layer (N = 4096, K = 7168): back-to-back launches over rotating weight
-    copies (> L2), CUDA events."""
+    blockwise linear entry point (two kernels; at M = 1 its own one-launch
+    matrix-vector form, `linear_launches` 1), at decode sizes of the
+    blockwise decode layer (N = 4096, K = 7168): back-to-back launches over
+    rotating weight copies (> L2), CUDA events."""
     torch, fq, dev, P, L = gpu.torch, gpu.fq, gpu.dev, gpu.P, gpu.L
     fused = []
     fN, fK = 4096, 7168
@@ -916,6 +917,7 @@ def measure_fused(gpu, peaks, synthetic):
         tu = gpu.time_graph(body_two, REPS)
         fb = gemm_bytes(fM, fN, fK, True)
         fused.append({"M": fM, "N": fN, "K": fK, "fused_us": round(fu, 3), "two_kernel_us": round(tu, 3),
+                      "linear_launches": int(L.fp8q_linear_blockwise_launches(fM, fK)),
                       "fused_hbm_frac": round(fb / (fu * 1e-6) / 1e9 / peaks["hbm_gbs"], 3),
                       "two_kernel_hbm_frac": round(fb / (tu * 1e-6) / 1e9 / peaks["hbm_gbs"], 3)})
     del fcopies
@@ -968,44 +970,54 @@ def measure_w8a16(gpu, peaks, synthetic):
 
 
 def measure_linear_one_token(gpu, peaks, synthetic):
-    """The channelwise linear entry point at one and two tokens on the four
-    decode layers, as planned (one fused launch where
-    fp8q_linear_channelwise_launches says 1) and with the schedule override
-    set to the planner's own GEMM plan (which forces the quantizer + GEMM):
-    back-to-back launches over rotating weight copies (> L2), CUDA events;
-    algorithmic bytes N*K + 2*M*K + M*K + 4*M + 2*M*N + 4*N."""
+    """The linear entry points at one and two tokens on the four channelwise
+    decode layers and the blockwise decode layer, as planned (one fused
+    launch where fp8q_linear_*_launches says 1) and with the schedule
+    override set to the planner's own GEMM plan (which forces the quantizer
+    + GEMM): back-to-back launches over rotating weight copies (> L2), CUDA
+    events; algorithmic bytes N*K + 3*M*K + 2*M*N plus the scales."""
     torch, fq, dev, P, L = gpu.torch, gpu.fq, gpu.dev, gpu.P, gpu.L
     rows = []
-    for (lab, N, K) in (("o_proj", 4096, 4096), ("qkv", 6144, 4096), ("down", 4096, 12288),
-                        ("gate_up", 24576, 4096)):
+    for (lab, N, K, bw) in (("o_proj", 4096, 4096, False), ("qkv", 6144, 4096, False),
+                            ("down", 4096, 12288, False), ("gate_up", 24576, 4096, False),
+                            ("blk_4096x7168", 4096, 7168, True)):
         w = synthetic.weights(N, K).to(dev)
-        wq0, ws = fq.fp8q_quant_per_token(w)
+        wq0, ws = fq.fp8q_quant_weight_block128(w) if bw else fq.fp8q_quant_per_token(w)
         del w
         wcp = [wq0] + [wq0.clone() for _ in range(REPS - 1)]
         for M in (1, 2):
+            m_pad = fq.ceil_align(M, 4) if bw else M
             x = synthetic.activations(M, K, outliers=True).to(dev)
-            xq = torch.empty((M, K), dtype=fq.E4M3, device=dev)
-            xs = torch.empty((M,), dtype=torch.float32, device=dev)
+            xq = torch.empty((m_pad, K), dtype=fq.E4M3, device=dev)
+            xs = torch.empty((K // 128 * m_pad if bw else M,), dtype=torch.float32, device=dev)
             out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-            need = fq.fp8q_workspace_bytes(M, N, K)
+            need = fq.fp8q_workspace_bytes(M, N, K, bw)
             work = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
 
-            def body(st, x=x, M=M, N=N, K=K, out=out, xq=xq, xs=xs, work=work, need=need, wcp=wcp):
+            def body(st, x=x, M=M, N=N, K=K, out=out, xq=xq, xs=xs, work=work, need=need, wcp=wcp, ws=ws, bw=bw,
+                     m_pad=m_pad):
                 for r in range(REPS):
-                    if L.fp8q_linear_channelwise(P(x.data_ptr()), P(wcp[r].data_ptr()), K, P(ws.data_ptr()), None,
-                                                 P(out.data_ptr()), M, N, K, P(xq.data_ptr()), P(xs.data_ptr()), 0,
-                                                 P(work.data_ptr()), need, P(st.cuda_stream)) != 0:
+                    if bw:
+                        rc = L.fp8q_linear_blockwise(P(x.data_ptr()), P(wcp[r].data_ptr()), P(ws.data_ptr()), None,
+                                                     P(out.data_ptr()), M, N, K, P(xq.data_ptr()), P(xs.data_ptr()),
+                                                     m_pad, 0, P(work.data_ptr()), need, P(st.cuda_stream))
+                    else:
+                        rc = L.fp8q_linear_channelwise(P(x.data_ptr()), P(wcp[r].data_ptr()), K, P(ws.data_ptr()),
+                                                       None, P(out.data_ptr()), M, N, K, P(xq.data_ptr()),
+                                                       P(xs.data_ptr()), 0, P(work.data_ptr()), need,
+                                                       P(st.cuda_stream))
+                    if rc != 0:
                         raise RuntimeError("linear failed")
 
-            launches = int(L.fp8q_linear_channelwise_launches(M, K))
+            launches = int(L.fp8q_linear_blockwise_launches(M, K) if bw else L.fp8q_linear_channelwise_launches(M, K))
             planned = gpu.time_graph(body, REPS)
-            plan = fq.fp8q_gemm_plan(M, N, K)
+            plan = fq.fp8q_gemm_plan(M, N, K, bw)
             fq.fp8q_set_plan_override(plan["swap_ab"], plan["mma_n"], 0 if plan["stream_k"] else plan["split_k"])
             try:
                 two = gpu.time_graph(body, REPS)
             finally:
                 fq.fp8q_set_plan_override(-1)
-            b = N * K + 3 * M * K + 4 * M + 2 * M * N + 4 * N
+            b = N * K + 3 * M * K + 2 * M * N + ((K // 128) * (4 * M + 4 * (N // 128)) if bw else 4 * M + 4 * N)
             rows.append({"shape": lab, "M": M, "N": N, "K": K, "launches": launches, "linear_us": round(planned, 3),
                          "quant_plus_gemm_us": round(two, 3),
                          "hbm_frac": round(b / (planned * 1e-6) / 1e9 / peaks["hbm_gbs"], 3)})

@@ -46,6 +46,7 @@ EXPORTED = (
     "fp8q_gemm_plan",
     "fp8q_workspace_bytes",
     "fp8q_linear_channelwise_launches",
+    "fp8q_linear_blockwise_launches",
     "fp8q_set_plan_override",
     "fp8q_device_status",
     "fp8q_last_device_status",
@@ -117,6 +118,8 @@ def load_library(path: str | None = None):
     L.fp8q_workspace_bytes.restype = SZ
     L.fp8q_linear_channelwise_launches.argtypes = [I64, I64]
     L.fp8q_linear_channelwise_launches.restype = ctypes.c_int32
+    L.fp8q_linear_blockwise_launches.argtypes = [I64, I64]
+    L.fp8q_linear_blockwise_launches.restype = ctypes.c_int32
     _lib = L
     return L
 
@@ -536,6 +539,12 @@ def fp8q_linear_channelwise_launches(M: int, K: int) -> int:
     """Kernel launches fp8q_linear_channelwise makes for M tokens of K values
     (1: the fused one-token form; 2: quantizer + GEMM; 0: nothing to do)."""
     return int(load_library().fp8q_linear_channelwise_launches(M, K))
+
+
+def fp8q_linear_blockwise_launches(M: int, K: int) -> int:
+    """Kernel launches fp8q_linear_blockwise makes for M tokens of K values
+    (1: the fused one-token form; 2: quantizer + GEMM; 0: nothing to do)."""
+    return int(load_library().fp8q_linear_blockwise_launches(M, K))
 
 
 def fp8q_set_plan_override(swap_ab: int, mma_n: int = 0, split_k: int = 1) -> None:

@@ -266,6 +266,12 @@ int32_t fp8q_linear_channelwise_launches(int64_t M, int64_t K)
     return linear_gemv_fits(M, K) && !plan_override_active() ? 1 : 2;
 }
 
+int32_t fp8q_linear_blockwise_launches(int64_t M, int64_t K)
+{
+    if (M <= 0 || K <= 0) return 0;
+    return linear_blk_gemv_fits(M, K) && !plan_override_active() ? 1 : 2;
+}
+
 fp8q_status fp8q_linear_blockwise(const void *x, const void *w, const float *w_scale, const void *bias, void *out,
                                   int64_t M, int64_t N, int64_t K, void *xq, float *xs, int64_t m_pad,
                                   fp8q_out_dtype out_dtype, void *workspace, size_t workspace_bytes, void *stream)
@@ -281,6 +287,11 @@ fp8q_status fp8q_linear_blockwise(const void *x, const void *w, const float *w_s
         !aligned16(xs) || !aligned4(w_scale))
         return FP8Q_ERR_INVALID_ARG;
     if (bias != nullptr && (reinterpret_cast<uintptr_t>(bias) & 1u)) return FP8Q_ERR_INVALID_ARG;
+    // One token: one launch, the group quantization fused into a
+    // matrix-vector product (unless a schedule override asks for the GEMM).
+    if (linear_blk_gemv_fits(M, K) && !plan_override_active())
+        return from_cuda(launch_linear_blk_gemv(x, w, w_scale, bias, out, xq, xs, m_pad, N, K, 1e-10f,
+                                                out_dtype == FP8Q_OUT_FP16, as_stream(stream)));
     s = fp8q_quant_per_token_group_row_padded(x, M, K, K, 128, 1e-10f, 4, xq, xs, m_pad, stream);
     if (s != FP8Q_OK) return s;
     return fp8q_scaled_mm_blockwise(xq, w, xs, w_scale, bias, out, M, m_pad, N, K, out_dtype, workspace,

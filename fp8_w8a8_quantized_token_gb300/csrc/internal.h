@@ -117,6 +117,12 @@ bool plan_override_active();
 // schedule override is set.  Measured on GB300 it is faster there than the
 // quantizer + tensor-core GEMM, and slower with two tokens or longer rows.
 inline bool linear_gemv_fits(int64_t M, int64_t K) { return M == 1 && K <= 4096; }
+// The blockwise linear for one token with K <= 8192 runs the same way, with
+// the group-128 quantization fused (linear_gemv.cu).
+inline bool linear_blk_gemv_fits(int64_t M, int64_t K) { return M == 1 && K <= 8192; }
+cudaError_t launch_linear_blk_gemv(const void *x, const void *w, const float *w_scale, const void *bias, void *out,
+                                   void *xq, float *xs, int64_t m_pad, int64_t N, int64_t K, float eps, bool out_fp16,
+                                   cudaStream_t st);
 cudaError_t launch_linear_pt_gemv(const void *x, const void *w, int64_t ldw, const float *w_scale, const void *bias,
                                   void *out, void *xq, float *xs, int64_t M, int64_t N, int64_t K, float eps,
                                   bool out_fp16, cudaStream_t st);

@@ -31,6 +31,16 @@
 // issues its first chunk's weight loads before the dependency wait; after
 // each row group it issues the next group's first chunk before the
 // cross-warp reduction.
+//
+// The blockwise linear for one token (linear_blk_gemv_kernel) is the same
+// kernel with the blockwise scheme's arithmetic ("Remove per-call padding
+// overhead of the FP8 blockwise GEMM" page, key source snippets): the row is
+// quantized in groups of 128 (the 8 lanes of a group reduce its amax; the
+// group quantizer's codes and scales bit for bit, CTA 0 storing them in the
+// row-padded layout), and each lane's 16 exact products are summed and then
+// scaled by the group scale times the weight block's scale (the CTA's 8
+// output channels lie in one 128-row block) before they are accumulated;
+// out = round(sum + bias[n]).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -165,6 +175,144 @@ __global__ void __launch_bounds__(32 * kWarps) linear_pt_gemv_kernel(
     }
 }
 
+template <typename OutT>
+__global__ void __launch_bounds__(32 * kWarps, 3) linear_blk_gemv_kernel(
+    const __nv_bfloat16 *__restrict__ x, const uint8_t *__restrict__ w, const float *__restrict__ w_scale,
+    const __nv_bfloat16 *__restrict__ bias, OutT *__restrict__ out, uint8_t *__restrict__ xq,
+    float *__restrict__ xs, int64_t m_pad, int N, int K, float eps, int preload)
+{
+    constexpr int ROWS = 8;
+    extern __shared__ __align__(16) uint8_t blk_dyn[];   // bf16 [K] decoded codes, then fp32 [K/128] scales
+    __shared__ float red[2][kWarps][ROWS][1];
+    __nv_bfloat16 *xdec = reinterpret_cast<__nv_bfloat16 *>(blk_dyn);
+    float *sgrp = reinterpret_cast<float *>(blk_dyn + static_cast<size_t>(K) * 2);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nchunks = (K + kChunk - 1) / kChunk;
+    const int groups = (N + ROWS - 1) / ROWS;
+    const int kblocks = K >> 7;
+    constexpr int kStride = 32 * kWarps * 16;
+
+    uint4 wv[ROWS];
+    int g = blockIdx.x;
+    if (preload && warp < nchunks && g < groups) gemv::load_weights<ROWS>(w, K, g * ROWS, N, K, warp, lane, wv);
+    pdl_wait();
+    pdl_trigger();
+    if (!preload && warp < nchunks && g < groups) gemv::load_weights<ROWS>(w, K, g * ROWS, N, K, warp, lane, wv);
+
+    // Group scales and codes.  A warp's pieces k = k0 + 16 * lane cover 512
+    // values; the loop bound is the warp's (K is a multiple of 128, so a
+    // group is either wholly inside or wholly past K).
+    for (int k0 = warp * kChunk; k0 < K; k0 += kStride) {
+        const int k = k0 + lane * 16;
+        const bool in = k < K;
+        Chunk16 v;
+        float am = 0.0f;
+        if (in) {
+            v = load_chunk(x + k);
+            am = chunk_amax(v, 0.0f);
+        }
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        if (in) {
+            const float sc = scale_of(am, eps);
+            const uint4 q = quant_chunk(v, sc);
+            if ((lane & 7) == 0) sgrp[k >> 7] = sc;
+            if (xq != nullptr && blockIdx.x == 0) {
+                *reinterpret_cast<uint4 *>(xq + k) = q;
+                if ((lane & 7) == 0) xs[static_cast<int64_t>(k >> 7) * m_pad] = sc;
+            }
+            const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+            uint32_t d[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float2 f = gemv::e4m3x2_to_f32x2(words[j >> 1] >> (16 * (j & 1)));
+                d[j] = __byte_perm(__float_as_uint(f.x), __float_as_uint(f.y), 0x7632);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(xdec + k);
+            dst[0] = make_uint4(d[0], d[1], d[2], d[3]);
+            dst[1] = make_uint4(d[4], d[5], d[6], d[7]);
+        }
+    }
+    __syncthreads();
+
+    for (int buf = 0; g < groups; g += gridDim.x, buf ^= 1) {
+        const int n0 = g * ROWS;
+        const float *ws_row = w_scale + static_cast<int64_t>(n0 >> 7) * kblocks;
+        float2 acc[ROWS][1];   // the scaled sum in .x (.y stays 0)
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) acc[r][0] = make_float2(0.0f, 0.0f);
+        for (int c = warp; c < nchunks; c += kWarps) {
+            if (c != warp) gemv::load_weights<ROWS>(w, K, n0, N, K, c, lane, wv);
+            const int k = c * kChunk + lane * 16;
+            if (k < K) {
+                float2 xa[1][8];
+                const uint4 *src = reinterpret_cast<const uint4 *>(xdec + k);
+                const uint4 lo = src[0], hi = src[1];
+                const uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    xa[0][j] = make_float2(__uint_as_float(words[j] << 16), __uint_as_float(words[j] & 0xFFFF0000u));
+                float2 t[ROWS][1];
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) t[r][0] = make_float2(0.0f, 0.0f);
+                gemv::fma_piece<ROWS, 1>(wv, xa, t);
+                const float f = sgrp[k >> 7] * __ldg(ws_row + (k >> 7));
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) acc[r][0].x = fmaf(t[r][0].x + t[r][0].y, f, acc[r][0].x);
+            }
+        }
+        const int gn = g + static_cast<int>(gridDim.x);
+        if (gn < groups && warp < nchunks) gemv::load_weights<ROWS>(w, K, gn * ROWS, N, K, warp, lane, wv);
+        const float sum = gemv::reduce_cta<ROWS, 1>(acc, red[buf], warp, lane);
+        if (threadIdx.x < ROWS) {
+            const int n = n0 + threadIdx.x;
+            if (n < N) {
+                const float b = bias != nullptr ? __bfloat162float(bias[n]) : 0.0f;
+                out[n] = gemv::to_out<OutT>(sum + b);
+            }
+        }
+    }
+}
+
+// Every CTA that fits: per_sm (from the occupancy of `kernel` with `smem`)
+// times the SMs, at most one per group.
+template <typename Kernel>
+cudaError_t persistent_grid(Kernel kernel, size_t smem, int groups, int *grid)
+{
+    int per_sm = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 32 * kWarps, smem);
+    if (e != cudaSuccess) return e;
+    const int sms = current_device_sms();
+    if (per_sm <= 0 || sms <= 0) return cudaErrorInvalidConfiguration;
+    *grid = groups < per_sm * sms ? groups : per_sm * sms;
+    return cudaSuccess;
+}
+
+template <typename OutT>
+cudaError_t launch_blk(const void *x, const void *w, const float *w_scale, const void *bias, void *out, void *xq,
+                       float *xs, int64_t m_pad, int N, int K, float eps, bool preload, cudaStream_t st)
+{
+    auto kernel = linear_blk_gemv_kernel<OutT>;
+    const size_t smem = static_cast<size_t>(K) * 2u + static_cast<size_t>(K / 128) * 4u;
+    if (smem > 48u * 1024u) return cudaErrorInvalidValue;
+    int grid = 0;
+    cudaError_t e = persistent_grid(kernel, smem, (N + 7) / 8, &grid);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(32 * kWarps);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<const __nv_bfloat16 *>(x), static_cast<const uint8_t *>(w),
+                              w_scale, static_cast<const __nv_bfloat16 *>(bias), static_cast<OutT *>(out),
+                              static_cast<uint8_t *>(xq), xs, m_pad, N, K, eps, preload ? 1 : 0);
+}
+
 template <int MT, typename OutT>
 cudaError_t launch_t(const void *x, const void *w, int64_t ldw, const float *w_scale, const void *bias, void *out,
                      void *xq, float *xs, int M, int N, int K, float eps, bool preload, cudaStream_t st)
@@ -172,16 +320,12 @@ cudaError_t launch_t(const void *x, const void *w, int64_t ldw, const float *w_s
     auto kernel = linear_pt_gemv_kernel<MT, OutT>;
     const size_t smem = static_cast<size_t>(MT) * static_cast<size_t>(K) * 2u;   // at most 48 KB (no opt-in)
     if (smem > 48u * 1024u) return cudaErrorInvalidValue;
-    int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 32 * kWarps, smem);
-    if (e != cudaSuccess) return e;
-    const int sms = current_device_sms();
-    if (per_sm <= 0 || sms <= 0) return cudaErrorInvalidConfiguration;
     // Every CTA that fits (fewer CTAs with whole rounds of groups each
     // measured slower: the rounds are latency-bound).
     constexpr int kRows = gemv::rows<MT>();
-    const int groups = (N + kRows - 1) / kRows;
-    const int grid = groups < per_sm * sms ? groups : per_sm * sms;
+    int grid = 0;
+    cudaError_t e = persistent_grid(kernel, smem, (N + kRows - 1) / kRows, &grid);
+    if (e != cudaSuccess) return e;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -214,6 +358,23 @@ cudaError_t launch_linear_pt_gemv(const void *x, const void *w, int64_t ldw, con
     if (e == cudaSuccess)
         note_launch_writes(st, out, static_cast<size_t>(M) * N * 2, xq, static_cast<size_t>(M) * K, xs,
                            static_cast<size_t>(M) * 4);
+    return e;
+}
+
+cudaError_t launch_linear_blk_gemv(const void *x, const void *w, const float *w_scale, const void *bias, void *out,
+                                   void *xq, float *xs, int64_t m_pad, int64_t N, int64_t K, float eps, bool out_fp16,
+                                   cudaStream_t st)
+{
+    if (!linear_blk_gemv_fits(1, K) || K % 128 != 0 || N % 128 != 0) return cudaErrorInvalidValue;
+    const size_t wbytes = static_cast<size_t>(N) * static_cast<size_t>(K);
+    const bool preload = !last_launch_writes_overlap(st, w, wbytes);
+    const int n = static_cast<int>(N), k = static_cast<int>(K);
+    const cudaError_t e =
+        out_fp16 ? launch_blk<__half>(x, w, w_scale, bias, out, xq, xs, m_pad, n, k, eps, preload, st)
+                 : launch_blk<__nv_bfloat16>(x, w, w_scale, bias, out, xq, xs, m_pad, n, k, eps, preload, st);
+    if (e == cudaSuccess)
+        note_launch_writes(st, out, static_cast<size_t>(N) * 2, xq, xq != nullptr ? static_cast<size_t>(K) : 0, xs,
+                           xs != nullptr ? static_cast<size_t>(K / 128) * static_cast<size_t>(m_pad) * 4 : 0);
     return e;
 }
 

@@ -288,7 +288,12 @@ FP8Q_API size_t fp8q_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t bl
  * codes and scales as after the two launches).  Its sums are accumulated in
  * another order than the tensor-core GEMM's, so its output is within the
  * GEMM tolerance of the two-kernel result rather than bit-identical.
- * fp8q_linear_channelwise_launches tells which form a call takes.
+ * fp8q_linear_blockwise with ONE token and K <= 8192 (no override) is one
+ * launch as well: the group-128 quantization fused into the matrix-vector
+ * product (each 16-value partial sum scaled by its group scale times its
+ * weight block's scale), xq row 0 and xs[kb * m_pad] written by CTA 0.
+ * fp8q_linear_channelwise_launches / fp8q_linear_blockwise_launches tell
+ * which form a call takes.
  * fp8q_linear_channelwise : xq e4m3 [M, K], xs fp32 [M].
  * fp8q_linear_blockwise   : xq e4m3 [m_pad, K], xs fp32 [K/128][m_pad],
  *   m_pad = ceil(M/4)*4 or a larger multiple of 4 -- the row-padded
@@ -309,6 +314,8 @@ FP8Q_API fp8q_status fp8q_linear_blockwise(const void *x, const void *w, const f
  * 1 (the fused one-token form), 2 (quantizer + GEMM), or 0 for M <= 0 or
  * K <= 0.  Host only; reads the schedule override. */
 FP8Q_API int32_t fp8q_linear_channelwise_launches(int64_t M, int64_t K);
+/* The same for fp8q_linear_blockwise. */
+FP8Q_API int32_t fp8q_linear_blockwise_launches(int64_t M, int64_t K);
 
 /* ---------------------------------------------------------------------------
  * fp8q_scaled_mm_w8a16 -- weight-only FP8 linear (W8A16): bf16 activations

@@ -171,3 +171,89 @@ def test_few_token_linear_wide_rows(dev, M, K):
     wq, ws = weights(dev, 136, K, seed=K)
     x = synthetic.activations(M, K, outliers=True, seed=K + M)
     check(dev, x, wq, ws, what=f"{M}x136x{K}")
+
+
+# ---------------------------------------------------------------------------
+# The blockwise linear for one token (group-128 quantization fused, K <= 8192)
+# ---------------------------------------------------------------------------
+
+def linear_blockwise(dev, x, wq, ws, bias=None, out_dtype=torch.bfloat16):
+    """fp8q_linear_blockwise through the C ABI with caller-owned, canary-filled
+    row-padded scratch; returns out, xq [m_pad, K], xs [K/128, m_pad]."""
+    L = fq.load_library()
+    M, K = x.shape
+    N = wq.shape[0]
+    m_pad = fq.ceil_align(M, 4)
+    xd = x.to(dev)
+    xq = torch.full((m_pad, K), 0x5A, dtype=torch.uint8, device=dev)
+    xs = torch.full((K // 128, m_pad), -3.0, dtype=torch.float32, device=dev)
+    out = torch.empty((M, N), dtype=out_dtype, device=dev)
+    bd = None if bias is None else bias.to(dev)
+    st = P(torch.cuda.current_stream(dev).cuda_stream)
+    rc = L.fp8q_linear_blockwise(P(xd.data_ptr()), P(wq.data_ptr()), P(ws.data_ptr()),
+                                 None if bd is None else P(bd.data_ptr()), P(out.data_ptr()), M, N, K,
+                                 P(xq.data_ptr()), P(xs.data_ptr()), m_pad,
+                                 fq.FP8Q_OUT_FP16 if out_dtype == torch.float16 else fq.FP8Q_OUT_BF16, None, 0, st)
+    assert rc == fq.FP8Q_OK
+    torch.cuda.synchronize()
+    return out, xq, xs
+
+
+def check_blockwise(dev, x, wq, ws, bias=None, out_dtype=torch.bfloat16, what=""):
+    M = x.shape[0]
+    out, xq, xs = linear_blockwise(dev, x, wq, ws, bias, out_dtype)
+    rq, rs = oracle.quant_group_row_padded(x, 128, threads=THREADS)
+    gq, gs = u8(xq), xs.cpu().numpy()
+    assert np.array_equal(gq[:M], rq[:M]), f"{what}: group codes differ from the oracle's"
+    assert np.array_equal(gs[:, :M], rs[:, :M]), f"{what}: group scales differ from the oracle's"
+    assert (gq[M:] == 0x5A).all() and (gs[:, M:] == -3.0).all(), f"{what}: padding rows written"
+    fp16 = out_dtype == torch.float16
+    ref = ref_values(oracle.gemm_blockwise(rq, u8(wq), rs, ws.cpu().numpy(), M, bias=bias, out_fp16=fp16), fp16)
+    assert_gemm_close(out_values(out), ref, what)
+    return out, xq, xs
+
+
+@pytest.mark.parametrize("N,K", [(4096, 7168), (256, 128), (384, 1152), (24576, 3072), (128, 8192), (256, 8320)])
+def test_one_token_blockwise_linear_parity(dev, N, K):
+    """The blockwise decode layer, one K block, a K that leaves a warp's
+    512-value span partly past the row (1152 = 2 x 512 + 128), a wide N, the
+    longest row the fused launch takes and one past it (two kernels)."""
+    assert fq.fp8q_linear_blockwise_launches(1, K) == (1 if K <= 8192 else 2)
+    w = synthetic.weights(N, K, seed=N + K)
+    wq, ws = fq.fp8q_quant_weight_block128(w.to(dev))
+    x = synthetic.activations(1, K, outliers=True, seed=K)
+    check_blockwise(dev, x, wq, ws, what=f"blockwise 1x{N}x{K}")
+
+
+def test_one_token_blockwise_linear_bias_fp16_and_special_groups(dev):
+    """Bias, fp16 output, and groups of zeros (scale eps / 448), of one huge
+    outlier and of E4M3 rounding midpoints."""
+    N, K = 512, 1024
+    w = synthetic.weights(N, K, seed=41)
+    wq, ws = fq.fp8q_quant_weight_block128(w.to(dev))
+    b = synthetic.bias(N, seed=42)
+    x = synthetic.activations(1, K, outliers=True, seed=43).float()
+    x[0, 128:256] = 0.0
+    x[0, 256:384] = 1e-3
+    x[0, 300] = 2.0e4
+    g = torch.Generator().manual_seed(44)
+    x[0, 384:512] = (torch.randint(8, 16, (128,), generator=g).float() + 0.5) / 8.0
+    x[0, 384] = 448.0
+    x = x.to(torch.bfloat16)
+    check_blockwise(dev, x, wq, ws, bias=b, what="blockwise bias bf16")
+    check_blockwise(dev, x, wq, ws, bias=b, out_dtype=torch.float16, what="blockwise bias fp16")
+
+
+def test_one_token_blockwise_same_codes_as_two_kernels(dev, schedule):
+    N, K = 4096, 7168
+    w = synthetic.weights(N, K, seed=51)
+    wq, ws = fq.fp8q_quant_weight_block128(w.to(dev))
+    x = synthetic.activations(1, K, outliers=True, seed=52)
+    out1, xq1, xs1 = check_blockwise(dev, x, wq, ws, what="fused")
+    plan = fq.fp8q_gemm_plan(1, N, K, True)
+    fq.fp8q_set_plan_override(plan["swap_ab"], plan["mma_n"], 0 if plan["stream_k"] else plan["split_k"])
+    assert fq.fp8q_linear_blockwise_launches(1, K) == 2
+    out2, xq2, xs2 = linear_blockwise(dev, x, wq, ws)
+    fq.fp8q_set_plan_override(-1)
+    assert torch.equal(xq1, xq2) and torch.equal(xs1, xs2)
+    assert_gemm_close(out_values(out1), out_values(out2), "blockwise fused vs two kernels")
