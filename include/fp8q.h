@@ -358,7 +358,9 @@ FP8Q_API fp8q_status fp8q_scaled_mm_w8a16(const void *x, int64_t ldx, const void
  * two-kernel fp8q_linear_blockwise on back-to-back layers (the activation
  * reads issued after the dependency wait queue behind the weight stream),
  * so fp8q_linear_blockwise does not use it; it is for callers that want a
- * single launch per layer.
+ * single launch per layer with the GEMM's tensor-core sums.  (For ONE token
+ * fp8q_linear_blockwise is itself a single, faster launch -- the
+ * matrix-vector form above -- whose sums run in another order.)
  * x   : bf16 [M, K], row stride ldx >= K (ldx % 8 == 0), 16-byte aligned.
  * w, w_scale, bias, out, out_dtype: as fp8q_linear_blockwise.  No scratch.
  * ------------------------------------------------------------------------- */
