@@ -71,6 +71,7 @@ PROFILE_CASES = {
     # the one-token channelwise linear (quantization fused, one launch)
     "linear1_oproj": ("linear1", 1, 4096, 4096),
     "linear1_gateup": ("linear1", 1, 24576, 4096),
+    "linear1_blockwise": ("linear1_blockwise", 1, 4096, 7168),
 }
 PROFILE_WARMUP = 2
 
@@ -338,6 +339,11 @@ def run_profile_case(name: str) -> int:
             torch.cuda.synchronize()
             for _ in range(n):
                 fq.fp8q_linear_channelwise(x, wq, ws)
+        elif kind == "linear1_blockwise":
+            wq, ws = fq.fp8q_quant_weight_block128(w)
+            torch.cuda.synchronize()
+            for _ in range(n):
+                fq.fp8q_linear_blockwise(x, wq, ws)
         elif kind == "channelwise":
             wq, ws = fq.fp8q_quant_per_token(w)
             xq, xs = fq.fp8q_quant_per_token(x)
