@@ -986,7 +986,8 @@ def measure_linear_one_token(gpu, peaks, synthetic):
     rows = []
     for (lab, N, K, bw) in (("o_proj", 4096, 4096, False), ("qkv", 6144, 4096, False),
                             ("down", 4096, 12288, False), ("gate_up", 24576, 4096, False),
-                            ("blk_4096x7168", 4096, 7168, True)):
+                            ("blk_4096x7168", 4096, 7168, True), ("blk_24576x3072", 24576, 3072, True),
+                            ("blk_3072x12288", 3072, 12288, True)):
         w = synthetic.weights(N, K).to(dev)
         wq0, ws = fq.fp8q_quant_weight_block128(w) if bw else fq.fp8q_quant_per_token(w)
         del w

@@ -57,8 +57,22 @@ namespace {
 using gemv::kChunk;
 using gemv::kWarps;
 
-template <int MT, typename OutT, int ROWS = gemv::rows<MT>()>
-__global__ void __launch_bounds__(32 * kWarps) linear_pt_gemv_kernel(
+// NCW: chunks per warp and group (ceil(K / 4096)); a warp requests all of
+// them at once.  Registers: NCW * ROWS * 4 for the weights, so the CTAs per
+// SM fall from 3 to 2 to 1 as NCW grows.
+constexpr int min_ctas(int ncw) { return ncw == 1 ? 3 : ncw == 2 ? 2 : 1; }
+
+// All NCW chunks of a group for this warp (zeros past K).
+template <int NCW, int ROWS>
+__device__ __forceinline__ void load_group(const uint8_t *__restrict__ w, int64_t ldw, int n0, int N, int K, int warp,
+                                           int lane, uint4 (&wv)[NCW][ROWS])
+{
+#pragma unroll
+    for (int i = 0; i < NCW; ++i) gemv::load_weights<ROWS>(w, ldw, n0, N, K, warp + i * kWarps, lane, wv[i]);
+}
+
+template <int MT, int NCW, typename OutT, int ROWS = gemv::rows<MT>()>
+__global__ void __launch_bounds__(32 * kWarps, min_ctas(NCW)) linear_pt_gemv_kernel(
     const __nv_bfloat16 *__restrict__ x, const uint8_t *__restrict__ w, int64_t ldw,
     const float *__restrict__ w_scale, const __nv_bfloat16 *__restrict__ bias, OutT *__restrict__ out,
     uint8_t *__restrict__ xq, float *__restrict__ xs, int M, int N, int K, float eps, int preload)
@@ -69,16 +83,15 @@ __global__ void __launch_bounds__(32 * kWarps) linear_pt_gemv_kernel(
     __shared__ float scale_sh[MT], rcp_sh[MT];
     __nv_bfloat16 *xdec = reinterpret_cast<__nv_bfloat16 *>(xdec_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nchunks = (K + kChunk - 1) / kChunk;
     const int groups = (N + ROWS - 1) / ROWS;
     constexpr int kStride = 32 * kWarps * 16;   // the CTA's 16-value pieces cover kStride of K per pass
 
-    uint4 wv[ROWS];
+    uint4 wv[NCW][ROWS];
     int g = blockIdx.x;
-    if (preload && warp < nchunks && g < groups) gemv::load_weights<ROWS>(w, ldw, g * ROWS, N, K, warp, lane, wv);
+    if (preload && g < groups) load_group<NCW, ROWS>(w, ldw, g * ROWS, N, K, warp, lane, wv);
     pdl_wait();
     pdl_trigger();
-    if (!preload && warp < nchunks && g < groups) gemv::load_weights<ROWS>(w, ldw, g * ROWS, N, K, warp, lane, wv);
+    if (!preload && g < groups) load_group<NCW, ROWS>(w, ldw, g * ROWS, N, K, warp, lane, wv);
 
     // Per-token scales: the amax of each thread's 16-value pieces k =
     // 16 * thread + kStride * j, then over lanes, then over warps.
@@ -141,10 +154,10 @@ __global__ void __launch_bounds__(32 * kWarps) linear_pt_gemv_kernel(
         for (int r = 0; r < ROWS; ++r)
 #pragma unroll
             for (int m = 0; m < MT; ++m) acc[r][m] = make_float2(0.0f, 0.0f);
-        // The first chunk's weights (c = warp) are already in wv.
-        for (int c = warp; c < nchunks; c += kWarps) {
-            if (c != warp) gemv::load_weights<ROWS>(w, ldw, n0, N, K, c, lane, wv);
-            const int k = c * kChunk + lane * 16;
+        // This warp's chunks c = warp + 8 i of the group are already in wv.
+#pragma unroll
+        for (int i = 0; i < NCW; ++i) {
+            const int k = (warp + i * kWarps) * kChunk + lane * 16;
             if (k < K) {
                 float2 xa[MT][8];
 #pragma unroll
@@ -156,12 +169,12 @@ __global__ void __launch_bounds__(32 * kWarps) linear_pt_gemv_kernel(
                     for (int j = 0; j < 8; ++j)
                         xa[m][j] = make_float2(__uint_as_float(words[j] << 16), __uint_as_float(words[j] & 0xFFFF0000u));
                 }
-                gemv::fma_piece<ROWS, MT>(wv, xa, acc);
+                gemv::fma_piece<ROWS, MT>(wv[i], xa, acc);
             }
         }
-        // The next group's first chunk, in flight during the reduction.
+        // The next group's chunks, in flight during the reduction.
         const int gn = g + static_cast<int>(gridDim.x);
-        if (gn < groups && warp < nchunks) gemv::load_weights<ROWS>(w, ldw, gn * ROWS, N, K, warp, lane, wv);
+        if (gn < groups) load_group<NCW, ROWS>(w, ldw, gn * ROWS, N, K, warp, lane, wv);
         const float sum = gemv::reduce_cta<ROWS, MT>(acc, red[buf], warp, lane);
         if (threadIdx.x < ROWS * MT) {
             const int r = threadIdx.x / MT, m = threadIdx.x % MT;
@@ -175,8 +188,8 @@ __global__ void __launch_bounds__(32 * kWarps) linear_pt_gemv_kernel(
     }
 }
 
-template <typename OutT>
-__global__ void __launch_bounds__(32 * kWarps, 3) linear_blk_gemv_kernel(
+template <int NCW, typename OutT>
+__global__ void __launch_bounds__(32 * kWarps, min_ctas(NCW)) linear_blk_gemv_kernel(
     const __nv_bfloat16 *__restrict__ x, const uint8_t *__restrict__ w, const float *__restrict__ w_scale,
     const __nv_bfloat16 *__restrict__ bias, OutT *__restrict__ out, uint8_t *__restrict__ xq,
     float *__restrict__ xs, int64_t m_pad, int N, int K, float eps, int preload)
@@ -187,17 +200,16 @@ __global__ void __launch_bounds__(32 * kWarps, 3) linear_blk_gemv_kernel(
     __nv_bfloat16 *xdec = reinterpret_cast<__nv_bfloat16 *>(blk_dyn);
     float *sgrp = reinterpret_cast<float *>(blk_dyn + static_cast<size_t>(K) * 2);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nchunks = (K + kChunk - 1) / kChunk;
     const int groups = (N + ROWS - 1) / ROWS;
     const int kblocks = K >> 7;
     constexpr int kStride = 32 * kWarps * 16;
 
-    uint4 wv[ROWS];
+    uint4 wv[NCW][ROWS];
     int g = blockIdx.x;
-    if (preload && warp < nchunks && g < groups) gemv::load_weights<ROWS>(w, K, g * ROWS, N, K, warp, lane, wv);
+    if (preload && g < groups) load_group<NCW, ROWS>(w, K, g * ROWS, N, K, warp, lane, wv);
     pdl_wait();
     pdl_trigger();
-    if (!preload && warp < nchunks && g < groups) gemv::load_weights<ROWS>(w, K, g * ROWS, N, K, warp, lane, wv);
+    if (!preload && g < groups) load_group<NCW, ROWS>(w, K, g * ROWS, N, K, warp, lane, wv);
 
     // Group scales and codes.  A warp's pieces k = k0 + 16 * lane cover 512
     // values; the loop bound is the warp's (K is a multiple of 128, so a
@@ -241,9 +253,9 @@ __global__ void __launch_bounds__(32 * kWarps, 3) linear_blk_gemv_kernel(
         float2 acc[ROWS][1];   // the scaled sum in .x (.y stays 0)
 #pragma unroll
         for (int r = 0; r < ROWS; ++r) acc[r][0] = make_float2(0.0f, 0.0f);
-        for (int c = warp; c < nchunks; c += kWarps) {
-            if (c != warp) gemv::load_weights<ROWS>(w, K, n0, N, K, c, lane, wv);
-            const int k = c * kChunk + lane * 16;
+#pragma unroll
+        for (int i = 0; i < NCW; ++i) {
+            const int k = (warp + i * kWarps) * kChunk + lane * 16;
             if (k < K) {
                 float2 xa[1][8];
                 const uint4 *src = reinterpret_cast<const uint4 *>(xdec + k);
@@ -255,14 +267,14 @@ __global__ void __launch_bounds__(32 * kWarps, 3) linear_blk_gemv_kernel(
                 float2 t[ROWS][1];
 #pragma unroll
                 for (int r = 0; r < ROWS; ++r) t[r][0] = make_float2(0.0f, 0.0f);
-                gemv::fma_piece<ROWS, 1>(wv, xa, t);
+                gemv::fma_piece<ROWS, 1>(wv[i], xa, t);
                 const float f = sgrp[k >> 7] * __ldg(ws_row + (k >> 7));
 #pragma unroll
                 for (int r = 0; r < ROWS; ++r) acc[r][0].x = fmaf(t[r][0].x + t[r][0].y, f, acc[r][0].x);
             }
         }
         const int gn = g + static_cast<int>(gridDim.x);
-        if (gn < groups && warp < nchunks) gemv::load_weights<ROWS>(w, K, gn * ROWS, N, K, warp, lane, wv);
+        if (gn < groups) load_group<NCW, ROWS>(w, K, gn * ROWS, N, K, warp, lane, wv);
         const float sum = gemv::reduce_cta<ROWS, 1>(acc, red[buf], warp, lane);
         if (threadIdx.x < ROWS) {
             const int n = n0 + threadIdx.x;
@@ -288,11 +300,11 @@ cudaError_t persistent_grid(Kernel kernel, size_t smem, int groups, int *grid)
     return cudaSuccess;
 }
 
-template <typename OutT>
+template <int NCW, typename OutT>
 cudaError_t launch_blk(const void *x, const void *w, const float *w_scale, const void *bias, void *out, void *xq,
                        float *xs, int64_t m_pad, int N, int K, float eps, bool preload, cudaStream_t st)
 {
-    auto kernel = linear_blk_gemv_kernel<OutT>;
+    auto kernel = linear_blk_gemv_kernel<NCW, OutT>;
     const size_t smem = static_cast<size_t>(K) * 2u + static_cast<size_t>(K / 128) * 4u;
     if (smem > 48u * 1024u) return cudaErrorInvalidValue;
     int grid = 0;
@@ -313,11 +325,11 @@ cudaError_t launch_blk(const void *x, const void *w, const float *w_scale, const
                               static_cast<uint8_t *>(xq), xs, m_pad, N, K, eps, preload ? 1 : 0);
 }
 
-template <int MT, typename OutT>
+template <int MT, int NCW, typename OutT>
 cudaError_t launch_t(const void *x, const void *w, int64_t ldw, const float *w_scale, const void *bias, void *out,
                      void *xq, float *xs, int M, int N, int K, float eps, bool preload, cudaStream_t st)
 {
-    auto kernel = linear_pt_gemv_kernel<MT, OutT>;
+    auto kernel = linear_pt_gemv_kernel<MT, NCW, OutT>;
     const size_t smem = static_cast<size_t>(MT) * static_cast<size_t>(K) * 2u;   // at most 48 KB (no opt-in)
     if (smem > 48u * 1024u) return cudaErrorInvalidValue;
     // Every CTA that fits (fewer CTAs with whole rounds of groups each
@@ -352,9 +364,10 @@ cudaError_t launch_linear_pt_gemv(const void *x, const void *w, int64_t ldw, con
     const size_t wbytes = static_cast<size_t>(N - 1) * static_cast<size_t>(ldw) + static_cast<size_t>(K);
     const bool preload = !last_launch_writes_overlap(st, w, wbytes);
     const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+    // One chunk per warp (K <= 4096): the rows this form is used for.
     const cudaError_t e =
-        out_fp16 ? launch_t<1, __half>(x, w, ldw, w_scale, bias, out, xq, xs, m, n, k, eps, preload, st)
-                 : launch_t<1, __nv_bfloat16>(x, w, ldw, w_scale, bias, out, xq, xs, m, n, k, eps, preload, st);
+        out_fp16 ? launch_t<1, 1, __half>(x, w, ldw, w_scale, bias, out, xq, xs, m, n, k, eps, preload, st)
+                 : launch_t<1, 1, __nv_bfloat16>(x, w, ldw, w_scale, bias, out, xq, xs, m, n, k, eps, preload, st);
     if (e == cudaSuccess)
         note_launch_writes(st, out, static_cast<size_t>(M) * N * 2, xq, static_cast<size_t>(M) * K, xs,
                            static_cast<size_t>(M) * 4);
@@ -369,9 +382,23 @@ cudaError_t launch_linear_blk_gemv(const void *x, const void *w, const float *w_
     const size_t wbytes = static_cast<size_t>(N) * static_cast<size_t>(K);
     const bool preload = !last_launch_writes_overlap(st, w, wbytes);
     const int n = static_cast<int>(N), k = static_cast<int>(K);
-    const cudaError_t e =
-        out_fp16 ? launch_blk<__half>(x, w, w_scale, bias, out, xq, xs, m_pad, n, k, eps, preload, st)
-                 : launch_blk<__nv_bfloat16>(x, w, w_scale, bias, out, xq, xs, m_pad, n, k, eps, preload, st);
+    cudaError_t e;
+    switch (gemv_chunks_per_warp(K)) {
+        case 1:
+            e = out_fp16 ? launch_blk<1, __half>(x, w, w_scale, bias, out, xq, xs, m_pad, n, k, eps, preload, st)
+                         : launch_blk<1, __nv_bfloat16>(x, w, w_scale, bias, out, xq, xs, m_pad, n, k, eps, preload,
+                                                        st);
+            break;
+        case 2:
+            e = out_fp16 ? launch_blk<2, __half>(x, w, w_scale, bias, out, xq, xs, m_pad, n, k, eps, preload, st)
+                         : launch_blk<2, __nv_bfloat16>(x, w, w_scale, bias, out, xq, xs, m_pad, n, k, eps, preload,
+                                                        st);
+            break;
+        default:
+            e = out_fp16 ? launch_blk<3, __half>(x, w, w_scale, bias, out, xq, xs, m_pad, n, k, eps, preload, st)
+                         : launch_blk<3, __nv_bfloat16>(x, w, w_scale, bias, out, xq, xs, m_pad, n, k, eps, preload,
+                                                        st);
+    }
     if (e == cudaSuccess)
         note_launch_writes(st, out, static_cast<size_t>(N) * 2, xq, xq != nullptr ? static_cast<size_t>(K) : 0, xs,
                            xs != nullptr ? static_cast<size_t>(K / 128) * static_cast<size_t>(m_pad) * 4 : 0);

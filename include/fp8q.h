@@ -288,7 +288,7 @@ FP8Q_API size_t fp8q_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t bl
  * codes and scales as after the two launches).  Its sums are accumulated in
  * another order than the tensor-core GEMM's, so its output is within the
  * GEMM tolerance of the two-kernel result rather than bit-identical.
- * fp8q_linear_blockwise with ONE token and K <= 8192 (no override) is one
+ * fp8q_linear_blockwise with ONE token and K <= 12288 (no override) is one
  * launch as well: the group-128 quantization fused into the matrix-vector
  * product (each 16-value partial sum scaled by its group scale times its
  * weight block's scale), xq row 0 and xs[kb * m_pad] written by CTA 0.

@@ -1,7 +1,8 @@
-"""GPU parity of the channelwise linear layer at decode sizes.  One token
-with K <= 4096 runs as ONE launch with the per-token quantization fused into
-a matrix-vector product on the CUDA cores; two to four tokens and longer rows
-take the quantizer and the tensor-core GEMM.  Either way the codes and scales
+"""GPU parity of the linear layers at decode sizes.  One token runs as ONE
+launch with the per-token (channelwise, K <= 4096) or group-128 (blockwise,
+K <= 12288) quantization fused into a matrix-vector product on the CUDA
+cores; two to four tokens and longer rows take the quantizer and the
+tensor-core GEMM.  Either way the codes and scales
 left in the caller's buffers are bit-exact against the oracle's per-token
 quantizer, the output is within the GEMM bar of the oracle's GEMM on those
 codes, and the fused launch leaves the same codes and scales as the
@@ -131,9 +132,9 @@ def test_few_token_linear_same_codes_as_two_kernels(dev, schedule):
 
 
 def test_few_token_linear_full_size_decode_layers(dev):
-    """The decode layers at their own sizes: qkv 6144x4096, down 4096x12288,
-    gate_up 24576x4096 at M = 1 and 4, every output against the oracle
-    (down's rows are longer than the fused launch takes)."""
+    """The decode layers at their own sizes: qkv 6144x4096, down 4096x12288
+    (two kernels), gate_up 24576x4096 at M = 1 and 4, every output against
+    the oracle."""
     for (N, K) in [(6144, 4096), (4096, 12288), (24576, 4096)]:
         wq, ws = weights(dev, N, K, seed=N)
         for M in (1, 4):
@@ -164,10 +165,11 @@ def test_few_token_linear_weights_rewritten_right_before(dev):
         assert_gemm_close(out_values(outs[i]), ref, f"iteration {i}")
 
 
-@pytest.mark.parametrize("M,K", [(1, 4096), (1, 4112), (1, 49152), (2, 32768)])
+@pytest.mark.parametrize("M,K", [(1, 4096), (1, 4112), (1, 12288), (1, 49152), (2, 32768)])
 def test_few_token_linear_wide_rows(dev, M, K):
-    """The longest row the fused launch takes (4096) and longer ones, which
-    take the quantizer and the GEMM."""
+    """The longest row the fused channelwise launch takes (4096) and longer
+    ones, which take the quantizer and the GEMM."""
+    assert fq.fp8q_linear_channelwise_launches(M, K) == (1 if M == 1 and K <= 4096 else 2)
     wq, ws = weights(dev, 136, K, seed=K)
     x = synthetic.activations(M, K, outliers=True, seed=K + M)
     check(dev, x, wq, ws, what=f"{M}x136x{K}")
@@ -213,12 +215,15 @@ def check_blockwise(dev, x, wq, ws, bias=None, out_dtype=torch.bfloat16, what=""
     return out, xq, xs
 
 
-@pytest.mark.parametrize("N,K", [(4096, 7168), (256, 128), (384, 1152), (24576, 3072), (128, 8192), (256, 8320)])
+@pytest.mark.parametrize("N,K", [(4096, 7168), (256, 128), (384, 1152), (24576, 3072), (128, 4224), (3072, 12288),
+                                 (256, 12416)])
 def test_one_token_blockwise_linear_parity(dev, N, K):
-    """The blockwise decode layer, one K block, a K that leaves a warp's
-    512-value span partly past the row (1152 = 2 x 512 + 128), a wide N, the
-    longest row the fused launch takes and one past it (two kernels)."""
-    assert fq.fp8q_linear_blockwise_launches(1, K) == (1 if K <= 8192 else 2)
+    """The blockwise decode layer (two chunks per warp), one K block, a K
+    that leaves a warp's 512-value span partly past the row (1152 = 2 x 512
+    + 128), a wide N, a second chunk for one warp only (4224), the longest
+    row the fused launch takes (three chunks per warp) and one past it (two
+    kernels)."""
+    assert fq.fp8q_linear_blockwise_launches(1, K) == (1 if K <= 12288 else 2)
     w = synthetic.weights(N, K, seed=N + K)
     wq, ws = fq.fp8q_quant_weight_block128(w.to(dev))
     x = synthetic.activations(1, K, outliers=True, seed=K)

@@ -189,10 +189,10 @@ def test_tuner_only_proposes_schedules_the_library_accepts(lib):
 
 
 def test_linear_channelwise_launch_count(lib):
-    """One token with rows up to 4096 values (channelwise) or 8192 values
-    (blockwise): one fused launch; otherwise the quantizer and the GEMM;
-    nothing for empty problems; two again while a schedule override asks for
-    the GEMM."""
+    """One token with rows up to 4096 (channelwise) or 12288 (blockwise)
+    values: one fused launch; otherwise the quantizer and the GEMM; nothing
+    for empty problems; two again while a schedule override asks for the
+    GEMM."""
     assert fq.fp8q_linear_channelwise_launches(1, 4096) == 1
     assert fq.fp8q_linear_channelwise_launches(1, 16) == 1
     assert fq.fp8q_linear_channelwise_launches(1, 4112) == 2
@@ -201,8 +201,8 @@ def test_linear_channelwise_launch_count(lib):
     assert fq.fp8q_linear_channelwise_launches(8192, 4096) == 2
     assert fq.fp8q_linear_channelwise_launches(0, 4096) == 0
     assert fq.fp8q_linear_blockwise_launches(1, 7168) == 1
-    assert fq.fp8q_linear_blockwise_launches(1, 8192) == 1
-    assert fq.fp8q_linear_blockwise_launches(1, 8320) == 2
+    assert fq.fp8q_linear_blockwise_launches(1, 12288) == 1
+    assert fq.fp8q_linear_blockwise_launches(1, 12416) == 2
     assert fq.fp8q_linear_blockwise_launches(2, 7168) == 2
     assert fq.fp8q_linear_blockwise_launches(0, 7168) == 0
     lib.fp8q_set_plan_override(1, 16, 4)
