@@ -111,15 +111,15 @@ cudaError_t launch_w8a16_gemv(const void *x, int64_t ldx, const void *w, int64_t
                               cudaStream_t st);
 // True while a schedule override (fp8q_set_plan_override / FP8Q_PLAN) is set.
 bool plan_override_active();
-// The channelwise W8A8 linear for one token with K <= 4096, and the
-// blockwise one for one token with K <= 12288, run as one launch with the
-// activation quantization fused (linear_gemv.cu), unless a schedule override
-// is set.  Each warp of the matrix-vector CTA owns ceil(K / 4096) 512-byte
-// chunks of a row per group and requests them together.  Measured on GB300
-// these are faster than the quantizer + tensor-core GEMM; with two tokens,
-// and for the channelwise 12288-wide down layer, they were slower.
+// The channelwise and blockwise linears for one token with K <= 12288 run
+// as one launch with the activation quantization fused (linear_gemv.cu),
+// unless a schedule override is set.  Each warp of the matrix-vector CTA
+// owns ceil(K / 4096) 512-byte chunks of a row per group and requests them
+// together.  Measured on GB300 this is faster than the quantizer +
+// tensor-core GEMM at K = 3072, 4096, 7168 and 12288; with two tokens it
+// was slower.
 inline int gemv_chunks_per_warp(int64_t K) { return static_cast<int>((K + 4095) / 4096); }
-inline bool linear_gemv_fits(int64_t M, int64_t K) { return M == 1 && K <= 4096; }
+inline bool linear_gemv_fits(int64_t M, int64_t K) { return M == 1 && K <= 12288; }
 inline bool linear_blk_gemv_fits(int64_t M, int64_t K) { return M == 1 && K <= 12288; }
 cudaError_t launch_linear_blk_gemv(const void *x, const void *w, const float *w_scale, const void *bias, void *out,
                                    void *xq, float *xs, int64_t m_pad, int64_t N, int64_t K, float eps, bool out_fp16,

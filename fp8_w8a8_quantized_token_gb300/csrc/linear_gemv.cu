@@ -60,7 +60,10 @@ using gemv::kWarps;
 // NCW: chunks per warp and group (ceil(K / 4096)); a warp requests all of
 // them at once.  Registers: NCW * ROWS * 4 for the weights, so the CTAs per
 // SM fall from 3 to 2 to 1 as NCW grows.
-constexpr int min_ctas(int ncw) { return ncw == 1 ? 3 : ncw == 2 ? 2 : 1; }
+// Output channels per CTA: 8, or 4 with three chunks per warp (12 uint4
+// registers per row), which keeps two CTAs per SM there.
+constexpr int gemv_rows_for(int ncw) { return ncw >= 3 ? 4 : 8; }
+constexpr int min_ctas(int ncw) { return ncw == 1 ? 3 : 2; }
 
 // All NCW chunks of a group for this warp (zeros past K).
 template <int NCW, int ROWS>
@@ -71,7 +74,7 @@ __device__ __forceinline__ void load_group(const uint8_t *__restrict__ w, int64_
     for (int i = 0; i < NCW; ++i) gemv::load_weights<ROWS>(w, ldw, n0, N, K, warp + i * kWarps, lane, wv[i]);
 }
 
-template <int MT, int NCW, typename OutT, int ROWS = gemv::rows<MT>()>
+template <int MT, int NCW, typename OutT, int ROWS = gemv_rows_for(NCW)>
 __global__ void __launch_bounds__(32 * kWarps, min_ctas(NCW)) linear_pt_gemv_kernel(
     const __nv_bfloat16 *__restrict__ x, const uint8_t *__restrict__ w, int64_t ldw,
     const float *__restrict__ w_scale, const __nv_bfloat16 *__restrict__ bias, OutT *__restrict__ out,
@@ -188,13 +191,12 @@ __global__ void __launch_bounds__(32 * kWarps, min_ctas(NCW)) linear_pt_gemv_ker
     }
 }
 
-template <int NCW, typename OutT>
+template <int NCW, typename OutT, int ROWS = gemv_rows_for(NCW)>
 __global__ void __launch_bounds__(32 * kWarps, min_ctas(NCW)) linear_blk_gemv_kernel(
     const __nv_bfloat16 *__restrict__ x, const uint8_t *__restrict__ w, const float *__restrict__ w_scale,
     const __nv_bfloat16 *__restrict__ bias, OutT *__restrict__ out, uint8_t *__restrict__ xq,
     float *__restrict__ xs, int64_t m_pad, int N, int K, float eps, int preload)
 {
-    constexpr int ROWS = 8;
     extern __shared__ __align__(16) uint8_t blk_dyn[];   // bf16 [K] decoded codes, then fp32 [K/128] scales
     __shared__ float red[2][kWarps][ROWS][1];
     __nv_bfloat16 *xdec = reinterpret_cast<__nv_bfloat16 *>(blk_dyn);
@@ -308,7 +310,8 @@ cudaError_t launch_blk(const void *x, const void *w, const float *w_scale, const
     const size_t smem = static_cast<size_t>(K) * 2u + static_cast<size_t>(K / 128) * 4u;
     if (smem > 48u * 1024u) return cudaErrorInvalidValue;
     int grid = 0;
-    cudaError_t e = persistent_grid(kernel, smem, (N + 7) / 8, &grid);
+    constexpr int kRows = gemv_rows_for(NCW);
+    cudaError_t e = persistent_grid(kernel, smem, (N + kRows - 1) / kRows, &grid);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -334,7 +337,7 @@ cudaError_t launch_t(const void *x, const void *w, int64_t ldw, const float *w_s
     if (smem > 48u * 1024u) return cudaErrorInvalidValue;
     // Every CTA that fits (fewer CTAs with whole rounds of groups each
     // measured slower: the rounds are latency-bound).
-    constexpr int kRows = gemv::rows<MT>();
+    constexpr int kRows = gemv_rows_for(NCW);
     int grid = 0;
     cudaError_t e = persistent_grid(kernel, smem, (N + kRows - 1) / kRows, &grid);
     if (e != cudaSuccess) return e;
@@ -364,10 +367,23 @@ cudaError_t launch_linear_pt_gemv(const void *x, const void *w, int64_t ldw, con
     const size_t wbytes = static_cast<size_t>(N - 1) * static_cast<size_t>(ldw) + static_cast<size_t>(K);
     const bool preload = !last_launch_writes_overlap(st, w, wbytes);
     const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
-    // One chunk per warp (K <= 4096): the rows this form is used for.
-    const cudaError_t e =
-        out_fp16 ? launch_t<1, 1, __half>(x, w, ldw, w_scale, bias, out, xq, xs, m, n, k, eps, preload, st)
-                 : launch_t<1, 1, __nv_bfloat16>(x, w, ldw, w_scale, bias, out, xq, xs, m, n, k, eps, preload, st);
+    cudaError_t e;
+    switch (gemv_chunks_per_warp(K)) {
+        case 1:
+            e = out_fp16 ? launch_t<1, 1, __half>(x, w, ldw, w_scale, bias, out, xq, xs, m, n, k, eps, preload, st)
+                         : launch_t<1, 1, __nv_bfloat16>(x, w, ldw, w_scale, bias, out, xq, xs, m, n, k, eps,
+                                                         preload, st);
+            break;
+        case 2:
+            e = out_fp16 ? launch_t<1, 2, __half>(x, w, ldw, w_scale, bias, out, xq, xs, m, n, k, eps, preload, st)
+                         : launch_t<1, 2, __nv_bfloat16>(x, w, ldw, w_scale, bias, out, xq, xs, m, n, k, eps,
+                                                         preload, st);
+            break;
+        default:
+            e = out_fp16 ? launch_t<1, 3, __half>(x, w, ldw, w_scale, bias, out, xq, xs, m, n, k, eps, preload, st)
+                         : launch_t<1, 3, __nv_bfloat16>(x, w, ldw, w_scale, bias, out, xq, xs, m, n, k, eps,
+                                                         preload, st);
+    }
     if (e == cudaSuccess)
         note_launch_writes(st, out, static_cast<size_t>(M) * N * 2, xq, static_cast<size_t>(M) * K, xs,
                            static_cast<size_t>(M) * 4);

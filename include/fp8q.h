@@ -281,7 +281,7 @@ FP8Q_API size_t fp8q_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t bl
 /* ---------------------------------------------------------------------------
  * Linear-layer compositions (no padding copies): quantize x into the
  * caller's buffers, then run the GEMM on them -- two launches, except:
- * fp8q_linear_channelwise with ONE token and K <= 4096 (and no schedule
+ * fp8q_linear_channelwise with ONE token and K <= 12288 (and no schedule
  * override set) runs as one launch, the per-token quantization fused into a
  * matrix-vector product on the CUDA cores (every CTA quantizes the row into
  * its shared memory; CTA 0 also writes xq and xs, so they hold the same

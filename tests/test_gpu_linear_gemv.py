@@ -1,6 +1,6 @@
-"""GPU parity of the linear layers at decode sizes.  One token runs as ONE
-launch with the per-token (channelwise, K <= 4096) or group-128 (blockwise,
-K <= 12288) quantization fused into a matrix-vector product on the CUDA
+"""GPU parity of the linear layers at decode sizes.  One token with K <=
+12288 runs as ONE launch with the per-token (channelwise) or group-128
+(blockwise) quantization fused into a matrix-vector product on the CUDA
 cores; two to four tokens and longer rows take the quantizer and the
 tensor-core GEMM.  Either way the codes and scales
 left in the caller's buffers are bit-exact against the oracle's per-token
@@ -84,8 +84,8 @@ def check(dev, x, wq, ws, bias=None, out_dtype=torch.bfloat16, what=""):
 @pytest.mark.parametrize("N,K", [(392, 1040), (8, 16), (4096, 4096), (264, 12288), (136, 4112)])
 def test_few_token_linear_parity(dev, M, N, K):
     """K not a multiple of the 512-byte chunk, a single 16-element piece, N
-    not a multiple of the CTA's rows; rows past 4096 and M > 1 on the
-    two-kernel path."""
+    not a multiple of the CTA's rows, one to three chunks per warp; M > 1 on
+    the two-kernel path."""
     wq, ws = weights(dev, N, K, seed=N + K)
     x = synthetic.activations(M, K, outliers=True, seed=M + K)
     check(dev, x, wq, ws, what=f"{M}x{N}x{K}")
@@ -133,8 +133,8 @@ def test_few_token_linear_same_codes_as_two_kernels(dev, schedule):
 
 def test_few_token_linear_full_size_decode_layers(dev):
     """The decode layers at their own sizes: qkv 6144x4096, down 4096x12288
-    (two kernels), gate_up 24576x4096 at M = 1 and 4, every output against
-    the oracle."""
+    (three chunks per warp at M = 1), gate_up 24576x4096 at M = 1 and 4,
+    every output against the oracle."""
     for (N, K) in [(6144, 4096), (4096, 12288), (24576, 4096)]:
         wq, ws = weights(dev, N, K, seed=N)
         for M in (1, 4):
@@ -165,11 +165,13 @@ def test_few_token_linear_weights_rewritten_right_before(dev):
         assert_gemm_close(out_values(outs[i]), ref, f"iteration {i}")
 
 
-@pytest.mark.parametrize("M,K", [(1, 4096), (1, 4112), (1, 12288), (1, 49152), (2, 32768)])
+@pytest.mark.parametrize("M,K", [(1, 4112), (1, 8208), (1, 12288), (1, 12304), (1, 49152), (2, 32768)])
 def test_few_token_linear_wide_rows(dev, M, K):
-    """The longest row the fused channelwise launch takes (4096) and longer
-    ones, which take the quantizer and the GEMM."""
-    assert fq.fp8q_linear_channelwise_launches(M, K) == (1 if M == 1 and K <= 4096 else 2)
+    """Rows of two and three chunks per warp (the last chunk present for one
+    warp only: 4112, 8208), the longest row the fused channelwise launch
+    takes (12288, four channels per CTA) and longer ones, which take the
+    quantizer and the GEMM."""
+    assert fq.fp8q_linear_channelwise_launches(M, K) == (1 if M == 1 and K <= 12288 else 2)
     wq, ws = weights(dev, 136, K, seed=K)
     x = synthetic.activations(M, K, outliers=True, seed=K + M)
     check(dev, x, wq, ws, what=f"{M}x136x{K}")

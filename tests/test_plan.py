@@ -189,14 +189,14 @@ def test_tuner_only_proposes_schedules_the_library_accepts(lib):
 
 
 def test_linear_channelwise_launch_count(lib):
-    """One token with rows up to 4096 (channelwise) or 12288 (blockwise)
-    values: one fused launch; otherwise the quantizer and the GEMM; nothing
-    for empty problems; two again while a schedule override asks for the
-    GEMM."""
+    """One token with rows up to 12288 values: one fused launch; otherwise
+    the quantizer and the GEMM; nothing for empty problems; two again while a
+    schedule override asks for the GEMM."""
     assert fq.fp8q_linear_channelwise_launches(1, 4096) == 1
     assert fq.fp8q_linear_channelwise_launches(1, 16) == 1
-    assert fq.fp8q_linear_channelwise_launches(1, 4112) == 2
-    assert fq.fp8q_linear_channelwise_launches(1, 12288) == 2
+    assert fq.fp8q_linear_channelwise_launches(1, 4112) == 1
+    assert fq.fp8q_linear_channelwise_launches(1, 12288) == 1
+    assert fq.fp8q_linear_channelwise_launches(1, 12304) == 2
     assert fq.fp8q_linear_channelwise_launches(2, 4096) == 2
     assert fq.fp8q_linear_channelwise_launches(8192, 4096) == 2
     assert fq.fp8q_linear_channelwise_launches(0, 4096) == 0
