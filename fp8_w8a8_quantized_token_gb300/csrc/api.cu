@@ -87,9 +87,12 @@ fp8q_status fp8q_quant_per_token(const void *x, int64_t M, int64_t K, int64_t ld
     if (s != FP8Q_OK || M == 0) return s;
     unsigned *status = device_status_ptr();
     if (status == nullptr) return FP8Q_ERR_CUDA;
-    const cudaError_t e = launch_quant_per_token(x, M, K, ldx, xq, x_scale, eps, status, as_stream(stream));
+    bool early_trigger = false;
+    const cudaError_t e =
+        launch_quant_per_token(x, M, K, ldx, xq, x_scale, eps, status, as_stream(stream), &early_trigger);
     if (e == cudaSuccess)
-        note_launch_writes(as_stream(stream), xq, static_cast<size_t>(M) * K, x_scale, static_cast<size_t>(M) * 4);
+        note_launch_writes(as_stream(stream), xq, static_cast<size_t>(M) * K, x_scale, static_cast<size_t>(M) * 4,
+                           nullptr, 0, early_trigger);
     return from_cuda(e);
 }
 
@@ -106,11 +109,12 @@ fp8q_status fp8q_quant_per_token_group_row_padded(const void *x, int64_t M, int6
     if (K > 0 && K % group_size != 0) return FP8Q_ERR_INVALID_ARG;
     const fp8q_status s = check_quant_common(x, M, K, ldx, xq, x_scale, eps);
     if (s != FP8Q_OK || M == 0) return s;
+    bool early_trigger = false;
     const cudaError_t e = launch_quant_group(x, M, K, ldx, group_size, xq, x_scale, m_pad, eps, current_device_sms(),
-                                             as_stream(stream));
+                                             as_stream(stream), false, false, &early_trigger);
     if (e == cudaSuccess)
         note_launch_writes(as_stream(stream), xq, static_cast<size_t>(M) * K, x_scale,
-                           static_cast<size_t>(K / group_size) * m_pad * 4);
+                           static_cast<size_t>(K / group_size) * m_pad * 4, nullptr, 0, early_trigger);
     return from_cuda(e);
 }
 
@@ -132,11 +136,13 @@ fp8q_status fp8q_quant_per_token_group_row_padded_ex(const void *x, int64_t M, i
     if (silu && (K > kMaxDim / 2 || ldx < 2 * K)) return FP8Q_ERR_INVALID_ARG;
     const fp8q_status s = check_quant_common(x, M, K, ldx, xq, x_scale, eps);
     if (s != FP8Q_OK || M == 0) return s;
+    bool early_trigger = false;
     const cudaError_t e = launch_quant_group(x, M, K, ldx, group_size, xq, x_scale, m_pad, eps, current_device_sms(),
-                                             as_stream(stream), (flags & FP8Q_QUANT_SCALE_UE8M0) != 0, silu);
+                                             as_stream(stream), (flags & FP8Q_QUANT_SCALE_UE8M0) != 0, silu,
+                                             &early_trigger);
     if (e == cudaSuccess)
         note_launch_writes(as_stream(stream), xq, static_cast<size_t>(M) * K, x_scale,
-                           static_cast<size_t>(K / group_size) * m_pad * 4);
+                           static_cast<size_t>(K / group_size) * m_pad * 4, nullptr, 0, early_trigger);
     return from_cuda(e);
 }
 

@@ -722,10 +722,10 @@ __global__ void __launch_bounds__(GemmCfg<SWAP, BN, STAGES, BLOCKWISE, TWO_SM, F
     // Weight slices of the first tile issued before the dependency wait.
     int npre = 0;
     if (warp == 0 && lane == 0) {
-        // Every kernel of the library triggers its dependents only after
-        // its own dependency wait, so the only kernel that may still run
-        // now is the immediate predecessor; the host clears p.preload when
-        // that kernel writes the weights.  Otherwise the first tile's weight
+        // The kernels that may still run now are the immediate
+        // predecessor and, when that is a quantizer that let this kernel
+        // launch before its own dependency wait, the one before it; the
+        // host clears p.preload when any of them writes the weights.  Otherwise the first tile's weight
         // slices stream into the ring right away and the activation slices
         // follow after pdl_wait().  Further weight slices of the first tile
         // are prefetched into L2 (always safe: L2 is the coherence point).

@@ -133,11 +133,17 @@ bool workspace_exchange_enabled()
 }
 
 namespace {
-// The device ranges the last library launch on a stream writes (up to three).
+// The device ranges the launches on a stream that may still be running when
+// the next library kernel starts may write: the last launch's, plus, when
+// that launch lets its successor start before its own dependency wait, the
+// ranges recorded before it (up to kMaxRanges; more are recorded as
+// "unknown", which every overlap test answers with yes).
+constexpr int kMaxRanges = 6;
 struct LaunchRecord {
     cudaStream_t stream;
-    bool used;
-    uintptr_t lo[3], hi[3];
+    bool used, unknown;
+    int n;
+    uintptr_t lo[kMaxRanges], hi[kMaxRanges];
 };
 std::mutex g_launch_mu;
 LaunchRecord g_launches[64];
@@ -145,21 +151,46 @@ int g_launch_next = 0;
 }  // namespace
 
 void note_launch_writes(cudaStream_t st, const void *base, size_t bytes, const void *base2, size_t bytes2,
-                        const void *base3, size_t bytes3)
+                        const void *base3, size_t bytes3, bool keep_previous)
 {
     std::lock_guard<std::mutex> g(g_launch_mu);
-    LaunchRecord rec = {st, true, {}, {}};
+    LaunchRecord rec = {};
+    rec.stream = st;
+    rec.used = true;
     const void *bases[3] = {base, base2, base3};
     const size_t sizes[3] = {bytes, bytes2, bytes3};
-    for (int i = 0; i < 3; ++i) {
-        rec.lo[i] = reinterpret_cast<uintptr_t>(bases[i]);
-        rec.hi[i] = bases[i] != nullptr ? rec.lo[i] + sizes[i] : 0;
-    }
+    for (int i = 0; i < 3; ++i)
+        if (bases[i] != nullptr && sizes[i] != 0) {
+            rec.lo[rec.n] = reinterpret_cast<uintptr_t>(bases[i]);
+            rec.hi[rec.n] = rec.lo[rec.n] + sizes[i];
+            ++rec.n;
+        }
+    LaunchRecord *slot = nullptr;
     for (auto &r : g_launches)
         if (r.used && r.stream == st) {
-            r = rec;
-            return;
+            slot = &r;
+            break;
         }
+    if (keep_previous) {
+        if (slot == nullptr) {
+            rec.unknown = true;   // nothing known about what may still run
+        } else {
+            rec.unknown = slot->unknown;
+            for (int i = 0; i < slot->n && !rec.unknown; ++i) {
+                if (rec.n == kMaxRanges) {
+                    rec.unknown = true;
+                    break;
+                }
+                rec.lo[rec.n] = slot->lo[i];
+                rec.hi[rec.n] = slot->hi[i];
+                ++rec.n;
+            }
+        }
+    }
+    if (slot != nullptr) {
+        *slot = rec;
+        return;
+    }
     g_launches[g_launch_next] = rec;
     g_launch_next = (g_launch_next + 1) % 64;
 }
@@ -170,7 +201,8 @@ bool last_launch_writes_overlap(cudaStream_t st, const void *base, size_t bytes)
     const uintptr_t lo = reinterpret_cast<uintptr_t>(base), hi = lo + bytes;
     for (const auto &r : g_launches)
         if (r.used && r.stream == st) {
-            for (int i = 0; i < 3; ++i)
+            if (r.unknown) return true;
+            for (int i = 0; i < r.n; ++i)
                 if (r.lo[i] < hi && lo < r.hi[i]) return true;
             return false;
         }

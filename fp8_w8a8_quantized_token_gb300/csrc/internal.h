@@ -13,11 +13,14 @@ namespace fp8q {
 // ---- quantizers (quant.cu) ------------------------------------------------
 // `status`: the device status word, where the many-row kernel's bounded
 // wait records a timeout.
+// `early_trigger` (may be null) is set when the kernel lets its successor
+// start before its own dependency wait (the record must then keep the
+// previous launch's ranges).
 cudaError_t launch_quant_per_token(const void *x, int64_t M, int64_t K, int64_t ldx, void *xq, float *xs, float eps,
-                                   unsigned *status, cudaStream_t st);
+                                   unsigned *status, cudaStream_t st, bool *early_trigger = nullptr);
 cudaError_t launch_quant_group(const void *x, int64_t M, int64_t K, int64_t ldx, int group, void *xq, float *xs,
                                int64_t m_pad, float eps, int num_sms, cudaStream_t st, bool ue8m0 = false,
-                               bool silu_and_mul = false);
+                               bool silu_and_mul = false, bool *early_trigger = nullptr);
 cudaError_t launch_quant_static(const void *x, int64_t M, int64_t K, int64_t ldx, const float *scale, void *xq,
                                 float *xs_rep, int num_sms, cudaStream_t st);
 cudaError_t launch_quant_weight_block128(const void *w, int64_t N, int64_t K, void *wq, float *ws, float eps,
@@ -189,13 +192,19 @@ bool make_tmap_3d_kblocks(CUtensorMap *map, const void *base, uint64_t K, uint64
 // default the library asks for no workspace and ignores one passed to it.
 bool workspace_exchange_enabled();
 
-// Per-stream record of the byte ranges (up to three) the library's most
-// recent launch on that stream writes.  With programmatic dependent launch, that launch is the
-// only kernel that may still be running when the next one starts (every
-// kernel triggers its dependents only after its own dependency wait), so a
-// GEMM may read its weights early unless they overlap these ranges.
+// Per-stream record of the byte ranges that the library kernels which may
+// still be running when the next one starts write.  With programmatic
+// dependent launch a kernel triggers its dependents after its own
+// dependency wait, so normally only the most recent launch can still be
+// running, and its ranges (up to three) are recorded.  A quantizer whose
+// input no earlier kernel on the stream is writing triggers at its start
+// instead (keep_previous): the launch before it may then still run as well,
+// and its ranges are kept in the record too.  A kernel reads before its own
+// dependency wait (a GEMM its weights, a quantizer its input) only what
+// overlaps none of the recorded ranges.
 void note_launch_writes(cudaStream_t st, const void *base, size_t bytes, const void *base2 = nullptr,
-                        size_t bytes2 = 0, const void *base3 = nullptr, size_t bytes3 = 0);
+                        size_t bytes2 = 0, const void *base3 = nullptr, size_t bytes3 = 0,
+                        bool keep_previous = false);
 bool last_launch_writes_overlap(cudaStream_t st, const void *base, size_t bytes);
 int current_device_sms();        // SM count of the current device (cached)
 

@@ -27,9 +27,9 @@
 // them.  The sum is scaled as the GEMM's epilogue does:
 // fmaf(sum * s[m], w_scale[n], bias[n]), rounded once.
 //
-// Unless the previous launch of the library wrote the weights, each warp
-// issues its first chunk's weight loads before the dependency wait; after
-// each row group it issues the next group's first chunk before the
+// Unless a library kernel that may still be running writes the weights,
+// each warp issues its first group's weight loads before the dependency
+// wait; after each row group it issues the next group's loads before the
 // cross-warp reduction.
 //
 // The blockwise linear for one token (linear_blk_gemv_kernel) is the same
@@ -38,8 +38,8 @@
 // quantized in groups of 128 (the 8 lanes of a group reduce its amax; the
 // group quantizer's codes and scales bit for bit, CTA 0 storing them in the
 // row-padded layout), and each lane's 16 exact products are summed and then
-// scaled by the group scale times the weight block's scale (the CTA's 8
-// output channels lie in one 128-row block) before they are accumulated;
+// scaled by the group scale times the weight block's scale (the CTA's 8 or
+// 4 output channels lie in one 128-row block) before they are accumulated;
 // out = round(sum + bias[n]).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>

@@ -57,10 +57,12 @@ __device__ __forceinline__ uint32_t quant4_f32(const float *y, float s, float r)
     return cvt_e4m3x2(a.x, a.y) | (cvt_e4m3x2(b.x, b.y) << 16);
 }
 
-// Programmatic dependent launch: each quantizer first waits for the
-// previous kernel in the stream (so every earlier kernel has completed), then
-// lets the next kernel launch.  When any kernel of this library starts, at
-// most its immediate predecessor can still be running.
+// Programmatic dependent launch: a quantizer first waits for the previous
+// kernel in the stream (so every earlier kernel has completed), then lets the
+// next kernel launch -- unless its input is written by no kernel that may
+// still be running, in which case it lets the next kernel launch at once and
+// waits only before its stores (the host then records the previous launch's
+// written ranges with its own, so the next kernel's early reads avoid both).
 __device__ __forceinline__ void pdl_enter()
 {
     pdl_wait();
@@ -74,17 +76,21 @@ __device__ __forceinline__ void pdl_enter()
 // two-pass kernel below.
 // ---------------------------------------------------------------------------
 //
-// With `early` set (the host found that the previous launch of the library
-// on this stream does not write x), the row is loaded, reduced and quantized
-// in registers before the dependency wait, so all of it overlaps the tail of
-// the previous kernel; only the stores of the codes and the scale wait.
+// With `early` set (the host found that no library kernel that may still be
+// running on this stream writes x), the kernel lets its successor launch at
+// once and loads, reduces and quantizes the row in registers before its
+// dependency wait, so all of it overlaps the tail of the previous kernel;
+// only the stores of the codes and the scale wait.
 template <int VPT>
 __global__ void __launch_bounds__(1024) quant_per_token_kernel(const __nv_bfloat16 *__restrict__ x, int64_t ldx,
                                                                uint8_t *__restrict__ xq, float *__restrict__ xs,
                                                                int K, float eps, int early)
 {
     __shared__ float warp_max[32];
-    if (!early) pdl_enter();
+    if (early)
+        pdl_trigger();
+    else
+        pdl_enter();
     const int64_t row = blockIdx.x;
     const int chunks = K >> 4;
     const __nv_bfloat16 *xr = x + row * ldx;
@@ -115,7 +121,7 @@ __global__ void __launch_bounds__(1024) quant_per_token_kernel(const __nv_bfloat
         const int ci = threadIdx.x + v * blockDim.x;
         if (ci < chunks) c[v].lo = quant_chunk(c[v], s);
     }
-    if (early) pdl_enter();
+    if (early) pdl_wait();
     if (threadIdx.x == 0) xs[row] = s;
     uint8_t *qr = xq + row * static_cast<int64_t>(K);
 #pragma unroll
@@ -171,11 +177,15 @@ __global__ void __launch_bounds__(256) quant_group_kernel(const __nv_bfloat16 *_
                                                           uint8_t *__restrict__ xq, float *__restrict__ xs,
                                                           int64_t M, int K, int64_t m_pad, float eps, int early)
 {
-    // With `early` (the previous launch of the library on this stream does
-    // not write x), each thread's first chunk is loaded and quantized before
-    // the dependency wait, which then comes right before its first store.
+    // With `early` (no library kernel that may still be running on this
+    // stream writes x), the kernel lets its successor launch at once, and
+    // each thread's first chunk is loaded and quantized before the
+    // dependency wait, which then comes right before its first store.
     bool waited = !early;
-    if (!early) pdl_enter();
+    if (early)
+        pdl_trigger();
+    else
+        pdl_enter();
     const int chunks_per_row = K >> 4;
     const int64_t total = M * chunks_per_row;
     // (row, chunk) of chunk index t, advanced by the grid stride without a
@@ -237,14 +247,14 @@ __global__ void __launch_bounds__(256) quant_group_kernel(const __nv_bfloat16 *_
                 q = quant_chunk(c, s);
             }
             if (!waited) {
-                pdl_enter();
+                pdl_wait();
                 waited = true;
             }
             *reinterpret_cast<uint4 *>(xq + row * static_cast<int64_t>(K) + (ci << 4)) = q;
             if ((ci & (TPG - 1)) == 0) xs[static_cast<int64_t>(ci / TPG) * m_pad + row] = s;
         }
     }
-    if (!waited) pdl_enter();   // threads without a chunk
+    if (!waited) pdl_wait();   // threads without a chunk
 }
 
 // ---------------------------------------------------------------------------
@@ -434,8 +444,9 @@ constexpr int64_t kManyRows = 1024;
 constexpr int64_t kBulkRows = 4096;
 
 cudaError_t launch_quant_per_token(const void *x, int64_t M, int64_t K, int64_t ldx, void *xq, float *xs, float eps,
-                                   unsigned *status, cudaStream_t st)
+                                   unsigned *status, cudaStream_t st, bool *early_trigger)
 {
+    if (early_trigger != nullptr) *early_trigger = false;
     if (M >= kBulkRows && K <= kBulkMaxK) return launch_per_token_bulk(x, M, K, ldx, xq, xs, eps, status, st);
     const int chunks = static_cast<int>(K >> 4);
     // Decode-size M (latency-bound, one CTA per row): one 16-element chunk
@@ -447,10 +458,11 @@ cudaError_t launch_quant_per_token(const void *x, int64_t M, int64_t K, int64_t 
     int threads = (chunks + 32 * per_thread - 1) / (32 * per_thread) * 32;
     if (threads > 1024) threads = 1024;
     const int vpt = (chunks + threads - 1) / threads;
-    // The rows may be read before the dependency wait unless the previous
-    // launch of the library on this stream writes them.
+    // The rows may be read before the dependency wait unless a library
+    // kernel that may still be running on this stream writes them.
     const size_t xbytes = (static_cast<size_t>(M - 1) * static_cast<size_t>(ldx) + static_cast<size_t>(K)) * 2u;
     const bool early = !last_launch_writes_overlap(st, x, xbytes);
+    if (early_trigger != nullptr) *early_trigger = early && vpt <= 4;
     switch (vpt) {
         case 1: return launch_per_token<1>(x, M, static_cast<int>(K), ldx, xq, xs, eps, threads, early, st);
         case 2: return launch_per_token<2>(x, M, static_cast<int>(K), ldx, xq, xs, eps, threads, early, st);
@@ -477,17 +489,19 @@ dim3 stream_grid(int64_t M, int64_t K, int num_sms)
 
 template <bool UE8M0, bool SILU>
 cudaError_t launch_group(const void *x, int64_t M, int64_t K, int64_t ldx, int group, void *xq, float *xs,
-                         int64_t m_pad, float eps, int num_sms, cudaStream_t st)
+                         int64_t m_pad, float eps, int num_sms, cudaStream_t st, bool *early_trigger)
 {
     const auto *xb = static_cast<const __nv_bfloat16 *>(x);
     auto *q = static_cast<uint8_t *>(xq);
     const dim3 g = stream_grid(M, K, num_sms), b(256);
     const int k = static_cast<int>(K);
     // The rows (2K values each with the silu input) may be read before the
-    // dependency wait unless the previous launch of the library writes them.
+    // dependency wait unless a library kernel that may still be running
+    // writes them.
     const size_t xbytes =
         (static_cast<size_t>(M - 1) * static_cast<size_t>(ldx) + static_cast<size_t>(SILU ? 2 * K : K)) * 2u;
     const int e = last_launch_writes_overlap(st, x, xbytes) ? 0 : 1;
+    if (early_trigger != nullptr) *early_trigger = e != 0;
     switch (group) {
         case 16: return launch_pdl(quant_group_kernel<1, UE8M0, SILU>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps, e);
         case 32: return launch_pdl(quant_group_kernel<2, UE8M0, SILU>, g, b, st, xb, ldx, q, xs, M, k, m_pad, eps, e);
@@ -499,13 +513,19 @@ cudaError_t launch_group(const void *x, int64_t M, int64_t K, int64_t ldx, int g
 }  // namespace
 
 cudaError_t launch_quant_group(const void *x, int64_t M, int64_t K, int64_t ldx, int group, void *xq, float *xs,
-                               int64_t m_pad, float eps, int num_sms, cudaStream_t st, bool ue8m0, bool silu_and_mul)
+                               int64_t m_pad, float eps, int num_sms, cudaStream_t st, bool ue8m0, bool silu_and_mul,
+                               bool *early_trigger)
 {
+    bool et = false;
+    cudaError_t e;
     if (silu_and_mul)
-        return ue8m0 ? launch_group<true, true>(x, M, K, ldx, group, xq, xs, m_pad, eps, num_sms, st)
-                     : launch_group<false, true>(x, M, K, ldx, group, xq, xs, m_pad, eps, num_sms, st);
-    return ue8m0 ? launch_group<true, false>(x, M, K, ldx, group, xq, xs, m_pad, eps, num_sms, st)
-                 : launch_group<false, false>(x, M, K, ldx, group, xq, xs, m_pad, eps, num_sms, st);
+        e = ue8m0 ? launch_group<true, true>(x, M, K, ldx, group, xq, xs, m_pad, eps, num_sms, st, &et)
+                  : launch_group<false, true>(x, M, K, ldx, group, xq, xs, m_pad, eps, num_sms, st, &et);
+    else
+        e = ue8m0 ? launch_group<true, false>(x, M, K, ldx, group, xq, xs, m_pad, eps, num_sms, st, &et)
+                  : launch_group<false, false>(x, M, K, ldx, group, xq, xs, m_pad, eps, num_sms, st, &et);
+    if (early_trigger != nullptr) *early_trigger = et;
+    return e;
 }
 
 cudaError_t launch_quant_static(const void *x, int64_t M, int64_t K, int64_t ldx, const float *scale, void *xq,

@@ -13,10 +13,9 @@
 //
 // The CTA shape is that of gemv_common.cuh.  Sums are reduced across lanes
 // with shuffles and across warps in shared memory, then scaled, biased and
-// rounded once.  Unless the previous
-// launch of the library wrote the weights, each warp issues its first
-// chunk's weight loads before the dependency wait, so the weight stream
-// overlaps the previous kernel's tail.
+// rounded once.  Unless a library kernel that may still be running writes
+// the weights, each warp issues its first chunk's weight loads before the
+// dependency wait, so the weight stream overlaps the previous kernel's tail.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
