@@ -796,7 +796,7 @@ def main():
     # Library kernels one pass launches: each linear entry point says how
     # many it takes for its (M, K).
     launches_per_pass = sum(int(L.fp8q_linear_blockwise_launches(p["M"], p["K"]) if p["bw"]
-                                else L.fp8q_linear_channelwise_launches(p["M"], p["K"])) for p in problems)
+                                else L.fp8q_linear_channelwise_launches(p["M"], p["N"], p["K"])) for p in problems)
     line = None
     if rank == 0:
         cpu = None
@@ -1016,7 +1016,8 @@ def measure_linear_one_token(gpu, peaks, synthetic):
                     if rc != 0:
                         raise RuntimeError("linear failed")
 
-            launches = int(L.fp8q_linear_blockwise_launches(M, K) if bw else L.fp8q_linear_channelwise_launches(M, K))
+            launches = int(L.fp8q_linear_blockwise_launches(M, K) if bw
+                           else L.fp8q_linear_channelwise_launches(M, N, K))
             planned = gpu.time_graph(body, REPS)
             plan = fq.fp8q_gemm_plan(M, N, K, bw)
             fq.fp8q_set_plan_override(plan["swap_ab"], plan["mma_n"], 0 if plan["stream_k"] else plan["split_k"])

@@ -116,7 +116,7 @@ def load_library(path: str | None = None):
     L.fp8q_version.restype = ctypes.c_int32
     L.fp8q_workspace_bytes.argtypes = [I64, I64, I64, I32]
     L.fp8q_workspace_bytes.restype = SZ
-    L.fp8q_linear_channelwise_launches.argtypes = [I64, I64]
+    L.fp8q_linear_channelwise_launches.argtypes = [I64, I64, I64]
     L.fp8q_linear_channelwise_launches.restype = ctypes.c_int32
     L.fp8q_linear_blockwise_launches.argtypes = [I64, I64]
     L.fp8q_linear_blockwise_launches.restype = ctypes.c_int32
@@ -535,10 +535,11 @@ def fp8q_workspace_bytes(M: int, N: int, K: int, blockwise: bool = False, device
         return int(load_library().fp8q_workspace_bytes(M, N, K, int(bool(blockwise))))
 
 
-def fp8q_linear_channelwise_launches(M: int, K: int) -> int:
+def fp8q_linear_channelwise_launches(M: int, N: int, K: int) -> int:
     """Kernel launches fp8q_linear_channelwise makes for M tokens of K values
-    (1: the fused one-token form; 2: quantizer + GEMM; 0: nothing to do)."""
-    return int(load_library().fp8q_linear_channelwise_launches(M, K))
+    against N output channels (1: the fused one-token form; 2: quantizer +
+    GEMM; 0: nothing to do)."""
+    return int(load_library().fp8q_linear_channelwise_launches(M, N, K))
 
 
 def fp8q_linear_blockwise_launches(M: int, K: int) -> int:

@@ -256,7 +256,7 @@ fp8q_status fp8q_linear_channelwise(const void *x, const void *b, int64_t ldb, c
     if (bias != nullptr && (reinterpret_cast<uintptr_t>(bias) & 1u)) return FP8Q_ERR_INVALID_ARG;
     // A few tokens: one launch, the quantization fused into matrix-vector
     // products (unless a schedule override asks for the GEMM).
-    if (linear_gemv_fits(M, K) && !plan_override_active()) {
+    if (linear_gemv_fits(M, N, K) && !plan_override_active()) {
         return from_cuda(launch_linear_pt_gemv(x, b, ldb, b_scale, bias, out, xq, xs, M, N, K, 1e-10f,
                                                out_dtype == FP8Q_OUT_FP16, as_stream(stream)));
     }
@@ -266,10 +266,10 @@ fp8q_status fp8q_linear_channelwise(const void *x, const void *b, int64_t ldb, c
                                       workspace_bytes, stream);
 }
 
-int32_t fp8q_linear_channelwise_launches(int64_t M, int64_t K)
+int32_t fp8q_linear_channelwise_launches(int64_t M, int64_t N, int64_t K)
 {
-    if (M <= 0 || K <= 0) return 0;
-    return linear_gemv_fits(M, K) && !plan_override_active() ? 1 : 2;
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    return linear_gemv_fits(M, N, K) && !plan_override_active() ? 1 : 2;
 }
 
 int32_t fp8q_linear_blockwise_launches(int64_t M, int64_t K)

@@ -119,10 +119,16 @@ bool plan_override_active();
 // unless a schedule override is set.  Each warp of the matrix-vector CTA
 // owns ceil(K / 4096) 512-byte chunks of a row per group and requests them
 // together.  Measured on GB300 this is faster than the quantizer +
-// tensor-core GEMM at K = 3072, 4096, 7168 and 12288; with two tokens it
-// was slower.
+// tensor-core GEMM at K = 3072, 4096, 7168 and 12288 (channelwise: for
+// small layers); with two tokens it was slower.
 inline int gemv_chunks_per_warp(int64_t K) { return static_cast<int>((K + 4095) / 4096); }
-inline bool linear_gemv_fits(int64_t M, int64_t K) { return M == 1 && K <= 12288; }
+// Channelwise: only layers of at most 4096 x 4096 weights.  Once the
+// quantizer lets the GEMM launch early, the two kernels are faster on
+// larger layers (qkv 6144 x 4096: 7.3 against 8.1 us; down, gate_up).
+inline bool linear_gemv_fits(int64_t M, int64_t N, int64_t K)
+{
+    return M == 1 && K <= 12288 && N * K <= 4096 * 4096;
+}
 inline bool linear_blk_gemv_fits(int64_t M, int64_t K) { return M == 1 && K <= 12288; }
 cudaError_t launch_linear_blk_gemv(const void *x, const void *w, const float *w_scale, const void *bias, void *out,
                                    void *xq, float *xs, int64_t m_pad, int64_t N, int64_t K, float eps, bool out_fp16,

@@ -363,7 +363,7 @@ cudaError_t launch_linear_pt_gemv(const void *x, const void *w, int64_t ldw, con
                                   void *out, void *xq, float *xs, int64_t M, int64_t N, int64_t K, float eps,
                                   bool out_fp16, cudaStream_t st)
 {
-    if (!linear_gemv_fits(M, K)) return cudaErrorInvalidValue;
+    if (!linear_gemv_fits(M, N, K)) return cudaErrorInvalidValue;
     const size_t wbytes = static_cast<size_t>(N - 1) * static_cast<size_t>(ldw) + static_cast<size_t>(K);
     const bool preload = !last_launch_writes_overlap(st, w, wbytes);
     const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);

@@ -281,8 +281,8 @@ FP8Q_API size_t fp8q_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t bl
 /* ---------------------------------------------------------------------------
  * Linear-layer compositions (no padding copies): quantize x into the
  * caller's buffers, then run the GEMM on them -- two launches, except:
- * fp8q_linear_channelwise with ONE token and K <= 12288 (and no schedule
- * override set) runs as one launch, the per-token quantization fused into a
+ * fp8q_linear_channelwise with ONE token, K <= 12288 and N * K <= 4096^2
+ * (and no schedule override set) runs as one launch, the per-token quantization fused into a
  * matrix-vector product on the CUDA cores (every CTA quantizes the row into
  * its shared memory; CTA 0 also writes xq and xs, so they hold the same
  * codes and scales as after the two launches).  Its sums are accumulated in
@@ -310,10 +310,10 @@ FP8Q_API fp8q_status fp8q_linear_blockwise(const void *x, const void *w, const f
                                   const void *bias, void *out, int64_t M, int64_t N, int64_t K,
                                   void *xq, float *xs, int64_t m_pad, fp8q_out_dtype out_dtype,
                                   void *workspace, size_t workspace_bytes, void *stream);
-/* Kernel launches fp8q_linear_channelwise makes for M tokens of K values:
- * 1 (the fused one-token form), 2 (quantizer + GEMM), or 0 for M <= 0 or
- * K <= 0.  Host only; reads the schedule override. */
-FP8Q_API int32_t fp8q_linear_channelwise_launches(int64_t M, int64_t K);
+/* Kernel launches fp8q_linear_channelwise makes for M tokens of K values
+ * against N output channels: 1 (the fused one-token form), 2 (quantizer +
+ * GEMM), or 0 for M, N or K <= 0.  Host only; reads the schedule override. */
+FP8Q_API int32_t fp8q_linear_channelwise_launches(int64_t M, int64_t N, int64_t K);
 /* The same for fp8q_linear_blockwise. */
 FP8Q_API int32_t fp8q_linear_blockwise_launches(int64_t M, int64_t K);
 

@@ -1,8 +1,9 @@
 """GPU parity of the linear layers at decode sizes.  One token with K <=
-12288 runs as ONE launch with the per-token (channelwise) or group-128
-(blockwise) quantization fused into a matrix-vector product on the CUDA
-cores; two to four tokens and longer rows take the quantizer and the
-tensor-core GEMM.  Either way the codes and scales
+12288 (channelwise: on layers of at most 4096 x 4096 weights) runs as ONE
+launch with the per-token (channelwise) or group-128 (blockwise)
+quantization fused into a matrix-vector product on the CUDA cores; two to
+four tokens, longer rows and larger channelwise layers take the quantizer
+and the tensor-core GEMM.  Either way the codes and scales
 left in the caller's buffers are bit-exact against the oracle's per-token
 quantizer, the output is within the GEMM bar of the oracle's GEMM on those
 codes, and the fused launch leaves the same codes and scales as the
@@ -132,9 +133,9 @@ def test_few_token_linear_same_codes_as_two_kernels(dev, schedule):
 
 
 def test_few_token_linear_full_size_decode_layers(dev):
-    """The decode layers at their own sizes: qkv 6144x4096, down 4096x12288
-    (three chunks per warp at M = 1), gate_up 24576x4096 at M = 1 and 4,
-    every output against the oracle."""
+    """The decode layers at their own sizes: qkv 6144x4096, down 4096x12288,
+    gate_up 24576x4096 at M = 1 and 4 (two kernels: larger than the fused
+    channelwise form takes), every output against the oracle."""
     for (N, K) in [(6144, 4096), (4096, 12288), (24576, 4096)]:
         wq, ws = weights(dev, N, K, seed=N)
         for M in (1, 4):
@@ -171,7 +172,7 @@ def test_few_token_linear_wide_rows(dev, M, K):
     warp only: 4112, 8208), the longest row the fused channelwise launch
     takes (12288, four channels per CTA) and longer ones, which take the
     quantizer and the GEMM."""
-    assert fq.fp8q_linear_channelwise_launches(M, K) == (1 if M == 1 and K <= 12288 else 2)
+    assert fq.fp8q_linear_channelwise_launches(M, 136, K) == (1 if M == 1 and K <= 12288 else 2)
     wq, ws = weights(dev, 136, K, seed=K)
     x = synthetic.activations(M, K, outliers=True, seed=K + M)
     check(dev, x, wq, ws, what=f"{M}x136x{K}")

@@ -189,17 +189,21 @@ def test_tuner_only_proposes_schedules_the_library_accepts(lib):
 
 
 def test_linear_channelwise_launch_count(lib):
-    """One token with rows up to 12288 values: one fused launch; otherwise
-    the quantizer and the GEMM; nothing for empty problems; two again while a
-    schedule override asks for the GEMM."""
-    assert fq.fp8q_linear_channelwise_launches(1, 4096) == 1
-    assert fq.fp8q_linear_channelwise_launches(1, 16) == 1
-    assert fq.fp8q_linear_channelwise_launches(1, 4112) == 1
-    assert fq.fp8q_linear_channelwise_launches(1, 12288) == 1
-    assert fq.fp8q_linear_channelwise_launches(1, 12304) == 2
-    assert fq.fp8q_linear_channelwise_launches(2, 4096) == 2
-    assert fq.fp8q_linear_channelwise_launches(8192, 4096) == 2
-    assert fq.fp8q_linear_channelwise_launches(0, 4096) == 0
+    """One token with rows up to 12288 values (channelwise: on layers of at
+    most 4096 x 4096 weights): one fused launch; otherwise the quantizer and
+    the GEMM; nothing for empty problems; two again while a schedule override
+    asks for the GEMM."""
+    assert fq.fp8q_linear_channelwise_launches(1, 4096, 4096) == 1
+    assert fq.fp8q_linear_channelwise_launches(1, 8, 16) == 1
+    assert fq.fp8q_linear_channelwise_launches(1, 136, 4112) == 1
+    assert fq.fp8q_linear_channelwise_launches(1, 136, 12288) == 1
+    assert fq.fp8q_linear_channelwise_launches(1, 136, 12304) == 2
+    assert fq.fp8q_linear_channelwise_launches(1, 6144, 4096) == 2     # larger layers: two kernels
+    assert fq.fp8q_linear_channelwise_launches(1, 4096, 12288) == 2
+    assert fq.fp8q_linear_channelwise_launches(1, 24576, 4096) == 2
+    assert fq.fp8q_linear_channelwise_launches(2, 4096, 4096) == 2
+    assert fq.fp8q_linear_channelwise_launches(8192, 4096, 4096) == 2
+    assert fq.fp8q_linear_channelwise_launches(0, 4096, 4096) == 0
     assert fq.fp8q_linear_blockwise_launches(1, 7168) == 1
     assert fq.fp8q_linear_blockwise_launches(1, 12288) == 1
     assert fq.fp8q_linear_blockwise_launches(1, 12416) == 2
@@ -207,7 +211,7 @@ def test_linear_channelwise_launch_count(lib):
     assert fq.fp8q_linear_blockwise_launches(0, 7168) == 0
     lib.fp8q_set_plan_override(1, 16, 4)
     try:
-        assert fq.fp8q_linear_channelwise_launches(1, 4096) == 2
+        assert fq.fp8q_linear_channelwise_launches(1, 4096, 4096) == 2
         assert fq.fp8q_linear_blockwise_launches(1, 7168) == 2
     finally:
         lib.fp8q_set_plan_override(-1, 0, 0)
